@@ -1,0 +1,435 @@
+/*
+ * mla_oracle.c -- plain CPU oracle for multi-head latent attention (MLA) computed
+ * from the compressed latent.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
+ * this file: only the test-suite, the smoke check and the CPU-baseline leg of the
+ * benchmark use it.  It shares no code, header, table or constant with the CUDA
+ * library; the two meet only in the seeded input generator, which holds none of
+ * the method's arithmetic.
+ *
+ * Everything is evaluated in IEEE double precision with plain loops, one output
+ * row at a time, in the order the definitions are written.  OpenMP only spreads
+ * independent (batch, head) or (batch, head, query) work over host cores; it never
+ * changes the order of any sum.
+ *
+ * Sources (pages; "LAGA" = "A Training-Memory Regression in MLA Sequence
+ * Parallelism: Why Megatron-Core Forbids Absorption, and LAGA -- a
+ * Communication-Efficient Fix", arXiv 2607.17644; "TPLA" = "TPLA: Tensor Parallel
+ * Latent Attention for Efficient Disaggregated Prefill and Decode Inference",
+ * arXiv 2508.15881; "Helix" = "Helix Parallelism: Rethinking Sharding Strategies
+ * for Interactive Multi-Million-Token LLM Decoding", arXiv 2507.07120):
+ *
+ *  - LAGA, "What carries the argument" and Fig. 2: explicit form = per-head K/V
+ *    rebuilt from the latent through W_kv_b, head-dim attention; absorbed form =
+ *    q_absorbed = W_kv_b^T q_nope, attention in latent space, un-absorb after.
+ *  - LAGA, axiom ledger (paper section 2.1): the kv_b up-projection is linear and
+ *    shared by all heads; the normalised latent LN(latent) is common to all heads.
+ *  - TPLA, "What carries the argument" / Proposition 1: that normalisation is an
+ *    RMSNorm of the latent c_KV.
+ *  - LAGA, "What carries the argument": only the d_kv latent plus "the small RoPE
+ *    band" travel, i.e. RoPE is decoupled and k_pe is shared across heads.
+ *  - Helix, "What carries the argument" and "Assumptions" (paper section 2.1.1):
+ *    partial attention outputs plus log-sum-exp scalars are rescaled and summed to
+ *    give the exact softmax output (the Flash-Decoding combine).
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *  - RMSNorm: y = x * w / sqrt(mean(x^2) + eps), no mean subtraction, no bias;
+ *    applied to c_KV only, never to k_pe.
+ *  - RoPE: half-split pairing (t, t + d_rope/2), theta_t = base^(-2t/d_rope);
+ *    query row i sits at absolute position q_offset + i, key j at position j,
+ *    a decode query at position kv_len - 1.
+ *  - Score scale: 1/sqrt(d_nope + d_rope) unless the caller passes another.
+ *  - W_kv_b rows: head h owns rows [h*(d_nope+d_v), (h+1)*(d_nope+d_v)); the first
+ *    d_nope rows give K_nope, the next d_v rows give V.  Each row has d_kv entries.
+ *  - Causal mask with offset: key j is visible to query i iff j <= q_offset + i.
+ *  - LSE is the natural log of the softmax normaliser, scale included.  A row that
+ *    sees no key has lse = -inf and output 0.
+ *  - Split-KV boundaries: contiguous chunks of ceil(kv_len / n_splits) keys; the
+ *    last chunk may be shorter or empty.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- RMSNorm ---- */
+/* One row: y_k = x_k * w_k / sqrt((1/d) * sum_k x_k^2 + eps).  TPLA, "What carries
+ * the argument" (RMSNorm of the latent); LAGA axiom ledger (LN(latent) shared by all
+ * heads). */
+static void rmsnorm_row(const double *x, const double *w, int d, double eps, double *y)
+{
+    double ss = 0.0;
+    for (int k = 0; k < d; ++k)
+        ss += x[k] * x[k];
+    double inv = 1.0 / sqrt(ss / (double)d + eps);
+    for (int k = 0; k < d; ++k)
+        y[k] = x[k] * inv * w[k];
+}
+
+void orc_rmsnorm(const double *x, const double *w, long rows, int d, double eps, double *y)
+{
+    for (long r = 0; r < rows; ++r)
+        rmsnorm_row(x + r * d, w, d, eps, y + r * d);
+}
+
+/* ------------------------------------------------------------------- RoPE ---- */
+/* Rotary embedding of one d_rope-wide band at absolute position pos, half-split
+ * pairing: for t < d_rope/2 the pair (x_t, x_{t+d/2}) is rotated by the angle
+ * pos * base^(-2t/d).  LAGA, "What carries the argument" ("the small RoPE band"). */
+static void rope_row(const double *x, double pos, int d, double base, double *y)
+{
+    int half = d / 2;
+    for (int t = 0; t < half; ++t) {
+        double theta = pow(base, -2.0 * (double)t / (double)d);
+        double a = pos * theta;
+        double c = cos(a), s = sin(a);
+        double x0 = x[t], x1 = x[t + half];
+        y[t] = x0 * c - x1 * s;
+        y[t + half] = x1 * c + x0 * s;
+    }
+}
+
+void orc_rope(const double *x, const double *pos, long rows, int d, double base, double *y)
+{
+    for (long r = 0; r < rows; ++r)
+        rope_row(x + r * d, pos[r], d, base, y + r * d);
+}
+
+/* ------------------------------------------------------ softmax attention ---- */
+/* Softmax over the given scores s[0..n): writes p[j] = exp(s_j - m) (unnormalised)
+ * and returns the log-sum-exp m + log(sum_j exp(s_j - m)); n == 0 gives -inf. */
+static double softmax_weights(const double *s, long n, double *p, double *z_out)
+{
+    if (n == 0) {
+        *z_out = 0.0;
+        return -INFINITY;
+    }
+    double m = s[0];
+    for (long j = 1; j < n; ++j)
+        if (s[j] > m)
+            m = s[j];
+    double z = 0.0;
+    for (long j = 0; j < n; ++j) {
+        p[j] = exp(s[j] - m);
+        z += p[j];
+    }
+    *z_out = z;
+    return m + log(z);
+}
+
+static double dot(const double *a, const double *b, int n)
+{
+    double acc = 0.0;
+    for (int k = 0; k < n; ++k)
+        acc += a[k] * b[k];
+    return acc;
+}
+
+/* Number of keys query row i (absolute position pos) may attend to. */
+static long visible_keys(int causal, long pos, long s_kv)
+{
+    if (!causal)
+        return s_kv;
+    long n = pos + 1;
+    return n < s_kv ? n : s_kv;
+}
+
+/* ----------------------------------------------- explicit form (LAGA / B1) ---- */
+/*
+ * Explicit MLA forward for batches [0,B), heads [head_begin, head_begin+head_count),
+ * queries at absolute positions q_off .. q_off+s_q-1 over a full latent of s_kv keys.
+ * LAGA, "What carries the argument" and Fig. 2: rebuild per-head K_nope/V from the
+ * normalised latent through W_kv_b (same matmul, reordered views -- the paper's
+ * section 3.3 "H_r slice"), then head-dim attention with q = [q_nope ; RoPE(q_pe)],
+ * k = [K_nope ; RoPE(k_pe)] (k_pe shared by all heads).
+ *
+ * Layouts (row-major): q_nope [B,s_q,head_count,Dn]; q_pe [B,s_q,head_count,Dr];
+ * c_kv [B,s_kv,Dk]; k_pe [B,s_kv,Dr]; w_kv_b [n_heads*(Dn+Dv), Dk]; rms_w [Dk];
+ * out [B,s_q,head_count,Dv]; lse [B,head_count,s_q].
+ */
+void orc_mla_explicit(int B, int s_q, int s_kv, int q_off, int causal,
+                      int n_heads, int head_begin, int head_count,
+                      int Dk, int Dn, int Dr, int Dv,
+                      double base, double eps, double scale,
+                      const double *q_nope, const double *q_pe, const double *c_kv,
+                      const double *k_pe, const double *w_kv_b, const double *rms_w,
+                      double *out, double *lse)
+{
+    (void)n_heads;
+    long kv_need = causal ? (long)q_off + s_q : s_kv;
+    if (kv_need > s_kv)
+        kv_need = s_kv;
+    int Dh = Dn + Dv;
+
+    /* Step 1 (per batch, shared by every head): normalised latent and rotated k_pe. */
+    double *chat = (double *)malloc(sizeof(double) * (size_t)B * (kv_need > 0 ? kv_need : 1) * Dk);
+    double *krot = (double *)malloc(sizeof(double) * (size_t)B * (kv_need > 0 ? kv_need : 1) * Dr);
+    for (int b = 0; b < B; ++b)
+        for (long j = 0; j < kv_need; ++j) {
+            rmsnorm_row(c_kv + ((size_t)b * s_kv + j) * Dk, rms_w, Dk, eps,
+                        chat + ((size_t)b * kv_need + j) * Dk);
+            rope_row(k_pe + ((size_t)b * s_kv + j) * Dr, (double)j, Dr, base,
+                     krot + ((size_t)b * kv_need + j) * Dr);
+        }
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int hl = 0; hl < head_count; ++hl) {
+            int h = head_begin + hl;
+            const double *wk = w_kv_b + (size_t)h * Dh * Dk;  /* Dn rows: K_nope */
+            const double *wv = wk + (size_t)Dn * Dk;          /* Dv rows: V      */
+            long nk = kv_need > 0 ? kv_need : 1;
+            double *kn = (double *)malloc(sizeof(double) * nk * Dn);
+            double *vv = (double *)malloc(sizeof(double) * nk * Dv);
+            double *sc = (double *)malloc(sizeof(double) * nk);
+            double *pw = (double *)malloc(sizeof(double) * nk);
+            double qr[1024];
+
+            /* Step 2: K_nope_j = W_K(h) chat_j, V_j = W_V(h) chat_j. */
+            for (long j = 0; j < kv_need; ++j) {
+                const double *cj = chat + ((size_t)b * kv_need + j) * Dk;
+                for (int d = 0; d < Dn; ++d)
+                    kn[j * Dn + d] = dot(wk + (size_t)d * Dk, cj, Dk);
+                for (int d = 0; d < Dv; ++d)
+                    vv[j * Dv + d] = dot(wv + (size_t)d * Dk, cj, Dk);
+            }
+
+            for (int i = 0; i < s_q; ++i) {
+                long pos = (long)q_off + i;
+                size_t qrow = ((size_t)b * s_q + i) * head_count + hl;
+                const double *qn = q_nope + qrow * Dn;
+                rope_row(q_pe + qrow * Dr, (double)pos, Dr, base, qr);
+                long n = visible_keys(causal, pos, s_kv);
+                /* Step 3: scores over the visible keys. */
+                for (long j = 0; j < n; ++j)
+                    sc[j] = scale * (dot(qn, kn + j * Dn, Dn) +
+                                     dot(qr, krot + ((size_t)b * kv_need + j) * Dr, Dr));
+                double z;
+                double l = softmax_weights(sc, n, pw, &z);
+                /* Step 4: o = sum_j softmax_j V_j. */
+                double *o = out + qrow * Dv;
+                for (int d = 0; d < Dv; ++d) {
+                    double acc = 0.0;
+                    for (long j = 0; j < n; ++j)
+                        acc += pw[j] * vv[j * Dv + d];
+                    o[d] = n > 0 ? acc / z : 0.0;
+                }
+                lse[((size_t)b * head_count + hl) * s_q + i] = l;
+            }
+            free(kn);
+            free(vv);
+            free(sc);
+            free(pw);
+        }
+    free(chat);
+    free(krot);
+}
+
+/* ----------------------------------------------- absorbed form (B2) ---- */
+/*
+ * Absorbed MLA forward, same arguments and layouts as orc_mla_explicit.
+ * LAGA, "What carries the argument" and Fig. 2 (absorb -> latent-attn -> un-absorb):
+ * q_abs = W_K(h)^T q_nope (d_kv wide), scores q_abs . chat_j + RoPE(q_pe) . RoPE(k_pe_j),
+ * latent accumulator o_lat = sum_j softmax_j chat_j, then out = W_V(h) o_lat.
+ */
+void orc_mla_absorbed(int B, int s_q, int s_kv, int q_off, int causal,
+                      int n_heads, int head_begin, int head_count,
+                      int Dk, int Dn, int Dr, int Dv,
+                      double base, double eps, double scale,
+                      const double *q_nope, const double *q_pe, const double *c_kv,
+                      const double *k_pe, const double *w_kv_b, const double *rms_w,
+                      double *out, double *lse)
+{
+    (void)n_heads;
+    long kv_need = causal ? (long)q_off + s_q : s_kv;
+    if (kv_need > s_kv)
+        kv_need = s_kv;
+    int Dh = Dn + Dv;
+    long nk = kv_need > 0 ? kv_need : 1;
+
+    double *chat = (double *)malloc(sizeof(double) * (size_t)B * nk * Dk);
+    double *krot = (double *)malloc(sizeof(double) * (size_t)B * nk * Dr);
+    for (int b = 0; b < B; ++b)
+        for (long j = 0; j < kv_need; ++j) {
+            rmsnorm_row(c_kv + ((size_t)b * s_kv + j) * Dk, rms_w, Dk, eps,
+                        chat + ((size_t)b * kv_need + j) * Dk);
+            rope_row(k_pe + ((size_t)b * s_kv + j) * Dr, (double)j, Dr, base,
+                     krot + ((size_t)b * kv_need + j) * Dr);
+        }
+
+#pragma omp parallel for collapse(3) schedule(dynamic, 16)
+    for (int b = 0; b < B; ++b)
+        for (int hl = 0; hl < head_count; ++hl)
+            for (int i = 0; i < s_q; ++i) {
+                int h = head_begin + hl;
+                const double *wk = w_kv_b + (size_t)h * Dh * Dk;
+                const double *wv = wk + (size_t)Dn * Dk;
+                double *qa = (double *)malloc(sizeof(double) * Dk);
+                double *ol = (double *)malloc(sizeof(double) * Dk);
+                double *sc = (double *)malloc(sizeof(double) * nk);
+                double *pw = (double *)malloc(sizeof(double) * nk);
+                double qr[1024];
+                long pos = (long)q_off + i;
+                size_t qrow = ((size_t)b * s_q + i) * head_count + hl;
+                const double *qn = q_nope + qrow * Dn;
+                /* absorb: q_abs_k = sum_d q_nope_d W_K(h)[d][k] */
+                for (int k = 0; k < Dk; ++k) {
+                    double acc = 0.0;
+                    for (int d = 0; d < Dn; ++d)
+                        acc += qn[d] * wk[(size_t)d * Dk + k];
+                    qa[k] = acc;
+                }
+                rope_row(q_pe + qrow * Dr, (double)pos, Dr, base, qr);
+                long n = visible_keys(causal, pos, s_kv);
+                for (long j = 0; j < n; ++j)
+                    sc[j] = scale * (dot(qa, chat + ((size_t)b * kv_need + j) * Dk, Dk) +
+                                     dot(qr, krot + ((size_t)b * kv_need + j) * Dr, Dr));
+                double z;
+                double l = softmax_weights(sc, n, pw, &z);
+                /* latent accumulator */
+                for (int k = 0; k < Dk; ++k) {
+                    double acc = 0.0;
+                    for (long j = 0; j < n; ++j)
+                        acc += pw[j] * chat[((size_t)b * kv_need + j) * Dk + k];
+                    ol[k] = n > 0 ? acc / z : 0.0;
+                }
+                /* un-absorb: out_d = sum_k W_V(h)[d][k] o_lat_k */
+                double *o = out + qrow * Dv;
+                for (int d = 0; d < Dv; ++d)
+                    o[d] = dot(wv + (size_t)d * Dk, ol, Dk);
+                lse[((size_t)b * head_count + hl) * s_q + i] = l;
+                free(qa);
+                free(ol);
+                free(sc);
+                free(pw);
+            }
+    free(chat);
+    free(krot);
+}
+
+/* ---------------------------------------------------- latent decode ---- */
+/*
+ * One decode query per sequence at position kv_len-1, all n_heads heads, over a
+ * latent cache that already holds normalised c_KV and rotated k_pe (what a prefill
+ * writes).  Absorbed-form scores, as the LAGA page says the absorb trick is used only
+ * in inference decode ("Core claim", abstract).  The result is the plain softmax over
+ * every cached key; part_out/part_lse (when not NULL) receive the same attention
+ * restricted to each contiguous split of ceil(kv_len/n_splits) keys: the latent
+ * accumulator normalised within the split [n_splits,B,H,Dk] and its log-sum-exp
+ * [n_splits,B,H].  The Helix page's rescale-and-sum turns those partials back into
+ * the unsplit result; that identity is what orc_lse_combine states.
+ *
+ * Layouts: q_nope [B,H,Dn]; q_pe [B,H,Dr] (not yet rotated); c_cache [B,kv_len,Dk];
+ * kpe_cache [B,kv_len,Dr]; out [B,H,Dv]; lse [B,H].
+ */
+void orc_mla_decode(int B, int kv_len, int n_splits, int n_heads,
+                    int Dk, int Dn, int Dr, int Dv, double base, double scale,
+                    const double *q_nope, const double *q_pe, const double *c_cache,
+                    const double *kpe_cache, const double *w_kv_b,
+                    double *out, double *lse, double *part_out, double *part_lse)
+{
+    int Dh = Dn + Dv;
+    long chunk = n_splits > 0 ? ((long)kv_len + n_splits - 1) / n_splits : kv_len;
+    long nk = kv_len > 0 ? kv_len : 1;
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < n_heads; ++h) {
+            const double *wk = w_kv_b + (size_t)h * Dh * Dk;
+            const double *wv = wk + (size_t)Dn * Dk;
+            double *qa = (double *)malloc(sizeof(double) * Dk);
+            double *ol = (double *)malloc(sizeof(double) * Dk);
+            double *sc = (double *)malloc(sizeof(double) * nk);
+            double *pw = (double *)malloc(sizeof(double) * nk);
+            double qr[1024];
+            size_t row = (size_t)b * n_heads + h;
+            const double *qn = q_nope + row * Dn;
+            for (int k = 0; k < Dk; ++k) {
+                double acc = 0.0;
+                for (int d = 0; d < Dn; ++d)
+                    acc += qn[d] * wk[(size_t)d * Dk + k];
+                qa[k] = acc;
+            }
+            rope_row(q_pe + row * Dr, (double)(kv_len - 1), Dr, base, qr);
+            const double *cb = c_cache + (size_t)b * kv_len * Dk;
+            const double *kb = kpe_cache + (size_t)b * kv_len * Dr;
+            for (long j = 0; j < kv_len; ++j)
+                sc[j] = scale * (dot(qa, cb + j * Dk, Dk) + dot(qr, kb + j * Dr, Dr));
+
+            /* unsplit softmax over all cached keys */
+            double z;
+            double l = softmax_weights(sc, kv_len, pw, &z);
+            for (int k = 0; k < Dk; ++k) {
+                double acc = 0.0;
+                for (long j = 0; j < kv_len; ++j)
+                    acc += pw[j] * cb[j * Dk + k];
+                ol[k] = kv_len > 0 ? acc / z : 0.0;
+            }
+            for (int d = 0; d < Dv; ++d)
+                out[row * Dv + d] = dot(wv + (size_t)d * Dk, ol, Dk);
+            lse[row] = l;
+
+            /* per-split partials: the same attention restricted to each key chunk */
+            if (part_out && part_lse)
+                for (int s = 0; s < n_splits; ++s) {
+                    long j0 = (long)s * chunk, j1 = j0 + chunk;
+                    if (j0 > kv_len)
+                        j0 = kv_len;
+                    if (j1 > kv_len)
+                        j1 = kv_len;
+                    double zs;
+                    double ls = softmax_weights(sc + j0, j1 - j0, pw, &zs);
+                    double *po = part_out + ((size_t)s * B * n_heads + row) * Dk;
+                    for (int k = 0; k < Dk; ++k) {
+                        double acc = 0.0;
+                        for (long j = j0; j < j1; ++j)
+                            acc += pw[j - j0] * cb[j * Dk + k];
+                        po[k] = j1 > j0 ? acc / zs : 0.0;
+                    }
+                    part_lse[(size_t)s * B * n_heads + row] = ls;
+                }
+            free(qa);
+            free(ol);
+            free(sc);
+            free(pw);
+        }
+}
+
+/* ------------------------------------------------------ LSE combine ---- */
+/*
+ * Helix, "What carries the argument" and "Assumptions" (paper section 2.1.1):
+ * given per-split outputs o_s (each normalised within its split) and their
+ * log-sum-exp l_s, the full result is lse = log sum_s exp(l_s) and
+ * o = sum_s exp(l_s - lse) o_s.  Splits with l_s = -inf (no keys) carry no weight;
+ * if every split is empty the row gives lse = -inf and o = 0.
+ * Layouts: part_out [n_splits,rows,D]; part_lse [n_splits,rows]; out [rows,D]; lse [rows].
+ */
+void orc_lse_combine(int n_splits, long rows, int D, const double *part_out,
+                     const double *part_lse, double *out, double *lse)
+{
+    for (long r = 0; r < rows; ++r) {
+        double m = -INFINITY;
+        for (int s = 0; s < n_splits; ++s)
+            if (part_lse[(size_t)s * rows + r] > m)
+                m = part_lse[(size_t)s * rows + r];
+        double *o = out + (size_t)r * D;
+        if (m == -INFINITY) {
+            for (int d = 0; d < D; ++d)
+                o[d] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double z = 0.0;
+        for (int s = 0; s < n_splits; ++s)
+            z += exp(part_lse[(size_t)s * rows + r] - m);
+        double l = m + log(z);
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int s = 0; s < n_splits; ++s)
+                acc += exp(part_lse[(size_t)s * rows + r] - l) *
+                       part_out[((size_t)s * rows + r) * D + d];
+            o[d] = acc;
+        }
+        lse[r] = l;
+    }
+}

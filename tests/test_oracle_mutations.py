@@ -1,0 +1,46 @@
+"""The pins have teeth: plausible mistakes planted in copies of the oracle are caught.
+
+Each mutation edits one line of ``oracle/mla_oracle.c`` in a temporary copy, builds
+it, and runs the pin suite against that build in a subprocess; the suite must fail.
+Nothing here touches the committed oracle or the GPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "mla_oracle.c")
+
+MUTATIONS = {
+    "rope_sign": ("y[t] = x0 * c - x1 * s;", "y[t] = x0 * c + x1 * s;"),
+    "rope_theta": ("pow(base, -2.0 * (double)t / (double)d)", "pow(base, -1.0 * (double)t / (double)d)"),
+    "rms_eps_outside_sqrt": ("1.0 / sqrt(ss / (double)d + eps)", "1.0 / (sqrt(ss / (double)d) + eps)"),
+    "dropped_rope_score_term": ("sc[j] = scale * (dot(qn, kn + j * Dn, Dn) +",
+                                "sc[j] = scale * (dot(qn, kn + j * Dn, Dn) + 0.0 *"),
+    "k_from_v_rows": ("kn[j * Dn + d] = dot(wk + (size_t)d * Dk, cj, Dk);",
+                      "kn[j * Dn + d] = dot(wk + (size_t)(d + 1) * Dk, cj, Dk);"),
+    "causal_off_by_one": ("long n = pos + 1;", "long n = pos;"),
+    "combine_weight": ("acc += exp(part_lse[(size_t)s * rows + r] - l) *",
+                       "acc += exp(part_lse[(size_t)s * rows + r] - m) *"),
+    "absorb_transposed": ("acc += qn[d] * wk[(size_t)d * Dk + k];\n                    qa[k] = acc;",
+                          "acc += qn[d] * wk[(size_t)k * Dn + d];\n                    qa[k] = acc;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: " + name
+    mutated = tmp_path / "mla_oracle_mut.c"
+    mutated.write_text(src.replace(old, new, 1))
+    lib = tmp_path / "libmla_oracle_mut.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                           "-ffp-contract=off", str(mutated), "-o", str(lib), "-lm"])
+    env = dict(os.environ, MLA_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "pins did not catch mutation %s:\n%s" % (name, r.stdout[-2000:])
