@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of MLA attention from the compressed latent on GB300.
+
+One step = one explicit (LAGA per-rank) prefill call on the DeepSeek-V2-Lite-shaped
+workload (bf16, batch 1, 4096 tokens, 16 heads, d_kv 512, qk 192, v 128, causal)
+followed by one split-KV latent decode call (bf16, batch 64, 128 heads, 32768 cached
+tokens, 8 splits).  The headline ``value`` is the prefill's TFLOP/s (algorithmic
+FLOPs: visible causal pairs x 2 x (192 + 128) plus the K/V reconstruction GEMM); the
+``decode`` object carries the decode's HBM GB/s.  Both are timed per call with CUDA
+events on the launching stream; the prefill's inputs fit in L2, so a 256 MB buffer
+is written between timed calls; the decode's 2.4 GB cache does not.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own copy of the workload (independent problems,
+no collective on the data path: weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA prefill fwd TFLOP/s (% of BF16 peak); decode HBM GB/s (% of 8 TB/s)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max clock
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks ----
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (read-only queries)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int):
+        self.samples, self.max_mhz, self.ok = [], None, False
+        self._stop = threading.Event()
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(device_index)
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(h)) != 0:
+                    return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0 and \
+                    self._reasons_fn(self.h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": "NVML unavailable"}
+        mhz = [s[0] for s in self.samples]
+        seen = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    seen.add(name)
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": sorted(seen),
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- helpers ----
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def randn(shape, std, dtype, g):
+    import torch
+    return (torch.randn(shape, generator=g, device="cuda", dtype=torch.float32) * std).to(dtype)
+
+
+def prefill_setup(cfg, seed=0):
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import mla
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    dt = cfg.torch_dtype
+    B, S, H = cfg.batch, cfg.s_q, cfg.n_heads
+    t = dict(q_nope=randn((B, S, H, cfg.d_nope), 1.0, dt, g), q_pe=randn((B, S, H, cfg.d_rope), 1.0, dt, g),
+             c_kv=randn((B, cfg.s_kv, cfg.d_kv), 1.0, dt, g), k_pe=randn((B, cfg.s_kv, cfg.d_rope), 1.0, dt, g),
+             w_kv_b=randn((H * (cfg.d_nope + cfg.d_v), cfg.d_kv), cfg.d_kv ** -0.5, dt, g),
+             rms_w=torch.ones(cfg.d_kv, dtype=dt, device="cuda"))
+    d = mla.dims_of(cfg)
+    out = torch.empty(B, S, H, cfg.d_v, dtype=dt, device="cuda")
+    lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
+    nbytes = mla.mla_latent_attn_workspace(ctypes.byref(d), 1 if dt == torch.bfloat16 else 0, B, S, cfg.s_kv,
+                                           cfg.q_offset, int(cfg.causal), H, cfg.head_shard)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    return d, t, out, lse, ws
+
+
+def prefill_call(cfg, d, t, out, lse, ws, stream):
+    from head_latent_attention_rmsnorm_gb300 import mla
+    st = mla.lib().mla_latent_attn_fwd(ctypes.byref(d), mla.MLA_BF16 if cfg.dtype == "bf16" else mla.MLA_F32,
+                                       cfg.batch, cfg.s_q, cfg.s_kv, cfg.q_offset, int(cfg.causal), 0,
+                                       cfg.n_heads, cfg.head_shard, t["q_nope"].data_ptr(), t["q_pe"].data_ptr(),
+                                       t["c_kv"].data_ptr(), t["k_pe"].data_ptr(), t["w_kv_b"].data_ptr(),
+                                       t["rms_w"].data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+                                       ws.numel(), stream)
+    if st != 0:
+        raise RuntimeError("mla_latent_attn_fwd: " + mla.mla_status_string(st))
+
+
+def decode_setup(cfg, seed=1):
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import mla
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    dt = cfg.torch_dtype
+    B, H, L = cfg.batch, cfg.n_heads, cfg.kv_len
+    t = dict(q_nope=randn((B, H, cfg.d_nope), 1.0, dt, g), q_pe=randn((B, H, cfg.d_rope), 1.0, dt, g),
+             c_cache=randn((B, L, cfg.d_kv), 1.0, dt, g), kpe_cache=randn((B, L, cfg.d_rope), 1.0, dt, g),
+             w_kv_b=randn((H * (cfg.d_nope + cfg.d_v), cfg.d_kv), cfg.d_kv ** -0.5, dt, g))
+    d = mla.dims(cfg.n_heads, cfg.d_kv, cfg.d_nope, cfg.d_rope, cfg.d_v, cfg.rope_base)
+    out = torch.empty(B, H, cfg.d_v, dtype=dt, device="cuda")
+    lse = torch.empty(B, H, dtype=torch.float32, device="cuda")
+    nbytes = mla.mla_decode_workspace(ctypes.byref(d), 1 if dt == torch.bfloat16 else 0, B, L, cfg.n_splits)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    return d, t, out, lse, ws
+
+
+def decode_call(cfg, d, t, out, lse, ws, stream):
+    from head_latent_attention_rmsnorm_gb300 import mla
+    st = mla.lib().mla_decode_splitkv(ctypes.byref(d), mla.MLA_BF16 if cfg.dtype == "bf16" else mla.MLA_F32,
+                                      cfg.batch, cfg.kv_len, cfg.n_splits, t["q_nope"].data_ptr(),
+                                      t["q_pe"].data_ptr(), t["c_cache"].data_ptr(), t["kpe_cache"].data_ptr(),
+                                      t["w_kv_b"].data_ptr(), out.data_ptr(), lse.data_ptr(), None, None,
+                                      ws.data_ptr(), ws.numel(), stream)
+    if st != 0:
+        raise RuntimeError("mla_decode_splitkv: " + mla.mla_status_string(st))
+
+
+def timed(fn, steps, warmup, world, flush=None):
+    """Per-call CUDA-event times (ms) of `steps` calls after `warmup` calls."""
+    import torch
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        if flush is not None:
+            flush.zero_()
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        if flush is not None:
+            flush.zero_()
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def dominant(prof: dict, candidates):
+    best = None
+    for k in candidates:
+        if k in prof and (best is None or prof[k][1] > prof[best][1]):
+            best = k
+    return best
+
+
+# -------------------------------------------------------------- our arm ----
+def run_ours(args, world, rank, local):
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import build as mla_build
+    from head_latent_attention_rmsnorm_gb300 import configs, mla
+
+    if rank == 0:
+        mla_build.build()
+    barrier(world)
+    mla.lib()
+    peaks, peak_kind = load_peaks()
+    pcfg, dcfg = configs.V2LITE, configs.DECODE
+    stream = torch.cuda.current_stream().cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    # ---- prefill
+    d, t, out, lse, ws = prefill_setup(pcfg)
+    pf = lambda: prefill_call(pcfg, d, t, out, lse, ws, stream)  # noqa: E731
+    pf()
+    torch.cuda.synchronize()
+    path = mla.last_path()
+    n0 = mla.launch_count()
+    mla.profile_enable(True)
+    mla.profile_reset()
+    with ClockSampler(local) as clk:
+        p_times = timed(pf, args.steps, args.warmup, world, flush)
+        prof_p = mla.profile_all()
+        launches_p = mla.launch_count() - n0
+        mla.profile_enable(False)
+
+        # ---- decode
+        dd, dt_, dout, dlse, dws = decode_setup(dcfg)
+        dfn = lambda: decode_call(dcfg, dd, dt_, dout, dlse, dws, stream)  # noqa: E731
+        dfn()
+        torch.cuda.synchronize()
+        dpath = mla.last_path()
+        n1 = mla.launch_count()
+        mla.profile_enable(True)
+        mla.profile_reset()
+        d_times = timed(dfn, args.steps, args.warmup, world)
+        prof_d = mla.profile_all()
+        launches_d = mla.launch_count() - n1
+        mla.profile_enable(False)
+    # the profiled launches in the timed region include the warm-up calls: count per call
+    per_call_p = launches_p / (args.steps + args.warmup)
+    per_call_d = launches_d / (args.steps + args.warmup)
+
+    flops = pcfg.flops()
+    p_ms = max_over_ranks(statistics.mean(p_times), world)
+    d_ms = max_over_ranks(statistics.mean(d_times), world)
+    value = world * flops["total"] / (p_ms * 1e-3) / 1e12
+    dbytes = dcfg.algorithmic_bytes()
+    d_gbs = world * dbytes / (d_ms * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernels (profiled over the timed regions)
+    calls = args.steps + args.warmup
+    kp = dominant(prof_p, ("tc_attn", "attn_simt"))
+    roof = None
+    if kp:
+        n, ms = prof_p[kp]
+        per_launch_flops = flops["attention"] * calls / n
+        ach = per_launch_flops / (ms / n * 1e-3) / 1e12
+        if kp == "tc_attn":
+            peak, bound, note = peaks.get("bf16_tflops", 1900.0), "tensor", "bf16 dense burst, " + peak_kind
+        else:
+            peak, bound, note = FP32_ALU_TFLOPS, "alu", "fp32 FMA lanes x max clock (SIMT kernel)"
+        roof = {"kernel": kp, "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": None, "peak_kind": note,
+                "launches": n, "avg_launch_us": round(ms / n * 1e3, 2),
+                "share_of_step": round(ms / (sum(v[1] for v in prof_p.values()) or 1), 3)}
+    kd = dominant(prof_d, ("tc_latent_attn", "attn_simt"))
+    droof = None
+    if kd:
+        n, ms = prof_d[kd]
+        per_launch = dcfg.cache_bytes() * calls / n
+        ach = per_launch / (ms / n * 1e-3) / 1e9
+        droof = {"kernel": kd, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks.get("hbm_gbs", 6800.0),
+                 "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4), "traffic": None,
+                 "peak_kind": peak_kind, "launches": n, "avg_launch_us": round(ms / n * 1e3, 2)}
+
+    # ---- end to end through the C ABI with pinned host buffers (prefill)
+    e2e = None
+    try:
+        host_in = {k: v.cpu().pin_memory() for k, v in t.items()}
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        s = torch.cuda.current_stream()
+
+        def e2e_step():
+            for k, v in host_in.items():
+                t[k].copy_(v, non_blocking=True)
+            pf()
+            host_out.copy_(out, non_blocking=True)
+            host_lse.copy_(lse, non_blocking=True)
+
+        ke = max(1, min(args.steps, 20))
+        e_times = timed(e2e_step, ke, min(args.warmup, 3), world)
+        e_ms = max_over_ranks(statistics.mean(e_times), world)
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+        e2e = {"value": round(world * flops["total"] / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
+        del s
+    except Exception as ex:  # keep the kernel numbers even if pinning fails
+        e2e = {"value": None, "unit": "TFLOP/s", "error": str(ex)[:200]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill()
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(p_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn, N(0,1); W_kv_b N(0,1/512))",
+        "config": {"workload": pcfg.name, "batch": pcfg.batch, "seq_len": pcfg.s_q, "n_heads": pcfg.n_heads,
+                   "head_shard": pcfg.head_shard, "causal": True,
+                   "flops_per_step": flops["total"], "l2": "256 MB buffer written between timed calls",
+                   "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"), "parallelism": "replicas" if world > 1 else "single"},
+        "frac_of_bf16_peak": round(value / world / peaks.get("bf16_tflops", 1900.0), 4),
+        "tokens_per_s": round(world * pcfg.batch * pcfg.s_q / (p_ms * 1e-3), 1),
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "gpu_launches": int(round((per_call_p + per_call_d) * args.steps)),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "decode": {"workload": dcfg.name, "value": round(d_gbs, 1), "unit": "GB/s", "ms_per_call": round(d_ms, 4),
+                   "bytes_per_call": dbytes, "frac_of_8TBps": round(d_gbs / world / 8000.0, 4),
+                   "frac_of_measured_hbm": round(d_gbs / world / peaks.get("hbm_gbs", 6800.0), 4),
+                   "tokens_per_s": round(world * dcfg.batch / (d_ms * 1e-3), 1),
+                   "kernel_path": {1: "simt", 2: "tcgen05"}.get(dpath, "?"), "roofline": droof,
+                   "l2": "inputs (2.4 GB) larger than L2"},
+        "kernels_prefill": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_p.items()},
+        "kernels_decode": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_d.items()},
+        "peaks": {"kind": peak_kind, "hbm_gbs": peaks.get("hbm_gbs"), "bf16_tflops": peaks.get("bf16_tflops")},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------- oracle (CPU) ----
+def oracle_prefill_sample(rows: int):
+    """Time the oracle on the last `rows` query rows of the V2-Lite prefill, all 16 heads.
+
+    Returns (seconds, algorithmic FLOPs of the sample, threads used)."""
+    import dataclasses
+
+    import oracle
+    from head_latent_attention_rmsnorm_gb300 import configs, inputs
+    cfg = configs.V2LITE
+    q0 = cfg.s_kv - rows
+    sub = dataclasses.replace(cfg, s_q=rows, q_offset=q0)
+    inp = {k: v.double().numpy() for k, v in inputs.prefill_inputs(sub).items()}
+    t0 = time.perf_counter()
+    oracle.mla_explicit(**inp, n_heads=cfg.n_heads, q_offset=q0, causal=True, base=cfg.rope_base, eps=cfg.rms_eps)
+    dt = time.perf_counter() - t0
+    f = sub.flops()
+    return dt, f["total"], int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def cpu_baseline_prefill():
+    oracle_build()
+    rows = 4096
+    dt, fl, cores = oracle_prefill_sample(rows)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": "fp64 oracle, V2-Lite prefill, all 16 heads, last %d of 4096 query rows "
+                      "(K/V rebuilt for all 4096 keys)" % rows}
+
+
+def oracle_build():
+    import oracle
+    oracle.build()
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    oracle_build()
+    rows = 256
+    for _ in range(args.warmup):
+        oracle_prefill_sample(rows)
+    times, fl, cores = [], 0, 1
+    for _ in range(args.steps):
+        dt, fl, cores = oracle_prefill_sample(rows)
+        times.append(dt)
+    ms = statistics.mean(times) * 1e3
+    v = fl / (ms * 1e-3) / 1e12
+    sample = ("fp64 oracle, V2-Lite prefill, all 16 heads, last %d of 4096 query rows "
+              "(K/V rebuilt for all 4096 keys)" % rows)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64, N(0,1))",
+            "config": {"workload": "v2lite_prefill_s4096_h16", "sample_rows": rows},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args)
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

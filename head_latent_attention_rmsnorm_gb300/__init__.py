@@ -5,13 +5,6 @@ The compute lives in ``libmla.so`` (hand-written CUDA behind a C ABI, declared i
 names.  The binding loads the library on first use and raises if it is missing:
 there is no other implementation behind it.
 """
-from . import configs, inputs  # noqa: F401  (plain data and seeded generators)
+from . import configs, inputs, mla  # noqa: F401
 
 __all__ = ["configs", "inputs", "mla"]
-
-
-def __getattr__(name):
-    if name == "mla":
-        from . import mla
-        return mla
-    raise AttributeError(name)

@@ -1,0 +1,267 @@
+"""Thin ctypes binding of ``libmla.so`` (declared in ``include/mla.h``).
+
+Two layers, argument marshalling only:
+
+* ``mla_latent_attn_fwd`` ... ``mla_lse_combine``, the ``*_workspace`` queries,
+  ``mla_status_string``, ``mla_check_device_error``: the C entry points under their
+  own names, taking integers for pointers and sizes.
+* ``latent_attn_fwd``, ``absorbed_attn_fwd``, ``decode_splitkv``, ``lse_combine``:
+  the same calls taking torch tensors; they allocate any output or workspace the
+  caller did not pass (through torch's allocator, so the CUDA caching allocator sees
+  every byte) and raise :class:`MlaError` on a non-OK status.
+
+Every step of the computation runs in the library's CUDA kernels.  If the library
+is missing this module raises on first use; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla.so")
+
+MLA_F32, MLA_BF16 = 0, 1
+STATUS = {0: "MLA_OK", -1: "MLA_ERR_NULL", -2: "MLA_ERR_SHAPE", -3: "MLA_ERR_DTYPE", -4: "MLA_ERR_ALIGN",
+          -5: "MLA_ERR_WORKSPACE", -6: "MLA_ERR_UNSUPPORTED", -7: "MLA_ERR_CUDA",
+          -8: "MLA_ERR_DEVICE_TIMEOUT", -9: "MLA_ERR_ALIAS"}
+PATH_NONE, PATH_SIMT, PATH_TC = 0, 1, 2
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__("%s: %s" % (where, mla_status_string(status)))
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int), ("d_kv", ctypes.c_int), ("d_nope", ctypes.c_int),
+                ("d_rope", ctypes.c_int), ("d_v", ctypes.c_int), ("rope_base", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("softmax_scale", ctypes.c_float)]
+
+
+def dims(n_heads, d_kv, d_nope, d_rope, d_v, rope_base=10000.0, rms_eps=1e-6, softmax_scale=0.0) -> Dims:
+    return Dims(n_heads, d_kv, d_nope, d_rope, d_v, rope_base, rms_eps, softmax_scale)
+
+
+def dims_of(cfg) -> Dims:
+    """Dims of a workload from :mod:`.configs`."""
+    eps = getattr(cfg, "rms_eps", 1e-6)
+    return dims(cfg.n_heads, cfg.d_kv, cfg.d_nope, cfg.d_rope, cfg.d_v, cfg.rope_base, eps)
+
+
+_lib = None
+_vp, _i, _sz, _fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmla.so is not built (run: python -m head_latent_attention_rmsnorm_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        D = ctypes.POINTER(Dims)
+        fwd = [D, _i, _i, _i, _i, _i, _i, _i, _i, _i] + [_vp] * 8 + [_vp, _sz, _vp]
+        for f in ("mla_latent_attn_fwd", "mla_absorbed_attn_fwd"):
+            getattr(L, f).argtypes = fwd
+            getattr(L, f).restype = _i
+        L.mla_decode_splitkv.argtypes = [D, _i, _i, _i, _i] + [_vp] * 9 + [_vp, _sz, _vp]
+        L.mla_decode_splitkv.restype = _i
+        L.mla_lse_combine.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
+        L.mla_lse_combine.restype = _i
+        for f in ("mla_latent_attn_workspace", "mla_absorbed_attn_workspace"):
+            getattr(L, f).argtypes = [D, _i, _i, _i, _i, _i, _i, _i, _i]
+            getattr(L, f).restype = _sz
+        L.mla_decode_workspace.argtypes = [D, _i, _i, _i, _i]
+        L.mla_decode_workspace.restype = _sz
+        L.mla_status_string.argtypes = [_i]
+        L.mla_status_string.restype = ctypes.c_char_p
+        L.mla_check_device_error.argtypes = [_vp]
+        L.mla_check_device_error.restype = _i
+        L.mla_last_path.argtypes = []
+        L.mla_last_path.restype = _i
+        L.mla_set_path_override.argtypes = [_i]
+        L.mla_set_path_override.restype = None
+        L.mla_launch_count.argtypes = []
+        L.mla_launch_count.restype = ctypes.c_ulonglong
+        L.mla_profile_enable.argtypes = [_i]
+        L.mla_profile_enable.restype = None
+        L.mla_profile_reset.argtypes = []
+        L.mla_profile_reset.restype = None
+        L.mla_profile_kernel.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_longlong),
+                                         ctypes.POINTER(ctypes.c_double)]
+        L.mla_profile_kernel.restype = _i
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------ raw C entry points ----
+def mla_latent_attn_fwd(*args) -> int:
+    return lib().mla_latent_attn_fwd(*args)
+
+
+def mla_absorbed_attn_fwd(*args) -> int:
+    return lib().mla_absorbed_attn_fwd(*args)
+
+
+def mla_decode_splitkv(*args) -> int:
+    return lib().mla_decode_splitkv(*args)
+
+
+def mla_lse_combine(*args) -> int:
+    return lib().mla_lse_combine(*args)
+
+
+def mla_latent_attn_workspace(*args) -> int:
+    return lib().mla_latent_attn_workspace(*args)
+
+
+def mla_absorbed_attn_workspace(*args) -> int:
+    return lib().mla_absorbed_attn_workspace(*args)
+
+
+def mla_decode_workspace(*args) -> int:
+    return lib().mla_decode_workspace(*args)
+
+
+def mla_status_string(status: int) -> str:
+    return lib().mla_status_string(status).decode()
+
+
+def mla_check_device_error(stream: int | None = None) -> int:
+    return lib().mla_check_device_error(stream)
+
+
+def last_path() -> int:
+    return lib().mla_last_path()
+
+
+def set_path_override(mode: int) -> None:
+    lib().mla_set_path_override(mode)
+
+
+KERNELS = ("latent_prep", "rope_rows", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
+           "tc_latent_attn", "tc_combine", "transpose")
+
+
+def launch_count() -> int:
+    return lib().mla_launch_count()
+
+
+def profile_enable(on: bool) -> None:
+    lib().mla_profile_enable(int(on))
+
+
+def profile_reset() -> None:
+    lib().mla_profile_reset()
+
+
+def profile_kernel(name: str) -> tuple[int, float]:
+    """(launches, summed device ms) recorded for kernel ``name`` while profiling was on."""
+    n, ms = ctypes.c_longlong(0), ctypes.c_double(0.0)
+    if lib().mla_profile_kernel(name.encode(), ctypes.byref(n), ctypes.byref(ms)) != 0:
+        raise RuntimeError("mla_profile_kernel failed for " + name)
+    return n.value, ms.value
+
+
+def profile_all() -> dict:
+    out = {}
+    for k in KERNELS:
+        n, ms = profile_kernel(k)
+        if n:
+            out[k] = (n, ms)
+    return out
+
+
+# ------------------------------------------------------------- tensor wrappers ----
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MLA_F32
+    if t.dtype == torch.bfloat16:
+        return MLA_BF16
+    raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MlaError(status, where)
+
+
+def _workspace(nbytes: int, device, workspace):
+    if workspace is not None:
+        return workspace
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def latent_attn_fwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, q_offset=0, causal=True,
+                    head_begin=0, head_shard=0, out=None, lse=None, workspace=None, stream=None,
+                    absorbed=False):
+    """Explicit (or, with ``absorbed=True``, absorbed) MLA prefill.  Returns (out, lse)."""
+    B, s_q, hc, _ = q_nope.shape
+    s_kv = c_kv.shape[1]
+    dt = _dt(q_nope)
+    if out is None:
+        out = torch.empty(B, s_q, hc, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty(B, hc, s_q, dtype=torch.float32, device=q_nope.device)
+    wsq = mla_absorbed_attn_workspace if absorbed else mla_latent_attn_workspace
+    nbytes = wsq(ctypes.byref(d), dt, B, s_q, s_kv, q_offset, int(causal), hc, head_shard)
+    ws = _workspace(nbytes, q_nope.device, workspace)
+    fn = mla_absorbed_attn_fwd if absorbed else mla_latent_attn_fwd
+    st = fn(ctypes.byref(d), dt, B, s_q, s_kv, q_offset, int(causal), head_begin, hc, head_shard,
+            _ptr(q_nope), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe), _ptr(w_kv_b), _ptr(rms_w), _ptr(out),
+            _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, fn.__name__)
+    return out, lse
+
+
+def absorbed_attn_fwd(d: Dims, *args, **kw):
+    return latent_attn_fwd(d, *args, absorbed=True, **kw)
+
+
+def decode_splitkv(d: Dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_splits=1, out=None, lse=None,
+                   part_out=None, part_lse=None, workspace=None, stream=None):
+    """Split-KV latent decode.  Returns (out, lse)."""
+    B, H, _ = q_nope.shape
+    L = c_cache.shape[1]
+    dt = _dt(q_nope)
+    if out is None:
+        out = torch.empty(B, H, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q_nope.device)
+    nbytes = mla_decode_workspace(ctypes.byref(d), dt, B, L, n_splits)
+    ws = _workspace(nbytes, q_nope.device, workspace)
+    st = mla_decode_splitkv(ctypes.byref(d), dt, B, L, n_splits, _ptr(q_nope), _ptr(q_pe), _ptr(c_cache),
+                            _ptr(kpe_cache), _ptr(w_kv_b), _ptr(out), _ptr(lse), _ptr(part_out),
+                            _ptr(part_lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "mla_decode_splitkv")
+    return out, lse
+
+
+def lse_combine(part_out, part_lse, *, out_dtype=torch.float32, out=None, lse=None, stream=None):
+    """Merge fp32 split partials [n, rows, D] / [n, rows].  Returns (out, lse)."""
+    n, rows, D = part_out.shape
+    if out is None:
+        out = torch.empty(rows, D, dtype=out_dtype, device=part_out.device)
+    if lse is None:
+        lse = torch.empty(rows, dtype=torch.float32, device=part_out.device)
+    st = mla_lse_combine(_dt(out), n, rows, D, _ptr(part_out), _ptr(part_lse), _ptr(out), _ptr(lse),
+                         _stream(stream))
+    _check(st, "mla_lse_combine")
+    return out, lse

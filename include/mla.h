@@ -1,0 +1,195 @@
+/*
+ * mla.h -- C ABI of libmla: multi-head latent attention (MLA) computed from the
+ * compressed latent, on one GB300 GPU (sm_103a).
+ *
+ * What the library computes (pages cited by title and section):
+ *  - "A Training-Memory Regression in MLA Sequence Parallelism ... LAGA"
+ *    (arXiv 2607.17644), "What carries the argument" and Fig. 2: the per-rank
+ *    compute of LAGA -- RMSNorm of the gathered latent c_KV, per-head K_nope/V
+ *    rebuilt locally through W_kv_b one head shard at a time (the paper's section
+ *    3.3 "H_r slice of W_kv_b(latent)"), decoupled RoPE on q_pe and on the k_pe
+ *    band shared by all heads, causal softmax attention, output plus log-sum-exp.
+ *    The absorbed form (q_absorbed = W_kv_b^T q_nope, latent-space attention,
+ *    un-absorb) is the companion path of the same figure.
+ *  - "TPLA: Tensor Parallel Latent Attention ..." (arXiv 2508.15881), "What
+ *    carries the argument": the latent normalisation is an RMSNorm.
+ *  - "Helix Parallelism ..." (arXiv 2507.07120), "What carries the argument" and
+ *    "Assumptions" (paper section 2.1.1): split-KV partial outputs and their
+ *    log-sum-exp scalars are rescaled and summed into the exact softmax output.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are dense, row-major, contiguous, in device memory (except where
+ *    stated), and every pointer must be 16-byte aligned.  The caller owns all
+ *    memory; the library never allocates device memory.  Scratch memory is the
+ *    caller's `workspace` (size from the matching *_workspace query).
+ *  - `mla_dtype` selects the storage type of every floating-point tensor except
+ *    the log-sum-exp and the split partials, which are always fp32.  Arithmetic is
+ *    fp32 (bf16 tensor-core products accumulate in fp32).
+ *  - Calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and do no host synchronisation, except mla_check_device_error.
+ *  - Inputs are never written.  Outputs and the workspace may not overlap any
+ *    input or each other (MLA_ERR_ALIAS).
+ *  - On any error status nothing has been launched, except MLA_ERR_CUDA, which
+ *    reports a failed launch or failed CUDA runtime call.
+ *  - Positions: query row i of a prefill call sits at absolute position q_offset+i,
+ *    key j at position j; a decode query sits at kv_len-1.  RoPE pairs (t, t+d/2)
+ *    with angle pos * rope_base^(-2t/d_rope).  Causal: key j visible iff
+ *    j <= q_offset + i.  LSE is the natural log of the softmax normaliser (scale
+ *    included); a row that sees no key gives lse = -inf and output 0.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_NULL = -1,           /* a required pointer is NULL                       */
+    MLA_ERR_SHAPE = -2,          /* a size, offset or head range is out of range      */
+    MLA_ERR_DTYPE = -3,          /* unknown mla_dtype                                 */
+    MLA_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned                  */
+    MLA_ERR_WORKSPACE = -5,      /* workspace_bytes below the *_workspace figure      */
+    MLA_ERR_UNSUPPORTED = -6,    /* dimensions this build has no kernel for           */
+    MLA_ERR_CUDA = -7,           /* a CUDA runtime call or kernel launch failed       */
+    MLA_ERR_DEVICE_TIMEOUT = -8, /* a bounded device-side wait gave up (see below)    */
+    MLA_ERR_ALIAS = -9           /* an output/workspace overlaps an input or another  */
+} mla_status;
+
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/* Per-model dimensions and constants. */
+typedef struct {
+    int n_heads;         /* H: query heads of the model                         */
+    int d_kv;            /* latent width of c_KV (512 for DeepSeek-V3)          */
+    int d_nope;          /* per-head non-rotary q/k width (128)                 */
+    int d_rope;          /* decoupled RoPE band width (64), even                */
+    int d_v;             /* per-head value width (128)                          */
+    float rope_base;     /* RoPE base (10000)                                   */
+    float rms_eps;       /* RMSNorm epsilon inside the square root (1e-6)       */
+    float softmax_scale; /* <= 0 selects 1/sqrt(d_nope + d_rope)                */
+} mla_dims;
+
+/*
+ * Prefill, explicit / LAGA per-rank compute.
+ * Queries are rows [q_offset, q_offset+s_q) of a sequence whose full latent of
+ * s_kv tokens is given (a simulated sequence-parallel rank when q_offset > 0).
+ * Heads [head_begin, head_begin+head_count) are computed; per-head K_nope/V are
+ * rebuilt head_shard heads at a time (0 = all at once) into the workspace, so the
+ * workspace grows with head_shard, not with head_count.
+ *   q_nope [B, s_q, head_count, d_nope]     q_pe [B, s_q, head_count, d_rope] (not rotated)
+ *   c_kv   [B, s_kv, d_kv]                  k_pe [B, s_kv, d_rope] (not rotated)
+ *   w_kv_b [n_heads*(d_nope+d_v), d_kv]: head h owns rows h*(d_nope+d_v) ..,
+ *          first d_nope rows -> K_nope, next d_v rows -> V
+ *   rms_w  [d_kv]
+ *   out    [B, s_q, head_count, d_v]        lse (fp32) [B, head_count, s_q]
+ * Causal calls need q_offset + s_q <= s_kv.  B, s_q or head_count of 0 is a no-op.
+ */
+mla_status mla_latent_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
+                               int q_offset, int causal, int head_begin, int head_count,
+                               int head_shard, const void *q_nope, const void *q_pe,
+                               const void *c_kv, const void *k_pe, const void *w_kv_b,
+                               const void *rms_w, void *out, float *lse, void *workspace,
+                               size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * Prefill, absorbed form (same arguments, layouts and result as
+ * mla_latent_attn_fwd): q_abs = W_K(h)^T q_nope (d_kv wide) and the latent
+ * accumulator o_lat (d_kv wide) are materialised per head shard in the
+ * workspace, then out = W_V(h) o_lat.  This is the companion path whose larger
+ * activation footprint the LAGA page measures.
+ */
+mla_status mla_absorbed_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
+                                 int q_offset, int causal, int head_begin, int head_count,
+                                 int head_shard, const void *q_nope, const void *q_pe,
+                                 const void *c_kv, const void *k_pe, const void *w_kv_b,
+                                 const void *rms_w, void *out, float *lse, void *workspace,
+                                 size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * Decode over a latent cache: one query per sequence at position kv_len-1, all
+ * n_heads heads, absorbed-form scores, keys split into n_splits contiguous chunks
+ * of ceil(kv_len/n_splits) (the last may be short or empty), partials merged by the
+ * log-sum-exp rescale.  The cache holds already-normalised c_KV and already-rotated
+ * k_pe (what a prefill writes); q_pe is given un-rotated.
+ *   q_nope [B, H, d_nope]   q_pe [B, H, d_rope]   c_cache [B, kv_len, d_kv]
+ *   kpe_cache [B, kv_len, d_rope]   w_kv_b as above   out [B, H, d_v]   lse (fp32) [B, H]
+ *   part_out (fp32, optional) [n_splits, B, H, d_kv]: per-split latent output,
+ *            normalised within the split;  part_lse (fp32, optional) [n_splits, B, H].
+ *   Pass both NULL to keep the partials in the workspace.
+ * 1 <= n_splits <= 256.  kv_len >= 1.
+ */
+mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int kv_len,
+                              int n_splits, const void *q_nope, const void *q_pe,
+                              const void *c_cache, const void *kpe_cache, const void *w_kv_b,
+                              void *out, float *lse, float *part_out, float *part_lse,
+                              void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * Log-sum-exp merge (Helix / Flash-Decoding combine):
+ *   lse[r] = log sum_s exp(part_lse[s][r]);  out[r][:] = sum_s exp(part_lse[s][r]-lse[r]) part_out[s][r][:]
+ * part_out fp32 [n_splits, rows, D], part_lse fp32 [n_splits, rows] -> out (out_dtype)
+ * [rows, D], lse fp32 [rows].  Splits with part_lse = -inf carry no weight.
+ * 1 <= n_splits <= 256.
+ */
+mla_status mla_lse_combine(mla_dtype out_dtype, int n_splits, int rows, int D,
+                           const float *part_out, const float *part_lse, void *out, float *lse,
+                           void *cuda_stream);
+
+/* Workspace bytes the matching call needs (0 on invalid arguments). */
+size_t mla_latent_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
+                                 int q_offset, int causal, int head_count, int head_shard);
+size_t mla_absorbed_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
+                                   int q_offset, int causal, int head_count, int head_shard);
+size_t mla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits);
+
+/* Static description of a status code. */
+const char *mla_status_string(mla_status status);
+
+/*
+ * Synchronises `cuda_stream`, then reads and clears the device-side error word.
+ * Kernels that spin on an mbarrier bound every wait by an iteration limit; when a
+ * limit is hit the kernel records it in that word and leaves without trapping.
+ * Returns MLA_ERR_DEVICE_TIMEOUT if any did since the last check, MLA_ERR_CUDA if
+ * the stream reports an error, MLA_OK otherwise.
+ */
+mla_status mla_check_device_error(void *cuda_stream);
+
+/*
+ * Which kernel family the last call on this host thread used, for tests and the
+ * benchmark: 0 = none yet, 1 = SIMT (CUDA cores, any dimensions, fp32 or bf16),
+ * 2 = tensor cores (tcgen05 + TMA, bf16 at the DeepSeek dimensions).
+ */
+int mla_last_path(void);
+
+/* Overrides the path choice on this host thread: 0 = automatic (default),
+ * 1 = force the SIMT kernels.  Used by tests to compare the two families. */
+void mla_set_path_override(int mode);
+
+/*
+ * Measurement hooks (not part of the computation).
+ * mla_launch_count: kernels this library has launched since load, all threads.
+ * mla_profile_enable(1): from now on every launch is bracketed by a pair of CUDA
+ *   events recorded on the launching stream (the caller's stream), grouped by
+ *   kernel name; mla_profile_enable(0) stops recording and drops what was recorded.
+ * mla_profile_kernel: synchronises the recorded events of kernel `name` and returns
+ *   the number of launches and their summed device time in milliseconds (0 launches
+ *   for an unknown name).  Names: "latent_prep", "rope_rows", "gemm_simt",
+ *   "attn_simt", "lse_combine", "tc_gemm", "tc_attn", "tc_latent_attn",
+ *   "tc_combine", "transpose".
+ * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
+ * Not thread-safe: profile from one host thread at a time.
+ */
+unsigned long long mla_launch_count(void);
+void mla_profile_enable(int on);
+int mla_profile_kernel(const char *name, long long *launches, double *total_ms);
+void mla_profile_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

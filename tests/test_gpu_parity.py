@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle on the same
+seeded inputs, element by element, plus GPU-side invariants (query-shard and
+head-range concatenation, split counts, explicit vs absorbed)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from head_latent_attention_rmsnorm_gb300 import build as mla_build
+from head_latent_attention_rmsnorm_gb300 import configs, inputs, mla
+
+from parity import check_lse, check_out, np_inputs, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    mla_build.build()
+    mla.lib()
+    yield
+    torch.cuda.synchronize()
+    assert mla.mla_check_device_error(None) == 0
+
+
+def dev(inp):
+    return {k: v.cuda() for k, v in inp.items()}
+
+
+def run_prefill(cfg, inp, *, absorbed=False, q_offset=None, head_begin=0, head_shard=None, causal=None):
+    d = mla.dims_of(cfg)
+    q_offset = cfg.q_offset if q_offset is None else q_offset
+    causal = cfg.causal if causal is None else causal
+    hs = cfg.head_shard if head_shard is None else head_shard
+    out, lse = mla.latent_attn_fwd(d, inp["q_nope"], inp["q_pe"], inp["c_kv"], inp["k_pe"], inp["w_kv_b"],
+                                   inp["rms_w"], q_offset=q_offset, causal=causal, head_begin=head_begin,
+                                   head_shard=hs, absorbed=absorbed)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_prefill(oracle, cfg, inp, *, absorbed=False, q_offset=None, head_begin=0, causal=None):
+    fn = oracle.mla_absorbed if absorbed else oracle.mla_explicit
+    n = np_inputs(inp)
+    return fn(**n, n_heads=cfg.n_heads, q_offset=cfg.q_offset if q_offset is None else q_offset,
+              causal=cfg.causal if causal is None else causal, head_begin=head_begin, base=cfg.rope_base,
+              eps=cfg.rms_eps)
+
+
+# ------------------------------------------------------------------- tiny fp32 ----
+@pytest.mark.parametrize("absorbed", [False, True])
+def test_tiny_fp32_full(oracle, absorbed):
+    cfg = configs.TINY
+    inp = inputs.prefill_inputs(cfg)
+    out, lse = run_prefill(cfg, dev(inp), absorbed=absorbed)
+    ro, rl = oracle_prefill(oracle, cfg, inp, absorbed=absorbed)
+    check_out(out, ro, torch.float32)
+    check_lse(lse, rl)
+
+
+def test_tiny_fp32_matches_golden_rows():
+    import os
+    cfg = configs.TINY
+    out, lse = run_prefill(cfg, dev(inputs.prefill_inputs(cfg)))
+    path = os.path.join(os.path.dirname(__file__), "golden", "tiny_fp32_oracle_rows.txt")
+    for line in open(path):
+        if line.startswith("#"):
+            continue
+        f = line.split()
+        i, h = int(f[0]), int(f[1])
+        assert abs(lse[0, h, i].item() - float(f[2])) <= 1e-3
+        np.testing.assert_allclose(to64(out[0, i, h, :8]), [float(x) for x in f[3:]], rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("absorbed", [False, True])
+def test_tiny_fp32_sp_shards(oracle, absorbed):
+    cfg = configs.TINY
+    full_in = inputs.prefill_inputs(cfg, q_rows=(0, cfg.s_kv))
+    full_o, full_l = run_prefill(cfg, dev(full_in), absorbed=absorbed, q_offset=0)
+    parts_o, parts_l = [], []
+    for off in cfg.sweep_offsets:
+        rows = (off, off + cfg.s_kv // len(cfg.sweep_offsets))
+        inp = inputs.prefill_inputs(cfg, q_rows=rows)
+        o, l = run_prefill(cfg, dev(inp), absorbed=absorbed, q_offset=off)
+        ro, rl = oracle_prefill(oracle, cfg, inp, absorbed=absorbed, q_offset=off)
+        check_out(o, ro, torch.float32, "shard@%d" % off)
+        check_lse(l, rl, "shard lse@%d" % off)
+        parts_o.append(o)
+        parts_l.append(l)
+    assert torch.equal(torch.cat(parts_o, 1), full_o)
+    assert torch.equal(torch.cat(parts_l, 2), full_l)
+
+
+def test_tiny_fp32_head_range_noncausal(oracle):
+    cfg = configs.TINY
+    inp = inputs.prefill_inputs(cfg)
+    sub = dict(inp, q_nope=inp["q_nope"][:, :, 1:3].contiguous(), q_pe=inp["q_pe"][:, :, 1:3].contiguous())
+    for causal in (True, False):
+        o, l = run_prefill(cfg, dev(sub), head_begin=1, head_shard=1, causal=causal)
+        ro, rl = oracle_prefill(oracle, cfg, sub, head_begin=1, causal=causal)
+        check_out(o, ro, torch.float32)
+        check_lse(l, rl)
+
+
+# --------------------------------------------------------------- ragged bf16 ----
+RAGGED = configs.Prefill("ragged_bf16", "bf16", batch=2, s_kv=300, s_q=200, q_offset=77, n_heads=8,
+                         d_kv=512, d_nope=128, d_rope=64, d_v=128, head_shard=3)
+
+
+@pytest.mark.parametrize("absorbed", [False, True])
+def test_ragged_bf16(oracle, absorbed):
+    cfg = RAGGED
+    inp = inputs.prefill_inputs(cfg)
+    sub = dict(inp, q_nope=inp["q_nope"][:, :, 2:7].contiguous(), q_pe=inp["q_pe"][:, :, 2:7].contiguous())
+    o, l = run_prefill(cfg, dev(sub), absorbed=absorbed, head_begin=2)
+    ro, rl = oracle_prefill(oracle, cfg, sub, absorbed=absorbed, head_begin=2)
+    check_out(o, ro, torch.bfloat16)
+    check_lse(l, rl)
+
+
+def test_ragged_bf16_noncausal_small_kv(oracle):
+    cfg = dataclasses.replace(RAGGED, s_kv=37, s_q=50, q_offset=3, causal=False, batch=1)
+    inp = inputs.prefill_inputs(cfg)
+    o, l = run_prefill(cfg, dev(inp))
+    ro, rl = oracle_prefill(oracle, cfg, inp)
+    check_out(o, ro, torch.bfloat16)
+    check_lse(l, rl)
+
+
+# --------------------------------------------------------- full-size prefill ----
+def test_v2lite_full(oracle):
+    cfg = configs.V2LITE
+    inp = inputs.prefill_inputs(cfg)
+    o, l = run_prefill(cfg, dev(inp))
+    ro, rl = oracle_prefill(oracle, cfg, inp)
+    check_out(o, ro, torch.bfloat16)
+    check_lse(l, rl)
+
+
+def test_v3_sampled_heads_and_absorbed(oracle):
+    cfg = configs.V3
+    inp = inputs.prefill_inputs(cfg)
+    d_in = dev(inp)
+    o, l = run_prefill(cfg, d_in)
+    for h0, hc in ((0, 2), (77, 1), (127, 1)):
+        sub = dict(inp, q_nope=inp["q_nope"][:, :, h0:h0 + hc], q_pe=inp["q_pe"][:, :, h0:h0 + hc])
+        ro, rl = oracle_prefill(oracle, cfg, sub, head_begin=h0)
+        check_out(o[:, :, h0:h0 + hc], ro, torch.bfloat16, "v3 heads %d+%d" % (h0, hc))
+        check_lse(l[:, h0:h0 + hc], rl)
+    oa, la = run_prefill(cfg, d_in, absorbed=True)
+    check_out(oa, o.float(), torch.bfloat16, "absorbed vs explicit")
+    check_lse(la, l)
+
+
+def test_v3_activation_memory_explicit_below_absorbed():
+    """LAGA, "What carries the argument": the explicit form's per-token intermediates
+    (n_h x (d_nope + d_v)) are smaller than the absorbed form's (n_h x d_kv)."""
+    cfg = configs.V3
+    d_in = dev(inputs.prefill_inputs(cfg))
+    peaks = {}
+    for absorbed in (False, True):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        run_prefill(cfg, d_in, absorbed=absorbed, head_shard=cfg.n_heads)
+        peaks[absorbed] = torch.cuda.max_memory_allocated() - base
+    assert peaks[False] < peaks[True]
+
+
+def test_sp8_rank_sweep_concatenates_and_matches_oracle(oracle):
+    cfg = configs.SP8_RANK7
+    S = cfg.s_kv
+    full_in = dev(inputs.prefill_inputs(cfg, q_rows=(0, S)))
+    full_o, full_l = run_prefill(cfg, full_in, q_offset=0)
+    outs, lses = [], []
+    for off in cfg.sweep_offsets:
+        sl = slice(off, off + cfg.s_q)
+        rank_in = dict(full_in, q_nope=full_in["q_nope"][:, sl].contiguous(),
+                       q_pe=full_in["q_pe"][:, sl].contiguous())
+        o, l = run_prefill(cfg, rank_in, q_offset=off)
+        outs.append(o)
+        lses.append(l)
+    assert torch.equal(torch.cat(outs, 1), full_o), "rank outputs do not concatenate to SP=1"
+    assert torch.equal(torch.cat(lses, 2), full_l)
+    # oracle on sampled rows/heads of the last rank (query offset 14336)
+    rank7 = outs[-1]
+    for q0, h0 in ((cfg.q_offset, 0), (cfg.q_offset + 1000, 64), (S - 48, 127)):
+        n = 48
+        inp = inputs.prefill_inputs(cfg, q_rows=(q0, q0 + n))
+        sub = dict(inp, q_nope=inp["q_nope"][:, :, h0:h0 + 1], q_pe=inp["q_pe"][:, :, h0:h0 + 1])
+        ro, rl = oracle_prefill(oracle, cfg, sub, q_offset=q0, head_begin=h0)
+        i0 = q0 - cfg.q_offset
+        check_out(rank7[:, i0:i0 + n, h0:h0 + 1], ro, torch.bfloat16, "rank7 rows %d head %d" % (q0, h0))
+        check_lse(lses[-1][:, h0:h0 + 1, i0:i0 + n], rl)
+
+
+# ------------------------------------------------------------------- decode ----
+def run_decode(cfg, inp, n_splits, partials=True):
+    d = mla.dims(cfg.n_heads, cfg.d_kv, cfg.d_nope, cfg.d_rope, cfg.d_v, cfg.rope_base)
+    B, H = cfg.batch, cfg.n_heads
+    po = torch.empty(n_splits, B, H, cfg.d_kv, device="cuda") if partials else None
+    pl = torch.empty(n_splits, B, H, device="cuda") if partials else None
+    o, l = mla.decode_splitkv(d, inp["q_nope"], inp["q_pe"], inp["c_cache"], inp["kpe_cache"], inp["w_kv_b"],
+                              n_splits=n_splits, part_out=po, part_lse=pl)
+    torch.cuda.synchronize()
+    return o, l, po, pl
+
+
+def test_decode_full_size(oracle):
+    cfg = configs.DECODE
+    inp = inputs.decode_inputs(cfg)
+    o, l, po, pl = run_decode(cfg, dev(inp), cfg.n_splits)
+    for b in (0, 37, 63):
+        sub = inputs.decode_inputs(cfg, batches=(b, b + 1))
+        n = np_inputs(sub)
+        ro, rl, rpo, rpl = oracle.mla_decode(**n, n_splits=cfg.n_splits, base=cfg.rope_base)
+        check_out(o[b:b + 1], ro, torch.bfloat16, "decode out b=%d" % b)
+        check_lse(l[b:b + 1], rl, "decode lse b=%d" % b)
+        check_out(po[:, b:b + 1], rpo, torch.bfloat16, "partials b=%d" % b)
+        check_lse(pl[:, b:b + 1], rpl, "partial lse b=%d" % b)
+
+
+@pytest.mark.parametrize("dtype,L,n_splits", [
+    ("bf16", 1000, 1), ("bf16", 1000, 2), ("bf16", 1000, 8), ("bf16", 1000, 13), ("bf16", 5, 8),
+    ("bf16", 1, 1), ("f32", 333, 13), ("f32", 64, 3)])
+def test_decode_splits(oracle, dtype, L, n_splits):
+    if dtype == "bf16":
+        cfg = dataclasses.replace(configs.DECODE, batch=3, kv_len=L, n_splits=n_splits)
+    else:
+        cfg = configs.Decode("dec_f32", "f32", batch=2, kv_len=L, n_splits=n_splits, n_heads=4, d_kv=64,
+                             d_nope=32, d_rope=16, d_v=32)
+    inp = inputs.decode_inputs(cfg)
+    o, l, po, pl = run_decode(cfg, dev(inp), n_splits)
+    ro, rl, rpo, rpl = oracle.mla_decode(**np_inputs(inp), n_splits=n_splits, base=cfg.rope_base)
+    check_out(o, ro, cfg.torch_dtype)
+    check_lse(l, rl)
+    check_out(po, rpo, cfg.torch_dtype, "partials")
+    check_lse(pl, rpl, "partial lse")
+    o2, l2, _, _ = run_decode(cfg, dev(inp), n_splits, partials=False)
+    assert torch.equal(o2, o) and torch.equal(l2, l)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_lse_combine(oracle, out_dtype):
+    g = np.random.default_rng(5)
+    n, rows, D = 7, 300, 136
+    po = g.standard_normal((n, rows, D)).astype(np.float32)
+    pl = (4 * g.standard_normal((n, rows))).astype(np.float32)
+    pl[3, :40] = -np.inf
+    pl[:, 7] = -np.inf                       # a row with no keys at all
+    po[:, 7] = 0
+    o, l = mla.lse_combine(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda(), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ro, rl = oracle.lse_combine(po, pl)
+    check_out(o, ro, out_dtype)
+    check_lse(l, rl)
+
+
+def test_empty_calls_are_noops():
+    cfg = configs.TINY
+    inp = dev(inputs.prefill_inputs(cfg))
+    d = mla.dims_of(cfg)
+    z = {k: (v[:, :0] if k in ("q_nope", "q_pe") else v) for k, v in inp.items()}
+    o, l = mla.latent_attn_fwd(d, z["q_nope"], z["q_pe"], z["c_kv"], z["k_pe"], z["w_kv_b"], z["rms_w"])
+    assert o.shape[1] == 0 and l.shape[2] == 0
