@@ -1,6 +1,14 @@
 // mla_api.cu -- the C ABI of libmla: argument validation, workspace layout and the
 // sequence of kernel launches for each entry point.  See include/mla.h for the
 // contract of every call.
+//
+// Two kernel families sit behind each entry point:
+//  * tensor cores (tcgen05 + TMA, tc_*.cu) for bf16 calls at the dimensions they
+//    were written for; their intermediates (normalised latent, rotated RoPE bands,
+//    K_nope, V^T, q_abs, o_lat) are stored as fp16, whose 11-bit significand keeps
+//    every score within ~3e-4 of exact;
+//  * CUDA cores (simt.cu) for fp32 calls and any other shape; their intermediates
+//    are fp32.
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -17,7 +25,6 @@ using namespace mla;
 thread_local int g_last_path = 0;
 thread_local int g_path_override = 0;
 
-inline size_t el_size(mla_dtype dt) { return dt == MLA_F32 ? 4 : 2; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Bump allocator over the caller's workspace; every sub-buffer is 256-byte aligned.
@@ -77,18 +84,18 @@ mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_E
 struct Prefill {
     int B, s_q, s_kv, q_offset, causal, head_begin, head_count, hs, n_shards;
     int Dk, Dn, Dr, Dv, H;
-    long kv_need;
+    long kv_need, kv_pad;
     bool tc;
+    int tin, tmid;   // storage of inputs, of intermediates
 };
 
-mla_status prefill_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_kv, int q_offset,
-                         int causal, int head_begin, int head_count, int head_shard, bool absorbed,
-                         Prefill *p) {
+mla_status prefill_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_kv, int q_offset, int causal,
+                         int head_begin, int head_count, int head_shard, bool absorbed, Prefill *p) {
     mla_status st = check_dims(d);
     if (st != MLA_OK) return st;
     if (!valid_dtype(dt)) return MLA_ERR_DTYPE;
-    if (B < 0 || s_q < 0 || s_kv < 0 || q_offset < 0 || head_begin < 0 || head_count < 0 ||
-        head_shard < 0 || head_begin + head_count > d->n_heads)
+    if (B < 0 || s_q < 0 || s_kv < 0 || q_offset < 0 || head_begin < 0 || head_count < 0 || head_shard < 0 ||
+        head_begin + head_count > d->n_heads)
         return MLA_ERR_SHAPE;
     if (causal && (long)q_offset + s_q > s_kv) return MLA_ERR_SHAPE;
     p->B = B;
@@ -106,85 +113,88 @@ mla_status prefill_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_
     p->Dv = d->d_v;
     p->H = d->n_heads;
     p->kv_need = causal ? (long)q_offset + s_q : s_kv;
+    p->kv_pad = (p->kv_need + 127) / 128 * 128;
     // SIMT register limits of the attention kernel
     if (!absorbed && (p->Dn + p->Dr > 640 || p->Dv > 512)) return MLA_ERR_UNSUPPORTED;
     if (absorbed && (p->Dk + p->Dr > 640 || p->Dk > 512)) return MLA_ERR_UNSUPPORTED;
     p->tc = false;
-    if (dt == MLA_BF16 && g_path_override != 1) {
+    if (dt == MLA_BF16 && g_path_override != 1 && p->kv_need >= 1) {
         p->tc = absorbed ? tc_absorbed_supported(p->Dk, p->Dn, p->Dr, p->Dv)
                          : tc_explicit_supported(p->Dk, p->Dn, p->Dr, p->Dv);
     }
+    p->tin = ty_of(dt);
+    p->tmid = p->tc ? TY_F16 : TY_F32;
     return MLA_OK;
 }
 
 struct PrefillWs {
-    void *chat, *kpe, *qpe, *k, *v, *qabs, *olat, *wukt;
+    void *chat, *kpe, *qpe, *k, *v, *qabs, *olat, *w16;
     size_t bytes;
 };
 
-PrefillWs prefill_ws(const Prefill &p, mla_dtype dt, bool absorbed, void *base) {
+PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
     Carve c;
     c.base = (char *)base;
     PrefillWs w{};
-    size_t es = el_size(dt);
-    long kv_pad = (p.kv_need + 127) / 128 * 128;
-    w.chat = c.take((size_t)p.B * kv_pad * p.Dk * es);
-    w.kpe = c.take((size_t)p.B * kv_pad * p.Dr * es);
+    const size_t es = ty_size(p.tmid);
+    w.chat = c.take((size_t)p.B * p.kv_pad * p.Dk * es);
+    w.kpe = c.take((size_t)p.B * p.kv_pad * p.Dr * es);
     w.qpe = c.take((size_t)p.B * p.s_q * p.head_count * p.Dr * es);
+    if (p.tc) w.w16 = c.take((size_t)p.hs * (p.Dn + p.Dv) * p.Dk * 2);
     if (!absorbed) {
         // per-shard K_nope and V (tensor-core path: V stored transposed)
-        w.k = c.take((size_t)p.B * p.hs * kv_pad * p.Dn * es);
-        w.v = c.take((size_t)p.B * p.hs * kv_pad * p.Dv * es);
+        w.k = c.take((size_t)p.B * p.hs * p.kv_pad * p.Dn * es);
+        w.v = c.take((size_t)p.B * p.hs * p.kv_pad * p.Dv * es);
     } else {
+        // per-shard absorbed intermediates: q_abs and the latent accumulator, d_kv wide
         w.qabs = c.take((size_t)p.B * p.s_q * p.hs * p.Dk * es);
         w.olat = c.take((size_t)p.B * p.s_q * p.hs * p.Dk * es);
-        if (p.tc) w.wukt = c.take((size_t)p.hs * p.Dk * p.Dn * es);
     }
     w.bytes = align_up(c.off, 256);
     return w;
 }
 
-mla_status prefill_common_checks(const Prefill &p, mla_dtype dt, bool absorbed, const void *q_nope,
-                                 const void *q_pe, const void *c_kv, const void *k_pe,
-                                 const void *w_kv_b, const void *rms_w, void *out, float *lse,
-                                 void *workspace, size_t workspace_bytes) {
-    size_t es = el_size(dt);
+mla_status prefill_common_checks(const Prefill &p, bool absorbed, const void *q_nope, const void *q_pe,
+                                 const void *c_kv, const void *k_pe, const void *w_kv_b, const void *rms_w,
+                                 void *out, float *lse, void *workspace, size_t workspace_bytes) {
+    const size_t es = ty_size(p.tin);
     const void *ptrs[] = {q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse};
     for (const void *q : ptrs)
         if (!q) return MLA_ERR_NULL;
     for (const void *q : ptrs)
         if (!aligned16(q)) return MLA_ERR_ALIGN;
-    PrefillWs w = prefill_ws(p, dt, absorbed, nullptr);
+    PrefillWs w = prefill_ws(p, absorbed, nullptr);
     if (workspace_bytes < w.bytes) return MLA_ERR_WORKSPACE;
     if (w.bytes && !workspace) return MLA_ERR_NULL;
     if (workspace && !aligned16(workspace)) return MLA_ERR_ALIGN;
     size_t nq = (size_t)p.B * p.s_q * p.head_count;
-    Range in[] = {rng(q_nope, nq * p.Dn * es), rng(q_pe, nq * p.Dr * es),
-                  rng(c_kv, (size_t)p.B * p.s_kv * p.Dk * es), rng(k_pe, (size_t)p.B * p.s_kv * p.Dr * es),
-                  rng(w_kv_b, (size_t)p.H * (p.Dn + p.Dv) * p.Dk * es), rng(rms_w, (size_t)p.Dk * es)};
+    Range in[] = {rng(q_nope, nq * p.Dn * es),
+                  rng(q_pe, nq * p.Dr * es),
+                  rng(c_kv, (size_t)p.B * p.s_kv * p.Dk * es),
+                  rng(k_pe, (size_t)p.B * p.s_kv * p.Dr * es),
+                  rng(w_kv_b, (size_t)p.H * (p.Dn + p.Dv) * p.Dk * es),
+                  rng(rms_w, (size_t)p.Dk * es)};
     Range outs[] = {rng(out, nq * p.Dv * es), rng(lse, nq * 4), rng(workspace, w.bytes)};
     return check_alias(in, 6, outs, 3);
 }
 
 // Common first steps of both prefill forms: normalised latent, rotated k_pe and q_pe.
-mla_status prefill_prep(const Prefill &p, mla_dtype dt, const mla_dims *d, const void *q_pe,
-                        const void *c_kv, const void *k_pe, const void *rms_w, const PrefillWs &w,
-                        cudaStream_t st) {
-    int kv_pad = (int)((p.kv_need + 127) / 128 * 128);
-    MLA_TRY(launch_latent_prep(dt, p.B, p.s_kv, (int)p.kv_need, kv_pad, p.Dk, p.Dr, c_kv, k_pe, rms_w,
-                               d->rms_eps, d->rope_base, w.chat, w.kpe, st));
+mla_status prefill_prep(const Prefill &p, const mla_dims *d, const void *q_pe, const void *c_kv, const void *k_pe,
+                        const void *rms_w, const PrefillWs &w, cudaStream_t st) {
+    MLA_TRY(launch_latent_prep(p.tin, p.tmid, p.B, p.s_kv, (int)p.kv_need, (int)p.kv_pad, p.Dk, p.Dr, c_kv, k_pe,
+                               rms_w, d->rms_eps, d->rope_base, w.chat, w.kpe, st));
     long rows = (long)p.B * p.s_q * p.head_count;
-    MLA_TRY(launch_rope_rows(dt, rows, p.Dr, q_pe, p.q_offset, p.head_count, p.s_q, d->rope_base,
-                             w.qpe, st));
+    MLA_TRY(launch_rope_rows(p.tin, p.tmid, rows, p.Dr, q_pe, p.q_offset, p.head_count, p.s_q, d->rope_base, w.qpe,
+                             st));
     return MLA_OK;
 }
 
 // ------------------------------------------------------ explicit, SIMT ----
-mla_status explicit_simt(const Prefill &p, mla_dtype dt, float scale, const void *q_nope,
-                         const void *w_kv_b, void *out, float *lse, const PrefillWs &w,
-                         cudaStream_t st) {
+mla_status explicit_simt(const Prefill &p, float scale, const void *q_nope, const void *w_kv_b, void *out,
+                         float *lse, const PrefillWs &w, cudaStream_t st) {
     const long Dh = p.Dn + p.Dv;
     const long kvn = p.kv_need;
+    const size_t ein = ty_size(p.tin);
     for (int s = 0; s < p.n_shards; ++s) {
         int h0 = s * p.hs;                        // local head index of the shard
         int nh = std::min(p.hs, p.head_count - h0);
@@ -199,21 +209,22 @@ mla_status explicit_simt(const Prefill &p, mla_dtype dt, float scale, const void
             g.nzb = p.B;
             g.nzh = nh;
             g.A = w.chat;
-            g.a_zb = (long)((p.kv_need + 127) / 128 * 128) * p.Dk;
-            g.a_zh = 0;
+            g.ta = p.tmid;
+            g.a_zb = p.kv_pad * p.Dk;
             g.a_m = p.Dk;
             g.a_k = 1;
-            g.B = (const char *)w_kv_b + ((hg * Dh + (part ? p.Dn : 0)) * p.Dk) * el_size(dt);
-            g.b_zb = 0;
+            g.B = (const char *)w_kv_b + ((hg * Dh + (part ? p.Dn : 0)) * p.Dk) * ein;
+            g.tb = p.tin;
             g.b_zh = Dh * p.Dk;
             g.b_n = p.Dk;
             g.b_k = 1;
             g.C = part == 0 ? w.k : w.v;
+            g.tc = p.tmid;
             g.c_zh = kvn * Dpart;
             g.c_zb = (long)p.hs * g.c_zh;
             g.c_m = Dpart;
             g.c_n = 1;
-            MLA_TRY(launch_gemm_simt(dt, g, st));
+            MLA_TRY(launch_gemm_simt(g, st));
         }
         AttnArgs a{};
         a.n_b = p.B;
@@ -222,23 +233,27 @@ mla_status explicit_simt(const Prefill &p, mla_dtype dt, float scale, const void
         a.D1 = p.Dn;
         a.D2 = p.Dr;
         a.Dv = p.Dv;
-        a.q1 = (const char *)q_nope + (size_t)h0 * p.Dn * el_size(dt);
+        a.q1 = (const char *)q_nope + (size_t)h0 * p.Dn * ein;
+        a.tq1 = p.tin;
         a.q1_b = (long)p.s_q * p.head_count * p.Dn;
         a.q1_h = p.Dn;
         a.q1_r = (long)p.head_count * p.Dn;
-        a.q2 = (const char *)w.qpe + (size_t)h0 * p.Dr * el_size(dt);
+        a.q2 = (const char *)w.qpe + (size_t)h0 * p.Dr * ty_size(p.tmid);
+        a.tq2 = p.tmid;
         a.q2_b = (long)p.s_q * p.head_count * p.Dr;
         a.q2_h = p.Dr;
         a.q2_r = (long)p.head_count * p.Dr;
         a.k1 = w.k;
+        a.tk1 = p.tmid;
         a.k1_b = (long)p.hs * kvn * p.Dn;
         a.k1_h = kvn * p.Dn;
         a.k1_r = p.Dn;
         a.k2 = w.kpe;
-        a.k2_b = (long)((p.kv_need + 127) / 128 * 128) * p.Dr;
-        a.k2_h = 0;
+        a.tk2 = p.tmid;
+        a.k2_b = p.kv_pad * p.Dr;
         a.k2_r = p.Dr;
         a.v = w.v;
+        a.tv = p.tmid;
         a.v_b = (long)p.hs * kvn * p.Dv;
         a.v_h = kvn * p.Dv;
         a.v_r = p.Dv;
@@ -248,7 +263,8 @@ mla_status explicit_simt(const Prefill &p, mla_dtype dt, float scale, const void
         a.causal = p.causal;
         a.pos0 = p.q_offset;
         a.scale = scale;
-        a.out = (char *)out + (size_t)h0 * p.Dv * el_size(dt);
+        a.out = (char *)out + (size_t)h0 * p.Dv * ein;
+        a.to = p.tin;
         a.o_b = (long)p.s_q * p.head_count * p.Dv;
         a.o_h = p.Dv;
         a.o_r = (long)p.head_count * p.Dv;
@@ -256,18 +272,16 @@ mla_status explicit_simt(const Prefill &p, mla_dtype dt, float scale, const void
         a.l_b = (long)p.head_count * p.s_q;
         a.l_h = p.s_q;
         a.l_r = 1;
-        MLA_TRY(launch_attn_simt(dt, a, st));
+        MLA_TRY(launch_attn_simt(a, st));
     }
     return MLA_OK;
 }
 
 // ------------------------------------------------------ absorbed, SIMT ----
-mla_status absorbed_simt(const Prefill &p, mla_dtype dt, float scale, const void *q_nope,
-                         const void *w_kv_b, void *out, float *lse, const PrefillWs &w,
-                         cudaStream_t st) {
+mla_status absorbed_simt(const Prefill &p, float scale, const void *q_nope, const void *w_kv_b, void *out,
+                         float *lse, const PrefillWs &w, cudaStream_t st) {
     const long Dh = p.Dn + p.Dv;
-    const long kv_pad = (p.kv_need + 127) / 128 * 128;
-    const size_t es = el_size(dt);
+    const size_t ein = ty_size(p.tin);
     for (int s = 0; s < p.n_shards; ++s) {
         int h0 = s * p.hs;
         int nh = std::min(p.hs, p.head_count - h0);
@@ -279,22 +293,24 @@ mla_status absorbed_simt(const Prefill &p, mla_dtype dt, float scale, const void
         g.K = p.Dn;
         g.nzb = p.B;
         g.nzh = nh;
-        g.A = (const char *)q_nope + (size_t)h0 * p.Dn * es;
+        g.A = (const char *)q_nope + (size_t)h0 * p.Dn * ein;
+        g.ta = p.tin;
         g.a_zb = (long)p.s_q * p.head_count * p.Dn;
         g.a_zh = p.Dn;
         g.a_m = (long)p.head_count * p.Dn;
         g.a_k = 1;
-        g.B = (const char *)w_kv_b + (size_t)(hg * Dh * p.Dk) * es;
-        g.b_zb = 0;
+        g.B = (const char *)w_kv_b + (size_t)(hg * Dh * p.Dk) * ein;
+        g.tb = p.tin;
         g.b_zh = Dh * p.Dk;
         g.b_n = 1;
         g.b_k = p.Dk;
         g.C = w.qabs;
+        g.tc = p.tmid;
         g.c_zb = (long)p.s_q * p.hs * p.Dk;
         g.c_zh = p.Dk;
         g.c_m = (long)p.hs * p.Dk;
         g.c_n = 1;
-        MLA_TRY(launch_gemm_simt(dt, g, st));
+        MLA_TRY(launch_gemm_simt(g, st));
         // latent attention: scores over [q_abs ; q_pe] . [chat ; kpe], values chat
         AttnArgs a{};
         a.n_b = p.B;
@@ -304,24 +320,26 @@ mla_status absorbed_simt(const Prefill &p, mla_dtype dt, float scale, const void
         a.D2 = p.Dr;
         a.Dv = p.Dk;
         a.q1 = w.qabs;
+        a.tq1 = p.tmid;
         a.q1_b = (long)p.s_q * p.hs * p.Dk;
         a.q1_h = p.Dk;
         a.q1_r = (long)p.hs * p.Dk;
-        a.q2 = (const char *)w.qpe + (size_t)h0 * p.Dr * es;
+        a.q2 = (const char *)w.qpe + (size_t)h0 * p.Dr * ty_size(p.tmid);
+        a.tq2 = p.tmid;
         a.q2_b = (long)p.s_q * p.head_count * p.Dr;
         a.q2_h = p.Dr;
         a.q2_r = (long)p.head_count * p.Dr;
         a.k1 = w.chat;
-        a.k1_b = kv_pad * p.Dk;
-        a.k1_h = 0;
+        a.tk1 = p.tmid;
+        a.k1_b = p.kv_pad * p.Dk;
         a.k1_r = p.Dk;
         a.k2 = w.kpe;
-        a.k2_b = kv_pad * p.Dr;
-        a.k2_h = 0;
+        a.tk2 = p.tmid;
+        a.k2_b = p.kv_pad * p.Dr;
         a.k2_r = p.Dr;
         a.v = w.chat;
-        a.v_b = kv_pad * p.Dk;
-        a.v_h = 0;
+        a.tv = p.tmid;
+        a.v_b = p.kv_pad * p.Dk;
         a.v_r = p.Dk;
         a.kv_len = p.kv_need;
         a.n_splits = 1;
@@ -330,6 +348,7 @@ mla_status absorbed_simt(const Prefill &p, mla_dtype dt, float scale, const void
         a.pos0 = p.q_offset;
         a.scale = scale;
         a.out = w.olat;
+        a.to = p.tmid;
         a.o_b = (long)p.s_q * p.hs * p.Dk;
         a.o_h = p.Dk;
         a.o_r = (long)p.hs * p.Dk;
@@ -337,7 +356,7 @@ mla_status absorbed_simt(const Prefill &p, mla_dtype dt, float scale, const void
         a.l_b = (long)p.head_count * p.s_q;
         a.l_h = p.s_q;
         a.l_r = 1;
-        MLA_TRY(launch_attn_simt(dt, a, st));
+        MLA_TRY(launch_attn_simt(a, st));
         // un-absorb: out[b][i][h0+hl][d] = sum_k o_lat[b][i][hl][k] * W_V(h)[d][k]
         GemmArgs u{};
         u.M = p.s_q;
@@ -346,21 +365,23 @@ mla_status absorbed_simt(const Prefill &p, mla_dtype dt, float scale, const void
         u.nzb = p.B;
         u.nzh = nh;
         u.A = w.olat;
+        u.ta = p.tmid;
         u.a_zb = (long)p.s_q * p.hs * p.Dk;
         u.a_zh = p.Dk;
         u.a_m = (long)p.hs * p.Dk;
         u.a_k = 1;
-        u.B = (const char *)w_kv_b + (size_t)((hg * Dh + p.Dn) * p.Dk) * es;
-        u.b_zb = 0;
+        u.B = (const char *)w_kv_b + (size_t)((hg * Dh + p.Dn) * p.Dk) * ein;
+        u.tb = p.tin;
         u.b_zh = Dh * p.Dk;
         u.b_n = p.Dk;
         u.b_k = 1;
-        u.C = (char *)out + (size_t)h0 * p.Dv * es;
+        u.C = (char *)out + (size_t)h0 * p.Dv * ein;
+        u.tc = p.tin;
         u.c_zb = (long)p.s_q * p.head_count * p.Dv;
         u.c_zh = p.Dv;
         u.c_m = (long)p.head_count * p.Dv;
         u.c_n = 1;
-        MLA_TRY(launch_gemm_simt(dt, u, st));
+        MLA_TRY(launch_gemm_simt(u, st));
     }
     return MLA_OK;
 }
@@ -370,6 +391,7 @@ struct Decode {
     int B, L, n, H, Dk, Dn, Dr, Dv;
     long chunk;
     bool tc;
+    int tin, tmid;
 };
 
 mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int n_splits, Decode *p) {
@@ -388,25 +410,27 @@ mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int 
     p->chunk = ((long)kv_len + n_splits - 1) / n_splits;
     if (p->Dk + p->Dr > 640 || p->Dk > 512) return MLA_ERR_UNSUPPORTED;
     p->tc = dt == MLA_BF16 && g_path_override != 1 && tc_decode_supported(p->Dk, p->Dn, p->Dr, p->Dv, p->H);
+    p->tin = ty_of(dt);
+    p->tmid = p->tc ? TY_F16 : TY_F32;
     return MLA_OK;
 }
 
 struct DecodeWs {
-    void *qabs, *qpe, *olat, *wukt;
+    void *qabs, *qpe, *olat, *w16;
     float *po, *pl;
     size_t bytes;
 };
 
-DecodeWs decode_ws(const Decode &p, mla_dtype dt, void *base, bool own_partials) {
+DecodeWs decode_ws(const Decode &p, void *base, bool own_partials) {
     Carve c;
     c.base = (char *)base;
     DecodeWs w{};
-    size_t es = el_size(dt);
+    const size_t es = ty_size(p.tmid);
     size_t rows = (size_t)p.B * p.H;
     w.qabs = c.take(rows * p.Dk * es);
     w.qpe = c.take(rows * p.Dr * es);
     w.olat = c.take(rows * p.Dk * es);
-    if (p.tc) w.wukt = c.take((size_t)p.H * p.Dk * p.Dn * es);
+    if (p.tc) w.w16 = c.take((size_t)p.H * (p.Dn + p.Dv) * p.Dk * 2);
     if (own_partials) {
         w.po = (float *)c.take((size_t)p.n * rows * p.Dk * 4);
         w.pl = (float *)c.take((size_t)p.n * rows * 4);
@@ -415,13 +439,13 @@ DecodeWs decode_ws(const Decode &p, mla_dtype dt, void *base, bool own_partials)
     return w;
 }
 
-mla_status decode_simt(const Decode &p, mla_dtype dt, float scale, const mla_dims *d, const void *q_nope,
-                       const void *q_pe, const void *c_cache, const void *kpe_cache, const void *w_kv_b,
-                       void *out, float *lse, float *po, float *pl, const DecodeWs &w, cudaStream_t st) {
-    const size_t es = el_size(dt);
+mla_status decode_simt(const Decode &p, float scale, const mla_dims *d, const void *q_nope, const void *q_pe,
+                       const void *c_cache, const void *kpe_cache, const void *w_kv_b, void *out, float *lse,
+                       float *po, float *pl, const DecodeWs &w, cudaStream_t st) {
+    const size_t ein = ty_size(p.tin);
     const long Dh = p.Dn + p.Dv;
     long rows = (long)p.B * p.H;
-    MLA_TRY(launch_rope_rows(dt, rows, p.Dr, q_pe, p.L - 1, 1, 1, d->rope_base, w.qpe, st));
+    MLA_TRY(launch_rope_rows(p.tin, p.tmid, rows, p.Dr, q_pe, p.L - 1, 1, 1, d->rope_base, w.qpe, st));
     GemmArgs g{};
     g.M = p.B;
     g.N = p.Dk;
@@ -429,18 +453,21 @@ mla_status decode_simt(const Decode &p, mla_dtype dt, float scale, const mla_dim
     g.nzb = 1;
     g.nzh = p.H;
     g.A = q_nope;
+    g.ta = p.tin;
     g.a_zh = p.Dn;
     g.a_m = (long)p.H * p.Dn;
     g.a_k = 1;
     g.B = w_kv_b;
+    g.tb = p.tin;
     g.b_zh = Dh * p.Dk;
     g.b_n = 1;
     g.b_k = p.Dk;
     g.C = w.qabs;
+    g.tc = p.tmid;
     g.c_zh = p.Dk;
     g.c_m = (long)p.H * p.Dk;
     g.c_n = 1;
-    MLA_TRY(launch_gemm_simt(dt, g, st));
+    MLA_TRY(launch_gemm_simt(g, st));
     AttnArgs a{};
     a.n_b = p.B;
     a.n_h = 1;
@@ -449,18 +476,23 @@ mla_status decode_simt(const Decode &p, mla_dtype dt, float scale, const mla_dim
     a.D2 = p.Dr;
     a.Dv = p.Dk;
     a.q1 = w.qabs;
+    a.tq1 = p.tmid;
     a.q1_b = (long)p.H * p.Dk;
     a.q1_r = p.Dk;
     a.q2 = w.qpe;
+    a.tq2 = p.tmid;
     a.q2_b = (long)p.H * p.Dr;
     a.q2_r = p.Dr;
     a.k1 = c_cache;
+    a.tk1 = p.tin;
     a.k1_b = (long)p.L * p.Dk;
     a.k1_r = p.Dk;
     a.k2 = kpe_cache;
+    a.tk2 = p.tin;
     a.k2_b = (long)p.L * p.Dr;
     a.k2_r = p.Dr;
     a.v = c_cache;
+    a.tv = p.tin;
     a.v_b = (long)p.L * p.Dk;
     a.v_r = p.Dk;
     a.kv_len = p.L;
@@ -477,8 +509,8 @@ mla_status decode_simt(const Decode &p, mla_dtype dt, float scale, const mla_dim
     a.pl_s = rows;
     a.pl_b = p.H;
     a.pl_r = 1;
-    MLA_TRY(launch_attn_simt(dt, a, st));
-    MLA_TRY(launch_lse_combine(dt, p.n, rows, p.Dk, po, pl, w.olat, lse, st));
+    MLA_TRY(launch_attn_simt(a, st));
+    MLA_TRY(launch_lse_combine(p.tmid, p.n, rows, p.Dk, po, pl, w.olat, lse, st));
     GemmArgs u{};
     u.M = p.B;
     u.N = p.Dv;
@@ -486,102 +518,100 @@ mla_status decode_simt(const Decode &p, mla_dtype dt, float scale, const mla_dim
     u.nzb = 1;
     u.nzh = p.H;
     u.A = w.olat;
+    u.ta = p.tmid;
     u.a_zh = p.Dk;
     u.a_m = (long)p.H * p.Dk;
     u.a_k = 1;
-    u.B = (const char *)w_kv_b + (size_t)p.Dn * p.Dk * es;
+    u.B = (const char *)w_kv_b + (size_t)p.Dn * p.Dk * ein;
+    u.tb = p.tin;
     u.b_zh = Dh * p.Dk;
     u.b_n = p.Dk;
     u.b_k = 1;
     u.C = out;
+    u.tc = p.tin;
     u.c_zh = p.Dv;
     u.c_m = (long)p.H * p.Dv;
     u.c_n = 1;
-    MLA_TRY(launch_gemm_simt(dt, u, st));
+    MLA_TRY(launch_gemm_simt(u, st));
     return MLA_OK;
 }
 
 mla_status prefill_entry(bool absorbed, const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
-                         int q_offset, int causal, int head_begin, int head_count, int head_shard,
-                         const void *q_nope, const void *q_pe, const void *c_kv, const void *k_pe,
-                         const void *w_kv_b, const void *rms_w, void *out, float *lse, void *workspace,
-                         size_t workspace_bytes, void *cuda_stream) {
+                         int q_offset, int causal, int head_begin, int head_count, int head_shard, const void *q_nope,
+                         const void *q_pe, const void *c_kv, const void *k_pe, const void *w_kv_b, const void *rms_w,
+                         void *out, float *lse, void *workspace, size_t workspace_bytes, void *cuda_stream) {
     Prefill p;
-    mla_status st = prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count,
-                                  head_shard, absorbed, &p);
+    mla_status st = prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count, head_shard,
+                                  absorbed, &p);
     if (st != MLA_OK) return st;
     if (B == 0 || s_q == 0 || head_count == 0) return MLA_OK;
-    st = prefill_common_checks(p, dtype, absorbed, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse,
-                               workspace, workspace_bytes);
+    st = prefill_common_checks(p, absorbed, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, workspace,
+                               workspace_bytes);
     if (st != MLA_OK) return st;
     cudaStream_t cs = (cudaStream_t)cuda_stream;
-    PrefillWs w = prefill_ws(p, dtype, absorbed, workspace);
+    PrefillWs w = prefill_ws(p, absorbed, workspace);
     float scale = scale_of(dims);
-    st = prefill_prep(p, dtype, dims, q_pe, c_kv, k_pe, rms_w, w, cs);
+    st = prefill_prep(p, dims, q_pe, c_kv, k_pe, rms_w, w, cs);
     if (st != MLA_OK) return st;
     g_last_path = p.tc ? 2 : 1;
     if (p.tc) {
         TcPrefill t{p.B, p.s_q, p.s_kv, p.q_offset, p.causal, p.head_begin, p.head_count, p.hs, p.n_shards,
                     p.Dk, p.Dn, p.Dr, p.Dv, p.H, p.kv_need, scale};
-        cudaError_t e = absorbed ? tc_absorbed_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe,
-                                                       w.qabs, w.olat, w.wukt, cs)
-                                 : tc_explicit_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe,
-                                                       w.k, w.v, cs);
+        cudaError_t e = absorbed ? tc_absorbed_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.qabs,
+                                                       w.olat, w.w16, cs)
+                                 : tc_explicit_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.k, w.v,
+                                                       w.w16, cs);
         return cuda_status(e);
     }
-    return absorbed ? absorbed_simt(p, dtype, scale, q_nope, w_kv_b, out, lse, w, cs)
-                    : explicit_simt(p, dtype, scale, q_nope, w_kv_b, out, lse, w, cs);
+    return absorbed ? absorbed_simt(p, scale, q_nope, w_kv_b, out, lse, w, cs)
+                    : explicit_simt(p, scale, q_nope, w_kv_b, out, lse, w, cs);
 }
 
 }  // namespace
 
 extern "C" {
 
-mla_status mla_latent_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
-                               int q_offset, int causal, int head_begin, int head_count, int head_shard,
-                               const void *q_nope, const void *q_pe, const void *c_kv, const void *k_pe,
-                               const void *w_kv_b, const void *rms_w, void *out, float *lse,
-                               void *workspace, size_t workspace_bytes, void *cuda_stream) {
-    return prefill_entry(false, dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count,
-                         head_shard, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, workspace,
-                         workspace_bytes, cuda_stream);
+mla_status mla_latent_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                               int causal, int head_begin, int head_count, int head_shard, const void *q_nope,
+                               const void *q_pe, const void *c_kv, const void *k_pe, const void *w_kv_b,
+                               const void *rms_w, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                               void *cuda_stream) {
+    return prefill_entry(false, dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count, head_shard,
+                         q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, workspace, workspace_bytes, cuda_stream);
 }
 
-mla_status mla_absorbed_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
-                                 int q_offset, int causal, int head_begin, int head_count, int head_shard,
-                                 const void *q_nope, const void *q_pe, const void *c_kv, const void *k_pe,
-                                 const void *w_kv_b, const void *rms_w, void *out, float *lse,
-                                 void *workspace, size_t workspace_bytes, void *cuda_stream) {
-    return prefill_entry(true, dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count,
-                         head_shard, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, workspace,
-                         workspace_bytes, cuda_stream);
+mla_status mla_absorbed_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                                 int causal, int head_begin, int head_count, int head_shard, const void *q_nope,
+                                 const void *q_pe, const void *c_kv, const void *k_pe, const void *w_kv_b,
+                                 const void *rms_w, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                 void *cuda_stream) {
+    return prefill_entry(true, dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count, head_shard,
+                         q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, workspace, workspace_bytes, cuda_stream);
 }
 
-size_t mla_latent_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
-                                 int q_offset, int causal, int head_count, int head_shard) {
+size_t mla_latent_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                                 int causal, int head_count, int head_shard) {
     Prefill p;
-    if (prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, 0, head_count, head_shard, false, &p) !=
-        MLA_OK)
+    if (prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, 0, head_count, head_shard, false, &p) != MLA_OK)
         return 0;
     if (B == 0 || s_q == 0 || head_count == 0) return 0;
-    return prefill_ws(p, dtype, false, nullptr).bytes;
+    return prefill_ws(p, false, nullptr).bytes;
 }
 
-size_t mla_absorbed_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
-                                   int q_offset, int causal, int head_count, int head_shard) {
+size_t mla_absorbed_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                                   int causal, int head_count, int head_shard) {
     Prefill p;
-    if (prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, 0, head_count, head_shard, true, &p) !=
-        MLA_OK)
+    if (prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, 0, head_count, head_shard, true, &p) != MLA_OK)
         return 0;
     if (B == 0 || s_q == 0 || head_count == 0) return 0;
-    return prefill_ws(p, dtype, true, nullptr).bytes;
+    return prefill_ws(p, true, nullptr).bytes;
 }
 
 size_t mla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits) {
     Decode p;
     if (decode_shape(dims, dtype, B, kv_len, n_splits, &p) != MLA_OK) return 0;
     if (B == 0) return 0;
-    return decode_ws(p, dtype, nullptr, true).bytes;
+    return decode_ws(p, nullptr, true).bytes;
 }
 
 mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits,
@@ -600,11 +630,11 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
         if (!aligned16(q)) return MLA_ERR_ALIGN;
     if ((part_out && !aligned16(part_out)) || (part_lse && !aligned16(part_lse))) return MLA_ERR_ALIGN;
     bool own = part_out == nullptr;
-    DecodeWs wsz = decode_ws(p, dtype, nullptr, true);   // the query always covers the own-partials case
+    DecodeWs wsz = decode_ws(p, nullptr, true);   // the query always covers the own-partials case
     if (workspace_bytes < wsz.bytes) return MLA_ERR_WORKSPACE;
     if (wsz.bytes && !workspace) return MLA_ERR_NULL;
     if (workspace && !aligned16(workspace)) return MLA_ERR_ALIGN;
-    size_t es = el_size(dtype);
+    const size_t es = ty_size(p.tin);
     size_t rows = (size_t)p.B * p.H;
     Range in[] = {rng(q_nope, rows * p.Dn * es), rng(q_pe, rows * p.Dr * es),
                   rng(c_cache, (size_t)p.B * p.L * p.Dk * es), rng(kpe_cache, (size_t)p.B * p.L * p.Dr * es),
@@ -613,7 +643,7 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
                     rng(part_out, (size_t)p.n * rows * p.Dk * 4), rng(part_lse, (size_t)p.n * rows * 4)};
     st = check_alias(in, 5, outs, 5);
     if (st != MLA_OK) return st;
-    DecodeWs w = decode_ws(p, dtype, workspace, own);
+    DecodeWs w = decode_ws(p, workspace, own);
     float *po = own ? w.po : part_out;
     float *pl = own ? w.pl : part_lse;
     cudaStream_t cs = (cudaStream_t)cuda_stream;
@@ -621,10 +651,10 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
     g_last_path = p.tc ? 2 : 1;
     if (p.tc) {
         TcDecode t{p.B, p.L, p.n, p.H, p.Dk, p.Dn, p.Dr, p.Dv, p.chunk, scale, dims->rope_base};
-        return cuda_status(tc_decode(t, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w.qabs,
-                                     w.qpe, w.olat, w.wukt, cs));
+        return cuda_status(tc_decode(t, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w.qabs, w.qpe,
+                                     w.olat, w.w16, cs));
     }
-    return decode_simt(p, dtype, scale, dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w, cs);
+    return decode_simt(p, scale, dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w, cs);
 }
 
 mla_status mla_lse_combine(mla_dtype out_dtype, int n_splits, int rows, int D, const float *part_out,
@@ -634,13 +664,13 @@ mla_status mla_lse_combine(mla_dtype out_dtype, int n_splits, int rows, int D, c
     if (rows == 0) return MLA_OK;
     if (!part_out || !part_lse || !out || !lse) return MLA_ERR_NULL;
     if (!aligned16(part_out) || !aligned16(part_lse) || !aligned16(out) || !aligned16(lse)) return MLA_ERR_ALIGN;
-    size_t es = el_size(out_dtype);
+    const size_t es = ty_size(ty_of(out_dtype));
     Range in[] = {rng(part_out, (size_t)n_splits * rows * D * 4), rng(part_lse, (size_t)n_splits * rows * 4)};
     Range outs[] = {rng(out, (size_t)rows * D * es), rng(lse, (size_t)rows * 4)};
     mla_status st = check_alias(in, 2, outs, 2);
     if (st != MLA_OK) return st;
     g_last_path = 1;
-    return cuda_status(launch_lse_combine(out_dtype, n_splits, rows, D, part_out, part_lse, out, lse,
+    return cuda_status(launch_lse_combine(ty_of(out_dtype), n_splits, rows, D, part_out, part_lse, out, lse,
                                           (cudaStream_t)cuda_stream));
 }
 

@@ -8,6 +8,11 @@
 
 namespace mla {
 
+// Storage codes of a tensor (element type in memory; arithmetic is always fp32).
+enum { TY_F16 = 0, TY_BF16 = 1, TY_F32 = 2 };
+inline int ty_of(mla_dtype dt) { return dt == MLA_F32 ? TY_F32 : TY_BF16; }
+inline size_t ty_size(int ty) { return ty == TY_F32 ? 4 : 2; }
+
 // Launch accounting / optional event timing around every kernel launch (profile.cu).
 void prof_begin(const char *name, cudaStream_t st);
 void prof_end(const char *name, cudaStream_t st);
@@ -18,58 +23,60 @@ struct ProfScope {
     ~ProfScope() { prof_end(n, s); }
 };
 
-// ----------------------------------------------------------------- SIMT path ----
+// ------------------------------------------------------------------ shared prep ----
 
-// One warp per latent row: chat = RMSNorm(c_kv) and kpe = RoPE(k_pe, j) for keys
-// j < n_rows of every batch.  c_kv [B, s_kv, Dk], k_pe [B, s_kv, Dr] -> chat
-// [B, pad_rows, Dk], kpe [B, pad_rows, Dr] (dtype of the call); rows n_rows..pad_rows-1
-// are zero-filled.
-cudaError_t launch_latent_prep(mla_dtype dt, int B, int s_kv, int n_rows, int pad_rows, int Dk,
-                               int Dr, const void *c_kv, const void *k_pe, const void *rms_w,
-                               float eps, float base, void *chat, void *kpe, cudaStream_t st);
+// One warp per latent row: chat = RMSNorm(c_kv) * rms_w and kpe = RoPE(k_pe, j) for
+// keys j < n_rows of every batch.  c_kv [B, s_kv, Dk], k_pe [B, s_kv, Dr] (storage
+// tin) -> chat [B, pad_rows, Dk], kpe [B, pad_rows, Dr] (storage tout); rows
+// n_rows..pad_rows-1 are zero-filled.
+cudaError_t launch_latent_prep(int tin, int tout, int B, int s_kv, int n_rows, int pad_rows, int Dk, int Dr,
+                               const void *c_kv, const void *k_pe, const void *rms_w, float eps, float base,
+                               void *chat, void *kpe, cudaStream_t st);
 
 // RoPE on `rows` rows of width Dr; row r sits at position pos0 + (r / pos_div) % pos_mod.
-cudaError_t launch_rope_rows(mla_dtype dt, long rows, int Dr, const void *x, long pos0,
-                             long pos_div, long pos_mod, float base, void *y, cudaStream_t st);
+cudaError_t launch_rope_rows(int tin, int tout, long rows, int Dr, const void *x, long pos0, long pos_div,
+                             long pos_mod, float base, void *y, cudaStream_t st);
+
+// y[i] = x[i] for i < n, converting storage type.
+cudaError_t launch_convert(int tin, const void *x, int tout, void *y, long n, cudaStream_t st);
+
+// ------------------------------------------------------------------- SIMT path ----
 
 // C(m,n) = sum_k A(m,k) B(n,k) for every (zb, zh), arbitrary element strides.
 struct GemmArgs {
     int M, N, K, nzb, nzh;
-    const void *A; long a_zb, a_zh, a_m, a_k;
-    const void *B; long b_zb, b_zh, b_n, b_k;
-    void *C; long c_zb, c_zh, c_m, c_n;
+    const void *A; int ta; long a_zb, a_zh, a_m, a_k;
+    const void *B; int tb; long b_zb, b_zh, b_n, b_k;
+    void *C; int tc; long c_zb, c_zh, c_m, c_n;
 };
-cudaError_t launch_gemm_simt(mla_dtype dt, const GemmArgs &g, cudaStream_t st);
+cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t st);
 
 // Softmax attention over rows x keys with the scores split in two bands
 // (q1.k1 over D1 dims + q2.k2 over D2 dims), values of width Dv.
 // Grid: z = (b, h) pairs, rows per pair, keys split into n_splits chunks.
 struct AttnArgs {
     int n_b, n_h, n_rows, D1, D2, Dv;
-    const void *q1; long q1_b, q1_h, q1_r;
-    const void *q2; long q2_b, q2_h, q2_r;
-    const void *k1; long k1_b, k1_h, k1_r;
-    const void *k2; long k2_b, k2_h, k2_r;
-    const void *v;  long v_b, v_h, v_r;
+    const void *q1; int tq1; long q1_b, q1_h, q1_r;
+    const void *q2; int tq2; long q2_b, q2_h, q2_r;
+    const void *k1; int tk1; long k1_b, k1_h, k1_r;
+    const void *k2; int tk2; long k2_b, k2_h, k2_r;
+    const void *v;  int tv;  long v_b, v_h, v_r;
     long kv_len;
     int n_splits; long chunk;
     int causal; long pos0;          // row r sits at absolute position pos0 + r
     float scale;
-    // normalised output (dtype of the call) and lse, used when part_out == nullptr
-    void *out; long o_b, o_h, o_r;
+    // normalised output and lse, used when part_out == nullptr
+    void *out; int to; long o_b, o_h, o_r;
     float *lse; long l_b, l_h, l_r;
     // split partials (fp32), output normalised within the split
     float *part_out; long po_s, po_b, po_h, po_r;
     float *part_lse; long pl_s, pl_b, pl_h, pl_r;
 };
-cudaError_t launch_attn_simt(mla_dtype dt, const AttnArgs &a, cudaStream_t st);
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
 
-// lse-combine: part_out [n][rows][D], part_lse [n][rows] -> out [rows][D] (dtype), lse [rows]
-cudaError_t launch_lse_combine(mla_dtype dt, int n, long rows, int D, const float *po,
-                               const float *pl, void *out, float *lse, cudaStream_t st);
-
-// ------------------------------------------------------------ tensor-core path ----
-// (declared in the tcgen05 translation units; see tc_*.cu)
+// lse-combine: part_out [n][rows][D], part_lse [n][rows] -> out [rows][D] (storage tout), lse [rows]
+cudaError_t launch_lse_combine(int tout, int n, long rows, int D, const float *po, const float *pl, void *out,
+                               float *lse, cudaStream_t st);
 
 // Reads and clears the bounded-wait error words of the tensor-core kernels.
 cudaError_t tc_read_and_clear_error(unsigned int *flags, cudaStream_t st);

@@ -22,16 +22,17 @@ bool tc_explicit_supported(int Dk, int Dn, int Dr, int Dv);
 bool tc_absorbed_supported(int Dk, int Dn, int Dr, int Dv);
 bool tc_decode_supported(int Dk, int Dn, int Dr, int Dv, int H);
 
-// Explicit prefill after the shared prep (chat, kpe, qpe already in the workspace):
-// per head shard, the K_nope / V^T reconstruction GEMMs and the attention kernel.
+// Explicit prefill after the shared prep (fp16 chat, kpe, qpe already in the
+// workspace): per head shard, an fp16 copy of the shard's W_kv_b rows, the K_nope /
+// V^T reconstruction GEMMs and the attention kernel.
 cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
-                                float *lse, const void *chat, const void *kpe, const void *qpe,
-                                void *kws, void *vws, cudaStream_t st);
+                                float *lse, const void *chat, const void *kpe, const void *qpe, void *kws,
+                                void *vws, void *w16, cudaStream_t st);
 cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
-                                float *lse, const void *chat, const void *kpe, const void *qpe,
-                                void *qabs, void *olat, void *wukt, cudaStream_t st);
+                                float *lse, const void *chat, const void *kpe, const void *qpe, void *qabs,
+                                void *olat, void *w16, cudaStream_t st);
 cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, const void *c_cache,
-                      const void *kpe_cache, const void *w_kv_b, void *out, float *lse, float *po,
-                      float *pl, void *qabs, void *qpe, void *olat, void *wukt, cudaStream_t st);
+                      const void *kpe_cache, const void *w_kv_b, void *out, float *lse, float *po, float *pl,
+                      void *qabs, void *qpe, void *olat, void *w16, cudaStream_t st);
 
 }  // namespace mla

@@ -1,0 +1,437 @@
+// tc_attn.cu -- explicit-form (LAGA per-rank) MLA prefill on the sm_103a tensor
+// cores, and the host sequence that drives it.
+//
+// Method ("A Training-Memory Regression in MLA Sequence Parallelism ... LAGA",
+// arXiv 2607.17644, "What carries the argument", Fig. 2 and the paper's section
+// 3.3): rebuild per-head K_nope / V from the normalised latent through W_kv_b one
+// head shard at a time, then head-dim causal attention with
+//   s_ij = scale * (q_nope_i . K_nope_j + RoPE(q_pe_i) . RoPE(k_pe_j)),
+// softmax over visible keys (j <= q_offset + i), output plus log-sum-exp.
+//
+// Kernel: one CTA per (128-query tile, head, batch), 192 threads.
+//   warp 0    TMA producer: Q tile once; K tiles (K_nope 128 + RoPE band 64 dims)
+//             and V^T tiles through two 2-deep rings.
+//   warp 1    tcgen05 issuer: S_j = Q K_j^T (M=128, N=128, K=192) into one of two
+//             TMEM S buffers; O += P_{j-1} V_{j-1} (M=128, N=128, K=128) with P read
+//             from TMEM where the softmax wrote it over S_{j-1}.
+//   warps 2-5 softmax, one query row per thread (TMEM lane = row): online softmax
+//             in the log2 domain; O in TMEM is rescaled only when a row maximum
+//             grows by more than 2^8 (the stale maximum keeps every p <= 256, exact
+//             after the final division); epilogue O / l and lse.
+// Operands are fp16 (11-bit significand): q_nope arrives as bf16 and is widened in
+// shared memory; K_nope, V^T and the rotated RoPE bands are produced in fp16.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "mla_internal.h"
+#include "tc.h"
+#include "tc_common.cuh"
+#include "tc_internal.h"
+
+namespace mla {
+
+__device__ unsigned g_tc_attn_err = 0;
+
+namespace {
+
+using namespace tc;
+
+constexpr int BQ = 128, BKV = 128;
+constexpr uint32_t BOX = 128 * 128;            // one 128-row x 64-element fp16 box
+constexpr uint32_t Q_BYTES = 3 * BOX;          // nope lo, nope hi, rope
+constexpr uint32_t K_BYTES = 3 * BOX;
+constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halves
+constexpr int KST = 2, VST = 2;
+constexpr uint32_t SMEM_BYTES = Q_BYTES + KST * K_BYTES + VST * V_BYTES + 1024 + 256;
+constexpr float RESCALE_LOG2 = 8.0f;
+
+struct AttnK {
+    int s_q, kv_need, q_offset, causal;
+    int head_off;       // first query/output head of this shard
+    float scale_log2;   // softmax scale * log2(e)
+    __nv_bfloat16 *out;
+    long out_b, out_i, out_h;
+    float *lse;
+    long lse_b, lse_h;
+    uint32_t idesc_s, idesc_pv;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(192, 1)
+    tc_attn_kernel(const __grid_constant__ CUtensorMap mQn, const __grid_constant__ CUtensorMap mQr,
+                   const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
+                   const __grid_constant__ CUtensorMap mV, AttnK p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sQ = smem;
+    uint8_t *sK = sQ + Q_BYTES;
+    uint8_t *sV = sK + KST * K_BYTES;
+    uint64_t *bars = (uint64_t *)(sV + VST * V_BYTES);
+    uint64_t *q_full = bars + 0, *q_ready = bars + 1;
+    uint64_t *k_full = bars + 2, *k_empty = bars + 4;
+    uint64_t *v_full = bars + 6, *v_empty = bars + 8;
+    uint64_t *s_full = bars + 10, *p_full = bars + 12;
+    uint64_t *o_done = bars + 14, *o_final = bars + 15;
+    uint32_t *tslot = (uint32_t *)(bars + 16);
+    volatile int *abort = (volatile int *)(tslot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qt = gridDim.x - 1 - blockIdx.x;   // heaviest (latest) query tiles first
+    const int q0 = qt * BQ, hl = blockIdx.y, b = blockIdx.z;
+    const int hq = p.head_off + hl;
+    const int kv_end = p.causal ? min(p.kv_need, p.q_offset + q0 + BQ) : p.kv_need;
+    const int nt = (kv_end + BKV - 1) / BKV;
+
+    if (tid == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_ready, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(o_final, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;   // S0: cols 0-127, S1: 128-255, O: 256-383
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&mQn);
+            tma_prefetch_desc(&mK);
+            tma_prefetch_desc(&mV);
+            mbar_arrive_expect_tx(q_full, Q_BYTES);
+            tma_load_4d(sQ, &mQn, q_full, 0, hq, q0, b);
+            tma_load_4d(sQ + BOX, &mQn, q_full, 64, hq, q0, b);
+            tma_load_4d(sQ + 2 * BOX, &mQr, q_full, 0, hq, q0, b);
+            for (int j = 0; j < nt; ++j) {
+                const int ks = j % KST, vs = j % VST;
+                if (j >= KST && !mbar_wait(&k_empty[ks], ((j / KST) - 1) & 1, abort, &g_tc_attn_err)) break;
+                uint8_t *kd = sK + ks * K_BYTES;
+                mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
+                tma_load_3d(kd, &mK, &k_full[ks], hl * 128, j * BKV, b);
+                tma_load_3d(kd + BOX, &mK, &k_full[ks], hl * 128 + 64, j * BKV, b);
+                tma_load_3d(kd + 2 * BOX, &mKr, &k_full[ks], 0, j * BKV, b);
+                if (j >= VST && !mbar_wait(&v_empty[vs], ((j / VST) - 1) & 1, abort, &g_tc_attn_err)) break;
+                uint8_t *vd = sV + vs * V_BYTES;
+                mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
+                tma_load_3d(vd, &mV, &v_full[vs], j * BKV, hl * 128, b);
+                tma_load_3d(vd + BOX, &mV, &v_full[vs], j * BKV + 64, hl * 128, b);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait(q_ready, 0, abort, &g_tc_attn_err);
+            const uint32_t o_tm = tmem + 256;
+            auto issue_pv = [&](int t) -> bool {
+                const int sb = t & 1, vs = t % VST;
+                if (!mbar_wait(&p_full[sb], (t >> 1) & 1, abort, &g_tc_attn_err)) return false;
+                if (!mbar_wait(&v_full[vs], (t / VST) & 1, abort, &g_tc_attn_err)) return false;
+                tc_fence_after();
+                const uint32_t p_tm = tmem + sb * 128;
+                const uint8_t *vd = sV + vs * V_BYTES;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    const uint64_t db = sdesc_kmajor(vd + kb * BOX);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ts(o_tm, p_tm + kb * 32 + k * 8, db + 2 * k, p.idesc_pv, (t | kb | k) != 0);
+                }
+                mma_commit(&v_empty[vs]);
+                mma_commit(o_done);
+                return true;
+            };
+            for (int j = 0; j < nt && ok; ++j) {
+                const int ks = j % KST, sb = j & 1;
+                if (!mbar_wait(&k_full[ks], (j / KST) & 1, abort, &g_tc_attn_err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t s_tm = tmem + sb * 128;
+                const uint8_t *kd = sK + ks * K_BYTES;
+#pragma unroll
+                for (int kb = 0; kb < 3; ++kb) {
+                    const uint64_t da = sdesc_kmajor(sQ + kb * BOX), db = sdesc_kmajor(kd + kb * BOX);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mma_ss(s_tm, da + 2 * k, db + 2 * k, p.idesc_s, (kb | k) != 0);
+                }
+                mma_commit(&s_full[sb]);
+                mma_commit(&k_empty[ks]);
+                if (j >= 1 && !issue_pv(j - 1)) ok = false;
+            }
+            if (ok && nt >= 1) issue_pv(nt - 1);
+            mma_commit(o_final);
+        }
+    } else {
+        // ---------------------------------------------------------- softmax warps
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int pos = p.q_offset + q0 + row;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        // widen this row of the bf16 q_nope boxes to fp16 in place
+        bool ok = mbar_wait(q_full, 0, abort, &g_tc_attn_err);
+        if (ok) {
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx) {
+                uint4 *rp = (uint4 *)(sQ + bx * BOX + row * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 v = rp[c];
+                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+                    rp[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
+
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < nt && ok; ++j) {
+            const int sb = j & 1;
+            if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort, &g_tc_attn_err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + sb * 128 + c * 32, s[c]);
+            tmem_ld_wait();
+            const int j0 = j * BKV;
+            const bool masked = (j0 + BKV > p.kv_need) || (p.causal && j0 + BKV - 1 > p.q_offset + q0);
+            float x[4][32];
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float v = __uint_as_float(s[c][i]) * p.scale_log2;
+                    if (masked) {
+                        const int key = j0 + c * 32 + i;
+                        if (key >= p.kv_need || (p.causal && key > pos)) v = -INFINITY;
+                    }
+                    x[c][i] = v;
+                    mt = fmaxf(mt, v);
+                }
+            const float m_new = fmaxf(m, mt);
+            const bool need = m_new > m + RESCALE_LOG2;   // also true on the first finite maximum
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_use = need ? m_new : m;
+                const float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_use);
+                if (j > 0) {
+                    if (!mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_attn_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + 256 + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(lane_base + 256 + c * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                l *= alpha;
+                m = m_use;
+            }
+            const float m_eff = (m == -INFINITY) ? 0.f : m;
+            float rs = 0.f;
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(x[c][2 * i] - m_eff), p1 = ex2(x[c][2 * i + 1] - m_eff);
+                    rs += p0 + p1;
+                    pk[c >> 1][(c & 1) * 16 + i] = pack_f16(p0, p1);
+                }
+            tmem_st32(lane_base + sb * 128, pk[0]);
+            tmem_st32(lane_base + sb * 128 + 32, pk[1]);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+            l += rs;
+        }
+        // ---- epilogue
+        if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, &g_tc_attn_err);
+        tc_fence_after();
+        const int qi = q0 + row;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint32_t o[4][32];
+        if (nt > 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + 256 + c * 32, o[c]);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c][i] = 0u;
+        }
+        if (ok && qi < p.s_q) {
+            uint4 *dst = (uint4 *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = pack_bf16(__uint_as_float(o[c][8 * v + 2 * i]) * inv,
+                                         __uint_as_float(o[c][8 * v + 2 * i + 1]) * inv);
+                    dst[c * 4 + v] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] =
+                l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool tc_explicit_supported(int Dk, int Dn, int Dr, int Dv) {
+    return Dk % 64 == 0 && Dk <= 4096 && Dn == 128 && Dr == 64 && Dv == 128;
+}
+
+cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out, float *lse,
+                                const void *chat, const void *kpe, const void *qpe, void *kws, void *vws,
+                                void *w16, cudaStream_t st) {
+    const long kv_pad = (p.kv_need + 127) / 128 * 128;
+    const long Dh = p.Dn + p.Dv;
+    cudaError_t e;
+    // maps that do not change across shards
+    CUtensorMap mQn, mQr, mKr;
+    {
+        unsigned long long d[4] = {(unsigned long long)p.Dn, (unsigned long long)p.head_count,
+                                   (unsigned long long)p.s_q, (unsigned long long)p.B};
+        unsigned long long s[3] = {(unsigned long long)p.Dn * 2, (unsigned long long)p.head_count * p.Dn * 2,
+                                   (unsigned long long)p.s_q * p.head_count * p.Dn * 2};
+        unsigned box[4] = {64, 1, 128, 1};
+        if ((e = make_tma_map(&mQn, q_nope, 4, d, s, box)) != cudaSuccess) return e;
+    }
+    {
+        unsigned long long d[4] = {(unsigned long long)p.Dr, (unsigned long long)p.head_count,
+                                   (unsigned long long)p.s_q, (unsigned long long)p.B};
+        unsigned long long s[3] = {(unsigned long long)p.Dr * 2, (unsigned long long)p.head_count * p.Dr * 2,
+                                   (unsigned long long)p.s_q * p.head_count * p.Dr * 2};
+        unsigned box[4] = {64, 1, 128, 1};
+        if ((e = make_tma_map(&mQr, qpe, 4, d, s, box)) != cudaSuccess) return e;
+    }
+    {
+        unsigned long long d[3] = {(unsigned long long)p.Dr, (unsigned long long)kv_pad, (unsigned long long)p.B};
+        unsigned long long s[2] = {(unsigned long long)p.Dr * 2, (unsigned long long)kv_pad * p.Dr * 2};
+        unsigned box[3] = {64, 128, 1};
+        if ((e = make_tma_map(&mKr, kpe, 3, d, s, box)) != cudaSuccess) return e;
+    }
+    CUtensorMap mK, mV;
+    {
+        unsigned long long d[3] = {(unsigned long long)p.hs * p.Dn, (unsigned long long)kv_pad,
+                                   (unsigned long long)p.B};
+        unsigned long long s[2] = {(unsigned long long)p.hs * p.Dn * 2, (unsigned long long)kv_pad * p.hs * p.Dn * 2};
+        unsigned box[3] = {64, 128, 1};
+        if ((e = make_tma_map(&mK, kws, 3, d, s, box)) != cudaSuccess) return e;
+    }
+    {
+        unsigned long long d[3] = {(unsigned long long)kv_pad, (unsigned long long)p.hs * p.Dv,
+                                   (unsigned long long)p.B};
+        unsigned long long s[2] = {(unsigned long long)kv_pad * 2, (unsigned long long)p.hs * p.Dv * kv_pad * 2};
+        unsigned box[3] = {64, 128, 1};
+        if ((e = make_tma_map(&mV, vws, 3, d, s, box)) != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(tc_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+
+    AttnK a;
+    a.s_q = p.s_q;
+    a.kv_need = (int)p.kv_need;
+    a.q_offset = p.q_offset;
+    a.causal = p.causal;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.out = (__nv_bfloat16 *)out;
+    a.out_b = (long)p.s_q * p.head_count * p.Dv;
+    a.out_i = (long)p.head_count * p.Dv;
+    a.out_h = p.Dv;
+    a.lse = lse;
+    a.lse_b = (long)p.head_count * p.s_q;
+    a.lse_h = p.s_q;
+    a.idesc_s = idesc_f16(128, 128, true);
+    a.idesc_pv = idesc_f16(128, 128, true);
+
+    TmaOperand latent{chat, p.Dk, kv_pad, p.B, (long)p.Dk * 2, kv_pad * p.Dk * 2, (int)kv_pad, 0, 1};
+    for (int s = 0; s < p.n_shards; ++s) {
+        const int h0 = s * p.hs;
+        const int nh = std::min(p.hs, p.head_count - h0);
+        const long hg = p.head_begin + h0;
+        // fp16 copy of this shard's W_kv_b rows: [nh][Dn+Dv][Dk]
+        e = launch_convert(1, (const char *)w_kv_b + hg * Dh * p.Dk * 2, 0, w16, (long)nh * Dh * p.Dk, st);
+        if (e != cudaSuccess) return e;
+        // K_nope[b][j][hl*Dn + d] = chat[b][j] . W_K(hg+hl)[d]
+        TmaOperand wk{w16, p.Dk, p.Dn, nh, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dn, 0, 0};
+        e = tc_gemm(latent, wk, (int)kv_pad, nh * p.Dn, p.Dk, p.B, true, kws, (long)p.hs * p.Dn, 1,
+                    kv_pad * p.hs * p.Dn, 0, st);
+        if (e != cudaSuccess) return e;
+        // V^T[b][hl*Dv + d][j] = W_V(hg+hl)[d] . chat[b][j]
+        TmaOperand wv{(const char *)w16 + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, nh, (long)p.Dk * 2, Dh * p.Dk * 2,
+                      p.Dv, 0, 0};
+        e = tc_gemm(wv, latent, nh * p.Dv, (int)kv_pad, p.Dk, p.B, true, vws, kv_pad, 1,
+                    (long)p.hs * p.Dv * kv_pad, 0, st);
+        if (e != cudaSuccess) return e;
+        a.head_off = h0;
+        dim3 grid((p.s_q + BQ - 1) / BQ, nh, p.B), block(192);
+        {
+            ProfScope ps("tc_attn", st);
+            tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mQn, mQr, mK, mKr, mV, a);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t tc_attn_read_and_clear_error(unsigned *flags, cudaStream_t st) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tc_attn_err, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return e;
+    if (v) {
+        unsigned z = 0;
+        e = cudaMemcpyToSymbolAsync(g_tc_attn_err, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    *flags |= v;
+    return e;
+}
+
+}  // namespace mla

@@ -1,0 +1,39 @@
+// tc_internal.h -- host-side helpers shared by the tensor-core translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+// A K-major 16-bit operand reached through a 3-D TMA map (k, row, z).  A tile of
+// `tile` GEMM rows starting at r0 is loaded from (row = r0 % rows_per_z,
+// z = zbase + r0 / rows_per_z + batch * z_per_batch); when rows_per_z < tile one
+// box spans tile / rows_per_z consecutive z-slices.
+struct TmaOperand {
+    const void *ptr;
+    long k_extent;    // elements along k (contiguous)
+    long rows;        // rows of one z-slice present in memory
+    long z_extent;    // z-slices present in memory
+    long row_stride;  // bytes between rows
+    long z_stride;    // bytes between z-slices
+    int rows_per_z;
+    int zbase;
+    int z_per_batch;
+};
+
+// Encodes a tiled TMA map for 16-bit elements with 128-byte swizzle and a box of
+// {64, ...}.  rank <= 5; strides in bytes for dims 1..rank-1.
+cudaError_t make_tma_map(CUtensorMap *map, const void *ptr, int rank, const unsigned long long *dims,
+                         const unsigned long long *strides, const unsigned *box);
+cudaError_t make_operand_map(CUtensorMap *map, const TmaOperand &op, int tile_rows);
+
+// C[batch](m, n) = sum_k A(m, k) B(n, k); K % 64 == 0.  out_kind: 0 fp16, 1 bf16, 2 fp32.
+cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int K, int batch, bool f16,
+                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st);
+
+cudaError_t tc_gemm_read_and_clear_error(unsigned *flags, cudaStream_t st);
+cudaError_t tc_attn_read_and_clear_error(unsigned *flags, cudaStream_t st);
+cudaError_t tc_latent_read_and_clear_error(unsigned *flags, cudaStream_t st);
+
+}  // namespace mla

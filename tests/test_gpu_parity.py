@@ -265,3 +265,28 @@ def test_empty_calls_are_noops():
     z = {k: (v[:, :0] if k in ("q_nope", "q_pe") else v) for k, v in inp.items()}
     o, l = mla.latent_attn_fwd(d, z["q_nope"], z["q_pe"], z["c_kv"], z["k_pe"], z["w_kv_b"], z["rms_w"])
     assert o.shape[1] == 0 and l.shape[2] == 0
+
+
+# ------------------------------------------------- tensor cores vs CUDA cores ----
+@pytest.mark.parametrize("absorbed", [False, True])
+def test_tensor_core_path_matches_simt_path(absorbed):
+    """Same bf16 call through both kernel families (the SIMT one forced)."""
+    cfg = dataclasses.replace(RAGGED, s_kv=700, s_q=500, q_offset=200, batch=1, head_shard=4)
+    d_in = dev(inputs.prefill_inputs(cfg))
+    o_tc, l_tc = run_prefill(cfg, d_in, absorbed=absorbed)
+    path_tc = mla.last_path()
+    mla.set_path_override(1)
+    try:
+        o_s, l_s = run_prefill(cfg, d_in, absorbed=absorbed)
+        assert mla.last_path() == mla.PATH_SIMT
+    finally:
+        mla.set_path_override(0)
+    check_out(o_tc, o_s.float(), torch.bfloat16, "tc vs simt (path %d)" % path_tc)
+    check_lse(l_tc, l_s)
+
+
+def test_explicit_bf16_uses_tensor_cores():
+    cfg = dataclasses.replace(RAGGED, batch=1)
+    d_in = dev(inputs.prefill_inputs(cfg))
+    run_prefill(cfg, d_in)
+    assert mla.last_path() == mla.PATH_TC
