@@ -129,8 +129,13 @@ mla_status prefill_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_
 
 struct PrefillWs {
     void *chat, *kpe, *qpe, *k, *v, *qabs, *olat, *w16;
+    float2 *rtab;
     size_t bytes;
 };
+
+// RoPE table positions of a prefill call: keys [0, kv_need) and queries
+// [q_offset, q_offset + s_q) (beyond kv_need only for non-causal calls).
+long rope_positions(const Prefill &p) { return std::max(p.kv_need, (long)p.q_offset + p.s_q); }
 
 PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
     Carve c;
@@ -140,6 +145,7 @@ PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
     w.chat = c.take((size_t)p.B * p.kv_pad * p.Dk * es);
     w.kpe = c.take((size_t)p.B * p.kv_pad * p.Dr * es);
     w.qpe = c.take((size_t)p.B * p.s_q * p.head_count * p.Dr * es);
+    w.rtab = (float2 *)c.take((size_t)rope_positions(p) * (p.Dr / 2) * sizeof(float2));
     if (p.tc) w.w16 = c.take((size_t)p.hs * (p.Dn + p.Dv) * p.Dk * 2);
     if (!absorbed) {
         // per-shard K_nope and V (tensor-core path: V stored transposed)
@@ -181,10 +187,11 @@ mla_status prefill_common_checks(const Prefill &p, bool absorbed, const void *q_
 // Common first steps of both prefill forms: normalised latent, rotated k_pe and q_pe.
 mla_status prefill_prep(const Prefill &p, const mla_dims *d, const void *q_pe, const void *c_kv, const void *k_pe,
                         const void *rms_w, const PrefillWs &w, cudaStream_t st) {
+    MLA_TRY(launch_rope_table(0, rope_positions(p), p.Dr, d->rope_base, w.rtab, st));
     MLA_TRY(launch_latent_prep(p.tin, p.tmid, p.B, p.s_kv, (int)p.kv_need, (int)p.kv_pad, p.Dk, p.Dr, c_kv, k_pe,
-                               rms_w, d->rms_eps, d->rope_base, w.chat, w.kpe, st));
+                               rms_w, d->rms_eps, w.rtab, w.chat, w.kpe, st));
     long rows = (long)p.B * p.s_q * p.head_count;
-    MLA_TRY(launch_rope_rows(p.tin, p.tmid, rows, p.Dr, q_pe, p.q_offset, p.head_count, p.s_q, d->rope_base, w.qpe,
+    MLA_TRY(launch_rope_rows(p.tin, p.tmid, rows, p.Dr, q_pe, p.q_offset, p.head_count, p.s_q, w.rtab, 0, w.qpe,
                              st));
     return MLA_OK;
 }
@@ -418,6 +425,7 @@ mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int 
 struct DecodeWs {
     void *qabs, *qpe, *olat, *w16;
     float *po, *pl;
+    float2 *rtab;
     size_t bytes;
 };
 
@@ -430,6 +438,7 @@ DecodeWs decode_ws(const Decode &p, void *base, bool own_partials) {
     w.qabs = c.take(rows * p.Dk * es);
     w.qpe = c.take(rows * p.Dr * es);
     w.olat = c.take(rows * p.Dk * es);
+    w.rtab = (float2 *)c.take((size_t)(p.Dr / 2) * sizeof(float2));
     if (p.tc) w.w16 = c.take((size_t)p.H * (p.Dn + p.Dv) * p.Dk * 2);
     if (own_partials) {
         w.po = (float *)c.take((size_t)p.n * rows * p.Dk * 4);
@@ -445,7 +454,8 @@ mla_status decode_simt(const Decode &p, float scale, const mla_dims *d, const vo
     const size_t ein = ty_size(p.tin);
     const long Dh = p.Dn + p.Dv;
     long rows = (long)p.B * p.H;
-    MLA_TRY(launch_rope_rows(p.tin, p.tmid, rows, p.Dr, q_pe, p.L - 1, 1, 1, d->rope_base, w.qpe, st));
+    MLA_TRY(launch_rope_table(p.L - 1, 1, p.Dr, d->rope_base, w.rtab, st));
+    MLA_TRY(launch_rope_rows(p.tin, p.tmid, rows, p.Dr, q_pe, p.L - 1, 1, 1, w.rtab, p.L - 1, w.qpe, st));
     GemmArgs g{};
     g.M = p.B;
     g.N = p.Dk;

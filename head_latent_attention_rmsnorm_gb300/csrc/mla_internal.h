@@ -25,17 +25,22 @@ struct ProfScope {
 
 // ------------------------------------------------------------------ shared prep ----
 
+// RoPE table: tab[(pos - pos0) * Dr/2 + t] = (cos, sin)(pos * base^(-2t/Dr)) for
+// positions [pos0, pos0 + n_pos), angles formed in double precision.
+cudaError_t launch_rope_table(long pos0, long n_pos, int Dr, float base, float2 *tab, cudaStream_t st);
+
 // One warp per latent row: chat = RMSNorm(c_kv) * rms_w and kpe = RoPE(k_pe, j) for
 // keys j < n_rows of every batch.  c_kv [B, s_kv, Dk], k_pe [B, s_kv, Dr] (storage
 // tin) -> chat [B, pad_rows, Dk], kpe [B, pad_rows, Dr] (storage tout); rows
-// n_rows..pad_rows-1 are zero-filled.
+// n_rows..pad_rows-1 are zero-filled.  `tab` covers positions from 0.
 cudaError_t launch_latent_prep(int tin, int tout, int B, int s_kv, int n_rows, int pad_rows, int Dk, int Dr,
-                               const void *c_kv, const void *k_pe, const void *rms_w, float eps, float base,
+                               const void *c_kv, const void *k_pe, const void *rms_w, float eps, const float2 *tab,
                                void *chat, void *kpe, cudaStream_t st);
 
-// RoPE on `rows` rows of width Dr; row r sits at position pos0 + (r / pos_div) % pos_mod.
+// RoPE on `rows` rows of width Dr; row r sits at position pos0 + (r / pos_div) % pos_mod;
+// `tab` starts at position tab_pos0.
 cudaError_t launch_rope_rows(int tin, int tout, long rows, int Dr, const void *x, long pos0, long pos_div,
-                             long pos_mod, float base, void *y, cudaStream_t st);
+                             long pos_mod, const float2 *tab, long tab_pos0, void *y, cudaStream_t st);
 
 // y[i] = x[i] for i < n, converting storage type.
 cudaError_t launch_convert(int tin, const void *x, int tout, void *y, long n, cudaStream_t st);

@@ -42,27 +42,36 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Rotates one Dr-wide band at `pos` (half-split pairs t, t+Dr/2).  The angle
-// pos*theta_t is formed and reduced in double precision: positions reach
-// 10^4..10^5, where a float angle would already be off by ~1e-3 rad.
-__device__ void rope_band(const void *x, int tx, long xo, void *y, int ty, long yo, int Dr, double pos,
-                          double base, int lane) {
+// cos/sin of pos * base^(-2t/Dr) for positions [pos0, pos0 + n_pos), t < Dr/2.
+// The angle is formed and reduced in double precision: positions reach 10^4..10^5,
+// where a float angle would already be off by ~1e-3 rad.
+__global__ void rope_table_kernel(long pos0, long n_pos, int half, int Dr, double base, float2 *tab) {
+    long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_pos * half) return;
+    long pos = pos0 + i / half;
+    int t = (int)(i % half);
+    double theta = pow(base, -2.0 * (double)t / (double)Dr);
+    double s, c;
+    sincos((double)pos * theta, &s, &c);
+    tab[i] = make_float2((float)c, (float)s);
+}
+
+// Rotates one Dr-wide band (half-split pairs t, t+Dr/2) with table row `cs`.
+__device__ __forceinline__ void rope_band(const void *x, int tx, long xo, void *y, int ty, long yo, int Dr,
+                                          const float2 *cs, int lane) {
     int half = Dr / 2;
     for (int t = lane; t < half; t += 32) {
-        double theta = pow(base, -2.0 * (double)t / (double)Dr);
-        double s, c;
-        sincos(pos * theta, &s, &c);
+        float2 r = cs[t];
         float x0 = ldx(x, tx, xo + t), x1 = ldx(x, tx, xo + t + half);
-        float cf = (float)c, sf = (float)s;
-        stx(y, ty, yo + t, x0 * cf - x1 * sf);
-        stx(y, ty, yo + t + half, x1 * cf + x0 * sf);
+        stx(y, ty, yo + t, x0 * r.x - x1 * r.y);
+        stx(y, ty, yo + t + half, x1 * r.x + x0 * r.y);
     }
 }
 
 // RMSNorm of c_kv rows and RoPE of k_pe rows.  Rows j in [n_rows, pad_rows) of each
 // batch are written as zeros, so that padded tiles read later hold finite values.
 __global__ void latent_prep_kernel(int B, int s_kv, int n_rows, int pad_rows, int Dk, int Dr, const void *c_kv,
-                                   const void *k_pe, const void *rms_w, int tin, float eps, float base,
+                                   const void *k_pe, const void *rms_w, int tin, float eps, const float2 *tab,
                                    void *chat, void *kpe, int tout) {
     long row = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     int lane = threadIdx.x % 32;
@@ -83,15 +92,71 @@ __global__ void latent_prep_kernel(int B, int s_kv, int n_rows, int pad_rows, in
     float inv = 1.0f / sqrtf(ss / (float)Dk + eps);
     for (int k = lane; k < Dk; k += 32)
         stx(chat, tout, row * Dk + k, ldx(c_kv, tin, xo + k) * inv * ldx(rms_w, tin, k));
-    rope_band(k_pe, tin, (b * s_kv + j) * Dr, kpe, tout, row * Dr, Dr, (double)j, (double)base, lane);
+    rope_band(k_pe, tin, (b * s_kv + j) * Dr, kpe, tout, row * Dr, Dr, tab + j * (Dr / 2), lane);
+}
+
+// Same, bf16 inputs with Dk a multiple of 256: each lane moves 16-byte vectors.
+template <typename TO>
+__global__ void latent_prep_vec_kernel(int B, int s_kv, int n_rows, int pad_rows, int Dk, int Dr,
+                                       const __nv_bfloat16 *c_kv, const __nv_bfloat16 *k_pe,
+                                       const __nv_bfloat16 *rms_w, float eps, const float2 *tab, TO *chat,
+                                       TO *kpe) {
+    long row = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    int lane = threadIdx.x % 32;
+    if (row >= (long)B * pad_rows) return;
+    long b = row / pad_rows, j = row % pad_rows;
+    const int nc = Dk / 256;                     // 16-byte chunks per lane
+    TO *y = chat + row * Dk;
+    if (j >= n_rows) {
+        for (int k = lane; k < Dk; k += 32) y[k] = TO(0.f);
+        for (int k = lane; k < Dr; k += 32) kpe[row * Dr + k] = TO(0.f);
+        return;
+    }
+    const uint4 *x = (const uint4 *)(c_kv + (b * s_kv + j) * Dk);
+    const uint4 *w = (const uint4 *)rms_w;
+    float v[4][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c < nc) {
+            uint4 q = x[c * 32 + lane];
+            const __nv_bfloat16 *e = (const __nv_bfloat16 *)&q;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[c][i] = __bfloat162float(e[i]);
+                ss += v[c][i] * v[c][i];
+            }
+        }
+    }
+    ss = warp_sum(ss);
+    float inv = 1.0f / sqrtf(ss / (float)Dk + eps);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c < nc) {
+            uint4 q = w[c * 32 + lane];
+            const __nv_bfloat16 *e = (const __nv_bfloat16 *)&q;
+            TO *dst = y + (c * 32 + lane) * 8;
+            if (sizeof(TO) == 2) {
+                __align__(16) __half hv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hv[i] = __float2half_rn(v[c][i] * inv * __bfloat162float(e[i]));
+                *(uint4 *)dst = *(const uint4 *)hv;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[i] = TO(v[c][i] * inv * __bfloat162float(e[i]));
+            }
+        }
+    }
+    rope_band(k_pe, TY_BF16, (b * s_kv + j) * Dr, kpe, sizeof(TO) == 4 ? TY_F32 : TY_F16, row * Dr, Dr,
+              tab + j * (Dr / 2), lane);
 }
 
 __global__ void rope_rows_kernel(long rows, int Dr, const void *x, int tin, long pos0, long pos_div, long pos_mod,
-                                 float base, void *y, int tout) {
+                                 const float2 *tab, long tab_pos0, void *y, int tout) {
     long r = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (r >= rows) return;
     long pos = pos0 + (r / pos_div) % pos_mod;
-    rope_band(x, tin, r * Dr, y, tout, r * Dr, Dr, (double)pos, (double)base, threadIdx.x % 32);
+    rope_band(x, tin, r * Dr, y, tout, r * Dr, Dr, tab + (pos - tab_pos0) * (Dr / 2), threadIdx.x % 32);
 }
 
 __global__ void convert_kernel(const void *x, int tin, void *y, int tout, long n) {
@@ -293,22 +358,41 @@ inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / 
 
 }  // namespace
 
+cudaError_t launch_rope_table(long pos0, long n_pos, int Dr, float base, float2 *tab, cudaStream_t st) {
+    long n = n_pos * (Dr / 2);
+    if (n == 0) return cudaSuccess;
+    ProfScope ps("rope_table", st);
+    rope_table_kernel<<<blocks_for(n, 256), 256, 0, st>>>(pos0, n_pos, Dr / 2, Dr, (double)base, tab);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_latent_prep(int tin, int tout, int B, int s_kv, int n_rows, int pad_rows, int Dk, int Dr,
-                               const void *c_kv, const void *k_pe, const void *rms_w, float eps, float base,
+                               const void *c_kv, const void *k_pe, const void *rms_w, float eps, const float2 *tab,
                                void *chat, void *kpe, cudaStream_t st) {
     long rows = (long)B * pad_rows;
     if (rows == 0) return cudaSuccess;
     ProfScope ps("latent_prep", st);
-    latent_prep_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(B, s_kv, n_rows, pad_rows, Dk, Dr, c_kv, k_pe, rms_w,
-                                                            tin, eps, base, chat, kpe, tout);
+    bool vec = tin == TY_BF16 && Dk % 256 == 0 && Dk <= 1024 && (((uintptr_t)c_kv | (uintptr_t)rms_w) & 15) == 0;
+    if (vec && tout == TY_F16)
+        latent_prep_vec_kernel<__half><<<blocks_for(rows, 8), 256, 0, st>>>(
+            B, s_kv, n_rows, pad_rows, Dk, Dr, (const __nv_bfloat16 *)c_kv, (const __nv_bfloat16 *)k_pe,
+            (const __nv_bfloat16 *)rms_w, eps, tab, (__half *)chat, (__half *)kpe);
+    else if (vec && tout == TY_F32)
+        latent_prep_vec_kernel<float><<<blocks_for(rows, 8), 256, 0, st>>>(
+            B, s_kv, n_rows, pad_rows, Dk, Dr, (const __nv_bfloat16 *)c_kv, (const __nv_bfloat16 *)k_pe,
+            (const __nv_bfloat16 *)rms_w, eps, tab, (float *)chat, (float *)kpe);
+    else
+        latent_prep_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(B, s_kv, n_rows, pad_rows, Dk, Dr, c_kv, k_pe,
+                                                                rms_w, tin, eps, tab, chat, kpe, tout);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rope_rows(int tin, int tout, long rows, int Dr, const void *x, long pos0, long pos_div,
-                             long pos_mod, float base, void *y, cudaStream_t st) {
+                             long pos_mod, const float2 *tab, long tab_pos0, void *y, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
     ProfScope ps("rope_rows", st);
-    rope_rows_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(rows, Dr, x, tin, pos0, pos_div, pos_mod, base, y, tout);
+    rope_rows_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(rows, Dr, x, tin, pos0, pos_div, pos_mod, tab, tab_pos0,
+                                                          y, tout);
     return cudaGetLastError();
 }
 

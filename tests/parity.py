@@ -38,7 +38,7 @@ def check_lse(gpu, ref, what="lse"):
     assert g.shape == r.shape, (what, g.shape, r.shape)
     both_inf = np.isneginf(g) & np.isneginf(r)
     assert np.array_equal(np.isneginf(g), np.isneginf(r)), what + ": -inf pattern differs"
-    d = np.abs(np.where(both_inf, 0.0, g - r))
+    d = np.abs(np.where(both_inf, 0.0, np.where(both_inf, 0.0, g) - np.where(both_inf, 0.0, r)))
     err = d.max() if d.size else 0.0
     assert err <= LSE_ABS, "%s: max abs err %.3e > %.0e" % (what, err, LSE_ABS)
     return err
