@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             getattr(L, f).restype = _i
         L.mla_decode_splitkv.argtypes = [D, _i, _i, _i, _i] + [_vp] * 9 + [_vp, _sz, _vp]
         L.mla_decode_splitkv.restype = _i
+        L.mla_decode_splitkv_noalloc.argtypes = [D, _i, _i, _i, _i] + [_vp] * 7 + [_vp]
+        L.mla_decode_splitkv_noalloc.restype = _i
         L.mla_lse_combine.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
         L.mla_lse_combine.restype = _i
         for f in ("mla_latent_attn_workspace", "mla_absorbed_attn_workspace"):
@@ -108,6 +110,13 @@ def mla_absorbed_attn_fwd(*args) -> int:
 
 def mla_decode_splitkv(*args) -> int:
     return lib().mla_decode_splitkv(*args)
+
+
+def mla_decode_splitkv_noalloc(*args) -> int:
+    return lib().mla_decode_splitkv_noalloc(*args)
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20   # MLA_NOALLOC_SCRATCH_BYTES in include/mla.h
 
 
 def mla_lse_combine(*args) -> int:

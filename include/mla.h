@@ -170,6 +170,34 @@ int mla_last_path(void);
 void mla_set_path_override(int mode);
 
 /*
+ * Split-KV decode that allocates nothing.  The pages have no counterpart: this is
+ * a library convenience for callers that cannot allocate device memory, such as
+ * code that runs while a stream is being captured into a CUDA graph (where
+ * cudaMalloc is refused), or a host runtime that owns every byte of device memory
+ * through its own pool and gives its plugins no allocator.
+ * It computes exactly what mla_decode_splitkv computes (same arguments and layouts,
+ * partials kept internally), using as its scratch a fixed array of
+ * MLA_NOALLOC_SCRATCH_BYTES bytes that the library defines in device memory; every
+ * GPU that loads the library holds that array until the process exits.
+ *  - A call needing more scratch than the array holds (see mla_decode_workspace)
+ *    returns MLA_ERR_WORKSPACE and launches nothing.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture begins.
+ *  - Every call shares the one array and leaves its contents behind.  Nothing in it
+ *    needs to start at zero: each call writes all the scratch it reads.  Calls
+ *    that overlap on the GPU (other streams, other host threads) race on it;
+ *    serialise them.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int B, int kv_len,
+                                      int n_splits, const void *q_nope, const void *q_pe,
+                                      const void *c_cache, const void *kpe_cache,
+                                      const void *w_kv_b, void *out, float *lse,
+                                      void *cuda_stream);
+
+/*
  * Measurement hooks (not part of the computation).
  * mla_launch_count: kernels this library has launched since load, all threads.
  * mla_profile_enable(1): from now on every launch is bracketed by a pair of CUDA
