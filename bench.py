@@ -374,6 +374,33 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """Only `warmup + steps` calls of one workload, no timing or report: the target of
+    ncu captures.  --only prefill|decode; --workload picks a prefill config by name."""
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import build as mla_build
+    from head_latent_attention_rmsnorm_gb300 import configs, mla
+    mla_build.build()
+    mla.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    if args.only == "prefill":
+        cfg = configs.ALL[args.workload] if args.workload else configs.V2LITE
+        d, t, out, lse, ws = prefill_setup(cfg)
+        fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
+    else:
+        cfg = configs.DECODE
+        d, t, out, lse, ws = decode_setup(cfg)
+        fn = lambda: decode_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    st = mla.mla_check_device_error(None)
+    print("%s %s: %d calls, path %d, device status %s" % (args.only, cfg.name, args.warmup + args.steps,
+                                                       mla.last_path(), mla.mla_status_string(st)))
+    if st != 0:
+        sys.exit(1)
+
+
 # -------------------------------------------------------- oracle (CPU) ----
 def oracle_prefill_sample(rows: int):
     """Time the oracle on the last `rows` query rows of the V2-Lite prefill, all 16 heads.
@@ -442,6 +469,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("prefill", "decode"), default=None,
+                    help="run only this workload's calls, without timing (profiling target)")
+    ap.add_argument("--workload", default=None, help="prefill workload name for --only prefill")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -451,6 +481,9 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup(args)
+    if args.only:
+        run_case(args)
+        return
     run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist

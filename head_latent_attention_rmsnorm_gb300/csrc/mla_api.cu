@@ -44,7 +44,7 @@ bool valid_dtype(mla_dtype dt) { return dt == MLA_F32 || dt == MLA_BF16; }
 mla_status check_dims(const mla_dims *d) {
     if (!d) return MLA_ERR_NULL;
     if (d->n_heads <= 0 || d->d_kv <= 0 || d->d_nope <= 0 || d->d_rope <= 0 || d->d_v <= 0 ||
-        (d->d_rope & 1) || !(d->rope_base > 0.f) || !(d->rms_eps >= 0.f))
+        (d->d_rope & 1) || d->d_rope > 1024 || !(d->rope_base > 0.f) || !(d->rms_eps >= 0.f))
         return MLA_ERR_SHAPE;
     return MLA_OK;
 }
@@ -119,7 +119,8 @@ mla_status prefill_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_
     if (absorbed && (p->Dk + p->Dr > 640 || p->Dk > 512)) return MLA_ERR_UNSUPPORTED;
     p->tc = false;
     if (dt == MLA_BF16 && g_path_override != 1 && p->kv_need >= 1) {
-        p->tc = absorbed ? tc_absorbed_supported(p->Dk, p->Dn, p->Dr, p->Dv)
+        // the absorbed form's per-head GEMMs tile the query rows by 128
+        p->tc = absorbed ? tc_absorbed_supported(p->Dk, p->Dn, p->Dr, p->Dv) && (s_q >= 128 || 128 % s_q == 0)
                          : tc_explicit_supported(p->Dk, p->Dn, p->Dr, p->Dv);
     }
     p->tin = ty_of(dt);
@@ -660,6 +661,9 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
     float scale = scale_of(dims);
     g_last_path = p.tc ? 2 : 1;
     if (p.tc) {
+        const long rows = (long)p.B * p.H;
+        MLA_TRY(launch_rope_table(p.L - 1, 1, p.Dr, dims->rope_base, w.rtab, cs));
+        MLA_TRY(launch_rope_rows(p.tin, TY_F16, rows, p.Dr, q_pe, p.L - 1, 1, 1, w.rtab, p.L - 1, w.qpe, cs));
         TcDecode t{p.B, p.L, p.n, p.H, p.Dk, p.Dn, p.Dr, p.Dv, p.chunk, scale, dims->rope_base};
         return cuda_status(tc_decode(t, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w.qabs, w.qpe,
                                      w.olat, w.w16, cs));

@@ -43,17 +43,23 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // cos/sin of pos * base^(-2t/Dr) for positions [pos0, pos0 + n_pos), t < Dr/2.
-// The angle is formed and reduced in double precision: positions reach 10^4..10^5,
-// where a float angle would already be off by ~1e-3 rad.
+// The angle is formed and reduced to [-pi, pi] in double precision (positions reach
+// 10^4..10^5, where a float angle would already be off by ~1e-3 rad); the reduced
+// angle then goes through the float sincos.  theta_t is computed once per block.
 __global__ void rope_table_kernel(long pos0, long n_pos, int half, int Dr, double base, float2 *tab) {
+    __shared__ double theta[512];
+    for (int t = threadIdx.x; t < half && t < 512; t += blockDim.x) theta[t] = pow(base, -2.0 * (double)t / (double)Dr);
+    __syncthreads();
     long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_pos * half) return;
     long pos = pos0 + i / half;
     int t = (int)(i % half);
-    double theta = pow(base, -2.0 * (double)t / (double)Dr);
-    double s, c;
-    sincos((double)pos * theta, &s, &c);
-    tab[i] = make_float2((float)c, (float)s);
+    const double two_pi = 6.283185307179586476925286766559;
+    double a = (double)pos * theta[t];
+    a -= two_pi * rint(a / two_pi);
+    float s, c;
+    sincosf((float)a, &s, &c);
+    tab[i] = make_float2(c, s);
 }
 
 // Rotates one Dr-wide band (half-split pairs t, t+Dr/2) with table row `cs`.

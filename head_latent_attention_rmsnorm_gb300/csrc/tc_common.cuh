@@ -51,14 +51,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+// Suspend-time hint (ns) of a try_wait: a waiting warp is parked, not re-issued,
+// until the phase completes or the hint elapses, so waiting warps do not take issue
+// slots from the warps that share their scheduler.
+constexpr uint32_t SUSPEND_HINT_NS = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_HINT_NS)
         : "memory");
     return ok != 0;
 }
@@ -178,6 +183,58 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ clusters ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_peer(uint32_t local_saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior
+// writes (including shared::cluster stores) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t peer_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(peer_bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_HINT_NS)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (for phases completed by the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  unsigned *err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*abort) return false;
+            if (global_ns() - t0 > WAIT_NS) break;
+        }
+    }
+    atomicOr(err, ERR_WAIT_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+
 // ------------------------------------------------------------- descriptors ----
 // Shared-memory matrix descriptor, 128-byte swizzle.  `lbo`/`sbo` in bytes.
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4
@@ -195,6 +252,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 }
 // K-major tile of 1024-byte atoms stacked along M/N.
 __device__ __forceinline__ uint64_t sdesc_kmajor(const void *tile) { return sdesc_sw128(smem_u32(tile), 16, 1024); }
+// MN-major operand: each 128-byte row holds 64 consecutive MN elements of one k; eight
+// k-rows form an atom (stride 1024 bytes along K); consecutive 64-element MN blocks
+// are `mn_block_bytes` apart (the leading byte offset).
+__device__ __forceinline__ uint64_t sdesc_mnmajor(const void *tile, uint32_t mn_block_bytes) {
+    return sdesc_sw128(smem_u32(tile), mn_block_bytes, 1024);
+}
 
 // Instruction descriptor, kind::f16: fp32 accumulate; `f16` selects fp16 (1) or
 // bf16 (0) operands; K-major A; B K-major unless b_mn.

@@ -290,3 +290,20 @@ def test_explicit_bf16_uses_tensor_cores():
     d_in = dev(inputs.prefill_inputs(cfg))
     run_prefill(cfg, d_in)
     assert mla.last_path() == mla.PATH_TC
+
+
+def test_decode_tensor_core_path_matches_simt_path():
+    cfg = dataclasses.replace(configs.DECODE, batch=2, kv_len=2500, n_splits=3)
+    inp = dev(inputs.decode_inputs(cfg))
+    o_tc, l_tc, po_tc, pl_tc = run_decode(cfg, inp, cfg.n_splits)
+    assert mla.last_path() == mla.PATH_TC
+    mla.set_path_override(1)
+    try:
+        o_s, l_s, po_s, pl_s = run_decode(cfg, inp, cfg.n_splits)
+        assert mla.last_path() == mla.PATH_SIMT
+    finally:
+        mla.set_path_override(0)
+    check_out(o_tc, o_s.float(), torch.bfloat16, "decode tc vs simt")
+    check_lse(l_tc, l_s)
+    check_out(po_tc, po_s, torch.bfloat16, "partials tc vs simt")
+    check_lse(pl_tc, pl_s)
