@@ -389,6 +389,9 @@ def run_case(args):
         fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
     else:
         cfg = configs.DECODE
+        if args.batch:
+            import dataclasses
+            cfg = dataclasses.replace(cfg, batch=args.batch)
         d, t, out, lse, ws = decode_setup(cfg)
         fn = lambda: decode_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
     for _ in range(args.warmup + args.steps):
@@ -472,6 +475,7 @@ def main():
     ap.add_argument("--only", choices=("prefill", "decode"), default=None,
                     help="run only this workload's calls, without timing (profiling target)")
     ap.add_argument("--workload", default=None, help="prefill workload name for --only prefill")
+    ap.add_argument("--batch", type=int, default=0, help="decode batch for --only decode (default 64)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
