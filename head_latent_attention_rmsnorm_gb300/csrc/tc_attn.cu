@@ -14,7 +14,8 @@
 //   warp 1    tcgen05 issuer: S_j = Q K_j^T (M=128, N=128, K=192) into one of two
 //             TMEM S buffers; O += P_{j-1} V_{j-1} (M=128, N=128, K=128) with P read
 //             from TMEM where the softmax wrote it over S_{j-1}.
-//   warps 2-5 softmax, one query row per thread (TMEM lane = row): online softmax
+//   warps 2-9 softmax, two threads per query row (TMEM lane = row; keys 0-63 and
+//             64-127 of each tile): online softmax
 //             in the log2 domain; O in TMEM is rescaled only when a row maximum
 //             grows by more than 2^8 (the stale maximum keeps every p <= 256, exact
 //             after the final division); epilogue O / l and lse.
@@ -44,7 +45,7 @@ constexpr uint32_t Q_BYTES = 3 * BOX;          // nope lo, nope hi, rope
 constexpr uint32_t K_BYTES = 3 * BOX;
 constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halves
 constexpr int KST = 2, VST = 2;
-constexpr uint32_t SMEM_BYTES = Q_BYTES + KST * K_BYTES + VST * V_BYTES + 1024 + 256;
+constexpr uint32_t SMEM_BYTES = Q_BYTES + KST * K_BYTES + VST * V_BYTES + 1024 + 256 + 4 * 2 * 2 * BQ;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct AttnK {
@@ -64,7 +65,7 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     tc_attn_kernel(const __grid_constant__ CUtensorMap mQn, const __grid_constant__ CUtensorMap mQr,
                    const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
                    const __grid_constant__ CUtensorMap mV, AttnK p) {
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *s_full = bars + 10, *p_full = bars + 12;
     uint64_t *o_done = bars + 14, *o_final = bars + 15;
     uint32_t *tslot = (uint32_t *)(bars + 16);
+    float (*red)[2][BQ] = (float (*)[2][BQ])(bars + 24);   // [tile parity][half][row] partial maxima
     volatile int *abort = (volatile int *)(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -91,14 +93,14 @@ __global__ void __launch_bounds__(192, 1)
 
     if (tid == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_ready, 4);
+        mbar_init(q_ready, 8);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&p_full[i], 8);
         }
         mbar_init(o_done, 1);
         mbar_init(o_final, 1);
@@ -184,123 +186,130 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ---------------------------------------------------------- softmax warps
-        const int quad = warp & 3;
+        // Two threads per query row: warps 2-5 take keys 0-63 of each tile, warps 6-9
+        // keys 64-127 (warp w and w+4 reach the same TMEM lanes).  The halves combine
+        // their row maxima through shared memory once per tile.
+        const int quad = warp & 3, hf = (warp - 2) >> 2;
         const int row = quad * 32 + lane;
         const int pos = p.q_offset + q0 + row;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        // widen this row of the bf16 q_nope boxes to fp16 in place
+        // widen this row's half of the bf16 q_nope tile to fp16 in place
         bool ok = mbar_wait(q_full, 0, abort, &g_tc_attn_err);
         if (ok) {
+            uint4 *rp = (uint4 *)(sQ + hf * BOX + row * 128);
 #pragma unroll
-            for (int bx = 0; bx < 2; ++bx) {
-                uint4 *rp = (uint4 *)(sQ + bx * BOX + row * 128);
+            for (int c = 0; c < 8; ++c) {
+                uint4 v = rp[c];
+                uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 v = rp[c];
-                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w[i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-                    rp[c] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
+                for (int i = 0; i < 4; ++i)
+                    w[i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+                rp[c] = make_uint4(w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
 
+        // A failed wait clears `ok` (warp-uniform) but never leaves the loop early: every
+        // softmax thread passes the same named barriers, so an abort cannot strand one.
         float m = -INFINITY, l = 0.f;
-        for (int j = 0; j < nt && ok; ++j) {
+        ok = __all_sync(0xffffffffu, ok);
+        for (int j = 0; j < nt; ++j) {
             const int sb = j & 1;
-            if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort, &g_tc_attn_err)) {
-                ok = false;
-                break;
-            }
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[sb], (j >> 1) & 1, abort, &g_tc_attn_err));
             tc_fence_after();
-            uint32_t s[4][32];
+            uint32_t s[2][32];
+            if (ok) {
+                tmem_ld32(lane_base + sb * 128 + hf * 64, s[0]);
+                tmem_ld32(lane_base + sb * 128 + hf * 64 + 32, s[1]);
+                tmem_ld_wait();
+            } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + sb * 128 + c * 32, s[c]);
-            tmem_ld_wait();
-            const int j0 = j * BKV;
-            const bool masked = (j0 + BKV > p.kv_need) || (p.causal && j0 + BKV - 1 > p.q_offset + q0);
-            float x[4][32];
-            float mt = -INFINITY;
+                for (int i = 0; i < 32; ++i) s[0][i] = s[1][i] = 0u;
+            }
+            const int j0 = j * BKV + hf * 64;
+            const bool masked = (j0 + 64 > p.kv_need) || (p.causal && j0 + 63 > p.q_offset + q0);
+            float x[64];
+            float ml = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float v = __uint_as_float(s[c][i]) * p.scale_log2;
-                    if (masked) {
-                        const int key = j0 + c * 32 + i;
-                        if (key >= p.kv_need || (p.causal && key > pos)) v = -INFINITY;
-                    }
-                    x[c][i] = v;
-                    mt = fmaxf(mt, v);
+            for (int c = 0; c < 64; ++c) {
+                float v = __uint_as_float(s[c >> 5][c & 31]);
+                if (masked) {
+                    const int key = j0 + c;
+                    if (key >= p.kv_need || (p.causal && key > pos)) v = -INFINITY;
                 }
+                x[c] = v;
+                ml = fmaxf(ml, v);
+            }
+            // both halves have read their S columns before either writes P over them
+            red[sb][hf][row] = ml;
+            named_bar_sync(1, 256);
+            const float mt = fmaxf(ml, red[sb][hf ^ 1][row]) * p.scale_log2;
             const float m_new = fmaxf(m, mt);
             const bool need = m_new > m + RESCALE_LOG2;   // also true on the first finite maximum
             if (__any_sync(0xffffffffu, need)) {
                 const float m_use = need ? m_new : m;
                 const float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_use);
-                if (j > 0) {
-                    if (!mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_attn_err)) {
-                        ok = false;
-                        break;
-                    }
+                if (j > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_attn_err));
+                if (j > 0 && ok) {
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(lane_base + 256 + c * 32, o);
+                        tmem_ld32(lane_base + 256 + hf * 64 + c * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(lane_base + 256 + c * 32, o);
+                        tmem_st32(lane_base + 256 + hf * 64 + c * 32, o);
                     }
                     tmem_st_wait();
                 }
                 l *= alpha;
                 m = m_use;
             }
-            const float m_eff = (m == -INFINITY) ? 0.f : m;
+            const float nm = (m == -INFINITY) ? 0.f : -m;
             float rs = 0.f;
-            uint32_t pk[2][32];
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(x[c][2 * i] - m_eff), p1 = ex2(x[c][2 * i + 1] - m_eff);
-                    rs += p0 + p1;
-                    pk[c >> 1][(c & 1) * 16 + i] = pack_f16(p0, p1);
-                }
-            tmem_st32(lane_base + sb * 128, pk[0]);
-            tmem_st32(lane_base + sb * 128 + 32, pk[1]);
-            tmem_st_wait();
+            for (int i = 0; i < 32; ++i) {
+                const float p0 = ex2(fmaf(x[2 * i], p.scale_log2, nm));
+                const float p1 = ex2(fmaf(x[2 * i + 1], p.scale_log2, nm));
+                rs += p0 + p1;
+                pk[i] = pack_f16(p0, p1);
+            }
+            if (ok) {
+                tmem_st32(lane_base + sb * 128 + hf * 32, pk);
+                tmem_st_wait();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[sb]);
             l += rs;
         }
-        // ---- epilogue
+        // ---- epilogue: combine the halves' row sums; each half stores its 64 columns
+        red[0][hf][row] = l;
+        named_bar_sync(1, 256);
+        l += red[0][hf ^ 1][row];
         if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, &g_tc_attn_err);
         tc_fence_after();
         const int qi = q0 + row;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint32_t o[4][32];
+        uint32_t o[2][32];
         if (nt > 0) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + 256 + c * 32, o[c]);
+            tmem_ld32(lane_base + 256 + hf * 64, o[0]);
+            tmem_ld32(lane_base + 256 + hf * 64 + 32, o[1]);
             tmem_ld_wait();
         } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[c][i] = 0u;
         }
         if (ok && qi < p.s_q) {
-            uint4 *dst = (uint4 *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h);
+            uint4 *dst = (uint4 *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h + hf * 64);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     uint32_t w[4];
@@ -310,8 +319,9 @@ __global__ void __launch_bounds__(192, 1)
                                          __uint_as_float(o[c][8 * v + 2 * i + 1]) * inv);
                     dst[c * 4 + v] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-            p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] =
-                l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (hf == 0)
+                p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] =
+                    l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
     }
     tc_fence_before();
@@ -409,7 +419,7 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
                     (long)p.hs * p.Dv * kv_pad, 0, st);
         if (e != cudaSuccess) return e;
         a.head_off = h0;
-        dim3 grid((p.s_q + BQ - 1) / BQ, nh, p.B), block(192);
+        dim3 grid((p.s_q + BQ - 1) / BQ, nh, p.B), block(320);
         {
             ProfScope ps("tc_attn", st);
             tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mQn, mQr, mK, mKr, mV, a);

@@ -54,17 +54,29 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 // Suspend-time hint (ns) of a try_wait: a waiting warp is parked, not re-issued,
 // until the phase completes or the hint elapses, so waiting warps do not take issue
 // slots from the warps that share their scheduler.
-constexpr uint32_t SUSPEND_HINT_NS = 1000000;
+#ifndef MLA_WAIT_SUSPEND_NS
+#define MLA_WAIT_SUSPEND_NS 1000000
+#endif
+constexpr uint32_t SUSPEND_HINT_NS = MLA_WAIT_SUSPEND_NS;
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_HINT_NS)
-        : "memory");
+    if (SUSPEND_HINT_NS > 0)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_HINT_NS)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 // Waits for the phase of `bar` with parity `parity` to complete.  Gives up after
@@ -106,6 +118,11 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
         "%6}], [%2];" ::"r"(smem_u32(dst)),
         "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
+}
+
+// Named barrier `id` over `n` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // Generic-proxy writes to shared memory -> visible to the async proxy (tensor core).
@@ -198,6 +215,22 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t local_saddr, uint32_t rank
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
     return r;
 }
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into another
+// CTA's shared memory (`dst`, `peer_bar`: shared::cluster addresses); completes as
+// transaction bytes on the destination mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void *src, uint32_t bytes, uint32_t peer_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(peer_bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk copy of this thread has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Orders this thread's prior memory operations (including shared::cluster stores)
+// at cluster scope.
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 __device__ __forceinline__ void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -209,13 +242,22 @@ __device__ __forceinline__ void mbar_arrive_peer(uint32_t peer_bar) {
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_HINT_NS)
-        : "memory");
+    if (SUSPEND_HINT_NS > 0)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_HINT_NS)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 // Bounded wait with cluster-scope acquire (for phases completed by the peer CTA).

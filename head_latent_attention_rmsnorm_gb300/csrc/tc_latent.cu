@@ -25,8 +25,10 @@
 // before the MMAs, so that q_abs can be held in fp16 (11-bit significand) and every
 // score stays within ~3e-4 of exact.
 //
-// Warps (320 threads): 0 TMA producer, 1 MMA issuer + TMEM owner, 2-5 softmax (one
-// row per thread), 6-9 converters.
+// Warps (256 threads): 0 TMA producer, 1 MMA issuer + TMEM owner, 2-5 softmax (one
+// row per thread), 6-7 converters.  The partial-score swap is one 32 KB bulk copy
+// (cp.async.bulk, shared::cta -> shared::cluster) per tile and direction, completing
+// as transaction bytes on the receiver's mbarrier.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -48,8 +50,8 @@ using namespace tc;
 constexpr int ROWS = 128, NK = 64, ST = 4;
 constexpr uint32_t BOX = NK * 128;               // 64 keys x 64 dims (16-bit): 8 KB
 constexpr uint32_t STAGE_BYTES = 5 * BOX;        // 4 latent boxes (+ RoPE box on rank 0)
-constexpr uint32_t XBUF_BYTES = ROWS * NK * 4;   // peer's partial scores
-constexpr uint32_t SMEM_BYTES = ST * STAGE_BYTES + XBUF_BYTES + 1024 + 512;
+constexpr uint32_t XBUF_BYTES = ROWS * NK * 4;   // one tile of partial scores (send or receive)
+constexpr uint32_t SMEM_BYTES = ST * STAGE_BYTES + 2 * XBUF_BYTES + 1024 + 512;
 // TMEM columns: accumulators at multiples of their width (O 256, S 64), the A operands
 // (P: 64 keys fp16 = 32 columns; Q: up to 320 dims fp16 = 160 columns) after them.
 constexpr uint32_t T_O = 0, T_S = 256, T_P = 320, T_Q = 352;
@@ -111,13 +113,15 @@ __device__ __forceinline__ Unit unit_of(const LatK &p, int u) {
 }
 
 template <bool CONVERT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     tc_latent_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR, LatK p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *stages = smem;
-    float *xbuf = (float *)(stages + ST * STAGE_BYTES);   // [row][64] peer partial, 16-byte slots rotated by row
-    uint64_t *bars = (uint64_t *)((uint8_t *)xbuf + XBUF_BYTES);
+    // [row][64] partial scores, 16-byte slots of a row rotated by the row index
+    float *xbuf = (float *)(stages + ST * STAGE_BYTES);          // received from the peer
+    float *sendbuf = (float *)((uint8_t *)xbuf + XBUF_BYTES);    // this CTA's, to the peer
+    uint64_t *bars = (uint64_t *)((uint8_t *)sendbuf + XBUF_BYTES);
     uint64_t *k_full = bars, *k_empty = bars + ST, *c_full = bars + 2 * ST;
     uint64_t *q_ready = bars + 3 * ST, *s_full = q_ready + 1, *s_free = q_ready + 2, *p_full = q_ready + 3;
     uint64_t *o_done = q_ready + 4, *o_final = q_ready + 5, *x_full = q_ready + 6, *x_empty = q_ready + 7;
@@ -133,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         for (int s = 0; s < ST; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
-            mbar_init(&c_full[s], 4);
+            mbar_init(&c_full[s], 2);   // the two converter warps
         }
         mbar_init(q_ready, 4);
         mbar_init(s_full, 1);
@@ -141,10 +145,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         mbar_init(p_full, 4);
         mbar_init(o_done, 1);
         mbar_init(o_final, 1);
-        mbar_init(x_full, 128);    // one arrival per softmax thread of the peer CTA
-        mbar_init(x_empty, 128);
+        mbar_init(x_full, 1);      // local expect_tx + the peer's bulk copy
+        mbar_init(x_empty, 4);     // one arrival per softmax warp of the peer CTA
         *abort = 0;
         fence_mbar_init();
+        mbar_arrive_expect_tx(x_full, XBUF_BYTES);   // arm the first tile's receive
     }
     if (warp == 1) {
         tmem_alloc(tslot, 512);
@@ -179,13 +184,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     } else if (warp >= 6) {
         // ---------------------------------------------- bf16 -> fp16 widening of tiles
         if (CONVERT) {
-            const int ct = tid - 6 * 32;                  // 0..127
+            const int ct = tid - 6 * 32;                  // 0..63
             const int n16 = (int)(stage_tx / 16);
             for (int j = 0; j < nt; ++j) {
                 const int s = j % ST;
                 if (!mbar_wait(&k_full[s], (j / ST) & 1, abort, &g_tc_latent_err)) break;
                 uint4 *t = (uint4 *)(stages + s * STAGE_BYTES);
-                for (int i = ct; i < n16; i += 128) {
+#pragma unroll 4
+                for (int i = ct; i < n16; i += 64) {
                     uint4 v = t[i];
                     uint32_t q[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -271,42 +277,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(q_ready);
         }
-        const uint32_t peer_row = map_peer(smem_u32(xbuf) + row * 256, peer);
+        const uint32_t peer_recv = map_peer(smem_u32(xbuf), peer);
         const uint32_t peer_x_full = map_peer(smem_u32(x_full), peer);
         const uint32_t peer_x_empty = map_peer(smem_u32(x_empty), peer);
+        const bool elected = warp == 2 && lane == 0;
+        float *my_send = sendbuf + row * 64;
         const float *my_row = xbuf + row * 64;
         float m = -INFINITY, l = 0.f;
+        // A failed wait clears `ok` (warp-uniform) but never leaves the loop early: every
+        // softmax thread passes the same named barriers, so an abort cannot strand one.
         bool ok = true;
-        for (int j = 0; j < nt && ok; ++j) {
-            if (!mbar_wait(s_full, j & 1, abort, &g_tc_latent_err)) {
-                ok = false;
-                break;
-            }
+        for (int j = 0; j < nt; ++j) {
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(s_full, j & 1, abort, &g_tc_latent_err));
             tc_fence_after();
             uint32_t sr[2][32];
-            tmem_ld32(lb + T_S, sr[0]);
-            tmem_ld32(lb + T_S + 32, sr[1]);
-            tmem_ld_wait();
+            if (ok) {
+                tmem_ld32(lb + T_S, sr[0]);
+                tmem_ld32(lb + T_S + 32, sr[1]);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sr[0][e] = sr[1][e] = 0u;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            // ---- swap partial scores with the peer CTA
-            if (j > 0 && !mbar_wait_cluster(x_empty, (j - 1) & 1, abort, &g_tc_latent_err)) {
-                ok = false;
-                break;
-            }
+            // ---- swap partial scores with the peer CTA: stage, then one bulk copy
+            named_bar_sync(1, 128);   // the previous copy has finished reading the send buffer
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int slot = (c + row) & 15;
                 const uint32_t *q = &sr[c >> 3][(c & 7) * 4];
-                st_peer_v4(peer_row + slot * 16, __uint_as_float(q[0]), __uint_as_float(q[1]),
-                           __uint_as_float(q[2]), __uint_as_float(q[3]));
+                *(float4 *)(my_send + slot * 4) =
+                    make_float4(__uint_as_float(q[0]), __uint_as_float(q[1]), __uint_as_float(q[2]),
+                                __uint_as_float(q[3]));
             }
-            mbar_arrive_peer(peer_x_full);
-            if (!mbar_wait_cluster(x_full, j & 1, abort, &g_tc_latent_err)) {
-                ok = false;
-                break;
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (elected) {
+                bool go = ok;
+                if (go && j > 0) go = mbar_wait_cluster(x_empty, (j - 1) & 1, abort, &g_tc_latent_err);
+                if (go) {
+                    bulk_copy_to_peer(peer_recv, sendbuf, XBUF_BYTES, peer_x_full);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                ok = go;
             }
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_cluster(x_full, j & 1, abort, &g_tc_latent_err));
             float x[64];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -320,7 +338,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
                     x[c * 4 + e] = (rank == 0 ? mine + ov[e] : ov[e] + mine) * p.scale_log2;
                 }
             }
-            mbar_arrive_peer(peer_x_empty);
+            __syncwarp();   // every lane has read its row of the received partial
+            if (lane == 0) {
+                if (warp == 2 && j + 1 < nt) mbar_arrive_expect_tx(x_full, XBUF_BYTES);   // arm the next receive
+                mbar_arrive_peer(peer_x_empty);
+            }
             const long key0 = w.kb + (long)j * NK;
             const bool masked = key0 + NK > w.ke || (p.mode == 1 && p.causal && key0 + NK - 1 > (long)p.q_offset + w.q0);
             float mt = -INFINITY;
@@ -339,11 +361,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
                 const float m_use = need ? m_new : m;
                 const float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_use);
                 if (j > 0) {
-                    if (!mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_latent_err)) {
-                        ok = false;
-                        break;
-                    }
+                    ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_latent_err));
                     pv_done = true;
+                }
+                if (j > 0 && ok) {
                     tc_fence_after();
                     for (int c = 0; c < 8; ++c) {
                         uint32_t o[32];
@@ -367,15 +388,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
                 rs += p0 + p1;
                 pk[e] = pack_f16(p0, p1);
             }
-            if (j > 0 && !pv_done) {   // P of the previous tile must have been consumed
-                if (!mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_latent_err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            if (j > 0 && !pv_done)   // P of the previous tile must have been consumed
+                ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_latent_err));
+            tc_fence_after();
+            if (ok) {
+                tmem_st32(lb + T_P, pk);
+                tmem_st_wait();
             }
-            tmem_st32(lb + T_P, pk);
-            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
@@ -452,7 +471,7 @@ cudaError_t launch_latent_attn(const void *cache, const void *kpe, long cache_ro
     p.idesc_s0 = idesc_f16(128, NK, true);
     p.idesc_s1 = idesc_f16(128, NK, true);
     p.idesc_pv = idesc_f16(128, 256, true, true);
-    dim3 grid((unsigned)(2 * units)), block(320);
+    dim3 grid((unsigned)(2 * units)), block(256);
     ProfScope ps("tc_latent_attn", st);
     if (convert) {
         e = cudaFuncSetAttribute(tc_latent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
