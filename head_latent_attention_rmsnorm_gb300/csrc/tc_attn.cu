@@ -231,17 +231,23 @@ __global__ void __launch_bounds__(320, 1)
             const int j0 = j * BKV + hf * 64;
             const bool masked = (j0 + 64 > p.kv_need) || (p.causal && j0 + 63 > p.q_offset + q0);
             float x[64];
-            float ml = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float v = __uint_as_float(s[c >> 5][c & 31]);
-                if (masked) {
+            for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(s[c >> 5][c & 31]);
+            if (masked) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
                     const int key = j0 + c;
-                    if (key >= p.kv_need || (p.causal && key > pos)) v = -INFINITY;
+                    if (key >= p.kv_need || (p.causal && key > pos)) x[c] = -INFINITY;
                 }
-                x[c] = v;
-                ml = fmaxf(ml, v);
             }
+            // independent accumulators: the reductions are latency chains otherwise
+            float mx[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = x[a];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+            const float ml = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             // both halves have read their S columns before either writes P over them
             red[sb][hf][row] = ml;
             named_bar_sync(1, 256);
@@ -269,15 +275,16 @@ __global__ void __launch_bounds__(320, 1)
                 m = m_use;
             }
             const float nm = (m == -INFINITY) ? 0.f : -m;
-            float rs = 0.f;
+            float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float p0 = ex2(fmaf(x[2 * i], p.scale_log2, nm));
                 const float p1 = ex2(fmaf(x[2 * i + 1], p.scale_log2, nm));
-                rs += p0 + p1;
+                ra[i & 7] += p0 + p1;
                 pk[i] = pack_f16(p0, p1);
             }
+            const float rs = ((ra[0] + ra[1]) + (ra[2] + ra[3])) + ((ra[4] + ra[5]) + (ra[6] + ra[7]));
             if (ok) {
                 tmem_st32(lane_base + sb * 128 + hf * 32, pk);
                 tmem_st_wait();

@@ -345,15 +345,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             }
             const long key0 = w.kb + (long)j * NK;
             const bool masked = key0 + NK > w.ke || (p.mode == 1 && p.causal && key0 + NK - 1 > (long)p.q_offset + w.q0);
-            float mt = -INFINITY;
+            if (masked) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                if (masked) {
+                for (int c = 0; c < 64; ++c) {
                     const long key = key0 + c;
                     if (key >= w.ke || (p.mode == 1 && p.causal && key > pos)) x[c] = -INFINITY;
                 }
-                mt = fmaxf(mt, x[c]);
             }
+            // independent accumulators: the reductions are latency chains otherwise
+            float mx[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = x[a];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float m_new = fmaxf(m, mt);
             const bool need = m_new > m + RESCALE_LOG2;
             bool pv_done = false;
@@ -380,14 +386,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 m = m_use;
             }
             const float m_eff = (m == -INFINITY) ? 0.f : m;
-            float rs = 0.f;
+            float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const float p0 = ex2(x[2 * e] - m_eff), p1 = ex2(x[2 * e + 1] - m_eff);
-                rs += p0 + p1;
+                ra[e & 7] += p0 + p1;
                 pk[e] = pack_f16(p0, p1);
             }
+            const float rs = ((ra[0] + ra[1]) + (ra[2] + ra[3])) + ((ra[4] + ra[5]) + (ra[6] + ra[7]));
             if (j > 0 && !pv_done)   // P of the previous tile must have been consumed
                 ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_latent_err));
             tc_fence_after();
