@@ -145,9 +145,12 @@ PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
     const size_t es = ty_size(p.tmid);
     w.chat = c.take((size_t)p.B * p.kv_pad * p.Dk * es);
     w.kpe = c.take((size_t)p.B * p.kv_pad * p.Dr * es);
-    w.qpe = c.take((size_t)p.B * p.s_q * p.head_count * p.Dr * es);
+    // the explicit tensor-core path rotates q_pe inside its attention kernel
+    const bool fused = p.tc && !absorbed;
+    if (!fused) w.qpe = c.take((size_t)p.B * p.s_q * p.head_count * p.Dr * es);
     w.rtab = (float2 *)c.take((size_t)rope_positions(p) * (p.Dr / 2) * sizeof(float2));
-    if (p.tc) w.w16 = c.take((size_t)p.hs * (p.Dn + p.Dv) * p.Dk * 2);
+    // fp16 W_kv_b rows: all heads of the call (explicit), one shard (absorbed transposes)
+    if (p.tc) w.w16 = c.take((size_t)(fused ? p.head_count : p.hs) * (p.Dn + p.Dv) * p.Dk * 2);
     if (!absorbed) {
         // per-shard K_nope and V (tensor-core path: V stored transposed)
         w.k = c.take((size_t)p.B * p.hs * p.kv_pad * p.Dn * es);
@@ -186,8 +189,17 @@ mla_status prefill_common_checks(const Prefill &p, bool absorbed, const void *q_
 }
 
 // Common first steps of both prefill forms: normalised latent, rotated k_pe and q_pe.
-mla_status prefill_prep(const Prefill &p, const mla_dims *d, const void *q_pe, const void *c_kv, const void *k_pe,
-                        const void *rms_w, const PrefillWs &w, cudaStream_t st) {
+mla_status prefill_prep(const Prefill &p, bool absorbed, const mla_dims *d, const void *q_pe, const void *c_kv,
+                        const void *k_pe, const void *w_kv_b, const void *rms_w, const PrefillWs &w,
+                        cudaStream_t st) {
+    if (p.tc && !absorbed) {
+        // one launch: table, normalised latent, rotated k_pe and the fp16 weight copy
+        const long Dh = p.Dn + p.Dv;
+        return cuda_status(launch_prep_tc(p.B, p.s_kv, (int)p.kv_need, (int)p.kv_pad, p.Dk, rope_positions(p),
+                                          d->rope_base, c_kv, k_pe, rms_w, d->rms_eps, w.rtab, w.chat, w.kpe,
+                                          (const char *)w_kv_b + (size_t)p.head_begin * Dh * p.Dk * 2, w.w16,
+                                          (long)p.head_count * Dh * p.Dk, st));
+    }
     MLA_TRY(launch_rope_table(0, rope_positions(p), p.Dr, d->rope_base, w.rtab, st));
     MLA_TRY(launch_latent_prep(p.tin, p.tmid, p.B, p.s_kv, (int)p.kv_need, (int)p.kv_pad, p.Dk, p.Dr, c_kv, k_pe,
                                rms_w, d->rms_eps, w.rtab, w.chat, w.kpe, st));
@@ -562,7 +574,7 @@ mla_status prefill_entry(bool absorbed, const mla_dims *dims, mla_dtype dtype, i
     cudaStream_t cs = (cudaStream_t)cuda_stream;
     PrefillWs w = prefill_ws(p, absorbed, workspace);
     float scale = scale_of(dims);
-    st = prefill_prep(p, dims, q_pe, c_kv, k_pe, rms_w, w, cs);
+    st = prefill_prep(p, absorbed, dims, q_pe, c_kv, k_pe, w_kv_b, rms_w, w, cs);
     if (st != MLA_OK) return st;
     g_last_path = p.tc ? 2 : 1;
     if (p.tc) {
@@ -570,8 +582,8 @@ mla_status prefill_entry(bool absorbed, const mla_dims *dims, mla_dtype dtype, i
                     p.Dk, p.Dn, p.Dr, p.Dv, p.H, p.kv_need, scale};
         cudaError_t e = absorbed ? tc_absorbed_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.qabs,
                                                        w.olat, w.w16, cs)
-                                 : tc_explicit_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.k, w.v,
-                                                       w.w16, cs);
+                                 : tc_explicit_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, q_pe, w.rtab,
+                                                       w.k, w.v, w.w16, cs);
         return cuda_status(e);
     }
     return absorbed ? absorbed_simt(p, scale, q_nope, w_kv_b, out, lse, w, cs)

@@ -46,20 +46,123 @@ __device__ __forceinline__ float warp_max(float v) {
 // The angle is formed and reduced to [-pi, pi] in double precision (positions reach
 // 10^4..10^5, where a float angle would already be off by ~1e-3 rad); the reduced
 // angle then goes through the float sincos.  theta_t is computed once per block.
+// (cos, sin) of pos * theta: the angle reduced by the nearest multiple of 2 pi in
+// double (a multiply by 1/(2 pi) picks the multiple; an off-by-one choice only leaves
+// the angle just outside [-pi, pi]), then the float sincos.
+__device__ __forceinline__ float2 rope_cs(long pos, double theta) {
+    const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
+    const double a = (double)pos * theta;
+    const double r = fma(-rint(a * inv_two_pi), two_pi, a);
+    float s, c;
+    sincosf((float)r, &s, &c);
+    return make_float2(c, s);
+}
+
 __global__ void rope_table_kernel(long pos0, long n_pos, int half, int Dr, double base, float2 *tab) {
     __shared__ double theta[512];
     for (int t = threadIdx.x; t < half && t < 512; t += blockDim.x) theta[t] = pow(base, -2.0 * (double)t / (double)Dr);
     __syncthreads();
     long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_pos * half) return;
-    long pos = pos0 + i / half;
-    int t = (int)(i % half);
-    const double two_pi = 6.283185307179586476925286766559;
-    double a = (double)pos * theta[t];
-    a -= two_pi * rint(a / two_pi);
-    float s, c;
-    sincosf((float)a, &s, &c);
-    tab[i] = make_float2(c, s);
+    tab[i] = rope_cs(pos0 + i / half, theta[i % half]);
+}
+
+// ---------------------------------------------- fused prep (tensor-core path) ----
+constexpr int PREP_DR = 64;          // RoPE width of the fused prep: one lane per frequency
+constexpr int PREP_W_PER_LANE = 8;   // 16-byte weight chunks a lane converts per task
+
+struct PrepTc {
+    int B, s_kv, n_rows, pad_rows, Dk;
+    long n_pos;                              // table positions [0, n_pos)
+    const __nv_bfloat16 *c_kv, *k_pe, *rms_w;
+    float eps;
+    float2 *tab;
+    __half *chat, *kpe;
+    const uint4 *w_src;                      // bf16 weights, 8 per chunk
+    uint4 *w_dst;                            // their fp16 copy
+    long w_chunks;
+    long row_tasks, tab_tasks, w_tasks;      // warps of each kind, in this order
+    double theta[PREP_DR / 2];
+};
+
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *(uint32_t *)&h;
+}
+
+// One warp per task: a latent row (b, j) of [0, B*pad_rows), a table-only position of
+// [pad_rows, n_pos), or a run of 32*PREP_W_PER_LANE weight chunks.
+__global__ void prep_tc_kernel(const __grid_constant__ PrepTc a) {
+    long g = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (g < a.row_tasks) {
+        const long b = g / a.pad_rows, j = g % a.pad_rows;
+        const float2 cs = rope_cs(j, a.theta[lane]);
+        if (b == 0 && j < a.n_pos) a.tab[j * (PREP_DR / 2) + lane] = cs;
+        const int Dk = a.Dk, nc = Dk / 256;
+        uint4 *y = (uint4 *)(a.chat + g * Dk);
+        __half *kp = a.kpe + g * PREP_DR;
+        if (j >= a.n_rows) {
+            for (int c = 0; c < nc; ++c) y[c * 32 + lane] = make_uint4(0, 0, 0, 0);
+            kp[lane] = kp[lane + 32] = __float2half_rn(0.f);
+            return;
+        }
+        const uint4 *x = (const uint4 *)(a.c_kv + (b * a.s_kv + j) * Dk);
+        const uint4 *w = (const uint4 *)a.rms_w;
+        float v[4][8];
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (c < nc) {
+                uint4 q = x[c * 32 + lane];
+                const __nv_bfloat16 *e = (const __nv_bfloat16 *)&q;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[c][i] = __bfloat162float(e[i]);
+                    ss += v[c][i] * v[c][i];
+                }
+            }
+        }
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)Dk + a.eps);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (c < nc) {
+                uint4 q = w[c * 32 + lane];
+                const __nv_bfloat16 *e = (const __nv_bfloat16 *)&q;
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = f16x2(v[c][2 * i] * inv * __bfloat162float(e[2 * i]),
+                                 v[c][2 * i + 1] * inv * __bfloat162float(e[2 * i + 1]));
+                y[c * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        // half-split pairs (t, t + 32): lane t rotates both by its own frequency
+        const __nv_bfloat16 *kx = a.k_pe + (b * a.s_kv + j) * PREP_DR;
+        const float x0 = __bfloat162float(kx[lane]), x1 = __bfloat162float(kx[lane + 32]);
+        kp[lane] = __float2half_rn(x0 * cs.x - x1 * cs.y);
+        kp[lane + 32] = __float2half_rn(x1 * cs.x + x0 * cs.y);
+    } else if ((g -= a.row_tasks) < a.tab_tasks) {
+        const long pos = a.pad_rows + g;
+        a.tab[pos * (PREP_DR / 2) + lane] = rope_cs(pos, a.theta[lane]);
+    } else if ((g -= a.tab_tasks) < a.w_tasks) {
+        const long c0 = g * 32 * PREP_W_PER_LANE + lane;
+#pragma unroll
+        for (int k = 0; k < PREP_W_PER_LANE; ++k) {
+            const long c = c0 + 32 * k;
+            if (c < a.w_chunks) {
+                const uint4 q = a.w_src[c];
+                const uint32_t in[4] = {q.x, q.y, q.z, q.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)   // bf16 -> fp32 is a shift; fp32 -> fp16 rounds
+                    o[i] = f16x2(__uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xffff0000u));
+                a.w_dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
 }
 
 // Rotates one Dr-wide band (half-split pairs t, t+Dr/2) with table row `cs`.
@@ -360,6 +463,60 @@ __global__ void lse_combine_kernel(int n, long rows, int D, const float *po, con
     if (lane == 0) lse[r] = L;
 }
 
+// The same merge for n <= 32 splits and D a multiple of 128 (up to 1024): lane s owns
+// split s's weight, each lane accumulates D/128 float4 columns in registers with all
+// of them loaded as 16-byte vectors.  Same weights and the same split order as
+// lse_combine_kernel, so the results are identical.
+template <typename TO>
+__global__ void lse_combine_vec_kernel(int n, long rows, int D, const float *po, const float *pl, TO *out,
+                                       float *lse) {
+    const long r = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (r >= rows) return;
+    const int nc = D / 128;
+    const float ls = lane < n ? pl[(long)lane * rows + r] : -INFINITY;
+    const float m = warp_max(ls);
+    if (m == -INFINITY) {
+        for (int d = lane; d < D; d += 32) out[r * D + d] = TO(0.f);
+        if (lane == 0) lse[r] = -INFINITY;
+        return;
+    }
+    const float z = warp_sum(lane < n ? expf(ls - m) : 0.f);
+    const float L = m + logf(z);
+    const float w = lane < n ? expf(ls - L) : 0.f;
+    float4 acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < n; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, w, s);
+        if (ws > 0.f) {
+            const float4 *src = (const float4 *)(po + ((long)s * rows + r) * D) + lane;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < nc) {
+                    const float4 v = src[k * 32];
+                    acc[k].x = fmaf(ws, v.x, acc[k].x);
+                    acc[k].y = fmaf(ws, v.y, acc[k].y);
+                    acc[k].z = fmaf(ws, v.z, acc[k].z);
+                    acc[k].w = fmaf(ws, v.w, acc[k].w);
+                }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < nc) {
+            TO *dst = out + r * D + (k * 32 + lane) * 4;
+            if (sizeof(TO) == 4) {
+                *(float4 *)dst = acc[k];
+            } else {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+                *(uint2 *)dst = make_uint2(*(uint32_t *)&lo, *(uint32_t *)&hi);
+            }
+        }
+    if (lane == 0) lse[r] = L;
+}
+
 inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / per); }
 
 }  // namespace
@@ -402,6 +559,39 @@ cudaError_t launch_rope_rows(int tin, int tout, long rows, int Dr, const void *x
     return cudaGetLastError();
 }
 
+bool prep_tc_supported(int Dk, int Dr) { return Dr == PREP_DR && Dk % 256 == 0 && Dk > 0 && Dk <= 1024; }
+
+cudaError_t launch_prep_tc(int B, int s_kv, int n_rows, int pad_rows, int Dk, long n_pos, float base,
+                           const void *c_kv, const void *k_pe, const void *rms_w, float eps, float2 *tab, void *chat,
+                           void *kpe, const void *w_src, void *w16, long n_w, cudaStream_t st) {
+    PrepTc a;
+    a.B = B;
+    a.s_kv = s_kv;
+    a.n_rows = n_rows;
+    a.pad_rows = pad_rows;
+    a.Dk = Dk;
+    a.n_pos = n_pos;
+    a.c_kv = (const __nv_bfloat16 *)c_kv;
+    a.k_pe = (const __nv_bfloat16 *)k_pe;
+    a.rms_w = (const __nv_bfloat16 *)rms_w;
+    a.eps = eps;
+    a.tab = tab;
+    a.chat = (__half *)chat;
+    a.kpe = (__half *)kpe;
+    a.w_src = (const uint4 *)w_src;
+    a.w_dst = (uint4 *)w16;
+    a.w_chunks = n_w / 8;
+    a.row_tasks = (long)B * pad_rows;
+    a.tab_tasks = n_pos > pad_rows ? n_pos - pad_rows : 0;
+    a.w_tasks = (a.w_chunks + 32 * PREP_W_PER_LANE - 1) / (32 * PREP_W_PER_LANE);
+    for (int t = 0; t < PREP_DR / 2; ++t) a.theta[t] = pow((double)base, -2.0 * t / (double)PREP_DR);
+    const long warps = a.row_tasks + a.tab_tasks + a.w_tasks;
+    if (warps == 0) return cudaSuccess;
+    ProfScope ps("prep", st);
+    prep_tc_kernel<<<blocks_for(warps, 8), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_convert(int tin, const void *x, int tout, void *y, long n, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     ProfScope ps("convert", st);
@@ -434,7 +624,14 @@ cudaError_t launch_lse_combine(int tout, int n, long rows, int D, const float *p
                                float *lse, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
     ProfScope ps("lse_combine", st);
-    lse_combine_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, out, tout, lse);
+    const bool vec = n <= 32 && D % 128 == 0 && D <= 1024 && ((uintptr_t)po & 15) == 0;
+    if (vec && tout == TY_F32 && ((uintptr_t)out & 15) == 0)
+        lse_combine_vec_kernel<float><<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, (float *)out, lse);
+    else if (vec && tout == TY_BF16 && ((uintptr_t)out & 7) == 0)
+        lse_combine_vec_kernel<__nv_bfloat16>
+            <<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, (__nv_bfloat16 *)out, lse);
+    else
+        lse_combine_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, out, tout, lse);
     return cudaGetLastError();
 }
 

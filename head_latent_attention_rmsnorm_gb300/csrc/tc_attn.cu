@@ -41,7 +41,8 @@ using namespace tc;
 
 constexpr int BQ = 128, BKV = 128;
 constexpr uint32_t BOX = 128 * 128;            // one 128-row x 64-element fp16 box
-constexpr uint32_t Q_BYTES = 3 * BOX;          // nope lo, nope hi, rope
+constexpr uint32_t Q_BYTES = 3 * BOX;          // nope lo, nope hi (TMA), rope (rotated in place)
+constexpr uint32_t QN_BYTES = 2 * BOX;         // the part of Q the TMA brings
 constexpr uint32_t K_BYTES = 3 * BOX;
 constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halves
 constexpr int KST = 2, VST = 2;
@@ -57,6 +58,9 @@ struct AttnK {
     float *lse;
     long lse_b, lse_h;
     uint32_t idesc_s, idesc_pv;
+    const __nv_bfloat16 *q_pe;   // un-rotated q_pe [b][i][head][64]
+    long qpe_b, qpe_i;
+    const float2 *tab;           // RoPE (cos, sin) of position p, frequency t at p * 32 + t
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -66,8 +70,8 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __global__ void __launch_bounds__(320, 1)
-    tc_attn_kernel(const __grid_constant__ CUtensorMap mQn, const __grid_constant__ CUtensorMap mQr,
-                   const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
+    tc_attn_kernel(const __grid_constant__ CUtensorMap mQn, const __grid_constant__ CUtensorMap mK,
+                   const __grid_constant__ CUtensorMap mKr,
                    const __grid_constant__ CUtensorMap mV, AttnK p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -121,10 +125,9 @@ __global__ void __launch_bounds__(320, 1)
             tma_prefetch_desc(&mQn);
             tma_prefetch_desc(&mK);
             tma_prefetch_desc(&mV);
-            mbar_arrive_expect_tx(q_full, Q_BYTES);
+            mbar_arrive_expect_tx(q_full, QN_BYTES);
             tma_load_4d(sQ, &mQn, q_full, 0, hq, q0, b);
             tma_load_4d(sQ + BOX, &mQn, q_full, 64, hq, q0, b);
-            tma_load_4d(sQ + 2 * BOX, &mQr, q_full, 0, hq, q0, b);
             for (int j = 0; j < nt; ++j) {
                 const int ks = j % KST, vs = j % VST;
                 if (j >= KST && !mbar_wait(&k_empty[ks], ((j / KST) - 1) & 1, abort, &g_tc_attn_err)) break;
@@ -193,6 +196,42 @@ __global__ void __launch_bounds__(320, 1)
         const int row = quad * 32 + lane;
         const int pos = p.q_offset + q0 + row;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        // RoPE of this row's q_pe, written as fp16 into the third Q box in the TMA's
+        // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)).  Half hf
+        // rotates the pairs (t, t + 32) for t in [16 hf, 16 hf + 16): chunks 2hf, 2hf+1
+        // and their partners 2hf+4, 2hf+5.
+        {
+            const int qi = q0 + row;
+            uint4 ya[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)}, yb[2] = {ya[0], ya[0]};
+            if (qi < p.s_q) {
+                const __nv_bfloat16 *src = p.q_pe + b * p.qpe_b + (long)qi * p.qpe_i + (long)hq * 64 + hf * 16;
+                const uint4 xa[2] = {((const uint4 *)src)[0], ((const uint4 *)src)[1]};
+                const uint4 xb[2] = {((const uint4 *)(src + 32))[0], ((const uint4 *)(src + 32))[1]};
+                const float4 *cs = (const float4 *)(p.tab + (long)(p.q_offset + qi) * 32 + hf * 16);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t wa[4] = {xa[h].x, xa[h].y, xa[h].z, xa[h].w};
+                    const uint32_t wb[4] = {xb[h].x, xb[h].y, xb[h].z, xb[h].w};
+                    uint32_t oa[4], ob[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {   // elements 8h + 2k, 8h + 2k + 1 of this half
+                        const float4 r = cs[h * 4 + k];   // (cos, sin) of both elements
+                        const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
+                        const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
+                        oa[k] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
+                        ob[k] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
+                    }
+                    ya[h] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+                    yb[h] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                }
+            }
+            uint8_t *rrow = sQ + 2 * BOX + row * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                *(uint4 *)(rrow + (((2 * hf + h) ^ (row & 7)) << 4)) = ya[h];
+                *(uint4 *)(rrow + (((2 * hf + 4 + h) ^ (row & 7)) << 4)) = yb[h];
+            }
+        }
         // widen this row's half of the bf16 q_nope tile to fp16 in place
         bool ok = mbar_wait(q_full, 0, abort, &g_tc_attn_err);
         if (ok) {
@@ -206,8 +245,8 @@ __global__ void __launch_bounds__(320, 1)
                     w[i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
                 rp[c] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            fence_proxy_async_smem();
         }
+        fence_proxy_async_smem();   // the generic-proxy writes above, before the MMAs read them
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
 
@@ -339,17 +378,18 @@ __global__ void __launch_bounds__(320, 1)
 }  // namespace
 
 bool tc_explicit_supported(int Dk, int Dn, int Dr, int Dv) {
-    return Dk % 64 == 0 && Dk <= 4096 && Dn == 128 && Dr == 64 && Dv == 128;
+    return prep_tc_supported(Dk, Dr) && Dn == 128 && Dv == 128;
 }
 
 cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out, float *lse,
-                                const void *chat, const void *kpe, const void *qpe, void *kws, void *vws,
-                                void *w16, cudaStream_t st) {
+                                const void *chat, const void *kpe, const void *q_pe, const float2 *rtab, void *kws,
+                                void *vws, const void *w16, cudaStream_t st) {
+    (void)w_kv_b;   // read through its fp16 copy w16
     const long kv_pad = (p.kv_need + 127) / 128 * 128;
     const long Dh = p.Dn + p.Dv;
     cudaError_t e;
     // maps that do not change across shards
-    CUtensorMap mQn, mQr, mKr;
+    CUtensorMap mQn, mKr;
     {
         unsigned long long d[4] = {(unsigned long long)p.Dn, (unsigned long long)p.head_count,
                                    (unsigned long long)p.s_q, (unsigned long long)p.B};
@@ -357,14 +397,6 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
                                    (unsigned long long)p.s_q * p.head_count * p.Dn * 2};
         unsigned box[4] = {64, 1, 128, 1};
         if ((e = make_tma_map(&mQn, q_nope, 4, d, s, box)) != cudaSuccess) return e;
-    }
-    {
-        unsigned long long d[4] = {(unsigned long long)p.Dr, (unsigned long long)p.head_count,
-                                   (unsigned long long)p.s_q, (unsigned long long)p.B};
-        unsigned long long s[3] = {(unsigned long long)p.Dr * 2, (unsigned long long)p.head_count * p.Dr * 2,
-                                   (unsigned long long)p.s_q * p.head_count * p.Dr * 2};
-        unsigned box[4] = {64, 1, 128, 1};
-        if ((e = make_tma_map(&mQr, qpe, 4, d, s, box)) != cudaSuccess) return e;
     }
     {
         unsigned long long d[3] = {(unsigned long long)p.Dr, (unsigned long long)kv_pad, (unsigned long long)p.B};
@@ -405,22 +437,24 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
     a.lse_h = p.s_q;
     a.idesc_s = idesc_f16(128, 128, true);
     a.idesc_pv = idesc_f16(128, 128, true);
+    a.q_pe = (const __nv_bfloat16 *)q_pe;
+    a.qpe_i = (long)p.head_count * p.Dr;
+    a.qpe_b = (long)p.s_q * a.qpe_i;
+    a.tab = rtab;
 
     TmaOperand latent{chat, p.Dk, kv_pad, p.B, (long)p.Dk * 2, kv_pad * p.Dk * 2, (int)kv_pad, 0, 1};
     for (int s = 0; s < p.n_shards; ++s) {
         const int h0 = s * p.hs;
         const int nh = std::min(p.hs, p.head_count - h0);
-        const long hg = p.head_begin + h0;
-        // fp16 copy of this shard's W_kv_b rows: [nh][Dn+Dv][Dk]
-        e = launch_convert(1, (const char *)w_kv_b + hg * Dh * p.Dk * 2, 0, w16, (long)nh * Dh * p.Dk, st);
-        if (e != cudaSuccess) return e;
-        // K_nope[b][j][hl*Dn + d] = chat[b][j] . W_K(hg+hl)[d]
-        TmaOperand wk{w16, p.Dk, p.Dn, nh, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dn, 0, 0};
+        // this shard's rows of the fp16 W_kv_b copy: [nh][Dn+Dv][Dk]
+        const char *ws = (const char *)w16 + (long)h0 * Dh * p.Dk * 2;
+        // K_nope[b][j][hl*Dn + d] = chat[b][j] . W_K(head_begin+h0+hl)[d]
+        TmaOperand wk{ws, p.Dk, p.Dn, nh, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dn, 0, 0};
         e = tc_gemm(latent, wk, (int)kv_pad, nh * p.Dn, p.Dk, p.B, true, kws, (long)p.hs * p.Dn, 1,
                     kv_pad * p.hs * p.Dn, 0, st);
         if (e != cudaSuccess) return e;
-        // V^T[b][hl*Dv + d][j] = W_V(hg+hl)[d] . chat[b][j]
-        TmaOperand wv{(const char *)w16 + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, nh, (long)p.Dk * 2, Dh * p.Dk * 2,
+        // V^T[b][hl*Dv + d][j] = W_V(head_begin+h0+hl)[d] . chat[b][j]
+        TmaOperand wv{ws + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, nh, (long)p.Dk * 2, Dh * p.Dk * 2,
                       p.Dv, 0, 0};
         e = tc_gemm(wv, latent, nh * p.Dv, (int)kv_pad, p.Dk, p.B, true, vws, kv_pad, 1,
                     (long)p.hs * p.Dv * kv_pad, 0, st);
@@ -429,7 +463,7 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
         dim3 grid((p.s_q + BQ - 1) / BQ, nh, p.B), block(320);
         {
             ProfScope ps("tc_attn", st);
-            tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mQn, mQr, mK, mKr, mV, a);
+            tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mQn, mK, mKr, mV, a);
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

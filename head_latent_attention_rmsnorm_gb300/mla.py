@@ -151,7 +151,7 @@ def set_path_override(mode: int) -> None:
     lib().mla_set_path_override(mode)
 
 
-KERNELS = ("latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
+KERNELS = ("prep", "latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
            "tc_gemm", "tc_attn", "tc_latent_attn", "transpose")
 
 

@@ -205,7 +205,7 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   kernel name; mla_profile_enable(0) stops recording and drops what was recorded.
  * mla_profile_kernel: synchronises the recorded events of kernel `name` and returns
  *   the number of launches and their summed device time in milliseconds (0 launches
- *   for an unknown name).  Names: "latent_prep", "rope_table", "rope_rows",
+ *   for an unknown name).  Names: "prep", "latent_prep", "rope_table", "rope_rows",
  *   "convert", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
  *   "tc_latent_attn", "transpose".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
