@@ -8,19 +8,22 @@
 //   s_ij = scale * (q_nope_i . K_nope_j + RoPE(q_pe_i) . RoPE(k_pe_j)),
 // softmax over visible keys (j <= q_offset + i), output plus log-sum-exp.
 //
-// Kernel: one CTA per (128-query tile, head, batch), 192 threads.
-//   warp 0    TMA producer: Q tile once; K tiles (K_nope 128 + RoPE band 64 dims)
-//             and V^T tiles through two 2-deep rings.
-//   warp 1    tcgen05 issuer: S_j = Q K_j^T (M=128, N=128, K=192) into one of two
-//             TMEM S buffers; O += P_{j-1} V_{j-1} (M=128, N=128, K=128) with P read
-//             from TMEM where the softmax wrote it over S_{j-1}.
-//   warps 2-9 softmax, two threads per query row (TMEM lane = row; keys 0-63 and
-//             64-127 of each tile): online softmax
-//             in the log2 domain; O in TMEM is rescaled only when a row maximum
-//             grows by more than 2^8 (the stale maximum keeps every p <= 256, exact
-//             after the final division); epilogue O / l and lse.
-// Operands are fp16 (11-bit significand): q_nope arrives as bf16 and is widened in
-// shared memory; K_nope, V^T and the rotated RoPE bands are produced in fp16.
+// Kernel: one CTA per (128-query tile, head, batch), 352 threads.
+//   warp 0    TMA producer of K tiles (K_nope 128 + RoPE band 64 dims), 3-deep ring.
+//   warp 10   TMA producer of V^T tiles, 2-deep ring (separate, so that a wait for a
+//             free V slot never holds back the next K tile).
+//   warp 1    tcgen05 issuer: S_j = Q K_j^T (M=128, N=128, K=192, Q from TMEM) into
+//             one of two TMEM S buffers; O += P_j V_j (M=128, N=128, K=128) with P read
+//             from TMEM where the softmax wrote it over S_j.  S_{j+1} is issued as soon
+//             as P.V_{j-1} has been issued.
+//   warps 2-9 first load this row's Q (bf16 q_nope widened to fp16, q_pe rotated by
+//             RoPE) straight into TMEM; then softmax, two threads per query row (TMEM
+//             lane = row; keys 0-63 and 64-127 of each tile): online softmax in the log2
+//             domain; O in TMEM is rescaled only when a row maximum grows by more than
+//             2^8 (the stale maximum keeps every p <= 256, exact after the final
+//             division); epilogue O / l and lse.
+// Operands are fp16 (11-bit significand); K_nope, V^T and the rotated k_pe band are
+// produced in fp16 by the reconstruction GEMMs and the prep launch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,12 +44,12 @@ using namespace tc;
 
 constexpr int BQ = 128, BKV = 128;
 constexpr uint32_t BOX = 128 * 128;            // one 128-row x 64-element fp16 box
-constexpr uint32_t Q_BYTES = 3 * BOX;          // nope lo, nope hi (TMA), rope (rotated in place)
-constexpr uint32_t QN_BYTES = 2 * BOX;         // the part of Q the TMA brings
-constexpr uint32_t K_BYTES = 3 * BOX;
+constexpr uint32_t K_BYTES = 3 * BOX;          // K_nope lo, K_nope hi, RoPE band
 constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halves
-constexpr int KST = 2, VST = 2;
-constexpr uint32_t SMEM_BYTES = Q_BYTES + KST * K_BYTES + VST * V_BYTES + 1024 + 256 + 4 * 2 * 2 * BQ;
+constexpr int KST = 3, VST = 2;
+constexpr uint32_t SMEM_BYTES = KST * K_BYTES + VST * V_BYTES + 1024 + 256 + 4 * 2 * 2 * BQ;
+// TMEM columns: S buffers 0-127 and 128-255, O 256-383, Q (192 fp16 = 96 columns) 384-479
+constexpr uint32_t T_O = 256, T_Q = 384;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct AttnK {
@@ -58,9 +61,11 @@ struct AttnK {
     float *lse;
     long lse_b, lse_h;
     uint32_t idesc_s, idesc_pv;
-    const __nv_bfloat16 *q_pe;   // un-rotated q_pe [b][i][head][64]
-    long qpe_b, qpe_i;
-    const float2 *tab;           // RoPE (cos, sin) of position p, frequency t at p * 32 + t
+    const __nv_bfloat16 *q_nope;   // [b][i][head][128]
+    const __nv_bfloat16 *q_pe;     // un-rotated q_pe [b][i][head][64]
+    int n_hq;                      // heads of the q tensors
+    int nh;                        // heads of this launch (grid x = nh * batch)
+    const float2 *tab;             // RoPE (cos, sin) of position p, frequency t at p * 32 + t
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -69,40 +74,44 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(320, 1)
-    tc_attn_kernel(const __grid_constant__ CUtensorMap mQn, const __grid_constant__ CUtensorMap mK,
-                   const __grid_constant__ CUtensorMap mKr,
+__global__ void __launch_bounds__(352, 1)
+    tc_attn_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
                    const __grid_constant__ CUtensorMap mV, AttnK p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sQ = smem;
-    uint8_t *sK = sQ + Q_BYTES;
+    uint8_t *sK = smem;
     uint8_t *sV = sK + KST * K_BYTES;
     uint64_t *bars = (uint64_t *)(sV + VST * V_BYTES);
-    uint64_t *q_full = bars + 0, *q_ready = bars + 1;
-    uint64_t *k_full = bars + 2, *k_empty = bars + 4;
-    uint64_t *v_full = bars + 6, *v_empty = bars + 8;
-    uint64_t *s_full = bars + 10, *p_full = bars + 12;
-    uint64_t *o_done = bars + 14, *o_final = bars + 15;
-    uint32_t *tslot = (uint32_t *)(bars + 16);
-    float (*red)[2][BQ] = (float (*)[2][BQ])(bars + 24);   // [tile parity][half][row] partial maxima
+    uint64_t *q_ready = bars + 0;
+    uint64_t *k_full = bars + 1, *k_empty = k_full + KST;
+    uint64_t *v_full = k_empty + KST, *v_empty = v_full + VST;
+    uint64_t *s_full = v_empty + VST, *p_full = s_full + 2;
+    uint64_t *o_done = p_full + 2, *o_final = o_done + 1;
+    uint32_t *tslot = (uint32_t *)(bars + 24);
+    float (*red)[2][BQ] = (float (*)[2][BQ])(bars + 32);   // [tile parity][half][row] partial maxima
     volatile int *abort = (volatile int *)(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qt = gridDim.x - 1 - blockIdx.x;   // heaviest (latest) query tiles first
-    const int q0 = qt * BQ, hl = blockIdx.y, b = blockIdx.z;
+    // x: (head, batch) pairs, y: query tiles from the latest (heaviest under the causal
+    // mask) down, so that the first waves take the heaviest tiles of every head
+    const int qt = gridDim.y - 1 - blockIdx.y;
+    const int hl = blockIdx.x % p.nh, b = blockIdx.x / p.nh;
+    const int q0 = qt * BQ;
     const int hq = p.head_off + hl;
     const int kv_end = p.causal ? min(p.kv_need, p.q_offset + q0 + BQ) : p.kv_need;
     const int nt = (kv_end + BKV - 1) / BKV;
 
     if (tid == 0) {
-        mbar_init(q_full, 1);
         mbar_init(q_ready, 8);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KST; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < VST; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 8);
         }
@@ -118,24 +127,29 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tslot;   // S0: cols 0-127, S1: 128-255, O: 256-383
+    const uint32_t tmem = *tslot;   // S0: cols 0-127, S1: 128-255, O: 256-383, Q: 384-479
 
     if (warp == 0) {
+        // ------------------------------------------------------- K tiles (TMA)
         if (lane == 0) {
-            tma_prefetch_desc(&mQn);
             tma_prefetch_desc(&mK);
-            tma_prefetch_desc(&mV);
-            mbar_arrive_expect_tx(q_full, QN_BYTES);
-            tma_load_4d(sQ, &mQn, q_full, 0, hq, q0, b);
-            tma_load_4d(sQ + BOX, &mQn, q_full, 64, hq, q0, b);
+            tma_prefetch_desc(&mKr);
             for (int j = 0; j < nt; ++j) {
-                const int ks = j % KST, vs = j % VST;
+                const int ks = j % KST;
                 if (j >= KST && !mbar_wait(&k_empty[ks], ((j / KST) - 1) & 1, abort, &g_tc_attn_err)) break;
                 uint8_t *kd = sK + ks * K_BYTES;
                 mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
                 tma_load_3d(kd, &mK, &k_full[ks], hl * 128, j * BKV, b);
                 tma_load_3d(kd + BOX, &mK, &k_full[ks], hl * 128 + 64, j * BKV, b);
                 tma_load_3d(kd + 2 * BOX, &mKr, &k_full[ks], 0, j * BKV, b);
+            }
+        }
+    } else if (warp == 10) {
+        // ----------------------------------------------------- V^T tiles (TMA)
+        if (lane == 0) {
+            tma_prefetch_desc(&mV);
+            for (int j = 0; j < nt; ++j) {
+                const int vs = j % VST;
                 if (j >= VST && !mbar_wait(&v_empty[vs], ((j / VST) - 1) & 1, abort, &g_tc_attn_err)) break;
                 uint8_t *vd = sV + vs * V_BYTES;
                 mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
@@ -144,47 +158,51 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait(q_ready, 0, abort, &g_tc_attn_err);
-            const uint32_t o_tm = tmem + 256;
+            auto issue_s = [&](int t) -> bool {
+                const int ks = t % KST;
+                if (!mbar_wait(&k_full[ks], (t / KST) & 1, abort, &g_tc_attn_err)) return false;
+                tc_fence_after();
+                const uint32_t s_tm = tmem + (t & 1) * 128;
+                const uint8_t *kd = sK + ks * K_BYTES;
+#pragma unroll
+                for (int kb = 0; kb < 3; ++kb) {
+                    const uint64_t db = sdesc_kmajor(kd + kb * BOX);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ts(s_tm, tmem + T_Q + (kb * 4 + k) * 8, db + 2 * k, p.idesc_s, (kb | k) != 0);
+                }
+                mma_commit(&s_full[t & 1]);
+                mma_commit(&k_empty[ks]);
+                return true;
+            };
             auto issue_pv = [&](int t) -> bool {
-                const int sb = t & 1, vs = t % VST;
-                if (!mbar_wait(&p_full[sb], (t >> 1) & 1, abort, &g_tc_attn_err)) return false;
+                const int vs = t % VST;
+                if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort, &g_tc_attn_err)) return false;
                 if (!mbar_wait(&v_full[vs], (t / VST) & 1, abort, &g_tc_attn_err)) return false;
                 tc_fence_after();
-                const uint32_t p_tm = tmem + sb * 128;
+                const uint32_t p_tm = tmem + (t & 1) * 128;
                 const uint8_t *vd = sV + vs * V_BYTES;
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     const uint64_t db = sdesc_kmajor(vd + kb * BOX);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ts(o_tm, p_tm + kb * 32 + k * 8, db + 2 * k, p.idesc_pv, (t | kb | k) != 0);
+                        mma_ts(tmem + T_O, p_tm + kb * 32 + k * 8, db + 2 * k, p.idesc_pv, (t | kb | k) != 0);
                 }
                 mma_commit(&v_empty[vs]);
                 mma_commit(o_done);
                 return true;
             };
+            // S_{j+1} goes into the buffer P_{j-1} occupied: it follows P.V_{j-1} in issue
+            // order, so the tensor pipe reads P_{j-1} before overwriting it.
+            if (ok && nt > 0) ok = issue_s(0);
             for (int j = 0; j < nt && ok; ++j) {
-                const int ks = j % KST, sb = j & 1;
-                if (!mbar_wait(&k_full[ks], (j / KST) & 1, abort, &g_tc_attn_err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t s_tm = tmem + sb * 128;
-                const uint8_t *kd = sK + ks * K_BYTES;
-#pragma unroll
-                for (int kb = 0; kb < 3; ++kb) {
-                    const uint64_t da = sdesc_kmajor(sQ + kb * BOX), db = sdesc_kmajor(kd + kb * BOX);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) mma_ss(s_tm, da + 2 * k, db + 2 * k, p.idesc_s, (kb | k) != 0);
-                }
-                mma_commit(&s_full[sb]);
-                mma_commit(&k_empty[ks]);
-                if (j >= 1 && !issue_pv(j - 1)) ok = false;
+                if (j + 1 < nt && !issue_s(j + 1)) ok = false;
+                if (ok && !issue_pv(j)) ok = false;
             }
-            if (ok && nt >= 1) issue_pv(nt - 1);
             mma_commit(o_final);
         }
     } else {
@@ -196,59 +214,55 @@ __global__ void __launch_bounds__(320, 1)
         const int row = quad * 32 + lane;
         const int pos = p.q_offset + q0 + row;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        // RoPE of this row's q_pe, written as fp16 into the third Q box in the TMA's
-        // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)).  Half hf
-        // rotates the pairs (t, t + 32) for t in [16 hf, 16 hf + 16): chunks 2hf, 2hf+1
-        // and their partners 2hf+4, 2hf+5.
+        // ---- this row's Q into TMEM: half hf widens q_nope dims [64 hf, 64 hf + 64) to
+        // fp16 (columns 32 hf ...), and rotates the RoPE pairs (t, t + 32) for t in
+        // [16 hf, 16 hf + 16) (q dims 128 + t and 160 + t: columns 64 + 8 hf ... and
+        // 80 + 8 hf ...).  Rows past s_q get zeros.
         {
             const int qi = q0 + row;
-            uint4 ya[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)}, yb[2] = {ya[0], ya[0]};
+            uint32_t qn[32], ra8[8], rb8[8];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) qn[e] = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ra8[e] = rb8[e] = 0u;
             if (qi < p.s_q) {
-                const __nv_bfloat16 *src = p.q_pe + b * p.qpe_b + (long)qi * p.qpe_i + (long)hq * 64 + hf * 16;
-                const uint4 xa[2] = {((const uint4 *)src)[0], ((const uint4 *)src)[1]};
-                const uint4 xb[2] = {((const uint4 *)(src + 32))[0], ((const uint4 *)(src + 32))[1]};
+                const long qrow = ((long)b * p.s_q + qi) * p.n_hq + hq;
+                const uint4 *src = (const uint4 *)(p.q_nope + qrow * 128 + hf * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = src[c];
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        qn[4 * c + i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+                }
+                const __nv_bfloat16 *pe = p.q_pe + qrow * 64 + hf * 16;
+                const uint4 xa[2] = {((const uint4 *)pe)[0], ((const uint4 *)pe)[1]};
+                const uint4 xb[2] = {((const uint4 *)(pe + 32))[0], ((const uint4 *)(pe + 32))[1]};
                 const float4 *cs = (const float4 *)(p.tab + (long)(p.q_offset + qi) * 32 + hf * 16);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t wa[4] = {xa[h].x, xa[h].y, xa[h].z, xa[h].w};
                     const uint32_t wb[4] = {xb[h].x, xb[h].y, xb[h].z, xb[h].w};
-                    uint32_t oa[4], ob[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {   // elements 8h + 2k, 8h + 2k + 1 of this half
                         const float4 r = cs[h * 4 + k];   // (cos, sin) of both elements
                         const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
                         const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
-                        oa[k] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
-                        ob[k] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
+                        ra8[4 * h + k] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
+                        rb8[4 * h + k] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
                     }
-                    ya[h] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-                    yb[h] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
                 }
             }
-            uint8_t *rrow = sQ + 2 * BOX + row * 128;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                *(uint4 *)(rrow + (((2 * hf + h) ^ (row & 7)) << 4)) = ya[h];
-                *(uint4 *)(rrow + (((2 * hf + 4 + h) ^ (row & 7)) << 4)) = yb[h];
-            }
+            tmem_st32(lane_base + T_Q + hf * 32, qn);
+            tmem_st8(lane_base + T_Q + 64 + hf * 8, ra8);
+            tmem_st8(lane_base + T_Q + 80 + hf * 8, rb8);
+            tmem_st_wait();
         }
-        // widen this row's half of the bf16 q_nope tile to fp16 in place
-        bool ok = mbar_wait(q_full, 0, abort, &g_tc_attn_err);
-        if (ok) {
-            uint4 *rp = (uint4 *)(sQ + hf * BOX + row * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 v = rp[c];
-                uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w[i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-                rp[c] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-        fence_proxy_async_smem();   // the generic-proxy writes above, before the MMAs read them
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
+        bool ok = true;
 
         // A failed wait clears `ok` (warp-uniform) but never leaves the loop early: every
         // softmax thread passes the same named barriers, so an abort cannot strand one.
@@ -302,11 +316,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(lane_base + 256 + hf * 64 + c * 32, o);
+                        tmem_ld32(lane_base + T_O + hf * 64 + c * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(lane_base + 256 + hf * 64 + c * 32, o);
+                        tmem_st32(lane_base + T_O + hf * 64 + c * 32, o);
                     }
                     tmem_st_wait();
                 }
@@ -343,8 +357,8 @@ __global__ void __launch_bounds__(320, 1)
         const float inv = l > 0.f ? 1.f / l : 0.f;
         uint32_t o[2][32];
         if (nt > 0) {
-            tmem_ld32(lane_base + 256 + hf * 64, o[0]);
-            tmem_ld32(lane_base + 256 + hf * 64 + 32, o[1]);
+            tmem_ld32(lane_base + T_O + hf * 64, o[0]);
+            tmem_ld32(lane_base + T_O + hf * 64 + 32, o[1]);
             tmem_ld_wait();
         } else {
 #pragma unroll
@@ -389,15 +403,7 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
     const long Dh = p.Dn + p.Dv;
     cudaError_t e;
     // maps that do not change across shards
-    CUtensorMap mQn, mKr;
-    {
-        unsigned long long d[4] = {(unsigned long long)p.Dn, (unsigned long long)p.head_count,
-                                   (unsigned long long)p.s_q, (unsigned long long)p.B};
-        unsigned long long s[3] = {(unsigned long long)p.Dn * 2, (unsigned long long)p.head_count * p.Dn * 2,
-                                   (unsigned long long)p.s_q * p.head_count * p.Dn * 2};
-        unsigned box[4] = {64, 1, 128, 1};
-        if ((e = make_tma_map(&mQn, q_nope, 4, d, s, box)) != cudaSuccess) return e;
-    }
+    CUtensorMap mKr;
     {
         unsigned long long d[3] = {(unsigned long long)p.Dr, (unsigned long long)kv_pad, (unsigned long long)p.B};
         unsigned long long s[2] = {(unsigned long long)p.Dr * 2, (unsigned long long)kv_pad * p.Dr * 2};
@@ -437,9 +443,9 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
     a.lse_h = p.s_q;
     a.idesc_s = idesc_f16(128, 128, true);
     a.idesc_pv = idesc_f16(128, 128, true);
+    a.q_nope = (const __nv_bfloat16 *)q_nope;
     a.q_pe = (const __nv_bfloat16 *)q_pe;
-    a.qpe_i = (long)p.head_count * p.Dr;
-    a.qpe_b = (long)p.s_q * a.qpe_i;
+    a.n_hq = p.head_count;
     a.tab = rtab;
 
     TmaOperand latent{chat, p.Dk, kv_pad, p.B, (long)p.Dk * 2, kv_pad * p.Dk * 2, (int)kv_pad, 0, 1};
@@ -460,10 +466,11 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
                     (long)p.hs * p.Dv * kv_pad, 0, st);
         if (e != cudaSuccess) return e;
         a.head_off = h0;
-        dim3 grid((p.s_q + BQ - 1) / BQ, nh, p.B), block(320);
+        a.nh = nh;
+        dim3 grid(nh * p.B, (p.s_q + BQ - 1) / BQ), block(352);
         {
             ProfScope ps("tc_attn", st);
-            tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mQn, mK, mKr, mV, a);
+            tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mK, mKr, mV, a);
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

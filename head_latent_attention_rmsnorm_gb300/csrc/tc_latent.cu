@@ -61,7 +61,7 @@ struct LatK {
     int mode;           // 0: decode (partials out), 1: absorbed prefill (o_lat out)
     int n_splits, row_tiles;
     long chunk, kv_len; // decode: keys per split, cache length
-    int s_q, q_offset, kv_need, causal, n_qtiles, nh, head_off;   // prefill
+    int s_q, q_offset, kv_need, causal, n_qtiles, nh, nb, head_off;   // prefill
     const __half *qa;   // q_abs rows (fp16, 512 wide)
     long qa_b, qa_h, qa_r;
     const __half *qp;   // rotated q_pe rows (fp16, 64 wide)
@@ -100,10 +100,12 @@ __device__ __forceinline__ Unit unit_of(const LatK &p, int u) {
         w.ke = w.kb + p.chunk < p.kv_len ? w.kb + p.chunk : p.kv_len;
         if (w.kb > p.kv_len) w.kb = p.kv_len;
     } else {
-        const int qt = p.n_qtiles - 1 - (u % p.n_qtiles);   // heaviest query tiles first
-        u /= p.n_qtiles;
-        w.hl = u % p.nh;
-        w.b = u / p.nh;
+        // (head, batch) pairs fastest, query tiles from the latest (heaviest under the
+        // causal mask) down: the first waves take the heaviest tiles of every head
+        const int hb = u % (p.nh * p.nb);
+        const int qt = p.n_qtiles - 1 - u / (p.nh * p.nb);
+        w.hl = hb % p.nh;
+        w.b = hb / p.nh;
         w.q0 = qt * ROWS;
         w.kb = 0;
         w.ke = p.causal ? min((long)p.kv_need, (long)p.q_offset + w.q0 + ROWS) : (long)p.kv_need;
@@ -636,6 +638,7 @@ cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const vo
         k.causal = p.causal;
         k.n_qtiles = (p.s_q + ROWS - 1) / ROWS;
         k.nh = nh;
+        k.nb = p.B;
         k.head_off = h0;
         k.qa = (const __half *)qabs;
         k.qa_b = (long)p.s_q * p.hs * p.Dk;
