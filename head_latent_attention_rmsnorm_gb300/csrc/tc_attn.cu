@@ -8,14 +8,17 @@
 //   s_ij = scale * (q_nope_i . K_nope_j + RoPE(q_pe_i) . RoPE(k_pe_j)),
 // softmax over visible keys (j <= q_offset + i), output plus log-sum-exp.
 //
-// Kernel: one CTA per (128-query tile, head, batch), 352 threads.
+// Kernel: one CTA per (128-query tile, head, batch), 384 threads.
 //   warp 0    TMA producer of K tiles (K_nope 128 + RoPE band 64 dims), 3-deep ring.
 //   warp 10   TMA producer of V^T tiles, 2-deep ring (separate, so that a wait for a
 //             free V slot never holds back the next K tile).
-//   warp 1    tcgen05 issuer: S_j = Q K_j^T (M=128, N=128, K=192, Q from TMEM) into
-//             one of two TMEM S buffers; O += P_j V_j (M=128, N=128, K=128) with P read
-//             from TMEM where the softmax wrote it over S_j.  S_{j+1} is issued as soon
-//             as P.V_{j-1} has been issued.
+//   warp 1    tcgen05 issuer of the scores: S_j = Q K_j^T (M=128, N=128, K=192, Q from
+//             TMEM) into TMEM S buffer j & 1, as soon as K_j has landed and P.V_{j-2}
+//             (which read that buffer) is done.  Also owns the TMEM allocation.
+//   warp 11   tcgen05 issuer of O += P_j V_j (M=128, N=128, K=128), P read from TMEM
+//             where the softmax wrote it over S_j.  Two issuing threads keep the tensor
+//             pipe fed: a thread that waits on an mbarrier between MMA batches leaves
+//             the pipe idle for ~100-200 cycles, so neither issuer waits on the other.
 //   warps 2-9 first load this row's Q (bf16 q_nope widened to fp16, q_pe rotated by
 //             RoPE) straight into TMEM; then softmax, two threads per query row (TMEM
 //             lane = row; keys 0-63 and 64-127 of each tile): online softmax in the log2
@@ -74,7 +77,7 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     tc_attn_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
                    const __grid_constant__ CUtensorMap mV, AttnK p) {
     extern __shared__ uint8_t smem_raw[];
@@ -85,8 +88,8 @@ __global__ void __launch_bounds__(352, 1)
     uint64_t *q_ready = bars + 0;
     uint64_t *k_full = bars + 1, *k_empty = k_full + KST;
     uint64_t *v_full = k_empty + KST, *v_empty = v_full + VST;
-    uint64_t *s_full = v_empty + VST, *p_full = s_full + 2;
-    uint64_t *o_done = p_full + 2, *o_final = o_done + 1;
+    uint64_t *s_full = v_empty + VST, *p_full = s_full + 2, *pv_done = p_full + 2;
+    uint64_t *o_done = pv_done + 2, *o_final = o_done + 1;
     uint32_t *tslot = (uint32_t *)(bars + 24);
     float (*red)[2][BQ] = (float (*)[2][BQ])(bars + 32);   // [tile parity][half][row] partial maxima
     volatile int *abort = (volatile int *)(tslot + 1);
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(352, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 8);
+            mbar_init(&pv_done[i], 1);
         }
         mbar_init(o_done, 1);
         mbar_init(o_final, 1);
@@ -158,12 +162,14 @@ __global__ void __launch_bounds__(352, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------- score MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait(q_ready, 0, abort, &g_tc_attn_err);
-            auto issue_s = [&](int t) -> bool {
+            for (int t = 0; t < nt && ok; ++t) {
                 const int ks = t % KST;
-                if (!mbar_wait(&k_full[ks], (t / KST) & 1, abort, &g_tc_attn_err)) return false;
+                // S buffer t & 1 last held P_{t-2}: P.V_{t-2} must have read it
+                if (t >= 2 && !mbar_wait(&pv_done[t & 1], ((t - 2) >> 1) & 1, abort, &g_tc_attn_err)) break;
+                if (!mbar_wait(&k_full[ks], (t / KST) & 1, abort, &g_tc_attn_err)) break;
                 tc_fence_after();
                 const uint32_t s_tm = tmem + (t & 1) * 128;
                 const uint8_t *kd = sK + ks * K_BYTES;
@@ -176,12 +182,15 @@ __global__ void __launch_bounds__(352, 1)
                 }
                 mma_commit(&s_full[t & 1]);
                 mma_commit(&k_empty[ks]);
-                return true;
-            };
-            auto issue_pv = [&](int t) -> bool {
+            }
+        }
+    } else if (warp == 11) {
+        // ------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            for (int t = 0; t < nt; ++t) {
                 const int vs = t % VST;
-                if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort, &g_tc_attn_err)) return false;
-                if (!mbar_wait(&v_full[vs], (t / VST) & 1, abort, &g_tc_attn_err)) return false;
+                if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort, &g_tc_attn_err)) break;
+                if (!mbar_wait(&v_full[vs], (t / VST) & 1, abort, &g_tc_attn_err)) break;
                 tc_fence_after();
                 const uint32_t p_tm = tmem + (t & 1) * 128;
                 const uint8_t *vd = sV + vs * V_BYTES;
@@ -193,15 +202,8 @@ __global__ void __launch_bounds__(352, 1)
                         mma_ts(tmem + T_O, p_tm + kb * 32 + k * 8, db + 2 * k, p.idesc_pv, (t | kb | k) != 0);
                 }
                 mma_commit(&v_empty[vs]);
+                mma_commit(&pv_done[t & 1]);
                 mma_commit(o_done);
-                return true;
-            };
-            // S_{j+1} goes into the buffer P_{j-1} occupied: it follows P.V_{j-1} in issue
-            // order, so the tensor pipe reads P_{j-1} before overwriting it.
-            if (ok && nt > 0) ok = issue_s(0);
-            for (int j = 0; j < nt && ok; ++j) {
-                if (j + 1 < nt && !issue_s(j + 1)) ok = false;
-                if (ok && !issue_pv(j)) ok = false;
             }
             mma_commit(o_final);
         }
@@ -467,7 +469,7 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
         if (e != cudaSuccess) return e;
         a.head_off = h0;
         a.nh = nh;
-        dim3 grid(nh * p.B, (p.s_q + BQ - 1) / BQ), block(352);
+        dim3 grid(nh * p.B, (p.s_q + BQ - 1) / BQ), block(384);
         {
             ProfScope ps("tc_attn", st);
             tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mK, mKr, mV, a);
@@ -493,3 +495,4 @@ cudaError_t tc_attn_read_and_clear_error(unsigned *flags, cudaStream_t st) {
 }
 
 }  // namespace mla
+
