@@ -458,15 +458,14 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
         const char *ws = (const char *)w16 + (long)h0 * Dh * p.Dk * 2;
         // K_nope[b][j][hl*Dn + d] = chat[b][j] . W_K(head_begin+h0+hl)[d]
         TmaOperand wk{ws, p.Dk, p.Dn, nh, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dn, 0, 0};
-        e = tc_gemm(latent, wk, (int)kv_pad, nh * p.Dn, p.Dk, p.B, true, kws, (long)p.hs * p.Dn, 1,
-                    kv_pad * p.hs * p.Dn, 0, st);
-        if (e != cudaSuccess) return e;
         // V^T[b][hl*Dv + d][j] = W_V(head_begin+h0+hl)[d] . chat[b][j]
         TmaOperand wv{ws + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, nh, (long)p.Dk * 2, Dh * p.Dk * 2,
                       p.Dv, 0, 0};
-        e = tc_gemm(wv, latent, nh * p.Dv, (int)kv_pad, p.Dk, p.B, true, vws, kv_pad, 1,
-                    (long)p.hs * p.Dv * kv_pad, 0, st);
-        if (e != cudaSuccess) return e;
+        // both products in one persistent launch
+        const GemmProblem kv[2] = {
+            {latent, wk, (int)kv_pad, nh * p.Dn, p.Dk, p.B, kws, (long)p.hs * p.Dn, 1, kv_pad * p.hs * p.Dn, 0},
+            {wv, latent, nh * p.Dv, (int)kv_pad, p.Dk, p.B, vws, kv_pad, 1, (long)p.hs * p.Dv * kv_pad, 0}};
+        if ((e = tc_gemm_group(kv, 2, true, st)) != cudaSuccess) return e;
         a.head_off = h0;
         a.nh = nh;
         dim3 grid(nh * p.B, (p.s_q + BQ - 1) / BQ), block(384);

@@ -9,12 +9,19 @@
 // the argument"; the paper's section 3.3 "H_r slice of W_kv_b(latent)") -- and the
 // absorb / un-absorb products of the absorbed form and of decode (same page, Fig. 2).
 //
-// One CTA computes one 128 x BN tile.  Warp 0 lane 0 streams 64-wide k-blocks of A
-// and B through a 4-stage TMA ring; warp 1 lane 0 issues tcgen05.mma (M=128, N=BN,
-// K=16 per instruction) into a TMEM accumulator; then all four warps drain TMEM
-// (thread = row) and store.
+// Persistent kernel: one CTA per SM walks the 128 x BN output tiles of one or two
+// problems (tile t, t + gridDim.x, ...).  Warp 0 lane 0 streams 64-wide k-blocks of
+// A and B through a 4-stage TMA ring that runs across tile boundaries; the MMA
+// issuers accumulate each tile into one of two TMEM accumulators (M=128, K=16 per
+// instruction); warps 2-5 drain a finished accumulator (thread = row) and store it
+// while the next tile accumulates into the other one.  For BN = 256 two issuing
+// threads (warps 1 and 6) each own half of the columns: a thread waiting on an
+// mbarrier between MMA batches leaves the tensor pipe idle for ~100-200 cycles, and
+// the other thread's MMAs fill that gap.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "mla_internal.h"
 #include "tc.h"
@@ -29,131 +36,196 @@ namespace {
 
 constexpr int BM = 128, BK = 64, STAGES = 4;
 
-struct GemmK {
+struct GemmP {
     int M, N, K;
     int a_rows_per_z, a_zbase, a_z_per_batch;
     int b_rows_per_z, b_zbase, b_z_per_batch;
     void *C;
     long c_m, c_n, c_batch;
     int out_kind;  // 0 fp16, 1 bf16, 2 fp32
-    uint32_t idesc;
+    int tiles_n, tiles_m, tiles;
 };
 
-template <int BN>
-__global__ void __launch_bounds__(128, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, GemmK p) {
+struct GemmK {
+    GemmP pr[2];
+    int total;         // tiles of both problems
+    uint32_t idesc;    // per issuer: M = 128, N = BN / issuers
+};
+
+struct Tile {
+    int prob, m0, n0, batch;
+};
+
+__device__ __forceinline__ Tile tile_of(const GemmK &p, int t) {
+    Tile r;
+    r.prob = t < p.pr[0].tiles ? 0 : 1;
+    const GemmP &q = p.pr[r.prob];
+    int u = r.prob ? t - p.pr[0].tiles : t;
+    r.n0 = (u % q.tiles_n);
+    u /= q.tiles_n;
+    r.m0 = (u % q.tiles_m) * BM;
+    r.batch = u / q.tiles_m;
+    return r;
+}
+
+template <int BN, int NISS>
+__global__ void __launch_bounds__(256, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
+                   const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1, GemmK p) {
     using namespace tc;
     constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
-    constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+    constexpr uint32_t ACC_COLS = BN < 32 ? 32 : BN;   // one accumulator; two are allocated
+    constexpr int NW = BN / NISS;                      // columns per issuer
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
     uint64_t *full = (uint64_t *)(sB + STAGES * B_BYTES);
     uint64_t *empty = full + STAGES;
-    uint64_t *accb = empty + STAGES;
-    uint32_t *tslot = (uint32_t *)(accb + 1);
+    uint64_t *acc_full = empty + STAGES, *acc_empty = acc_full + 2;
+    uint32_t *tslot = (uint32_t *)(acc_empty + 2);
     volatile int *abort = (volatile int *)(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM, batch = blockIdx.z;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], NISS);
         }
-        mbar_init(accb, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], NISS);
+            mbar_init(&acc_empty[a], 4);   // the four epilogue warps
+        }
         *abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&ta);
-        tma_prefetch_desc(&tb);
     }
     if (warp == 1) {
-        tmem_alloc(tslot, TMEM_COLS);
+        tmem_alloc(tslot, 2 * ACC_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int nk = p.K / BK;
 
-    if (warp == 0 && lane == 0) {
-        const int a_r = m0 % p.a_rows_per_z, a_z = p.a_zbase + m0 / p.a_rows_per_z + batch * p.a_z_per_batch;
-        const int b_r = n0 % p.b_rows_per_z, b_z = p.b_zbase + n0 / p.b_rows_per_z + batch * p.b_z_per_batch;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % STAGES;
-            if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1, abort, &g_tc_gemm_err)) break;
-            mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
-            tma_load_3d(sA + s * A_BYTES, &ta, &full[s], kb * BK, a_r, a_z);
-            tma_load_3d(sB + s * B_BYTES, &tb, &full[s], kb * BK, b_r, b_z);
-        }
-    } else if (warp == 1 && lane == 0) {
-        bool ok = true;
-        for (int kb = 0; kb < nk && ok; ++kb) {
-            const int s = kb % STAGES;
-            if (!mbar_wait(&full[s], (kb / STAGES) & 1, abort, &g_tc_gemm_err)) {
-                ok = false;
-                break;
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&ta0);
+            tma_prefetch_desc(&tb0);
+            if (p.pr[1].tiles) {
+                tma_prefetch_desc(&ta1);
+                tma_prefetch_desc(&tb1);
             }
-            tc_fence_after();
-            const uint64_t da = sdesc_kmajor(sA + s * A_BYTES), db = sdesc_kmajor(sB + s * B_BYTES);
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-                mma_ss(tmem, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
-            mma_commit(&empty[s]);
-        }
-        mma_commit(accb);
-    }
-    __syncwarp();
-
-    // ---- epilogue: thread = row, 32 columns per TMEM load
-    const bool ok = mbar_wait(accb, 0, abort, &g_tc_gemm_err);
-    tc_fence_after();
-    const long row = m0 + warp * 32 + lane;
-    if (ok) {
-        char *C = (char *)p.C;
-        const int esz = p.out_kind == 2 ? 4 : 2;
-        for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, r);
-            tmem_ld_wait();
-            const int nb = n0 + c * 32;
-            if (row >= p.M || nb >= p.N) continue;
-            const long base = p.c_batch * batch + row * p.c_m;
-            if (p.c_n == 1 && nb + 32 <= p.N) {
-                if (esz == 2) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0 = __uint_as_float(r[2 * i]), x1 = __uint_as_float(r[2 * i + 1]);
-                        w[i] = p.out_kind == 0 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.total && ok; t += gridDim.x) {
+                const Tile w = tile_of(p, t);
+                const GemmP &q = p.pr[w.prob];
+                const CUtensorMap *ma = w.prob ? &ta1 : &ta0, *mb = w.prob ? &tb1 : &tb0;
+                const int n0 = w.n0 * BN;
+                const int a_r = w.m0 % q.a_rows_per_z, a_z = q.a_zbase + w.m0 / q.a_rows_per_z + w.batch * q.a_z_per_batch;
+                const int b_r = n0 % q.b_rows_per_z, b_z = q.b_zbase + n0 / q.b_rows_per_z + w.batch * q.b_z_per_batch;
+                for (int kb = 0; kb < q.K / BK; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, abort, &g_tc_gemm_err)) {
+                        ok = false;
+                        break;
                     }
-                    uint4 *dst = (uint4 *)(C + (base + nb) * 2);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                } else {
-                    uint4 *dst = (uint4 *)(C + (base + nb) * 4);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-                }
-            } else {
-                for (int i = 0; i < 32; ++i) {
-                    const int n = nb + i;
-                    if (n >= p.N) break;
-                    const float x = __uint_as_float(r[i]);
-                    const long off = base + (long)n * p.c_n;
-                    if (p.out_kind == 0) ((__half *)C)[off] = __float2half_rn(x);
-                    else if (p.out_kind == 1) ((__nv_bfloat16 *)C)[off] = __float2bfloat16_rn(x);
-                    else ((float *)C)[off] = x;
+                    mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+                    tma_load_3d(sA + s * A_BYTES, ma, &full[s], kb * BK, a_r, a_z);
+                    tma_load_3d(sB + s * B_BYTES, mb, &full[s], kb * BK, b_r, b_z);
                 }
             }
+        }
+    } else if (warp == 1 || (NISS == 2 && warp == 6)) {
+        // ------------------------------------------------- MMA issuer(s): columns [c0, c0 + NW)
+        if (lane == 0) {
+            const int c0 = warp == 1 ? 0 : NW;
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.total && ok; t += gridDim.x, ++lt) {
+                const Tile w = tile_of(p, t);
+                const int a = lt & 1;
+                // the epilogue has drained what tile lt-2 left in accumulator a
+                if (lt >= 2 && !mbar_wait(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)) break;
+                const uint32_t d = tmem + a * ACC_COLS + c0;
+                const int nk = p.pr[w.prob].K / BK;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(&full[s], (it / STAGES) & 1, abort, &g_tc_gemm_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = sdesc_kmajor(sA + s * A_BYTES);
+                    const uint64_t db = sdesc_kmajor(sB + s * B_BYTES + c0 * 128);   // rows c0.. of the B tile
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) mma_ss(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
+                    mma_commit(&empty[s]);
+                }
+                mma_commit(&acc_full[a]);
+            }
+        }
+    } else if (warp >= 2 && warp <= 5) {
+        // ------------------------------------------------ epilogue: thread = row
+        const int quad = warp & 3;
+        int lt = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.total; t += gridDim.x, ++lt) {
+            const Tile w = tile_of(p, t);
+            const GemmP &q = p.pr[w.prob];
+            const int a = lt & 1;
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[a], (lt >> 1) & 1, abort, &g_tc_gemm_err));
+            tc_fence_after();
+            const long row = w.m0 + quad * 32 + lane;
+            const int n0 = w.n0 * BN;
+            char *C = (char *)q.C;
+            const int esz = q.out_kind == 2 ? 4 : 2;
+            for (int c = 0; c < BN / 32 && ok; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + a * ACC_COLS + c * 32, r);
+                tmem_ld_wait();
+                const int nb = n0 + c * 32;
+                if (row >= q.M || nb >= q.N) continue;
+                const long base = q.c_batch * w.batch + row * q.c_m;
+                if (q.c_n == 1 && nb + 32 <= q.N) {
+                    if (esz == 2) {
+                        uint32_t o[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float x0 = __uint_as_float(r[2 * i]), x1 = __uint_as_float(r[2 * i + 1]);
+                            o[i] = q.out_kind == 0 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
+                        }
+                        uint4 *dst = (uint4 *)(C + (base + nb) * 2);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    } else {
+                        uint4 *dst = (uint4 *)(C + (base + nb) * 4);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                    }
+                } else {
+                    for (int i = 0; i < 32; ++i) {
+                        const int n = nb + i;
+                        if (n >= q.N) break;
+                        const float x = __uint_as_float(r[i]);
+                        const long off = base + (long)n * q.c_n;
+                        if (q.out_kind == 0) ((__half *)C)[off] = __float2half_rn(x);
+                        else if (q.out_kind == 1) ((__nv_bfloat16 *)C)[off] = __float2bfloat16_rn(x);
+                        else ((float *)C)[off] = x;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem, 2 * ACC_COLS);
 }
 
 template <int BN>
@@ -161,57 +233,92 @@ size_t gemm_smem() {
     return STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
 }
 
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+template <int BN, int NISS>
+cudaError_t launch_gemm(const CUtensorMap *maps, const GemmK &p, cudaStream_t st) {
+    const size_t sm = gemm_smem<BN>();
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, NISS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    // 64-wide tiles need 97 KB of shared memory and 128 TMEM columns: two CTAs per SM
+    const int grid = std::min(p.total, num_sms() * (BN == 64 ? 2 : 1));
+    tc_gemm_kernel<BN, NISS><<<grid, 256, sm, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaStream_t st) {
+    if (n_probs < 1 || n_probs > 2) return cudaErrorInvalidValue;
+    int maxN = 0;
+    for (int i = 0; i < n_probs; ++i) {
+        if (probs[i].K % BK || probs[i].K != probs[0].K) return cudaErrorInvalidValue;
+        maxN = std::max(maxN, probs[i].N);
+    }
+    const int BN = maxN >= 256 ? 256 : (maxN >= 128 ? 128 : 64);
+    CUtensorMap maps[4];
+    GemmK p{};
+    p.total = 0;
+    for (int i = 0; i < 2; ++i) {
+        GemmP &q = p.pr[i];
+        if (i >= n_probs) {
+            q.tiles = 0;
+            maps[2 * i] = maps[0];
+            maps[2 * i + 1] = maps[1];
+            continue;
+        }
+        const GemmProblem &g = probs[i];
+        cudaError_t e = make_operand_map(&maps[2 * i], g.A, BM);
+        if (e != cudaSuccess) return e;
+        e = make_operand_map(&maps[2 * i + 1], g.B, BN);
+        if (e != cudaSuccess) return e;
+        q.M = g.M;
+        q.N = g.N;
+        q.K = g.K;
+        q.a_rows_per_z = g.A.rows_per_z;
+        q.a_zbase = g.A.zbase;
+        q.a_z_per_batch = g.A.z_per_batch;
+        q.b_rows_per_z = g.B.rows_per_z;
+        q.b_zbase = g.B.zbase;
+        q.b_z_per_batch = g.B.z_per_batch;
+        q.C = g.C;
+        q.c_m = g.c_m;
+        q.c_n = g.c_n;
+        q.c_batch = g.c_batch;
+        q.out_kind = g.out_kind;
+        q.tiles_n = (g.N + BN - 1) / BN;
+        q.tiles_m = (g.M + BM - 1) / BM;
+        q.tiles = (g.M == 0 || g.N == 0) ? 0 : q.tiles_n * q.tiles_m * g.batch;
+        p.total += q.tiles;
+    }
+    if (p.total == 0) return cudaSuccess;
+    ProfScope ps("tc_gemm", st);
+    switch (BN) {
+        case 256:
+            p.idesc = tc::idesc_f16(BM, 128, f16);
+            return launch_gemm<256, 2>(maps, p, st);
+        case 128:
+            p.idesc = tc::idesc_f16(BM, 128, f16);
+            return launch_gemm<128, 1>(maps, p, st);
+        default:
+            p.idesc = tc::idesc_f16(BM, 64, f16);
+            return launch_gemm<64, 1>(maps, p, st);
+    }
+}
 
 cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int K, int batch, bool f16,
                     void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st) {
     if (M == 0 || N == 0 || batch == 0) return cudaSuccess;
-    if (K % BK) return cudaErrorInvalidValue;
-    const int BN = N >= 256 ? 256 : (N >= 128 ? 128 : 64);
-    CUtensorMap ma, mb;
-    cudaError_t e = make_operand_map(&ma, A, BM);
-    if (e != cudaSuccess) return e;
-    e = make_operand_map(&mb, B, BN);
-    if (e != cudaSuccess) return e;
-    GemmK p;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.a_rows_per_z = A.rows_per_z;
-    p.a_zbase = A.zbase;
-    p.a_z_per_batch = A.z_per_batch;
-    p.b_rows_per_z = B.rows_per_z;
-    p.b_zbase = B.zbase;
-    p.b_z_per_batch = B.z_per_batch;
-    p.C = C;
-    p.c_m = c_m;
-    p.c_n = c_n;
-    p.c_batch = c_batch;
-    p.out_kind = out_kind;
-    p.idesc = tc::idesc_f16(BM, BN, f16);
-    dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM, batch), block(128);
-    ProfScope ps("tc_gemm", st);
-    switch (BN) {
-        case 256: {
-            size_t sm = gemm_smem<256>();
-            e = cudaFuncSetAttribute(tc_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-            if (e == cudaSuccess) tc_gemm_kernel<256><<<grid, block, sm, st>>>(ma, mb, p);
-            break;
-        }
-        case 128: {
-            size_t sm = gemm_smem<128>();
-            e = cudaFuncSetAttribute(tc_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-            if (e == cudaSuccess) tc_gemm_kernel<128><<<grid, block, sm, st>>>(ma, mb, p);
-            break;
-        }
-        default: {
-            size_t sm = gemm_smem<64>();
-            e = cudaFuncSetAttribute(tc_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-            if (e == cudaSuccess) tc_gemm_kernel<64><<<grid, block, sm, st>>>(ma, mb, p);
-        }
-    }
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    GemmProblem g{A, B, M, N, K, batch, C, c_m, c_n, c_batch, out_kind};
+    return tc_gemm_group(&g, 1, f16, st);
 }
 
 cudaError_t tc_gemm_read_and_clear_error(unsigned *flags, cudaStream_t st) {

@@ -29,8 +29,18 @@ cudaError_t make_tma_map(CUtensorMap *map, const void *ptr, int rank, const unsi
 cudaError_t make_operand_map(CUtensorMap *map, const TmaOperand &op, int tile_rows);
 
 // C[batch](m, n) = sum_k A(m, k) B(n, k); K % 64 == 0.  out_kind: 0 fp16, 1 bf16, 2 fp32.
+struct GemmProblem {
+    TmaOperand A, B;
+    int M, N, K, batch;
+    void *C;
+    long c_m, c_n, c_batch;
+    int out_kind;
+};
 cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int K, int batch, bool f16,
                     void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st);
+// One persistent launch over the tiles of one or two problems (same K, same operand
+// type): the explicit path's K_nope and V^T products share one launch.
+cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaStream_t st);
 
 cudaError_t tc_gemm_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_attn_read_and_clear_error(unsigned *flags, cudaStream_t st);
