@@ -32,6 +32,11 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA prefill fwd TFLOP/s (% of BF16 peak); decode HBM GB/s (% of 8 TB/s)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max clock
+# DRAM bytes (read + write) per launch of the dominant kernels, from the ncu captures
+# summarised under profiles/ (None until the current kernel has been captured).  The
+# decode capture runs B = 8; its traffic grows in proportion to the batch, so the
+# B = 64 launch is 8x that.
+NCU_TRAFFIC = {"tc_attn": 62.88e6, "tc_latent_attn": 306.51e6 * 8}
 
 
 def load_peaks():
@@ -249,37 +254,38 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream().cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
-    # ---- prefill
+    # ---- prefill and decode: the timed passes carry no per-launch events
     d, t, out, lse, ws = prefill_setup(pcfg)
     pf = lambda: prefill_call(pcfg, d, t, out, lse, ws, stream)  # noqa: E731
     pf()
     torch.cuda.synchronize()
     path = mla.last_path()
-    n0 = mla.launch_count()
-    mla.profile_enable(True)
-    mla.profile_reset()
+    dd, dt_, dout, dlse, dws = decode_setup(dcfg)
+    dfn = lambda: decode_call(dcfg, dd, dt_, dout, dlse, dws, stream)  # noqa: E731
+    dfn()
+    torch.cuda.synchronize()
+    dpath = mla.last_path()
     with ClockSampler(local) as clk:
+        n0 = mla.launch_count()
         p_times = timed(pf, args.steps, args.warmup, world, flush)
-        prof_p = mla.profile_all()
         launches_p = mla.launch_count() - n0
-        mla.profile_enable(False)
-
-        # ---- decode
-        dd, dt_, dout, dlse, dws = decode_setup(dcfg)
-        dfn = lambda: decode_call(dcfg, dd, dt_, dout, dlse, dws, stream)  # noqa: E731
-        dfn()
-        torch.cuda.synchronize()
-        dpath = mla.last_path()
         n1 = mla.launch_count()
-        mla.profile_enable(True)
-        mla.profile_reset()
         d_times = timed(dfn, args.steps, args.warmup, world)
-        prof_d = mla.profile_all()
         launches_d = mla.launch_count() - n1
-        mla.profile_enable(False)
-    # the profiled launches in the timed region include the warm-up calls: count per call
     per_call_p = launches_p / (args.steps + args.warmup)
     per_call_d = launches_d / (args.steps + args.warmup)
+
+    # ---- second pass of the same calls with a CUDA-event pair around every launch
+    # (on the launching stream): per-kernel times for the roofline
+    def profiled(fn, fl):
+        mla.profile_enable(True)
+        mla.profile_reset()
+        timed(fn, args.steps, args.warmup, world, fl)
+        prof = mla.profile_all()
+        mla.profile_enable(False)
+        return prof
+    prof_p = profiled(pf, flush)
+    prof_d = profiled(dfn, None)
 
     flops = pcfg.flops()
     p_ms = max_over_ranks(statistics.mean(p_times), world)
@@ -288,7 +294,7 @@ def run_ours(args, world, rank, local):
     dbytes = dcfg.algorithmic_bytes()
     d_gbs = world * dbytes / (d_ms * 1e-3) / 1e9
 
-    # ---- roofline of the dominant kernels (profiled over the timed regions)
+    # ---- roofline of the dominant kernels (from the profiled pass)
     calls = args.steps + args.warmup
     kp = dominant(prof_p, ("tc_attn", "attn_simt"))
     roof = None
@@ -301,7 +307,7 @@ def run_ours(args, world, rank, local):
         else:
             peak, bound, note = FP32_ALU_TFLOPS, "alu", "fp32 FMA lanes x max clock (SIMT kernel)"
         roof = {"kernel": kp, "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": None, "peak_kind": note,
+                "frac": round(ach / peak, 4), "traffic": NCU_TRAFFIC.get(kp), "peak_kind": note,
                 "launches": n, "avg_launch_us": round(ms / n * 1e3, 2),
                 "share_of_step": round(ms / (sum(v[1] for v in prof_p.values()) or 1), 3)}
     kd = dominant(prof_d, ("tc_latent_attn", "attn_simt"))
@@ -311,7 +317,8 @@ def run_ours(args, world, rank, local):
         per_launch = dcfg.cache_bytes() * calls / n
         ach = per_launch / (ms / n * 1e-3) / 1e9
         droof = {"kernel": kd, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks.get("hbm_gbs", 6800.0),
-                 "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4), "traffic": None,
+                 "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4),
+                 "traffic": NCU_TRAFFIC.get(kd),
                  "peak_kind": peak_kind, "launches": n, "avg_launch_us": round(ms / n * 1e3, 2)}
 
     # ---- end to end through the C ABI with pinned host buffers (prefill)
