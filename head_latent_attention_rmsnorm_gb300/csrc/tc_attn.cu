@@ -8,23 +8,24 @@
 //   s_ij = scale * (q_nope_i . K_nope_j + RoPE(q_pe_i) . RoPE(k_pe_j)),
 // softmax over visible keys (j <= q_offset + i), output plus log-sum-exp.
 //
-// Kernel: one CTA per (128-query tile, head, batch), 384 threads.
+// Kernel: one CTA per (128-query tile, head, batch), 640 threads.
 //   warp 0    TMA producer of K tiles (K_nope 128 + RoPE band 64 dims), 3-deep ring.
-//   warp 10   TMA producer of V^T tiles, 2-deep ring (separate, so that a wait for a
+//   warp 18   TMA producer of V^T tiles, 2-deep ring (separate, so that a wait for a
 //             free V slot never holds back the next K tile).
 //   warp 1    tcgen05 issuer of the scores: S_j = Q K_j^T (M=128, N=128, K=192, Q from
 //             TMEM) into TMEM S buffer j & 1, as soon as K_j has landed and P.V_{j-2}
 //             (which read that buffer) is done.  Also owns the TMEM allocation.
-//   warp 11   tcgen05 issuer of O += P_j V_j (M=128, N=128, K=128), P read from TMEM
+//   warp 19   tcgen05 issuer of O += P_j V_j (M=128, N=128, K=128), P read from TMEM
 //             where the softmax wrote it over S_j.  Two issuing threads keep the tensor
 //             pipe fed: a thread that waits on an mbarrier between MMA batches leaves
 //             the pipe idle for ~100-200 cycles, so neither issuer waits on the other.
-//   warps 2-9 first load this row's Q (bf16 q_nope widened to fp16, q_pe rotated by
-//             RoPE) straight into TMEM; then softmax, two threads per query row (TMEM
-//             lane = row; keys 0-63 and 64-127 of each tile): online softmax in the log2
+//   warps 2-17 first load this row's Q (bf16 q_nope widened to fp16, q_pe rotated by
+//             RoPE) straight into TMEM; then softmax, four threads per query row (TMEM
+//             lane = row; 32 keys of each tile each): online softmax in the log2
 //             domain; O in TMEM is rescaled only when a row maximum grows by more than
 //             2^8 (the stale maximum keeps every p <= 256, exact after the final
-//             division); epilogue O / l and lse.
+//             division); epilogue O / l and lse.  Sixteen softmax warps (four per
+//             scheduler) hide the TMEM-load and exp latencies of one another.
 // Operands are fp16 (11-bit significand); K_nope, V^T and the rotated k_pe band are
 // produced in fp16 by the reconstruction GEMMs and the prep launch.
 #include <cuda_bf16.h>
@@ -50,7 +51,10 @@ constexpr uint32_t BOX = 128 * 128;            // one 128-row x 64-element fp16 
 constexpr uint32_t K_BYTES = 3 * BOX;          // K_nope lo, K_nope hi, RoPE band
 constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halves
 constexpr int KST = 3, VST = 2;
-constexpr uint32_t SMEM_BYTES = KST * K_BYTES + VST * V_BYTES + 1024 + 256 + 4 * 2 * 2 * BQ;
+constexpr int NSM = 16;                       // softmax warps: four threads per query row
+// K/V rings, 1 KB alignment slack, 256 B of barriers, row-max exchange [2][4][BQ] and
+// row-sum exchange [4][BQ]
+constexpr uint32_t SMEM_BYTES = KST * K_BYTES + VST * V_BYTES + 1024 + 256 + 4 * (2 * 4 + 4) * BQ;
 // TMEM columns: S buffers 0-127 and 128-255, O 256-383, Q (192 fp16 = 96 columns) 384-479
 constexpr uint32_t T_O = 256, T_Q = 384;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -77,7 +81,7 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(640, 1)
     tc_attn_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
                    const __grid_constant__ CUtensorMap mV, AttnK p) {
     extern __shared__ uint8_t smem_raw[];
@@ -91,7 +95,8 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t *s_full = v_empty + VST, *p_full = s_full + 2, *pv_done = p_full + 2;
     uint64_t *o_done = pv_done + 2, *o_final = o_done + 1;
     uint32_t *tslot = (uint32_t *)(bars + 24);
-    float (*red)[2][BQ] = (float (*)[2][BQ])(bars + 32);   // [tile parity][half][row] partial maxima
+    float (*red)[4][BQ] = (float (*)[4][BQ])(bars + 32);   // [tile parity][quarter][row] partial maxima
+    float (*lred)[BQ] = (float (*)[BQ])((float *)(bars + 32) + 2 * 4 * BQ);   // [quarter][row] row sums
     volatile int *abort = (volatile int *)(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -105,7 +110,7 @@ __global__ void __launch_bounds__(384, 1)
     const int nt = (kv_end + BKV - 1) / BKV;
 
     if (tid == 0) {
-        mbar_init(q_ready, 8);
+        mbar_init(q_ready, NSM);
         for (int i = 0; i < KST; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 8);
+            mbar_init(&p_full[i], NSM);
             mbar_init(&pv_done[i], 1);
         }
         mbar_init(o_done, 1);
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(384, 1)
                 tma_load_3d(kd + 2 * BOX, &mKr, &k_full[ks], 0, j * BKV, b);
             }
         }
-    } else if (warp == 10) {
+    } else if (warp == 2 + NSM) {
         // ----------------------------------------------------- V^T tiles (TMA)
         if (lane == 0) {
             tma_prefetch_desc(&mV);
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(384, 1)
                 mma_commit(&k_empty[ks]);
             }
         }
-    } else if (warp == 11) {
+    } else if (warp == 3 + NSM) {
         // ------------------------------------------------------------ P.V issuer
         if (lane == 0) {
             for (int t = 0; t < nt; ++t) {
@@ -207,106 +212,109 @@ __global__ void __launch_bounds__(384, 1)
             }
             mma_commit(o_final);
         }
-    } else {
+    } else if (warp >= 2 && warp < 2 + NSM) {
         // ---------------------------------------------------------- softmax warps
-        // Two threads per query row: warps 2-5 take keys 0-63 of each tile, warps 6-9
-        // keys 64-127 (warp w and w+4 reach the same TMEM lanes).  The halves combine
-        // their row maxima through shared memory once per tile.
-        const int quad = warp & 3, hf = (warp - 2) >> 2;
+        // Four threads per query row: warps 2-5 take keys 0-31 of each tile, warps 6-9
+        // keys 32-63, 10-13 keys 64-95, 14-17 keys 96-127 (warps w, w+4, w+8, w+12 reach
+        // the same TMEM lanes).  The quarters combine their row maxima through shared
+        // memory once per tile.
+        const int quad = warp & 3, qr = (warp - 2) >> 2;
         const int row = quad * 32 + lane;
         const int pos = p.q_offset + q0 + row;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        // ---- this row's Q into TMEM: half hf widens q_nope dims [64 hf, 64 hf + 64) to
-        // fp16 (columns 32 hf ...), and rotates the RoPE pairs (t, t + 32) for t in
-        // [16 hf, 16 hf + 16) (q dims 128 + t and 160 + t: columns 64 + 8 hf ... and
-        // 80 + 8 hf ...).  Rows past s_q get zeros.
+        // ---- this row's Q into TMEM: quarter qr widens q_nope dims [32 qr, 32 qr + 32)
+        // to fp16 (columns 16 qr ...); quarters 0 and 1 also rotate the RoPE pairs
+        // (t, t + 32) for t in [16 qr, 16 qr + 16) (q dims 128 + t and 160 + t: columns
+        // 64 + 8 qr ... and 80 + 8 qr ...).  Rows past s_q get zeros.
         {
             const int qi = q0 + row;
-            uint32_t qn[32], ra8[8], rb8[8];
+            uint32_t qn[16], ra8[8], rb8[8];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) qn[e] = 0u;
+            for (int e = 0; e < 16; ++e) qn[e] = 0u;
 #pragma unroll
             for (int e = 0; e < 8; ++e) ra8[e] = rb8[e] = 0u;
             if (qi < p.s_q) {
                 const long qrow = ((long)b * p.s_q + qi) * p.n_hq + hq;
-                const uint4 *src = (const uint4 *)(p.q_nope + qrow * 128 + hf * 64);
+                const uint4 *src = (const uint4 *)(p.q_nope + qrow * 128 + qr * 32);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     const uint4 v = src[c];
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         qn[4 * c + i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
                 }
-                const __nv_bfloat16 *pe = p.q_pe + qrow * 64 + hf * 16;
-                const uint4 xa[2] = {((const uint4 *)pe)[0], ((const uint4 *)pe)[1]};
-                const uint4 xb[2] = {((const uint4 *)(pe + 32))[0], ((const uint4 *)(pe + 32))[1]};
-                const float4 *cs = (const float4 *)(p.tab + (long)(p.q_offset + qi) * 32 + hf * 16);
+                if (qr < 2) {
+                    const __nv_bfloat16 *pe = p.q_pe + qrow * 64 + qr * 16;
+                    const uint4 xa[2] = {((const uint4 *)pe)[0], ((const uint4 *)pe)[1]};
+                    const uint4 xb[2] = {((const uint4 *)(pe + 32))[0], ((const uint4 *)(pe + 32))[1]};
+                    const float4 *cs = (const float4 *)(p.tab + (long)(p.q_offset + qi) * 32 + qr * 16);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t wa[4] = {xa[h].x, xa[h].y, xa[h].z, xa[h].w};
-                    const uint32_t wb[4] = {xb[h].x, xb[h].y, xb[h].z, xb[h].w};
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t wa[4] = {xa[h].x, xa[h].y, xa[h].z, xa[h].w};
+                        const uint32_t wb[4] = {xb[h].x, xb[h].y, xb[h].z, xb[h].w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {   // elements 8h + 2k, 8h + 2k + 1 of this half
-                        const float4 r = cs[h * 4 + k];   // (cos, sin) of both elements
-                        const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
-                        const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
-                        ra8[4 * h + k] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
-                        rb8[4 * h + k] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
+                        for (int k = 0; k < 4; ++k) {   // elements 8h + 2k, 8h + 2k + 1 of this part
+                            const float4 r = cs[h * 4 + k];   // (cos, sin) of both elements
+                            const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
+                            const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
+                            ra8[4 * h + k] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
+                            rb8[4 * h + k] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
+                        }
                     }
                 }
             }
-            tmem_st32(lane_base + T_Q + hf * 32, qn);
-            tmem_st8(lane_base + T_Q + 64 + hf * 8, ra8);
-            tmem_st8(lane_base + T_Q + 80 + hf * 8, rb8);
+            tmem_st16(lane_base + T_Q + qr * 16, qn);
+            if (qr < 2) {   // warp-uniform
+                tmem_st8(lane_base + T_Q + 64 + qr * 8, ra8);
+                tmem_st8(lane_base + T_Q + 80 + qr * 8, rb8);
+            }
             tmem_st_wait();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
-        bool ok = true;
 
         // A failed wait clears `ok` (warp-uniform) but never leaves the loop early: every
         // softmax thread passes the same named barriers, so an abort cannot strand one.
+        bool ok = true;
         float m = -INFINITY, l = 0.f;
-        ok = __all_sync(0xffffffffu, ok);
         for (int j = 0; j < nt; ++j) {
             const int sb = j & 1;
             ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[sb], (j >> 1) & 1, abort, &g_tc_attn_err));
             tc_fence_after();
-            uint32_t s[2][32];
+            uint32_t sr[32];
             if (ok) {
-                tmem_ld32(lane_base + sb * 128 + hf * 64, s[0]);
-                tmem_ld32(lane_base + sb * 128 + hf * 64 + 32, s[1]);
+                tmem_ld32(lane_base + sb * 128 + qr * 32, sr);
                 tmem_ld_wait();
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[0][i] = s[1][i] = 0u;
+                for (int i = 0; i < 32; ++i) sr[i] = 0u;
             }
-            const int j0 = j * BKV + hf * 64;
-            const bool masked = (j0 + 64 > p.kv_need) || (p.causal && j0 + 63 > p.q_offset + q0);
-            float x[64];
+            const int j0 = j * BKV + qr * 32;
+            const bool masked = (j0 + 32 > p.kv_need) || (p.causal && j0 + 31 > p.q_offset + q0);
+            float x[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(s[c >> 5][c & 31]);
+            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sr[c]);
             if (masked) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 32; ++c) {
                     const int key = j0 + c;
                     if (key >= p.kv_need || (p.causal && key > pos)) x[c] = -INFINITY;
                 }
             }
             // independent accumulators: the reductions are latency chains otherwise
-            float mx[8];
+            float mx[4];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) mx[a] = x[a];
+            for (int a = 0; a < 4; ++a) mx[a] = x[a];
 #pragma unroll
-            for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-            const float ml = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            // both halves have read their S columns before either writes P over them
-            red[sb][hf][row] = ml;
-            named_bar_sync(1, 256);
-            const float mt = fmaxf(ml, red[sb][hf ^ 1][row]) * p.scale_log2;
+            for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], x[c]);
+            const float ml = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            // all four quarters have read their S columns before any writes P over them
+            red[sb][qr][row] = ml;
+            named_bar_sync(1, 32 * NSM);
+            const float mt =
+                fmaxf(fmaxf(red[sb][0][row], red[sb][1][row]), fmaxf(red[sb][2][row], red[sb][3][row])) * p.scale_log2;
             const float m_new = fmaxf(m, mt);
             const bool need = m_new > m + RESCALE_LOG2;   // also true on the first finite maximum
             if (__any_sync(0xffffffffu, need)) {
@@ -315,33 +323,30 @@ __global__ void __launch_bounds__(384, 1)
                 if (j > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_attn_err));
                 if (j > 0 && ok) {
                     tc_fence_after();
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + T_O + qr * 32, o);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_base + T_O + hf * 64 + c * 32, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(lane_base + T_O + hf * 64 + c * 32, o);
-                    }
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(lane_base + T_O + qr * 32, o);
                     tmem_st_wait();
                 }
                 l *= alpha;
                 m = m_use;
             }
             const float nm = (m == -INFINITY) ? 0.f : -m;
-            float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[32];
+            float ra[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
                 const float p0 = ex2(fmaf(x[2 * i], p.scale_log2, nm));
                 const float p1 = ex2(fmaf(x[2 * i + 1], p.scale_log2, nm));
-                ra[i & 7] += p0 + p1;
+                ra[i & 3] += p0 + p1;
                 pk[i] = pack_f16(p0, p1);
             }
-            const float rs = ((ra[0] + ra[1]) + (ra[2] + ra[3])) + ((ra[4] + ra[5]) + (ra[6] + ra[7]));
+            const float rs = (ra[0] + ra[1]) + (ra[2] + ra[3]);
             if (ok) {
-                tmem_st32(lane_base + sb * 128 + hf * 32, pk);
+                tmem_st16(lane_base + sb * 128 + qr * 16, pk);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -349,39 +354,34 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) mbar_arrive(&p_full[sb]);
             l += rs;
         }
-        // ---- epilogue: combine the halves' row sums; each half stores its 64 columns
-        red[0][hf][row] = l;
-        named_bar_sync(1, 256);
-        l += red[0][hf ^ 1][row];
+        // ---- epilogue: combine the quarters' row sums (own exchange array: a slower
+        // quarter may still be reading the last tile's maxima); each stores 32 columns
+        lred[qr][row] = l;
+        named_bar_sync(1, 32 * NSM);
+        l = (lred[0][row] + lred[1][row]) + (lred[2][row] + lred[3][row]);
         if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, &g_tc_attn_err);
         tc_fence_after();
         const int qi = q0 + row;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint32_t o[2][32];
+        uint32_t o[32];
         if (nt > 0) {
-            tmem_ld32(lane_base + T_O + hf * 64, o[0]);
-            tmem_ld32(lane_base + T_O + hf * 64 + 32, o[1]);
+            tmem_ld32(lane_base + T_O + qr * 32, o);
             tmem_ld_wait();
         } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[c][i] = 0u;
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
         if (ok && qi < p.s_q) {
-            uint4 *dst = (uint4 *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h + hf * 64);
+            uint4 *dst = (uint4 *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h + qr * 32);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int v = 0; v < 4; ++v) {
+                uint32_t w[4];
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w[i] = pack_bf16(__uint_as_float(o[c][8 * v + 2 * i]) * inv,
-                                         __uint_as_float(o[c][8 * v + 2 * i + 1]) * inv);
-                    dst[c * 4 + v] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            if (hf == 0)
+                for (int i = 0; i < 4; ++i)
+                    w[i] = pack_bf16(__uint_as_float(o[8 * v + 2 * i]) * inv, __uint_as_float(o[8 * v + 2 * i + 1]) * inv);
+                dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (qr == 0)
                 p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] =
                     l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
@@ -468,7 +468,7 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
         if ((e = tc_gemm_group(kv, 2, true, st)) != cudaSuccess) return e;
         a.head_off = h0;
         a.nh = nh;
-        dim3 grid(nh * p.B, (p.s_q + BQ - 1) / BQ), block(384);
+        dim3 grid(nh * p.B, (p.s_q + BQ - 1) / BQ), block(32 * (NSM + 4));
         {
             ProfScope ps("tc_attn", st);
             tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mK, mKr, mV, a);
