@@ -8,7 +8,9 @@
 //   s_ij = scale * (q_nope_i . K_nope_j + RoPE(q_pe_i) . RoPE(k_pe_j)),
 // softmax over visible keys (j <= q_offset + i), output plus log-sum-exp.
 //
-// Kernel: one CTA per (128-query tile, head, batch), 640 threads.
+// Kernel: persistent, one CTA per SM (640 threads) walking work units = (128-query
+// tile, head, batch), heaviest first under the causal mask, in rounds that alternate
+// direction; TMEM, barriers and the TMA rings carry over from one unit to the next.
 //   warp 0    TMA producer of K tiles (K_nope 128 + RoPE band 64 dims), 3-deep ring.
 //   warp 18   TMA producer of V^T tiles, 2-deep ring (separate, so that a wait for a
 //             free V slot never holds back the next K tile).
@@ -71,9 +73,29 @@ struct AttnK {
     const __nv_bfloat16 *q_nope;   // [b][i][head][128]
     const __nv_bfloat16 *q_pe;     // un-rotated q_pe [b][i][head][64]
     int n_hq;                      // heads of the q tensors
-    int nh;                        // heads of this launch (grid x = nh * batch)
+    int nh, nb, n_qt, units;       // heads of this launch, batch, query tiles, work units
     const float2 *tab;             // RoPE (cos, sin) of position p, frequency t at p * 32 + t
 };
+
+// One work unit = (128-query tile, head, batch).  Units are numbered heaviest first
+// under the causal mask: (head, batch) fastest, query tiles from the latest down.
+struct Work {
+    int hl, b, q0, nt;
+};
+__device__ __forceinline__ Work work_of(const AttnK &p, int u) {
+    const int nhb = p.nh * p.nb;
+    const int hb = u % nhb;
+    Work w;
+    w.hl = hb % p.nh;
+    w.b = hb / p.nh;
+    w.q0 = (p.n_qt - 1 - u / nhb) * BQ;
+    const int kv_end = p.causal ? min(p.kv_need, p.q_offset + w.q0 + BQ) : p.kv_need;
+    w.nt = (kv_end + BKV - 1) / BKV;
+    return w;
+}
+// Unit of round k for CTA c of G: rounds alternate direction over the heaviest-first
+// list, so every CTA gets a mix of heavy and light units.
+__device__ __forceinline__ int unit_at(int k, int c, int G) { return (k & 1) ? (k + 1) * G - 1 - c : k * G + c; }
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -93,21 +115,14 @@ __global__ void __launch_bounds__(640, 1)
     uint64_t *k_full = bars + 1, *k_empty = k_full + KST;
     uint64_t *v_full = k_empty + KST, *v_empty = v_full + VST;
     uint64_t *s_full = v_empty + VST, *p_full = s_full + 2, *pv_done = p_full + 2;
-    uint64_t *o_done = pv_done + 2, *o_final = o_done + 1;
+    uint64_t *o_done = pv_done + 2, *o_final = o_done + 1, *o_free = o_final + 1;
     uint32_t *tslot = (uint32_t *)(bars + 24);
     float (*red)[4][BQ] = (float (*)[4][BQ])(bars + 32);   // [tile parity][quarter][row] partial maxima
     float (*lred)[BQ] = (float (*)[BQ])((float *)(bars + 32) + 2 * 4 * BQ);   // [quarter][row] row sums
     volatile int *abort = (volatile int *)(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // x: (head, batch) pairs, y: query tiles from the latest (heaviest under the causal
-    // mask) down, so that the first waves take the heaviest tiles of every head
-    const int qt = gridDim.y - 1 - blockIdx.y;
-    const int hl = blockIdx.x % p.nh, b = blockIdx.x / p.nh;
-    const int q0 = qt * BQ;
-    const int hq = p.head_off + hl;
-    const int kv_end = p.causal ? min(p.kv_need, p.q_offset + q0 + BQ) : p.kv_need;
-    const int nt = (kv_end + BKV - 1) / BKV;
+    const int G = gridDim.x, c = blockIdx.x;
 
     if (tid == 0) {
         mbar_init(q_ready, NSM);
@@ -126,6 +141,7 @@ __global__ void __launch_bounds__(640, 1)
         }
         mbar_init(o_done, 1);
         mbar_init(o_final, 1);
+        mbar_init(o_free, NSM);   // the softmax warps have read O out of TMEM
         *abort = 0;
         fence_mbar_init();
     }
@@ -138,79 +154,129 @@ __global__ void __launch_bounds__(640, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;   // S0: cols 0-127, S1: 128-255, O: 256-383, Q: 384-479
 
+    // Every role walks the same units in the same order and counts key tiles T across
+    // units, so ring slots and barrier parities continue from one unit to the next.
     if (warp == 0) {
         // ------------------------------------------------------- K tiles (TMA)
         if (lane == 0) {
             tma_prefetch_desc(&mK);
             tma_prefetch_desc(&mKr);
-            for (int j = 0; j < nt; ++j) {
-                const int ks = j % KST;
-                if (j >= KST && !mbar_wait(&k_empty[ks], ((j / KST) - 1) & 1, abort, &g_tc_attn_err)) break;
-                uint8_t *kd = sK + ks * K_BYTES;
-                mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
-                tma_load_3d(kd, &mK, &k_full[ks], hl * 128, j * BKV, b);
-                tma_load_3d(kd + BOX, &mK, &k_full[ks], hl * 128 + 64, j * BKV, b);
-                tma_load_3d(kd + 2 * BOX, &mKr, &k_full[ks], 0, j * BKV, b);
+            bool ok = true;
+            int T = 0;
+            for (int k = 0; k * G < p.units && ok; ++k) {
+                const int u = unit_at(k, c, G);
+                if (u >= p.units) continue;
+                const Work w = work_of(p, u);
+                for (int j = 0; j < w.nt; ++j, ++T) {
+                    const int ks = T % KST;
+                    if (T >= KST && !mbar_wait(&k_empty[ks], ((T / KST) - 1) & 1, abort, &g_tc_attn_err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *kd = sK + ks * K_BYTES;
+                    mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
+                    tma_load_3d(kd, &mK, &k_full[ks], w.hl * 128, j * BKV, w.b);
+                    tma_load_3d(kd + BOX, &mK, &k_full[ks], w.hl * 128 + 64, j * BKV, w.b);
+                    tma_load_3d(kd + 2 * BOX, &mKr, &k_full[ks], 0, j * BKV, w.b);
+                }
             }
         }
     } else if (warp == 2 + NSM) {
         // ----------------------------------------------------- V^T tiles (TMA)
         if (lane == 0) {
             tma_prefetch_desc(&mV);
-            for (int j = 0; j < nt; ++j) {
-                const int vs = j % VST;
-                if (j >= VST && !mbar_wait(&v_empty[vs], ((j / VST) - 1) & 1, abort, &g_tc_attn_err)) break;
-                uint8_t *vd = sV + vs * V_BYTES;
-                mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
-                tma_load_3d(vd, &mV, &v_full[vs], j * BKV, hl * 128, b);
-                tma_load_3d(vd + BOX, &mV, &v_full[vs], j * BKV + 64, hl * 128, b);
+            bool ok = true;
+            int T = 0;
+            for (int k = 0; k * G < p.units && ok; ++k) {
+                const int u = unit_at(k, c, G);
+                if (u >= p.units) continue;
+                const Work w = work_of(p, u);
+                for (int j = 0; j < w.nt; ++j, ++T) {
+                    const int vs = T % VST;
+                    if (T >= VST && !mbar_wait(&v_empty[vs], ((T / VST) - 1) & 1, abort, &g_tc_attn_err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *vd = sV + vs * V_BYTES;
+                    mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
+                    tma_load_3d(vd, &mV, &v_full[vs], j * BKV, w.hl * 128, w.b);
+                    tma_load_3d(vd + BOX, &mV, &v_full[vs], j * BKV + 64, w.hl * 128, w.b);
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- score MMA issuer
         if (lane == 0) {
-            bool ok = mbar_wait(q_ready, 0, abort, &g_tc_attn_err);
-            for (int t = 0; t < nt && ok; ++t) {
-                const int ks = t % KST;
-                // S buffer t & 1 last held P_{t-2}: P.V_{t-2} must have read it
-                if (t >= 2 && !mbar_wait(&pv_done[t & 1], ((t - 2) >> 1) & 1, abort, &g_tc_attn_err)) break;
-                if (!mbar_wait(&k_full[ks], (t / KST) & 1, abort, &g_tc_attn_err)) break;
-                tc_fence_after();
-                const uint32_t s_tm = tmem + (t & 1) * 128;
-                const uint8_t *kd = sK + ks * K_BYTES;
+            bool ok = true;
+            int T = 0, n = 0;   // key tiles, units so far
+            for (int k = 0; k * G < p.units && ok; ++k) {
+                const int u = unit_at(k, c, G);
+                if (u >= p.units) continue;
+                const Work w = work_of(p, u);
+                // this unit's Q is in TMEM
+                if (!mbar_wait(q_ready, n & 1, abort, &g_tc_attn_err)) break;
+                ++n;
+                for (int j = 0; j < w.nt; ++j, ++T) {
+                    const int ks = T % KST;
+                    if (!mbar_wait(&k_full[ks], (T / KST) & 1, abort, &g_tc_attn_err)) {
+                        ok = false;
+                        break;
+                    }
+                    // S buffer T & 1 last held P_{T-2}: P.V_{T-2} must have read it
+                    if (T >= 2 && !mbar_wait(&pv_done[T & 1], ((T - 2) >> 1) & 1, abort, &g_tc_attn_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t s_tm = tmem + (T & 1) * 128;
+                    const uint8_t *kd = sK + ks * K_BYTES;
 #pragma unroll
-                for (int kb = 0; kb < 3; ++kb) {
-                    const uint64_t db = sdesc_kmajor(kd + kb * BOX);
+                    for (int kb = 0; kb < 3; ++kb) {
+                        const uint64_t db = sdesc_kmajor(kd + kb * BOX);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ts(s_tm, tmem + T_Q + (kb * 4 + k) * 8, db + 2 * k, p.idesc_s, (kb | k) != 0);
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            mma_ts(s_tm, tmem + T_Q + (kb * 4 + k4) * 8, db + 2 * k4, p.idesc_s, (kb | k4) != 0);
+                    }
+                    mma_commit(&s_full[T & 1]);
+                    mma_commit(&k_empty[ks]);
                 }
-                mma_commit(&s_full[t & 1]);
-                mma_commit(&k_empty[ks]);
             }
         }
     } else if (warp == 3 + NSM) {
         // ------------------------------------------------------------ P.V issuer
         if (lane == 0) {
-            for (int t = 0; t < nt; ++t) {
-                const int vs = t % VST;
-                if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort, &g_tc_attn_err)) break;
-                if (!mbar_wait(&v_full[vs], (t / VST) & 1, abort, &g_tc_attn_err)) break;
-                tc_fence_after();
-                const uint32_t p_tm = tmem + (t & 1) * 128;
-                const uint8_t *vd = sV + vs * V_BYTES;
+            bool ok = true;
+            int T = 0, n = 0;
+            for (int k = 0; k * G < p.units && ok; ++k) {
+                const int u = unit_at(k, c, G);
+                if (u >= p.units) continue;
+                const Work w = work_of(p, u);
+                // the epilogue of the previous unit has read O before P.V_0 overwrites it
+                if (n > 0 && !mbar_wait(o_free, (n - 1) & 1, abort, &g_tc_attn_err)) break;
+                ++n;
+                for (int j = 0; j < w.nt; ++j, ++T) {
+                    const int vs = T % VST;
+                    if (!mbar_wait(&p_full[T & 1], (T >> 1) & 1, abort, &g_tc_attn_err) ||
+                        !mbar_wait(&v_full[vs], (T / VST) & 1, abort, &g_tc_attn_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t p_tm = tmem + (T & 1) * 128;
+                    const uint8_t *vd = sV + vs * V_BYTES;
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    const uint64_t db = sdesc_kmajor(vd + kb * BOX);
+                    for (int kb = 0; kb < 2; ++kb) {
+                        const uint64_t db = sdesc_kmajor(vd + kb * BOX);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ts(tmem + T_O, p_tm + kb * 32 + k * 8, db + 2 * k, p.idesc_pv, (t | kb | k) != 0);
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            mma_ts(tmem + T_O, p_tm + kb * 32 + k4 * 8, db + 2 * k4, p.idesc_pv, (j | kb | k4) != 0);
+                    }
+                    mma_commit(&v_empty[vs]);
+                    mma_commit(&pv_done[T & 1]);
+                    mma_commit(o_done);
                 }
-                mma_commit(&v_empty[vs]);
-                mma_commit(&pv_done[t & 1]);
-                mma_commit(o_done);
+                mma_commit(o_final);
             }
-            mma_commit(o_final);
         }
     } else if (warp >= 2 && warp < 2 + NSM) {
         // ---------------------------------------------------------- softmax warps
@@ -220,170 +286,217 @@ __global__ void __launch_bounds__(640, 1)
         // memory once per tile.
         const int quad = warp & 3, qr = (warp - 2) >> 2;
         const int row = quad * 32 + lane;
-        const int pos = p.q_offset + q0 + row;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        // ---- this row's Q into TMEM: quarter qr widens q_nope dims [32 qr, 32 qr + 32)
-        // to fp16 (columns 16 qr ...); quarters 0 and 1 also rotate the RoPE pairs
-        // (t, t + 32) for t in [16 qr, 16 qr + 16) (q dims 128 + t and 160 + t: columns
-        // 64 + 8 qr ... and 80 + 8 qr ...).  Rows past s_q get zeros.
-        {
-            const int qi = q0 + row;
-            uint32_t qn[16], ra8[8], rb8[8];
+        // A failed wait clears `ok` (warp-uniform) but never leaves the loops early:
+        // every softmax thread passes the same named barriers, so an abort cannot strand
+        // one.
+        bool ok = true;
+        int T = 0, n = 0;
+        // q_nope / q_pe of a unit's row (HBM): read ahead, during the previous unit's
+        // epilogue; the RoPE table (L2) is read when the unit starts
+        uint4 qv[4], xa[2], xb[2];
+        auto read_q = [&](int u) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) qn[e] = 0u;
+            for (int e = 0; e < 4; ++e) qv[e] = make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ra8[e] = rb8[e] = 0u;
-            if (qi < p.s_q) {
-                const long qrow = ((long)b * p.s_q + qi) * p.n_hq + hq;
-                const uint4 *src = (const uint4 *)(p.q_nope + qrow * 128 + qr * 32);
+            for (int e = 0; e < 2; ++e) xa[e] = xb[e] = make_uint4(0, 0, 0, 0);
+            if (u >= p.units) return;
+            const Work w = work_of(p, u);
+            const int qi = w.q0 + row;
+            if (qi >= p.s_q) return;
+            const long qrow = ((long)w.b * p.s_q + qi) * p.n_hq + p.head_off + w.hl;
+            const uint4 *src = (const uint4 *)(p.q_nope + qrow * 128 + qr * 32);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v = src[c];
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            for (int e = 0; e < 4; ++e) qv[e] = src[e];
+            if (qr < 2) {
+                const uint4 *pe = (const uint4 *)(p.q_pe + qrow * 64 + qr * 16);
+                xa[0] = pe[0];
+                xa[1] = pe[1];
+                xb[0] = pe[4];   // elements 32 + 16 qr ...
+                xb[1] = pe[5];
+            }
+        };
+        // this CTA's units in order: round k, skipping rounds past the end
+        auto next_unit = [&](int k) -> int {
+            for (; k * G < p.units; ++k)
+                if (unit_at(k, c, G) < p.units) return k;
+            return k;
+        };
+        int k = next_unit(0);
+        if (k * G < p.units) read_q(unit_at(k, c, G));
+        for (; k * G < p.units; k = next_unit(k + 1)) {
+            const int u = unit_at(k, c, G);
+            const Work w = work_of(p, u);
+            const int hq = p.head_off + w.hl, b = w.b, q0 = w.q0, nt = w.nt;
+            const int pos = p.q_offset + q0 + row;
+            // ---- this row's Q into TMEM (the previous unit's score MMAs have all completed:
+            // their S tiles were read below).  Quarter qr widens q_nope dims [32 qr, 32 qr +
+            // 32) to fp16 (columns 16 qr ...); quarters 0 and 1 also rotate the RoPE pairs
+            // (t, t + 32) for t in [16 qr, 16 qr + 16) (q dims 128 + t and 160 + t: columns
+            // 64 + 8 qr ... and 80 + 8 qr ...).  Rows past s_q get zeros.
+            {
+                const int qi = q0 + row;
+                float4 cs[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) cs[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (qi < p.s_q && qr < 2) {
+                    const float4 *tb = (const float4 *)(p.tab + (long)(p.q_offset + qi) * 32 + qr * 16);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cs[e] = tb[e];
+                }
+                uint32_t qn[16], ra8[8], rb8[8];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint32_t wv[4] = {qv[cc].x, qv[cc].y, qv[cc].z, qv[cc].w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        qn[4 * c + i] = pack_f16(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+                        qn[4 * cc + i] = pack_f16(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xffff0000u));
                 }
-                if (qr < 2) {
-                    const __nv_bfloat16 *pe = p.q_pe + qrow * 64 + qr * 16;
-                    const uint4 xa[2] = {((const uint4 *)pe)[0], ((const uint4 *)pe)[1]};
-                    const uint4 xb[2] = {((const uint4 *)(pe + 32))[0], ((const uint4 *)(pe + 32))[1]};
-                    const float4 *cs = (const float4 *)(p.tab + (long)(p.q_offset + qi) * 32 + qr * 16);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t wa[4] = {xa[h].x, xa[h].y, xa[h].z, xa[h].w};
-                        const uint32_t wb[4] = {xb[h].x, xb[h].y, xb[h].z, xb[h].w};
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t wa[4] = {xa[h].x, xa[h].y, xa[h].z, xa[h].w};
+                    const uint32_t wb[4] = {xb[h].x, xb[h].y, xb[h].z, xb[h].w};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {   // elements 8h + 2k, 8h + 2k + 1 of this part
-                            const float4 r = cs[h * 4 + k];   // (cos, sin) of both elements
-                            const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
-                            const float b0 = __uint_as_float(wb[k] << 16), b1 = __uint_as_float(wb[k] & 0xffff0000u);
-                            ra8[4 * h + k] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
-                            rb8[4 * h + k] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
-                        }
+                    for (int k2 = 0; k2 < 4; ++k2) {   // elements 8h + 2k2, +1 of this part
+                        const float4 r = cs[h * 4 + k2];   // (cos, sin) of both elements
+                        const float a0 = __uint_as_float(wa[k2] << 16), a1 = __uint_as_float(wa[k2] & 0xffff0000u);
+                        const float b0 = __uint_as_float(wb[k2] << 16), b1 = __uint_as_float(wb[k2] & 0xffff0000u);
+                        ra8[4 * h + k2] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
+                        rb8[4 * h + k2] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
                     }
                 }
-            }
-            tmem_st16(lane_base + T_Q + qr * 16, qn);
-            if (qr < 2) {   // warp-uniform
-                tmem_st8(lane_base + T_Q + 64 + qr * 8, ra8);
-                tmem_st8(lane_base + T_Q + 80 + qr * 8, rb8);
-            }
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q_ready);
-
-        // A failed wait clears `ok` (warp-uniform) but never leaves the loop early: every
-        // softmax thread passes the same named barriers, so an abort cannot strand one.
-        bool ok = true;
-        float m = -INFINITY, l = 0.f;
-        for (int j = 0; j < nt; ++j) {
-            const int sb = j & 1;
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[sb], (j >> 1) & 1, abort, &g_tc_attn_err));
-            tc_fence_after();
-            uint32_t sr[32];
-            if (ok) {
-                tmem_ld32(lane_base + sb * 128 + qr * 32, sr);
-                tmem_ld_wait();
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sr[i] = 0u;
-            }
-            const int j0 = j * BKV + qr * 32;
-            const bool masked = (j0 + 32 > p.kv_need) || (p.causal && j0 + 31 > p.q_offset + q0);
-            float x[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sr[c]);
-            if (masked) {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int key = j0 + c;
-                    if (key >= p.kv_need || (p.causal && key > pos)) x[c] = -INFINITY;
+                tmem_st16(lane_base + T_Q + qr * 16, qn);
+                if (qr < 2) {   // warp-uniform
+                    tmem_st8(lane_base + T_Q + 64 + qr * 8, ra8);
+                    tmem_st8(lane_base + T_Q + 80 + qr * 8, rb8);
                 }
-            }
-            // independent accumulators: the reductions are latency chains otherwise
-            float mx[4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) mx[a] = x[a];
-#pragma unroll
-            for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], x[c]);
-            const float ml = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            // all four quarters have read their S columns before any writes P over them
-            red[sb][qr][row] = ml;
-            named_bar_sync(1, 32 * NSM);
-            const float mt =
-                fmaxf(fmaxf(red[sb][0][row], red[sb][1][row]), fmaxf(red[sb][2][row], red[sb][3][row])) * p.scale_log2;
-            const float m_new = fmaxf(m, mt);
-            const bool need = m_new > m + RESCALE_LOG2;   // also true on the first finite maximum
-            if (__any_sync(0xffffffffu, need)) {
-                const float m_use = need ? m_new : m;
-                const float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_use);
-                if (j > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (j - 1) & 1, abort, &g_tc_attn_err));
-                if (j > 0 && ok) {
-                    tc_fence_after();
-                    uint32_t o[32];
-                    tmem_ld32(lane_base + T_O + qr * 32, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(lane_base + T_O + qr * 32, o);
-                    tmem_st_wait();
-                }
-                l *= alpha;
-                m = m_use;
-            }
-            const float nm = (m == -INFINITY) ? 0.f : -m;
-            float ra[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float p0 = ex2(fmaf(x[2 * i], p.scale_log2, nm));
-                const float p1 = ex2(fmaf(x[2 * i + 1], p.scale_log2, nm));
-                ra[i & 3] += p0 + p1;
-                pk[i] = pack_f16(p0, p1);
-            }
-            const float rs = (ra[0] + ra[1]) + (ra[2] + ra[3]);
-            if (ok) {
-                tmem_st16(lane_base + sb * 128 + qr * 16, pk);
                 tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
-            l += rs;
-        }
-        // ---- epilogue: combine the quarters' row sums (own exchange array: a slower
-        // quarter may still be reading the last tile's maxima); each stores 32 columns
-        lred[qr][row] = l;
-        named_bar_sync(1, 32 * NSM);
-        l = (lred[0][row] + lred[1][row]) + (lred[2][row] + lred[3][row]);
-        if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, &g_tc_attn_err);
-        tc_fence_after();
-        const int qi = q0 + row;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint32_t o[32];
-        if (nt > 0) {
-            tmem_ld32(lane_base + T_O + qr * 32, o);
-            tmem_ld_wait();
-        } else {
+            if (lane == 0) mbar_arrive(q_ready);
+
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < nt; ++j, ++T) {
+                const int sb = T & 1;
+                ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[sb], (T >> 1) & 1, abort, &g_tc_attn_err));
+                tc_fence_after();
+                uint32_t sr[32];
+                if (ok) {
+                    tmem_ld32(lane_base + sb * 128 + qr * 32, sr);
+                    tmem_ld_wait();
+                } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        if (ok && qi < p.s_q) {
-            uint4 *dst = (uint4 *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h + qr * 32);
+                    for (int i = 0; i < 32; ++i) sr[i] = 0u;
+                }
+                const int j0 = j * BKV + qr * 32;
+                const bool masked = (j0 + 32 > p.kv_need) || (p.causal && j0 + 31 > p.q_offset + q0);
+                float x[32];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                uint32_t w[4];
+                for (int cc = 0; cc < 32; ++cc) x[cc] = __uint_as_float(sr[cc]);
+                if (masked) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w[i] = pack_bf16(__uint_as_float(o[8 * v + 2 * i]) * inv, __uint_as_float(o[8 * v + 2 * i + 1]) * inv);
-                dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int cc = 0; cc < 32; ++cc) {
+                        const int key = j0 + cc;
+                        if (key >= p.kv_need || (p.causal && key > pos)) x[cc] = -INFINITY;
+                    }
+                }
+                // independent accumulators: the reductions are latency chains otherwise
+                float mx[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) mx[a] = x[a];
+#pragma unroll
+                for (int cc = 4; cc < 32; ++cc) mx[cc & 3] = fmaxf(mx[cc & 3], x[cc]);
+                const float ml = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                // all four quarters have read their S columns before any writes P over them
+                red[sb][qr][row] = ml;
+                named_bar_sync(1, 32 * NSM);
+                const float mt =
+                    fmaxf(fmaxf(red[sb][0][row], red[sb][1][row]), fmaxf(red[sb][2][row], red[sb][3][row])) *
+                    p.scale_log2;
+                const float m_new = fmaxf(m, mt);
+                const bool need = m_new > m + RESCALE_LOG2;   // also true on the first finite maximum
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_use = need ? m_new : m;
+                    const float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_use);
+                    // O holds this unit's sum only after its first P.V; before that it is
+                    // overwritten (accumulate off), so there is nothing to rescale
+                    if (j > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (T - 1) & 1, abort, &g_tc_attn_err));
+                    if (j > 0 && ok) {
+                        tc_fence_after();
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + T_O + qr * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(lane_base + T_O + qr * 32, o);
+                        tmem_st_wait();
+                    }
+                    l *= alpha;
+                    m = m_use;
+                }
+                const float nm = (m == -INFINITY) ? 0.f : -m;
+                float ra[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(x[2 * i], p.scale_log2, nm));
+                    const float p1 = ex2(fmaf(x[2 * i + 1], p.scale_log2, nm));
+                    ra[i & 3] += p0 + p1;
+                    pk[i] = pack_f16(p0, p1);
+                }
+                const float rs = (ra[0] + ra[1]) + (ra[2] + ra[3]);
+                if (ok) {
+                    tmem_st16(lane_base + sb * 128 + qr * 16, pk);
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[sb]);
+                l += rs;
             }
-            if (qr == 0)
-                p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] =
-                    l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            // ---- epilogue: combine the quarters' row sums (own exchange array: a slower
+            // quarter may still be reading the last tile's maxima); each stores 32 columns
+            lred[qr][row] = l;
+            named_bar_sync(1, 32 * NSM);
+            l = (lred[0][row] + lred[1][row]) + (lred[2][row] + lred[3][row]);
+            {
+                const int kn = next_unit(k + 1);
+                read_q(kn * G < p.units ? unit_at(kn, c, G) : p.units);
+            }
+            if (nt > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_final, n & 1, abort, &g_tc_attn_err));
+            tc_fence_after();
+            const int qi = q0 + row;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint32_t o[32];
+            if (nt > 0) {
+                tmem_ld32(lane_base + T_O + qr * 32, o);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);   // the next unit's P.V_0 may overwrite O
+            // the row-sum array is rewritten by the next unit only after its first tile's
+            // barrier, which every quarter reaches after reading it here
+            if (ok && qi < p.s_q) {
+                uint4 *dst = (uint4 *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h + qr * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        wv[i] = pack_bf16(__uint_as_float(o[8 * v + 2 * i]) * inv,
+                                          __uint_as_float(o[8 * v + 2 * i + 1]) * inv);
+                    dst[v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+                if (qr == 0)
+                    p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] =
+                        l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            }
+            ++n;
         }
     }
     tc_fence_before();
@@ -429,6 +542,9 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
     }
     e = cudaFuncSetAttribute(tc_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    int dev = 0, n_sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
 
     AttnK a;
     a.s_q = p.s_q;
@@ -468,7 +584,11 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
         if ((e = tc_gemm_group(kv, 2, true, st)) != cudaSuccess) return e;
         a.head_off = h0;
         a.nh = nh;
-        dim3 grid(nh * p.B, (p.s_q + BQ - 1) / BQ), block(32 * (NSM + 4));
+        a.nb = p.B;
+        a.n_qt = (p.s_q + BQ - 1) / BQ;
+        a.units = nh * p.B * a.n_qt;
+        // persistent: one CTA per SM walks the units
+        dim3 grid(std::min(a.units, n_sms)), block(32 * (NSM + 4));
         {
             ProfScope ps("tc_attn", st);
             tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mK, mKr, mV, a);
