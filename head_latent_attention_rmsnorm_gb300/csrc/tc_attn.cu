@@ -153,12 +153,16 @@ __global__ void __launch_bounds__(640, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;   // S0: cols 0-127, S1: 128-255, O: 256-383, Q: 384-479
+    // The prologue overlaps the reconstruction GEMM (programmatic launch).  Every role
+    // waits for it (pdl_wait) before touching K_nope, V^T, the rotated k_pe or the RoPE
+    // table; the softmax warps first read their first unit's q rows, which are inputs.
 
     // Every role walks the same units in the same order and counts key tiles T across
     // units, so ring slots and barrier parities continue from one unit to the next.
     if (warp == 0) {
         // ------------------------------------------------------- K tiles (TMA)
         if (lane == 0) {
+            pdl_wait();
             tma_prefetch_desc(&mK);
             tma_prefetch_desc(&mKr);
             bool ok = true;
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(640, 1)
     } else if (warp == 2 + NSM) {
         // ----------------------------------------------------- V^T tiles (TMA)
         if (lane == 0) {
+            pdl_wait();
             tma_prefetch_desc(&mV);
             bool ok = true;
             int T = 0;
@@ -207,6 +212,7 @@ __global__ void __launch_bounds__(640, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------- score MMA issuer
         if (lane == 0) {
+            pdl_wait();
             bool ok = true;
             int T = 0, n = 0;   // key tiles, units so far
             for (int k = 0; k * G < p.units && ok; ++k) {
@@ -245,6 +251,7 @@ __global__ void __launch_bounds__(640, 1)
     } else if (warp == 3 + NSM) {
         // ------------------------------------------------------------ P.V issuer
         if (lane == 0) {
+            pdl_wait();
             bool ok = true;
             int T = 0, n = 0;
             for (int k = 0; k * G < p.units && ok; ++k) {
@@ -324,6 +331,7 @@ __global__ void __launch_bounds__(640, 1)
         };
         int k = next_unit(0);
         if (k * G < p.units) read_q(unit_at(k, c, G));
+        pdl_wait();
         for (; k * G < p.units; k = next_unit(k + 1)) {
             const int u = unit_at(k, c, G);
             const Work w = work_of(p, u);
@@ -591,9 +599,19 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
         dim3 grid(std::min(a.units, n_sms)), block(32 * (NSM + 4));
         {
             ProfScope ps("tc_attn", st);
-            tc_attn_kernel<<<grid, block, SMEM_BYTES, st>>>(mK, mKr, mV, a);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = grid;
+            cfg.blockDim = block;
+            cfg.dynamicSmemBytes = SMEM_BYTES;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the GEMM's tail
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, tc_attn_kernel, mK, mKr, mV, a);
         }
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

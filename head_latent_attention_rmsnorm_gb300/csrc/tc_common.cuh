@@ -213,6 +213,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------ programmatic dependent launch ----
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel of the stream is still running; pdl_wait() blocks until that kernel
+// has completed and its memory is visible (a no-op for an ordinary launch), and
+// pdl_launch_dependents() lets the next such kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ clusters ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

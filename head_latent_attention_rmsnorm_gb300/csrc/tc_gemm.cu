@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the prologue above overlaps the previous kernel; its outputs are read below
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -250,8 +253,17 @@ cudaError_t launch_gemm(const CUtensorMap *maps, const GemmK &p, cudaStream_t st
     if (e != cudaSuccess) return e;
     // 64-wide tiles need 97 KB of shared memory and 128 TMEM columns: two CTAs per SM
     const int grid = std::min(p.total, num_sms() * (BN == 64 ? 2 : 1));
-    tc_gemm_kernel<BN, NISS><<<grid, 256, sm, st>>>(maps[0], maps[1], maps[2], maps[3], p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the previous kernel's tail
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, NISS>, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 }  // namespace
