@@ -51,14 +51,20 @@ using namespace tc;
 constexpr int BQ = 128, BKV = 128;
 constexpr uint32_t BOX = 128 * 128;            // one 128-row x 64-element fp16 box
 constexpr uint32_t K_BYTES = 3 * BOX;          // K_nope lo, K_nope hi, RoPE band
-constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halves
+constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halves (what the TMA brings)
+// Each V^T box is followed by 16 constant rows (a row of ones, 15 of zeros): the P.V MMA
+// runs with N = 144, so O column 128 accumulates the row sum of P exactly as the MMA used
+// it, and the softmax needs no sum of its own.
+constexpr uint32_t ONES = 16 * 128;
+constexpr uint32_t VBOX = BOX + ONES;          // one key half of a V slot
+constexpr uint32_t V_SLOT = 2 * VBOX;
 constexpr int KST = 3, VST = 2;
 constexpr int NSM = 16;                       // softmax warps: four threads per query row
-// K/V rings, 1 KB alignment slack, 256 B of barriers, row-max exchange [2][4][BQ] and
-// row-sum exchange [4][BQ]
-constexpr uint32_t SMEM_BYTES = KST * K_BYTES + VST * V_BYTES + 1024 + 256 + 4 * (2 * 4 + 4) * BQ;
-// TMEM columns: S buffers 0-127 and 128-255, O 256-383, Q (192 fp16 = 96 columns) 384-479
-constexpr uint32_t T_O = 256, T_Q = 384;
+// K/V rings, 1 KB alignment slack, 256 B of barriers, row-max exchange [2][4][BQ]
+constexpr uint32_t SMEM_BYTES = KST * K_BYTES + VST * V_SLOT + 1024 + 256 + 4 * (2 * 4) * BQ;
+// TMEM columns: S buffers 0-127 and 128-255, O 256-399 (dv 0-127, row sum 128, zeros),
+// Q (192 fp16 = 96 columns) 400-495
+constexpr uint32_t T_O = 256, T_L = T_O + 128, T_Q = 400;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct AttnK {
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(640, 1)
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sK = smem;
     uint8_t *sV = sK + KST * K_BYTES;
-    uint64_t *bars = (uint64_t *)(sV + VST * V_BYTES);
+    uint64_t *bars = (uint64_t *)(sV + VST * V_SLOT);
     uint64_t *q_ready = bars + 0;
     uint64_t *k_full = bars + 1, *k_empty = k_full + KST;
     uint64_t *v_full = k_empty + KST, *v_empty = v_full + VST;
@@ -118,7 +124,6 @@ __global__ void __launch_bounds__(640, 1)
     uint64_t *o_done = pv_done + 2, *o_final = o_done + 1, *o_free = o_final + 1;
     uint32_t *tslot = (uint32_t *)(bars + 24);
     float (*red)[4][BQ] = (float (*)[4][BQ])(bars + 32);   // [tile parity][quarter][row] partial maxima
-    float (*lred)[BQ] = (float (*)[BQ])((float *)(bars + 32) + 2 * 4 * BQ);   // [quarter][row] row sums
     volatile int *abort = (volatile int *)(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -149,6 +154,14 @@ __global__ void __launch_bounds__(640, 1)
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
+    // the constant rows after every V^T box: row 0 ones (fp16 1.0), rows 1-15 zeros (a
+    // row that is constant is unchanged by the 128-byte swizzle)
+    for (int i = tid; i < VST * 2 * (int)(ONES / 16); i += blockDim.x) {
+        const int box = i / (ONES / 16), off = i % (ONES / 16);   // 16-byte chunk of the block
+        const uint32_t v = off < 8 ? 0x3c003c00u : 0u;             // first 128-byte row: ones
+        *(uint4 *)(sV + (box >> 1) * V_SLOT + (box & 1) * VBOX + BOX + off * 16) = make_uint4(v, v, v, v);
+    }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -202,10 +215,10 @@ __global__ void __launch_bounds__(640, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t *vd = sV + vs * V_BYTES;
+                    uint8_t *vd = sV + vs * V_SLOT;
                     mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
                     tma_load_3d(vd, &mV, &v_full[vs], j * BKV, w.hl * 128, w.b);
-                    tma_load_3d(vd + BOX, &mV, &v_full[vs], j * BKV + 64, w.hl * 128, w.b);
+                    tma_load_3d(vd + VBOX, &mV, &v_full[vs], j * BKV + 64, w.hl * 128, w.b);
                 }
             }
         }
@@ -270,10 +283,10 @@ __global__ void __launch_bounds__(640, 1)
                     }
                     tc_fence_after();
                     const uint32_t p_tm = tmem + (T & 1) * 128;
-                    const uint8_t *vd = sV + vs * V_BYTES;
+                    const uint8_t *vd = sV + vs * V_SLOT;
 #pragma unroll
                     for (int kb = 0; kb < 2; ++kb) {
-                        const uint64_t db = sdesc_kmajor(vd + kb * BOX);
+                        const uint64_t db = sdesc_kmajor(vd + kb * VBOX);   // 144 rows: V^T + constant rows
 #pragma unroll
                         for (int k4 = 0; k4 < 4; ++k4)
                             mma_ts(tmem + T_O, p_tm + kb * 32 + k4 * 8, db + 2 * k4, p.idesc_pv, (j | kb | k4) != 0);
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(640, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(q_ready);
 
-            float m = -INFINITY, l = 0.f;
+            float m = -INFINITY;
             for (int j = 0; j < nt; ++j, ++T) {
                 const int sb = T & 1;
                 ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[sb], (T >> 1) & 1, abort, &g_tc_attn_err));
@@ -438,22 +451,20 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                         tmem_st32(lane_base + T_O + qr * 32, o);
+                        if (qr == 0) {   // the row sum is rescaled with the row (warp-uniform)
+                            const uint32_t lv = tmem_ld1(lane_base + T_L);
+                            tmem_ld_wait();
+                            tmem_st1(lane_base + T_L, __float_as_uint(__uint_as_float(lv) * alpha));
+                        }
                         tmem_st_wait();
                     }
-                    l *= alpha;
                     m = m_use;
                 }
                 const float nm = (m == -INFINITY) ? 0.f : -m;
-                float ra[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(x[2 * i], p.scale_log2, nm));
-                    const float p1 = ex2(fmaf(x[2 * i + 1], p.scale_log2, nm));
-                    ra[i & 3] += p0 + p1;
-                    pk[i] = pack_f16(p0, p1);
-                }
-                const float rs = (ra[0] + ra[1]) + (ra[2] + ra[3]);
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_f16(ex2(fmaf(x[2 * i], p.scale_log2, nm)), ex2(fmaf(x[2 * i + 1], p.scale_log2, nm)));
                 if (ok) {
                     tmem_st16(lane_base + sb * 128 + qr * 16, pk);
                     tmem_st_wait();
@@ -461,13 +472,8 @@ __global__ void __launch_bounds__(640, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[sb]);
-                l += rs;
             }
-            // ---- epilogue: combine the quarters' row sums (own exchange array: a slower
-            // quarter may still be reading the last tile's maxima); each stores 32 columns
-            lred[qr][row] = l;
-            named_bar_sync(1, 32 * NSM);
-            l = (lred[0][row] + lred[1][row]) + (lred[2][row] + lred[3][row]);
+            // ---- epilogue: the row sum is O's column 128; each quarter stores 32 columns
             {
                 const int kn = next_unit(k + 1);
                 read_q(kn * G < p.units ? unit_at(kn, c, G) : p.units);
@@ -475,15 +481,18 @@ __global__ void __launch_bounds__(640, 1)
             if (nt > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_final, n & 1, abort, &g_tc_attn_err));
             tc_fence_after();
             const int qi = q0 + row;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
             uint32_t o[32];
+            float l = 0.f;
             if (nt > 0) {
                 tmem_ld32(lane_base + T_O + qr * 32, o);
+                const uint32_t lv = tmem_ld1(lane_base + T_L);
                 tmem_ld_wait();
+                l = __uint_as_float(lv);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = 0u;
             }
+            const float inv = l > 0.f ? 1.f / l : 0.f;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);   // the next unit's P.V_0 may overwrite O
@@ -568,7 +577,7 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
     a.lse_b = (long)p.head_count * p.s_q;
     a.lse_h = p.s_q;
     a.idesc_s = idesc_f16(128, 128, true);
-    a.idesc_pv = idesc_f16(128, 128, true);
+    a.idesc_pv = idesc_f16(128, 144, true);   // 128 dv columns + the row-sum column block
     a.q_nope = (const __nv_bfloat16 *)q_nope;
     a.q_pe = (const __nv_bfloat16 *)q_pe;
     a.n_hq = p.head_count;
