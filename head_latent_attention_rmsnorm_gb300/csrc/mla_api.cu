@@ -145,9 +145,8 @@ PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
     const size_t es = ty_size(p.tmid);
     w.chat = c.take((size_t)p.B * p.kv_pad * p.Dk * es);
     w.kpe = c.take((size_t)p.B * p.kv_pad * p.Dr * es);
-    // the explicit tensor-core path rotates q_pe inside its attention kernel
-    const bool fused = p.tc && !absorbed;
-    if (!fused) w.qpe = c.take((size_t)p.B * p.s_q * p.head_count * p.Dr * es);
+    const bool fused = p.tc && !absorbed;   // the explicit tensor-core path
+    w.qpe = c.take((size_t)p.B * p.s_q * p.head_count * p.Dr * es);
     w.rtab = (float2 *)c.take((size_t)rope_positions(p) * (p.Dr / 2) * sizeof(float2));
     // fp16 W_kv_b rows: all heads of the call (explicit), one shard (absorbed transposes)
     if (p.tc) w.w16 = c.take((size_t)(fused ? p.head_count : p.hs) * (p.Dn + p.Dv) * p.Dk * 2);
@@ -193,12 +192,13 @@ mla_status prefill_prep(const Prefill &p, bool absorbed, const mla_dims *d, cons
                         const void *k_pe, const void *w_kv_b, const void *rms_w, const PrefillWs &w,
                         cudaStream_t st) {
     if (p.tc && !absorbed) {
-        // one launch: table, normalised latent, rotated k_pe and the fp16 weight copy
+        // one launch: table, normalised latent, rotated k_pe and q_pe, fp16 weight copy
         const long Dh = p.Dn + p.Dv;
         return cuda_status(launch_prep_tc(p.B, p.s_kv, (int)p.kv_need, (int)p.kv_pad, p.Dk, rope_positions(p),
                                           d->rope_base, c_kv, k_pe, rms_w, d->rms_eps, w.rtab, w.chat, w.kpe,
                                           (const char *)w_kv_b + (size_t)p.head_begin * Dh * p.Dk * 2, w.w16,
-                                          (long)p.head_count * Dh * p.Dk, st));
+                                          (long)p.head_count * Dh * p.Dk, q_pe, w.qpe, p.s_q, p.q_offset,
+                                          p.head_count, st));
     }
     MLA_TRY(launch_rope_table(0, rope_positions(p), p.Dr, d->rope_base, w.rtab, st));
     MLA_TRY(launch_latent_prep(p.tin, p.tmid, p.B, p.s_kv, (int)p.kv_need, (int)p.kv_pad, p.Dk, p.Dr, c_kv, k_pe,
@@ -582,8 +582,8 @@ mla_status prefill_entry(bool absorbed, const mla_dims *dims, mla_dtype dtype, i
                     p.Dk, p.Dn, p.Dr, p.Dv, p.H, p.kv_need, scale};
         cudaError_t e = absorbed ? tc_absorbed_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.qabs,
                                                        w.olat, w.w16, cs)
-                                 : tc_explicit_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, q_pe, w.rtab,
-                                                       w.k, w.v, w.w16, cs);
+                                 : tc_explicit_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.k,
+                                                       w.v, w.w16, cs);
         return cuda_status(e);
     }
     return absorbed ? absorbed_simt(p, scale, q_nope, w_kv_b, out, lse, w, cs)

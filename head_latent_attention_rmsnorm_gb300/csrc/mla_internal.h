@@ -48,12 +48,14 @@ cudaError_t launch_convert(int tin, const void *x, int tout, void *y, long n, cu
 // Every prep step of the tensor-core explicit prefill in one launch (bf16 in, fp16
 // out; Dr == 64, Dk a multiple of 256 up to 1024): the RoPE table for positions
 // [0, n_pos), chat = RMSNorm(c_kv) * rms_w and kpe = RoPE(k_pe, j) as in
-// launch_latent_prep, and an fp16 copy of the n_w bf16 weights w_src -> w16
-// (n_w a multiple of 8).
+// launch_latent_prep, an fp16 copy of the n_w bf16 weights w_src -> w16 (n_w a multiple
+// of 8), and qpe = RoPE(q_pe) in fp16 for q rows [B][s_q][n_hq] at positions q_offset + i
+// (n_pos must cover them).
 bool prep_tc_supported(int Dk, int Dr);
 cudaError_t launch_prep_tc(int B, int s_kv, int n_rows, int pad_rows, int Dk, long n_pos, float base,
                            const void *c_kv, const void *k_pe, const void *rms_w, float eps, float2 *tab, void *chat,
-                           void *kpe, const void *w_src, void *w16, long n_w, cudaStream_t st);
+                           void *kpe, const void *w_src, void *w16, long n_w, const void *q_pe, void *qpe, int s_q,
+                           int q_offset, int n_hq, cudaStream_t st);
 
 // ------------------------------------------------------------------- SIMT path ----
 

@@ -83,8 +83,49 @@ struct PrepTc {
     uint4 *w_dst;                            // their fp16 copy
     long w_chunks;
     long row_tasks, tab_tasks, w_tasks;      // warps of each kind, in this order
+    // q_pe rows [B][s_q][n_hq][64] at positions q_offset + i, rotated into fp16 qpe
+    const __nv_bfloat16 *q_pe;
+    __half *qpe;
+    int s_q, q_offset, n_hq;
     double theta[PREP_DR / 2];
 };
+
+// RoPE of every q_pe row at position `pos` (one query index of every batch row b in
+// [b0, b1) and every head), with lane t holding (cos, sin) of frequency t.  Eight rows
+// per pass: lane l takes row l / 4 and the pairs (t, t + 32) for t in [8 (l % 4), +8),
+// as two 16-byte reads and two 16-byte writes; the eight (cos, sin) it needs are the same
+// for every row (one position) and are gathered once.
+__device__ __forceinline__ void rope_q_at(const PrepTc &a, long pos, int b0, int b1, float2 cs, int lane) {
+    const long i = pos - a.q_offset;
+    if (i < 0 || i >= a.s_q) return;   // uniform across the warp
+    const int ch = lane & 3, rsub = lane >> 2;
+    float2 r[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        r[e] = make_float2(__shfl_sync(0xffffffffu, cs.x, 8 * ch + e), __shfl_sync(0xffffffffu, cs.y, 8 * ch + e));
+    const long rows = (long)(b1 - b0) * a.n_hq;
+    for (long r0 = 0; r0 < rows; r0 += 8) {
+        const long rr = r0 + rsub;
+        if (rr >= rows) continue;
+        const int b = b0 + (int)(rr / a.n_hq), h = (int)(rr % a.n_hq);
+        const long base = (((long)b * a.s_q + i) * a.n_hq + h) * PREP_DR + 8 * ch;
+        const uint4 xa = *(const uint4 *)(a.q_pe + base), xb = *(const uint4 *)(a.q_pe + base + 32);
+        const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
+        uint32_t oa[4], ob[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {   // elements 2k, 2k + 1 of this lane's 8
+            const float a0 = __uint_as_float(wa[k] << 16), a1 = __uint_as_float(wa[k] & 0xffff0000u);
+            const float c0 = __uint_as_float(wb[k] << 16), c1 = __uint_as_float(wb[k] & 0xffff0000u);
+            const float2 r0 = r[2 * k], r1 = r[2 * k + 1];
+            __half2 lo = __floats2half2_rn(a0 * r0.x - c0 * r0.y, a1 * r1.x - c1 * r1.y);
+            __half2 hi = __floats2half2_rn(c0 * r0.x + a0 * r0.y, c1 * r1.x + a1 * r1.y);
+            oa[k] = *(uint32_t *)&lo;
+            ob[k] = *(uint32_t *)&hi;
+        }
+        *(uint4 *)(a.qpe + base) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+        *(uint4 *)(a.qpe + base + 32) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    }
+}
 
 __device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -102,6 +143,7 @@ __global__ void prep_tc_kernel(const __grid_constant__ PrepTc a) {
         const long b = g / a.pad_rows, j = g % a.pad_rows;
         const float2 cs = rope_cs(j, a.theta[lane]);
         if (b == 0 && j < a.n_pos) a.tab[j * (PREP_DR / 2) + lane] = cs;
+        if (a.qpe) rope_q_at(a, j, (int)b, (int)b + 1, cs, lane);
         const int Dk = a.Dk, nc = Dk / 256;
         uint4 *y = (uint4 *)(a.chat + g * Dk);
         __half *kp = a.kpe + g * PREP_DR;
@@ -148,7 +190,9 @@ __global__ void prep_tc_kernel(const __grid_constant__ PrepTc a) {
         kp[lane + 32] = __float2half_rn(x1 * cs.x + x0 * cs.y);
     } else if ((g -= a.row_tasks) < a.tab_tasks) {
         const long pos = a.pad_rows + g;
-        a.tab[pos * (PREP_DR / 2) + lane] = rope_cs(pos, a.theta[lane]);
+        const float2 cs = rope_cs(pos, a.theta[lane]);
+        a.tab[pos * (PREP_DR / 2) + lane] = cs;
+        if (a.qpe) rope_q_at(a, pos, 0, a.B, cs, lane);
     } else if ((g -= a.tab_tasks) < a.w_tasks) {
         const long c0 = g * 32 * PREP_W_PER_LANE + lane;
 #pragma unroll
@@ -565,7 +609,8 @@ bool prep_tc_supported(int Dk, int Dr) { return Dr == PREP_DR && Dk % 256 == 0 &
 
 cudaError_t launch_prep_tc(int B, int s_kv, int n_rows, int pad_rows, int Dk, long n_pos, float base,
                            const void *c_kv, const void *k_pe, const void *rms_w, float eps, float2 *tab, void *chat,
-                           void *kpe, const void *w_src, void *w16, long n_w, cudaStream_t st) {
+                           void *kpe, const void *w_src, void *w16, long n_w, const void *q_pe, void *qpe, int s_q,
+                           int q_offset, int n_hq, cudaStream_t st) {
     PrepTc a;
     a.B = B;
     a.s_kv = s_kv;
@@ -583,6 +628,11 @@ cudaError_t launch_prep_tc(int B, int s_kv, int n_rows, int pad_rows, int Dk, lo
     a.w_src = (const uint4 *)w_src;
     a.w_dst = (uint4 *)w16;
     a.w_chunks = n_w / 8;
+    a.q_pe = (const __nv_bfloat16 *)q_pe;
+    a.qpe = (__half *)qpe;
+    a.s_q = s_q;
+    a.q_offset = q_offset;
+    a.n_hq = n_hq;
     a.row_tasks = (long)B * pad_rows;
     a.tab_tasks = n_pos > pad_rows ? n_pos - pad_rows : 0;
     a.w_tasks = (a.w_chunks + 32 * PREP_W_PER_LANE - 1) / (32 * PREP_W_PER_LANE);

@@ -25,11 +25,11 @@ bool tc_decode_supported(int Dk, int Dn, int Dr, int Dv, int H);
 // Explicit prefill after the shared prep (fp16 chat, kpe, qpe already in the
 // workspace): per head shard, an fp16 copy of the shard's W_kv_b rows, the K_nope /
 // V^T reconstruction GEMMs and the attention kernel.
-// q_pe: the caller's un-rotated bf16 q_pe (rotated inside the attention kernel with
-// `rtab`); w16: fp16 copy of the head_count heads' W_kv_b rows [head_count][Dn+Dv][Dk].
+// qpe: the rotated q_pe in fp16 [B][s_q][head_count][64]; w16: fp16 copy of the
+// head_count heads' W_kv_b rows [head_count][Dn+Dv][Dk].
 cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
-                                float *lse, const void *chat, const void *kpe, const void *q_pe,
-                                const float2 *rtab, void *kws, void *vws, const void *w16, cudaStream_t st);
+                                float *lse, const void *chat, const void *kpe, const void *qpe, void *kws,
+                                void *vws, const void *w16, cudaStream_t st);
 cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
                                 float *lse, const void *chat, const void *kpe, const void *qpe, void *qabs,
                                 void *olat, void *w16, cudaStream_t st);

@@ -58,10 +58,11 @@ constexpr uint32_t V_BYTES = 2 * BOX;          // V^T: 128 dv rows x 2 key halve
 constexpr uint32_t ONES = 16 * 128;
 constexpr uint32_t VBOX = BOX + ONES;          // one key half of a V slot
 constexpr uint32_t V_SLOT = 2 * VBOX;
-constexpr int KST = 3, VST = 2;
+constexpr int KST = 2, VST = 2;
+constexpr uint32_t QS_BYTES = 3 * BOX;         // staged Q of the next unit: q_nope lo, hi (bf16), rotated q_pe (fp16)
 constexpr int NSM = 16;                       // softmax warps: four threads per query row
-// K/V rings, 1 KB alignment slack, 256 B of barriers, row-max exchange [2][4][BQ]
-constexpr uint32_t SMEM_BYTES = KST * K_BYTES + VST * V_SLOT + 1024 + 256 + 4 * (2 * 4) * BQ;
+// Q staging, K/V rings, 1 KB alignment slack, 256 B of barriers, row-max exchange [2][4][BQ]
+constexpr uint32_t SMEM_BYTES = QS_BYTES + KST * K_BYTES + VST * V_SLOT + 1024 + 256 + 4 * (2 * 4) * BQ;
 // TMEM columns: S buffers 0-127 and 128-255, O 256-399 (dv 0-127, row sum 128, zeros),
 // Q (192 fp16 = 96 columns) 400-495
 constexpr uint32_t T_O = 256, T_L = T_O + 128, T_Q = 400;
@@ -76,11 +77,7 @@ struct AttnK {
     float *lse;
     long lse_b, lse_h;
     uint32_t idesc_s, idesc_pv;
-    const __nv_bfloat16 *q_nope;   // [b][i][head][128]
-    const __nv_bfloat16 *q_pe;     // un-rotated q_pe [b][i][head][64]
-    int n_hq;                      // heads of the q tensors
     int nh, nb, n_qt, units;       // heads of this launch, batch, query tiles, work units
-    const float2 *tab;             // RoPE (cos, sin) of position p, frequency t at p * 32 + t
 };
 
 // One work unit = (128-query tile, head, batch).  Units are numbered heaviest first
@@ -109,19 +106,21 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(640, 1)
-    tc_attn_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
+__global__ void __launch_bounds__(32 * (NSM + 4), 1)
+    tc_attn_kernel(const __grid_constant__ CUtensorMap mQn, const __grid_constant__ CUtensorMap mQr,
+                   const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mKr,
                    const __grid_constant__ CUtensorMap mV, AttnK p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sK = smem;
+    uint8_t *sQs = smem;
+    uint8_t *sK = sQs + QS_BYTES;
     uint8_t *sV = sK + KST * K_BYTES;
     uint64_t *bars = (uint64_t *)(sV + VST * V_SLOT);
     uint64_t *q_ready = bars + 0;
     uint64_t *k_full = bars + 1, *k_empty = k_full + KST;
     uint64_t *v_full = k_empty + KST, *v_empty = v_full + VST;
     uint64_t *s_full = v_empty + VST, *p_full = s_full + 2, *pv_done = p_full + 2;
-    uint64_t *o_done = pv_done + 2, *o_final = o_done + 1, *o_free = o_final + 1;
+    uint64_t *o_done = pv_done + 2, *o_final = o_done + 1, *o_free = o_final + 1, *qs_full = o_free + 1;
     uint32_t *tslot = (uint32_t *)(bars + 24);
     float (*red)[4][BQ] = (float (*)[4][BQ])(bars + 32);   // [tile parity][quarter][row] partial maxima
     volatile int *abort = (volatile int *)(tslot + 1);
@@ -147,6 +146,7 @@ __global__ void __launch_bounds__(640, 1)
         mbar_init(o_done, 1);
         mbar_init(o_final, 1);
         mbar_init(o_free, NSM);   // the softmax warps have read O out of TMEM
+        mbar_init(qs_full, 1);    // a unit's Q has landed in the staging buffer
         *abort = 0;
         fence_mbar_init();
     }
@@ -173,17 +173,28 @@ __global__ void __launch_bounds__(640, 1)
     // Every role walks the same units in the same order and counts key tiles T across
     // units, so ring slots and barrier parities continue from one unit to the next.
     if (warp == 0) {
-        // ------------------------------------------------------- K tiles (TMA)
+        // ------------------------------- Q of each unit and K tiles (TMA)
         if (lane == 0) {
             pdl_wait();
+            tma_prefetch_desc(&mQn);
+            tma_prefetch_desc(&mQr);
             tma_prefetch_desc(&mK);
             tma_prefetch_desc(&mKr);
             bool ok = true;
-            int T = 0;
+            int T = 0, n = 0;
             for (int k = 0; k * G < p.units && ok; ++k) {
                 const int u = unit_at(k, c, G);
                 if (u >= p.units) continue;
                 const Work w = work_of(p, u);
+                // this unit's Q into the staging buffer, once the softmax warps have moved
+                // the previous unit's Q into TMEM (this runs a couple of key tiles ahead of
+                // them, so the load has that long to land)
+                if (n > 0 && !mbar_wait(q_ready, (n - 1) & 1, abort, &g_tc_attn_err)) break;
+                ++n;
+                mbar_arrive_expect_tx(qs_full, QS_BYTES);
+                tma_load_4d(sQs, &mQn, qs_full, 0, p.head_off + w.hl, w.q0, w.b);
+                tma_load_4d(sQs + BOX, &mQn, qs_full, 64, p.head_off + w.hl, w.q0, w.b);
+                tma_load_4d(sQs + 2 * BOX, &mQr, qs_full, 0, p.head_off + w.hl, w.q0, w.b);
                 for (int j = 0; j < w.nt; ++j, ++T) {
                     const int ks = T % KST;
                     if (T >= KST && !mbar_wait(&k_empty[ks], ((T / KST) - 1) & 1, abort, &g_tc_attn_err)) {
@@ -312,82 +323,46 @@ __global__ void __launch_bounds__(640, 1)
         // one.
         bool ok = true;
         int T = 0, n = 0;
-        // q_nope / q_pe of a unit's row (HBM): read ahead, during the previous unit's
-        // epilogue; the RoPE table (L2) is read when the unit starts
-        uint4 qv[4], xa[2], xb[2];
-        auto read_q = [&](int u) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) qv[e] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) xa[e] = xb[e] = make_uint4(0, 0, 0, 0);
-            if (u >= p.units) return;
-            const Work w = work_of(p, u);
-            const int qi = w.q0 + row;
-            if (qi >= p.s_q) return;
-            const long qrow = ((long)w.b * p.s_q + qi) * p.n_hq + p.head_off + w.hl;
-            const uint4 *src = (const uint4 *)(p.q_nope + qrow * 128 + qr * 32);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) qv[e] = src[e];
-            if (qr < 2) {
-                const uint4 *pe = (const uint4 *)(p.q_pe + qrow * 64 + qr * 16);
-                xa[0] = pe[0];
-                xa[1] = pe[1];
-                xb[0] = pe[4];   // elements 32 + 16 qr ...
-                xb[1] = pe[5];
-            }
-        };
         // this CTA's units in order: round k, skipping rounds past the end
         auto next_unit = [&](int k) -> int {
             for (; k * G < p.units; ++k)
                 if (unit_at(k, c, G) < p.units) return k;
             return k;
         };
-        int k = next_unit(0);
-        if (k * G < p.units) read_q(unit_at(k, c, G));
-        pdl_wait();
-        for (; k * G < p.units; k = next_unit(k + 1)) {
+        for (int k = next_unit(0); k * G < p.units; k = next_unit(k + 1)) {
             const int u = unit_at(k, c, G);
             const Work w = work_of(p, u);
             const int hq = p.head_off + w.hl, b = w.b, q0 = w.q0, nt = w.nt;
             const int pos = p.q_offset + q0 + row;
-            // ---- this row's Q into TMEM (the previous unit's score MMAs have all completed:
-            // their S tiles were read below).  Quarter qr widens q_nope dims [32 qr, 32 qr +
-            // 32) to fp16 (columns 16 qr ...); quarters 0 and 1 also rotate the RoPE pairs
-            // (t, t + 32) for t in [16 qr, 16 qr + 16) (q dims 128 + t and 160 + t: columns
-            // 64 + 8 qr ... and 80 + 8 qr ...).  Rows past s_q get zeros.
+            // ---- this row's Q from the staging buffer into TMEM (the previous unit's score
+            // MMAs have all completed: their S tiles were read below).  Quarter qr widens
+            // q_nope dims [32 qr, 32 qr + 32) to fp16 (columns 16 qr ...); quarters 0 and 1
+            // also copy the rotated q_pe elements t and t + 32 for t in [16 qr, 16 qr + 16)
+            // (columns 64 + 8 qr ... and 80 + 8 qr ...).  Rows past s_q arrive as zeros.
+            // 16-byte chunk c of row r of a staged box sits at chunk c ^ (r & 7).
             {
-                const int qi = q0 + row;
-                float4 cs[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) cs[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (qi < p.s_q && qr < 2) {
-                    const float4 *tb = (const float4 *)(p.tab + (long)(p.q_offset + qi) * 32 + qr * 16);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) cs[e] = tb[e];
-                }
-                uint32_t qn[16], ra8[8], rb8[8];
+                ok = __all_sync(0xffffffffu, ok && mbar_wait(qs_full, n & 1, abort, &g_tc_attn_err));
+                const uint8_t *qrow_s = sQs + (qr >> 1) * BOX + row * 128;
+                uint32_t qn[16];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const uint32_t wv[4] = {qv[cc].x, qv[cc].y, qv[cc].z, qv[cc].w};
+                    const uint4 v = *(const uint4 *)(qrow_s + (((4 * (qr & 1) + cc) ^ (row & 7)) << 4));
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         qn[4 * cc + i] = pack_f16(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xffff0000u));
                 }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t wa[4] = {xa[h].x, xa[h].y, xa[h].z, xa[h].w};
-                    const uint32_t wb[4] = {xb[h].x, xb[h].y, xb[h].z, xb[h].w};
-#pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2) {   // elements 8h + 2k2, +1 of this part
-                        const float4 r = cs[h * 4 + k2];   // (cos, sin) of both elements
-                        const float a0 = __uint_as_float(wa[k2] << 16), a1 = __uint_as_float(wa[k2] & 0xffff0000u);
-                        const float b0 = __uint_as_float(wb[k2] << 16), b1 = __uint_as_float(wb[k2] & 0xffff0000u);
-                        ra8[4 * h + k2] = pack_f16(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
-                        rb8[4 * h + k2] = pack_f16(b0 * r.x + a0 * r.y, b1 * r.z + a1 * r.w);
-                    }
-                }
                 tmem_st16(lane_base + T_Q + qr * 16, qn);
                 if (qr < 2) {   // warp-uniform
+                    const uint8_t *prow = sQs + 2 * BOX + row * 128;
+                    uint32_t ra8[8], rb8[8];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 va = *(const uint4 *)(prow + (((2 * qr + h) ^ (row & 7)) << 4));
+                        const uint4 vb = *(const uint4 *)(prow + (((2 * qr + 4 + h) ^ (row & 7)) << 4));
+                        ra8[4 * h] = va.x, ra8[4 * h + 1] = va.y, ra8[4 * h + 2] = va.z, ra8[4 * h + 3] = va.w;
+                        rb8[4 * h] = vb.x, rb8[4 * h + 1] = vb.y, rb8[4 * h + 2] = vb.z, rb8[4 * h + 3] = vb.w;
+                    }
                     tmem_st8(lane_base + T_Q + 64 + qr * 8, ra8);
                     tmem_st8(lane_base + T_Q + 80 + qr * 8, rb8);
                 }
@@ -474,10 +449,6 @@ __global__ void __launch_bounds__(640, 1)
                 if (lane == 0) mbar_arrive(&p_full[sb]);
             }
             // ---- epilogue: the row sum is O's column 128; each quarter stores 32 columns
-            {
-                const int kn = next_unit(k + 1);
-                read_q(kn * G < p.units ? unit_at(kn, c, G) : p.units);
-            }
             if (nt > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_final, n & 1, abort, &g_tc_attn_err));
             tc_fence_after();
             const int qi = q0 + row;
@@ -528,14 +499,30 @@ bool tc_explicit_supported(int Dk, int Dn, int Dr, int Dv) {
 }
 
 cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out, float *lse,
-                                const void *chat, const void *kpe, const void *q_pe, const float2 *rtab, void *kws,
-                                void *vws, const void *w16, cudaStream_t st) {
+                                const void *chat, const void *kpe, const void *qpe, void *kws, void *vws,
+                                const void *w16, cudaStream_t st) {
     (void)w_kv_b;   // read through its fp16 copy w16
     const long kv_pad = (p.kv_need + 127) / 128 * 128;
     const long Dh = p.Dn + p.Dv;
     cudaError_t e;
     // maps that do not change across shards
-    CUtensorMap mKr;
+    CUtensorMap mQn, mQr, mKr;
+    {
+        unsigned long long d[4] = {(unsigned long long)p.Dn, (unsigned long long)p.head_count,
+                                   (unsigned long long)p.s_q, (unsigned long long)p.B};
+        unsigned long long s[3] = {(unsigned long long)p.Dn * 2, (unsigned long long)p.head_count * p.Dn * 2,
+                                   (unsigned long long)p.s_q * p.head_count * p.Dn * 2};
+        unsigned box[4] = {64, 1, 128, 1};
+        if ((e = make_tma_map(&mQn, q_nope, 4, d, s, box)) != cudaSuccess) return e;
+    }
+    {
+        unsigned long long d[4] = {(unsigned long long)p.Dr, (unsigned long long)p.head_count,
+                                   (unsigned long long)p.s_q, (unsigned long long)p.B};
+        unsigned long long s[3] = {(unsigned long long)p.Dr * 2, (unsigned long long)p.head_count * p.Dr * 2,
+                                   (unsigned long long)p.s_q * p.head_count * p.Dr * 2};
+        unsigned box[4] = {64, 1, 128, 1};
+        if ((e = make_tma_map(&mQr, qpe, 4, d, s, box)) != cudaSuccess) return e;
+    }
     {
         unsigned long long d[3] = {(unsigned long long)p.Dr, (unsigned long long)kv_pad, (unsigned long long)p.B};
         unsigned long long s[2] = {(unsigned long long)p.Dr * 2, (unsigned long long)kv_pad * p.Dr * 2};
@@ -578,10 +565,6 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
     a.lse_h = p.s_q;
     a.idesc_s = idesc_f16(128, 128, true);
     a.idesc_pv = idesc_f16(128, 144, true);   // 128 dv columns + the row-sum column block
-    a.q_nope = (const __nv_bfloat16 *)q_nope;
-    a.q_pe = (const __nv_bfloat16 *)q_pe;
-    a.n_hq = p.head_count;
-    a.tab = rtab;
 
     TmaOperand latent{chat, p.Dk, kv_pad, p.B, (long)p.Dk * 2, kv_pad * p.Dk * 2, (int)kv_pad, 0, 1};
     for (int s = 0; s < p.n_shards; ++s) {
@@ -618,7 +601,7 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, tc_attn_kernel, mK, mKr, mV, a);
+            e = cudaLaunchKernelEx(&cfg, tc_attn_kernel, mQn, mQr, mK, mKr, mV, a);
         }
         if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     }
