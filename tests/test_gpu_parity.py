@@ -128,6 +128,20 @@ def test_ragged_bf16_noncausal_small_kv(oracle):
     check_lse(l, rl)
 
 
+@pytest.mark.parametrize("absorbed", [False, True])
+def test_ragged_bf16_noncausal_queries_past_keys(oracle, absorbed):
+    """Non-causal: 100 keys, queries at positions 120..149, i.e. past the keys and past
+    the 128-row key padding (their RoPE angles come from positions no key has)."""
+    big = dataclasses.replace(RAGGED, s_kv=160, s_q=30, q_offset=120, causal=False, batch=2)
+    inp = inputs.prefill_inputs(big)
+    inp = dict(inp, c_kv=inp["c_kv"][:, :100].contiguous(), k_pe=inp["k_pe"][:, :100].contiguous())
+    cfg = dataclasses.replace(big, s_kv=100)
+    o, l = run_prefill(cfg, dev(inp), absorbed=absorbed)
+    ro, rl = oracle_prefill(oracle, cfg, inp, absorbed=absorbed)
+    check_out(o, ro, torch.bfloat16)
+    check_lse(l, rl)
+
+
 # --------------------------------------------------------- full-size prefill ----
 def test_v2lite_full(oracle):
     cfg = configs.V2LITE
