@@ -36,7 +36,7 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max
 # summarised under profiles/ (None until the current kernel has been captured).  The
 # decode capture runs B = 8; its traffic grows in proportion to the batch, so the
 # B = 64 launch is 8x that.
-NCU_TRAFFIC = {"tc_attn": 63.00e6, "tc_latent_attn": 306.51e6 * 8}
+NCU_TRAFFIC = {"tc_attn": 63.00e6}
 
 
 def load_peaks():
@@ -310,7 +310,7 @@ def run_ours(args, world, rank, local):
                 "frac": round(ach / peak, 4), "traffic": NCU_TRAFFIC.get(kp), "peak_kind": note,
                 "launches": n, "avg_launch_us": round(ms / n * 1e3, 2),
                 "share_of_step": round(ms / (sum(v[1] for v in prof_p.values()) or 1), 3)}
-    kd = dominant(prof_d, ("tc_latent_attn", "attn_simt"))
+    kd = dominant(prof_d, ("tc_decode_attn", "attn_simt"))
     droof = None
     if kd:
         n, ms = prof_d[kd]

@@ -120,6 +120,12 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
+// Brings `bytes` (a multiple of 16, 16-byte aligned address) of global memory into
+// L2 without touching shared memory.
+__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)p), "r"(bytes) : "memory");
+}
+
 // Named barrier `id` over `n` threads (a multiple of 32) of the CTA.
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -174,6 +180,16 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// The same arrival, on the barrier at this offset in every CTA of the cluster whose
+// rank bit is set in `cta_mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane (base lane + i).
@@ -256,6 +272,20 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void *src,
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Waits until all but the newest `N` committed bulk-copy groups of this thread have
+// finished reading their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+// Waits until every committed bulk copy of this thread has completed (writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Arrive on another CTA's mbarrier and add `bytes` to the transaction count its
+// current phase waits for (the bytes of a bulk copy that will complete on it).
+__device__ __forceinline__ void mbar_arrive_expect_tx_peer(uint32_t peer_bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(peer_bar),
+                 "r"(bytes)
+                 : "memory");
+}
 
 // Orders this thread's prior memory operations (including shared::cluster stores)
 // at cluster scope.

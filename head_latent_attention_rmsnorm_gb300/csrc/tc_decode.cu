@@ -1,0 +1,555 @@
+// tc_decode.cu -- split-KV latent decode on the sm_103a tensor cores.
+//
+// Method: "A Training-Memory Regression in MLA Sequence Parallelism ... LAGA"
+// (arXiv 2607.17644), Fig. 2 absorbed dataflow and "Core claim" (the absorbed form is
+// the decode form): s_hj = scale * (q_abs_h . c_j + RoPE(q_pe_h) . RoPE(k_pe_j)),
+// o_h = sum_j softmax_j(s_hj) c_j over the latent cache; "Helix Parallelism ..."
+// (arXiv 2507.07120), "What carries the argument": each key split yields a partial
+// output and its log-sum-exp, merged afterwards by the rescale-and-sum.
+//
+// One work unit = the 128 heads of one sequence against one key split.  Its fp32
+// accumulator (128 heads x 512 latent dims) fills the whole tensor memory of an SM,
+// so a unit runs on a cluster of two CTAs with different jobs:
+//   rank 0 (scores): q_abs | RoPE(q_pe) (fp16, 576 wide) in TMEM; each 64-key tile of
+//     the cache (latent + RoPE band) arrives through a two-deep TMA ring and four warps
+//     widen it to fp16 in place; S = Q.K^T on the tensor core (A from TMEM),
+//     double-buffered in TMEM; four warps run the online
+//     softmax (one thread per head), write P in bf16 (already in the MMA operand
+//     layout) with the per-head rescale factors into a staging slot, and one bulk copy
+//     per tile moves that slot into rank 1's shared memory;
+//   rank 1 (accumulator): O (128 x 512 fp32) in all 512 TMEM columns; streams the same
+//     tiles' latent rows (an L2 hit: rank 0 prefetches the tiles into L2 ahead of
+//     use) and issues O += P.C with both operands in shared memory; four warps rescale
+//     rows of O when rank 0 reports a grown row maximum, and write the normalised
+//     partial output at the end.
+// P only flows from rank 0 to rank 1, through four slots, so rank 0 runs up to four
+// tiles ahead and the cross-CTA latency stays off the critical path.
+//
+// Precision: scores use q_abs and RoPE(q_pe) in fp16 (11-bit significand) against the
+// cache widened exactly from bf16, because a score's rounding error lands directly in
+// the log-sum-exp of a split with few keys (bf16 q_abs: ~1.4e-3 per score on N(0,1)
+// data, fp16: ~1.7e-4).  P multiplies the bf16 cache on rank 1 in bf16: its rounding
+// only perturbs the weights of an average (relative 2^-9), and the row sums use the
+// unrounded fp32 probabilities.
+//
+// Warps (320 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 MMA issuer
+// and TMEM owner, 2-5 softmax, 6-9 bf16 -> fp16 widening; rank 1 -- 0 TMA producer,
+// 1 MMA issuer and TMEM owner, 2-5 rescale + epilogue, 6-9 idle.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "mla_internal.h"
+#include "tc.h"
+#include "tc_common.cuh"
+#include "tc_internal.h"
+
+namespace mla {
+
+__device__ unsigned g_tc_decode_err = 0;
+
+namespace {
+
+using namespace tc;
+
+constexpr int ROWS = 128, NK = 64, NTHREADS = 320, NCONV = 4;
+constexpr int KST = 2;     // rank 0: key-tile stages (one per S buffer)
+constexpr int VST = 2;     // rank 1: latent-tile stages
+constexpr int NPB = 4;     // rank 1: P slots
+constexpr int PF = 6;      // tiles prefetched into L2 ahead of the TMA loads
+constexpr uint32_t BOX = NK * 128;          // 64 keys x 64 dims, bf16: 8 KB
+constexpr uint32_t KSTAGE = 9 * BOX;        // 512 latent + 64 RoPE dims
+constexpr uint32_t VSTAGE = 8 * BOX;        // 512 latent dims
+// One P transfer: P [128 heads][64 keys] bf16, K-major with the 128-byte swizzle; the
+// rescale factor of every head; 1/l of every head (meaningful on the last tile); one
+// "some head rescaled" word per softmax warp.
+constexpr uint32_t X_P = 0, X_ALPHA = 16384, X_INVL = X_ALPHA + 512, X_FLAG = X_INVL + 512;
+constexpr uint32_t X_BYTES = X_FLAG + 16;   // bytes copied per tile
+constexpr uint32_t XSLOT = 18432;           // slot stride: a multiple of the 1024-byte swizzle atom
+// rank 0: K stages then two staging slots; rank 1: V stages then the P slots.  The
+// barriers sit after both layouts, at the same offset in both CTAs (the peer addresses
+// them by offset).
+constexpr uint32_t OFF_STG = KST * KSTAGE;
+constexpr uint32_t OFF_PB = VST * VSTAGE;
+constexpr uint32_t OFF_BAR = (OFF_STG + 2 * XSLOT > OFF_PB + NPB * XSLOT) ? OFF_STG + 2 * XSLOT : OFF_PB + NPB * XSLOT;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+constexpr uint32_t T_S = 0, T_Q = 2 * NK;   // rank 0 TMEM columns: S buffers, then Q (288 columns)
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr unsigned FULL = 0xffffffffu;
+
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_STG % 1024 == 0 && OFF_PB % 1024 == 0 && XSLOT % 1024 == 0, "swizzle atoms 1024-aligned");
+static_assert(T_Q + 288 <= 512, "TMEM budget of rank 0");
+
+struct DecK {
+    int n_splits, row_tiles;
+    long chunk, kv_len;                 // keys per split, cache length
+    const __half *qa;                   // q_abs rows [b][h][512]
+    long qa_b, qa_r;
+    const __half *qp;                   // rotated q_pe rows [b][h][64]
+    long qp_b, qp_r;
+    const __nv_bfloat16 *cache, *kpe;   // [B][kv_len][512], [B][kv_len][64] (for the L2 prefetch)
+    float scale_log2;
+    float *po, *pl;                     // partials [split][b][h][512], [split][b][h]
+    long po_s, po_b, pl_s, pl_b;
+    uint32_t idesc_s, idesc_pv;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+struct Unit {
+    int b, split, r0;   // sequence, key split, first head
+    long kb, ke;        // key range [kb, ke)
+    int nt;             // 64-key tiles
+};
+
+__device__ __forceinline__ Unit unit_of(const DecK &p, int u) {
+    Unit w{};
+    w.r0 = (u % p.row_tiles) * ROWS;
+    u /= p.row_tiles;
+    w.split = u % p.n_splits;
+    w.b = u / p.n_splits;
+    w.kb = min((long)w.split * p.chunk, p.kv_len);
+    w.ke = min(w.kb + p.chunk, p.kv_len);
+    w.nt = w.ke > w.kb ? (int)((w.ke - w.kb + NK - 1) / NK) : 0;
+    return w;
+}
+
+// After an abandoned wait: give TMA loads that were already issued time to land
+// before the CTA's shared memory is released (bounded: 100 microseconds).
+__device__ void settle() {
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 100000ull) {
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR, DecK p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
+    // rank 0
+    uint64_t *k_full = bars, *k_empty = bars + 2, *s_full = bars + 4, *q_ready = bars + 6;
+    // both: P slot t % NPB consumed by the P.C MMAs of tile t (one multicast commit
+    // completes it in both CTAs)
+    uint64_t *p_empty = bars + 7;
+    // rank 1
+    uint64_t *p_full = bars + 11, *pc_ready = bars + 15, *v_full = bars + 19, *v_empty = bars + 21;
+    uint64_t *o_final = bars + 23;
+    // rank 0: tile widened and S buffer drained
+    uint64_t *c_full = bars + 24;
+    uint32_t *tslot = (uint32_t *)(bars + 26);
+    volatile int *abort = (volatile int *)(tslot + 1);
+    unsigned *err = &g_tc_decode_err;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const Unit w = unit_of(p, blockIdx.x >> 1);
+    const int nt = w.nt;
+
+    if (tid == 0) {
+        if (rank == 0) {
+            for (int s = 0; s < KST; ++s) {
+                mbar_init(&k_full[s], 1);
+                mbar_init(&k_empty[s], 1);
+                mbar_init(&s_full[s], 1);
+                mbar_init(&c_full[s], NCONV + 4);   // widening warps + one per softmax warp (S buffer free)
+            }
+            mbar_init(q_ready, 4);
+        } else {
+            for (int s = 0; s < NPB; ++s) {
+                mbar_init(&p_full[s], 1);   // this CTA's expect_tx + the bulk copy's bytes
+                mbar_init(&pc_ready[s], 4);
+            }
+            for (int s = 0; s < VST; ++s) {
+                mbar_init(&v_full[s], 1);
+                mbar_init(&v_empty[s], 1);
+            }
+            mbar_init(o_final, 1);
+        }
+        for (int s = 0; s < NPB; ++s) mbar_init(&p_empty[s], 1);
+        *abort = 0;
+        fence_mbar_init();
+        if (rank == 0) {   // both S buffers start free: the softmax warps' arrivals for tiles 0 and 1
+            for (int s = 0; s < KST; ++s)
+                for (int i = 0; i < 4; ++i) mbar_arrive(&c_full[s]);
+        } else {           // every P slot armed for its first transfer
+            for (int s = 0; s < NPB; ++s) mbar_arrive_expect_tx(&p_full[s], X_BYTES);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers exist before any cross-CTA arrival
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (rank == 0) {
+        if (warp == 0) {
+            // ---------------------------------------------- TMA producer + L2 prefetch
+            if (lane == 0 && nt > 0) {
+                tma_prefetch_desc(&mC);
+                tma_prefetch_desc(&mR);
+                auto prefetch = [&](int t) {
+                    const long key0 = w.kb + (long)t * NK;
+                    const int rows = (int)min((long)NK, p.kv_len - key0);
+                    const long row = (long)w.b * p.kv_len + key0;
+                    for (int r = 0; r < rows; r += 16)
+                        l2_prefetch(p.cache + (row + r) * 512, (uint32_t)min(16, rows - r) * 1024u);
+                    l2_prefetch(p.kpe + row * 64, (uint32_t)rows * 128u);
+                };
+                for (int t = 0; t < nt && t < PF; ++t) prefetch(t);
+                int t = 0;
+                for (; t < nt; ++t) {
+                    const int s = t & 1;
+                    if (t >= KST && !mbar_wait(&k_empty[s], ((t >> 1) - 1) & 1, abort, err)) break;
+                    uint8_t *dst = smem + s * KSTAGE;
+                    const int key0 = (int)(w.kb + (long)t * NK);
+                    mbar_arrive_expect_tx(&k_full[s], KSTAGE);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * BOX, &mC, &k_full[s], 64 * i, key0, w.b);
+                    tma_load_3d(dst + 8 * BOX, &mR, &k_full[s], 0, key0, w.b);
+                    if (t + PF < nt) prefetch(t + PF);
+                }
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------------------ S = Q.K^T issuer
+            if (lane == 0 && nt > 0) {
+                bool ok = mbar_wait(q_ready, 0, abort, err);
+                for (int t = 0; t < nt && ok; ++t) {
+                    const int s = t & 1;
+                    // tile widened and S buffer s drained by the softmax (one barrier)
+                    if (!mbar_wait(&c_full[s], (t >> 1) & 1, abort, err)) break;
+                    tc_fence_after();
+                    const uint8_t *tile = smem + s * KSTAGE;
+#pragma unroll 4
+                    for (int kk = 0; kk < 36; ++kk)   // 16 dims per step: 32 latent, 4 RoPE
+                        mma_ts(tmem + T_S + s * NK, tmem + T_Q + kk * 8,
+                               sdesc_kmajor(tile + (kk >> 2) * BOX) + 2 * (kk & 3), p.idesc_s, kk != 0);
+                    mma_commit(&k_empty[s]);
+                    mma_commit(&s_full[s]);
+                }
+            }
+        } else if (warp < 6) {
+            // ---------------------------------------------------------- softmax warps
+            const int quad = warp & 3, row = quad * 32 + lane;
+            const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
+            if (nt > 0) {   // this head's q_abs | RoPE(q_pe) row into TMEM (fp16 pairs)
+                const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r);
+                const uint4 *qp = (const uint4 *)(p.qp + w.b * p.qp_b + (long)(w.r0 + row) * p.qp_r);
+                for (int c = 0; c < 18; ++c) {   // 16 columns (32 values) per step
+                    const uint4 *sp = c < 16 ? qa + c * 4 : qp + (c - 16) * 4;
+                    uint32_t r16[16];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 x = sp[v];
+                        r16[4 * v] = x.x;
+                        r16[4 * v + 1] = x.y;
+                        r16[4 * v + 2] = x.z;
+                        r16[4 * v + 3] = x.w;
+                    }
+                    tmem_st16(lb + T_Q + c * 16, r16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_ready);
+            }
+            const uint32_t peer_slot0 = map_peer(smem_u32(smem + OFF_PB), 1);
+            const uint32_t peer_full0 = map_peer(smem_u32(p_full), 1);   // armed by rank 1 itself
+            const bool elected = warp == 2 && lane == 0;
+            const float c = p.scale_log2;
+            float m = -INFINITY, l = 0.f;   // running maximum (scaled, log2 units) and sum
+            bool ok = true;
+            for (int t = 0; t < nt; ++t) {
+                const int s = t & 1;
+                ok = __all_sync(FULL, ok && mbar_wait(&s_full[s], (t >> 1) & 1, abort, err));
+                tc_fence_after();
+                uint32_t sr[2][32];
+                if (ok) {
+                    tmem_ld32(lb + T_S + s * NK, sr[0]);
+                    tmem_ld32(lb + T_S + s * NK + 32, sr[1]);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sr[0][e] = sr[1][e] = 0u;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c_full[s]);   // S buffer s may take tile t + 2
+                float x[64];
+#pragma unroll
+                for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sr[e >> 5][e & 31]);
+                const long key0 = w.kb + (long)t * NK;
+                if (key0 + NK > w.ke) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (key0 + e >= w.ke) x[e] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) mx[a] = x[a];
+#pragma unroll
+                for (int e = 8; e < 64; ++e) mx[e & 7] = fmaxf(mx[e & 7], x[e]);
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+                // the accumulator is rescaled only when the row maximum grows by > 2^8
+                const bool need = mt > m + RESCALE_LOG2;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = m == -INFINITY ? 0.f : ex2(m - mt);
+                    m = mt;
+                }
+                l *= alpha;
+                const float m_eff = m == -INFINITY ? 0.f : m;
+                float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2(fmaf(x[2 * e], c, -m_eff)), p1 = ex2(fmaf(x[2 * e + 1], c, -m_eff));
+                    ra[e & 7] += p0 + p1;
+                    pk[e] = pack_bf16(p0, p1);
+                }
+                l += ((ra[0] + ra[1]) + (ra[2] + ra[3])) + ((ra[4] + ra[5]) + (ra[6] + ra[7]));
+                const bool rescaled = __any_sync(FULL, need && t > 0);
+                // staging slot s is free: the copy of tile t - 2 finished reading it
+                named_bar_sync(1, 128);
+                uint8_t *stg = smem + OFF_STG + s * XSLOT;
+                uint4 *prow = (uint4 *)(stg + X_P + row * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)   // 16-byte chunk j of the row at j ^ (row mod 8)
+                    prow[j ^ (row & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                ((float *)(stg + X_ALPHA))[row] = alpha;
+                if (t == nt - 1) ((float *)(stg + X_INVL))[row] = l > 0.f ? 1.f / l : 0.f;
+                if (lane == 0) ((uint32_t *)(stg + X_FLAG))[quad] = rescaled ? 1u : 0u;
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (elected) {
+                    const int pb = t % NPB;
+                    bool go = ok;
+                    if (go && t >= NPB) go = mbar_wait_cluster(&p_empty[pb], ((t / NPB) - 1) & 1, abort, err);
+                    if (go) {
+                        bulk_copy_to_peer(peer_slot0 + pb * XSLOT, stg, X_BYTES, peer_full0 + pb * 8);
+                        bulk_commit();
+                        bulk_wait_read<1>();   // the copy of tile t - 1 has read its slot
+                    }
+                    ok = go;
+                }
+            }
+            if (elected) bulk_wait_all();   // nothing in flight into the peer at exit
+            if (ok)
+                p.pl[w.split * p.pl_s + w.b * p.pl_b + w.r0 + row] =
+                    l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        } else {
+            // ------------------------------------------ bf16 -> fp16 widening, in place
+            constexpr int NCT = NCONV * 32, PER = (int)(KSTAGE / 16) / NCT, BATCH = 12;
+            static_assert((int)(KSTAGE / 16) % NCT == 0 && PER % BATCH == 0, "widening split");
+            const int ct = tid - 6 * 32;
+            for (int t = 0; t < nt; ++t) {
+                const int s = t & 1;
+                if (!mbar_wait(&k_full[s], (t >> 1) & 1, abort, err)) break;
+                uint4 *q = (uint4 *)(smem + s * KSTAGE) + ct;
+                for (int b = 0; b < PER; b += BATCH) {   // BATCH independent loads in flight per thread
+                    uint4 v[BATCH];
+#pragma unroll
+                    for (int k = 0; k < BATCH; ++k) v[k] = q[(b + k) * NCT];
+#pragma unroll
+                    for (int k = 0; k < BATCH; ++k) {
+                        uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            u[e] = pack_f16(__uint_as_float(u[e] << 16), __uint_as_float(u[e] & 0xffff0000u));
+                        q[(b + k) * NCT] = make_uint4(u[0], u[1], u[2], u[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c_full[s]);
+            }
+        }
+    } else {
+        if (warp == 0) {
+            // -------------------------------------------- TMA producer (latent rows)
+            if (lane == 0 && nt > 0) {
+                tma_prefetch_desc(&mC);
+                for (int t = 0; t < nt; ++t) {
+                    const int s = t % VST;
+                    if (t >= VST && !mbar_wait(&v_empty[s], ((t / VST) - 1) & 1, abort, err)) break;
+                    uint8_t *dst = smem + s * VSTAGE;
+                    const int key0 = (int)(w.kb + (long)t * NK);
+                    mbar_arrive_expect_tx(&v_full[s], VSTAGE);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * BOX, &mC, &v_full[s], 64 * i, key0, w.b);
+                }
+            }
+        } else if (warp == 1) {
+            // ---------------------------------------------------- O += P.C issuer
+            if (lane == 0 && nt > 0) {
+                for (int t = 0; t < nt; ++t) {
+                    const int s = t % VST, pb = t % NPB;
+                    if (!mbar_wait(&v_full[s], (t / VST) & 1, abort, err)) break;
+                    if (!mbar_wait(&pc_ready[pb], (t / NPB) & 1, abort, err)) break;
+                    tc_fence_after();
+                    const uint8_t *tile = smem + s * VSTAGE;
+                    const uint64_t pa = sdesc_kmajor(smem + OFF_PB + pb * XSLOT);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {   // 16 keys per step; N = 256 latent dims per MMA
+                        const uint32_t acc = (t | kk) != 0;
+                        mma_ss(tmem, pa + 2 * kk, sdesc_mnmajor(tile + kk * 2048, BOX), p.idesc_pv, acc);
+                        mma_ss(tmem + 256, pa + 2 * kk, sdesc_mnmajor(tile + 4 * BOX + kk * 2048, BOX), p.idesc_pv,
+                               acc);
+                    }
+                    mma_commit(&v_empty[s]);
+                    mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
+                }
+                mma_commit(o_final);
+            }
+        } else if (warp < 6) {
+            // ------------------------------------------- row rescale + epilogue warps
+            const int quad = warp & 3, row = quad * 32 + lane;
+            const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
+            float inv_l = 0.f;
+            bool ok = true;
+            for (int t = 0; t < nt && ok; ++t) {
+                const int pb = t % NPB;
+                ok = __all_sync(FULL, mbar_wait_cluster(&p_full[pb], (t / NPB) & 1, abort, err));
+                if (!ok) break;
+                if (warp == 2 && lane == 0 && t + NPB < nt)   // arm the slot for tile t + NPB
+                    mbar_arrive_expect_tx(&p_full[pb], X_BYTES);
+                const uint8_t *xs = smem + OFF_PB + pb * XSLOT;
+                const uint32_t *fl = (const uint32_t *)(xs + X_FLAG);
+                if ((fl[0] | fl[1] | fl[2] | fl[3]) != 0u) {   // the same answer in every thread
+                    // O must hold tile t - 1's product before it is rescaled.  Slot q's
+                    // previous phase is waited for first, so the parity test is never
+                    // two phases behind.
+                    const int q = (t - 1) % NPB, k = (t - 1) / NPB;
+                    bool g = k == 0 || mbar_wait(&p_empty[q], (k - 1) & 1, abort, err);
+                    g = g && mbar_wait(&p_empty[q], k & 1, abort, err);
+                    ok = __all_sync(FULL, g);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const float a = ((const float *)(xs + X_ALPHA))[row];
+                    if (__any_sync(FULL, a != 1.f)) {
+                        for (int cc = 0; cc < 16; ++cc) {
+                            uint32_t o[32];
+                            tmem_ld32(lb + cc * 32, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+                            tmem_st32(lb + cc * 32, o);
+                        }
+                        tmem_st_wait();
+                    }
+                    tc_fence_before();
+                }
+                if (t == nt - 1) inv_l = ((const float *)(xs + X_INVL))[row];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pc_ready[pb]);
+            }
+            // ---- epilogue: the normalised partial output of this split
+            if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, err);
+            ok = __all_sync(FULL, ok);
+            tc_fence_after();
+            if (ok) {
+                float *dst = p.po + w.split * p.po_s + w.b * p.po_b + (long)(w.r0 + row) * 512;
+                for (int cc = 0; cc < 16; ++cc) {
+                    uint32_t o[32];
+                    if (nt > 0) {
+                        tmem_ld32(lb + cc * 32, o);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
+                    float4 *d4 = (float4 *)(dst + cc * 32);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        d4[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                            __uint_as_float(o[4 * v + 2]) * inv_l,
+                                            __uint_as_float(o[4 * v + 3]) * inv_l);
+                }
+            }
+        }
+    }
+    if (tid == 0 && *abort) settle();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // the peer may still address this CTA's barriers and slots until here
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+// Partial latent outputs and log-sum-exps of every (sequence, key split, 128 heads).
+// qa: q_abs [B][H][512] fp16; qp: rotated q_pe [B][H][64] fp16; cache [B][L][512],
+// kpe [B][L][64] bf16; po [n][B][H][512] fp32, pl [n][B][H].
+cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache, const void *kpe, int B, long L,
+                               int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st) {
+    const long units = (long)B * n_splits * (H / ROWS);
+    if (units == 0) return cudaSuccess;
+    CUtensorMap mC, mR;
+    cudaError_t e;
+    {
+        unsigned long long d[3] = {512, (unsigned long long)L, (unsigned long long)B};
+        unsigned long long s[2] = {1024, (unsigned long long)L * 1024};
+        unsigned box[3] = {64, NK, 1};
+        if ((e = make_tma_map(&mC, cache, 3, d, s, box)) != cudaSuccess) return e;
+    }
+    {
+        unsigned long long d[3] = {64, (unsigned long long)L, (unsigned long long)B};
+        unsigned long long s[2] = {128, (unsigned long long)L * 128};
+        unsigned box[3] = {64, NK, 1};
+        if ((e = make_tma_map(&mR, kpe, 3, d, s, box)) != cudaSuccess) return e;
+    }
+    DecK p{};
+    p.n_splits = n_splits;
+    p.row_tiles = H / ROWS;
+    p.chunk = chunk;
+    p.kv_len = L;
+    p.qa = (const __half *)qa;
+    p.qa_b = (long)H * 512;
+    p.qa_r = 512;
+    p.qp = (const __half *)qp;
+    p.qp_b = (long)H * 64;
+    p.qp_r = 64;
+    p.cache = (const __nv_bfloat16 *)cache;
+    p.kpe = (const __nv_bfloat16 *)kpe;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.po = po;
+    p.pl = pl;
+    p.po_s = (long)B * H * 512;
+    p.po_b = (long)H * 512;
+    p.pl_s = (long)B * H;
+    p.pl_b = H;
+    p.idesc_s = idesc_f16(128, NK, true);
+    p.idesc_pv = idesc_f16(128, 256, false, true);
+    ProfScope ps("tc_decode_attn", st);
+    e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e == cudaSuccess)
+        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t tc_decode_read_and_clear_error(unsigned *flags, cudaStream_t st) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tc_decode_err, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return e;
+    if (v) {
+        unsigned z = 0;
+        e = cudaMemcpyToSymbolAsync(g_tc_decode_err, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    *flags |= v;
+    return e;
+}
+
+}  // namespace mla

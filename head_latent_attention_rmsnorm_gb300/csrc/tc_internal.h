@@ -45,5 +45,13 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
 cudaError_t tc_gemm_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_attn_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_latent_read_and_clear_error(unsigned *flags, cudaStream_t st);
+cudaError_t tc_decode_read_and_clear_error(unsigned *flags, cudaStream_t st);
+
+// Split-KV latent decode attention (tc_decode.cu): partial latent outputs and
+// log-sum-exps of every (sequence, key split, 128 heads).  qa: q_abs [B][H][512] fp16;
+// qp: rotated q_pe [B][H][64] fp16; cache [B][L][512], kpe [B][L][64] bf16;
+// po [n_splits][B][H][512] fp32, pl [n_splits][B][H] fp32.  H % 128 == 0.
+cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache, const void *kpe, int B, long L,
+                               int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st);
 
 }  // namespace mla

@@ -573,26 +573,7 @@ cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, c
     }
     if (e != cudaSuccess) return e;
     // 2. per (sequence, split, 128 heads): partial latent output and its lse
-    LatK k{};
-    k.mode = 0;
-    k.n_splits = p.n;
-    k.row_tiles = p.H / ROWS;
-    k.chunk = p.chunk;
-    k.kv_len = p.L;
-    k.qa = (const __half *)qabs;
-    k.qa_b = (long)p.H * p.Dk;
-    k.qa_r = p.Dk;
-    k.qp = (const __half *)qpe;
-    k.qp_b = (long)p.H * p.Dr;
-    k.qp_r = p.Dr;
-    k.scale_log2 = p.scale * 1.4426950408889634f;
-    k.po = po;
-    k.pl = pl;
-    k.po_s = rows * p.Dk;
-    k.po_b = (long)p.H * p.Dk;
-    k.pl_s = rows;
-    k.pl_b = p.H;
-    e = launch_latent_attn(c_cache, kpe_cache, p.L, p.B, true, k, (long)p.B * p.n * k.row_tiles, st);
+    e = launch_decode_attn(qabs, qpe, c_cache, kpe_cache, p.B, p.L, p.H, p.n, p.chunk, p.scale, po, pl, st);
     if (e != cudaSuccess) return e;
     // 3. log-sum-exp merge of the splits -> o_lat (bf16) and lse
     if ((e = launch_lse_combine(TY_BF16, p.n, rows, p.Dk, po, pl, olat, lse, st)) != cudaSuccess) return e;
@@ -676,6 +657,7 @@ cudaError_t tc_read_and_clear_error(unsigned int *flags, cudaStream_t st) {
     cudaError_t e = tc_gemm_read_and_clear_error(flags, st);
     if (e == cudaSuccess) e = tc_attn_read_and_clear_error(flags, st);
     if (e == cudaSuccess) e = tc_latent_read_and_clear_error(flags, st);
+    if (e == cudaSuccess) e = tc_decode_read_and_clear_error(flags, st);
     return e;
 }
 

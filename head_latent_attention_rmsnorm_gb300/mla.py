@@ -152,7 +152,7 @@ def set_path_override(mode: int) -> None:
 
 
 KERNELS = ("prep", "latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
-           "tc_gemm", "tc_attn", "tc_latent_attn", "transpose")
+           "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose")
 
 
 def launch_count() -> int:

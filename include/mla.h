@@ -207,7 +207,7 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   the number of launches and their summed device time in milliseconds (0 launches
  *   for an unknown name).  Names: "prep", "latent_prep", "rope_table", "rope_rows",
  *   "convert", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
- *   "tc_latent_attn", "transpose".
+ *   "tc_latent_attn", "tc_decode_attn", "transpose".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
  * Not thread-safe: profile from one host thread at a time.
  */
