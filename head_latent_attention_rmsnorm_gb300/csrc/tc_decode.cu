@@ -10,31 +10,38 @@
 // One work unit = the 128 heads of one sequence against one key split.  Its fp32
 // accumulator (128 heads x 512 latent dims) fills the whole tensor memory of an SM,
 // so a unit runs on a cluster of two CTAs with different jobs:
-//   rank 0 (scores): q_abs | RoPE(q_pe) (fp16, 576 wide) in TMEM; each 64-key tile of
-//     the cache (latent + RoPE band) arrives through a two-deep TMA ring and four warps
-//     widen it to fp16 in place; S = Q.K^T on the tensor core (A from TMEM),
-//     double-buffered in TMEM; four warps run the online
-//     softmax (one thread per head), write P in bf16 (already in the MMA operand
+//   rank 0 (scores): Q in bf16 in TMEM; each 64-key tile of the bf16 cache (latent +
+//     RoPE band) arrives through a two-deep TMA ring and is used as it lands; S = Q.K^T
+//     on the tensor core (A from TMEM), double-buffered in TMEM; four warps run the
+//     online softmax (one thread per head), write P in bf16 (already in the MMA operand
 //     layout) with the per-head rescale factors into a staging slot, and one bulk copy
 //     per tile moves that slot into rank 1's shared memory;
 //   rank 1 (accumulator): O (128 x 512 fp32) in all 512 TMEM columns; streams the same
 //     tiles' latent rows (an L2 hit: rank 0 prefetches the tiles into L2 ahead of
 //     use) and issues O += P.C with both operands in shared memory; four warps rescale
 //     rows of O when rank 0 reports a grown row maximum, and write the normalised
-//     partial output at the end.
+//     partial output and the split's log-sum-exp at the end.
 // P only flows from rank 0 to rank 1, through four slots, so rank 0 runs up to four
 // tiles ahead and the cross-CTA latency stays off the critical path.
 //
-// Precision: scores use q_abs and RoPE(q_pe) in fp16 (11-bit significand) against the
-// cache widened exactly from bf16, because a score's rounding error lands directly in
-// the log-sum-exp of a split with few keys (bf16 q_abs: ~1.4e-3 per score on N(0,1)
-// data, fp16: ~1.7e-4).  P multiplies the bf16 cache on rank 1 in bf16: its rounding
-// only perturbs the weights of an average (relative 2^-9), and the row sums use the
-// unrounded fp32 probabilities.
+// Precision.  The tensor core takes bf16 against the bf16 cache, but a score's rounding
+// error lands directly in the log-sum-exp of a split with few keys (q_abs rounded to
+// bf16: ~1.4e-3 per score on N(0,1) data, in fp16: ~1.7e-4).  So q_abs arrives in fp16
+// and is split q = q_hi + q_lo with q_hi = bf16(q):
+//   * RoPE band: both halves go through the tensor core (8 more MMAs per tile), so that
+//     part of every score is as exact as fp16 q_pe;
+//   * latent band: the MMA uses q_hi only.  The missing term delta_j = scale * q_lo . c_j
+//     shifts a split's log-sum-exp by sum_j w_j delta_j + O(delta^2), and
+//     sum_j w_j delta_j = scale * q_lo . (sum_j w_j c_j) = scale * q_lo . o, the split's
+//     own normalised output, which rank 1 holds at the end: it adds that term (the
+//     second-order remainder, half the w-variance of delta, is ~1e-6).  The output
+//     itself moves by sum_j w_j (delta_j - mean delta) c_j, ~1e-3 of |c| at most.
+// P multiplies the cache on rank 1 in bf16: its rounding only perturbs the weights of an
+// average (relative 2^-9), and the row sums use the unrounded fp32 probabilities.
 //
-// Warps (320 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 MMA issuer
-// and TMEM owner, 2-5 softmax, 6-9 bf16 -> fp16 widening; rank 1 -- 0 TMA producer,
-// 1 MMA issuer and TMEM owner, 2-5 rescale + epilogue, 6-9 idle.
+// Warps (256 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 MMA issuer
+// and TMEM owner, 2-5 softmax; rank 1 -- 0 TMA producer, 1 MMA issuer and TMEM owner,
+// 2-5 rescale + epilogue.  Warps 6-7 are idle.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -51,7 +58,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int ROWS = 128, NK = 64, NTHREADS = 320, NCONV = 4;
+constexpr int ROWS = 128, NK = 64, NTHREADS = 256;
 constexpr int KST = 2;     // rank 0: key-tile stages (one per S buffer)
 constexpr int VST = 2;     // rank 1: latent-tile stages
 constexpr int NPB = 4;     // rank 1: P slots
@@ -60,9 +67,9 @@ constexpr uint32_t BOX = NK * 128;          // 64 keys x 64 dims, bf16: 8 KB
 constexpr uint32_t KSTAGE = 9 * BOX;        // 512 latent + 64 RoPE dims
 constexpr uint32_t VSTAGE = 8 * BOX;        // 512 latent dims
 // One P transfer: P [128 heads][64 keys] bf16, K-major with the 128-byte swizzle; the
-// rescale factor of every head; 1/l of every head (meaningful on the last tile); one
-// "some head rescaled" word per softmax warp.
-constexpr uint32_t X_P = 0, X_ALPHA = 16384, X_INVL = X_ALPHA + 512, X_FLAG = X_INVL + 512;
+// rescale factor of every head; 1/l and m + log2(l) of every head (meaningful on the
+// last tile); one "some head rescaled" word per softmax warp.
+constexpr uint32_t X_P = 0, X_ALPHA = 16384, X_INVL = X_ALPHA + 512, X_LSE = X_INVL + 512, X_FLAG = X_LSE + 512;
 constexpr uint32_t X_BYTES = X_FLAG + 16;   // bytes copied per tile
 constexpr uint32_t XSLOT = 18432;           // slot stride: a multiple of the 1024-byte swizzle atom
 // rank 0: K stages then two staging slots; rank 1: V stages then the P slots.  The
@@ -72,13 +79,16 @@ constexpr uint32_t OFF_STG = KST * KSTAGE;
 constexpr uint32_t OFF_PB = VST * VSTAGE;
 constexpr uint32_t OFF_BAR = (OFF_STG + 2 * XSLOT > OFF_PB + NPB * XSLOT) ? OFF_STG + 2 * XSLOT : OFF_PB + NPB * XSLOT;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
-constexpr uint32_t T_S = 0, T_Q = 2 * NK;   // rank 0 TMEM columns: S buffers, then Q (288 columns)
+// rank 0 TMEM columns: S buffers; bf16 q_hi of the latent band (256 columns); the RoPE
+// band's q_hi and q_lo (32 columns each)
+constexpr uint32_t T_S = 0, T_Q = 2 * NK, T_QP = T_Q + 256, T_QL = T_QP + 32;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned FULL = 0xffffffffu;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_STG % 1024 == 0 && OFF_PB % 1024 == 0 && XSLOT % 1024 == 0, "swizzle atoms 1024-aligned");
-static_assert(T_Q + 288 <= 512, "TMEM budget of rank 0");
+static_assert(T_QL + 32 <= 512, "TMEM budget of rank 0");
+static_assert(X_FLAG + 16 <= XSLOT, "P transfer fits its slot");
 
 struct DecK {
     int n_splits, row_tiles;
@@ -139,9 +149,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // rank 1
     uint64_t *p_full = bars + 11, *pc_ready = bars + 15, *v_full = bars + 19, *v_empty = bars + 21;
     uint64_t *o_final = bars + 23;
-    // rank 0: tile widened and S buffer drained
-    uint64_t *c_full = bars + 24;
-    uint32_t *tslot = (uint32_t *)(bars + 26);
+    uint32_t *tslot = (uint32_t *)(bars + 24);
     volatile int *abort = (volatile int *)(tslot + 1);
     unsigned *err = &g_tc_decode_err;
 
@@ -153,10 +161,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (tid == 0) {
         if (rank == 0) {
             for (int s = 0; s < KST; ++s) {
-                mbar_init(&k_full[s], 1);
+                mbar_init(&k_full[s], 5);   // the producer's expect_tx + one per softmax warp (S buffer free)
                 mbar_init(&k_empty[s], 1);
                 mbar_init(&s_full[s], 1);
-                mbar_init(&c_full[s], NCONV + 4);   // widening warps + one per softmax warp (S buffer free)
             }
             mbar_init(q_ready, 4);
         } else {
@@ -175,7 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         fence_mbar_init();
         if (rank == 0) {   // both S buffers start free: the softmax warps' arrivals for tiles 0 and 1
             for (int s = 0; s < KST; ++s)
-                for (int i = 0; i < 4; ++i) mbar_arrive(&c_full[s]);
+                for (int i = 0; i < 4; ++i) mbar_arrive(&k_full[s]);
         } else {           // every P slot armed for its first transfer
             for (int s = 0; s < NPB; ++s) mbar_arrive_expect_tx(&p_full[s], X_BYTES);
         }
@@ -224,14 +231,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 bool ok = mbar_wait(q_ready, 0, abort, err);
                 for (int t = 0; t < nt && ok; ++t) {
                     const int s = t & 1;
-                    // tile widened and S buffer s drained by the softmax (one barrier)
-                    if (!mbar_wait(&c_full[s], (t >> 1) & 1, abort, err)) break;
+                    // tile landed and S buffer s drained by the softmax (one barrier)
+                    if (!mbar_wait(&k_full[s], (t >> 1) & 1, abort, err)) break;
                     tc_fence_after();
-                    const uint8_t *tile = smem + s * KSTAGE;
-#pragma unroll 4
-                    for (int kk = 0; kk < 36; ++kk)   // 16 dims per step: 32 latent, 4 RoPE
-                        mma_ts(tmem + T_S + s * NK, tmem + T_Q + kk * 8,
-                               sdesc_kmajor(tile + (kk >> 2) * BOX) + 2 * (kk & 3), p.idesc_s, kk != 0);
+                    // descriptors as constant offsets from one base: the issuing thread
+                    // spends no arithmetic between MMAs
+                    const uint64_t d0 = sdesc_kmajor(smem + s * KSTAGE);
+                    const uint32_t dt = tmem + T_S + s * NK, at = tmem + T_Q;
+#pragma unroll
+                    for (int kk = 0; kk < 32; ++kk)   // latent band: 16 dims per step, q_hi only
+                        mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (BOX >> 4) + 2 * (kk & 3)), p.idesc_s,
+                               kk != 0);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)    // RoPE band: q_hi then q_lo against the same box
+                        mma_ts(dt, tmem + (kk < 4 ? T_QP : T_QL) + (kk & 3) * 8,
+                               d0 + (uint64_t)(8 * (BOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
                     mma_commit(&k_empty[s]);
                     mma_commit(&s_full[s]);
                 }
@@ -240,21 +254,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // ---------------------------------------------------------- softmax warps
             const int quad = warp & 3, row = quad * 32 + lane;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
-            if (nt > 0) {   // this head's q_abs | RoPE(q_pe) row into TMEM (fp16 pairs)
+            if (nt > 0) {   // this head's Q into TMEM: bf16(q_abs), then the RoPE band's bf16 halves
                 const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r);
                 const uint4 *qp = (const uint4 *)(p.qp + w.b * p.qp_b + (long)(w.r0 + row) * p.qp_r);
-                for (int c = 0; c < 18; ++c) {   // 16 columns (32 values) per step
+                for (int c = 0; c < 18; ++c) {   // 32 fp16 values per step
                     const uint4 *sp = c < 16 ? qa + c * 4 : qp + (c - 16) * 4;
-                    uint32_t r16[16];
+                    uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const uint4 x = sp[v];
-                        r16[4 * v] = x.x;
-                        r16[4 * v + 1] = x.y;
-                        r16[4 * v + 2] = x.z;
-                        r16[4 * v + 3] = x.w;
+                        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
+                            const uint32_t h = pack_bf16(f.x, f.y);
+                            hi[4 * v + e] = h;
+                            lo[4 * v + e] = pack_bf16(f.x - __uint_as_float(h << 16), f.y - __uint_as_float(h & 0xffff0000u));
+                        }
                     }
-                    tmem_st16(lb + T_Q + c * 16, r16);
+                    if (c < 16) {
+                        tmem_st16(lb + T_Q + c * 16, hi);
+                    } else {
+                        tmem_st16(lb + T_QP + (c - 16) * 16, hi);
+                        tmem_st16(lb + T_QL + (c - 16) * 16, lo);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -282,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&c_full[s]);   // S buffer s may take tile t + 2
+                if (lane == 0) mbar_arrive(&k_full[s]);   // S buffer s may take tile t + 2
                 float x[64];
 #pragma unroll
                 for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sr[e >> 5][e & 31]);
@@ -326,7 +349,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 for (int j = 0; j < 8; ++j)   // 16-byte chunk j of the row at j ^ (row mod 8)
                     prow[j ^ (row & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 ((float *)(stg + X_ALPHA))[row] = alpha;
-                if (t == nt - 1) ((float *)(stg + X_INVL))[row] = l > 0.f ? 1.f / l : 0.f;
+                if (t == nt - 1) {
+                    ((float *)(stg + X_INVL))[row] = l > 0.f ? 1.f / l : 0.f;
+                    ((float *)(stg + X_LSE))[row] = l > 0.f ? m + log2f(l) : -INFINITY;
+                }
                 if (lane == 0) ((uint32_t *)(stg + X_FLAG))[quad] = rescaled ? 1u : 0u;
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
@@ -343,35 +369,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (elected) bulk_wait_all();   // nothing in flight into the peer at exit
-            if (ok)
-                p.pl[w.split * p.pl_s + w.b * p.pl_b + w.r0 + row] =
-                    l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-        } else {
-            // ------------------------------------------ bf16 -> fp16 widening, in place
-            constexpr int NCT = NCONV * 32, PER = (int)(KSTAGE / 16) / NCT, BATCH = 12;
-            static_assert((int)(KSTAGE / 16) % NCT == 0 && PER % BATCH == 0, "widening split");
-            const int ct = tid - 6 * 32;
-            for (int t = 0; t < nt; ++t) {
-                const int s = t & 1;
-                if (!mbar_wait(&k_full[s], (t >> 1) & 1, abort, err)) break;
-                uint4 *q = (uint4 *)(smem + s * KSTAGE) + ct;
-                for (int b = 0; b < PER; b += BATCH) {   // BATCH independent loads in flight per thread
-                    uint4 v[BATCH];
-#pragma unroll
-                    for (int k = 0; k < BATCH; ++k) v[k] = q[(b + k) * NCT];
-#pragma unroll
-                    for (int k = 0; k < BATCH; ++k) {
-                        uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            u[e] = pack_f16(__uint_as_float(u[e] << 16), __uint_as_float(u[e] & 0xffff0000u));
-                        q[(b + k) * NCT] = make_uint4(u[0], u[1], u[2], u[3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c_full[s]);
-            }
         }
     } else {
         if (warp == 0) {
@@ -396,14 +393,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     if (!mbar_wait(&v_full[s], (t / VST) & 1, abort, err)) break;
                     if (!mbar_wait(&pc_ready[pb], (t / NPB) & 1, abort, err)) break;
                     tc_fence_after();
-                    const uint8_t *tile = smem + s * VSTAGE;
                     const uint64_t pa = sdesc_kmajor(smem + OFF_PB + pb * XSLOT);
+                    const uint64_t vb = sdesc_mnmajor(smem + s * VSTAGE, BOX);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {   // 16 keys per step; N = 256 latent dims per MMA
                         const uint32_t acc = (t | kk) != 0;
-                        mma_ss(tmem, pa + 2 * kk, sdesc_mnmajor(tile + kk * 2048, BOX), p.idesc_pv, acc);
-                        mma_ss(tmem + 256, pa + 2 * kk, sdesc_mnmajor(tile + 4 * BOX + kk * 2048, BOX), p.idesc_pv,
-                               acc);
+                        mma_ss(tmem, pa + 2 * kk, vb + (uint64_t)(kk * (2048 >> 4)), p.idesc_pv, acc);
+                        mma_ss(tmem + 256, pa + 2 * kk, vb + (uint64_t)((4 * BOX + kk * 2048) >> 4), p.idesc_pv, acc);
                     }
                     mma_commit(&v_empty[s]);
                     mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
@@ -414,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // ------------------------------------------- row rescale + epilogue warps
             const int quad = warp & 3, row = quad * 32 + lane;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
-            float inv_l = 0.f;
+            float inv_l = 0.f, lse2 = -INFINITY;   // 1/l and m + log2(l) from rank 0's last transfer
             bool ok = true;
             for (int t = 0; t < nt && ok; ++t) {
                 const int pb = t % NPB;
@@ -448,16 +444,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     }
                     tc_fence_before();
                 }
-                if (t == nt - 1) inv_l = ((const float *)(xs + X_INVL))[row];
+                if (t == nt - 1) {
+                    inv_l = ((const float *)(xs + X_INVL))[row];
+                    lse2 = ((const float *)(xs + X_LSE))[row];
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pc_ready[pb]);
             }
-            // ---- epilogue: the normalised partial output of this split
+            // ---- epilogue: the normalised partial output of this split, and its
+            // log-sum-exp with the first-order term of the latent q_lo added
             if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, err);
             ok = __all_sync(FULL, ok);
             tc_fence_after();
             if (ok) {
                 float *dst = p.po + w.split * p.po_s + w.b * p.po_b + (long)(w.r0 + row) * 512;
+                const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r);
+                float dot[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int cc = 0; cc < 16; ++cc) {
                     uint32_t o[32];
                     if (nt > 0) {
@@ -467,13 +469,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = 0u;
                     }
+                    float ov[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(o[e]) * inv_l;
                     float4 *d4 = (float4 *)(dst + cc * 32);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        d4[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                            __uint_as_float(o[4 * v + 2]) * inv_l,
-                                            __uint_as_float(o[4 * v + 3]) * inv_l);
+                    for (int v = 0; v < 8; ++v) d4[v] = make_float4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {   // q_lo = q - bf16(q), rounded as rank 0 rounded q_hi
+                        const uint4 x = qa[cc * 4 + v];
+                        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
+                            const uint32_t h = pack_bf16(f.x, f.y);
+                            dot[e] = fmaf(f.x - __uint_as_float(h << 16), ov[8 * v + 2 * e], dot[e]);
+                            dot[e] = fmaf(f.y - __uint_as_float(h & 0xffff0000u), ov[8 * v + 2 * e + 1], dot[e]);
+                        }
+                    }
                 }
+                const float corr = ((dot[0] + dot[1]) + (dot[2] + dot[3])) * p.scale_log2;
+                p.pl[w.split * p.pl_s + w.b * p.pl_b + w.r0 + row] =
+                    nt > 0 && lse2 > -INFINITY ? (lse2 + corr) * 0.69314718055994531f : -INFINITY;
             }
         }
     }
@@ -527,7 +544,7 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
     p.po_b = (long)H * 512;
     p.pl_s = (long)B * H;
     p.pl_b = H;
-    p.idesc_s = idesc_f16(128, NK, true);
+    p.idesc_s = idesc_f16(128, NK, false);
     p.idesc_pv = idesc_f16(128, 256, false, true);
     ProfScope ps("tc_decode_attn", st);
     e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
