@@ -203,6 +203,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -294,6 +303,21 @@ __device__ __forceinline__ void st_peer_v4(uint32_t addr, float a, float b, floa
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
 }
+// Stores into another CTA's shared memory (`addr`, `peer_bar`: shared::cluster
+// addresses); each store completes its bytes as transactions on the destination
+// mbarrier, so the receiver needs no other signal.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t peer_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(peer_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t peer_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+                 "r"(peer_bar)
+                 : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior
 // writes (including shared::cluster stores) at cluster scope.
 __device__ __forceinline__ void mbar_arrive_peer(uint32_t peer_bar) {
@@ -353,6 +377,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 }
 // K-major tile of 1024-byte atoms stacked along M/N.
 __device__ __forceinline__ uint64_t sdesc_kmajor(const void *tile) { return sdesc_sw128(smem_u32(tile), 16, 1024); }
+// K-major tile with the 64-byte swizzle: rows of 32 16-bit elements (64 bytes), eight
+// rows per 512-byte atom, atoms stacked along M/N; 16-byte chunk c of row r sits at
+// chunk c ^ ((r >> 1) & 3) of the row (layout type 4 in bits 61-63).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(const void *tile) {
+    return (sdesc_sw128(smem_u32(tile), 16, 512) & ~((uint64_t)7 << 61)) | ((uint64_t)4 << 61);
+}
 // MN-major operand: each 128-byte row holds 64 consecutive MN elements of one k; eight
 // k-rows form an atom (stride 1024 bytes along K); consecutive 64-element MN blocks
 // are `mn_block_bytes` apart (the leading byte offset).

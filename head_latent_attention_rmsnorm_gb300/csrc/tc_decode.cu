@@ -10,19 +10,21 @@
 // One work unit = the 128 heads of one sequence against one key split.  Its fp32
 // accumulator (128 heads x 512 latent dims) fills the whole tensor memory of an SM,
 // so a unit runs on a cluster of two CTAs with different jobs:
-//   rank 0 (scores): Q in bf16 in TMEM; each 64-key tile of the bf16 cache (latent +
+//   rank 0 (scores): Q in bf16 in TMEM; each 96-key tile of the bf16 cache (latent +
 //     RoPE band) arrives through a two-deep TMA ring and is used as it lands; S = Q.K^T
-//     on the tensor core (A from TMEM), double-buffered in TMEM; four warps run the
-//     online softmax (one thread per head), write P in bf16 (already in the MMA operand
-//     layout) with the per-head rescale factors into a staging slot, and one bulk copy
-//     per tile moves that slot into rank 1's shared memory;
+//     on the tensor core (A from TMEM, N = 96: the widest score tile that fits TMEM
+//     beside Q, and one that runs at the full MMA rate, which N = 64 does not),
+//     double-buffered in TMEM; eight warps run the online softmax (two threads per
+//     head, swapping row maxima through shared memory) and store P in bf16 (already in
+//     the MMA operand layout) with the per-head rescale factors straight into rank 1's
+//     shared memory (st.async, completing bytes on the receiving slot's barrier);
 //   rank 1 (accumulator): O (128 x 512 fp32) in all 512 TMEM columns; streams the same
-//     tiles' latent rows (an L2 hit: rank 0 prefetches the tiles into L2 ahead of
-//     use) and issues O += P.C with both operands in shared memory; four warps rescale
-//     rows of O when rank 0 reports a grown row maximum, and write the normalised
-//     partial output and the split's log-sum-exp at the end.
-// P only flows from rank 0 to rank 1, through four slots, so rank 0 runs up to four
-// tiles ahead and the cross-CTA latency stays off the critical path.
+//     tiles' latent rows in 32-key sub-tiles (L2 hits: rank 0 prefetches the tiles into
+//     L2 ahead of use) and issues O += P.C with both operands in shared memory; four
+//     warps rescale rows of O when rank 0 reports a grown row maximum, and write the
+//     normalised partial output and the split's log-sum-exp at the end.
+// P only flows from rank 0 to rank 1, through three slots, so rank 0 runs ahead and the
+// cross-CTA latency stays off the critical path.
 //
 // Precision.  The tensor core takes bf16 against the bf16 cache, but a score's rounding
 // error lands directly in the log-sum-exp of a split with few keys (q_abs rounded to
@@ -39,9 +41,9 @@
 // P multiplies the cache on rank 1 in bf16: its rounding only perturbs the weights of an
 // average (relative 2^-9), and the row sums use the unrounded fp32 probabilities.
 //
-// Warps (256 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 MMA issuer
-// and TMEM owner, 2-5 softmax; rank 1 -- 0 TMA producer, 1 MMA issuer and TMEM owner,
-// 2-5 rescale + epilogue.  Warps 6-7 are idle.
+// Warps (320 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 MMA issuer
+// and TMEM owner, 2-9 softmax (two threads per head); rank 1 -- 0 TMA producer, 1 MMA
+// issuer and TMEM owner, 2-5 rescale + epilogue, 6-9 idle.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -58,26 +60,34 @@ namespace {
 
 using namespace tc;
 
-constexpr int ROWS = 128, NK = 64, NTHREADS = 256;
+constexpr int ROWS = 128, NK = 96, NTHREADS = 320;
 constexpr int KST = 2;     // rank 0: key-tile stages (one per S buffer)
-constexpr int VST = 2;     // rank 1: latent-tile stages
-constexpr int NPB = 4;     // rank 1: P slots
-constexpr int PF = 6;      // tiles prefetched into L2 ahead of the TMA loads
-constexpr uint32_t BOX = NK * 128;          // 64 keys x 64 dims, bf16: 8 KB
-constexpr uint32_t KSTAGE = 9 * BOX;        // 512 latent + 64 RoPE dims
-constexpr uint32_t VSTAGE = 8 * BOX;        // 512 latent dims
-// One P transfer: P [128 heads][64 keys] bf16, K-major with the 128-byte swizzle; the
-// rescale factor of every head; 1/l and m + log2(l) of every head (meaningful on the
-// last tile); one "some head rescaled" word per softmax warp.
-constexpr uint32_t X_P = 0, X_ALPHA = 16384, X_INVL = X_ALPHA + 512, X_LSE = X_INVL + 512, X_FLAG = X_LSE + 512;
-constexpr uint32_t X_BYTES = X_FLAG + 16;   // bytes copied per tile
-constexpr uint32_t XSLOT = 18432;           // slot stride: a multiple of the 1024-byte swizzle atom
-// rank 0: K stages then two staging slots; rank 1: V stages then the P slots.  The
-// barriers sit after both layouts, at the same offset in both CTAs (the peer addresses
-// them by offset).
-constexpr uint32_t OFF_STG = KST * KSTAGE;
+constexpr int VSUB = 32;   // rank 1: keys per latent sub-tile
+constexpr int VST = 4;     // rank 1: latent sub-tile stages
+constexpr int NPB = 3;     // rank 1: P slots
+constexpr int PF = 4;      // tiles prefetched into L2 ahead of the TMA loads
+constexpr uint32_t KBOX = NK * 128;         // 96 keys x 64 dims, bf16: 12 KB
+constexpr uint32_t KSTAGE = 9 * KBOX;       // boxes 0-7 latent dims, box 8 the RoPE band
+constexpr uint32_t VBOX = VSUB * 128;       // 32 keys x 64 dims: 4 KB
+constexpr uint32_t VSTAGE = 8 * VBOX;       // 512 latent dims
+// One P transfer, written by rank 0's softmax threads straight into a rank-1 slot with
+// st.async (each store completes its bytes on the slot's barrier).  P [128 heads][96
+// keys] bf16 as the K-major A operand of P.C: keys 0-63 in a 128-byte-swizzled block
+// (128 B per head), keys 64-95 in a 64-byte-swizzled block (64 B per head).  Then the
+// per-head extras: rescale factor, 1/l and m + log2(l) (written on the last tile only),
+// and one "some head rescaled" word per lane quarter.
+constexpr uint32_t P_BLK1 = 16384, P_BYTES = 16384 + 8192;
+constexpr uint32_t X_ALPHA = 0, X_INVL = 512, X_LSE = 1024, X_FLAG = 1536;
+constexpr uint32_t XOFF = P_BYTES;           // extras within a rank-1 slot
+constexpr uint32_t XSLOT = 26624;            // rank-1 slot stride (1024-aligned)
+constexpr uint32_t T_BYTES = P_BYTES + 512 + 16, T_BYTES_LAST = T_BYTES + 1024;   // bytes of one transfer
+// rank 0: K stages, then the two halves' row maxima (double-buffered); rank 1: V
+// sub-tile stages, then the P slots.  The barriers sit after both layouts, at the same
+// offset in both CTAs (the peer addresses them by offset).
+constexpr uint32_t OFF_RED = KST * KSTAGE;
 constexpr uint32_t OFF_PB = VST * VSTAGE;
-constexpr uint32_t OFF_BAR = (OFF_STG + 2 * XSLOT > OFF_PB + NPB * XSLOT) ? OFF_STG + 2 * XSLOT : OFF_PB + NPB * XSLOT;
+constexpr uint32_t END0 = OFF_RED + 2 * 2 * ROWS * 4, END1 = OFF_PB + NPB * XSLOT;
+constexpr uint32_t OFF_BAR = END0 > END1 ? END0 : END1;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
 // rank 0 TMEM columns: S buffers; bf16 q_hi of the latent band (256 columns); the RoPE
 // band's q_hi and q_lo (32 columns each)
@@ -86,9 +96,10 @@ constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned FULL = 0xffffffffu;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_STG % 1024 == 0 && OFF_PB % 1024 == 0 && XSLOT % 1024 == 0, "swizzle atoms 1024-aligned");
+static_assert(KSTAGE % 1024 == 0 && OFF_PB % 1024 == 0 && XSLOT % 1024 == 0, "swizzle atoms aligned");
+static_assert(XOFF + X_FLAG + 16 <= XSLOT, "P transfer layout");
 static_assert(T_QL + 32 <= 512, "TMEM budget of rank 0");
-static_assert(X_FLAG + 16 <= XSLOT, "P transfer fits its slot");
+static_assert(NK % VSUB == 0 && NK % 16 == 0 && NK <= 128, "tile shape");
 
 struct DecK {
     int n_splits, row_tiles;
@@ -113,7 +124,7 @@ __device__ __forceinline__ float ex2(float x) {
 struct Unit {
     int b, split, r0;   // sequence, key split, first head
     long kb, ke;        // key range [kb, ke)
-    int nt;             // 64-key tiles
+    int nt;             // key tiles
 };
 
 __device__ __forceinline__ Unit unit_of(const DecK &p, int u) {
@@ -137,19 +148,22 @@ __device__ void settle() {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-    tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR, DecK p) {
+    tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR,
+                     const __grid_constant__ CUtensorMap mV, DecK p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
-    // rank 0
-    uint64_t *k_full = bars, *k_empty = bars + 2, *s_full = bars + 4, *q_ready = bars + 6;
+    // rank 0: k_full = the tile landed + S buffer drained
+    uint64_t *k_full = bars, *k_empty = bars + 4, *s_full = bars + 6;
+    uint64_t *q_ready = bars + 10;
+    float *red = (float *)(smem + OFF_RED);   // rank 0: [tile parity][half][row] row maxima
     // both: P slot t % NPB consumed by the P.C MMAs of tile t (one multicast commit
     // completes it in both CTAs)
-    uint64_t *p_empty = bars + 7;
+    uint64_t *p_empty = bars + 11;
     // rank 1
-    uint64_t *p_full = bars + 11, *pc_ready = bars + 15, *v_full = bars + 19, *v_empty = bars + 21;
-    uint64_t *o_final = bars + 23;
-    uint32_t *tslot = (uint32_t *)(bars + 24);
+    uint64_t *p_full = bars + 14, *pc_ready = bars + 17, *v_full = bars + 20, *v_empty = bars + 24;
+    uint64_t *o_final = bars + 28;
+    uint32_t *tslot = (uint32_t *)(bars + 29);
     volatile int *abort = (volatile int *)(tslot + 1);
     unsigned *err = &g_tc_decode_err;
 
@@ -161,14 +175,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (tid == 0) {
         if (rank == 0) {
             for (int s = 0; s < KST; ++s) {
-                mbar_init(&k_full[s], 5);   // the producer's expect_tx + one per softmax warp (S buffer free)
+                mbar_init(&k_full[s], 9);   // the producer's expect_tx + one per softmax warp (S buffer free)
                 mbar_init(&k_empty[s], 1);
                 mbar_init(&s_full[s], 1);
             }
             mbar_init(q_ready, 4);
         } else {
             for (int s = 0; s < NPB; ++s) {
-                mbar_init(&p_full[s], 1);   // this CTA's expect_tx + the bulk copy's bytes
+                mbar_init(&p_full[s], 1);   // this CTA's expect_tx + the bytes of rank 0's stores
                 mbar_init(&pc_ready[s], 4);
             }
             for (int s = 0; s < VST; ++s) {
@@ -182,9 +196,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         fence_mbar_init();
         if (rank == 0) {   // both S buffers start free: the softmax warps' arrivals for tiles 0 and 1
             for (int s = 0; s < KST; ++s)
-                for (int i = 0; i < 4; ++i) mbar_arrive(&k_full[s]);
+                for (int i = 0; i < 8; ++i) mbar_arrive(&k_full[s]);
         } else {           // every P slot armed for its first transfer
-            for (int s = 0; s < NPB; ++s) mbar_arrive_expect_tx(&p_full[s], X_BYTES);
+            for (int s = 0; s < NPB; ++s) mbar_arrive_expect_tx(&p_full[s], s == nt - 1 ? T_BYTES_LAST : T_BYTES);
         }
     }
     if (warp == 1) {
@@ -212,16 +226,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     l2_prefetch(p.kpe + row * 64, (uint32_t)rows * 128u);
                 };
                 for (int t = 0; t < nt && t < PF; ++t) prefetch(t);
-                int t = 0;
-                for (; t < nt; ++t) {
+                for (int t = 0; t < nt; ++t) {
                     const int s = t & 1;
-                    if (t >= KST && !mbar_wait(&k_empty[s], ((t >> 1) - 1) & 1, abort, err)) break;
+                    const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of tile t - 2 in this stage
+                    if (t >= KST && !mbar_wait(&k_empty[s], ph, abort, err)) break;
                     uint8_t *dst = smem + s * KSTAGE;
                     const int key0 = (int)(w.kb + (long)t * NK);
                     mbar_arrive_expect_tx(&k_full[s], KSTAGE);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * BOX, &mC, &k_full[s], 64 * i, key0, w.b);
-                    tma_load_3d(dst + 8 * BOX, &mR, &k_full[s], 0, key0, w.b);
+                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * KBOX, &mC, &k_full[s], 64 * i, key0, w.b);
+                    tma_load_3d(dst + 8 * KBOX, &mR, &k_full[s], 0, key0, w.b);
                     if (t + PF < nt) prefetch(t + PF);
                 }
             }
@@ -240,21 +254,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const uint32_t dt = tmem + T_S + s * NK, at = tmem + T_Q;
 #pragma unroll
                     for (int kk = 0; kk < 32; ++kk)   // latent band: 16 dims per step, q_hi only
-                        mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (BOX >> 4) + 2 * (kk & 3)), p.idesc_s,
+                        mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s,
                                kk != 0);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)    // RoPE band: q_hi then q_lo against the same box
                         mma_ts(dt, tmem + (kk < 4 ? T_QP : T_QL) + (kk & 3) * 8,
-                               d0 + (uint64_t)(8 * (BOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
+                               d0 + (uint64_t)(8 * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
                     mma_commit(&k_empty[s]);
                     mma_commit(&s_full[s]);
                 }
             }
-        } else if (warp < 6) {
+        } else if (warp >= 2 && warp < 10) {
             // ---------------------------------------------------------- softmax warps
-            const int quad = warp & 3, row = quad * 32 + lane;
+            // two threads per head: warps 2-5 take keys 0-47 of a tile, warps 6-9 keys 48-95
+            const int quad = warp & 3, row = quad * 32 + lane, h = (warp - 2) >> 2;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
-            if (nt > 0) {   // this head's Q into TMEM: bf16(q_abs), then the RoPE band's bf16 halves
+            if (nt > 0 && h == 0) {   // this head's Q into TMEM: bf16(q_abs), then the RoPE band's bf16 halves
                 const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r);
                 const uint4 *qp = (const uint4 *)(p.qp + w.b * p.qp_b + (long)(w.r0 + row) * p.qp_r);
                 for (int c = 0; c < 18; ++c) {   // 32 fp16 values per step
@@ -267,9 +282,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
-                            const uint32_t h = pack_bf16(f.x, f.y);
-                            hi[4 * v + e] = h;
-                            lo[4 * v + e] = pack_bf16(f.x - __uint_as_float(h << 16), f.y - __uint_as_float(h & 0xffff0000u));
+                            const uint32_t hb = pack_bf16(f.x, f.y);
+                            hi[4 * v + e] = hb;
+                            lo[4 * v + e] =
+                                pack_bf16(f.x - __uint_as_float(hb << 16), f.y - __uint_as_float(hb & 0xffff0000u));
                         }
                     }
                     if (c < 16) {
@@ -286,43 +302,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
             const uint32_t peer_slot0 = map_peer(smem_u32(smem + OFF_PB), 1);
             const uint32_t peer_full0 = map_peer(smem_u32(p_full), 1);   // armed by rank 1 itself
-            const bool elected = warp == 2 && lane == 0;
             const float c = p.scale_log2;
-            float m = -INFINITY, l = 0.f;   // running maximum (scaled, log2 units) and sum
+            constexpr int HK = NK / 2;   // keys per thread
+            float m = -INFINITY, l = 0.f;   // running maximum (scaled, log2 units), this half's sum
             bool ok = true;
             for (int t = 0; t < nt; ++t) {
-                const int s = t & 1;
+                const int s = t & 1, pb = t % NPB;
                 ok = __all_sync(FULL, ok && mbar_wait(&s_full[s], (t >> 1) & 1, abort, err));
                 tc_fence_after();
-                uint32_t sr[2][32];
-                if (ok) {
-                    tmem_ld32(lb + T_S + s * NK, sr[0]);
-                    tmem_ld32(lb + T_S + s * NK + 32, sr[1]);
+                uint32_t sa[32], sb[16];
+                if (ok) {   // half 0: columns 0-31, 32-47; half 1: columns 48-63, 64-95
+                    const uint32_t base = lb + T_S + s * NK + h * HK;
+                    if (h == 0) {
+                        tmem_ld32(base, sa);
+                        tmem_ld16(base + 32, sb);
+                    } else {
+                        tmem_ld16(base, sb);
+                        tmem_ld32(base + 16, sa);
+                    }
                     tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) sr[0][e] = sr[1][e] = 0u;
+                    for (int e = 0; e < 32; ++e) sa[e] = 0u;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sb[e] = 0u;
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&k_full[s]);   // S buffer s may take tile t + 2
-                float x[64];
+                float x[HK];   // this thread's keys, in key order
 #pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sr[e >> 5][e & 31]);
-                const long key0 = w.kb + (long)t * NK;
-                if (key0 + NK > w.ke) {
+                for (int e = 0; e < HK; ++e)
+                    x[e] = __uint_as_float(h == 0 ? (e < 32 ? sa[e] : sb[e - 32]) : (e < 16 ? sb[e] : sa[e - 16]));
+                const long key0 = w.kb + (long)t * NK + h * HK;
+                if (key0 + HK > w.ke) {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e)
+                    for (int e = 0; e < HK; ++e)
                         if (key0 + e >= w.ke) x[e] = -INFINITY;
                 }
                 float mx[8];
 #pragma unroll
                 for (int a = 0; a < 8; ++a) mx[a] = x[a];
 #pragma unroll
-                for (int e = 8; e < 64; ++e) mx[e & 7] = fmaxf(mx[e & 7], x[e]);
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+                for (int e = 8; e < HK; ++e) mx[e & 7] = fmaxf(mx[e & 7], x[e]);
+                float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                // the row maximum of the tile: this half's and the partner thread's
+                red[(s * 2 + h) * ROWS + row] = mt;
+                named_bar_sync(1, 256);
+                mt = fmaxf(mt, red[(s * 2 + (h ^ 1)) * ROWS + row]) * c;
                 // the accumulator is rescaled only when the row maximum grows by > 2^8
+                // (both threads of a row take the same decision from the same numbers)
                 const bool need = mt > m + RESCALE_LOG2;
                 float alpha = 1.f;
                 if (need) {
@@ -332,81 +362,94 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 l *= alpha;
                 const float m_eff = m == -INFINITY ? 0.f : m;
                 float ra[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[32];
+                uint32_t pk[HK / 2];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
+                for (int e = 0; e < HK / 2; ++e) {
                     const float p0 = ex2(fmaf(x[2 * e], c, -m_eff)), p1 = ex2(fmaf(x[2 * e + 1], c, -m_eff));
                     ra[e & 7] += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
                 l += ((ra[0] + ra[1]) + (ra[2] + ra[3])) + ((ra[4] + ra[5]) + (ra[6] + ra[7]));
                 const bool rescaled = __any_sync(FULL, need && t > 0);
-                // staging slot s is free: the copy of tile t - 2 finished reading it
-                named_bar_sync(1, 128);
-                uint8_t *stg = smem + OFF_STG + s * XSLOT;
-                uint4 *prow = (uint4 *)(stg + X_P + row * 128);
+                // P slot pb of rank 1 is free once its P.C MMAs of tile t - NPB are done
+                if (t >= NPB) ok = __all_sync(FULL, ok && mbar_wait_cluster(&p_empty[pb], ((t / NPB) - 1) & 1, abort, err));
+                if (ok) {
+                    const uint32_t slot = peer_slot0 + pb * XSLOT, bar = peer_full0 + pb * 8;
+                    // 16-byte chunk j (8 keys) of this thread: keys 8j .. 8j+7 of the tile
 #pragma unroll
-                for (int j = 0; j < 8; ++j)   // 16-byte chunk j of the row at j ^ (row mod 8)
-                    prow[j ^ (row & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                ((float *)(stg + X_ALPHA))[row] = alpha;
-                if (t == nt - 1) {
-                    ((float *)(stg + X_INVL))[row] = l > 0.f ? 1.f / l : 0.f;
-                    ((float *)(stg + X_LSE))[row] = l > 0.f ? m + log2f(l) : -INFINITY;
-                }
-                if (lane == 0) ((uint32_t *)(stg + X_FLAG))[quad] = rescaled ? 1u : 0u;
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (elected) {
-                    const int pb = t % NPB;
-                    bool go = ok;
-                    if (go && t >= NPB) go = mbar_wait_cluster(&p_empty[pb], ((t / NPB) - 1) & 1, abort, err);
-                    if (go) {
-                        bulk_copy_to_peer(peer_slot0 + pb * XSLOT, stg, X_BYTES, peer_full0 + pb * 8);
-                        bulk_commit();
-                        bulk_wait_read<1>();   // the copy of tile t - 1 has read its slot
+                    for (int q = 0; q < HK / 8; ++q) {
+                        const int j = h * (HK / 8) + q;
+                        const uint32_t dst = j < 8 ? slot + row * 128 + ((j ^ (row & 7)) << 4)
+                                                   : slot + P_BLK1 + row * 64 + (((j - 8) ^ ((row >> 1) & 3)) << 4);
+                        st_async_v4(dst, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3], bar);
                     }
-                    ok = go;
+                    if (h == 0) {
+                        st_async_b32(slot + XOFF + X_ALPHA + row * 4, __float_as_uint(alpha), bar);
+                        if (lane == 0) st_async_b32(slot + XOFF + X_FLAG + quad * 4, rescaled ? 1u : 0u, bar);
+                    }
+                }
+                if (t == nt - 1) {   // the row's sum: this half's plus the partner's (the other
+                                     // parity's slots: both threads are past their last reads)
+                    red[((s ^ 1) * 2 + h) * ROWS + row] = l;
+                    named_bar_sync(1, 256);
+                    const float lt = l + red[((s ^ 1) * 2 + (h ^ 1)) * ROWS + row];
+                    if (ok && h == 0) {
+                        const uint32_t slot = peer_slot0 + pb * XSLOT, bar = peer_full0 + pb * 8;
+                        st_async_b32(slot + XOFF + X_INVL + row * 4, __float_as_uint(lt > 0.f ? 1.f / lt : 0.f), bar);
+                        st_async_b32(slot + XOFF + X_LSE + row * 4,
+                                     __float_as_uint(lt > 0.f ? m + log2f(lt) : -INFINITY), bar);
+                    }
                 }
             }
-            if (elected) bulk_wait_all();   // nothing in flight into the peer at exit
         }
     } else {
         if (warp == 0) {
-            // -------------------------------------------- TMA producer (latent rows)
+            // ---------------------------------- TMA producer (latent rows, 32-key sub-tiles)
             if (lane == 0 && nt > 0) {
-                tma_prefetch_desc(&mC);
-                for (int t = 0; t < nt; ++t) {
-                    const int s = t % VST;
-                    if (t >= VST && !mbar_wait(&v_empty[s], ((t / VST) - 1) & 1, abort, err)) break;
+                tma_prefetch_desc(&mV);
+                for (int g = 0; g < 3 * nt; ++g) {
+                    const int s = g % VST;
+                    if (g >= VST && !mbar_wait(&v_empty[s], ((g / VST) - 1) & 1, abort, err)) break;
                     uint8_t *dst = smem + s * VSTAGE;
-                    const int key0 = (int)(w.kb + (long)t * NK);
+                    const int key0 = (int)(w.kb + (long)(g / 3) * NK + (g % 3) * VSUB);
                     mbar_arrive_expect_tx(&v_full[s], VSTAGE);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * BOX, &mC, &v_full[s], 64 * i, key0, w.b);
+                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * VBOX, &mV, &v_full[s], 64 * i, key0, w.b);
                 }
             }
         } else if (warp == 1) {
             // ---------------------------------------------------- O += P.C issuer
             if (lane == 0 && nt > 0) {
-                for (int t = 0; t < nt; ++t) {
-                    const int s = t % VST, pb = t % NPB;
-                    if (!mbar_wait(&v_full[s], (t / VST) & 1, abort, err)) break;
+                bool ok = true;
+                for (int t = 0; t < nt && ok; ++t) {
+                    const int pb = t % NPB;
                     if (!mbar_wait(&pc_ready[pb], (t / NPB) & 1, abort, err)) break;
-                    tc_fence_after();
-                    const uint64_t pa = sdesc_kmajor(smem + OFF_PB + pb * XSLOT);
-                    const uint64_t vb = sdesc_mnmajor(smem + s * VSTAGE, BOX);
+                    const uint8_t *slot = smem + OFF_PB + pb * XSLOT;
+                    const uint64_t pa0 = sdesc_kmajor(slot), pa1 = sdesc_kmajor_sw64(slot + P_BLK1);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {   // 16 keys per step; N = 256 latent dims per MMA
-                        const uint32_t acc = (t | kk) != 0;
-                        mma_ss(tmem, pa + 2 * kk, vb + (uint64_t)(kk * (2048 >> 4)), p.idesc_pv, acc);
-                        mma_ss(tmem + 256, pa + 2 * kk, vb + (uint64_t)((4 * BOX + kk * 2048) >> 4), p.idesc_pv, acc);
+                    for (int i = 0; i < NK / VSUB; ++i) {
+                        const int g = 3 * t + i, s = g % VST;
+                        if (!mbar_wait(&v_full[s], (g / VST) & 1, abort, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t vb = sdesc_mnmajor(smem + s * VSTAGE, VBOX);
+#pragma unroll
+                        for (int j = 0; j < VSUB / 16; ++j) {   // 16 keys per step; N = 256 latent dims per MMA
+                            const int kk = i * (VSUB / 16) + j;  // key step within the tile
+                            const uint64_t pa = kk < 4 ? pa0 + (uint64_t)(2 * kk) : pa1 + (uint64_t)(2 * (kk - 4));
+                            const uint32_t acc = (t | kk) != 0;
+                            mma_ss(tmem, pa, vb + (uint64_t)(j * (2048 >> 4)), p.idesc_pv, acc);
+                            mma_ss(tmem + 256, pa, vb + (uint64_t)((4 * VBOX + j * 2048) >> 4), p.idesc_pv, acc);
+                        }
+                        mma_commit(&v_empty[s]);
                     }
-                    mma_commit(&v_empty[s]);
-                    mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
+                    if (ok) mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
                 }
                 mma_commit(o_final);
             }
-        } else if (warp < 6) {
+        } else if (warp >= 2 && warp < 6) {
             // ------------------------------------------- row rescale + epilogue warps
             const int quad = warp & 3, row = quad * 32 + lane;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
@@ -417,8 +460,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 ok = __all_sync(FULL, mbar_wait_cluster(&p_full[pb], (t / NPB) & 1, abort, err));
                 if (!ok) break;
                 if (warp == 2 && lane == 0 && t + NPB < nt)   // arm the slot for tile t + NPB
-                    mbar_arrive_expect_tx(&p_full[pb], X_BYTES);
-                const uint8_t *xs = smem + OFF_PB + pb * XSLOT;
+                    mbar_arrive_expect_tx(&p_full[pb], t + NPB == nt - 1 ? T_BYTES_LAST : T_BYTES);
+                const uint8_t *xs = smem + OFF_PB + pb * XSLOT + XOFF;
                 const uint32_t *fl = (const uint32_t *)(xs + X_FLAG);
                 if ((fl[0] | fl[1] | fl[2] | fl[3]) != 0u) {   // the same answer in every thread
                     // O must hold tile t - 1's product before it is rescaled.  Slot q's
@@ -510,13 +553,14 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
                                int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st) {
     const long units = (long)B * n_splits * (H / ROWS);
     if (units == 0) return cudaSuccess;
-    CUtensorMap mC, mR;
+    CUtensorMap mC, mR, mV;
     cudaError_t e;
     {
         unsigned long long d[3] = {512, (unsigned long long)L, (unsigned long long)B};
         unsigned long long s[2] = {1024, (unsigned long long)L * 1024};
-        unsigned box[3] = {64, NK, 1};
+        unsigned box[3] = {64, NK, 1}, vbox[3] = {64, VSUB, 1};
         if ((e = make_tma_map(&mC, cache, 3, d, s, box)) != cudaSuccess) return e;
+        if ((e = make_tma_map(&mV, cache, 3, d, s, vbox)) != cudaSuccess) return e;
     }
     {
         unsigned long long d[3] = {64, (unsigned long long)L, (unsigned long long)B};
@@ -549,7 +593,7 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
     ProfScope ps("tc_decode_attn", st);
     e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e == cudaSuccess)
-        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, p);
+        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, mV, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
