@@ -203,6 +203,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
 // 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -377,6 +383,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 }
 // K-major tile of 1024-byte atoms stacked along M/N.
 __device__ __forceinline__ uint64_t sdesc_kmajor(const void *tile) { return sdesc_sw128(smem_u32(tile), 16, 1024); }
+// K-major tile with the 32-byte swizzle: rows of 16 16-bit elements (32 bytes), eight
+// rows per 256-byte atom; 16-byte chunk c of row r sits at chunk c ^ ((r >> 2) & 1)
+// (layout type 6).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw32(const void *tile) {
+    return (sdesc_sw128(smem_u32(tile), 16, 256) & ~((uint64_t)7 << 61)) | ((uint64_t)6 << 61);
+}
 // K-major tile with the 64-byte swizzle: rows of 32 16-bit elements (64 bytes), eight
 // rows per 512-byte atom, atoms stacked along M/N; 16-byte chunk c of row r sits at
 // chunk c ^ ((r >> 1) & 3) of the row (layout type 4 in bits 61-63).

@@ -10,20 +10,21 @@
 // One work unit = the 128 heads of one sequence against one key split.  Its fp32
 // accumulator (128 heads x 512 latent dims) fills the whole tensor memory of an SM,
 // so a unit runs on a cluster of two CTAs with different jobs:
-//   rank 0 (scores): Q in bf16 in TMEM; each 96-key tile of the bf16 cache (latent +
+//   rank 0 (scores): Q in bf16 in TMEM; each 80-key tile of the bf16 cache (latent +
 //     RoPE band) arrives through a two-deep TMA ring and is used as it lands; S = Q.K^T
-//     on the tensor core (A from TMEM, N = 96: the widest score tile that fits TMEM
-//     beside Q, and one that runs at the full MMA rate, which N = 64 does not),
-//     double-buffered in TMEM; eight warps run the online softmax (two threads per
-//     head, swapping row maxima through shared memory) and store P in bf16 (already in
-//     the MMA operand layout) with the per-head rescale factors straight into rank 1's
-//     shared memory (st.async, completing bytes on the receiving slot's barrier);
+//     on the tensor core (A from TMEM; an N = 80 MMA costs what an N = 64 one does),
+//     double-buffered in TMEM, issued by two threads that take alternate tiles (one
+//     issuing thread could not keep the tensor pipe fed); eight warps run the online
+//     softmax (two threads per head, swapping row maxima through shared memory) and
+//     stage P in bf16 (already in the MMA operand layout) in one of two staging slots;
+//     a copier warp moves it and the per-head rescale factors into rank 1's shared
+//     memory with two bulk copies;
 //   rank 1 (accumulator): O (128 x 512 fp32) in all 512 TMEM columns; streams the same
-//     tiles' latent rows in 32-key sub-tiles (L2 hits: rank 0 prefetches the tiles into
-//     L2 ahead of use) and issues O += P.C with both operands in shared memory; four
+//     tiles' latent rows (L2 hits: rank 0 prefetches the tiles into L2 ahead of use)
+//     and issues O += P.C with both operands in shared memory; four
 //     warps rescale rows of O when rank 0 reports a grown row maximum, and write the
 //     normalised partial output and the split's log-sum-exp at the end.
-// P only flows from rank 0 to rank 1, through three slots, so rank 0 runs ahead and the
+// P only flows from rank 0 to rank 1, through two slots, so rank 0 runs ahead and the
 // cross-CTA latency stays off the critical path.
 //
 // Precision.  The tensor core takes bf16 against the bf16 cache, but a score's rounding
@@ -41,9 +42,9 @@
 // P multiplies the cache on rank 1 in bf16: its rounding only perturbs the weights of an
 // average (relative 2^-9), and the row sums use the unrounded fp32 probabilities.
 //
-// Warps (320 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 MMA issuer
-// and TMEM owner, 2-9 softmax (two threads per head); rank 1 -- 0 TMA producer, 1 MMA
-// issuer and TMEM owner, 2-5 rescale + epilogue, 6-9 idle.
+// Warps (384 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 and 11 MMA
+// issuers (1 also owns TMEM), 2-9 softmax (two threads per head), 10 copier; rank 1 --
+// 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 rescale + epilogue, 6-11 idle.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -60,31 +61,28 @@ namespace {
 
 using namespace tc;
 
-constexpr int ROWS = 128, NK = 96, NTHREADS = 320;
+constexpr int ROWS = 128, NK = 80, NTHREADS = 384;
 constexpr int KST = 2;     // rank 0: key-tile stages (one per S buffer)
-constexpr int VSUB = 32;   // rank 1: keys per latent sub-tile
-constexpr int VST = 4;     // rank 1: latent sub-tile stages
-constexpr int NPB = 3;     // rank 1: P slots
+constexpr int VST = 2;     // rank 1: latent-tile stages
+constexpr int NPB = 2;     // rank 1: P slots (= rank 0's staging slots)
 constexpr int PF = 4;      // tiles prefetched into L2 ahead of the TMA loads
-constexpr uint32_t KBOX = NK * 128;         // 96 keys x 64 dims, bf16: 12 KB
+constexpr uint32_t KBOX = NK * 128;         // 80 keys x 64 dims, bf16: 10 KB
 constexpr uint32_t KSTAGE = 9 * KBOX;       // boxes 0-7 latent dims, box 8 the RoPE band
-constexpr uint32_t VBOX = VSUB * 128;       // 32 keys x 64 dims: 4 KB
-constexpr uint32_t VSTAGE = 8 * VBOX;       // 512 latent dims
-// One P transfer, written by rank 0's softmax threads straight into a rank-1 slot with
-// st.async (each store completes its bytes on the slot's barrier).  P [128 heads][96
-// keys] bf16 as the K-major A operand of P.C: keys 0-63 in a 128-byte-swizzled block
-// (128 B per head), keys 64-95 in a 64-byte-swizzled block (64 B per head).  Then the
-// per-head extras: rescale factor, 1/l and m + log2(l) (written on the last tile only),
-// and one "some head rescaled" word per lane quarter.
-constexpr uint32_t P_BLK1 = 16384, P_BYTES = 16384 + 8192;
-constexpr uint32_t X_ALPHA = 0, X_INVL = 512, X_LSE = 1024, X_FLAG = 1536;
+constexpr uint32_t VSTAGE = 8 * KBOX;       // 512 latent dims
+// One P transfer.  P [128 heads][80 keys] bf16 as the K-major A operand of P.C: keys
+// 0-63 in a 128-byte-swizzled block (128 B per head), keys 64-79 in a 32-byte-swizzled
+// block (32 B per head).  Then the per-head extras: rescale factor, 1/l and
+// m + log2(l) (meaningful on the last tile), and one "some head rescaled" word per lane
+// quarter.
+constexpr uint32_t P_BLK1 = 16384, P_BYTES = 16384 + 4096;
+constexpr uint32_t X_ALPHA = 0, X_INVL = 512, X_LSE = 1024, X_FLAG = 1536, X_BYTES = X_FLAG + 16;
 constexpr uint32_t XOFF = P_BYTES;           // extras within a rank-1 slot
-constexpr uint32_t XSLOT = 26624;            // rank-1 slot stride (1024-aligned)
-constexpr uint32_t T_BYTES = P_BYTES + 512 + 16, T_BYTES_LAST = T_BYTES + 1024;   // bytes of one transfer
-// rank 0: K stages, then the two halves' row maxima (double-buffered); rank 1: V
-// sub-tile stages, then the P slots.  The barriers sit after both layouts, at the same
-// offset in both CTAs (the peer addresses them by offset).
-constexpr uint32_t OFF_RED = KST * KSTAGE;
+constexpr uint32_t XSLOT = 22528;            // rank-1 slot stride (1024-aligned)
+// rank 0: K stages, two P staging slots, their extras, the two halves' row maxima
+// (double-buffered); rank 1: latent stages, then the P slots.  The barriers sit after
+// both layouts, at the same offset in both CTAs (the peer addresses them by offset).
+constexpr uint32_t OFF_STG = KST * KSTAGE, OFF_EXT = OFF_STG + NPB * P_BYTES, EXT_STRIDE = 1664;
+constexpr uint32_t OFF_RED = OFF_EXT + NPB * EXT_STRIDE;
 constexpr uint32_t OFF_PB = VST * VSTAGE;
 constexpr uint32_t END0 = OFF_RED + 2 * 2 * ROWS * 4, END1 = OFF_PB + NPB * XSLOT;
 constexpr uint32_t OFF_BAR = END0 > END1 ? END0 : END1;
@@ -96,10 +94,12 @@ constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned FULL = 0xffffffffu;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(KSTAGE % 1024 == 0 && OFF_PB % 1024 == 0 && XSLOT % 1024 == 0, "swizzle atoms aligned");
-static_assert(XOFF + X_FLAG + 16 <= XSLOT, "P transfer layout");
+static_assert(KSTAGE % 1024 == 0 && OFF_STG % 1024 == 0 && P_BYTES % 1024 == 0 && OFF_PB % 1024 == 0 &&
+                  XSLOT % 1024 == 0,
+              "swizzle atoms aligned");
+static_assert(XOFF + X_BYTES <= XSLOT && X_BYTES <= EXT_STRIDE && OFF_EXT % 16 == 0, "P transfer layout");
 static_assert(T_QL + 32 <= 512, "TMEM budget of rank 0");
-static_assert(NK % VSUB == 0 && NK % 16 == 0 && NK <= 128, "tile shape");
+static_assert(NK == 80, "P layout: one 64-key block and one 16-key block");
 
 struct DecK {
     int n_splits, row_tiles;
@@ -148,13 +148,13 @@ __device__ void settle() {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-    tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR,
-                     const __grid_constant__ CUtensorMap mV, DecK p) {
+    tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR, DecK p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
-    // rank 0: k_full = the tile landed + S buffer drained
-    uint64_t *k_full = bars, *k_empty = bars + 4, *s_full = bars + 6;
+    // rank 0: k_full = the tile landed + S buffer drained; staged = the softmax warps
+    // have staged the tile's P; stg_free = the copy to rank 1 has read the staging slot
+    uint64_t *k_full = bars, *stg_free = bars + 2, *k_empty = bars + 4, *s_full = bars + 6, *staged = bars + 8;
     uint64_t *q_ready = bars + 10;
     float *red = (float *)(smem + OFF_RED);   // rank 0: [tile parity][half][row] row maxima
     // both: P slot t % NPB consumed by the P.C MMAs of tile t (one multicast commit
@@ -176,8 +176,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         if (rank == 0) {
             for (int s = 0; s < KST; ++s) {
                 mbar_init(&k_full[s], 9);   // the producer's expect_tx + one per softmax warp (S buffer free)
+                mbar_init(&stg_free[s], 1);
                 mbar_init(&k_empty[s], 1);
                 mbar_init(&s_full[s], 1);
+                mbar_init(&staged[s], 8);
             }
             mbar_init(q_ready, 4);
         } else {
@@ -198,7 +200,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             for (int s = 0; s < KST; ++s)
                 for (int i = 0; i < 8; ++i) mbar_arrive(&k_full[s]);
         } else {           // every P slot armed for its first transfer
-            for (int s = 0; s < NPB; ++s) mbar_arrive_expect_tx(&p_full[s], s == nt - 1 ? T_BYTES_LAST : T_BYTES);
+            for (int s = 0; s < NPB; ++s) mbar_arrive_expect_tx(&p_full[s], P_BYTES + X_BYTES);
         }
     }
     if (warp == 1) {
@@ -239,11 +241,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     if (t + PF < nt) prefetch(t + PF);
                 }
             }
-        } else if (warp == 1) {
-            // ------------------------------------------------------ S = Q.K^T issuer
+        } else if (warp == 1 || warp == 11) {
+            // --------------------- S = Q.K^T issuers: warp 1 even tiles, warp 11 odd tiles
             if (lane == 0 && nt > 0) {
                 bool ok = mbar_wait(q_ready, 0, abort, err);
-                for (int t = 0; t < nt && ok; ++t) {
+                for (int t = warp == 1 ? 0 : 1; t < nt && ok; t += 2) {
                     const int s = t & 1;
                     // tile landed and S buffer s drained by the softmax (one barrier)
                     if (!mbar_wait(&k_full[s], (t >> 1) & 1, abort, err)) break;
@@ -266,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
         } else if (warp >= 2 && warp < 10) {
             // ---------------------------------------------------------- softmax warps
-            // two threads per head: warps 2-5 take keys 0-47 of a tile, warps 6-9 keys 48-95
+            // two threads per head: warps 2-5 take keys 0-39 of a tile, warps 6-9 keys 40-79
             const int quad = warp & 3, row = quad * 32 + lane, h = (warp - 2) >> 2;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
             if (nt > 0 && h == 0) {   // this head's Q into TMEM: bf16(q_abs), then the RoPE band's bf16 halves
@@ -300,32 +302,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(q_ready);
             }
-            const uint32_t peer_slot0 = map_peer(smem_u32(smem + OFF_PB), 1);
-            const uint32_t peer_full0 = map_peer(smem_u32(p_full), 1);   // armed by rank 1 itself
             const float c = p.scale_log2;
             constexpr int HK = NK / 2;   // keys per thread
             float m = -INFINITY, l = 0.f;   // running maximum (scaled, log2 units), this half's sum
             bool ok = true;
             for (int t = 0; t < nt; ++t) {
-                const int s = t & 1, pb = t % NPB;
+                const int s = t & 1;
                 ok = __all_sync(FULL, ok && mbar_wait(&s_full[s], (t >> 1) & 1, abort, err));
                 tc_fence_after();
-                uint32_t sa[32], sb[16];
-                if (ok) {   // half 0: columns 0-31, 32-47; half 1: columns 48-63, 64-95
+                uint32_t sa[32], sb[8];
+                if (ok) {   // half 0: columns 0-31, 32-39; half 1: columns 40-47, 48-79
                     const uint32_t base = lb + T_S + s * NK + h * HK;
                     if (h == 0) {
                         tmem_ld32(base, sa);
-                        tmem_ld16(base + 32, sb);
+                        tmem_ld8(base + 32, sb);
                     } else {
-                        tmem_ld16(base, sb);
-                        tmem_ld32(base + 16, sa);
+                        tmem_ld8(base, sb);
+                        tmem_ld32(base + 8, sa);
                     }
                     tmem_ld_wait();
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) sa[e] = 0u;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) sb[e] = 0u;
+                    for (int e = 0; e < 8; ++e) sb[e] = 0u;
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -333,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 float x[HK];   // this thread's keys, in key order
 #pragma unroll
                 for (int e = 0; e < HK; ++e)
-                    x[e] = __uint_as_float(h == 0 ? (e < 32 ? sa[e] : sb[e - 32]) : (e < 16 ? sb[e] : sa[e - 16]));
+                    x[e] = __uint_as_float(h == 0 ? (e < 32 ? sa[e] : sb[e - 32]) : (e < 8 ? sb[e] : sa[e - 8]));
                 const long key0 = w.kb + (long)t * NK + h * HK;
                 if (key0 + HK > w.ke) {
 #pragma unroll
@@ -371,81 +371,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 }
                 l += ((ra[0] + ra[1]) + (ra[2] + ra[3])) + ((ra[4] + ra[5]) + (ra[6] + ra[7]));
                 const bool rescaled = __any_sync(FULL, need && t > 0);
-                // P slot pb of rank 1 is free once its P.C MMAs of tile t - NPB are done
-                if (t >= NPB) ok = __all_sync(FULL, ok && mbar_wait_cluster(&p_empty[pb], ((t / NPB) - 1) & 1, abort, err));
-                if (ok) {
-                    const uint32_t slot = peer_slot0 + pb * XSLOT, bar = peer_full0 + pb * 8;
-                    // 16-byte chunk j (8 keys) of this thread: keys 8j .. 8j+7 of the tile
-#pragma unroll
-                    for (int q = 0; q < HK / 8; ++q) {
-                        const int j = h * (HK / 8) + q;
-                        const uint32_t dst = j < 8 ? slot + row * 128 + ((j ^ (row & 7)) << 4)
-                                                   : slot + P_BLK1 + row * 64 + (((j - 8) ^ ((row >> 1) & 3)) << 4);
-                        st_async_v4(dst, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3], bar);
-                    }
-                    if (h == 0) {
-                        st_async_b32(slot + XOFF + X_ALPHA + row * 4, __float_as_uint(alpha), bar);
-                        if (lane == 0) st_async_b32(slot + XOFF + X_FLAG + quad * 4, rescaled ? 1u : 0u, bar);
-                    }
-                }
+                uint8_t *ext = smem + OFF_EXT + s * EXT_STRIDE;
                 if (t == nt - 1) {   // the row's sum: this half's plus the partner's (the other
                                      // parity's slots: both threads are past their last reads)
                     red[((s ^ 1) * 2 + h) * ROWS + row] = l;
                     named_bar_sync(1, 256);
                     const float lt = l + red[((s ^ 1) * 2 + (h ^ 1)) * ROWS + row];
-                    if (ok && h == 0) {
-                        const uint32_t slot = peer_slot0 + pb * XSLOT, bar = peer_full0 + pb * 8;
-                        st_async_b32(slot + XOFF + X_INVL + row * 4, __float_as_uint(lt > 0.f ? 1.f / lt : 0.f), bar);
-                        st_async_b32(slot + XOFF + X_LSE + row * 4,
-                                     __float_as_uint(lt > 0.f ? m + log2f(lt) : -INFINITY), bar);
+                    if (h == 0) {
+                        ((float *)(ext + X_INVL))[row] = lt > 0.f ? 1.f / lt : 0.f;
+                        ((float *)(ext + X_LSE))[row] = lt > 0.f ? m + log2f(lt) : -INFINITY;
                     }
                 }
+                // staging slot s: its copy of tile t - 2 has read it
+                if (t >= 2) ok = __all_sync(FULL, ok && mbar_wait(&stg_free[s], ((t >> 1) - 1) & 1, abort, err));
+                // 16-byte chunk j holds keys 8j .. 8j+7 of the tile
+                uint8_t *stg = smem + OFF_STG + s * P_BYTES;
+#pragma unroll
+                for (int q = 0; q < HK / 8; ++q) {
+                    const int j = h * (HK / 8) + q;
+                    uint8_t *dst = j < 8 ? stg + row * 128 + ((j ^ (row & 7)) << 4)
+                                         : stg + P_BLK1 + row * 32 + (((j - 8) ^ ((row >> 2) & 1)) << 4);
+                    *(uint4 *)dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+                if (h == 0) {
+                    ((float *)(ext + X_ALPHA))[row] = alpha;
+                    if (lane == 0) ((uint32_t *)(ext + X_FLAG))[quad] = rescaled ? 1u : 0u;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&staged[s]);
+            }
+        } else if (warp == 10) {
+            // ------------------------------- copier: staged P and extras -> rank 1
+            if (lane == 0 && nt > 0) {
+                const uint32_t peer_slot0 = map_peer(smem_u32(smem + OFF_PB), 1);
+                const uint32_t peer_full0 = map_peer(smem_u32(p_full), 1);   // armed by rank 1 itself
+                for (int t = 0; t < nt; ++t) {
+                    const int s = t & 1, pb = t % NPB;
+                    if (!mbar_wait(&staged[s], (t >> 1) & 1, abort, err)) break;
+                    // P slot pb of rank 1 is free once its P.C MMAs of tile t - NPB are done
+                    if (t >= NPB && !mbar_wait_cluster(&p_empty[pb], ((t / NPB) - 1) & 1, abort, err)) break;
+                    const uint32_t dst = peer_slot0 + pb * XSLOT, bar = peer_full0 + pb * 8;
+                    bulk_copy_to_peer(dst, smem + OFF_STG + s * P_BYTES, P_BYTES, bar);
+                    bulk_copy_to_peer(dst + XOFF, smem + OFF_EXT + s * EXT_STRIDE, X_BYTES, bar);
+                    bulk_commit();
+                    bulk_wait_read<0>();   // the staging has been read
+                    mbar_arrive(&stg_free[s]);
+                }
+                bulk_wait_all();   // nothing in flight into the peer at exit
             }
         }
     } else {
         if (warp == 0) {
-            // ---------------------------------- TMA producer (latent rows, 32-key sub-tiles)
+            // ------------------------------------------------ TMA producer (latent rows)
             if (lane == 0 && nt > 0) {
-                tma_prefetch_desc(&mV);
-                for (int g = 0; g < 3 * nt; ++g) {
-                    const int s = g % VST;
-                    if (g >= VST && !mbar_wait(&v_empty[s], ((g / VST) - 1) & 1, abort, err)) break;
+                tma_prefetch_desc(&mC);
+                for (int t = 0; t < nt; ++t) {
+                    const int s = t % VST;
+                    if (t >= VST && !mbar_wait(&v_empty[s], ((t / VST) - 1) & 1, abort, err)) break;
                     uint8_t *dst = smem + s * VSTAGE;
-                    const int key0 = (int)(w.kb + (long)(g / 3) * NK + (g % 3) * VSUB);
+                    const int key0 = (int)(w.kb + (long)t * NK);
                     mbar_arrive_expect_tx(&v_full[s], VSTAGE);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * VBOX, &mV, &v_full[s], 64 * i, key0, w.b);
+                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * KBOX, &mC, &v_full[s], 64 * i, key0, w.b);
                 }
             }
         } else if (warp == 1) {
             // ---------------------------------------------------- O += P.C issuer
             if (lane == 0 && nt > 0) {
-                bool ok = true;
-                for (int t = 0; t < nt && ok; ++t) {
-                    const int pb = t % NPB;
+                for (int t = 0; t < nt; ++t) {
+                    const int s = t % VST, pb = t % NPB;
+                    if (!mbar_wait(&v_full[s], (t / VST) & 1, abort, err)) break;
                     if (!mbar_wait(&pc_ready[pb], (t / NPB) & 1, abort, err)) break;
+                    tc_fence_after();
                     const uint8_t *slot = smem + OFF_PB + pb * XSLOT;
-                    const uint64_t pa0 = sdesc_kmajor(slot), pa1 = sdesc_kmajor_sw64(slot + P_BLK1);
+                    const uint64_t pa0 = sdesc_kmajor(slot), pa1 = sdesc_kmajor_sw32(slot + P_BLK1);
+                    const uint64_t vb = sdesc_mnmajor(smem + s * VSTAGE, KBOX);
 #pragma unroll
-                    for (int i = 0; i < NK / VSUB; ++i) {
-                        const int g = 3 * t + i, s = g % VST;
-                        if (!mbar_wait(&v_full[s], (g / VST) & 1, abort, err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t vb = sdesc_mnmajor(smem + s * VSTAGE, VBOX);
-#pragma unroll
-                        for (int j = 0; j < VSUB / 16; ++j) {   // 16 keys per step; N = 256 latent dims per MMA
-                            const int kk = i * (VSUB / 16) + j;  // key step within the tile
-                            const uint64_t pa = kk < 4 ? pa0 + (uint64_t)(2 * kk) : pa1 + (uint64_t)(2 * (kk - 4));
-                            const uint32_t acc = (t | kk) != 0;
-                            mma_ss(tmem, pa, vb + (uint64_t)(j * (2048 >> 4)), p.idesc_pv, acc);
-                            mma_ss(tmem + 256, pa, vb + (uint64_t)((4 * VBOX + j * 2048) >> 4), p.idesc_pv, acc);
-                        }
-                        mma_commit(&v_empty[s]);
+                    for (int kk = 0; kk < NK / 16; ++kk) {   // 16 keys per step; N = 256 latent dims per MMA
+                        const uint64_t pa = kk < 4 ? pa0 + (uint64_t)(2 * kk) : pa1;
+                        const uint32_t acc = (t | kk) != 0;
+                        mma_ss(tmem, pa, vb + (uint64_t)(kk * (2048 >> 4)), p.idesc_pv, acc);
+                        mma_ss(tmem + 256, pa, vb + (uint64_t)((4 * KBOX + kk * 2048) >> 4), p.idesc_pv, acc);
                     }
-                    if (ok) mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
+                    mma_commit(&v_empty[s]);
+                    mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
                 }
                 mma_commit(o_final);
             }
@@ -460,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 ok = __all_sync(FULL, mbar_wait_cluster(&p_full[pb], (t / NPB) & 1, abort, err));
                 if (!ok) break;
                 if (warp == 2 && lane == 0 && t + NPB < nt)   // arm the slot for tile t + NPB
-                    mbar_arrive_expect_tx(&p_full[pb], t + NPB == nt - 1 ? T_BYTES_LAST : T_BYTES);
+                    mbar_arrive_expect_tx(&p_full[pb], P_BYTES + X_BYTES);
                 const uint8_t *xs = smem + OFF_PB + pb * XSLOT + XOFF;
                 const uint32_t *fl = (const uint32_t *)(xs + X_FLAG);
                 if ((fl[0] | fl[1] | fl[2] | fl[3]) != 0u) {   // the same answer in every thread
@@ -553,14 +563,13 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
                                int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st) {
     const long units = (long)B * n_splits * (H / ROWS);
     if (units == 0) return cudaSuccess;
-    CUtensorMap mC, mR, mV;
+    CUtensorMap mC, mR;
     cudaError_t e;
     {
         unsigned long long d[3] = {512, (unsigned long long)L, (unsigned long long)B};
         unsigned long long s[2] = {1024, (unsigned long long)L * 1024};
-        unsigned box[3] = {64, NK, 1}, vbox[3] = {64, VSUB, 1};
+        unsigned box[3] = {64, NK, 1};
         if ((e = make_tma_map(&mC, cache, 3, d, s, box)) != cudaSuccess) return e;
-        if ((e = make_tma_map(&mV, cache, 3, d, s, vbox)) != cudaSuccess) return e;
     }
     {
         unsigned long long d[3] = {64, (unsigned long long)L, (unsigned long long)B};
@@ -593,7 +602,7 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
     ProfScope ps("tc_decode_attn", st);
     e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e == cudaSuccess)
-        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, mV, p);
+        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
