@@ -1,5 +1,6 @@
-// tc_latent.cu -- latent-space (absorbed-form) attention on the sm_103a tensor cores:
-// the kernel behind the split-KV decode and the absorbed prefill.
+// tc_latent.cu -- latent-space (absorbed-form) attention on the sm_103a tensor cores for
+// the absorbed prefill, and the host side of the split-KV decode (whose attention kernel
+// is in tc_decode.cu).
 //
 // Method: "A Training-Memory Regression in MLA Sequence Parallelism ... LAGA"
 // (arXiv 2607.17644), Fig. 2 absorbed dataflow and "Core claim" (the absorb trick is
@@ -8,9 +9,8 @@
 // (arXiv 2507.07120), "What carries the argument": each key split yields a partial
 // output plus its log-sum-exp, merged later by the rescale-and-sum.
 //
-// Shape of the problem: one work unit = 128 rows (128 heads of one sequence for
-// decode; 128 queries of one head for the absorbed prefill) against a range of keys.
-// Its fp32 accumulator (128 x 512) fills the whole of one SM's TMEM, and Q
+// Shape of the problem: one work unit = 128 queries of one head against the keys they
+// see.  Its fp32 accumulator (128 x 512) fills the whole of one SM's TMEM, and Q
 // (128 x 576) does not fit in shared memory next to the key stages.  So a unit runs
 // on a cluster of two CTAs that split the 512 latent dimensions:
 //   * CTA r holds Q's dims [256r, 256r+256) in TMEM (rank 0 also the 64-dim RoPE
@@ -21,12 +21,11 @@
 //     online softmax;
 //   * each CTA accumulates its own half of the latent output, O_r += P . C_r, with P
 //     from TMEM and the key tile itself as the (MN-major) B operand.
-// Decode reads a bf16 cache; converter warps widen each tile to fp16 in shared memory
-// before the MMAs, so that q_abs can be held in fp16 (11-bit significand) and every
-// score stays within ~3e-4 of exact.
+// The prefill prep writes the latent, q_abs and the rotated q_pe in fp16 (11-bit
+// significand), so every score stays within ~3e-4 of exact.
 //
 // Warps (256 threads): 0 TMA producer, 1 MMA issuer + TMEM owner, 2-5 softmax (one
-// row per thread), 6-7 converters.  The partial-score swap is one 32 KB bulk copy
+// row per thread), 6-7 idle.  The partial-score swap is one 32 KB bulk copy
 // (cp.async.bulk, shared::cta -> shared::cluster) per tile and direction, completing
 // as transaction bytes on the receiver's mbarrier.
 #include <cuda_bf16.h>
@@ -58,20 +57,15 @@ constexpr uint32_t T_O = 0, T_S = 256, T_P = 320, T_Q = 352;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct LatK {
-    int mode;           // 0: decode (partials out), 1: absorbed prefill (o_lat out)
-    int n_splits, row_tiles;
-    long chunk, kv_len; // decode: keys per split, cache length
-    int s_q, q_offset, kv_need, causal, n_qtiles, nh, nb, head_off;   // prefill
+    int s_q, q_offset, kv_need, causal, n_qtiles, nh, nb, head_off;
     const __half *qa;   // q_abs rows (fp16, 512 wide)
     long qa_b, qa_h, qa_r;
     const __half *qp;   // rotated q_pe rows (fp16, 64 wide)
     long qp_b, qp_h, qp_r;
     float scale_log2;
-    float *po, *pl;     // decode partials [split][b][row][512], [split][b][row]
-    long po_s, po_b, pl_s, pl_b;
-    __nv_bfloat16 *ol;  // prefill o_lat [b][i][hl][512]
+    __nv_bfloat16 *ol;  // o_lat [b][i][hl][512]
     long ol_b, ol_h, ol_r;
-    float *lse;         // prefill lse [b][head][i]
+    float *lse;         // lse [b][head][i]
     long l_b, l_h;
     uint32_t idesc_s0, idesc_s1, idesc_pv;
 };
@@ -84,37 +78,26 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Work unit of a cluster: which rows, which keys, where Q lives and where results go.
 struct Unit {
-    int b, split, hl, q0, r0;   // r0: first row (decode: head) of the unit
-    long kb, ke;                // key range [kb, ke)
-    int nt;                     // 64-key tiles
+    int b, hl, q0;   // sequence, head within the shard, first query row
+    long kb, ke;     // key range [kb, ke)
+    int nt;          // 64-key tiles
 };
 
 __device__ __forceinline__ Unit unit_of(const LatK &p, int u) {
     Unit w{};
-    if (p.mode == 0) {
-        w.r0 = (u % p.row_tiles) * ROWS;
-        u /= p.row_tiles;
-        w.split = u % p.n_splits;
-        w.b = u / p.n_splits;
-        w.kb = (long)w.split * p.chunk;
-        w.ke = w.kb + p.chunk < p.kv_len ? w.kb + p.chunk : p.kv_len;
-        if (w.kb > p.kv_len) w.kb = p.kv_len;
-    } else {
-        // (head, batch) pairs fastest, query tiles from the latest (heaviest under the
-        // causal mask) down: the first waves take the heaviest tiles of every head
-        const int hb = u % (p.nh * p.nb);
-        const int qt = p.n_qtiles - 1 - u / (p.nh * p.nb);
-        w.hl = hb % p.nh;
-        w.b = hb / p.nh;
-        w.q0 = qt * ROWS;
-        w.kb = 0;
-        w.ke = p.causal ? min((long)p.kv_need, (long)p.q_offset + w.q0 + ROWS) : (long)p.kv_need;
-    }
+    // (head, batch) pairs fastest, query tiles from the latest (heaviest under the
+    // causal mask) down: the first waves take the heaviest tiles of every head
+    const int hb = u % (p.nh * p.nb);
+    const int qt = p.n_qtiles - 1 - u / (p.nh * p.nb);
+    w.hl = hb % p.nh;
+    w.b = hb / p.nh;
+    w.q0 = qt * ROWS;
+    w.kb = 0;
+    w.ke = p.causal ? min((long)p.kv_need, (long)p.q_offset + w.q0 + ROWS) : (long)p.kv_need;
     w.nt = w.ke > w.kb ? (int)((w.ke - w.kb + NK - 1) / NK) : 0;
     return w;
 }
 
-template <bool CONVERT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     tc_latent_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR, LatK p) {
     extern __shared__ uint8_t smem_raw[];
@@ -124,7 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     float *xbuf = (float *)(stages + ST * STAGE_BYTES);          // received from the peer
     float *sendbuf = (float *)((uint8_t *)xbuf + XBUF_BYTES);    // this CTA's, to the peer
     uint64_t *bars = (uint64_t *)((uint8_t *)sendbuf + XBUF_BYTES);
-    uint64_t *k_full = bars, *k_empty = bars + ST, *c_full = bars + 2 * ST;
+    uint64_t *k_full = bars, *k_empty = bars + ST;
     uint64_t *q_ready = bars + 3 * ST, *s_full = q_ready + 1, *s_free = q_ready + 2, *p_full = q_ready + 3;
     uint64_t *o_done = q_ready + 4, *o_final = q_ready + 5, *x_full = q_ready + 6, *x_empty = q_ready + 7;
     uint32_t *tslot = (uint32_t *)(q_ready + 8);
@@ -139,7 +122,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         for (int s = 0; s < ST; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
-            mbar_init(&c_full[s], 2);   // the two converter warps
         }
         mbar_init(q_ready, 4);
         mbar_init(s_full, 1);
@@ -183,29 +165,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 if (rank == 0) tma_load_3d(dst + 4 * BOX, &mR, &k_full[s], 0, key0, w.b);
             }
         }
-    } else if (warp >= 6) {
-        // ---------------------------------------------- bf16 -> fp16 widening of tiles
-        if (CONVERT) {
-            const int ct = tid - 6 * 32;                  // 0..63
-            const int n16 = (int)(stage_tx / 16);
-            for (int j = 0; j < nt; ++j) {
-                const int s = j % ST;
-                if (!mbar_wait(&k_full[s], (j / ST) & 1, abort, &g_tc_latent_err)) break;
-                uint4 *t = (uint4 *)(stages + s * STAGE_BYTES);
-#pragma unroll 4
-                for (int i = ct; i < n16; i += 64) {
-                    uint4 v = t[i];
-                    uint32_t q[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        q[e] = pack_f16(__uint_as_float(q[e] << 16), __uint_as_float(q[e] & 0xffff0000u));
-                    t[i] = make_uint4(q[0], q[1], q[2], q[3]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c_full[s]);
-            }
-        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && nt > 0) {
@@ -226,8 +185,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             };
             for (int j = 0; j < nt && ok; ++j) {
                 const int s = j % ST;
-                uint64_t *ready = CONVERT ? &c_full[s] : &k_full[s];
-                if (!mbar_wait(ready, (j / ST) & 1, abort, &g_tc_latent_err)) {
+                if (!mbar_wait(&k_full[s], (j / ST) & 1, abort, &g_tc_latent_err)) {
                     ok = false;
                     break;
                 }
@@ -246,20 +204,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             if (ok) issue_pv(nt - 1);
             mma_commit(o_final);
         }
-    } else {
+    } else if (warp < 6) {
         // ---------------------------------------------------------- softmax warps
         const int quad = warp & 3, row = quad * 32 + lane;
         const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
-        const int i = w.q0 + row;                                    // prefill query row
-        const bool valid = p.mode == 0 || i < p.s_q;
-        const long pos = p.mode == 0 ? 0 : (long)p.q_offset + i;
+        const int i = w.q0 + row;   // query row
+        const bool valid = i < p.s_q;
+        const long pos = (long)p.q_offset + i;
         // ---- this row of Q into TMEM: latent dims [256 rank, +256), rank 0 also the RoPE band
         {
-            const __half *qa = p.mode == 0 ? p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r
-                                           : p.qa + w.b * p.qa_b + (long)w.hl * p.qa_h + (long)i * p.qa_r;
-            const __half *qp = p.mode == 0 ? p.qp + w.b * p.qp_b + (long)(w.r0 + row) * p.qp_r
-                                           : p.qp + w.b * p.qp_b + (long)(p.head_off + w.hl) * p.qp_h +
-                                                 (long)i * p.qp_r;
+            const __half *qa = p.qa + w.b * p.qa_b + (long)w.hl * p.qa_h + (long)i * p.qa_r;
+            const __half *qp = p.qp + w.b * p.qp_b + (long)(p.head_off + w.hl) * p.qp_h + (long)i * p.qp_r;
             const uint4 *src = (const uint4 *)(qa + 256 * rank);
             for (int c = 0; c < (rank == 0 ? 5 : 4); ++c) {
                 const uint4 *sp = c < 4 ? src + c * 8 : (const uint4 *)qp;
@@ -346,12 +301,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 mbar_arrive_peer(peer_x_empty);
             }
             const long key0 = w.kb + (long)j * NK;
-            const bool masked = key0 + NK > w.ke || (p.mode == 1 && p.causal && key0 + NK - 1 > (long)p.q_offset + w.q0);
+            const bool masked = key0 + NK > w.ke || (p.causal && key0 + NK - 1 > (long)p.q_offset + w.q0);
             if (masked) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const long key = key0 + c;
-                    if (key >= w.ke || (p.mode == 1 && p.causal && key > pos)) x[c] = -INFINITY;
+                    if (key >= w.ke || (p.causal && key > pos)) x[c] = -INFINITY;
                 }
             }
             // independent accumulators: the reductions are latency chains otherwise
@@ -424,31 +379,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 for (int e = 0; e < 32; ++e) o[e] = 0u;
             }
             if (!ok || !valid) continue;
-            if (p.mode == 0) {
-                float4 *dst = (float4 *)(p.po + w.split * p.po_s + w.b * p.po_b + (long)(w.r0 + row) * 512 +
-                                         256 * rank + c * 32);
+            uint4 *dst = (uint4 *)(p.ol + w.b * p.ol_b + (long)w.hl * p.ol_h + (long)i * p.ol_r + 256 * rank + c * 32);
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                         __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
-            } else {
-                uint4 *dst = (uint4 *)(p.ol + w.b * p.ol_b + (long)w.hl * p.ol_h + (long)i * p.ol_r + 256 * rank +
-                                       c * 32);
+            for (int v = 0; v < 4; ++v) {
+                uint32_t q[4];
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint32_t q[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        q[e] = pack_bf16(__uint_as_float(o[8 * v + 2 * e]) * inv,
-                                         __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
-                    dst[v] = make_uint4(q[0], q[1], q[2], q[3]);
-                }
+                for (int e = 0; e < 4; ++e)
+                    q[e] = pack_bf16(__uint_as_float(o[8 * v + 2 * e]) * inv, __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
+                dst[v] = make_uint4(q[0], q[1], q[2], q[3]);
             }
         }
-        if (ok && valid && rank == 0) {
-            if (p.mode == 0) p.pl[w.split * p.pl_s + w.b * p.pl_b + w.r0 + row] = lse;
-            else p.lse[w.b * p.l_b + (long)(p.head_off + w.hl) * p.l_h + i] = lse;
-        }
+        if (ok && valid && rank == 0) p.lse[w.b * p.l_b + (long)(p.head_off + w.hl) * p.l_h + i] = lse;
     }
     tc_fence_before();
     __syncthreads();
@@ -459,9 +400,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 }  // namespace
 
 // Launches the latent attention over `units` work units (two CTAs each).
-// cache: [B][rows][512] (+ kpe [B][rows][64]); `convert` widens bf16 tiles to fp16.
-cudaError_t launch_latent_attn(const void *cache, const void *kpe, long cache_rows, int B, bool convert, LatK &p,
-                               long units, cudaStream_t st) {
+// cache: [B][rows][512] fp16 (+ kpe [B][rows][64] fp16).
+cudaError_t launch_latent_attn(const void *cache, const void *kpe, long cache_rows, int B, LatK &p, long units,
+                               cudaStream_t st) {
     if (units == 0) return cudaSuccess;
     CUtensorMap mC, mR;
     cudaError_t e;
@@ -482,13 +423,8 @@ cudaError_t launch_latent_attn(const void *cache, const void *kpe, long cache_ro
     p.idesc_pv = idesc_f16(128, 256, true, true);
     dim3 grid((unsigned)(2 * units)), block(256);
     ProfScope ps("tc_latent_attn", st);
-    if (convert) {
-        e = cudaFuncSetAttribute(tc_latent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (e == cudaSuccess) tc_latent_kernel<true><<<grid, block, SMEM_BYTES, st>>>(mC, mR, p);
-    } else {
-        e = cudaFuncSetAttribute(tc_latent_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (e == cudaSuccess) tc_latent_kernel<false><<<grid, block, SMEM_BYTES, st>>>(mC, mR, p);
-    }
+    e = cudaFuncSetAttribute(tc_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e == cudaSuccess) tc_latent_kernel<<<grid, block, SMEM_BYTES, st>>>(mC, mR, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -612,7 +548,6 @@ cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const vo
             if (e != cudaSuccess) return e;
         }
         LatK k{};
-        k.mode = 1;
         k.s_q = p.s_q;
         k.q_offset = p.q_offset;
         k.kv_need = (int)p.kv_need;
@@ -637,7 +572,7 @@ cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const vo
         k.lse = lse;
         k.l_b = HL * p.s_q;
         k.l_h = p.s_q;
-        e = launch_latent_attn(chat, kpe, kv_pad, p.B, false, k, (long)p.B * nh * k.n_qtiles, st);
+        e = launch_latent_attn(chat, kpe, kv_pad, p.B, k, (long)p.B * nh * k.n_qtiles, st);
         if (e != cudaSuccess) return e;
         for (int b = 0; b < p.B; ++b) {
             // out[b][i][h0+hl][d] = sum_k o_lat[b][i][hl][k] W_V(hg+hl)[d][k]
