@@ -8,7 +8,11 @@ tokens, 8 splits).  The headline ``value`` is the prefill's TFLOP/s (algorithmic
 FLOPs: visible causal pairs x 2 x (192 + 128) plus the K/V reconstruction GEMM); the
 ``decode`` object carries the decode's HBM GB/s.  Both are timed per call with CUDA
 events on the launching stream; the prefill's inputs fit in L2, so a 256 MB buffer
-is written between timed calls; the decode's 2.4 GB cache does not.
+is written between timed calls; the decode's 2.4 GB cache does not.  After the timed
+regions, rank 0 at N = 1 also reports the V3-shaped prefill and the simulated SP=8
+rank-7 prefill (``other_prefill_configs``) and the allocator's peak memory of the
+explicit against the absorbed V3 prefill (``activation_memory``); --no-extras skips
+them.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -239,6 +243,50 @@ def dominant(prof: dict, candidates):
     return best
 
 
+def other_prefill_configs(stream, steps=5, warmup=3):
+    """Whole-call throughput of the V3-shaped prefill (128 heads, shards of 16) and of
+    the simulated SP=8 rank 7 (16384 latent rows, last 2048 queries): reported beside
+    the headline, not part of it."""
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import configs
+    res = {}
+    for cfg in (configs.V3, configs.SP8_RANK7):
+        d, t, out, lse, ws = prefill_setup(cfg)
+        fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
+        ms = statistics.mean(timed(fn, steps, warmup, 1))
+        fl = cfg.flops()["total"]
+        res[cfg.name] = {"ms_per_call": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1),
+                         "flops_per_call": fl, "head_shard": cfg.head_shard}
+        del d, t, out, lse, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def activation_memory():
+    """Peak device memory the CUDA caching allocator sees for one V3-shaped prefill call
+    (outputs + workspace), explicit (head shards of 16 and 128) against absorbed."""
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import configs, mla
+    cfg = configs.V3
+    d, t, _, _, _ = prefill_setup(cfg)
+    res = {}
+    for absorbed in (False, True):
+        for hs in (16, cfg.n_heads):
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            base = torch.cuda.memory_allocated()
+            torch.cuda.reset_peak_memory_stats()
+            fn = mla.absorbed_attn_fwd if absorbed else mla.latent_attn_fwd
+            o, l = fn(d, t["q_nope"], t["q_pe"], t["c_kv"], t["k_pe"], t["w_kv_b"], t["rms_w"], head_shard=hs)
+            torch.cuda.synchronize()
+            res["%s_hs%d_MB" % ("absorbed" if absorbed else "explicit", hs)] = round(
+                (torch.cuda.max_memory_allocated() - base) / 1e6, 1)
+            del o, l
+    res["workload"] = cfg.name
+    res["counts"] = "out + lse + workspace, torch.cuda.max_memory_allocated() minus the inputs"
+    return res
+
+
 # -------------------------------------------------------------- our arm ----
 def run_ours(args, world, rank, local):
     import torch
@@ -347,6 +395,15 @@ def run_ours(args, world, rank, local):
     except Exception as ex:  # keep the kernel numbers even if pinning fails
         e2e = {"value": None, "unit": "TFLOP/s", "error": str(ex)[:200]}
 
+    # ---- beside the headline: the other prefill configs and the activation memory
+    # (after every timed region; rank 0 at N = 1 only, so replicas are not slowed)
+    others, mem = None, None
+    if rank == 0 and world == 1 and not args.no_extras:
+        del d, t, out, lse, ws, dd, dt_, dout, dlse, dws, flush
+        torch.cuda.empty_cache()
+        others = other_prefill_configs(stream)
+        mem = activation_memory()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill()
@@ -374,6 +431,8 @@ def run_ours(args, world, rank, local):
                    "tokens_per_s": round(world * dcfg.batch / (d_ms * 1e-3), 1),
                    "kernel_path": {1: "simt", 2: "tcgen05"}.get(dpath, "?"), "roofline": droof,
                    "l2": "inputs (2.4 GB) larger than L2"},
+        "other_prefill_configs": others,
+        "activation_memory": mem,
         "kernels_prefill": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_p.items()},
         "kernels_decode": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_d.items()},
         "peaks": {"kind": peak_kind, "hbm_gbs": peaks.get("hbm_gbs"), "bf16_tflops": peaks.get("bf16_tflops")},
@@ -479,6 +538,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the V3 / SP=8-rank prefill timings and the activation-memory measurement")
     ap.add_argument("--only", choices=("prefill", "decode"), default=None,
                     help="run only this workload's calls, without timing (profiling target)")
     ap.add_argument("--workload", default=None, help="prefill workload name for --only prefill")

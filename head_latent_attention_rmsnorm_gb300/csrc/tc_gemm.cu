@@ -10,7 +10,8 @@
 // absorb / un-absorb products of the absorbed form and of decode (same page, Fig. 2).
 //
 // Persistent kernel: one CTA per SM walks the 128 x BN output tiles of one or two
-// problems (tile t, t + gridDim.x, ...).  Warp 0 lane 0 streams 64-wide k-blocks of
+// problems (tile t, t + gridDim.x, ...); 256-wide problems use the pair kernel below
+// (two SMs per 256 x 256 tile).  Warp 0 lane 0 streams 64-wide k-blocks of
 // A and B through a 4-stage TMA ring that runs across tile boundaries; the MMA
 // issuers accumulate each tile into one of two TMEM accumulators (M=128, K=16 per
 // instruction); warps 2-5 drain a finished accumulator (thread = row) and store it
@@ -231,6 +232,201 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 1) tmem_dealloc(tmem, 2 * ACC_COLS);
 }
 
+// ---------------------------------------------------------------- pair kernel ----
+// The same GEMM on 256 x 256 tiles computed by a cluster of two CTAs (two SMs) with
+// cta_group::2 MMAs (M = 256): CTA r holds A rows [m0 + 128 r, +128) and, of the 256 B
+// rows (output columns), [n0 + 64 r, +64) and [n0 + 128 + 64 r, +64), so every MMA reads
+// half of its operand bytes from each SM.  A one-CTA 128 x 256 tile moves 12 KB of
+// operands per 16-deep MMA step through each SM's shared memory twice (TMA write, MMA
+// read), above the port's 128 B/clk at the tensor rate; the pair moves 8 KB.  The
+// leader (rank 0) issues the MMAs from two threads, each owning 128 output columns
+// (N = 128 per MMA: 64 columns from each CTA); both CTAs load, and both drain their own
+// accumulator rows.
+constexpr int PST = 6;   // stages of the pair kernel's ring
+constexpr uint32_t PA_BYTES = 128 * BK * 2, PB_BYTES = 128 * BK * 2;
+
+__device__ __forceinline__ Tile pair_tile_of(const GemmK &p, int t) {
+    Tile r;
+    r.prob = t < p.pr[0].tiles ? 0 : 1;
+    const GemmP &q = p.pr[r.prob];
+    int u = r.prob ? t - p.pr[0].tiles : t;
+    r.n0 = (u % q.tiles_n) * 256;
+    u /= q.tiles_n;
+    r.m0 = (u % q.tiles_m) * 256;
+    r.batch = u / q.tiles_m;
+    return r;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
+                        const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1, GemmK p) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + PST * PA_BYTES;
+    uint64_t *full = (uint64_t *)(sB + PST * PB_BYTES);   // leader: both CTAs' bytes of a stage landed
+    uint64_t *empty = full + PST;                         // both: the stage's MMAs are done
+    uint64_t *acc_full = empty + PST, *acc_empty = acc_full + 2;
+    uint32_t *tslot = (uint32_t *)(acc_empty + 2);
+    volatile int *abort = (volatile int *)(tslot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
+
+    if (tid == 0) {
+        for (int s = 0; s < PST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 2);   // one commit per issuing thread
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 2);
+            mbar_init(&acc_empty[a], 8);   // the epilogue warps of both CTAs
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tslot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers and TMEM exist before any cross-CTA traffic
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            tma_prefetch_desc(&ta0);
+            tma_prefetch_desc(&tb0);
+            if (p.pr[1].tiles) {
+                tma_prefetch_desc(&ta1);
+                tma_prefetch_desc(&tb1);
+            }
+            const uint32_t full0 = map_peer(smem_u32(full), 0);   // the leader's barriers
+            int it = 0;
+            bool ok = true;
+            for (int t = pair; t < p.total && ok; t += pairs) {
+                const Tile w = pair_tile_of(p, t);
+                const GemmP &q = p.pr[w.prob];
+                const CUtensorMap *ma = w.prob ? &ta1 : &ta0, *mb = w.prob ? &tb1 : &tb0;
+                const int ar = w.m0 + 128 * (int)rank;
+                const int a_r = ar % q.a_rows_per_z, a_z = q.a_zbase + ar / q.a_rows_per_z + w.batch * q.a_z_per_batch;
+                int b_r[2], b_z[2];
+                for (int h = 0; h < 2; ++h) {
+                    const int br = w.n0 + 128 * h + 64 * (int)rank;
+                    b_r[h] = br % q.b_rows_per_z;
+                    b_z[h] = q.b_zbase + br / q.b_rows_per_z + w.batch * q.b_z_per_batch;
+                }
+                for (int kb = 0; kb < q.K / BK; ++kb, ++it) {
+                    const int s = it % PST;
+                    if (it >= PST && !mbar_wait(&empty[s], ((it / PST) - 1) & 1, abort, &g_tc_gemm_err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (PA_BYTES + PB_BYTES));
+                    const uint32_t bar = full0 + s * 8;
+                    tma_load_3d_pair(sA + s * PA_BYTES, ma, bar, kb * BK, a_r, a_z);
+                    tma_load_3d_pair(sB + s * PB_BYTES, mb, bar, kb * BK, b_r[0], b_z[0]);
+                    tma_load_3d_pair(sB + s * PB_BYTES + PB_BYTES / 2, mb, bar, kb * BK, b_r[1], b_z[1]);
+                }
+            }
+        }
+    } else if (rank == 0 && (warp == 1 || warp == 6)) {
+        // -------------------------- MMA issuers (leader): output columns [128 h, +128)
+        if (lane == 0) {
+            const int h = warp == 1 ? 0 : 1;
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int t = pair; t < p.total && ok; t += pairs, ++lt) {
+                const Tile w = pair_tile_of(p, t);
+                const int a = lt & 1;
+                // both CTAs' epilogues have drained what tile lt-2 left in accumulator a
+                if (lt >= 2 && !mbar_wait_cluster(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)) break;
+                const uint32_t d = tmem + a * 256 + h * 128;
+                const int nk = p.pr[w.prob].K / BK;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % PST;
+                    if (!mbar_wait(&full[s], (it / PST) & 1, abort, &g_tc_gemm_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = sdesc_kmajor(sA + s * PA_BYTES);
+                    const uint64_t db = sdesc_kmajor(sB + s * PB_BYTES + h * (PB_BYTES / 2));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) mma_ss_pair(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
+                    mma_commit_pair(&empty[s], 3);
+                }
+                mma_commit_pair(&acc_full[a], 3);
+            }
+        }
+    } else if (warp >= 2 && warp <= 5) {
+        // ------------------------------------ epilogue (both CTAs): thread = row
+        const int quad = warp & 3;
+        const uint32_t acc_empty0 = map_peer(smem_u32(acc_empty), 0);
+        int lt = 0;
+        bool ok = true;
+        for (int t = pair; t < p.total; t += pairs, ++lt) {
+            const Tile w = pair_tile_of(p, t);
+            const GemmP &q = p.pr[w.prob];
+            const int a = lt & 1;
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[a], (lt >> 1) & 1, abort, &g_tc_gemm_err));
+            tc_fence_after();
+            const long row = w.m0 + 128 * (long)rank + quad * 32 + lane;
+            char *C = (char *)q.C;
+            const int esz = q.out_kind == 2 ? 4 : 2;
+            for (int c = 0; c < 8 && ok; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + a * 256 + c * 32, r);
+                tmem_ld_wait();
+                const int nb = w.n0 + c * 32;
+                if (row >= q.M || nb >= q.N) continue;
+                const long base = q.c_batch * w.batch + row * q.c_m;
+                if (q.c_n == 1 && nb + 32 <= q.N) {
+                    if (esz == 2) {
+                        uint32_t o[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float x0 = __uint_as_float(r[2 * i]), x1 = __uint_as_float(r[2 * i + 1]);
+                            o[i] = q.out_kind == 0 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
+                        }
+                        uint4 *dst = (uint4 *)(C + (base + nb) * 2);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    } else {
+                        uint4 *dst = (uint4 *)(C + (base + nb) * 4);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                    }
+                } else {
+                    for (int i = 0; i < 32; ++i) {
+                        const int n = nb + i;
+                        if (n >= q.N) break;
+                        const float x = __uint_as_float(r[i]);
+                        const long off = base + (long)n * q.c_n;
+                        if (q.out_kind == 0) ((__half *)C)[off] = __float2half_rn(x);
+                        else if (q.out_kind == 1) ((__nv_bfloat16 *)C)[off] = __float2bfloat16_rn(x);
+                        else ((float *)C)[off] = x;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_peer(acc_empty0 + a * 8);   // the leader's barrier (own CTA for rank 0)
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // the leader's MMAs read this CTA's shared memory until here
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
 template <int BN>
 size_t gemm_smem() {
     return STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
@@ -244,6 +440,24 @@ int num_sms() {
             n = 148;
     }
     return n;
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap *maps, const GemmK &p, cudaStream_t st) {
+    const size_t sm = PST * (PA_BYTES + PB_BYTES) + 1024 + 256;
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    const int grid = 2 * std::min(p.total, num_sms() / 2);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the previous kernel's tail
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 template <int BN, int NISS>
@@ -276,6 +490,10 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         maxN = std::max(maxN, probs[i].N);
     }
     const int BN = maxN >= 256 ? 256 : (maxN >= 128 ? 128 : 64);
+    // 256-wide problems run on SM pairs: 256 x 256 tiles, A boxes of 128 rows per CTA,
+    // B boxes of 64 rows (two per CTA)
+    const bool pair = BN == 256;
+    const int TM = pair ? 256 : BM, TN = BN;
     CUtensorMap maps[4];
     GemmK p{};
     p.total = 0;
@@ -290,7 +508,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         const GemmProblem &g = probs[i];
         cudaError_t e = make_operand_map(&maps[2 * i], g.A, BM);
         if (e != cudaSuccess) return e;
-        e = make_operand_map(&maps[2 * i + 1], g.B, BN);
+        e = make_operand_map(&maps[2 * i + 1], g.B, pair ? 64 : BN);
         if (e != cudaSuccess) return e;
         q.M = g.M;
         q.N = g.N;
@@ -306,8 +524,8 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         q.c_n = g.c_n;
         q.c_batch = g.c_batch;
         q.out_kind = g.out_kind;
-        q.tiles_n = (g.N + BN - 1) / BN;
-        q.tiles_m = (g.M + BM - 1) / BM;
+        q.tiles_n = (g.N + TN - 1) / TN;
+        q.tiles_m = (g.M + TM - 1) / TM;
         q.tiles = (g.M == 0 || g.N == 0) ? 0 : q.tiles_n * q.tiles_m * g.batch;
         p.total += q.tiles;
     }
@@ -315,8 +533,8 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
     ProfScope ps("tc_gemm", st);
     switch (BN) {
         case 256:
-            p.idesc = tc::idesc_f16(BM, 128, f16);
-            return launch_gemm<256, 2>(maps, p, st);
+            p.idesc = tc::idesc_f16(256, 128, f16);   // cta_group::2: M = 256 across the pair
+            return launch_gemm_pair(maps, p, st);
         case 128:
             p.idesc = tc::idesc_f16(BM, 128, f16);
             return launch_gemm<128, 1>(maps, p, st);
