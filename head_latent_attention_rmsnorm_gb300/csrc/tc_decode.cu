@@ -44,7 +44,7 @@
 //
 // Warps (384 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 and 11 MMA
 // issuers (1 also owns TMEM), 2-9 softmax (two threads per head), 10 copier; rank 1 --
-// 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 rescale + epilogue, 6-11 idle.
+// 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 rescale, 2-9 epilogue, 10-11 idle.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -83,8 +83,8 @@ constexpr uint32_t XSLOT = 22528;            // rank-1 slot stride (1024-aligned
 // both layouts, at the same offset in both CTAs (the peer addresses them by offset).
 constexpr uint32_t OFF_STG = KST * KSTAGE, OFF_EXT = OFF_STG + NPB * P_BYTES, EXT_STRIDE = 1664;
 constexpr uint32_t OFF_RED = OFF_EXT + NPB * EXT_STRIDE;
-constexpr uint32_t OFF_PB = VST * VSTAGE;
-constexpr uint32_t END0 = OFF_RED + 2 * 2 * ROWS * 4, END1 = OFF_PB + NPB * XSLOT;
+constexpr uint32_t OFF_PB = VST * VSTAGE, OFF_RED1 = OFF_PB + NPB * XSLOT;   // rank 1: the epilogue's dot halves
+constexpr uint32_t END0 = OFF_RED + 2 * 2 * ROWS * 4, END1 = OFF_RED1 + 2 * ROWS * 4;
 constexpr uint32_t OFF_BAR = END0 > END1 ? END0 : END1;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
 // rank 0 TMEM columns: S buffers; bf16 q_hi of the latent band (256 columns); the RoPE
@@ -181,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 mbar_init(&s_full[s], 1);
                 mbar_init(&staged[s], 8);
             }
-            mbar_init(q_ready, 4);
+            mbar_init(q_ready, 8);
         } else {
             for (int s = 0; s < NPB; ++s) {
                 mbar_init(&p_full[s], 1);   // this CTA's expect_tx + the bytes of rank 0's stores
@@ -271,30 +271,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // two threads per head: warps 2-5 take keys 0-39 of a tile, warps 6-9 keys 40-79
             const int quad = warp & 3, row = quad * 32 + lane, h = (warp - 2) >> 2;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
-            if (nt > 0 && h == 0) {   // this head's Q into TMEM: bf16(q_abs), then the RoPE band's bf16 halves
+            if (nt > 0) {
+                // this head's Q into TMEM: bf16(q_abs) (steps 0-15), then the RoPE band's
+                // bf16 halves (steps 16-17), 32 fp16 values per step; the head's two
+                // threads take nine steps each, loaded three steps at a time
                 const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r);
                 const uint4 *qp = (const uint4 *)(p.qp + w.b * p.qp_b + (long)(w.r0 + row) * p.qp_r);
-                for (int c = 0; c < 18; ++c) {   // 32 fp16 values per step
-                    const uint4 *sp = c < 16 ? qa + c * 4 : qp + (c - 16) * 4;
-                    uint32_t hi[16], lo[16];
+                const int c0 = 9 * h;
+                for (int b3 = 0; b3 < 9; b3 += 3) {
+                    uint4 xq[3][4];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 x = sp[v];
-                        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+                    for (int i = 0; i < 3; ++i) {
+                        const int c = c0 + b3 + i;
+                        const uint4 *sp = c < 16 ? qa + c * 4 : qp + (c - 16) * 4;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
-                            const uint32_t hb = pack_bf16(f.x, f.y);
-                            hi[4 * v + e] = hb;
-                            lo[4 * v + e] =
-                                pack_bf16(f.x - __uint_as_float(hb << 16), f.y - __uint_as_float(hb & 0xffff0000u));
-                        }
+                        for (int v = 0; v < 4; ++v) xq[i][v] = sp[v];
                     }
-                    if (c < 16) {
-                        tmem_st16(lb + T_Q + c * 16, hi);
-                    } else {
-                        tmem_st16(lb + T_QP + (c - 16) * 16, hi);
-                        tmem_st16(lb + T_QL + (c - 16) * 16, lo);
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) {
+                        const int c = c0 + b3 + i;
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint32_t u[4] = {xq[i][v].x, xq[i][v].y, xq[i][v].z, xq[i][v].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
+                                const uint32_t hb = pack_bf16(f.x, f.y);
+                                hi[4 * v + e] = hb;
+                                lo[4 * v + e] = pack_bf16(f.x - __uint_as_float(hb << 16),
+                                                          f.y - __uint_as_float(hb & 0xffff0000u));
+                            }
+                        }
+                        if (c < 16) {
+                            tmem_st16(lb + T_Q + c * 16, hi);
+                        } else {
+                            tmem_st16(lb + T_QP + (c - 16) * 16, hi);
+                            tmem_st16(lb + T_QL + (c - 16) * 16, lo);
+                        }
                     }
                 }
                 tmem_st_wait();
@@ -459,13 +473,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 }
                 mma_commit(o_final);
             }
-        } else if (warp >= 2 && warp < 6) {
-            // ------------------------------------------- row rescale + epilogue warps
-            const int quad = warp & 3, row = quad * 32 + lane;
+        } else if (warp >= 2 && warp < 10) {
+            // ------------------------ row rescale (warps 2-5) + epilogue (warps 2-9)
+            const int quad = warp & 3, row = quad * 32 + lane, g = (warp - 2) >> 2;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
             float inv_l = 0.f, lse2 = -INFINITY;   // 1/l and m + log2(l) from rank 0's last transfer
             bool ok = true;
-            for (int t = 0; t < nt && ok; ++t) {
+            for (int t = 0; t < nt && ok && g == 0; ++t) {
                 const int pb = t % NPB;
                 ok = __all_sync(FULL, mbar_wait_cluster(&p_full[pb], (t / NPB) & 1, abort, err));
                 if (!ok) break;
@@ -478,9 +492,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     // previous phase is waited for first, so the parity test is never
                     // two phases behind.
                     const int q = (t - 1) % NPB, k = (t - 1) / NPB;
-                    bool g = k == 0 || mbar_wait(&p_empty[q], (k - 1) & 1, abort, err);
-                    g = g && mbar_wait(&p_empty[q], k & 1, abort, err);
-                    ok = __all_sync(FULL, g);
+                    bool gw = k == 0 || mbar_wait(&p_empty[q], (k - 1) & 1, abort, err);
+                    gw = gw && mbar_wait(&p_empty[q], k & 1, abort, err);
+                    ok = __all_sync(FULL, gw);
                     if (!ok) break;
                     tc_fence_after();
                     const float a = ((const float *)(xs + X_ALPHA))[row];
@@ -504,19 +518,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pc_ready[pb]);
             }
-            // ---- epilogue: the normalised partial output of this split, and its
-            // log-sum-exp with the first-order term of the latent q_lo added
+            // ---- epilogue: the normalised partial output of this split (warps 2-5 latent
+            // dims 0-255, warps 6-9 dims 256-511) and its log-sum-exp with the first-order
+            // term of the latent q_lo added.  The q_abs row is loaded before the wait.
+            const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r) + 32 * g;
+            uint4 qv[16];   // the first half of this thread's 256 q_abs values
+#pragma unroll
+            for (int v = 0; v < 16; ++v) qv[v] = qa[v];
+            // 1/l of the row from the warps that received the transfers
+            float *red1 = (float *)(smem + OFF_RED1);
+            if (g == 0) red1[ROWS + row] = inv_l;
+            named_bar_sync(2, 256);
+            if (g == 1) inv_l = red1[ROWS + row];
             if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, err);
             ok = __all_sync(FULL, ok);
             tc_fence_after();
+            float dot[4] = {0.f, 0.f, 0.f, 0.f};
             if (ok) {
-                float *dst = p.po + w.split * p.po_s + w.b * p.po_b + (long)(w.r0 + row) * 512;
-                const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r);
-                float dot[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int cc = 0; cc < 16; ++cc) {
+                float *dst = p.po + w.split * p.po_s + w.b * p.po_b + (long)(w.r0 + row) * 512 + 256 * g;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    if (cc == 4) {   // the second half of the q_abs values
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) qv[v] = qa[16 + v];
+                    }
                     uint32_t o[32];
                     if (nt > 0) {
-                        tmem_ld32(lb + cc * 32, o);
+                        tmem_ld32(lb + 256 * g + cc * 32, o);
                         tmem_ld_wait();
                     } else {
 #pragma unroll
@@ -530,18 +558,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     for (int v = 0; v < 8; ++v) d4[v] = make_float4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {   // q_lo = q - bf16(q), rounded as rank 0 rounded q_hi
-                        const uint4 x = qa[cc * 4 + v];
+                        const uint4 x = qv[(cc & 3) * 4 + v];
                         const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
-                            const uint32_t h = pack_bf16(f.x, f.y);
-                            dot[e] = fmaf(f.x - __uint_as_float(h << 16), ov[8 * v + 2 * e], dot[e]);
-                            dot[e] = fmaf(f.y - __uint_as_float(h & 0xffff0000u), ov[8 * v + 2 * e + 1], dot[e]);
+                            const uint32_t hb = pack_bf16(f.x, f.y);
+                            dot[e] = fmaf(f.x - __uint_as_float(hb << 16), ov[8 * v + 2 * e], dot[e]);
+                            dot[e] = fmaf(f.y - __uint_as_float(hb & 0xffff0000u), ov[8 * v + 2 * e + 1], dot[e]);
                         }
                     }
                 }
-                const float corr = ((dot[0] + dot[1]) + (dot[2] + dot[3])) * p.scale_log2;
+            }
+            // the two halves' dot products meet in shared memory
+            if (g == 1) red1[row] = (dot[0] + dot[1]) + (dot[2] + dot[3]);
+            named_bar_sync(3, 256);
+            if (g == 0 && ok) {
+                const float corr = ((dot[0] + dot[1]) + (dot[2] + dot[3]) + red1[row]) * p.scale_log2;
                 p.pl[w.split * p.pl_s + w.b * p.pl_b + w.r0 + row] =
                     nt > 0 && lse2 > -INFINITY ? (lse2 + corr) * 0.69314718055994531f : -INFINITY;
             }
