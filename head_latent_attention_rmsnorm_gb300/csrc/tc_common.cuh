@@ -103,6 +103,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)m) : "memory");
 }
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1,
                                             int c2) {
     asm volatile(
@@ -136,6 +143,14 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m
         "%4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"((uint64_t)m), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// Tile store shared -> global through a 2-D TMA map (bulk-group completion: wait with
+// bulk_wait_read / bulk_wait_all after bulk_commit).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)m),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // Named barrier `id` over `n` threads (a multiple of 32) of the CTA.

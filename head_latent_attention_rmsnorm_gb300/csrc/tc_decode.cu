@@ -148,14 +148,16 @@ __device__ void settle() {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-    tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR, DecK p) {
+    tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR,
+                     const __grid_constant__ CUtensorMap mP, const __grid_constant__ CUtensorMap mQa,
+                     const __grid_constant__ CUtensorMap mQp, DecK p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
     // rank 0: k_full = the tile landed + S buffer drained; staged = the softmax warps
     // have staged the tile's P; stg_free = the copy to rank 1 has read the staging slot
     uint64_t *k_full = bars, *stg_free = bars + 2, *k_empty = bars + 4, *s_full = bars + 6, *staged = bars + 8;
-    uint64_t *q_ready = bars + 10;
+    uint64_t *q_ready = bars + 10, *q_full = bars + 30;   // Q in TMEM / Q staged in the K stages
     float *red = (float *)(smem + OFF_RED);   // rank 0: [tile parity][half][row] row maxima
     // both: P slot t % NPB consumed by the P.C MMAs of tile t (one multicast commit
     // completes it in both CTAs)
@@ -182,6 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 mbar_init(&staged[s], 8);
             }
             mbar_init(q_ready, 8);
+            mbar_init(q_full, 1);
         } else {
             for (int s = 0; s < NPB; ++s) {
                 mbar_init(&p_full[s], 1);   // this CTA's expect_tx + the bytes of rank 0's stores
@@ -227,8 +230,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         l2_prefetch(p.cache + (row + r) * 512, (uint32_t)min(16, rows - r) * 1024u);
                     l2_prefetch(p.kpe + row * 64, (uint32_t)rows * 128u);
                 };
+                // the unit's Q block (128 heads: q_abs in eight 64-dim boxes, the rotated
+                // q_pe in one) staged in the K stages; the softmax threads move it to TMEM
+                tma_prefetch_desc(&mQa);
+                tma_prefetch_desc(&mQp);
+                const int qrow = w.b * p.row_tiles * ROWS + w.r0;
+                mbar_arrive_expect_tx(q_full, 9 * 128 * 128);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) tma_load_2d(smem + i * 16384, &mQa, q_full, 64 * i, qrow);
+                tma_load_2d(smem + 8 * 16384, &mQp, q_full, 0, qrow);
                 for (int t = 0; t < nt && t < PF; ++t) prefetch(t);
-                for (int t = 0; t < nt; ++t) {
+                // the stages hold Q until it is in TMEM
+                bool go = mbar_wait(q_ready, 0, abort, err);
+                for (int t = 0; t < nt && go; ++t) {
                     const int s = t & 1;
                     const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of tile t - 2 in this stage
                     if (t >= KST && !mbar_wait(&k_empty[s], ph, abort, err)) break;
@@ -272,43 +286,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const int quad = warp & 3, row = quad * 32 + lane, h = (warp - 2) >> 2;
             const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
             if (nt > 0) {
-                // this head's Q into TMEM: bf16(q_abs) (steps 0-15), then the RoPE band's
-                // bf16 halves (steps 16-17), 32 fp16 values per step; the head's two
-                // threads take nine steps each, loaded three steps at a time
-                const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r);
-                const uint4 *qp = (const uint4 *)(p.qp + w.b * p.qp_b + (long)(w.r0 + row) * p.qp_r);
-                const int c0 = 9 * h;
-                for (int b3 = 0; b3 < 9; b3 += 3) {
-                    uint4 xq[3][4];
+                // this head's Q into TMEM from the staged block: bf16(q_abs) (steps 0-15),
+                // then the RoPE band's bf16 halves (steps 16-17), 32 fp16 values per step; a
+                // step is half a 128-byte row of a box (16-byte chunk j at j ^ (row mod 8));
+                // the head's two threads take nine steps each
+                const bool staged_q = __all_sync(FULL, mbar_wait(q_full, 0, abort, err));
+                for (int c = 9 * h; c < 9 * h + 9 && staged_q; ++c) {
+                    const uint8_t *box = smem + (c < 16 ? (c >> 1) : 8) * 16384 + row * 128;
+                    const int half = c < 16 ? (c & 1) : c - 16;
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int i = 0; i < 3; ++i) {
-                        const int c = c0 + b3 + i;
-                        const uint4 *sp = c < 16 ? qa + c * 4 : qp + (c - 16) * 4;
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 x = *(const uint4 *)(box + (((half * 4 + v) ^ (row & 7)) << 4));
+                        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) xq[i][v] = sp[v];
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
+                            const uint32_t hb = pack_bf16(f.x, f.y);
+                            hi[4 * v + e] = hb;
+                            lo[4 * v + e] =
+                                pack_bf16(f.x - __uint_as_float(hb << 16), f.y - __uint_as_float(hb & 0xffff0000u));
+                        }
                     }
-#pragma unroll
-                    for (int i = 0; i < 3; ++i) {
-                        const int c = c0 + b3 + i;
-                        uint32_t hi[16], lo[16];
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint32_t u[4] = {xq[i][v].x, xq[i][v].y, xq[i][v].z, xq[i][v].w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
-                                const uint32_t hb = pack_bf16(f.x, f.y);
-                                hi[4 * v + e] = hb;
-                                lo[4 * v + e] = pack_bf16(f.x - __uint_as_float(hb << 16),
-                                                          f.y - __uint_as_float(hb & 0xffff0000u));
-                            }
-                        }
-                        if (c < 16) {
-                            tmem_st16(lb + T_Q + c * 16, hi);
-                        } else {
-                            tmem_st16(lb + T_QP + (c - 16) * 16, hi);
-                            tmem_st16(lb + T_QL + (c - 16) * 16, lo);
-                        }
+                    if (c < 16) {
+                        tmem_st16(lb + T_Q + c * 16, hi);
+                    } else {
+                        tmem_st16(lb + T_QP + (c - 16) * 16, hi);
+                        tmem_st16(lb + T_QL + (c - 16) * 16, lo);
                     }
                 }
                 tmem_st_wait();
@@ -448,6 +452,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     mbar_arrive_expect_tx(&v_full[s], VSTAGE);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * KBOX, &mC, &v_full[s], 64 * i, key0, w.b);
+                    if (t == (nt > 3 ? nt - 3 : 0)) {   // the epilogue's q_abs rows (128 KB) into L2
+                        const __half *q0 = p.qa + w.b * p.qa_b + (long)w.r0 * p.qa_r;
+                        for (int k = 0; k < 8; ++k) l2_prefetch(q0 + k * 16 * 512, 16 * 1024);
+                    }
                 }
             }
         } else if (warp == 1) {
@@ -535,7 +543,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
             float dot[4] = {0.f, 0.f, 0.f, 0.f};
             if (ok) {
-                float *dst = p.po + w.split * p.po_s + w.b * p.po_b + (long)(w.r0 + row) * 512 + 256 * g;
+                // 32 x 32 fp32 blocks staged per warp in the (now idle) latent stages, 128-byte
+                // swizzled (chunk j of a row at j ^ (row mod 8)), written by TMA tile stores
+                uint8_t *blk = smem + (warp - 2) * 8192;
+                const int prow = (int)(((long)w.split * p.po_s + w.b * p.po_b) / 512) + w.r0 + quad * 32;
+                if (lane == 0) tma_prefetch_desc(&mP);
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
                     if (cc == 4) {   // the second half of the q_abs values
@@ -553,9 +565,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     float ov[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(o[e]) * inv_l;
-                    float4 *d4 = (float4 *)(dst + cc * 32);
+                    uint8_t *buf = blk + (cc & 1) * 4096;
+                    if (cc >= 2) {   // this buffer's store from two chunks ago has read it
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+                    }
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) d4[v] = make_float4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
+                    for (int v = 0; v < 8; ++v)
+                        *(float4 *)(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+                            make_float4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {   // columns in fp16 units of the map: 2 per fp32 value
+                        tma_store_2d(&mP, buf, (256 * g + 32 * cc) * 2, prow);
+                        bulk_commit();
+                    }
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {   // q_lo = q - bf16(q), rounded as rank 0 rounded q_hi
                         const uint4 x = qv[(cc & 3) * 4 + v];
@@ -570,6 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
+            if (lane == 0) bulk_wait_all();   // the partial output is written before exit
             // the two halves' dot products meet in shared memory
             if (g == 1) red1[row] = (dot[0] + dot[1]) + (dot[2] + dot[3]);
             named_bar_sync(3, 256);
@@ -596,8 +621,21 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
                                int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st) {
     const long units = (long)B * n_splits * (H / ROWS);
     if (units == 0) return cudaSuccess;
-    CUtensorMap mC, mR;
+    CUtensorMap mC, mR, mP, mQa, mQp;
     cudaError_t e;
+    {   // q_abs [B * H][512] and the rotated q_pe [B * H][64], fp16, boxes of 128 rows
+        unsigned long long d[2] = {512, (unsigned long long)B * H}, s[1] = {1024};
+        unsigned box[2] = {64, 128};
+        if ((e = make_tma_map(&mQa, qa, 2, d, s, box)) != cudaSuccess) return e;
+        unsigned long long dp[2] = {64, (unsigned long long)B * H}, sp[1] = {128};
+        if ((e = make_tma_map(&mQp, qp, 2, dp, sp, box)) != cudaSuccess) return e;
+    }
+    {   // the fp32 partial output as rows of 1024 16-bit units (2 KB), boxes of 32 x 32 fp32
+        unsigned long long d[2] = {1024, (unsigned long long)n_splits * B * H};
+        unsigned long long s[1] = {2048};
+        unsigned box[2] = {64, 32};
+        if ((e = make_tma_map(&mP, po, 2, d, s, box)) != cudaSuccess) return e;
+    }
     {
         unsigned long long d[3] = {512, (unsigned long long)L, (unsigned long long)B};
         unsigned long long s[2] = {1024, (unsigned long long)L * 1024};
@@ -635,7 +673,7 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
     ProfScope ps("tc_decode_attn", st);
     e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e == cudaSuccess)
-        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, p);
+        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, mP, mQa, mQp, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
