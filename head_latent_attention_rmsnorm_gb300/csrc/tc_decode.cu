@@ -84,6 +84,10 @@ constexpr uint32_t XSLOT = 22528;            // rank-1 slot stride (1024-aligned
 constexpr uint32_t OFF_STG = KST * KSTAGE, OFF_EXT = OFF_STG + NPB * P_BYTES, EXT_STRIDE = 1664;
 constexpr uint32_t OFF_RED = OFF_EXT + NPB * EXT_STRIDE;
 constexpr uint32_t OFF_PB = VST * VSTAGE, OFF_RED1 = OFF_PB + NPB * XSLOT;   // rank 1: the epilogue's dot halves
+// rank 1's epilogue, in the latent stages once the last MMAs are done: eight 4 KB output
+// staging buffers, then the q_abs block (eight 16 KB boxes)
+constexpr uint32_t QB_OFF = 8 * 4096;
+static_assert(QB_OFF + 8 * 16384 <= OFF_PB, "epilogue staging fits the latent stages");
 constexpr uint32_t END0 = OFF_RED + 2 * 2 * ROWS * 4, END1 = OFF_RED1 + 2 * ROWS * 4;
 constexpr uint32_t OFF_BAR = END0 > END1 ? END0 : END1;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
@@ -158,6 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // have staged the tile's P; stg_free = the copy to rank 1 has read the staging slot
     uint64_t *k_full = bars, *stg_free = bars + 2, *k_empty = bars + 4, *s_full = bars + 6, *staged = bars + 8;
     uint64_t *q_ready = bars + 10, *q_full = bars + 30;   // Q in TMEM / Q staged in the K stages
+    uint64_t *qb_full = bars + 31;   // rank 1: the q_abs block staged for the epilogue
     float *red = (float *)(smem + OFF_RED);   // rank 0: [tile parity][half][row] row maxima
     // both: P slot t % NPB consumed by the P.C MMAs of tile t (one multicast commit
     // completes it in both CTAs)
@@ -195,6 +200,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 mbar_init(&v_empty[s], 1);
             }
             mbar_init(o_final, 1);
+            mbar_init(qb_full, 1);
         }
         for (int s = 0; s < NPB; ++s) mbar_init(&p_empty[s], 1);
         *abort = 0;
@@ -457,6 +463,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         for (int k = 0; k < 8; ++k) l2_prefetch(q0 + k * 16 * 512, 16 * 1024);
                     }
                 }
+                // once the last P.C MMAs are done the latent stages are free: the unit's
+                // q_abs block goes there for the epilogue (eight 64-dim boxes of 128 rows)
+                if (mbar_wait(o_final, 0, abort, err)) {
+                    tma_prefetch_desc(&mQa);
+                    const int qrow = w.b * p.row_tiles * ROWS + w.r0;
+                    mbar_arrive_expect_tx(qb_full, 8 * 128 * 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) tma_load_2d(smem + QB_OFF + i * 16384, &mQa, qb_full, 64 * i, qrow);
+                }
             }
         } else if (warp == 1) {
             // ---------------------------------------------------- O += P.C issuer
@@ -529,31 +544,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // ---- epilogue: the normalised partial output of this split (warps 2-5 latent
             // dims 0-255, warps 6-9 dims 256-511) and its log-sum-exp with the first-order
             // term of the latent q_lo added.  The q_abs row is loaded before the wait.
-            const uint4 *qa = (const uint4 *)(p.qa + w.b * p.qa_b + (long)(w.r0 + row) * p.qa_r) + 32 * g;
-            uint4 qv[16];   // the first half of this thread's 256 q_abs values
-#pragma unroll
-            for (int v = 0; v < 16; ++v) qv[v] = qa[v];
             // 1/l of the row from the warps that received the transfers
             float *red1 = (float *)(smem + OFF_RED1);
             if (g == 0) red1[ROWS + row] = inv_l;
             named_bar_sync(2, 256);
             if (g == 1) inv_l = red1[ROWS + row];
             if (ok && nt > 0) ok = mbar_wait(o_final, 0, abort, err);
+            if (ok && nt > 0) ok = mbar_wait(qb_full, 0, abort, err);
             ok = __all_sync(FULL, ok);
             tc_fence_after();
             float dot[4] = {0.f, 0.f, 0.f, 0.f};
             if (ok) {
                 // 32 x 32 fp32 blocks staged per warp in the (now idle) latent stages, 128-byte
                 // swizzled (chunk j of a row at j ^ (row mod 8)), written by TMA tile stores
-                uint8_t *blk = smem + (warp - 2) * 8192;
+                uint8_t *buf = smem + (warp - 2) * 4096;
                 const int prow = (int)(((long)w.split * p.po_s + w.b * p.po_b) / 512) + w.r0 + quad * 32;
                 if (lane == 0) tma_prefetch_desc(&mP);
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
-                    if (cc == 4) {   // the second half of the q_abs values
-#pragma unroll
-                        for (int v = 0; v < 16; ++v) qv[v] = qa[16 + v];
-                    }
                     uint32_t o[32];
                     if (nt > 0) {
                         tmem_ld32(lb + 256 * g + cc * 32, o);
@@ -565,9 +573,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     float ov[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(o[e]) * inv_l;
-                    uint8_t *buf = blk + (cc & 1) * 4096;
-                    if (cc >= 2) {   // this buffer's store from two chunks ago has read it
-                        if (lane == 0) bulk_wait_read<1>();
+                    if (cc >= 1) {   // the previous chunk's store has read the buffer
+                        if (lane == 0) bulk_wait_read<0>();
                         __syncwarp();
                     }
 #pragma unroll
@@ -580,9 +587,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                         tma_store_2d(&mP, buf, (256 * g + 32 * cc) * 2, prow);
                         bulk_commit();
                     }
+                    // dims 256 g + 32 cc .. +31: half (cc & 1) of the row of box 4 g + cc / 2
+                    const uint8_t *qrow_s = smem + QB_OFF + (4 * g + cc / 2) * 16384 + row * 128;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {   // q_lo = q - bf16(q), rounded as rank 0 rounded q_hi
-                        const uint4 x = qv[(cc & 3) * 4 + v];
+                        const uint4 x = *(const uint4 *)(qrow_s + ((((cc & 1) * 4 + v) ^ (row & 7)) << 4));
                         const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
