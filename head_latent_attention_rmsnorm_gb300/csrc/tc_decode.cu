@@ -560,7 +560,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 uint8_t *buf = smem + (warp - 2) * 4096;
                 const int prow = (int)(((long)w.split * p.po_s + w.b * p.po_b) / 512) + w.r0 + quad * 32;
                 if (lane == 0) tma_prefetch_desc(&mP);
-#pragma unroll
+                // kept rolled: the body's code is fetched once (the cache stream leaves no code in L2)
+#pragma unroll 1
                 for (int cc = 0; cc < 8; ++cc) {
                     uint32_t o[32];
                     if (nt > 0) {
