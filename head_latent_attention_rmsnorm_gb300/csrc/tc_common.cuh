@@ -132,6 +132,10 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
 __device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)p), "r"(bytes) : "memory");
 }
+// Hints the 128-byte line holding `p` into L2 through the load/store path (no TMA unit).
+__device__ __forceinline__ void l2_prefetch_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"((uint64_t)__cvta_generic_to_global(p)));
+}
 
 // The same load for a CTA pair running cta_group::2 MMAs: the destination is this
 // CTA's shared memory, the completion is counted on `bar_cluster` (a shared::cluster
@@ -235,6 +239,13 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+// True in exactly one lane of the (fully active) warp.  MMA issue loops run on the whole
+// warp and issue from the elected lane, which keeps the loop warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+    return pred != 0;
 }
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {

@@ -263,27 +263,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
         } else if (warp == 1 || warp == 11) {
             // --------------------- S = Q.K^T issuers: warp 1 even tiles, warp 11 odd tiles
-            if (lane == 0 && nt > 0) {
-                bool ok = mbar_wait(q_ready, 0, abort, err);
+            // The whole warp runs the loop and one elected lane issues: with warp-uniform
+            // control flow the operands stay in uniform registers and an MMA issues in
+            // about two thirds of the time a lane-divergent issuer takes.
+            if (nt > 0) {
+                bool ok = __all_sync(FULL, mbar_wait(q_ready, 0, abort, err));
                 for (int t = warp == 1 ? 0 : 1; t < nt && ok; t += 2) {
                     const int s = t & 1;
                     // tile landed and S buffer s drained by the softmax (one barrier)
-                    if (!mbar_wait(&k_full[s], (t >> 1) & 1, abort, err)) break;
+                    if (!__all_sync(FULL, mbar_wait(&k_full[s], (t >> 1) & 1, abort, err))) break;
                     tc_fence_after();
                     // descriptors as constant offsets from one base: the issuing thread
                     // spends no arithmetic between MMAs
                     const uint64_t d0 = sdesc_kmajor(smem + s * KSTAGE);
                     const uint32_t dt = tmem + T_S + s * NK, at = tmem + T_Q;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < 32; ++kk)   // latent band: 16 dims per step, q_hi only
-                        mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s,
-                               kk != 0);
+                        for (int kk = 0; kk < 32; ++kk)   // latent band: 16 dims per step, q_hi only
+                            mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (KBOX >> 4) + 2 * (kk & 3)),
+                                   p.idesc_s, kk != 0);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)    // RoPE band: q_hi then q_lo against the same box
-                        mma_ts(dt, tmem + (kk < 4 ? T_QP : T_QL) + (kk & 3) * 8,
-                               d0 + (uint64_t)(8 * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
-                    mma_commit(&k_empty[s]);
-                    mma_commit(&s_full[s]);
+                        for (int kk = 0; kk < 8; ++kk)    // RoPE band: q_hi then q_lo against the same box
+                            mma_ts(dt, tmem + (kk < 4 ? T_QP : T_QL) + (kk & 3) * 8,
+                                   d0 + (uint64_t)(8 * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
+                        mma_commit(&k_empty[s]);
+                        mma_commit(&s_full[s]);
+                    }
+                    __syncwarp();
                 }
             }
         } else if (warp >= 2 && warp < 10) {
