@@ -13,14 +13,15 @@
 //   rank 0 (scores): Q in bf16 in TMEM; each 80-key tile of the bf16 cache (latent +
 //     RoPE band) arrives through a two-deep TMA ring and is used as it lands; S = Q.K^T
 //     on the tensor core (A from TMEM; an N = 80 MMA costs what an N = 64 one does),
-//     double-buffered in TMEM, issued by two threads that take alternate tiles (one
-//     issuing thread could not keep the tensor pipe fed); eight warps run the online
+//     double-buffered in TMEM, issued by two warps that take alternate tiles, each
+//     running its loop warp-uniformly and issuing from one elected lane; eight warps run the online
 //     softmax (two threads per head, swapping row maxima through shared memory) and
 //     stage P in bf16 (already in the MMA operand layout) in one of two staging slots;
 //     a copier warp moves it and the per-head rescale factors into rank 1's shared
 //     memory with two bulk copies;
 //   rank 1 (accumulator): O (128 x 512 fp32) in all 512 TMEM columns; streams the same
-//     tiles' latent rows (L2 hits: rank 0 prefetches the tiles into L2 ahead of use)
+//     tiles' latent rows (L2 hits: an idle warp here prefetches rank 0's next tiles
+//     into L2, away from rank 0's TMA unit)
 //     and issues O += P.C with both operands in shared memory; four
 //     warps rescale rows of O when rank 0 reports a grown row maximum, and write the
 //     normalised partial output and the split's log-sum-exp at the end.
@@ -42,9 +43,9 @@
 // P multiplies the cache on rank 1 in bf16: its rounding only perturbs the weights of an
 // average (relative 2^-9), and the row sums use the unrounded fp32 probabilities.
 //
-// Warps (384 threads per CTA): rank 0 -- 0 TMA producer (+ L2 prefetch), 1 and 11 MMA
-// issuers (1 also owns TMEM), 2-9 softmax (two threads per head), 10 copier; rank 1 --
-// 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 rescale, 2-9 epilogue, 10-11 idle.
+// Warps (384 threads per CTA): rank 0 -- 0 TMA producer, 1 and 11 MMA issuers (1 also
+// owns TMEM), 2-9 softmax (two threads per head), 10 copier; rank 1 -- 0 TMA producer,
+// 1 MMA issuer and TMEM owner, 2-5 rescale, 2-9 epilogue, 10 L2 prefetch, 11 idle.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -65,7 +66,7 @@ constexpr int ROWS = 128, NK = 80, NTHREADS = 384;
 constexpr int KST = 2;     // rank 0: key-tile stages (one per S buffer)
 constexpr int VST = 2;     // rank 1: latent-tile stages
 constexpr int NPB = 2;     // rank 1: P slots (= rank 0's staging slots)
-constexpr int PF = 4;      // tiles prefetched into L2 ahead of the TMA loads
+constexpr int PF1 = 4;     // key tiles prefetched into L2 ahead of rank 1's latent loads
 constexpr uint32_t KBOX = NK * 128;         // 80 keys x 64 dims, bf16: 10 KB
 constexpr uint32_t KSTAGE = 9 * KBOX;       // boxes 0-7 latent dims, box 8 the RoPE band
 constexpr uint32_t VSTAGE = 8 * KBOX;       // 512 latent dims
@@ -172,6 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     uint64_t *o_final = bars + 28;
     uint32_t *tslot = (uint32_t *)(bars + 29);
     volatile int *abort = (volatile int *)(tslot + 1);
+    volatile int *prog = (volatile int *)(bars + 27);   // rank 1: latent tiles whose loads are issued
     unsigned *err = &g_tc_decode_err;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -204,6 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         for (int s = 0; s < NPB; ++s) mbar_init(&p_empty[s], 1);
         *abort = 0;
+        *prog = 0;
         fence_mbar_init();
         if (rank == 0) {   // both S buffers start free: the softmax warps' arrivals for tiles 0 and 1
             for (int s = 0; s < KST; ++s)
@@ -224,18 +227,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 
     if (rank == 0) {
         if (warp == 0) {
-            // ---------------------------------------------- TMA producer + L2 prefetch
+            // ---------------------------------------------------------------- TMA producer
             if (lane == 0 && nt > 0) {
                 tma_prefetch_desc(&mC);
                 tma_prefetch_desc(&mR);
-                auto prefetch = [&](int t) {
-                    const long key0 = w.kb + (long)t * NK;
-                    const int rows = (int)min((long)NK, p.kv_len - key0);
-                    const long row = (long)w.b * p.kv_len + key0;
-                    for (int r = 0; r < rows; r += 16)
-                        l2_prefetch(p.cache + (row + r) * 512, (uint32_t)min(16, rows - r) * 1024u);
-                    l2_prefetch(p.kpe + row * 64, (uint32_t)rows * 128u);
-                };
                 // the unit's Q block (128 heads: q_abs in eight 64-dim boxes, the rotated
                 // q_pe in one) staged in the K stages; the softmax threads move it to TMEM
                 tma_prefetch_desc(&mQa);
@@ -245,7 +240,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) tma_load_2d(smem + i * 16384, &mQa, q_full, 64 * i, qrow);
                 tma_load_2d(smem + 8 * 16384, &mQp, q_full, 0, qrow);
-                for (int t = 0; t < nt && t < PF; ++t) prefetch(t);
                 // the stages hold Q until it is in TMEM
                 bool go = mbar_wait(q_ready, 0, abort, err);
                 for (int t = 0; t < nt && go; ++t) {
@@ -258,7 +252,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * KBOX, &mC, &k_full[s], 64 * i, key0, w.b);
                     tma_load_3d(dst + 8 * KBOX, &mR, &k_full[s], 0, key0, w.b);
-                    if (t + PF < nt) prefetch(t + PF);
                 }
             }
         } else if (warp == 1 || warp == 11) {
@@ -464,6 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     mbar_arrive_expect_tx(&v_full[s], VSTAGE);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * KBOX, &mC, &v_full[s], 64 * i, key0, w.b);
+                    *prog = t + 1;   // paces the prefetching warp
                     if (t == (nt > 3 ? nt - 3 : 0)) {   // the epilogue's q_abs rows (128 KB) into L2
                         const __half *q0 = p.qa + w.b * p.qa_b + (long)w.r0 * p.qa_r;
                         for (int k = 0; k < 8; ++k) l2_prefetch(q0 + k * 16 * 512, 16 * 1024);
@@ -479,28 +473,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     for (int i = 0; i < 8; ++i) tma_load_2d(smem + QB_OFF + i * 16384, &mQa, qb_full, 64 * i, qrow);
                 }
             }
+        } else if (warp == 10) {
+            // ------------------------------- L2 prefetch of the key tiles rank 0 loads next
+            // Issued from this CTA, whose TMA unit has room: a thread issuing bulk
+            // prefetches waits behind them, and in rank 0's producer that wait held back
+            // every stage refill.  This CTA's latent loads trail rank 0's key loads by
+            // about two tiles; tile t + PF1 is prefetched once tile t's rows load here.
+            if (lane == 0 && nt > 0) {
+                auto prefetch = [&](int t) {
+                    const long key0 = w.kb + (long)t * NK;
+                    const int rows = (int)min((long)NK, p.kv_len - key0);
+                    const long row = (long)w.b * p.kv_len + key0;
+                    for (int r = 0; r < rows; r += 16)
+                        l2_prefetch(p.cache + (row + r) * 512, (uint32_t)min(16, rows - r) * 1024u);
+                    l2_prefetch(p.kpe + row * 64, (uint32_t)rows * 128u);
+                };
+                for (int t = 0; t < nt && t < PF1; ++t) prefetch(t);
+                const uint64_t t0 = global_ns();
+                for (int t = PF1; t < nt; ++t) {
+                    bool ok = true;
+                    while (*prog < t - PF1 + 1) {   // the latent loads of tile t - PF1 are issued
+                        if (*abort || global_ns() - t0 > WAIT_NS) {
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                    if (!ok) break;
+                    prefetch(t);
+                }
+            }
         } else if (warp == 1) {
             // ---------------------------------------------------- O += P.C issuer
-            if (lane == 0 && nt > 0) {
+            // (warp-uniform loop, one elected lane issues, as for the score MMAs)
+            if (nt > 0) {
+                bool ok = true;
                 for (int t = 0; t < nt; ++t) {
                     const int s = t % VST, pb = t % NPB;
-                    if (!mbar_wait(&v_full[s], (t / VST) & 1, abort, err)) break;
-                    if (!mbar_wait(&pc_ready[pb], (t / NPB) & 1, abort, err)) break;
+                    ok = __all_sync(FULL, mbar_wait(&v_full[s], (t / VST) & 1, abort, err));
+                    ok = ok && __all_sync(FULL, mbar_wait(&pc_ready[pb], (t / NPB) & 1, abort, err));
+                    if (!ok) break;
                     tc_fence_after();
                     const uint8_t *slot = smem + OFF_PB + pb * XSLOT;
                     const uint64_t pa0 = sdesc_kmajor(slot), pa1 = sdesc_kmajor_sw32(slot + P_BLK1);
                     const uint64_t vb = sdesc_mnmajor(smem + s * VSTAGE, KBOX);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < NK / 16; ++kk) {   // 16 keys per step; N = 256 latent dims per MMA
-                        const uint64_t pa = kk < 4 ? pa0 + (uint64_t)(2 * kk) : pa1;
-                        const uint32_t acc = (t | kk) != 0;
-                        mma_ss(tmem, pa, vb + (uint64_t)(kk * (2048 >> 4)), p.idesc_pv, acc);
-                        mma_ss(tmem + 256, pa, vb + (uint64_t)((4 * KBOX + kk * 2048) >> 4), p.idesc_pv, acc);
+                        for (int kk = 0; kk < NK / 16; ++kk) {   // 16 keys per step; N = 256 latent dims per MMA
+                            const uint64_t pa = kk < 4 ? pa0 + (uint64_t)(2 * kk) : pa1;
+                            const uint32_t acc = (t | kk) != 0;
+                            mma_ss(tmem, pa, vb + (uint64_t)(kk * (2048 >> 4)), p.idesc_pv, acc);
+                            mma_ss(tmem + 256, pa, vb + (uint64_t)((4 * KBOX + kk * 2048) >> 4), p.idesc_pv, acc);
+                        }
+                        mma_commit(&v_empty[s]);
+                        mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
                     }
-                    mma_commit(&v_empty[s]);
-                    mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
+                    __syncwarp();
                 }
-                mma_commit(o_final);
+                if (elect_one()) mma_commit(o_final);
+                __syncwarp();
             }
         } else if (warp >= 2 && warp < 10) {
             // ------------------------ row rescale (warps 2-5) + epilogue (warps 2-9)
