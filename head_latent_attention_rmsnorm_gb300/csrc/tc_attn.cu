@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- score MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform control flow keeps the operands in
+        // uniform registers) and one elected lane issues the MMAs.
+        {
             pdl_wait();
             bool ok = true;
             int T = 0, n = 0;   // key tiles, units so far
@@ -244,37 +246,40 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
                 if (u >= p.units) continue;
                 const Work w = work_of(p, u);
                 // this unit's Q is in TMEM
-                if (!mbar_wait(q_ready, n & 1, abort, &g_tc_attn_err)) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(q_ready, n & 1, abort, &g_tc_attn_err))) break;
                 ++n;
                 for (int j = 0; j < w.nt; ++j, ++T) {
                     const int ks = T % KST;
-                    if (!mbar_wait(&k_full[ks], (T / KST) & 1, abort, &g_tc_attn_err)) {
-                        ok = false;
-                        break;
-                    }
+                    bool go = __all_sync(0xffffffffu, mbar_wait(&k_full[ks], (T / KST) & 1, abort, &g_tc_attn_err));
                     // S buffer T & 1 last held P_{T-2}: P.V_{T-2} must have read it
-                    if (T >= 2 && !mbar_wait(&pv_done[T & 1], ((T - 2) >> 1) & 1, abort, &g_tc_attn_err)) {
+                    if (go && T >= 2)
+                        go = __all_sync(0xffffffffu, mbar_wait(&pv_done[T & 1], ((T - 2) >> 1) & 1, abort, &g_tc_attn_err));
+                    if (!go) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t s_tm = tmem + (T & 1) * 128;
                     const uint8_t *kd = sK + ks * K_BYTES;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kb = 0; kb < 3; ++kb) {
-                        const uint64_t db = sdesc_kmajor(kd + kb * BOX);
+                        for (int kb = 0; kb < 3; ++kb) {
+                            const uint64_t db = sdesc_kmajor(kd + kb * BOX);
 #pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            mma_ts(s_tm, tmem + T_Q + (kb * 4 + k4) * 8, db + 2 * k4, p.idesc_s, (kb | k4) != 0);
+                            for (int k4 = 0; k4 < 4; ++k4)
+                                mma_ts(s_tm, tmem + T_Q + (kb * 4 + k4) * 8, db + 2 * k4, p.idesc_s, (kb | k4) != 0);
+                        }
+                        mma_commit(&s_full[T & 1]);
+                        mma_commit(&k_empty[ks]);
                     }
-                    mma_commit(&s_full[T & 1]);
-                    mma_commit(&k_empty[ks]);
+                    __syncwarp();
                 }
             }
         }
     } else if (warp == 3 + NSM) {
         // ------------------------------------------------------------ P.V issuer
-        if (lane == 0) {
+        // (warp-uniform loop, one elected lane issues, as for the scores)
+        {
             pdl_wait();
             bool ok = true;
             int T = 0, n = 0;
@@ -283,30 +288,35 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
                 if (u >= p.units) continue;
                 const Work w = work_of(p, u);
                 // the epilogue of the previous unit has read O before P.V_0 overwrites it
-                if (n > 0 && !mbar_wait(o_free, (n - 1) & 1, abort, &g_tc_attn_err)) break;
+                if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(o_free, (n - 1) & 1, abort, &g_tc_attn_err))) break;
                 ++n;
                 for (int j = 0; j < w.nt; ++j, ++T) {
                     const int vs = T % VST;
-                    if (!mbar_wait(&p_full[T & 1], (T >> 1) & 1, abort, &g_tc_attn_err) ||
-                        !mbar_wait(&v_full[vs], (T / VST) & 1, abort, &g_tc_attn_err)) {
+                    bool go = __all_sync(0xffffffffu, mbar_wait(&p_full[T & 1], (T >> 1) & 1, abort, &g_tc_attn_err));
+                    go = go && __all_sync(0xffffffffu, mbar_wait(&v_full[vs], (T / VST) & 1, abort, &g_tc_attn_err));
+                    if (!go) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t p_tm = tmem + (T & 1) * 128;
                     const uint8_t *vd = sV + vs * V_SLOT;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kb = 0; kb < 2; ++kb) {
-                        const uint64_t db = sdesc_kmajor(vd + kb * VBOX);   // 144 rows: V^T + constant rows
+                        for (int kb = 0; kb < 2; ++kb) {
+                            const uint64_t db = sdesc_kmajor(vd + kb * VBOX);   // 144 rows: V^T + constant rows
 #pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            mma_ts(tmem + T_O, p_tm + kb * 32 + k4 * 8, db + 2 * k4, p.idesc_pv, (j | kb | k4) != 0);
+                            for (int k4 = 0; k4 < 4; ++k4)
+                                mma_ts(tmem + T_O, p_tm + kb * 32 + k4 * 8, db + 2 * k4, p.idesc_pv, (j | kb | k4) != 0);
+                        }
+                        mma_commit(&v_empty[vs]);
+                        mma_commit(&pv_done[T & 1]);
+                        mma_commit(o_done);
                     }
-                    mma_commit(&v_empty[vs]);
-                    mma_commit(&pv_done[T & 1]);
-                    mma_commit(o_done);
+                    __syncwarp();
                 }
-                mma_commit(o_final);
+                if (elect_one()) mma_commit(o_final);
+                __syncwarp();
             }
         }
     } else if (warp >= 2 && warp < 2 + NSM) {
