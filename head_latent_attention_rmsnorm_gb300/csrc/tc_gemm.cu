@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(256, 1)
         }
     } else if (warp == 1 || (NISS == 2 && warp == 6)) {
         // ------------------------------------------------- MMA issuer(s): columns [c0, c0 + NW)
-        if (lane == 0) {
+        // (warp-uniform loop; one elected lane issues)
+        {
             const int c0 = warp == 1 ? 0 : NW;
             int it = 0, lt = 0;
             bool ok = true;
@@ -153,23 +154,28 @@ __global__ void __launch_bounds__(256, 1)
                 const Tile w = tile_of(p, t);
                 const int a = lt & 1;
                 // the epilogue has drained what tile lt-2 left in accumulator a
-                if (lt >= 2 && !mbar_wait(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)) break;
+                if (lt >= 2 && !__all_sync(0xffffffffu, mbar_wait(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)))
+                    break;
                 const uint32_t d = tmem + a * ACC_COLS + c0;
                 const int nk = p.pr[w.prob].K / BK;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % STAGES;
-                    if (!mbar_wait(&full[s], (it / STAGES) & 1, abort, &g_tc_gemm_err)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / STAGES) & 1, abort, &g_tc_gemm_err))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t da = sdesc_kmajor(sA + s * A_BYTES);
                     const uint64_t db = sdesc_kmajor(sB + s * B_BYTES + c0 * 128);   // rows c0.. of the B tile
+                    if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) mma_ss(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
-                    mma_commit(&empty[s]);
+                        for (int k = 0; k < BK / 16; ++k) mma_ss(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
+                        mma_commit(&empty[s]);
+                    }
+                    __syncwarp();
                 }
-                mma_commit(&acc_full[a]);
+                if (elect_one()) mma_commit(&acc_full[a]);
+                __syncwarp();
             }
         }
     } else if (warp >= 2 && warp <= 5) {
@@ -339,7 +345,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
     } else if (rank == 0 && (warp == 1 || warp == 6)) {
         // -------------------------- MMA issuers (leader): output columns [128 h, +128)
-        if (lane == 0) {
+        // (warp-uniform loop; one elected lane issues)
+        {
             const int h = warp == 1 ? 0 : 1;
             int it = 0, lt = 0;
             bool ok = true;
@@ -347,23 +354,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 const Tile w = pair_tile_of(p, t);
                 const int a = lt & 1;
                 // both CTAs' epilogues have drained what tile lt-2 left in accumulator a
-                if (lt >= 2 && !mbar_wait_cluster(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)) break;
+                if (lt >= 2 &&
+                    !__all_sync(0xffffffffu, mbar_wait_cluster(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)))
+                    break;
                 const uint32_t d = tmem + a * 256 + h * 128;
                 const int nk = p.pr[w.prob].K / BK;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % PST;
-                    if (!mbar_wait(&full[s], (it / PST) & 1, abort, &g_tc_gemm_err)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / PST) & 1, abort, &g_tc_gemm_err))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t da = sdesc_kmajor(sA + s * PA_BYTES);
                     const uint64_t db = sdesc_kmajor(sB + s * PB_BYTES + h * (PB_BYTES / 2));
+                    if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) mma_ss_pair(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
-                    mma_commit_pair(&empty[s], 3);
+                        for (int k = 0; k < BK / 16; ++k) mma_ss_pair(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
+                        mma_commit_pair(&empty[s], 3);
+                    }
+                    __syncwarp();
                 }
-                mma_commit_pair(&acc_full[a], 3);
+                if (elect_one()) mma_commit_pair(&acc_full[a], 3);
+                __syncwarp();
             }
         }
     } else if (warp >= 2 && warp <= 5) {

@@ -167,42 +167,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && nt > 0) {
-            bool ok = mbar_wait(q_ready, 0, abort, &g_tc_latent_err);
+        // (warp-uniform loop; one elected lane issues)
+        if (nt > 0) {
+            bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort, &g_tc_latent_err));
             const int nks = rank == 0 ? 20 : 16;          // 16-dim k-steps of the partial score
             const uint32_t idesc_s = rank == 0 ? p.idesc_s0 : p.idesc_s1;
             auto issue_pv = [&](int t) -> bool {
-                if (!mbar_wait(p_full, t & 1, abort, &g_tc_latent_err)) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(p_full, t & 1, abort, &g_tc_latent_err))) return false;
                 tc_fence_after();
                 const uint8_t *tile = stages + (t % ST) * STAGE_BYTES;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)   // 16 keys per step; B = 256 dims x 16 keys, MN-major
-                    mma_ts(tmem + T_O, tmem + T_P + kk * 8, sdesc_mnmajor(tile + kk * 2048, BOX), p.idesc_pv,
-                           (t | kk) != 0);
-                mma_commit(&k_empty[t % ST]);
-                mma_commit(o_done);
+                    for (int kk = 0; kk < 4; ++kk)   // 16 keys per step; B = 256 dims x 16 keys, MN-major
+                        mma_ts(tmem + T_O, tmem + T_P + kk * 8, sdesc_mnmajor(tile + kk * 2048, BOX), p.idesc_pv,
+                               (t | kk) != 0);
+                    mma_commit(&k_empty[t % ST]);
+                    mma_commit(o_done);
+                }
+                __syncwarp();
                 return true;
             };
             for (int j = 0; j < nt && ok; ++j) {
                 const int s = j % ST;
-                if (!mbar_wait(&k_full[s], (j / ST) & 1, abort, &g_tc_latent_err)) {
-                    ok = false;
-                    break;
-                }
-                if (j > 0 && !mbar_wait(s_free, (j - 1) & 1, abort, &g_tc_latent_err)) {
+                bool go = __all_sync(0xffffffffu, mbar_wait(&k_full[s], (j / ST) & 1, abort, &g_tc_latent_err));
+                if (go && j > 0) go = __all_sync(0xffffffffu, mbar_wait(s_free, (j - 1) & 1, abort, &g_tc_latent_err));
+                if (!go) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint8_t *tile = stages + s * STAGE_BYTES;
-                for (int kk = 0; kk < nks; ++kk)
-                    mma_ts(tmem + T_S, tmem + T_Q + kk * 8, sdesc_kmajor(tile + (kk >> 2) * BOX) + 2 * (kk & 3),
-                           idesc_s, kk != 0);
-                mma_commit(s_full);
+                if (elect_one()) {
+                    for (int kk = 0; kk < nks; ++kk)
+                        mma_ts(tmem + T_S, tmem + T_Q + kk * 8, sdesc_kmajor(tile + (kk >> 2) * BOX) + 2 * (kk & 3),
+                               idesc_s, kk != 0);
+                    mma_commit(s_full);
+                }
+                __syncwarp();
                 if (j > 0 && !issue_pv(j - 1)) ok = false;
             }
             if (ok) issue_pv(nt - 1);
-            mma_commit(o_final);
+            if (elect_one()) mma_commit(o_final);
+            __syncwarp();
         }
     } else if (warp < 6) {
         // ---------------------------------------------------------- softmax warps
