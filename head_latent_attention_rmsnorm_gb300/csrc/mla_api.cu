@@ -436,7 +436,7 @@ mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int 
 }
 
 struct DecodeWs {
-    void *qabs, *qpe, *olat, *w16;
+    void *qabs, *qpe, *olat;
     float *po, *pl;
     float2 *rtab;
     size_t bytes;
@@ -452,7 +452,6 @@ DecodeWs decode_ws(const Decode &p, void *base, bool own_partials) {
     w.qpe = c.take(rows * p.Dr * es);
     w.olat = c.take(rows * p.Dk * es);
     w.rtab = (float2 *)c.take((size_t)(p.Dr / 2) * sizeof(float2));
-    if (p.tc) w.w16 = c.take((size_t)p.H * (p.Dn + p.Dv) * p.Dk * 2);
     if (own_partials) {
         w.po = (float *)c.take((size_t)p.n * rows * p.Dk * 4);
         w.pl = (float *)c.take((size_t)p.n * rows * 4);
@@ -678,7 +677,7 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
         MLA_TRY(launch_rope_rows(p.tin, TY_F16, rows, p.Dr, q_pe, p.L - 1, 1, 1, w.rtab, p.L - 1, w.qpe, cs));
         TcDecode t{p.B, p.L, p.n, p.H, p.Dk, p.Dn, p.Dr, p.Dv, p.chunk, scale, dims->rope_base};
         return cuda_status(tc_decode(t, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w.qabs, w.qpe,
-                                     w.olat, w.w16, cs));
+                                     w.olat, cs));
     }
     return decode_simt(p, scale, dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w, cs);
 }

@@ -475,13 +475,13 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor(const void *tile, uint32_t mn_
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulate; `f16` selects fp16 (1) or
-// bf16 (0) operands; K-major A; B K-major unless b_mn.
+// bf16 (0) operands; A K-major unless a_mn, B K-major unless b_mn.
 //   bits 4-5 D format (1 = f32)   bits 7-9 A format   bits 10-12 B format (0 f16, 1 bf16)
-//   bit 15 A major (0 = K)        bit 16 B major (1 = MN)
+//   bit 15 A major (1 = MN)       bit 16 B major (1 = MN)
 //   bits 17-22 N >> 3             bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool f16, bool b_mn = false) {
-    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((b_mn ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool f16, bool b_mn = false, bool a_mn = false) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // fp32 pair -> packed f16x2 / bf16x2 (low half = first argument).

@@ -1,6 +1,8 @@
 // tc_gemm.cu -- batched "TN" GEMM on the sm_103a tensor cores:
 //   C[z](m, n) = sum_k A[z](m, k) * B[z](n, k)      (fp16 or bf16 in, fp32 accumulate)
-// A and B are K-major (k contiguous) and reached through 3-D TMA maps (k, row, z);
+// A and B are K-major (k contiguous) and reached through 3-D TMA maps (k, row, z); A
+// may instead be m-major (m contiguous, one row per k: the decode absorb reads W_K in
+// place that way);
 // C is written with arbitrary element strides as fp16, bf16 or fp32.
 //
 // This carries the K_nope / V reconstruction of the explicit path -- LAGA's local
@@ -51,6 +53,7 @@ struct GemmK {
     GemmP pr[2];
     int total;         // tiles of both problems
     uint32_t idesc;    // per issuer: M = 128, N = BN / issuers
+    int a_mn;          // A stored m-major (both problems): two 64-row boxes per stage
 };
 
 struct Tile {
@@ -138,7 +141,12 @@ __global__ void __launch_bounds__(256, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
-                    tma_load_3d(sA + s * A_BYTES, ma, &full[s], kb * BK, a_r, a_z);
+                    if (p.a_mn) {   // 64 m x 64 k boxes: m-major (k rows of 128 bytes)
+                        tma_load_3d(sA + s * A_BYTES, ma, &full[s], a_r, kb * BK, a_z);
+                        tma_load_3d(sA + s * A_BYTES + A_BYTES / 2, ma, &full[s], a_r + 64, kb * BK, a_z);
+                    } else {
+                        tma_load_3d(sA + s * A_BYTES, ma, &full[s], kb * BK, a_r, a_z);
+                    }
                     tma_load_3d(sB + s * B_BYTES, mb, &full[s], kb * BK, b_r, b_z);
                 }
             }
@@ -165,11 +173,15 @@ __global__ void __launch_bounds__(256, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t da = sdesc_kmajor(sA + s * A_BYTES);
+                    // A k-major: 16 k = 32 bytes along a row; m-major: 16 k = 16 rows of 128 bytes
+                    // (the two 64-m boxes 8 KB apart)
+                    const uint64_t da = p.a_mn ? sdesc_mnmajor(sA + s * A_BYTES, A_BYTES / 2) : sdesc_kmajor(sA + s * A_BYTES);
+                    const uint32_t dk = p.a_mn ? (2048 >> 4) : 2;
                     const uint64_t db = sdesc_kmajor(sB + s * B_BYTES + c0 * 128);   // rows c0.. of the B tile
                     if (elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) mma_ss(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_ss(d, da + (uint64_t)(dk * k), db + 2 * k, p.idesc, (kb | k) != 0);
                         mma_commit(&empty[s]);
                     }
                     __syncwarp();
@@ -499,10 +511,11 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
     if (n_probs < 1 || n_probs > 2) return cudaErrorInvalidValue;
     int maxN = 0;
     for (int i = 0; i < n_probs; ++i) {
-        if (probs[i].K % BK || probs[i].K != probs[0].K) return cudaErrorInvalidValue;
+        if (probs[i].K % BK || probs[i].K != probs[0].K || probs[i].a_mn != probs[0].a_mn) return cudaErrorInvalidValue;
         maxN = std::max(maxN, probs[i].N);
     }
     const int BN = maxN >= 256 ? 256 : (maxN >= 128 ? 128 : 64);
+    if (probs[0].a_mn && BN == 256) return cudaErrorInvalidValue;   // m-major A: single-CTA tiles only
     // 256-wide problems run on SM pairs: 256 x 256 tiles, A boxes of 128 rows per CTA,
     // B boxes of 64 rows (two per CTA)
     const bool pair = BN == 256;
@@ -519,7 +532,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
             continue;
         }
         const GemmProblem &g = probs[i];
-        cudaError_t e = make_operand_map(&maps[2 * i], g.A, BM);
+        cudaError_t e = g.a_mn ? make_operand_map_mn(&maps[2 * i], g.A) : make_operand_map(&maps[2 * i], g.A, BM);
         if (e != cudaSuccess) return e;
         e = make_operand_map(&maps[2 * i + 1], g.B, pair ? 64 : BN);
         if (e != cudaSuccess) return e;
@@ -543,24 +556,25 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         p.total += q.tiles;
     }
     if (p.total == 0) return cudaSuccess;
+    p.a_mn = probs[0].a_mn ? 1 : 0;
     ProfScope ps("tc_gemm", st);
     switch (BN) {
         case 256:
             p.idesc = tc::idesc_f16(256, 128, f16);   // cta_group::2: M = 256 across the pair
             return launch_gemm_pair(maps, p, st);
         case 128:
-            p.idesc = tc::idesc_f16(BM, 128, f16);
+            p.idesc = tc::idesc_f16(BM, 128, f16, false, p.a_mn != 0);
             return launch_gemm<128, 1>(maps, p, st);
         default:
-            p.idesc = tc::idesc_f16(BM, 64, f16);
+            p.idesc = tc::idesc_f16(BM, 64, f16, false, p.a_mn != 0);
             return launch_gemm<64, 1>(maps, p, st);
     }
 }
 
 cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int K, int batch, bool f16,
-                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st) {
+                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st, bool a_mn) {
     if (M == 0 || N == 0 || batch == 0) return cudaSuccess;
-    GemmProblem g{A, B, M, N, K, batch, C, c_m, c_n, c_batch, out_kind};
+    GemmProblem g{A, B, M, N, K, batch, C, c_m, c_n, c_batch, out_kind, a_mn};
     return tc_gemm_group(&g, 1, f16, st);
 }
 

@@ -27,6 +27,8 @@ struct TmaOperand {
 cudaError_t make_tma_map(CUtensorMap *map, const void *ptr, int rank, const unsigned long long *dims,
                          const unsigned long long *strides, const unsigned *box);
 cudaError_t make_operand_map(CUtensorMap *map, const TmaOperand &op, int tile_rows);
+// An m-major operand (m contiguous): boxes of 64 m x 64 k of one z-slice.
+cudaError_t make_operand_map_mn(CUtensorMap *map, const TmaOperand &op);
 
 // C[batch](m, n) = sum_k A(m, k) B(n, k); K % 64 == 0.  out_kind: 0 fp16, 1 bf16, 2 fp32.
 struct GemmProblem {
@@ -35,9 +37,12 @@ struct GemmProblem {
     void *C;
     long c_m, c_n, c_batch;
     int out_kind;
+    // A stored m-major (m contiguous, one row per k): then A.k_extent is the m extent and
+    // A.rows the k extent.  Tiles of 64 or 128 columns only (not the pair kernel).
+    bool a_mn = false;
 };
 cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int K, int batch, bool f16,
-                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st);
+                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st, bool a_mn = false);
 // One persistent launch over the tiles of one or two problems (same K, same operand
 // type): the explicit path's K_nope and V^T products share one launch.
 cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaStream_t st);

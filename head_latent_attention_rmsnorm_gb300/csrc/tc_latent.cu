@@ -494,17 +494,17 @@ bool tc_decode_supported(int Dk, int Dn, int Dr, int Dv, int H) {
 
 cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, const void *c_cache,
                       const void *kpe_cache, const void *w_kv_b, void *out, float *lse, float *po, float *pl,
-                      void *qabs, void *qpe, void *olat, void *w16, cudaStream_t st) {
+                      void *qabs, void *qpe, void *olat, cudaStream_t st) {
     (void)q_pe;   // rotated into qpe (fp16) by the caller
     const long Dh = p.Dn + p.Dv, rows = (long)p.B * p.H;
     cudaError_t e;
     const bool tc_small_gemms = tileable(p.B, tile_n(p.B));
     // 1. q_abs[b][h][k] = sum_d q_nope[b][h][d] W_K(h)[d][k]  (fp16 out, fp32 accumulate)
     if (tc_small_gemms) {
-        if ((e = transpose_wk(w_kv_b, 0, p.H, (int)Dh, p.Dn, p.Dk, w16, st)) != cudaSuccess) return e;
-        TmaOperand A{w16, p.Dn, p.Dk, p.H, (long)p.Dn * 2, (long)p.Dk * p.Dn * 2, p.Dk, 0, 1};
+        // A = W_K(h) read in place, m-major: rows d < Dn of head h's block, k contiguous
+        TmaOperand A{w_kv_b, p.Dk, p.Dn, p.H, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dk, 0, 1};
         TmaOperand Bq{q_nope, p.Dn, p.B, p.H, (long)p.H * p.Dn * 2, (long)p.Dn * 2, p.B, 0, 1};
-        e = tc_gemm(A, Bq, p.Dk, p.B, p.Dn, p.H, false, qabs, 1, (long)p.H * p.Dk, p.Dk, 0, st);
+        e = tc_gemm(A, Bq, p.Dk, p.B, p.Dn, p.H, false, qabs, 1, (long)p.H * p.Dk, p.Dk, 0, st, true);
     } else {
         GemmArgs g{};
         g.M = p.B; g.N = p.Dk; g.K = p.Dn; g.nzb = 1; g.nzh = p.H;

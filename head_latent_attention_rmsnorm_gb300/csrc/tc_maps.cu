@@ -56,4 +56,15 @@ cudaError_t make_operand_map(CUtensorMap *map, const TmaOperand &op, int tile_ro
     return make_tma_map(map, op.ptr, 3, dims, strides, box);
 }
 
+cudaError_t make_operand_map_mn(CUtensorMap *map, const TmaOperand &op) {
+    unsigned long long dims[3] = {(unsigned long long)op.k_extent, (unsigned long long)op.rows,
+                                  (unsigned long long)(op.z_extent < 1 ? 1 : op.z_extent)};
+    unsigned long long zs = (unsigned long long)op.z_stride;
+    if (op.z_extent <= 1) zs = (unsigned long long)op.rows * (unsigned long long)op.row_stride;
+    zs = (zs + 15) / 16 * 16;
+    unsigned long long strides[2] = {(unsigned long long)op.row_stride, zs};
+    unsigned box[3] = {64, 64, 1};
+    return make_tma_map(map, op.ptr, 3, dims, strides, box);
+}
+
 }  // namespace mla
