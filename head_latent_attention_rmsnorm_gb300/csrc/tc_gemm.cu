@@ -47,6 +47,7 @@ struct GemmP {
     long c_m, c_n, c_batch;
     int out_kind;  // 0 fp16, 1 bf16, 2 fp32
     int tiles_n, tiles_m, tiles;
+    int c_tma;     // pair kernel: C written by TMA tile stores (16-bit, n contiguous, aligned)
 };
 
 struct GemmK {
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(256, 1)
 // accumulator rows.
 constexpr int PST = 6;   // stages of the pair kernel's ring
 constexpr uint32_t PA_BYTES = 128 * BK * 2, PB_BYTES = 128 * BK * 2;
+constexpr uint32_t PC_BYTES = 4 * 2 * 4096;   // four epilogue warps x two 32-row x 64-column 16-bit buffers
 
 __device__ __forceinline__ Tile pair_tile_of(const GemmK &p, int t) {
     Tile r;
@@ -277,13 +279,15 @@ __device__ __forceinline__ Tile pair_tile_of(const GemmK &p, int t) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
-                        const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1, GemmK p) {
+                        const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
+                        const __grid_constant__ CUtensorMap tc0, const __grid_constant__ CUtensorMap tc1, GemmK p) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + PST * PA_BYTES;
-    uint64_t *full = (uint64_t *)(sB + PST * PB_BYTES);   // leader: both CTAs' bytes of a stage landed
+    uint8_t *sC = sB + PST * PB_BYTES;                    // epilogue staging: two 4 KB buffers per warp
+    uint64_t *full = (uint64_t *)(sC + PC_BYTES);         // leader: both CTAs' bytes of a stage landed
     uint64_t *empty = full + PST;                         // both: the stage's MMAs are done
     uint64_t *acc_full = empty + PST, *acc_empty = acc_full + 2;
     uint32_t *tslot = (uint32_t *)(acc_empty + 2);
@@ -395,14 +399,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         // ------------------------------------ epilogue (both CTAs): thread = row
         const int quad = warp & 3;
         const uint32_t acc_empty0 = map_peer(smem_u32(acc_empty), 0);
-        int lt = 0;
+        int lt = 0, nst = 0;   // tiles, TMA-stored chunks so far
         bool ok = true;
+        if (lane == 0) {
+            tma_prefetch_desc(&tc0);
+            tma_prefetch_desc(&tc1);
+        }
         for (int t = pair; t < p.total; t += pairs, ++lt) {
             const Tile w = pair_tile_of(p, t);
             const GemmP &q = p.pr[w.prob];
             const int a = lt & 1;
             ok = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[a], (lt >> 1) & 1, abort, &g_tc_gemm_err));
             tc_fence_after();
+            if (q.c_tma) {
+                // 64-column chunks: TMEM -> 16-bit -> a 128-byte-swizzled 32-row buffer of
+                // this warp (chunk j of a row at j ^ (row mod 8)) -> one TMA tile store
+                // (rows past M and columns past N are clipped by the store)
+                const CUtensorMap *mc = w.prob ? &tc1 : &tc0;
+                const int row0 = w.m0 + 128 * (int)rank + quad * 32;
+                for (int cc = 0; cc < 4 && ok; ++cc, ++nst) {
+                    uint32_t r0[32], r1[32];
+                    const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + a * 256 + cc * 64;
+                    tmem_ld32(ta, r0);
+                    tmem_ld32(ta + 32, r1);
+                    tmem_ld_wait();
+                    uint32_t o[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float x0 = __uint_as_float(r0[2 * i]), x1 = __uint_as_float(r0[2 * i + 1]);
+                        const float y0 = __uint_as_float(r1[2 * i]), y1 = __uint_as_float(r1[2 * i + 1]);
+                        o[i] = q.out_kind == 0 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
+                        o[16 + i] = q.out_kind == 0 ? pack_f16(y0, y1) : pack_bf16(y0, y1);
+                    }
+                    uint8_t *buf = sC + (warp - 2) * 8192 + (nst & 1) * 4096;
+                    if (lane == 0) bulk_wait_read<1>();   // the store that used this buffer has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *(uint4 *)(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                            make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(mc, buf, w.n0 + cc * 64, row0, w.batch);
+                        bulk_commit();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_peer(acc_empty0 + a * 8);
+                continue;
+            }
             const long row = w.m0 + 128 * (long)rank + quad * 32 + lane;
             char *C = (char *)q.C;
             const int esz = q.out_kind == 2 ? 4 : 2;
@@ -445,6 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_peer(acc_empty0 + a * 8);   // the leader's barrier (own CTA for rank 0)
         }
+        if (lane == 0) bulk_wait_all();   // the tile stores have completed before the CTA leaves
     }
     tc_fence_before();
     __syncthreads();
@@ -468,7 +516,7 @@ int num_sms() {
 }
 
 cudaError_t launch_gemm_pair(const CUtensorMap *maps, const GemmK &p, cudaStream_t st) {
-    const size_t sm = PST * (PA_BYTES + PB_BYTES) + 1024 + 256;
+    const size_t sm = PST * (PA_BYTES + PB_BYTES) + PC_BYTES + 1024 + 256;
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     const int grid = 2 * std::min(p.total, num_sms() / 2);
@@ -482,7 +530,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap *maps, const GemmK &p, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, maps[0], maps[1], maps[2], maps[3], p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
 template <int BN, int NISS>
@@ -520,7 +568,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
     // B boxes of 64 rows (two per CTA)
     const bool pair = BN == 256;
     const int TM = pair ? 256 : BM, TN = BN;
-    CUtensorMap maps[4];
+    CUtensorMap maps[6];   // A, B of problem 0, A, B of problem 1, C of problems 0 and 1 (pair kernel)
     GemmK p{};
     p.total = 0;
     for (int i = 0; i < 2; ++i) {
@@ -529,6 +577,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
             q.tiles = 0;
             maps[2 * i] = maps[0];
             maps[2 * i + 1] = maps[1];
+            maps[4 + i] = maps[4];
             continue;
         }
         const GemmProblem &g = probs[i];
@@ -554,6 +603,19 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         q.tiles_m = (g.M + TM - 1) / TM;
         q.tiles = (g.M == 0 || g.N == 0) ? 0 : q.tiles_n * q.tiles_m * g.batch;
         p.total += q.tiles;
+        // the pair kernel writes 16-bit, n-contiguous outputs with 16-byte aligned rows
+        // through TMA tile stores (boxes of 64 columns x 32 rows, columns in whole boxes)
+        q.c_tma = 0;
+        if (pair && g.out_kind != 2 && g.c_n == 1 && g.N % 64 == 0 && (g.c_m * 2) % 16 == 0 &&
+            (g.batch <= 1 || (g.c_batch * 2) % 16 == 0) && ((uintptr_t)g.C % 16) == 0) {
+            unsigned long long dims[3] = {(unsigned long long)g.N, (unsigned long long)g.M,
+                                          (unsigned long long)(g.batch < 1 ? 1 : g.batch)};
+            unsigned long long zs = g.batch <= 1 ? (unsigned long long)g.M * g.c_m * 2 : (unsigned long long)g.c_batch * 2;
+            unsigned long long strides[2] = {(unsigned long long)g.c_m * 2, zs};
+            unsigned box[3] = {64, 32, 1};
+            if (make_tma_map(&maps[4 + i], g.C, 3, dims, strides, box) == cudaSuccess) q.c_tma = 1;
+        }
+        if (!q.c_tma) maps[4 + i] = maps[2 * i];   // unused placeholder
     }
     if (p.total == 0) return cudaSuccess;
     p.a_mn = probs[0].a_mn ? 1 : 0;
