@@ -47,7 +47,7 @@ struct GemmP {
     long c_m, c_n, c_batch;
     int out_kind;  // 0 fp16, 1 bf16, 2 fp32
     int tiles_n, tiles_m, tiles;
-    int c_tma;     // pair kernel: C written by TMA tile stores (16-bit, n contiguous, aligned)
+    int c_stage;   // pair kernel: C staged per warp and written in whole 128-byte rows (16-bit, n contiguous, aligned)
 };
 
 struct GemmK {
@@ -258,12 +258,13 @@ __global__ void __launch_bounds__(256, 1)
 // half of its operand bytes from each SM.  A one-CTA 128 x 256 tile moves 12 KB of
 // operands per 16-deep MMA step through each SM's shared memory twice (TMA write, MMA
 // read), above the port's 128 B/clk at the tensor rate; the pair moves 8 KB.  The
-// leader (rank 0) issues the MMAs from two threads, each owning 128 output columns
+// leader (rank 0) issues the MMAs from two warps, each owning 128 output columns
 // (N = 128 per MMA: 64 columns from each CTA); both CTAs load, and both drain their own
-// accumulator rows.
-constexpr int PST = 6;   // stages of the pair kernel's ring
+// accumulator rows: 16-bit outputs through a per-warp shared-memory staging of the whole
+// tile slice (accumulator released before the stores), written in whole 128-byte rows.
+constexpr int PST = 5;   // stages of the pair kernel's ring
 constexpr uint32_t PA_BYTES = 128 * BK * 2, PB_BYTES = 128 * BK * 2;
-constexpr uint32_t PC_BYTES = 4 * 2 * 4096;   // four epilogue warps x two 32-row x 64-column 16-bit buffers
+constexpr uint32_t PC_BYTES = 4 * 4 * 4096;   // four epilogue warps x a 32-row x 256-column 16-bit tile slice
 
 __device__ __forceinline__ Tile pair_tile_of(const GemmK &p, int t) {
     Tile r;
@@ -279,8 +280,7 @@ __device__ __forceinline__ Tile pair_tile_of(const GemmK &p, int t) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
-                        const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
-                        const __grid_constant__ CUtensorMap tc0, const __grid_constant__ CUtensorMap tc1, GemmK p) {
+                        const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1, GemmK p) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -399,55 +399,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         // ------------------------------------ epilogue (both CTAs): thread = row
         const int quad = warp & 3;
         const uint32_t acc_empty0 = map_peer(smem_u32(acc_empty), 0);
-        int lt = 0, nst = 0;   // tiles, TMA-stored chunks so far
+        int lt = 0;
         bool ok = true;
-        if (lane == 0) {
-            tma_prefetch_desc(&tc0);
-            tma_prefetch_desc(&tc1);
-        }
         for (int t = pair; t < p.total; t += pairs, ++lt) {
             const Tile w = pair_tile_of(p, t);
             const GemmP &q = p.pr[w.prob];
             const int a = lt & 1;
             ok = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[a], (lt >> 1) & 1, abort, &g_tc_gemm_err));
             tc_fence_after();
-            if (q.c_tma) {
-                // 64-column chunks: TMEM -> 16-bit -> a 128-byte-swizzled 32-row buffer of
-                // this warp (chunk j of a row at j ^ (row mod 8)) -> one TMA tile store
-                // (rows past M and columns past N are clipped by the store)
-                const CUtensorMap *mc = w.prob ? &tc1 : &tc0;
-                const int row0 = w.m0 + 128 * (int)rank + quad * 32;
-                for (int cc = 0; cc < 4 && ok; ++cc, ++nst) {
-                    uint32_t r0[32], r1[32];
-                    const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + a * 256 + cc * 64;
-                    tmem_ld32(ta, r0);
-                    tmem_ld32(ta + 32, r1);
+            if (q.c_stage) {
+                // The warp's 32 rows x 256 columns: TMEM -> 16-bit -> four 128-byte-swizzled
+                // 32 x 64 buffers (chunk j of a row at j ^ (row mod 8)); the accumulator is
+                // released as soon as it has been read, then the buffers are read back four
+                // rows per instruction and stored in whole 128-byte rows.  (TMA tile stores
+                // from here queued in the TMA unit behind the producer's operand loads, and
+                // releasing the accumulator after the stores waited for them to land.)
+                char *const C = (char *)q.C;
+                const long cbase = q.c_batch * w.batch, c_m = q.c_m;
+                const int row0 = w.m0 + 128 * (int)rank + quad * 32, M = q.M, N = q.N;
+                const bool f16out = q.out_kind == 0;
+                const uint32_t sbuf0 = smem_u32(sC + (warp - 2) * 16384);
+                const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + a * 256;
+                __syncwarp();   // every lane has read the previous tile's buffers
+                uint32_t r[2][64];
+                if (ok) {
+                    tmem_ld32(tq, *reinterpret_cast<uint32_t(*)[32]>(&r[0][0]));
+                    tmem_ld32(tq + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[0][32]));
                     tmem_ld_wait();
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    if (ok && cc < 3) {   // the next chunk's columns load while this one is packed
+                        tmem_ld32(tq + (cc + 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[(cc + 1) & 1][0]));
+                        tmem_ld32(tq + (cc + 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[(cc + 1) & 1][32]));
+                    }
                     uint32_t o[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float x0 = __uint_as_float(r0[2 * i]), x1 = __uint_as_float(r0[2 * i + 1]);
-                        const float y0 = __uint_as_float(r1[2 * i]), y1 = __uint_as_float(r1[2 * i + 1]);
-                        o[i] = q.out_kind == 0 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
-                        o[16 + i] = q.out_kind == 0 ? pack_f16(y0, y1) : pack_bf16(y0, y1);
+                    for (int i = 0; i < 32; ++i) {
+                        const float x0 = __uint_as_float(r[cc & 1][2 * i]), x1 = __uint_as_float(r[cc & 1][2 * i + 1]);
+                        o[i] = f16out ? pack_f16(x0, x1) : pack_bf16(x0, x1);
                     }
-                    uint8_t *buf = sC + (warp - 2) * 8192 + (nst & 1) * 4096;
-                    if (lane == 0) bulk_wait_read<1>();   // the store that used this buffer has read it
-                    __syncwarp();
+                    const uint32_t buf = sbuf0 + cc * 4096;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        *(uint4 *)(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                            make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(mc, buf, w.n0 + cc * 64, row0, w.batch);
-                        bulk_commit();
-                    }
+                        st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), o[4 * j], o[4 * j + 1], o[4 * j + 2],
+                                     o[4 * j + 3]);
+                    if (ok && cc < 3) tmem_ld_wait();
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_peer(acc_empty0 + a * 8);
+                const int j = lane & 7;
+#pragma unroll 1
+                for (int cc = 0; cc < 4 && ok; ++cc) {
+                    const int n = w.n0 + cc * 64;
+                    if (n >= N) break;
+                    const uint32_t buf = sbuf0 + cc * 4096;
+                    uint4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3);
+                        v[i] = ld_shared_v4(buf + rr * 128 + ((j ^ (rr & 7)) << 4));
+                    }
+                    char *dst = C + (cbase + (long)(row0 + (lane >> 3)) * c_m + n) * 2 + j * 16;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (row0 + 4 * i + (lane >> 3) < M) *(uint4 *)(dst + (long)(4 * i) * c_m * 2) = v[i];
+                }
                 continue;
             }
             const long row = w.m0 + 128 * (long)rank + quad * 32 + lane;
@@ -492,7 +510,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_peer(acc_empty0 + a * 8);   // the leader's barrier (own CTA for rank 0)
         }
-        if (lane == 0) bulk_wait_all();   // the tile stores have completed before the CTA leaves
     }
     tc_fence_before();
     __syncthreads();
@@ -530,7 +547,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap *maps, const GemmK &p, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 template <int BN, int NISS>
@@ -568,7 +585,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
     // B boxes of 64 rows (two per CTA)
     const bool pair = BN == 256;
     const int TM = pair ? 256 : BM, TN = BN;
-    CUtensorMap maps[6];   // A, B of problem 0, A, B of problem 1, C of problems 0 and 1 (pair kernel)
+    CUtensorMap maps[4];
     GemmK p{};
     p.total = 0;
     for (int i = 0; i < 2; ++i) {
@@ -577,7 +594,6 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
             q.tiles = 0;
             maps[2 * i] = maps[0];
             maps[2 * i + 1] = maps[1];
-            maps[4 + i] = maps[4];
             continue;
         }
         const GemmProblem &g = probs[i];
@@ -603,19 +619,10 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         q.tiles_m = (g.M + TM - 1) / TM;
         q.tiles = (g.M == 0 || g.N == 0) ? 0 : q.tiles_n * q.tiles_m * g.batch;
         p.total += q.tiles;
-        // the pair kernel writes 16-bit, n-contiguous outputs with 16-byte aligned rows
-        // through TMA tile stores (boxes of 64 columns x 32 rows, columns in whole boxes)
-        q.c_tma = 0;
-        if (pair && g.out_kind != 2 && g.c_n == 1 && g.N % 64 == 0 && (g.c_m * 2) % 16 == 0 &&
-            (g.batch <= 1 || (g.c_batch * 2) % 16 == 0) && ((uintptr_t)g.C % 16) == 0) {
-            unsigned long long dims[3] = {(unsigned long long)g.N, (unsigned long long)g.M,
-                                          (unsigned long long)(g.batch < 1 ? 1 : g.batch)};
-            unsigned long long zs = g.batch <= 1 ? (unsigned long long)g.M * g.c_m * 2 : (unsigned long long)g.c_batch * 2;
-            unsigned long long strides[2] = {(unsigned long long)g.c_m * 2, zs};
-            unsigned box[3] = {64, 32, 1};
-            if (make_tma_map(&maps[4 + i], g.C, 3, dims, strides, box) == cudaSuccess) q.c_tma = 1;
-        }
-        if (!q.c_tma) maps[4 + i] = maps[2 * i];   // unused placeholder
+        // the pair kernel writes 16-bit, n-contiguous outputs with 16-byte aligned rows in
+        // whole 128-byte row pieces (columns in whole 64-column chunks)
+        q.c_stage = pair && g.out_kind != 2 && g.c_n == 1 && g.N % 64 == 0 && (g.c_m * 2) % 16 == 0 &&
+                    (g.batch <= 1 || (g.c_batch * 2) % 16 == 0) && ((uintptr_t)g.C % 16) == 0;
     }
     if (p.total == 0) return cudaSuccess;
     p.a_mn = probs[0].a_mn ? 1 : 0;
