@@ -339,49 +339,52 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
                 if (unit_at(k, c, G) < p.units) return k;
             return k;
         };
-        for (int k = next_unit(0); k * G < p.units; k = next_unit(k + 1)) {
+        // ---- a unit's Q from the staging buffer into TMEM (the previous unit's score MMAs
+        // have all completed: their S tiles were read).  Run for unit n + 1 right after unit
+        // n's last tile, before unit n's epilogue, so that the next unit's first score MMAs
+        // overlap the last P.V and the epilogue.  Quarter qr widens q_nope dims [32 qr,
+        // 32 qr + 32) to fp16 (columns 16 qr ...); quarters 0 and 1 also copy the rotated q_pe
+        // elements t and t + 32 for t in [16 qr, 16 qr + 16) (columns 64 + 8 qr ... and
+        // 80 + 8 qr ...).  Rows past s_q arrive as zeros.  16-byte chunk c of row r of a staged
+        // box sits at chunk c ^ (r & 7).
+        auto load_q = [&](int nn) {
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(qs_full, nn & 1, abort, &g_tc_attn_err));
+            const uint8_t *qrow_s = sQs + (qr >> 1) * BOX + row * 128;
+            uint32_t qn[16];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint4 v = *(const uint4 *)(qrow_s + (((4 * (qr & 1) + cc) ^ (row & 7)) << 4));
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    qn[4 * cc + i] = pack_f16(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xffff0000u));
+            }
+            tmem_st16(lane_base + T_Q + qr * 16, qn);
+            if (qr < 2) {   // warp-uniform
+                const uint8_t *prow = sQs + 2 * BOX + row * 128;
+                uint32_t ra8[8], rb8[8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 va = *(const uint4 *)(prow + (((2 * qr + h) ^ (row & 7)) << 4));
+                    const uint4 vb = *(const uint4 *)(prow + (((2 * qr + 4 + h) ^ (row & 7)) << 4));
+                    ra8[4 * h] = va.x, ra8[4 * h + 1] = va.y, ra8[4 * h + 2] = va.z, ra8[4 * h + 3] = va.w;
+                    rb8[4 * h] = vb.x, rb8[4 * h + 1] = vb.y, rb8[4 * h + 2] = vb.z, rb8[4 * h + 3] = vb.w;
+                }
+                tmem_st8(lane_base + T_Q + 64 + qr * 8, ra8);
+                tmem_st8(lane_base + T_Q + 80 + qr * 8, rb8);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_ready);
+        };
+        int k = next_unit(0);
+        if (k * G < p.units) load_q(0);
+        for (; k * G < p.units;) {
             const int u = unit_at(k, c, G);
             const Work w = work_of(p, u);
             const int hq = p.head_off + w.hl, b = w.b, q0 = w.q0, nt = w.nt;
             const int pos = p.q_offset + q0 + row;
-            // ---- this row's Q from the staging buffer into TMEM (the previous unit's score
-            // MMAs have all completed: their S tiles were read below).  Quarter qr widens
-            // q_nope dims [32 qr, 32 qr + 32) to fp16 (columns 16 qr ...); quarters 0 and 1
-            // also copy the rotated q_pe elements t and t + 32 for t in [16 qr, 16 qr + 16)
-            // (columns 64 + 8 qr ... and 80 + 8 qr ...).  Rows past s_q arrive as zeros.
-            // 16-byte chunk c of row r of a staged box sits at chunk c ^ (r & 7).
-            {
-                ok = __all_sync(0xffffffffu, ok && mbar_wait(qs_full, n & 1, abort, &g_tc_attn_err));
-                const uint8_t *qrow_s = sQs + (qr >> 1) * BOX + row * 128;
-                uint32_t qn[16];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const uint4 v = *(const uint4 *)(qrow_s + (((4 * (qr & 1) + cc) ^ (row & 7)) << 4));
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        qn[4 * cc + i] = pack_f16(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xffff0000u));
-                }
-                tmem_st16(lane_base + T_Q + qr * 16, qn);
-                if (qr < 2) {   // warp-uniform
-                    const uint8_t *prow = sQs + 2 * BOX + row * 128;
-                    uint32_t ra8[8], rb8[8];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 va = *(const uint4 *)(prow + (((2 * qr + h) ^ (row & 7)) << 4));
-                        const uint4 vb = *(const uint4 *)(prow + (((2 * qr + 4 + h) ^ (row & 7)) << 4));
-                        ra8[4 * h] = va.x, ra8[4 * h + 1] = va.y, ra8[4 * h + 2] = va.z, ra8[4 * h + 3] = va.w;
-                        rb8[4 * h] = vb.x, rb8[4 * h + 1] = vb.y, rb8[4 * h + 2] = vb.z, rb8[4 * h + 3] = vb.w;
-                    }
-                    tmem_st8(lane_base + T_Q + 64 + qr * 8, ra8);
-                    tmem_st8(lane_base + T_Q + 80 + qr * 8, rb8);
-                }
-                tmem_st_wait();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_ready);
-
             float m = -INFINITY;
             for (int j = 0; j < nt; ++j, ++T) {
                 const int sb = T & 1;
@@ -458,6 +461,8 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[sb]);
             }
+            const int k_next = next_unit(k + 1);
+            if (k_next * G < p.units) load_q(n + 1);
             // ---- epilogue: the row sum is O's column 128; each quarter stores 32 columns
             if (nt > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_final, n & 1, abort, &g_tc_attn_err));
             tc_fence_after();
@@ -495,6 +500,7 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
                         l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
             ++n;
+            k = k_next;
         }
     }
     tc_fence_before();
