@@ -449,22 +449,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_peer(acc_empty0 + a * 8);
-                const int j = lane & 7;
+                // 32-byte piece j of a 128-byte row per lane: eight rows per store instruction
+                const int j = lane & 3;
 #pragma unroll 1
                 for (int cc = 0; cc < 4 && ok; ++cc) {
                     const int n = w.n0 + cc * 64;
                     if (n >= N) break;
                     const uint32_t buf = sbuf0 + cc * 4096;
-                    uint4 v[8];
+                    uint32_t v[4][8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int rr = 4 * i + (lane >> 3);
-                        v[i] = ld_shared_v4(buf + rr * 128 + ((j ^ (rr & 7)) << 4));
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = 8 * i + (lane >> 2);
+                        const uint4 a0 = ld_shared_v4(buf + rr * 128 + (((2 * j) ^ (rr & 7)) << 4));
+                        const uint4 a1 = ld_shared_v4(buf + rr * 128 + (((2 * j + 1) ^ (rr & 7)) << 4));
+                        v[i][0] = a0.x, v[i][1] = a0.y, v[i][2] = a0.z, v[i][3] = a0.w;
+                        v[i][4] = a1.x, v[i][5] = a1.y, v[i][6] = a1.z, v[i][7] = a1.w;
                     }
-                    char *dst = C + (cbase + (long)(row0 + (lane >> 3)) * c_m + n) * 2 + j * 16;
+                    char *dst = C + (cbase + (long)(row0 + (lane >> 2)) * c_m + n) * 2 + j * 32;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (row0 + 4 * i + (lane >> 3) < M) *(uint4 *)(dst + (long)(4 * i) * c_m * 2) = v[i];
+                    for (int i = 0; i < 4; ++i)
+                        if (row0 + 8 * i + (lane >> 2) < M) st_global_v8(dst + (long)(8 * i) * c_m * 2, v[i]);
                 }
                 continue;
             }
@@ -619,10 +623,10 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         q.tiles_m = (g.M + TM - 1) / TM;
         q.tiles = (g.M == 0 || g.N == 0) ? 0 : q.tiles_n * q.tiles_m * g.batch;
         p.total += q.tiles;
-        // the pair kernel writes 16-bit, n-contiguous outputs with 16-byte aligned rows in
+        // the pair kernel writes 16-bit, n-contiguous outputs with 32-byte aligned rows in
         // whole 128-byte row pieces (columns in whole 64-column chunks)
-        q.c_stage = pair && g.out_kind != 2 && g.c_n == 1 && g.N % 64 == 0 && (g.c_m * 2) % 16 == 0 &&
-                    (g.batch <= 1 || (g.c_batch * 2) % 16 == 0) && ((uintptr_t)g.C % 16) == 0;
+        q.c_stage = pair && g.out_kind != 2 && g.c_n == 1 && g.N % 64 == 0 && (g.c_m * 2) % 32 == 0 &&
+                    (g.batch <= 1 || (g.c_batch * 2) % 32 == 0) && ((uintptr_t)g.C % 32) == 0;
     }
     if (p.total == 0) return cudaSuccess;
     p.a_mn = probs[0].a_mn ? 1 : 0;
