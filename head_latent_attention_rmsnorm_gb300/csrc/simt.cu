@@ -134,7 +134,7 @@ __device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
 
 // One warp per task: a latent row (b, j) of [0, B*pad_rows), a table-only position of
 // [pad_rows, n_pos), or a run of 32*PREP_W_PER_LANE weight chunks.
-__global__ void prep_tc_kernel(const __grid_constant__ PrepTc a) {
+__global__ void __launch_bounds__(256, 5) prep_tc_kernel(const __grid_constant__ PrepTc a) {
     // the reconstruction GEMM may launch now (it waits for this grid before its loads)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     long g = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
