@@ -141,25 +141,38 @@ __global__ void __launch_bounds__(256, 5) prep_tc_kernel(const __grid_constant__
     const int lane = threadIdx.x % 32;
     if (g < a.row_tasks) {
         const long b = g / a.pad_rows, j = g % a.pad_rows;
+        const int Dk = a.Dk, nc = Dk / 256;
+        const bool live = j < a.n_rows;
+        // this row's latent and k_pe loads first: their latency overlaps the angle and the
+        // q_pe rotation below
+        uint4 xr[4];
+        float x0 = 0.f, x1 = 0.f;
+        if (live) {
+            const uint4 *x = (const uint4 *)(a.c_kv + (b * a.s_kv + j) * Dk);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (c < nc) xr[c] = x[c * 32 + lane];
+            const __nv_bfloat16 *kx = a.k_pe + (b * a.s_kv + j) * PREP_DR;
+            x0 = __bfloat162float(kx[lane]);
+            x1 = __bfloat162float(kx[lane + 32]);
+        }
         const float2 cs = rope_cs(j, a.theta[lane]);
         if (b == 0 && j < a.n_pos) a.tab[j * (PREP_DR / 2) + lane] = cs;
         if (a.qpe) rope_q_at(a, j, (int)b, (int)b + 1, cs, lane);
-        const int Dk = a.Dk, nc = Dk / 256;
         uint4 *y = (uint4 *)(a.chat + g * Dk);
         __half *kp = a.kpe + g * PREP_DR;
-        if (j >= a.n_rows) {
+        if (!live) {
             for (int c = 0; c < nc; ++c) y[c * 32 + lane] = make_uint4(0, 0, 0, 0);
             kp[lane] = kp[lane + 32] = __float2half_rn(0.f);
             return;
         }
-        const uint4 *x = (const uint4 *)(a.c_kv + (b * a.s_kv + j) * Dk);
         const uint4 *w = (const uint4 *)a.rms_w;
         float v[4][8];
         float ss = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             if (c < nc) {
-                uint4 q = x[c * 32 + lane];
+                uint4 q = xr[c];
                 const __nv_bfloat16 *e = (const __nv_bfloat16 *)&q;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -184,8 +197,6 @@ __global__ void __launch_bounds__(256, 5) prep_tc_kernel(const __grid_constant__
             }
         }
         // half-split pairs (t, t + 32): lane t rotates both by its own frequency
-        const __nv_bfloat16 *kx = a.k_pe + (b * a.s_kv + j) * PREP_DR;
-        const float x0 = __bfloat162float(kx[lane]), x1 = __bfloat162float(kx[lane + 32]);
         kp[lane] = __float2half_rn(x0 * cs.x - x1 * cs.y);
         kp[lane + 32] = __float2half_rn(x1 * cs.x + x0 * cs.y);
     } else if ((g -= a.row_tasks) < a.tab_tasks) {
