@@ -132,10 +132,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
 __device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)p), "r"(bytes) : "memory");
 }
-// Hints the 128-byte line holding `p` into L2 through the load/store path (no TMA unit).
-__device__ __forceinline__ void l2_prefetch_line(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"((uint64_t)__cvta_generic_to_global(p)));
-}
 
 // The same load for a CTA pair running cta_group::2 MMAs: the destination is this
 // CTA's shared memory, the completion is counted on `bar_cluster` (a shared::cluster
@@ -154,12 +150,6 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int c0, int c1) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)m),
                  "r"(smem_u32(src)), "r"(c0), "r"(c1)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *src, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"((uint64_t)m),
-                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
 
@@ -304,15 +294,6 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr));
 }
-// 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -389,36 +370,7 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 // Waits until every committed bulk copy of this thread has completed (writes done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Arrive on another CTA's mbarrier and add `bytes` to the transaction count its
-// current phase waits for (the bytes of a bulk copy that will complete on it).
-__device__ __forceinline__ void mbar_arrive_expect_tx_peer(uint32_t peer_bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(peer_bar),
-                 "r"(bytes)
-                 : "memory");
-}
 
-// Orders this thread's prior memory operations (including shared::cluster stores)
-// at cluster scope.
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-__device__ __forceinline__ void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-// Stores into another CTA's shared memory (`addr`, `peer_bar`: shared::cluster
-// addresses); each store completes its bytes as transactions on the destination
-// mbarrier, so the receiver needs no other signal.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t peer_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     addr),
-                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(peer_bar)
-                 : "memory");
-}
-__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t peer_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
-                 "r"(peer_bar)
-                 : "memory");
-}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior
 // writes (including shared::cluster stores) at cluster scope.
 __device__ __forceinline__ void mbar_arrive_peer(uint32_t peer_bar) {
@@ -483,12 +435,6 @@ __device__ __forceinline__ uint64_t sdesc_kmajor(const void *tile) { return sdes
 // (layout type 6).
 __device__ __forceinline__ uint64_t sdesc_kmajor_sw32(const void *tile) {
     return (sdesc_sw128(smem_u32(tile), 16, 256) & ~((uint64_t)7 << 61)) | ((uint64_t)6 << 61);
-}
-// K-major tile with the 64-byte swizzle: rows of 32 16-bit elements (64 bytes), eight
-// rows per 512-byte atom, atoms stacked along M/N; 16-byte chunk c of row r sits at
-// chunk c ^ ((r >> 1) & 3) of the row (layout type 4 in bits 61-63).
-__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(const void *tile) {
-    return (sdesc_sw128(smem_u32(tile), 16, 512) & ~((uint64_t)7 << 61)) | ((uint64_t)4 << 61);
 }
 // MN-major operand: each 128-byte row holds 64 consecutive MN elements of one k; eight
 // k-rows form an atom (stride 1024 bytes along K); consecutive 64-element MN blocks
