@@ -59,13 +59,17 @@ __device__ __forceinline__ float2 rope_cs(long pos, double theta) {
     return make_float2(c, s);
 }
 
-__global__ void rope_table_kernel(long pos0, long n_pos, int half, int Dr, double base, float2 *tab) {
-    __shared__ double theta[512];
-    for (int t = threadIdx.x; t < half && t < 512; t += blockDim.x) theta[t] = pow(base, -2.0 * (double)t / (double)Dr);
-    __syncthreads();
+// The frequencies base^(-2t/Dr), computed in double on the host (the device's fp64
+// pow is a long latency chain at GB300's fp64 rate).
+constexpr int ROPE_MAX_HALF = 320;   // Dr <= 640 - Dn (validated by the callers)
+struct RopeTheta {
+    double v[ROPE_MAX_HALF];
+};
+
+__global__ void rope_table_kernel(long pos0, long n_pos, int half, const __grid_constant__ RopeTheta th, float2 *tab) {
     long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_pos * half) return;
-    tab[i] = rope_cs(pos0 + i / half, theta[i % half]);
+    tab[i] = rope_cs(pos0 + i / half, th.v[i % half]);
 }
 
 // ---------------------------------------------- fused prep (tensor-core path) ----
@@ -581,8 +585,11 @@ inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / 
 cudaError_t launch_rope_table(long pos0, long n_pos, int Dr, float base, float2 *tab, cudaStream_t st) {
     long n = n_pos * (Dr / 2);
     if (n == 0) return cudaSuccess;
+    if (Dr / 2 > ROPE_MAX_HALF) return cudaErrorInvalidValue;
+    RopeTheta th;
+    for (int t = 0; t < Dr / 2; ++t) th.v[t] = pow((double)base, -2.0 * (double)t / (double)Dr);
     ProfScope ps("rope_table", st);
-    rope_table_kernel<<<blocks_for(n, 256), 256, 0, st>>>(pos0, n_pos, Dr / 2, Dr, (double)base, tab);
+    rope_table_kernel<<<blocks_for(n, 256), 256, 0, st>>>(pos0, n_pos, Dr / 2, th, tab);
     return cudaGetLastError();
 }
 

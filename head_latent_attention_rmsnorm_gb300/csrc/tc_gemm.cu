@@ -15,12 +15,10 @@
 // problems (tile t, t + gridDim.x, ...); 256-wide problems use the pair kernel below
 // (two SMs per 256 x 256 tile).  Warp 0 lane 0 streams 64-wide k-blocks of
 // A and B through a 4-stage TMA ring that runs across tile boundaries; the MMA
-// issuers accumulate each tile into one of two TMEM accumulators (M=128, K=16 per
-// instruction); warps 2-5 drain a finished accumulator (thread = row) and store it
-// while the next tile accumulates into the other one.  For BN = 256 two issuing
-// threads (warps 1 and 6) each own half of the columns: a thread waiting on an
-// mbarrier between MMA batches leaves the tensor pipe idle for ~100-200 cycles, and
-// the other thread's MMAs fill that gap.
+// issuer (warp 1, a warp-uniform loop issuing from one elected lane) accumulates each
+// tile into one of two TMEM accumulators (M=128, K=16 per instruction); warps 2-5 drain
+// a finished accumulator (thread = row) and store it while the next tile accumulates
+// into the other one.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -53,7 +51,7 @@ struct GemmP {
 struct GemmK {
     GemmP pr[2];
     int total;         // tiles of both problems
-    uint32_t idesc;    // per issuer: M = 128, N = BN / issuers
+    uint32_t idesc;    // M = 128, N = BN (the pair kernel: M = 256, N = 128 per issuing warp)
     int a_mn;          // A stored m-major (both problems): two 64-row boxes per stage
 };
 
@@ -73,14 +71,13 @@ __device__ __forceinline__ Tile tile_of(const GemmK &p, int t) {
     return r;
 }
 
-template <int BN, int NISS>
+template <int BN>
 __global__ void __launch_bounds__(256, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
                    const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1, GemmK p) {
     using namespace tc;
     constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
     constexpr uint32_t ACC_COLS = BN < 32 ? 32 : BN;   // one accumulator; two are allocated
-    constexpr int NW = BN / NISS;                      // columns per issuer
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
@@ -96,10 +93,10 @@ __global__ void __launch_bounds__(256, 1)
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NISS);
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&acc_full[a], NISS);
+            mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], 4);   // the four epilogue warps
         }
         *abort = 0;
@@ -152,11 +149,10 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         }
-    } else if (warp == 1 || (NISS == 2 && warp == 6)) {
-        // ------------------------------------------------- MMA issuer(s): columns [c0, c0 + NW)
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
         // (warp-uniform loop; one elected lane issues)
         {
-            const int c0 = warp == 1 ? 0 : NW;
             int it = 0, lt = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < p.total && ok; t += gridDim.x, ++lt) {
@@ -165,7 +161,7 @@ __global__ void __launch_bounds__(256, 1)
                 // the epilogue has drained what tile lt-2 left in accumulator a
                 if (lt >= 2 && !__all_sync(0xffffffffu, mbar_wait(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)))
                     break;
-                const uint32_t d = tmem + a * ACC_COLS + c0;
+                const uint32_t d = tmem + a * ACC_COLS;
                 const int nk = p.pr[w.prob].K / BK;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -178,7 +174,7 @@ __global__ void __launch_bounds__(256, 1)
                     // (the two 64-m boxes 8 KB apart)
                     const uint64_t da = p.a_mn ? sdesc_mnmajor(sA + s * A_BYTES, A_BYTES / 2) : sdesc_kmajor(sA + s * A_BYTES);
                     const uint32_t dk = p.a_mn ? (2048 >> 4) : 2;
-                    const uint64_t db = sdesc_kmajor(sB + s * B_BYTES + c0 * 128);   // rows c0.. of the B tile
+                    const uint64_t db = sdesc_kmajor(sB + s * B_BYTES);
                     if (elect_one()) {
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
@@ -255,9 +251,9 @@ __global__ void __launch_bounds__(256, 1)
 // The same GEMM on 256 x 256 tiles computed by a cluster of two CTAs (two SMs) with
 // cta_group::2 MMAs (M = 256): CTA r holds A rows [m0 + 128 r, +128) and, of the 256 B
 // rows (output columns), [n0 + 64 r, +64) and [n0 + 128 + 64 r, +64), so every MMA reads
-// half of its operand bytes from each SM.  A one-CTA 128 x 256 tile moves 12 KB of
-// operands per 16-deep MMA step through each SM's shared memory twice (TMA write, MMA
-// read), above the port's 128 B/clk at the tensor rate; the pair moves 8 KB.  The
+// half of its operand bytes from each SM.  A one-CTA 128 x 256 tile loads 12 KB of
+// operands per 16-deep MMA step into its SM; the pair loads 8 KB per SM, and the
+// operand loads (about 90-130 GB/s per SM from L2) pace this GEMM.  The
 // leader (rank 0) issues the MMAs from two warps, each owning 128 output columns
 // (N = 128 per MMA: 64 columns from each CTA); both CTAs load, and both drain their own
 // accumulator rows: 16-bit outputs through a per-warp shared-memory staging of the whole
@@ -554,10 +550,10 @@ cudaError_t launch_gemm_pair(const CUtensorMap *maps, const GemmK &p, cudaStream
     return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, maps[0], maps[1], maps[2], maps[3], p);
 }
 
-template <int BN, int NISS>
+template <int BN>
 cudaError_t launch_gemm(const CUtensorMap *maps, const GemmK &p, cudaStream_t st) {
     const size_t sm = gemm_smem<BN>();
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, NISS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     // 64-wide tiles need 97 KB of shared memory and 128 TMEM columns: two CTAs per SM
     const int grid = std::min(p.total, num_sms() * (BN == 64 ? 2 : 1));
@@ -571,7 +567,7 @@ cudaError_t launch_gemm(const CUtensorMap *maps, const GemmK &p, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, NISS>, maps[0], maps[1], maps[2], maps[3], p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN>, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 }  // namespace
@@ -637,10 +633,10 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
             return launch_gemm_pair(maps, p, st);
         case 128:
             p.idesc = tc::idesc_f16(BM, 128, f16, false, p.a_mn != 0);
-            return launch_gemm<128, 1>(maps, p, st);
+            return launch_gemm<128>(maps, p, st);
         default:
             p.idesc = tc::idesc_f16(BM, 64, f16, false, p.a_mn != 0);
-            return launch_gemm<64, 1>(maps, p, st);
+            return launch_gemm<64>(maps, p, st);
     }
 }
 
