@@ -498,7 +498,8 @@ cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, c
     (void)q_pe;   // rotated into qpe (fp16) by the caller
     const long Dh = p.Dn + p.Dv, rows = (long)p.B * p.H;
     cudaError_t e;
-    const bool tc_small_gemms = tileable(p.B, tile_n(p.B));
+    // q_nope is the absorb product's N operand and o_lat the un-absorb product's M operand
+    const bool tc_small_gemms = tileable(p.B, tile_n(p.B)) && tileable(p.B, 128);
     // 1. q_abs[b][h][k] = sum_d q_nope[b][h][d] W_K(h)[d][k]  (fp16 out, fp32 accumulate)
     if (tc_small_gemms) {
         // A = W_K(h) read in place, m-major: rows d < Dn of head h's block, k contiguous
@@ -519,12 +520,13 @@ cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, c
     if (e != cudaSuccess) return e;
     // 3. log-sum-exp merge of the splits -> o_lat (bf16) and lse
     if ((e = launch_lse_combine(TY_BF16, p.n, rows, p.Dk, po, pl, olat, lse, st)) != cudaSuccess) return e;
-    // 4. out[b][h][d] = sum_k o_lat[b][h][k] W_V(h)[d][k]
+    // 4. out[b][h][d] = sum_k o_lat[b][h][k] W_V(h)[d][k]: rows b (M), columns d (N), so
+    //    each output row is written contiguously (a 128-row tile holds B = 64 valid rows)
     if (tc_small_gemms) {
-        TmaOperand A{(const char *)w_kv_b + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, p.H, (long)p.Dk * 2,
-                     Dh * p.Dk * 2, p.Dv, 0, 1};
-        TmaOperand Bo{olat, p.Dk, p.B, p.H, (long)p.H * p.Dk * 2, (long)p.Dk * 2, p.B, 0, 1};
-        return tc_gemm(A, Bo, p.Dv, p.B, p.Dk, p.H, false, out, 1, (long)p.H * p.Dv, p.Dv, 1, st);
+        TmaOperand Ao{olat, p.Dk, p.B, p.H, (long)p.H * p.Dk * 2, (long)p.Dk * 2, p.B, 0, 1};
+        TmaOperand Bw{(const char *)w_kv_b + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, p.H, (long)p.Dk * 2,
+                      Dh * p.Dk * 2, p.Dv, 0, 1};
+        return tc_gemm(Ao, Bw, p.B, p.Dv, p.Dk, p.H, false, out, (long)p.H * p.Dv, 1, p.Dv, 1, st);
     }
     GemmArgs u{};
     u.M = p.B; u.N = p.Dv; u.K = p.Dk; u.nzb = 1; u.nzh = p.H;
