@@ -11,7 +11,9 @@
 // accumulator (128 heads x 512 latent dims) fills the whole tensor memory of an SM,
 // so a unit runs on a cluster of two CTAs with different jobs:
 //   rank 0 (scores): Q in bf16 in TMEM; each 80-key tile of the bf16 cache (latent +
-//     RoPE band) arrives through a two-deep TMA ring and is used as it lands; S = Q.K^T
+//     RoPE band) arrives through a two-deep TMA ring whose stages fill and drain in
+//     three groups of three 64-dim boxes (a group of tile t + 2 loads as soon as tile t's
+//     MMAs have read it, which keeps the SM's TMA unit busy); S = Q.K^T
 //     on the tensor core (A from TMEM; an N = 80 MMA costs what an N = 64 one does),
 //     double-buffered in TMEM, issued by two warps that take alternate tiles, each
 //     running its loop warp-uniformly and issuing from one elected lane; eight warps run the online
@@ -64,6 +66,7 @@ using namespace tc;
 
 constexpr int ROWS = 128, NK = 80, NTHREADS = 384;
 constexpr int KST = 2;     // rank 0: key-tile stages (one per S buffer)
+constexpr int KGRP = 3;    // rank 0: a stage fills and drains in three groups of three boxes
 constexpr int VST = 2;     // rank 1: latent-tile stages
 constexpr int NPB = 2;     // rank 1: P slots (= rank 0's staging slots)
 constexpr int PF1 = 4;     // key tiles prefetched into L2 ahead of rank 1's latent loads
@@ -159,9 +162,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + OFF_BAR);
-    // rank 0: k_full = the tile landed + S buffer drained; staged = the softmax warps
+    // rank 0: s_free = S buffer drained by the softmax warps; grp_full / grp_empty
+    // [stage][group] = three boxes of a stage landed / read by the MMAs; staged = the softmax warps
     // have staged the tile's P; stg_free = the copy to rank 1 has read the staging slot
-    uint64_t *k_full = bars, *stg_free = bars + 2, *k_empty = bars + 4, *s_full = bars + 6, *staged = bars + 8;
+    uint64_t *s_free = bars, *stg_free = bars + 2, *s_full = bars + 6, *staged = bars + 8;
+    uint64_t *grp_full = bars + 32, *grp_empty = bars + 32 + KST * KGRP;   // [stage][group]
     uint64_t *q_ready = bars + 10, *q_full = bars + 30;   // Q in TMEM / Q staged in the K stages
     uint64_t *qb_full = bars + 31;   // rank 1: the q_abs block staged for the epilogue
     float *red = (float *)(smem + OFF_RED);   // rank 0: [tile parity][half][row] row maxima
@@ -184,11 +189,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (tid == 0) {
         if (rank == 0) {
             for (int s = 0; s < KST; ++s) {
-                mbar_init(&k_full[s], 9);   // the producer's expect_tx + one per softmax warp (S buffer free)
+                mbar_init(&s_free[s], 8);   // one arrival per softmax warp
                 mbar_init(&stg_free[s], 1);
-                mbar_init(&k_empty[s], 1);
                 mbar_init(&s_full[s], 1);
                 mbar_init(&staged[s], 8);
+            }
+            for (int i = 0; i < KST * KGRP; ++i) {
+                mbar_init(&grp_full[i], 1);
+                mbar_init(&grp_empty[i], 1);
             }
             mbar_init(q_ready, 8);
             mbar_init(q_full, 1);
@@ -210,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         fence_mbar_init();
         if (rank == 0) {   // both S buffers start free: the softmax warps' arrivals for tiles 0 and 1
             for (int s = 0; s < KST; ++s)
-                for (int i = 0; i < 8; ++i) mbar_arrive(&k_full[s]);
+                for (int i = 0; i < 8; ++i) mbar_arrive(&s_free[s]);
         } else {           // every P slot armed for its first transfer
             for (int s = 0; s < NPB; ++s) mbar_arrive_expect_tx(&p_full[s], P_BYTES + X_BYTES);
         }
@@ -245,13 +253,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 for (int t = 0; t < nt && go; ++t) {
                     const int s = t & 1;
                     const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of tile t - 2 in this stage
-                    if (t >= KST && !mbar_wait(&k_empty[s], ph, abort, err)) break;
                     uint8_t *dst = smem + s * KSTAGE;
                     const int key0 = (int)(w.kb + (long)t * NK);
-                    mbar_arrive_expect_tx(&k_full[s], KSTAGE);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * KBOX, &mC, &k_full[s], 64 * i, key0, w.b);
-                    tma_load_3d(dst + 8 * KBOX, &mR, &k_full[s], 0, key0, w.b);
+                    for (int g = 0; g < KGRP && go; ++g) {   // a group refills once tile t - 2 has read it
+                        uint64_t *full = &grp_full[s * KGRP + g];
+                        if (t >= KST && !mbar_wait(&grp_empty[s * KGRP + g], ph, abort, err)) go = false;
+                        if (!go) break;
+                        mbar_arrive_expect_tx(full, 3 * KBOX);
+                        for (int i = 3 * g; i < 3 * g + 3; ++i) {
+                            if (i < 8) tma_load_3d(dst + i * KBOX, &mC, full, 64 * i, key0, w.b);
+                            else tma_load_3d(dst + 8 * KBOX, &mR, full, 0, key0, w.b);
+                        }
+                    }
+                    if (!go) break;
                 }
             }
         } else if (warp == 1 || warp == 11) {
@@ -263,26 +277,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 bool ok = __all_sync(FULL, mbar_wait(q_ready, 0, abort, err));
                 for (int t = warp == 1 ? 0 : 1; t < nt && ok; t += 2) {
                     const int s = t & 1;
-                    // tile landed and S buffer s drained by the softmax (one barrier)
-                    if (!__all_sync(FULL, mbar_wait(&k_full[s], (t >> 1) & 1, abort, err))) break;
-                    tc_fence_after();
-                    // descriptors as constant offsets from one base: the issuing thread
-                    // spends no arithmetic between MMAs
+                    const uint32_t ph = (t >> 1) & 1;
+                    // S buffer s drained by the softmax, then the stage group by group
+                    if (!__all_sync(FULL, mbar_wait(&s_free[s], ph, abort, err))) break;
                     const uint64_t d0 = sdesc_kmajor(smem + s * KSTAGE);
                     const uint32_t dt = tmem + T_S + s * NK, at = tmem + T_Q;
-                    if (elect_one()) {
+                    bool go = true;
 #pragma unroll
-                        for (int kk = 0; kk < 32; ++kk)   // latent band: 16 dims per step, q_hi only
-                            mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (KBOX >> 4) + 2 * (kk & 3)),
-                                   p.idesc_s, kk != 0);
+                    for (int g = 0; g < KGRP; ++g) {
+                        go = go && __all_sync(FULL, mbar_wait(&grp_full[s * KGRP + g], ph, abort, err));
+                        if (!go) break;
+                        tc_fence_after();
+                        if (elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)    // RoPE band: q_hi then q_lo against the same box
-                            mma_ts(dt, tmem + (kk < 4 ? T_QP : T_QL) + (kk & 3) * 8,
-                                   d0 + (uint64_t)(8 * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
-                        mma_commit(&k_empty[s]);
-                        mma_commit(&s_full[s]);
+                            for (int kk = 12 * g; kk < 12 * g + 12 && kk < 32; ++kk)   // latent band, q_hi only
+                                mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (KBOX >> 4) + 2 * (kk & 3)),
+                                       p.idesc_s, kk != 0);
+                            if (g == KGRP - 1) {
+#pragma unroll
+                                for (int kk = 0; kk < 8; ++kk)   // RoPE band: q_hi then q_lo against the same box
+                                    mma_ts(dt, tmem + (kk < 4 ? T_QP : T_QL) + (kk & 3) * 8,
+                                           d0 + (uint64_t)(8 * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
+                            }
+                            mma_commit(&grp_empty[s * KGRP + g]);
+                            if (g == KGRP - 1) mma_commit(&s_full[s]);
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
+                    if (!go) break;
                 }
             }
         } else if (warp >= 2 && warp < 10) {
@@ -352,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&k_full[s]);   // S buffer s may take tile t + 2
+                if (lane == 0) mbar_arrive(&s_free[s]);   // S buffer s may take tile t + 2
                 float x[HK];   // this thread's keys, in key order
 #pragma unroll
                 for (int e = 0; e < HK; ++e)
