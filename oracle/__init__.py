@@ -10,7 +10,8 @@ for the page citations and the readings taken where the pages are silent).  This
 module compiles it with gcc and exposes numpy-in / numpy-out wrappers.
 
 Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``):
-  rmsnorm, rope, mla_explicit, mla_absorbed, mla_decode, lse_combine -- all pinned.
+  rmsnorm, rope, mla_explicit, mla_absorbed, mla_decode, lse_combine, tpla_decode --
+  all pinned.
 """
 from __future__ import annotations
 
@@ -54,8 +55,9 @@ def _load():
         lib.orc_mla_absorbed.argtypes = fwd
         lib.orc_mla_decode.argtypes = [i, i, i, i, i, i, i, i, d, d] + [_dp] * 9
         lib.orc_lse_combine.argtypes = [i, l, i, _dp, _dp, _dp, _dp]
+        lib.orc_tpla_decode.argtypes = [i, i, i, i, i, i, i, i, d, d, d] + [_dp] * 8
         for f in ("orc_rmsnorm", "orc_rope", "orc_mla_explicit", "orc_mla_absorbed",
-                  "orc_mla_decode", "orc_lse_combine"):
+                  "orc_mla_decode", "orc_lse_combine", "orc_tpla_decode"):
             getattr(lib, f).restype = None
         _lib = lib
     return _lib
@@ -140,6 +142,29 @@ def mla_decode(q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_splits=1, base=100
                            _p(q_nope), _p(q_pe), _p(c_cache), _p(kpe_cache), _p(w_kv_b),
                            _p(out), _p(lse), _p(po), _p(pl))
     return out, lse, po, pl
+
+
+def tpla_decode(q_nope, q_pe, c_raw, kpe_cache, w_kv_b, rms_w, *, shards=2, eps=1e-6,
+                base=10000.0, scale=None):
+    """TPLA latent decode over ``shards`` latent shards (see ``orc_tpla_decode``).
+
+    ``c_raw`` [B,L,Dk] is the latent before normalisation (each shard is RMSNormed on its
+    own).  Returns (out [B,H,Dv] summed over shards, shard_lse [shards,B,H])."""
+    q_nope, q_pe, c_raw, kpe_cache, w_kv_b, rms_w = map(_f64, (q_nope, q_pe, c_raw, kpe_cache, w_kv_b, rms_w))
+    B, H, dn = q_nope.shape
+    dr = q_pe.shape[-1]
+    L, dk = c_raw.shape[1], c_raw.shape[2]
+    if dk % shards:
+        raise ValueError("d_kv must divide into the shards")
+    dv = w_kv_b.shape[0] // H - dn
+    if scale is None:
+        scale = default_scale(dn, dr)
+    out = np.zeros((B, H, dv))
+    slse = np.zeros((shards, B, H))
+    _load().orc_tpla_decode(B, L, shards, H, dk, dn, dr, dv, float(base), float(scale), float(eps),
+                            _p(q_nope), _p(q_pe), _p(c_raw), _p(kpe_cache), _p(w_kv_b), _p(rms_w),
+                            _p(out), _p(slse))
+    return out, slse
 
 
 def lse_combine(part_out, part_lse):

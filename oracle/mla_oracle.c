@@ -395,6 +395,91 @@ void orc_mla_decode(int B, int kv_len, int n_splits, int n_heads,
         }
 }
 
+/* ------------------------------------------------- TPLA latent decode ---- */
+/*
+ * TPLA, "The reading" and "What carries the argument": the latent c_KV and each head's
+ * input dimension are split into g shards; every shard attends with all query heads over
+ * its own part of the latent (a local softmax over its own scores) and the shards'
+ * outputs are summed (the all-reduce).  The page calls the result a grouped latent
+ * attention with replicated heads.  Readings where the page is silent (each one is in
+ * the design notes):
+ *  - no orthogonal reparameterisation (U = I): its Hadamard and PCA forms need
+ *    calibration data;
+ *  - shard i owns latent dims [i Dk/g, (i+1) Dk/g) and normalises them by its own
+ *    RMSNorm with the matching slice of the weight (Condition 1 read as a per-shard
+ *    norm);
+ *  - every shard also reads the whole RoPE band (576 -> 320 dims per shard at g = 2);
+ *  - the score scale stays 1/sqrt(d_nope + d_rope) and the local softmax is not
+ *    rescaled (the referee report's second major comment: the deployed form uses an
+ *    unscaled local softmax).
+ * Inputs as orc_mla_decode, except that c_raw [B,kv_len,Dk] is the latent before any
+ * normalisation (rms_w [Dk], eps).  Outputs: out [B,H,Dv], the sum over shards, and
+ * shard_lse [g,B,H], each shard's log-sum-exp.
+ */
+void orc_tpla_decode(int B, int kv_len, int g, int n_heads, int Dk, int Dn, int Dr, int Dv,
+                     double base, double scale, double eps,
+                     const double *q_nope, const double *q_pe, const double *c_raw,
+                     const double *kpe_cache, const double *w_kv_b, const double *rms_w,
+                     double *out, double *shard_lse)
+{
+    int Dh = Dn + Dv, ds = Dk / g;
+    long nk = kv_len > 0 ? kv_len : 1;
+    /* the per-shard normalised latent of every cached key */
+    double *chat = (double *)malloc(sizeof(double) * (size_t)B * nk * Dk);
+    for (long r = 0; r < (long)B * kv_len; ++r)
+        for (int i = 0; i < g; ++i)
+            rmsnorm_row(c_raw + r * Dk + (size_t)i * ds, rms_w + (size_t)i * ds, ds, eps,
+                        chat + r * Dk + (size_t)i * ds);
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < n_heads; ++h) {
+            const double *wk = w_kv_b + (size_t)h * Dh * Dk;
+            const double *wv = wk + (size_t)Dn * Dk;
+            double *qa = (double *)malloc(sizeof(double) * Dk);
+            double *ol = (double *)malloc(sizeof(double) * Dk);
+            double *sc = (double *)malloc(sizeof(double) * nk);
+            double *pw = (double *)malloc(sizeof(double) * nk);
+            double qr[1024];
+            size_t row = (size_t)b * n_heads + h;
+            const double *qn = q_nope + row * Dn;
+            for (int k = 0; k < Dk; ++k) {
+                double acc = 0.0;
+                for (int d = 0; d < Dn; ++d)
+                    acc += qn[d] * wk[(size_t)d * Dk + k];
+                qa[k] = acc;
+            }
+            rope_row(q_pe + row * Dr, (double)(kv_len - 1), Dr, base, qr);
+            const double *cb = chat + (size_t)b * kv_len * Dk;
+            const double *kb = kpe_cache + (size_t)b * kv_len * Dr;
+            for (int d = 0; d < Dv; ++d)
+                out[row * Dv + d] = 0.0;
+            for (int i = 0; i < g; ++i) {
+                const int k0 = i * ds;
+                /* this shard's scores: its latent dims plus the whole RoPE band */
+                for (long j = 0; j < kv_len; ++j)
+                    sc[j] = scale * (dot(qa + k0, cb + j * Dk + k0, ds) + dot(qr, kb + j * Dr, Dr));
+                double z;
+                double l = softmax_weights(sc, kv_len, pw, &z);
+                for (int k = k0; k < k0 + ds; ++k) {
+                    double acc = 0.0;
+                    for (long j = 0; j < kv_len; ++j)
+                        acc += pw[j] * cb[j * Dk + k];
+                    ol[k] = kv_len > 0 ? acc / z : 0.0;
+                }
+                /* this shard's part of the up-projection, summed over the shards */
+                for (int d = 0; d < Dv; ++d)
+                    out[row * Dv + d] += dot(wv + (size_t)d * Dk + k0, ol + k0, ds);
+                shard_lse[(size_t)i * B * n_heads + row] = l;
+            }
+            free(qa);
+            free(ol);
+            free(sc);
+            free(pw);
+        }
+    free(chat);
+}
+
 /* ------------------------------------------------------ LSE combine ---- */
 /*
  * Helix, "What carries the argument" and "Assumptions" (paper section 2.1.1):

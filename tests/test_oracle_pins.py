@@ -14,6 +14,10 @@
 * Decode    -- split partials merged by the log-sum-exp rescale equal the unsplit
               result (Helix, "Assumptions", paper section 2.1.1); decode at position
               L-1 equals the last row of a prefill over the same latent.
+* TPLA      -- one shard is plain latent decode; g shards equal the sum of g independent
+              latent decodes over the shard slices (TPLA, "The reading"), and the same
+              sum rebuilt from library routines (torch rms_norm per shard, matmul,
+              softmax, logsumexp).
 """
 import math
 
@@ -285,6 +289,68 @@ def test_decode_equals_last_prefill_row(oracle):
                                        inp["w_kv_b"], n_splits=4)
     np.testing.assert_allclose(out, o_ref[:, 0], rtol=0, atol=1e-11)
     np.testing.assert_allclose(lse, l_ref[:, :, 0], rtol=0, atol=1e-11)
+
+
+def _tpla_inputs(B, H, L, dk, dn, dr, dv, seed):
+    inp = _decode_inputs(B, H, L, dk, dn, dr, dv, seed)
+    g = np.random.default_rng(seed + 1)
+    c_raw = inp.pop("c_cache") * (1.0 + 2.0 * g.random((1, 1, dk)))   # shards differ in scale
+    return dict(inp, c_raw=c_raw, rms_w=1.0 + 0.2 * g.standard_normal(dk))
+
+
+def test_tpla_one_shard_is_latent_decode(oracle):
+    B, H, L, dk, dn, dr, dv = 2, 3, 57, 32, 16, 8, 16
+    inp = _tpla_inputs(B, H, L, dk, dn, dr, dv, 61)
+    out, slse = oracle.tpla_decode(**inp, shards=1, eps=EPS)
+    cache = oracle.rmsnorm(inp["c_raw"].reshape(-1, dk), inp["rms_w"], EPS).reshape(B, L, dk)
+    ref, lse, _, _ = oracle.mla_decode(inp["q_nope"], inp["q_pe"], cache, inp["kpe_cache"],
+                                       inp["w_kv_b"], n_splits=3)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(slse[0], lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("shards", [2, 4])
+def test_tpla_shards_sum_of_slice_decodes(oracle, shards):
+    B, H, L, dk, dn, dr, dv = 2, 3, 41, 32, 16, 8, 16
+    inp = _tpla_inputs(B, H, L, dk, dn, dr, dv, 71)
+    out, slse = oracle.tpla_decode(**inp, shards=shards, eps=EPS)
+    ds, acc = dk // shards, 0.0
+    for i in range(shards):
+        sl = slice(i * ds, (i + 1) * ds)
+        ci = np.ascontiguousarray(inp["c_raw"][..., sl]).reshape(-1, ds)
+        ci = oracle.rmsnorm(ci, inp["rms_w"][sl], EPS).reshape(B, L, ds)
+        oi, li, _, _ = oracle.mla_decode(inp["q_nope"], inp["q_pe"], ci, inp["kpe_cache"],
+                                         np.ascontiguousarray(inp["w_kv_b"][:, sl]), n_splits=2,
+                                         scale=oracle.default_scale(dn, dr))
+        acc = acc + oi
+        np.testing.assert_allclose(slse[i], li, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out, acc, rtol=0, atol=1e-12)
+    full, _, _, _ = oracle.mla_decode(inp["q_nope"], inp["q_pe"],
+                                      oracle.rmsnorm(inp["c_raw"].reshape(-1, dk), inp["rms_w"], EPS)
+                                      .reshape(B, L, dk), inp["kpe_cache"], inp["w_kv_b"])
+    assert np.abs(out - full).max() > 1e-3          # sharding really changes the result
+
+
+def test_tpla_matches_library_composition(oracle):
+    B, H, L, dk, dn, dr, dv, G = 2, 4, 37, 32, 16, 8, 16, 2
+    inp = _tpla_inputs(B, H, L, dk, dn, dr, dv, 81)
+    out, slse = oracle.tpla_decode(**inp, shards=G, eps=EPS)
+    t = {k: torch.from_numpy(v) for k, v in inp.items()}
+    W = t["w_kv_b"].reshape(H, dn + dv, dk)
+    q_abs = torch.einsum("bhd,hdk->bhk", t["q_nope"], W[:, :dn])
+    qr = torch.from_numpy(_rope_complex(inp["q_pe"], np.full((B, H), L - 1.0), dr))
+    scale = 1.0 / math.sqrt(dn + dr)
+    ref_o = torch.zeros(B, H, dv, dtype=torch.float64)
+    ds = dk // G
+    for i in range(G):
+        sl = slice(i * ds, (i + 1) * ds)
+        c = F.rms_norm(t["c_raw"][..., sl], (ds,), t["rms_w"][sl], EPS)       # [B,L,ds]
+        s = (torch.einsum("bhk,blk->bhl", q_abs[..., sl], c)
+             + torch.einsum("bhr,blr->bhl", qr, t["kpe_cache"])) * scale
+        o_lat = torch.einsum("bhl,blk->bhk", torch.softmax(s, -1), c)
+        ref_o += torch.einsum("hdk,bhk->bhd", W[:, dn:, sl], o_lat)
+        np.testing.assert_allclose(slse[i], torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out, ref_o.numpy(), rtol=0, atol=1e-12)
 
 
 def test_golden_rows_unchanged(oracle):
