@@ -213,6 +213,66 @@ def decode_call(cfg, d, t, out, lse, ws, stream):
         raise RuntimeError("mla_decode_splitkv: " + mla.mla_status_string(st))
 
 
+def tpla_setup(cfg, n_shards, seed=1):
+    """The decode workload with its latent cache normalised per shard (the cache write of
+    a TPLA deployment) and a workspace for the TPLA decode over ``n_shards`` shards."""
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import inputs, mla
+    d, t, out, _, _ = decode_setup(cfg, seed)
+    dt = cfg.torch_dtype
+    w = inputs.norm_weight(cfg.d_kv, dt).cuda()
+    t["c_raw"], t["norm_w"] = t["c_cache"], w
+    t["c_cache"] = mla.rmsnorm(t["c_raw"], w, n_shards=n_shards)
+    slse = torch.empty(n_shards, cfg.batch, cfg.n_heads, dtype=torch.float32, device="cuda")
+    nbytes = mla.mla_tpla_decode_workspace(ctypes.byref(d), mla.MLA_BF16 if cfg.dtype == "bf16" else mla.MLA_F32,
+                                           cfg.batch, cfg.kv_len, cfg.n_splits, n_shards)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    return d, t, out, slse, ws
+
+
+def tpla_call(cfg, n_shards, d, t, out, slse, ws, stream):
+    from head_latent_attention_rmsnorm_gb300 import mla
+    st = mla.lib().mla_tpla_decode(ctypes.byref(d), mla.MLA_BF16 if cfg.dtype == "bf16" else mla.MLA_F32,
+                                   cfg.batch, cfg.kv_len, cfg.n_splits, n_shards, t["q_nope"].data_ptr(),
+                                   t["q_pe"].data_ptr(), t["c_cache"].data_ptr(), t["kpe_cache"].data_ptr(),
+                                   t["w_kv_b"].data_ptr(), out.data_ptr(), slse.data_ptr(), ws.data_ptr(),
+                                   ws.numel(), stream)
+    if st != 0:
+        raise RuntimeError("mla_tpla_decode: " + mla.mla_status_string(st))
+
+
+def tpla_extra(dcfg, stream, hbm_peak, n_shards=2, steps=10, warmup=3):
+    """TPLA decode (latent cut into two shards, each attended by all heads with its own
+    softmax, outputs summed) on the decode workload, and the per-shard RMSNorm that
+    writes its cache, timed over the whole cache: reported beside the headline."""
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import mla
+    d, t, out, slse, ws = tpla_setup(dcfg, n_shards)
+    fn = lambda: tpla_call(dcfg, n_shards, d, t, out, slse, ws, stream)  # noqa: E731
+    ms = statistics.mean(timed(fn, steps, warmup, 1))
+    nbytes = dcfg.algorithmic_bytes()
+    normed = torch.empty_like(t["c_raw"])
+    nfn = lambda: mla.rmsnorm(t["c_raw"], t["norm_w"], n_shards=n_shards, out=normed)  # noqa: E731
+    n_ms = statistics.mean(timed(nfn, steps, warmup, 1))
+    n_bytes = 2 * t["c_raw"].numel() * t["c_raw"].element_size() + t["norm_w"].numel() * 2
+    mla.profile_reset()
+    mla.profile_enable(True)
+    fn()
+    prof = mla.profile_all()
+    mla.profile_enable(False)
+    path = mla.last_path()
+    del d, t, out, slse, ws, normed
+    torch.cuda.empty_cache()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": dcfg.name + "_tpla%d" % n_shards, "n_shards": n_shards, "ms_per_call": round(ms, 4),
+            "GB/s": round(gbs, 1), "bytes_per_call": nbytes, "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+            "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"),
+            "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()},
+            "cache_rmsnorm": {"rows": dcfg.batch * dcfg.kv_len, "ms": round(n_ms, 4), "bytes": n_bytes,
+                              "GB/s": round(n_bytes / (n_ms * 1e-3) / 1e9, 1),
+                              "frac_of_measured_hbm": round(n_bytes / (n_ms * 1e-3) / 1e9 / hbm_peak, 4)}}
+
+
 def timed(fn, steps, warmup, world, flush=None):
     """Per-call CUDA-event times (ms) of `steps` calls after `warmup` calls."""
     import torch
@@ -397,12 +457,13 @@ def run_ours(args, world, rank, local):
 
     # ---- beside the headline: the other prefill configs and the activation memory
     # (after every timed region; rank 0 at N = 1 only, so replicas are not slowed)
-    others, mem = None, None
+    others, mem, tpla = None, None, None
     if rank == 0 and world == 1 and not args.no_extras:
         del d, t, out, lse, ws, dd, dt_, dout, dlse, dws, flush
         torch.cuda.empty_cache()
         others = other_prefill_configs(stream)
         mem = activation_memory()
+        tpla = tpla_extra(dcfg, stream, peaks.get("hbm_gbs", 6800.0))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -432,6 +493,7 @@ def run_ours(args, world, rank, local):
                    "kernel_path": {1: "simt", 2: "tcgen05"}.get(dpath, "?"), "roofline": droof,
                    "l2": "inputs (2.4 GB) larger than L2"},
         "other_prefill_configs": others,
+        "tpla_decode": tpla,
         "activation_memory": mem,
         "kernels_prefill": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_p.items()},
         "kernels_decode": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_d.items()},
@@ -458,8 +520,12 @@ def run_case(args):
         if args.batch:
             import dataclasses
             cfg = dataclasses.replace(cfg, batch=args.batch)
-        d, t, out, lse, ws = decode_setup(cfg)
-        fn = lambda: decode_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
+        if args.only == "tpla":
+            d, t, out, slse, ws = tpla_setup(cfg, 2)
+            fn = lambda: tpla_call(cfg, 2, d, t, out, slse, ws, stream)  # noqa: E731
+        else:
+            d, t, out, lse, ws = decode_setup(cfg)
+            fn = lambda: decode_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
     for _ in range(args.warmup + args.steps):
         fn()
     torch.cuda.synchronize()
@@ -540,7 +606,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the V3 / SP=8-rank prefill timings and the activation-memory measurement")
-    ap.add_argument("--only", choices=("prefill", "decode"), default=None,
+    ap.add_argument("--only", choices=("prefill", "decode", "tpla"), default=None,
                     help="run only this workload's calls, without timing (profiling target)")
     ap.add_argument("--workload", default=None, help="prefill workload name for --only prefill")
     ap.add_argument("--batch", type=int, default=0, help="decode batch for --only decode (default 64)")

@@ -409,16 +409,19 @@ mla_status absorbed_simt(const Prefill &p, float scale, const void *q_nope, cons
 // ------------------------------------------------------------ decode shapes ----
 struct Decode {
     int B, L, n, H, Dk, Dn, Dr, Dv;
+    int g;   // latent shards (TPLA); 1 for plain latent decode
     long chunk;
     bool tc;
     int tin, tmid;
 };
 
-mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int n_splits, Decode *p) {
+mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int n_splits, Decode *p, int g = 1) {
     mla_status st = check_dims(d);
     if (st != MLA_OK) return st;
     if (!valid_dtype(dt)) return MLA_ERR_DTYPE;
     if (B < 0 || kv_len < 1 || n_splits < 1 || n_splits > 256) return MLA_ERR_SHAPE;
+    if (g < 1 || g > 16 || d->d_kv % g) return MLA_ERR_SHAPE;
+    p->g = g;
     p->B = B;
     p->L = kv_len;
     p->n = n_splits;
@@ -429,7 +432,7 @@ mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int 
     p->Dv = d->d_v;
     p->chunk = ((long)kv_len + n_splits - 1) / n_splits;
     if (p->Dk + p->Dr > 640 || p->Dk > 512) return MLA_ERR_UNSUPPORTED;
-    p->tc = dt == MLA_BF16 && g_path_override != 1 && tc_decode_supported(p->Dk, p->Dn, p->Dr, p->Dv, p->H);
+    p->tc = dt == MLA_BF16 && g_path_override != 1 && tc_decode_supported(p->Dk, p->Dn, p->Dr, p->Dv, p->H * g);
     p->tin = ty_of(dt);
     p->tmid = p->tc ? TY_F16 : TY_F32;
     return MLA_OK;
@@ -437,6 +440,7 @@ mla_status decode_shape(const mla_dims *d, mla_dtype dt, int B, int kv_len, int 
 
 struct DecodeWs {
     void *qabs, *qpe, *olat;
+    void *qx, *qpx;   // TPLA: the g query rows of every head
     float *po, *pl;
     float2 *rtab;
     size_t bytes;
@@ -452,9 +456,13 @@ DecodeWs decode_ws(const Decode &p, void *base, bool own_partials) {
     w.qpe = c.take(rows * p.Dr * es);
     w.olat = c.take(rows * p.Dk * es);
     w.rtab = (float2 *)c.take((size_t)(p.Dr / 2) * sizeof(float2));
+    if (p.g > 1) {
+        w.qx = c.take(rows * p.g * p.Dk * es);
+        w.qpx = c.take(rows * p.g * p.Dr * es);
+    }
     if (own_partials) {
-        w.po = (float *)c.take((size_t)p.n * rows * p.Dk * 4);
-        w.pl = (float *)c.take((size_t)p.n * rows * 4);
+        w.po = (float *)c.take((size_t)p.n * rows * p.g * p.Dk * 4);
+        w.pl = (float *)c.take((size_t)p.n * rows * p.g * 4);
     }
     w.bytes = align_up(c.off, 256);
     return w;
@@ -490,20 +498,23 @@ mla_status decode_simt(const Decode &p, float scale, const mla_dims *d, const vo
     g.c_m = (long)p.H * p.Dk;
     g.c_n = 1;
     MLA_TRY(launch_gemm_simt(g, st));
+    // TPLA: g query rows per head, each seeing only its shard of the latent
+    const int HX = p.H * p.g;
+    if (p.g > 1) MLA_TRY(launch_tpla_expand(p.tmid, p.B, p.H, p.g, p.Dk, p.Dr, w.qabs, w.qpe, w.qx, w.qpx, st));
     AttnArgs a{};
     a.n_b = p.B;
     a.n_h = 1;
-    a.n_rows = p.H;
+    a.n_rows = HX;
     a.D1 = p.Dk;
     a.D2 = p.Dr;
     a.Dv = p.Dk;
-    a.q1 = w.qabs;
+    a.q1 = p.g > 1 ? w.qx : w.qabs;
     a.tq1 = p.tmid;
-    a.q1_b = (long)p.H * p.Dk;
+    a.q1_b = (long)HX * p.Dk;
     a.q1_r = p.Dk;
-    a.q2 = w.qpe;
+    a.q2 = p.g > 1 ? w.qpx : w.qpe;
     a.tq2 = p.tmid;
-    a.q2_b = (long)p.H * p.Dr;
+    a.q2_b = (long)HX * p.Dr;
     a.q2_r = p.Dr;
     a.k1 = c_cache;
     a.tk1 = p.tin;
@@ -524,15 +535,18 @@ mla_status decode_simt(const Decode &p, float scale, const mla_dims *d, const vo
     a.pos0 = p.L - 1;
     a.scale = scale;
     a.part_out = po;
-    a.po_s = rows * p.Dk;
-    a.po_b = (long)p.H * p.Dk;
+    a.po_s = rows * p.g * p.Dk;
+    a.po_b = (long)HX * p.Dk;
     a.po_r = p.Dk;
     a.part_lse = pl;
-    a.pl_s = rows;
-    a.pl_b = p.H;
+    a.pl_s = rows * p.g;
+    a.pl_b = HX;
     a.pl_r = 1;
     MLA_TRY(launch_attn_simt(a, st));
-    MLA_TRY(launch_lse_combine(p.tmid, p.n, rows, p.Dk, po, pl, w.olat, lse, st));
+    if (p.g > 1)
+        MLA_TRY(launch_tpla_combine(p.tmid, p.n, p.B, p.H, p.g, p.Dk, po, pl, w.olat, lse, st));
+    else
+        MLA_TRY(launch_lse_combine(p.tmid, p.n, rows, p.Dk, po, pl, w.olat, lse, st));
     GemmArgs u{};
     u.M = p.B;
     u.N = p.Dv;
@@ -636,12 +650,23 @@ size_t mla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv
     return decode_ws(p, nullptr, true).bytes;
 }
 
-mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits,
-                              const void *q_nope, const void *q_pe, const void *c_cache, const void *kpe_cache,
-                              const void *w_kv_b, void *out, float *lse, float *part_out, float *part_lse,
-                              void *workspace, size_t workspace_bytes, void *cuda_stream) {
+size_t mla_tpla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits,
+                                 int n_shards) {
     Decode p;
-    mla_status st = decode_shape(dims, dtype, B, kv_len, n_splits, &p);
+    if (decode_shape(dims, dtype, B, kv_len, n_splits, &p, n_shards) != MLA_OK) return 0;
+    if (B == 0) return 0;
+    return decode_ws(p, nullptr, true).bytes;
+}
+
+namespace {
+// Split-KV latent decode over g latent shards (g = 1: plain latent decode).  With g > 1
+// `lse` is the shard log-sum-exps [g][B][H] and the partials stay in the workspace.
+mla_status decode_call(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits, int g,
+                       const void *q_nope, const void *q_pe, const void *c_cache, const void *kpe_cache,
+                       const void *w_kv_b, void *out, float *lse, float *part_out, float *part_lse, void *workspace,
+                       size_t workspace_bytes, void *cuda_stream) {
+    Decode p;
+    mla_status st = decode_shape(dims, dtype, B, kv_len, n_splits, &p, g);
     if (st != MLA_OK) return st;
     if (B == 0) return MLA_OK;
     const void *ptrs[] = {q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse};
@@ -661,7 +686,7 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
     Range in[] = {rng(q_nope, rows * p.Dn * es), rng(q_pe, rows * p.Dr * es),
                   rng(c_cache, (size_t)p.B * p.L * p.Dk * es), rng(kpe_cache, (size_t)p.B * p.L * p.Dr * es),
                   rng(w_kv_b, (size_t)p.H * (p.Dn + p.Dv) * p.Dk * es)};
-    Range outs[] = {rng(out, rows * p.Dv * es), rng(lse, rows * 4), rng(workspace, wsz.bytes),
+    Range outs[] = {rng(out, rows * p.Dv * es), rng(lse, rows * p.g * 4), rng(workspace, wsz.bytes),
                     rng(part_out, (size_t)p.n * rows * p.Dk * 4), rng(part_lse, (size_t)p.n * rows * 4)};
     st = check_alias(in, 5, outs, 5);
     if (st != MLA_OK) return st;
@@ -675,11 +700,45 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
         const long rows = (long)p.B * p.H;
         MLA_TRY(launch_rope_table(p.L - 1, 1, p.Dr, dims->rope_base, w.rtab, cs));
         MLA_TRY(launch_rope_rows(p.tin, TY_F16, rows, p.Dr, q_pe, p.L - 1, 1, 1, w.rtab, p.L - 1, w.qpe, cs));
-        TcDecode t{p.B, p.L, p.n, p.H, p.Dk, p.Dn, p.Dr, p.Dv, p.chunk, scale, dims->rope_base};
+        TcDecode t{p.B, p.L, p.n, p.H, p.Dk, p.Dn, p.Dr, p.Dv, p.chunk, scale, dims->rope_base, p.g};
         return cuda_status(tc_decode(t, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w.qabs, w.qpe,
-                                     w.olat, cs));
+                                     w.olat, w.qx, w.qpx, cs));
     }
     return decode_simt(p, scale, dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w, cs);
+}
+}  // namespace
+
+mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits,
+                              const void *q_nope, const void *q_pe, const void *c_cache, const void *kpe_cache,
+                              const void *w_kv_b, void *out, float *lse, float *part_out, float *part_lse,
+                              void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    return decode_call(dims, dtype, B, kv_len, n_splits, 1, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse,
+                       part_out, part_lse, workspace, workspace_bytes, cuda_stream);
+}
+
+mla_status mla_tpla_decode(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits, int n_shards,
+                           const void *q_nope, const void *q_pe, const void *c_cache, const void *kpe_cache,
+                           const void *w_kv_b, void *out, float *shard_lse, void *workspace, size_t workspace_bytes,
+                           void *cuda_stream) {
+    return decode_call(dims, dtype, B, kv_len, n_splits, n_shards, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out,
+                       shard_lse, nullptr, nullptr, workspace, workspace_bytes, cuda_stream);
+}
+
+mla_status mla_rmsnorm(mla_dtype dtype, long rows, int d, int n_shards, float eps, const void *x, const void *w,
+                       void *y, void *cuda_stream) {
+    if (!valid_dtype(dtype)) return MLA_ERR_DTYPE;
+    if (rows < 0 || d < 1 || n_shards < 1 || d % n_shards || !(eps >= 0.f)) return MLA_ERR_SHAPE;
+    if (rows == 0) return MLA_OK;
+    if (!x || !w || !y) return MLA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MLA_ERR_ALIGN;
+    const size_t es = ty_size(ty_of(dtype));
+    Range in[] = {rng(x, (size_t)rows * d * es), rng(w, (size_t)d * es)};
+    Range outs[] = {rng(y, (size_t)rows * d * es)};
+    mla_status st = check_alias(in, 2, outs, 1);
+    if (st != MLA_OK) return st;
+    g_last_path = 1;
+    return cuda_status(launch_rmsnorm_shards(ty_of(dtype), rows, d, n_shards, eps, x, w, y,
+                                             (cudaStream_t)cuda_stream));
 }
 
 mla_status mla_lse_combine(mla_dtype out_dtype, int n_splits, int rows, int D, const float *part_out,

@@ -95,6 +95,21 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_lse_combine(int tout, int n, long rows, int D, const float *po, const float *pl, void *out,
                                float *lse, cudaStream_t st);
 
+// y = per-shard RMSNorm of x [rows][D]: each of the g shards of D/g columns is scaled by
+// its own 1/sqrt(mean square + eps) and multiplied by the matching slice of w [D].
+cudaError_t launch_rmsnorm_shards(int ty, long rows, int D, int g, float eps, const void *x, const void *w, void *y,
+                                  cudaStream_t st);
+
+// TPLA decode around the latent decode kernels: qa [B][H][Dk], qp [B][H][Dr] -> qx
+// [B][g][H][Dk] (row (b,i,h) zero outside shard i's dims), qpx [B][g][H][Dr] (replicated);
+// storage ty.
+cudaError_t launch_tpla_expand(int ty, int B, int H, int g, int Dk, int Dr, const void *qa, const void *qp, void *qx,
+                               void *qpx, cudaStream_t st);
+// Split partials po [n][B][g][H][Dk], pl [n][B][g][H] -> out [B][H][Dk] (shard i's dims from
+// rows (b,i,h), storage tout) and the shard log-sum-exps slse [g][B][H].
+cudaError_t launch_tpla_combine(int tout, int n, int B, int H, int g, int Dk, const float *po, const float *pl,
+                                void *out, float *slse, cudaStream_t st);
+
 // Reads and clears the bounded-wait error words of the tensor-core kernels.
 cudaError_t tc_read_and_clear_error(unsigned int *flags, cudaStream_t st);
 

@@ -13,6 +13,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "mla_internal.h"
 
 namespace mla {
@@ -702,6 +704,188 @@ cudaError_t launch_lse_combine(int tout, int n, long rows, int D, const float *p
             <<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, (__nv_bfloat16 *)out, lse);
     else
         lse_combine_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, out, tout, lse);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- latent shards ----
+__device__ __forceinline__ long ty_size_dev(int ty) { return ty == TY_F32 ? 4 : 2; }
+
+// A 16-byte piece as 4 fp32 or 8 fp16/bf16 values, and back.
+__device__ __forceinline__ void unpack16(uint4 v, int ty, float *f) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int t = 0; t < 4; ++t) {
+        if (ty == TY_F32) {
+            f[t] = __uint_as_float(u[t]);
+        } else if (ty == TY_BF16) {
+            f[2 * t] = __uint_as_float(u[t] << 16);
+            f[2 * t + 1] = __uint_as_float(u[t] & 0xffff0000u);
+        } else {
+            const __half2 h = *(const __half2 *)&u[t];
+            f[2 * t] = __low2float(h);
+            f[2 * t + 1] = __high2float(h);
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 pack16(const float *f, int ty) {
+    uint32_t u[4];
+    for (int t = 0; t < 4; ++t) {
+        if (ty == TY_F32) {
+            u[t] = __float_as_uint(f[t]);
+        } else if (ty == TY_BF16) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * t], f[2 * t + 1]);
+            u[t] = *(const uint32_t *)&h;
+        } else {
+            const __half2 h = __floats2half2_rn(f[2 * t], f[2 * t + 1]);
+            u[t] = *(const uint32_t *)&h;
+        }
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+// TPLA ("The reading"): the latent row is cut into g equal shards and each shard is
+// RMS-normalised on its own with the matching slice of the weight (g = 1: the plain
+// RMSNorm of the LAGA page's step 1).  One warp per (row, shard); with `vec` each lane
+// moves 16-byte pieces (the shard's byte width is then a multiple of 16).
+__global__ void rmsnorm_shards_kernel(int ty, long rows, int D, int g, float eps, bool vec, const void *x,
+                                      const void *w, void *y) {
+    const long u = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (u >= rows * g) return;
+    const long r = u / g;
+    const int ds = D / g, k0 = (int)(u % g) * ds;
+    const long o = r * D + k0;
+    float ss = 0.f;
+    if (vec) {
+        const int per = ty == TY_F32 ? 4 : 8, nv = ds / per;
+        const uint4 *src = (const uint4 *)((const char *)x + o * ty_size_dev(ty));
+        for (int c = lane; c < nv; c += 32) {
+            const uint4 v = src[c];
+            float f[8];
+            unpack16(v, ty, f);
+            for (int t = 0; t < per; ++t) ss = fmaf(f[t], f[t], ss);
+        }
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)ds + eps);
+        uint4 *dst = (uint4 *)((char *)y + o * ty_size_dev(ty));
+        const uint4 *wv = (const uint4 *)((const char *)w + (long)k0 * ty_size_dev(ty));
+        for (int c = lane; c < nv; c += 32) {
+            float f[8], fw[8];
+            unpack16(src[c], ty, f);
+            unpack16(wv[c], ty, fw);
+            for (int t = 0; t < per; ++t) f[t] = f[t] * inv * fw[t];
+            dst[c] = pack16(f, ty);
+        }
+        return;
+    }
+    for (int k = lane; k < ds; k += 32) {
+        const float v = ldx(x, ty, o + k);
+        ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)ds + eps);
+    for (int k = lane; k < ds; k += 32) stx(y, ty, o + k, ldx(x, ty, o + k) * inv * ldx(w, ty, k0 + k));
+}
+
+// TPLA decode, query side: every head becomes g query rows, one per latent shard.  Row
+// (b, i, h) keeps q_abs[b][h] on shard i's dims and zero elsewhere, so its score over
+// the full latent row is the shard-local score q_abs_i . c_i; the rotated q_pe is
+// replicated (every shard also reads the whole RoPE band).
+// qa [B][H][Dk], qp [B][H][Dr] -> qx [B][g][H][Dk], qpx [B][g][H][Dr]; storage `ty`.
+// With `vec` every shard's byte width and Dr's are multiples of 16 and pieces of 16
+// bytes move at a time.
+__global__ void tpla_expand_kernel(int ty, int B, int H, int g, int Dk, int Dr, bool vec, const void *qa,
+                                   const void *qp, void *qx, void *qpx) {
+    const long es = ty_size_dev(ty), per = vec ? 16 / es : 1;
+    const long nk = Dk / per, nr = Dr / per, row_units = nk + nr;
+    const long total = (long)B * g * H * row_units, ds = Dk / g;
+    for (long u = (long)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += (long)gridDim.x * blockDim.x) {
+        const long row = u / row_units, c = u % row_units;   // row = (b * g + i) * H + h
+        const long h = row % H, bi = row / H, i = bi % g, b = bi / g;
+        const long src_row = b * H + h;
+        if (c < nk) {
+            const long k = c * per;
+            const bool keep = k / ds == i;
+            if (vec) {
+                const uint4 v = keep ? ((const uint4 *)qa)[src_row * nk + c] : make_uint4(0, 0, 0, 0);
+                ((uint4 *)qx)[row * nk + c] = v;
+            } else {
+                stx(qx, ty, row * Dk + k, keep ? ldx(qa, ty, src_row * Dk + k) : 0.f);
+            }
+        } else {
+            const long t = c - nk;
+            if (vec)
+                ((uint4 *)qpx)[row * nr + t] = ((const uint4 *)qp)[src_row * nr + t];
+            else
+                stx(qpx, ty, row * Dr + t, ldx(qp, ty, src_row * Dr + t));
+        }
+    }
+}
+
+// TPLA decode, output side: rows (b, i, h) of the split partials are merged by the
+// log-sum-exp rescale, only over shard i's dims, into o_lat[b][h] (each shard fills its
+// own dims, so the later W_V product sums the shards' up-projections), and each row's
+// log-sum-exp goes to shard_lse[i][b][h].
+// po [n][B][g][H][Dk], pl [n][B][g][H] (fp32) -> out [B][H][Dk] (storage `to`).
+__global__ void tpla_combine_kernel(int n, int B, int H, int g, int Dk, const float *po, const float *pl, void *out,
+                                    int to, float *slse) {
+    const long rows = (long)B * g * H;
+    const long r = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (r >= rows) return;
+    const long h = r % H, bi = r / H, i = bi % g, b = bi / g;
+    const int ds = Dk / g, k0 = (int)i * ds;
+    const long orow = (b * H + h) * Dk + k0;
+    float m = -INFINITY;
+    for (int s = lane; s < n; s += 32) m = fmaxf(m, pl[(long)s * rows + r]);
+    m = warp_max(m);
+    float L = -INFINITY;
+    if (m != -INFINITY) {
+        float z = 0.f;
+        for (int s = lane; s < n; s += 32) z += expf(pl[(long)s * rows + r] - m);
+        L = m + logf(warp_sum(z));
+    }
+    for (int d = lane; d < ds; d += 32) {
+        float acc = 0.f;
+        if (m != -INFINITY)
+            for (int s = 0; s < n; ++s) {
+                const float wt = expf(pl[(long)s * rows + r] - L);
+                if (wt > 0.f) acc = fmaf(wt, po[((long)s * rows + r) * Dk + k0 + d], acc);
+            }
+        stx(out, to, orow + d, acc);
+    }
+    if (lane == 0) slse[(i * B + b) * H + h] = L;
+}
+
+cudaError_t launch_rmsnorm_shards(int ty, long rows, int D, int g, float eps, const void *x, const void *w, void *y,
+                                  cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    ProfScope ps("rmsnorm", st);
+    const bool vec = ((long)(D / g) * (long)ty_size(ty)) % 16 == 0 && ((uintptr_t)x & 15) == 0 &&
+                     ((uintptr_t)y & 15) == 0 && ((uintptr_t)w & 15) == 0;
+    rmsnorm_shards_kernel<<<blocks_for(rows * g, 8), 256, 0, st>>>(ty, rows, D, g, eps, vec, x, w, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tpla_expand(int ty, int B, int H, int g, int Dk, int Dr, const void *qa, const void *qp, void *qx,
+                               void *qpx, cudaStream_t st) {
+    if ((long)B * H == 0) return cudaSuccess;
+    ProfScope ps("tpla_expand", st);
+    const long es = (long)ty_size(ty);
+    const bool vec = ((long)(Dk / g) * es) % 16 == 0 && (Dr * es) % 16 == 0 && ((uintptr_t)qa & 15) == 0 &&
+                     ((uintptr_t)qp & 15) == 0 && ((uintptr_t)qx & 15) == 0 && ((uintptr_t)qpx & 15) == 0;
+    const long per = vec ? 16 / es : 1, units = (long)B * g * H * ((Dk + Dr) / per);
+    const long blocks = std::min<long>((units + 255) / 256, 152L * 16);
+    tpla_expand_kernel<<<(unsigned)blocks, 256, 0, st>>>(ty, B, H, g, Dk, Dr, vec, qa, qp, qx, qpx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tpla_combine(int tout, int n, int B, int H, int g, int Dk, const float *po, const float *pl,
+                                void *out, float *slse, cudaStream_t st) {
+    const long rows = (long)B * g * H;
+    if (rows == 0) return cudaSuccess;
+    ProfScope ps("tpla_combine", st);
+    tpla_combine_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(n, B, H, g, Dk, po, pl, out, tout, slse);
     return cudaGetLastError();
 }
 

@@ -16,6 +16,7 @@ struct TcDecode {
     int B, L, n, H, Dk, Dn, Dr, Dv;
     long chunk;
     float scale, rope_base;
+    int g;   // latent shards (TPLA); 1 for plain latent decode
 };
 
 bool tc_explicit_supported(int Dk, int Dn, int Dr, int Dv);
@@ -35,6 +36,6 @@ cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const vo
                                 void *olat, void *w16, cudaStream_t st);
 cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, const void *c_cache,
                       const void *kpe_cache, const void *w_kv_b, void *out, float *lse, float *po, float *pl,
-                      void *qabs, void *qpe, void *olat, cudaStream_t st);
+                      void *qabs, void *qpe, void *olat, void *qx, void *qpx, cudaStream_t st);
 
 }  // namespace mla

@@ -494,7 +494,7 @@ bool tc_decode_supported(int Dk, int Dn, int Dr, int Dv, int H) {
 
 cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, const void *c_cache,
                       const void *kpe_cache, const void *w_kv_b, void *out, float *lse, float *po, float *pl,
-                      void *qabs, void *qpe, void *olat, cudaStream_t st) {
+                      void *qabs, void *qpe, void *olat, void *qx, void *qpx, cudaStream_t st) {
     (void)q_pe;   // rotated into qpe (fp16) by the caller
     const long Dh = p.Dn + p.Dv, rows = (long)p.B * p.H;
     cudaError_t e;
@@ -515,11 +515,23 @@ cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, c
         e = launch_gemm_simt(g, st);
     }
     if (e != cudaSuccess) return e;
-    // 2. per (sequence, split, 128 heads): partial latent output and its lse
-    e = launch_decode_attn(qabs, qpe, c_cache, kpe_cache, p.B, p.L, p.H, p.n, p.chunk, p.scale, po, pl, st);
+    if (p.g > 1) {
+        // TPLA: g query rows per head, row (b, i, h) zero outside latent shard i
+        if ((e = launch_tpla_expand(TY_F16, p.B, p.H, p.g, p.Dk, p.Dr, qabs, qpe, qx, qpx, st)) != cudaSuccess)
+            return e;
+        // 2. the same decode kernel over g*H query rows
+        e = launch_decode_attn(qx, qpx, c_cache, kpe_cache, p.B, p.L, p.H * p.g, p.n, p.chunk, p.scale, po, pl, st);
+        if (e != cudaSuccess) return e;
+        // 3. each shard's merge over its own dims -> o_lat (bf16), shard lse [g][B][H]
+        e = launch_tpla_combine(TY_BF16, p.n, p.B, p.H, p.g, p.Dk, po, pl, olat, lse, st);
+    } else {
+        // 2. per (sequence, split, 128 heads): partial latent output and its lse
+        e = launch_decode_attn(qabs, qpe, c_cache, kpe_cache, p.B, p.L, p.H, p.n, p.chunk, p.scale, po, pl, st);
+        if (e != cudaSuccess) return e;
+        // 3. log-sum-exp merge of the splits -> o_lat (bf16) and lse
+        e = launch_lse_combine(TY_BF16, p.n, rows, p.Dk, po, pl, olat, lse, st);
+    }
     if (e != cudaSuccess) return e;
-    // 3. log-sum-exp merge of the splits -> o_lat (bf16) and lse
-    if ((e = launch_lse_combine(TY_BF16, p.n, rows, p.Dk, po, pl, olat, lse, st)) != cudaSuccess) return e;
     // 4. out[b][h][d] = sum_k o_lat[b][h][k] W_V(h)[d][k]: rows b (M), columns d (N), so
     //    each output row is written contiguously (a 128-row tile holds B = 64 valid rows)
     if (tc_small_gemms) {

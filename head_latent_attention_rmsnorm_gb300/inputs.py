@@ -19,6 +19,7 @@ BLOCK = 256
 # tensor ids (part of the stream key)
 Q_NOPE, Q_PE, C_KV, K_PE, W_KV_B = 1, 2, 3, 4, 5
 DEC_Q_NOPE, DEC_Q_PE, DEC_C_CACHE, DEC_KPE_CACHE = 11, 12, 13, 14
+NORM_W = 15
 
 
 def normal_rows(seed: int, tid: int, n_rows: int, row_elems: int, std: float = 1.0,
@@ -92,3 +93,9 @@ def decode_inputs(cfg, seed: int = 0, batches: tuple[int, int] | None = None,
         d["w_kv_b"] = to_torch(normal_rows(seed, W_KV_B, rows, cfg.d_kv, std=cfg.d_kv ** -0.5), dt,
                                (rows, cfg.d_kv))
     return d
+
+
+def norm_weight(d: int, dtype: torch.dtype, seed: int = 0, std: float = 0.1) -> torch.Tensor:
+    """A latent-norm weight [d] drawn as 1 + N(0, std^2), rounded to ``dtype`` (the
+    prefill workloads use all ones; shard tests want a weight whose slices differ)."""
+    return to_torch(1.0 + normal_rows(seed, NORM_W, 1, d, std), dtype, (d,))

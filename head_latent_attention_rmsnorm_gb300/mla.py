@@ -5,7 +5,8 @@ Two layers, argument marshalling only:
 * ``mla_latent_attn_fwd`` ... ``mla_lse_combine``, the ``*_workspace`` queries,
   ``mla_status_string``, ``mla_check_device_error``: the C entry points under their
   own names, taking integers for pointers and sizes.
-* ``latent_attn_fwd``, ``absorbed_attn_fwd``, ``decode_splitkv``, ``lse_combine``:
+* ``latent_attn_fwd``, ``absorbed_attn_fwd``, ``decode_splitkv``, ``lse_combine``,
+  ``tpla_decode``, ``rmsnorm``:
   the same calls taking torch tensors; they allocate any output or workspace the
   caller did not pass (through torch's allocator, so the CUDA caching allocator sees
   every byte) and raise :class:`MlaError` on a non-OK status.
@@ -78,6 +79,12 @@ def lib() -> ctypes.CDLL:
             getattr(L, f).restype = _sz
         L.mla_decode_workspace.argtypes = [D, _i, _i, _i, _i]
         L.mla_decode_workspace.restype = _sz
+        L.mla_tpla_decode.argtypes = [D, _i, _i, _i, _i, _i] + [_vp] * 7 + [_vp, _sz, _vp]
+        L.mla_tpla_decode.restype = _i
+        L.mla_tpla_decode_workspace.argtypes = [D, _i, _i, _i, _i, _i]
+        L.mla_tpla_decode_workspace.restype = _sz
+        L.mla_rmsnorm.argtypes = [_i, ctypes.c_long, _i, _i, ctypes.c_float, _vp, _vp, _vp, _vp]
+        L.mla_rmsnorm.restype = _i
         L.mla_status_string.argtypes = [_i]
         L.mla_status_string.restype = ctypes.c_char_p
         L.mla_check_device_error.argtypes = [_vp]
@@ -135,6 +142,18 @@ def mla_decode_workspace(*args) -> int:
     return lib().mla_decode_workspace(*args)
 
 
+def mla_tpla_decode(*args) -> int:
+    return lib().mla_tpla_decode(*args)
+
+
+def mla_tpla_decode_workspace(*args) -> int:
+    return lib().mla_tpla_decode_workspace(*args)
+
+
+def mla_rmsnorm(*args) -> int:
+    return lib().mla_rmsnorm(*args)
+
+
 def mla_status_string(status: int) -> str:
     return lib().mla_status_string(status).decode()
 
@@ -152,7 +171,8 @@ def set_path_override(mode: int) -> None:
 
 
 KERNELS = ("prep", "latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
-           "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose")
+           "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "tpla_expand",
+           "tpla_combine")
 
 
 def launch_count() -> int:
@@ -261,6 +281,38 @@ def decode_splitkv(d: Dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_split
                             _ptr(part_lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "mla_decode_splitkv")
     return out, lse
+
+
+def tpla_decode(d: Dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_shards=2, n_splits=1, out=None,
+                shard_lse=None, workspace=None, stream=None):
+    """TPLA decode over ``n_shards`` latent shards (``c_cache`` normalised per shard, as
+    :func:`rmsnorm` with the same ``n_shards`` writes it).  Returns (out, shard_lse)."""
+    B, H, _ = q_nope.shape
+    L = c_cache.shape[1]
+    dt = _dt(q_nope)
+    if out is None:
+        out = torch.empty(B, H, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
+    if shard_lse is None:
+        shard_lse = torch.empty(n_shards, B, H, dtype=torch.float32, device=q_nope.device)
+    nbytes = mla_tpla_decode_workspace(ctypes.byref(d), dt, B, L, n_splits, n_shards)
+    ws = _workspace(nbytes, q_nope.device, workspace)
+    st = mla_tpla_decode(ctypes.byref(d), dt, B, L, n_splits, n_shards, _ptr(q_nope), _ptr(q_pe), _ptr(c_cache),
+                         _ptr(kpe_cache), _ptr(w_kv_b), _ptr(out), _ptr(shard_lse), _ptr(ws),
+                         ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "mla_tpla_decode")
+    return out, shard_lse
+
+
+def rmsnorm(x, w, *, n_shards=1, eps=1e-6, out=None, stream=None):
+    """RMSNorm over the last dim of ``x``, cut into ``n_shards`` shards normalised on
+    their own.  Returns ``out``."""
+    d = x.shape[-1]
+    if out is None:
+        out = torch.empty_like(x)
+    st = mla_rmsnorm(_dt(x), x.numel() // d if d else 0, d, n_shards, float(eps), _ptr(x), _ptr(w), _ptr(out),
+                     _stream(stream))
+    _check(st, "mla_rmsnorm")
+    return out
 
 
 def lse_combine(part_out, part_lse, *, out_dtype=torch.float32, out=None, lse=None, stream=None):

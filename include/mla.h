@@ -12,7 +12,9 @@
  *    The absorbed form (q_absorbed = W_kv_b^T q_nope, latent-space attention,
  *    un-absorb) is the companion path of the same figure.
  *  - "TPLA: Tensor Parallel Latent Attention ..." (arXiv 2508.15881), "What
- *    carries the argument": the latent normalisation is an RMSNorm.
+ *    carries the argument": the latent normalisation is an RMSNorm; "The reading":
+ *    the latent cut into shards, each attended with all heads and its own softmax,
+ *    outputs summed (mla_tpla_decode, with the per-shard norm of mla_rmsnorm).
  *  - "Helix Parallelism ..." (arXiv 2507.07120), "What carries the argument" and
  *    "Assumptions" (paper section 2.1.1): split-KV partial outputs and their
  *    log-sum-exp scalars are rescaled and summed into the exact softmax output.
@@ -129,6 +131,39 @@ mla_status mla_decode_splitkv(const mla_dims *dims, mla_dtype dtype, int B, int 
                               void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
+ * TPLA decode (TPLA page, "The reading" and "What carries the argument"): the latent
+ * is cut into n_shards equal shards of d_kv/n_shards dims; every shard attends with all
+ * n_heads heads over its own dims plus the whole RoPE band, with its own softmax, and
+ * the shards' up-projected outputs are summed (what an all-reduce over tensor-parallel
+ * ranks would add).  Readings: no orthogonal reparameterisation of the latent, the
+ * score scale of mla_dims unchanged, the local softmaxes not rescaled.
+ *   c_cache [B, kv_len, d_kv]: each shard RMS-normalised on its own, as
+ *            mla_rmsnorm(..., n_shards, ...) writes it; kpe_cache already rotated.
+ *   q_nope, q_pe, kpe_cache, w_kv_b, out: as mla_decode_splitkv.
+ *   shard_lse (fp32) [n_shards, B, H]: each shard's log-sum-exp over its scores.
+ * n_shards = 1 computes exactly mla_decode_splitkv (shard_lse = its lse).
+ * 1 <= n_shards <= 16 and n_shards divides d_kv; other sizes as mla_decode_splitkv.
+ * Split partials always stay in the workspace (mla_tpla_decode_workspace).
+ * The tensor-core path needs bf16, the DeepSeek dimensions and n_heads * n_shards a
+ * multiple of 128; anything else runs on the SIMT kernels.
+ */
+mla_status mla_tpla_decode(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits,
+                           int n_shards, const void *q_nope, const void *q_pe, const void *c_cache,
+                           const void *kpe_cache, const void *w_kv_b, void *out, float *shard_lse,
+                           void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * RMSNorm of `rows` rows of x [rows, d] into y, each row cut into n_shards shards of
+ * d/n_shards columns normalised on their own (LAGA page, step 1 of the forward for
+ * n_shards = 1; TPLA page, "The reading", for the per-shard latent norm):
+ *   y[r][i*ds + t] = x[r][i*ds + t] / sqrt(mean_t' x[r][i*ds + t']^2 + eps) * w[i*ds + t]
+ * w [d] in the same dtype; fp32 arithmetic.  1 <= n_shards, n_shards divides d, eps >= 0.
+ * This is the cache write of a TPLA decode (the latent of every new token).
+ */
+mla_status mla_rmsnorm(mla_dtype dtype, long rows, int d, int n_shards, float eps, const void *x,
+                       const void *w, void *y, void *cuda_stream);
+
+/*
  * Log-sum-exp merge (Helix / Flash-Decoding combine):
  *   lse[r] = log sum_s exp(part_lse[s][r]);  out[r][:] = sum_s exp(part_lse[s][r]-lse[r]) part_out[s][r][:]
  * part_out fp32 [n_splits, rows, D], part_lse fp32 [n_splits, rows] -> out (out_dtype)
@@ -145,6 +180,8 @@ size_t mla_latent_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, i
 size_t mla_absorbed_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
                                    int q_offset, int causal, int head_count, int head_shard);
 size_t mla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits);
+size_t mla_tpla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv_len,
+                                 int n_splits, int n_shards);
 
 /* Static description of a status code. */
 const char *mla_status_string(mla_status status);
@@ -207,7 +244,7 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   the number of launches and their summed device time in milliseconds (0 launches
  *   for an unknown name).  Names: "prep", "latent_prep", "rope_table", "rope_rows",
  *   "convert", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
- *   "tc_latent_attn", "tc_decode_attn", "transpose".
+ *   "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "tpla_expand", "tpla_combine".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
  * Not thread-safe: profile from one host thread at a time.
  */

@@ -149,8 +149,10 @@ def tpla_decode(q_nope, q_pe, c_raw, kpe_cache, w_kv_b, rms_w, *, shards=2, eps=
     """TPLA latent decode over ``shards`` latent shards (see ``orc_tpla_decode``).
 
     ``c_raw`` [B,L,Dk] is the latent before normalisation (each shard is RMSNormed on its
-    own).  Returns (out [B,H,Dv] summed over shards, shard_lse [shards,B,H])."""
-    q_nope, q_pe, c_raw, kpe_cache, w_kv_b, rms_w = map(_f64, (q_nope, q_pe, c_raw, kpe_cache, w_kv_b, rms_w))
+    own); with ``rms_w=None`` it is taken as already normalised shard by shard.
+    Returns (out [B,H,Dv] summed over shards, shard_lse [shards,B,H])."""
+    q_nope, q_pe, c_raw, kpe_cache, w_kv_b = map(_f64, (q_nope, q_pe, c_raw, kpe_cache, w_kv_b))
+    rms_w = None if rms_w is None else _f64(rms_w)
     B, H, dn = q_nope.shape
     dr = q_pe.shape[-1]
     L, dk = c_raw.shape[1], c_raw.shape[2]
@@ -162,7 +164,8 @@ def tpla_decode(q_nope, q_pe, c_raw, kpe_cache, w_kv_b, rms_w, *, shards=2, eps=
     out = np.zeros((B, H, dv))
     slse = np.zeros((shards, B, H))
     _load().orc_tpla_decode(B, L, shards, H, dk, dn, dr, dv, float(base), float(scale), float(eps),
-                            _p(q_nope), _p(q_pe), _p(c_raw), _p(kpe_cache), _p(w_kv_b), _p(rms_w),
+                            _p(q_nope), _p(q_pe), _p(c_raw), _p(kpe_cache), _p(w_kv_b),
+                            None if rms_w is None else _p(rms_w),
                             _p(out), _p(slse))
     return out, slse
 

@@ -413,8 +413,9 @@ void orc_mla_decode(int B, int kv_len, int n_splits, int n_heads,
  *    rescaled (the referee report's second major comment: the deployed form uses an
  *    unscaled local softmax).
  * Inputs as orc_mla_decode, except that c_raw [B,kv_len,Dk] is the latent before any
- * normalisation (rms_w [Dk], eps).  Outputs: out [B,H,Dv], the sum over shards, and
- * shard_lse [g,B,H], each shard's log-sum-exp.
+ * normalisation (rms_w [Dk], eps); with rms_w NULL it is taken as already normalised
+ * shard by shard (what a deployed cache holds).  Outputs: out [B,H,Dv], the sum over
+ * shards, and shard_lse [g,B,H], each shard's log-sum-exp.
  */
 void orc_tpla_decode(int B, int kv_len, int g, int n_heads, int Dk, int Dn, int Dr, int Dv,
                      double base, double scale, double eps,
@@ -427,9 +428,13 @@ void orc_tpla_decode(int B, int kv_len, int g, int n_heads, int Dk, int Dn, int 
     /* the per-shard normalised latent of every cached key */
     double *chat = (double *)malloc(sizeof(double) * (size_t)B * nk * Dk);
     for (long r = 0; r < (long)B * kv_len; ++r)
-        for (int i = 0; i < g; ++i)
-            rmsnorm_row(c_raw + r * Dk + (size_t)i * ds, rms_w + (size_t)i * ds, ds, eps,
-                        chat + r * Dk + (size_t)i * ds);
+        for (int i = 0; i < g; ++i) {
+            if (rms_w)
+                rmsnorm_row(c_raw + r * Dk + (size_t)i * ds, rms_w + (size_t)i * ds, ds, eps,
+                            chat + r * Dk + (size_t)i * ds);
+            else
+                memcpy(chat + r * Dk + (size_t)i * ds, c_raw + r * Dk + (size_t)i * ds, sizeof(double) * ds);
+        }
 
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int b = 0; b < B; ++b)

@@ -149,6 +149,61 @@ def test_decode_rejects(L, over, status):
     assert mla.mla_decode_splitkv(*args) == status
 
 
+def tpla_args(**over):
+    d = mla.dims(**V3)
+    a = dict(dims=ctypes.byref(d), dtype=mla.MLA_BF16, B=64, kv_len=32768, n_splits=8, n_shards=2,
+             q_nope=fake(1), q_pe=fake(2), c_cache=fake(3), kpe_cache=fake(4), w_kv_b=fake(5), out=fake(6),
+             slse=fake(7), workspace=fake(8), workspace_bytes=1 << 32, stream=None)
+    a.update(over)
+    a["_d"] = d
+    keys = ["dims", "dtype", "B", "kv_len", "n_splits", "n_shards", "q_nope", "q_pe", "c_cache", "kpe_cache",
+            "w_kv_b", "out", "slse", "workspace", "workspace_bytes", "stream"]
+    return [a[k] for k in keys], a
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(c_cache=None), -1),
+    (dict(slse=None), -1),
+    (dict(n_shards=0), -2),
+    (dict(n_shards=3), -2),                   # 512 latent dims do not split into 3
+    (dict(n_shards=32), -2),
+    (dict(n_splits=0), -2),
+    (dict(dtype=5), -3),
+    (dict(slse=fake(7) + 4), -4),
+    (dict(workspace_bytes=4096), -5),
+    (dict(slse=fake(3) + 1024), -9),          # shard lse inside the cache
+    (dict(B=0), 0),
+])
+def test_tpla_decode_rejects(L, over, status):
+    args, keep = tpla_args(**over)
+    assert mla.mla_tpla_decode(*args) == status
+
+
+def test_tpla_workspace_grows_with_shards(L):
+    d = mla.dims(**V3)
+    w1 = mla.mla_tpla_decode_workspace(ctypes.byref(d), mla.MLA_BF16, 64, 32768, 8, 1)
+    w2 = mla.mla_tpla_decode_workspace(ctypes.byref(d), mla.MLA_BF16, 64, 32768, 8, 2)
+    assert w1 == mla.mla_decode_workspace(ctypes.byref(d), mla.MLA_BF16, 64, 32768, 8)
+    # the partials double and the expanded query rows are added
+    assert w2 - w1 >= 8 * 64 * 128 * 512 * 4
+    assert mla.mla_tpla_decode_workspace(ctypes.byref(d), mla.MLA_BF16, 64, 32768, 8, 3) == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((mla.MLA_BF16, 10, 512, 2, 1e-6, None, fake(2), fake(3)), -1),
+    ((mla.MLA_BF16, 10, 512, 3, 1e-6, fake(1), fake(2), fake(3)), -2),
+    ((mla.MLA_BF16, 10, 512, 0, 1e-6, fake(1), fake(2), fake(3)), -2),
+    ((mla.MLA_BF16, -1, 512, 1, 1e-6, fake(1), fake(2), fake(3)), -2),
+    ((mla.MLA_BF16, 10, 512, 1, -1.0, fake(1), fake(2), fake(3)), -2),
+    ((9, 10, 512, 1, 1e-6, fake(1), fake(2), fake(3)), -3),
+    ((mla.MLA_BF16, 10, 512, 1, 1e-6, fake(1), fake(2) + 2, fake(3)), -4),
+    ((mla.MLA_BF16, 10, 512, 1, 1e-6, fake(1), fake(2), fake(1) + 4096), -9),
+    ((mla.MLA_BF16, 0, 512, 1, 1e-6, fake(1), fake(2), fake(3)), 0),
+])
+def test_rmsnorm_rejects(L, args, status):
+    assert mla.mla_rmsnorm(*args, None) == status
+
+
 @pytest.mark.parametrize("args,status", [
     ((mla.MLA_F32, 0, 10, 8, fake(1), fake(2), fake(3), fake(4), None), -2),
     ((mla.MLA_F32, 4, 10, 8, None, fake(2), fake(3), fake(4), None), -1),

@@ -321,3 +321,112 @@ def test_decode_tensor_core_path_matches_simt_path():
     check_lse(l_tc, l_s)
     check_out(po_tc, po_s, torch.bfloat16, "partials tc vs simt")
     check_lse(pl_tc, pl_s)
+
+
+# --------------------------------------------------------------------- TPLA ----
+def tpla_cfg(dtype, L, n_splits, n_heads=None):
+    if dtype == "bf16":
+        return dataclasses.replace(configs.DECODE, batch=3, kv_len=L, n_splits=n_splits,
+                                   n_heads=n_heads or configs.DECODE.n_heads)
+    return configs.Decode("dec_f32", "f32", batch=2, kv_len=L, n_splits=n_splits, n_heads=n_heads or 4, d_kv=64,
+                          d_nope=32, d_rope=16, d_v=32)
+
+
+def run_tpla(cfg, d_inp, g, cache=None):
+    d = mla.dims(cfg.n_heads, cfg.d_kv, cfg.d_nope, cfg.d_rope, cfg.d_v, cfg.rope_base)
+    cache = d_inp["c_cache"] if cache is None else cache
+    o, sl = mla.tpla_decode(d, d_inp["q_nope"], d_inp["q_pe"], cache, d_inp["kpe_cache"], d_inp["w_kv_b"],
+                            n_shards=g, n_splits=cfg.n_splits)
+    torch.cuda.synchronize()
+    return o, sl
+
+
+@pytest.mark.parametrize("dtype,L,n_splits,g,heads", [
+    ("bf16", 1000, 1, 2, None), ("bf16", 1000, 8, 2, None), ("bf16", 1000, 13, 4, None),
+    ("bf16", 5, 8, 2, None), ("bf16", 1, 1, 2, None), ("bf16", 777, 4, 2, 64),
+    ("f32", 333, 13, 2, None), ("f32", 64, 3, 4, None), ("f32", 50, 2, 2, 3)])
+def test_tpla_decode(oracle, dtype, L, n_splits, g, heads):
+    """Decode over a cache normalised shard by shard (the call's contract): the same
+    seeded cache values go to both sides."""
+    cfg = tpla_cfg(dtype, L, n_splits, heads)
+    inp = inputs.decode_inputs(cfg)
+    o, sl = run_tpla(cfg, dev(inp), g)
+    if dtype == "bf16":
+        assert mla.last_path() == mla.PATH_TC
+    n = np_inputs(inp)
+    ro, rsl = oracle.tpla_decode(n["q_nope"], n["q_pe"], n["c_cache"], n["kpe_cache"], n["w_kv_b"], None,
+                                 shards=g, base=cfg.rope_base)
+    check_out(o, ro, cfg.torch_dtype, "tpla out")
+    check_lse(sl, rsl, "tpla shard lse")
+
+
+def test_tpla_one_shard_is_plain_decode():
+    cfg = tpla_cfg("bf16", 1000, 8)
+    inp = dev(inputs.decode_inputs(cfg))
+    o1, sl = run_tpla(cfg, inp, 1)
+    o, l, _, _ = run_decode(cfg, inp, cfg.n_splits, partials=False)
+    assert torch.equal(o1, o) and torch.equal(sl[0], l)
+
+
+def test_tpla_tensor_core_path_matches_simt_path():
+    cfg = tpla_cfg("bf16", 2500, 3)
+    inp = dev(inputs.decode_inputs(cfg))
+    o_tc, l_tc = run_tpla(cfg, inp, 2)
+    assert mla.last_path() == mla.PATH_TC
+    mla.set_path_override(1)
+    try:
+        o_s, l_s = run_tpla(cfg, inp, 2)
+        assert mla.last_path() == mla.PATH_SIMT
+    finally:
+        mla.set_path_override(0)
+    check_out(o_tc, o_s.float(), torch.bfloat16, "tpla tc vs simt")
+    check_lse(l_tc, l_s)
+
+
+@pytest.mark.parametrize("dtype,rows,d,g", [("bf16", 1000, 512, 1), ("bf16", 1000, 512, 2), ("bf16", 333, 512, 4),
+                                            ("f32", 257, 64, 4), ("f32", 100, 30, 3), ("bf16", 50, 36, 3)])
+def test_rmsnorm_shards(oracle, dtype, rows, d, g):
+    """The per-shard latent norm (the TPLA cache write) against the oracle's RMSNorm of
+    each shard slice; vector and scalar layouts both covered."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = inputs.to_torch(inputs.normal_rows(3, inputs.DEC_C_CACHE, rows, d, 2.0), tdt, (rows, d))
+    w = inputs.norm_weight(d, tdt, seed=3)
+    y = mla.rmsnorm(x.cuda(), w.cuda(), n_shards=g, eps=1e-6)
+    torch.cuda.synchronize()
+    xs, ws, ds = to64(x), to64(w), d // g
+    ref = np.concatenate([oracle.rmsnorm(np.ascontiguousarray(xs[:, i * ds:(i + 1) * ds]), ws[i * ds:(i + 1) * ds],
+                                         1e-6) for i in range(g)], 1)
+    check_out(y, ref, tdt, "rmsnorm shards")
+
+
+def test_tpla_cache_write_then_decode(oracle):
+    """The whole TPLA chain on the GPU -- per-shard RMSNorm of the raw latent, then the
+    decode -- against the oracle from the raw latent.  The normalised cache is rounded
+    to bf16 before the decode reads it; over 2000 keys that rounding averages out in the
+    log-sum-exp, so the usual bars apply."""
+    cfg = tpla_cfg("bf16", 2000, 4)
+    inp = inputs.decode_inputs(cfg)
+    w = inputs.norm_weight(cfg.d_kv, cfg.torch_dtype)
+    d_inp = dev(inp)
+    cache = mla.rmsnorm(d_inp["c_cache"], w.cuda(), n_shards=2)
+    o, sl = run_tpla(cfg, d_inp, 2, cache=cache)
+    n = np_inputs(inp)
+    ro, rsl = oracle.tpla_decode(n["q_nope"], n["q_pe"], n["c_cache"], n["kpe_cache"], n["w_kv_b"], to64(w),
+                                 shards=2, base=cfg.rope_base)
+    check_out(o, ro, torch.bfloat16, "tpla chain out")
+    check_lse(sl, rsl, "tpla chain lse")
+
+
+def test_tpla_full_size_sampled(oracle):
+    """The bench's TPLA workload (64 sequences x 32768 keys, 128 heads, 8 splits, two
+    shards) in the bench's launch configuration; sequences 0 and 63 against the oracle."""
+    cfg = configs.DECODE
+    inp = inputs.decode_inputs(cfg)
+    o, sl = run_tpla(cfg, dev(inp), 2)
+    assert mla.last_path() == mla.PATH_TC
+    for b in (0, 63):
+        n = np_inputs(inputs.decode_inputs(cfg, batches=(b, b + 1)))
+        ro, rsl = oracle.tpla_decode(n["q_nope"], n["q_pe"], n["c_cache"], n["kpe_cache"], n["w_kv_b"], None,
+                                     shards=2, base=cfg.rope_base)
+        check_out(o[b:b + 1], ro, torch.bfloat16, "tpla out b=%d" % b)
+        check_lse(sl[:, b:b + 1], rsl, "tpla lse b=%d" % b)

@@ -331,6 +331,20 @@ def test_tpla_shards_sum_of_slice_decodes(oracle, shards):
     assert np.abs(out - full).max() > 1e-3          # sharding really changes the result
 
 
+def test_tpla_normalised_cache_mode(oracle):
+    """rms_w=None reads the cache as already normalised: it equals normalising first."""
+    B, H, L, dk, dn, dr, dv, G = 2, 3, 29, 32, 16, 8, 16, 4
+    inp = _tpla_inputs(B, H, L, dk, dn, dr, dv, 91)
+    out, slse = oracle.tpla_decode(**inp, shards=G, eps=EPS)
+    ds = dk // G
+    c = inp["c_raw"].reshape(-1, G, ds)
+    chat = np.stack([oracle.rmsnorm(np.ascontiguousarray(c[:, i]), inp["rms_w"][i * ds:(i + 1) * ds], EPS)
+                     for i in range(G)], 1).reshape(B, L, dk)
+    o2, l2 = oracle.tpla_decode(**dict(inp, c_raw=chat, rms_w=None), shards=G)
+    np.testing.assert_allclose(o2, out, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l2, slse, rtol=0, atol=1e-13)
+
+
 def test_tpla_matches_library_composition(oracle):
     B, H, L, dk, dn, dr, dv, G = 2, 4, 37, 32, 16, 8, 16, 2
     inp = _tpla_inputs(B, H, L, dk, dn, dr, dv, 81)
