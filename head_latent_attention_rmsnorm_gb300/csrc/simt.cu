@@ -713,6 +713,7 @@ __device__ __forceinline__ long ty_size_dev(int ty) { return ty == TY_F32 ? 4 : 
 // A 16-byte piece as 4 fp32 or 8 fp16/bf16 values, and back.
 __device__ __forceinline__ void unpack16(uint4 v, int ty, float *f) {
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
     for (int t = 0; t < 4; ++t) {
         if (ty == TY_F32) {
             f[t] = __uint_as_float(u[t]);
@@ -729,6 +730,7 @@ __device__ __forceinline__ void unpack16(uint4 v, int ty, float *f) {
 
 __device__ __forceinline__ uint4 pack16(const float *f, int ty) {
     uint32_t u[4];
+#pragma unroll
     for (int t = 0; t < 4; ++t) {
         if (ty == TY_F32) {
             u[t] = __float_as_uint(f[t]);
@@ -787,6 +789,61 @@ __global__ void rmsnorm_shards_kernel(int ty, long rows, int D, int g, float eps
     for (int k = lane; k < ds; k += 32) stx(y, ty, o + k, ldx(x, ty, o + k) * inv * ldx(w, ty, k0 + k));
 }
 
+// The same norm with whole rows in registers: each warp takes two rows, lane l holds
+// their 16-byte pieces l, l + 32, ... (NP per row, all loaded before any arithmetic),
+// and every shard covers a whole number of 512-byte rounds, so piece p of every lane
+// lies in shard p / (NP / g) and each shard's sum is one warp reduction.
+template <int NP>
+__global__ void __launch_bounds__(256) rmsnorm_rows_kernel(int ty, long rows, int D, int g, float eps,
+                                                           const uint4 *x, const uint4 *w, uint4 *y) {
+    constexpr int RW = 2;
+    const long r0 = ((long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * RW;
+    const int lane = threadIdx.x % 32;
+    if (r0 >= rows) return;
+    const int per = ty == TY_F32 ? 4 : 8, sp = NP / g, ds = D / g;
+    uint4 v[RW][NP];
+#pragma unroll
+    for (int q = 0; q < RW; ++q)
+#pragma unroll
+        for (int p = 0; p < NP; ++p)
+            v[q][p] = r0 + q < rows ? x[(r0 + q) * (NP * 32) + p * 32 + lane] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int q = 0; q < RW; ++q) {
+        float ps[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            float f[8];
+            unpack16(v[q][p], ty, f);
+            float a = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (t < per) a = fmaf(f[t], f[t], a);
+            ps[p] = a;
+        }
+        float inv[NP];
+        for (int i = 0; i < g; ++i) {
+            float a = 0.f;
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+                if (p / sp == i) a += ps[p];
+            a = 1.0f / sqrtf(warp_sum(a) / (float)ds + eps);
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+                if (p / sp == i) inv[p] = a;
+        }
+        if (r0 + q >= rows) break;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            float f[8], fw[8];
+            unpack16(v[q][p], ty, f);
+            unpack16(w[p * 32 + lane], ty, fw);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) f[t] = f[t] * inv[p] * fw[t];
+            y[(r0 + q) * (NP * 32) + p * 32 + lane] = pack16(f, ty);
+        }
+    }
+}
+
 // TPLA decode, query side: every head becomes g query rows, one per latent shard.  Row
 // (b, i, h) keeps q_abs[b][h] on shard i's dims and zero elsewhere, so its score over
 // the full latent row is the shard-local score q_abs_i . c_i; the rotated q_pe is
@@ -827,8 +884,8 @@ __global__ void tpla_expand_kernel(int ty, int B, int H, int g, int Dk, int Dr, 
 // own dims, so the later W_V product sums the shards' up-projections), and each row's
 // log-sum-exp goes to shard_lse[i][b][h].
 // po [n][B][g][H][Dk], pl [n][B][g][H] (fp32) -> out [B][H][Dk] (storage `to`).
-__global__ void tpla_combine_kernel(int n, int B, int H, int g, int Dk, const float *po, const float *pl, void *out,
-                                    int to, float *slse) {
+__global__ void tpla_combine_kernel(int n, int B, int H, int g, int Dk, bool vec, const float *po, const float *pl,
+                                    void *out, int to, float *slse) {
     const long rows = (long)B * g * H;
     const long r = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -844,6 +901,29 @@ __global__ void tpla_combine_kernel(int n, int B, int H, int g, int Dk, const fl
         float z = 0.f;
         for (int s = lane; s < n; s += 32) z += expf(pl[(long)s * rows + r] - m);
         L = m + logf(warp_sum(z));
+    }
+    if (vec) {
+        // lane s holds split s's weight; 16-byte loads of the shard's partial columns
+        const float wl = lane < n && m != -INFINITY ? expf(pl[(long)lane * rows + r] - L) : 0.f;
+        for (int c = lane; c < ds / 4; c += 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < n; ++s) {
+                const float wt = __shfl_sync(0xffffffffu, wl, s);
+                if (wt > 0.f) {
+                    const float4 v = *(const float4 *)(po + ((long)s * rows + r) * Dk + k0 + 4 * c);
+                    acc.x = fmaf(wt, v.x, acc.x);
+                    acc.y = fmaf(wt, v.y, acc.y);
+                    acc.z = fmaf(wt, v.z, acc.z);
+                    acc.w = fmaf(wt, v.w, acc.w);
+                }
+            }
+            stx(out, to, orow + 4 * c, acc.x);
+            stx(out, to, orow + 4 * c + 1, acc.y);
+            stx(out, to, orow + 4 * c + 2, acc.z);
+            stx(out, to, orow + 4 * c + 3, acc.w);
+        }
+        if (lane == 0) slse[(i * B + b) * H + h] = L;
+        return;
     }
     for (int d = lane; d < ds; d += 32) {
         float acc = 0.f;
@@ -863,6 +943,17 @@ cudaError_t launch_rmsnorm_shards(int ty, long rows, int D, int g, float eps, co
     ProfScope ps("rmsnorm", st);
     const bool vec = ((long)(D / g) * (long)ty_size(ty)) % 16 == 0 && ((uintptr_t)x & 15) == 0 &&
                      ((uintptr_t)y & 15) == 0 && ((uintptr_t)w & 15) == 0;
+    const long row_bytes = (long)D * (long)ty_size(ty), np = row_bytes / 512;
+    if (vec && ((long)(D / g) * (long)ty_size(ty)) % 512 == 0 && (np == 1 || np == 2 || np == 4 || np == 8)) {
+        const unsigned blocks = blocks_for((rows + 1) / 2, 8);
+        const uint4 *xv = (const uint4 *)x, *wv = (const uint4 *)w;
+        uint4 *yv = (uint4 *)y;
+        if (np == 1) rmsnorm_rows_kernel<1><<<blocks, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, yv);
+        if (np == 2) rmsnorm_rows_kernel<2><<<blocks, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, yv);
+        if (np == 4) rmsnorm_rows_kernel<4><<<blocks, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, yv);
+        if (np == 8) rmsnorm_rows_kernel<8><<<blocks, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, yv);
+        return cudaGetLastError();
+    }
     rmsnorm_shards_kernel<<<blocks_for(rows * g, 8), 256, 0, st>>>(ty, rows, D, g, eps, vec, x, w, y);
     return cudaGetLastError();
 }
@@ -885,7 +976,8 @@ cudaError_t launch_tpla_combine(int tout, int n, int B, int H, int g, int Dk, co
     const long rows = (long)B * g * H;
     if (rows == 0) return cudaSuccess;
     ProfScope ps("tpla_combine", st);
-    tpla_combine_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(n, B, H, g, Dk, po, pl, out, tout, slse);
+    const bool vec = n <= 32 && (Dk / g) % 128 == 0 && ((uintptr_t)po & 15) == 0;
+    tpla_combine_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(n, B, H, g, Dk, vec, po, pl, out, tout, slse);
     return cudaGetLastError();
 }
 

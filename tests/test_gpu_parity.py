@@ -383,7 +383,8 @@ def test_tpla_tensor_core_path_matches_simt_path():
     check_lse(l_tc, l_s)
 
 
-@pytest.mark.parametrize("dtype,rows,d,g", [("bf16", 1000, 512, 1), ("bf16", 1000, 512, 2), ("bf16", 333, 512, 4),
+@pytest.mark.parametrize("dtype,rows,d,g", [("bf16", 1000, 512, 1), ("bf16", 1000, 512, 2), ("bf16", 333, 512, 2),
+                                            ("bf16", 77, 2048, 4), ("f32", 101, 256, 2), ("bf16", 333, 512, 4),
                                             ("f32", 257, 64, 4), ("f32", 100, 30, 3), ("bf16", 50, 36, 3)])
 def test_rmsnorm_shards(oracle, dtype, rows, d, g):
     """The per-shard latent norm (the TPLA cache write) against the oracle's RMSNorm of
