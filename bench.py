@@ -40,7 +40,7 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max
 # summarised under profiles/ (None until the current kernel has been captured).  The
 # decode capture runs B = 8; its traffic grows in proportion to the batch, so the
 # B = 64 launch is 8x that.
-NCU_TRAFFIC = {"tc_attn": 62.01e6, "tc_decode_attn": 314.83e6 * 8}
+NCU_TRAFFIC = {"tc_attn": 62.01e6, "tc_decode_attn": 310.95e6 * 8}
 
 
 def load_peaks():

@@ -45,6 +45,11 @@
 // P multiplies the cache on rank 1 in bf16: its rounding only perturbs the weights of an
 // average (relative 2^-9), and the row sums use the unrounded fp32 probabilities.
 //
+// TPLA (two latent shards, each with its own softmax): a unit whose heads all belong to
+// shard i loads only that shard's four latent boxes and the RoPE box per key tile (in
+// two groups of three and two boxes), issues the shard's 16 latent score MMAs and the 8
+// RoPE ones, runs P.C at N = 256 over the shard's dims, and writes those dims only.
+//
 // Warps (384 threads per CTA): rank 0 -- 0 TMA producer, 1 and 11 MMA issuers (1 also
 // owns TMEM), 2-9 softmax (two threads per head), 10 copier; rank 1 -- 0 TMA producer,
 // 1 MMA issuer and TMEM owner, 2-5 rescale, 2-9 epilogue, 10 L2 prefetch, 11 idle.
@@ -121,6 +126,10 @@ struct DecK {
     float *po, *pl;                     // partials [split][b][h][512], [split][b][h]
     long po_s, po_b, pl_s, pl_b;
     uint32_t idesc_s, idesc_pv;
+    // TPLA with two latent shards: rows [b][i][h] of g = 2 shards x shard_rows heads
+    // (shard_rows a multiple of 128, so a unit's heads all belong to shard r0 /
+    // shard_rows); 0 = plain decode over all 512 dims
+    int shard_rows;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -131,6 +140,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 struct Unit {
     int b, split, r0;   // sequence, key split, first head
+    int shard;          // TPLA latent shard of the unit's rows (dims 256 shard ..), -1 = all dims
     long kb, ke;        // key range [kb, ke)
     int nt;             // key tiles
 };
@@ -144,6 +154,7 @@ __device__ __forceinline__ Unit unit_of(const DecK &p, int u) {
     w.kb = min((long)w.split * p.chunk, p.kv_len);
     w.ke = min(w.kb + p.chunk, p.kv_len);
     w.nt = w.ke > w.kb ? (int)((w.ke - w.kb + NK - 1) / NK) : 0;
+    w.shard = p.shard_rows ? w.r0 / p.shard_rows : -1;
     return w;
 }
 
@@ -155,6 +166,9 @@ __device__ void settle() {
     }
 }
 
+// SHD: the TPLA two-shard units (a template parameter so that the plain decode's issue
+// loops carry no shard branches).
+template <bool SHD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mR,
                      const __grid_constant__ CUtensorMap mP, const __grid_constant__ CUtensorMap mQa,
@@ -185,6 +199,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const Unit w = unit_of(p, blockIdx.x >> 1);
     const int nt = w.nt;
+    constexpr bool shd = SHD;
+    const int box0 = shd ? 4 * w.shard : 0;   // first latent box of the unit's dims
+    constexpr int ngrp = shd ? 2 : KGRP;      // box groups per key stage
 
     if (tid == 0) {
         if (rank == 0) {
@@ -255,14 +272,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const uint32_t ph = ((t >> 1) - 1) & 1;   // phase of tile t - 2 in this stage
                     uint8_t *dst = smem + s * KSTAGE;
                     const int key0 = (int)(w.kb + (long)t * NK);
-                    for (int g = 0; g < KGRP && go; ++g) {   // a group refills once tile t - 2 has read it
+                    for (int g = 0; g < ngrp && go; ++g) {   // a group refills once tile t - 2 has read it
                         uint64_t *full = &grp_full[s * KGRP + g];
                         if (t >= KST && !mbar_wait(&grp_empty[s * KGRP + g], ph, abort, err)) go = false;
                         if (!go) break;
-                        mbar_arrive_expect_tx(full, 3 * KBOX);
-                        for (int i = 3 * g; i < 3 * g + 3; ++i) {
-                            if (i < 8) tma_load_3d(dst + i * KBOX, &mC, full, 64 * i, key0, w.b);
-                            else tma_load_3d(dst + 8 * KBOX, &mR, full, 0, key0, w.b);
+                        if (!shd) {
+                            mbar_arrive_expect_tx(full, 3 * KBOX);
+                            for (int i = 3 * g; i < 3 * g + 3; ++i) {
+                                if (i < 8) tma_load_3d(dst + i * KBOX, &mC, full, 64 * i, key0, w.b);
+                                else tma_load_3d(dst + 8 * KBOX, &mR, full, 0, key0, w.b);
+                            }
+                        } else {   // the shard's boxes 0-3 (group 0: three, group 1: one + RoPE)
+                            mbar_arrive_expect_tx(full, (g == 0 ? 3 : 2) * KBOX);
+                            for (int j = 3 * g; j < 3 * g + 3 && j < 5; ++j) {
+                                const int i = box0 + j;   // same slot as in the full layout
+                                if (j < 4) tma_load_3d(dst + i * KBOX, &mC, full, 64 * i, key0, w.b);
+                                else tma_load_3d(dst + 8 * KBOX, &mR, full, 0, key0, w.b);
+                            }
                         }
                     }
                     if (!go) break;
@@ -285,22 +311,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     bool go = true;
 #pragma unroll
                     for (int g = 0; g < KGRP; ++g) {
+                        if (g >= ngrp) break;
                         go = go && __all_sync(FULL, mbar_wait(&grp_full[s * KGRP + g], ph, abort, err));
                         if (!go) break;
                         tc_fence_after();
                         if (elect_one()) {
+                            if (!shd) {
 #pragma unroll
-                            for (int kk = 12 * g; kk < 12 * g + 12 && kk < 32; ++kk)   // latent band, q_hi only
-                                mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (KBOX >> 4) + 2 * (kk & 3)),
-                                       p.idesc_s, kk != 0);
-                            if (g == KGRP - 1) {
+                                for (int kk = 12 * g; kk < 12 * g + 12 && kk < 32; ++kk)   // latent band, q_hi only
+                                    mma_ts(dt, at + kk * 8, d0 + (uint64_t)((kk >> 2) * (KBOX >> 4) + 2 * (kk & 3)),
+                                           p.idesc_s, kk != 0);
+                            } else {   // the shard's latent boxes of this group
+#pragma unroll
+                                for (int j = 3 * g; j < 3 * g + 3 && j < 4; ++j)
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q) {
+                                        const int kk = 4 * (box0 + j) + q;
+                                        mma_ts(dt, at + kk * 8, d0 + (uint64_t)((box0 + j) * (KBOX >> 4) + 2 * q),
+                                               p.idesc_s, (j | q) != 0);
+                                    }
+                            }
+                            if (g == ngrp - 1) {
 #pragma unroll
                                 for (int kk = 0; kk < 8; ++kk)   // RoPE band: q_hi then q_lo against the same box
                                     mma_ts(dt, tmem + (kk < 4 ? T_QP : T_QL) + (kk & 3) * 8,
                                            d0 + (uint64_t)(8 * (KBOX >> 4) + 2 * (kk & 3)), p.idesc_s, 1);
                             }
                             mma_commit(&grp_empty[s * KGRP + g]);
-                            if (g == KGRP - 1) mma_commit(&s_full[s]);
+                            if (g == ngrp - 1) mma_commit(&s_full[s]);
                         }
                         __syncwarp();
                     }
@@ -476,9 +514,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     if (t >= VST && !mbar_wait(&v_empty[s], ((t / VST) - 1) & 1, abort, err)) break;
                     uint8_t *dst = smem + s * VSTAGE;
                     const int key0 = (int)(w.kb + (long)t * NK);
-                    mbar_arrive_expect_tx(&v_full[s], VSTAGE);
+                    constexpr int nbx = shd ? 4 : 8;   // the unit's latent boxes, into slots 0 ..
+                    mbar_arrive_expect_tx(&v_full[s], nbx * KBOX);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) tma_load_3d(dst + i * KBOX, &mC, &v_full[s], 64 * i, key0, w.b);
+                    for (int i = 0; i < nbx; ++i)
+                        tma_load_3d(dst + i * KBOX, &mC, &v_full[s], 64 * (box0 + i), key0, w.b);
                     *prog = t + 1;   // paces the prefetching warp
                     if (t == (nt > 3 ? nt - 3 : 0)) {   // the epilogue's q_abs rows (128 KB) into L2
                         const __half *q0 = p.qa + w.b * p.qa_b + (long)w.r0 * p.qa_r;
@@ -545,7 +585,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                             const uint64_t pa = kk < 4 ? pa0 + (uint64_t)(2 * kk) : pa1;
                             const uint32_t acc = (t | kk) != 0;
                             mma_ss(tmem, pa, vb + (uint64_t)(kk * (2048 >> 4)), p.idesc_pv, acc);
-                            mma_ss(tmem + 256, pa, vb + (uint64_t)((4 * KBOX + kk * 2048) >> 4), p.idesc_pv, acc);
+                            if (!shd)
+                                mma_ss(tmem + 256, pa, vb + (uint64_t)((4 * KBOX + kk * 2048) >> 4), p.idesc_pv, acc);
                         }
                         mma_commit(&v_empty[s]);
                         mma_commit_mc(&p_empty[pb], 3);   // slot pb consumed: tells rank 0 and this CTA
@@ -581,7 +622,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     tc_fence_after();
                     const float a = ((const float *)(xs + X_ALPHA))[row];
                     if (__any_sync(FULL, a != 1.f)) {
-                        for (int cc = 0; cc < 16; ++cc) {
+                        for (int cc = 0; cc < (shd ? 8 : 16); ++cc) {
                             uint32_t o[32];
                             tmem_ld32(lb + cc * 32, o);
                             tmem_ld_wait();
@@ -620,11 +661,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 const int prow = (int)(((long)w.split * p.po_s + w.b * p.po_b) / 512) + w.r0 + quad * 32;
                 if (lane == 0) tma_prefetch_desc(&mP);
                 // kept rolled: the body's code is fetched once (the cache stream leaves no code in L2)
+                // this warp's columns: TMEM column tc0 + 32 cc holds latent dim od0 + 32 cc
+                constexpr int ncc = shd ? 4 : 8;
+                const int tc0 = shd ? 128 * g : 256 * g, od0 = 256 * (shd ? w.shard : 0) + tc0;
 #pragma unroll 1
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = 0; cc < ncc; ++cc) {
                     uint32_t o[32];
                     if (nt > 0) {
-                        tmem_ld32(lb + 256 * g + cc * 32, o);
+                        tmem_ld32(lb + tc0 + cc * 32, o);
                         tmem_ld_wait();
                     } else {
 #pragma unroll
@@ -644,14 +688,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {   // columns in fp16 units of the map: 2 per fp32 value
-                        tma_store_2d(&mP, buf, (256 * g + 32 * cc) * 2, prow);
+                        tma_store_2d(&mP, buf, (od0 + 32 * cc) * 2, prow);
                         bulk_commit();
                     }
-                    // dims 256 g + 32 cc .. +31: half (cc & 1) of the row of box 4 g + cc / 2
-                    const uint8_t *qrow_s = smem + QB_OFF + (4 * g + cc / 2) * 16384 + row * 128;
+                    // dims od0 + 32 cc .. +31: half (od / 32) & 1 of the row of box od / 64
+                    const int od = od0 + 32 * cc;
+                    const uint8_t *qrow_s = smem + QB_OFF + (od >> 6) * 16384 + row * 128;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {   // q_lo = q - bf16(q), rounded as rank 0 rounded q_hi
-                        const uint4 x = *(const uint4 *)(qrow_s + ((((cc & 1) * 4 + v) ^ (row & 7)) << 4));
+                        const uint4 x = *(const uint4 *)(qrow_s + (((((od >> 5) & 1) * 4 + v) ^ (row & 7)) << 4));
                         const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -687,9 +732,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 // qa: q_abs [B][H][512] fp16; qp: rotated q_pe [B][H][64] fp16; cache [B][L][512],
 // kpe [B][L][64] bf16; po [n][B][H][512] fp32, pl [n][B][H].
 cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache, const void *kpe, int B, long L,
-                               int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st) {
+                               int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st,
+                               int shard_rows) {
     const long units = (long)B * n_splits * (H / ROWS);
     if (units == 0) return cudaSuccess;
+    if (shard_rows && (shard_rows % ROWS != 0 || H != 2 * shard_rows)) return cudaErrorInvalidValue;
     CUtensorMap mC, mR, mP, mQa, mQp;
     cudaError_t e;
     {   // q_abs [B * H][512] and the rotated q_pe [B * H][64], fp16, boxes of 128 rows
@@ -739,10 +786,12 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
     p.pl_b = H;
     p.idesc_s = idesc_f16(128, NK, false);
     p.idesc_pv = idesc_f16(128, 256, false, true);
+    p.shard_rows = shard_rows;
     ProfScope ps("tc_decode_attn", st);
-    e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    auto kern = shard_rows ? tc_decode_kernel<true> : tc_decode_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e == cudaSuccess)
-        tc_decode_kernel<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, mP, mQa, mQp, p);
+        kern<<<dim3((unsigned)(2 * units)), dim3(NTHREADS), SMEM_BYTES, st>>>(mC, mR, mP, mQa, mQp, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

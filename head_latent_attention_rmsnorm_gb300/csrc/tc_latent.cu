@@ -519,8 +519,11 @@ cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, c
         // TPLA: g query rows per head, row (b, i, h) zero outside latent shard i
         if ((e = launch_tpla_expand(TY_F16, p.B, p.H, p.g, p.Dk, p.Dr, qabs, qpe, qx, qpx, st)) != cudaSuccess)
             return e;
-        // 2. the same decode kernel over g*H query rows
-        e = launch_decode_attn(qx, qpx, c_cache, kpe_cache, p.B, p.L, p.H * p.g, p.n, p.chunk, p.scale, po, pl, st);
+        // 2. the decode kernel over g*H query rows; at g = 2 with whole 128-head blocks per
+        //    shard each unit reads and multiplies only its shard's latent dims
+        const int shard_rows = p.g == 2 && p.H % 128 == 0 ? p.H : 0;
+        e = launch_decode_attn(qx, qpx, c_cache, kpe_cache, p.B, p.L, p.H * p.g, p.n, p.chunk, p.scale, po, pl, st,
+                               shard_rows);
         if (e != cudaSuccess) return e;
         // 3. each shard's merge over its own dims -> o_lat (bf16), shard lse [g][B][H]
         e = launch_tpla_combine(TY_BF16, p.n, p.B, p.H, p.g, p.Dk, po, pl, olat, lse, st);
