@@ -10,8 +10,8 @@ for the page citations and the readings taken where the pages are silent).  This
 module compiles it with gcc and exposes numpy-in / numpy-out wrappers.
 
 Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``):
-  rmsnorm, rope, mla_explicit, mla_absorbed, mla_decode, lse_combine, tpla_decode --
-  all pinned.
+  rmsnorm, rope, mla_explicit, mla_absorbed, mla_decode, lse_combine, tpla_decode,
+  mla_explicit_bwd -- all pinned.
 """
 from __future__ import annotations
 
@@ -56,8 +56,9 @@ def _load():
         lib.orc_mla_decode.argtypes = [i, i, i, i, i, i, i, i, d, d] + [_dp] * 9
         lib.orc_lse_combine.argtypes = [i, l, i, _dp, _dp, _dp, _dp]
         lib.orc_tpla_decode.argtypes = [i, i, i, i, i, i, i, i, d, d, d] + [_dp] * 8
+        lib.orc_mla_explicit_bwd.argtypes = [i, i, i, i, i, i, i, i, i, i, i, i, d, d, d] + [_dp] * 13
         for f in ("orc_rmsnorm", "orc_rope", "orc_mla_explicit", "orc_mla_absorbed",
-                  "orc_mla_decode", "orc_lse_combine", "orc_tpla_decode"):
+                  "orc_mla_decode", "orc_lse_combine", "orc_tpla_decode", "orc_mla_explicit_bwd"):
             getattr(lib, f).restype = None
         _lib = lib
     return _lib
@@ -117,6 +118,26 @@ def _fwd(fn, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, n_heads, q_offset=0, ca
 def mla_explicit(*args, **kw):
     """Explicit/LAGA MLA forward.  Returns (out [B,s_q,H_loc,Dv], lse [B,H_loc,s_q])."""
     return _fwd(_load().orc_mla_explicit, *args, **kw)
+
+
+def mla_explicit_bwd(q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, dout, *, n_heads, q_offset=0, causal=True,
+                     head_begin=0, base=10000.0, eps=1e-6, scale=None):
+    """Gradients of :func:`mla_explicit`'s output contracted with ``dout``.  Returns a
+    dict: q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w (each shaped like its input)."""
+    q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, dout = map(_f64, (q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, dout))
+    B, s_q, hc, dn = q_nope.shape
+    dr = q_pe.shape[-1]
+    s_kv, dk = c_kv.shape[1], c_kv.shape[2]
+    dv = w_kv_b.shape[0] // n_heads - dn
+    if scale is None:
+        scale = default_scale(dn, dr)
+    g = {k: np.zeros_like(v) for k, v in
+         dict(q_nope=q_nope, q_pe=q_pe, c_kv=c_kv, k_pe=k_pe, w_kv_b=w_kv_b, rms_w=rms_w).items()}
+    _load().orc_mla_explicit_bwd(B, s_q, s_kv, q_offset, int(bool(causal)), n_heads, head_begin, hc, dk, dn, dr,
+                                 dv, float(base), float(eps), float(scale), _p(q_nope), _p(q_pe), _p(c_kv),
+                                 _p(k_pe), _p(w_kv_b), _p(rms_w), _p(dout), _p(g["q_nope"]), _p(g["q_pe"]),
+                                 _p(g["c_kv"]), _p(g["k_pe"]), _p(g["w_kv_b"]), _p(g["rms_w"]))
+    return g
 
 
 def mla_absorbed(*args, **kw):

@@ -395,6 +395,166 @@ void orc_mla_decode(int B, int kv_len, int n_splits, int n_heads,
         }
 }
 
+/* ------------------------------------------------- explicit backward ---- */
+/*
+ * Gradients of the explicit forward (orc_mla_explicit) for a given upstream gradient
+ * dout [B,s_q,head_count,Dv] of the output; the log-sum-exp is not differentiated.
+ * LAGA, "What carries the argument": the sequence-parallel method is claimed to give the
+ * same gradients as the baseline (bit-identical at one rank, within 2e-5 / 1e-3 at more),
+ * so a backward pass is part of what the method computes; the pages print no backward
+ * formulas, so these are the chain rule through the forward's own steps, written in
+ * reverse order:
+ *   dP_ij = dO_i . V_j,  D_i = dO_i . o_i,  dS_ij = P_ij (dP_ij - D_i)      (softmax)
+ *   dq_nope_i = scale sum_j dS_ij K_nope_j,   dq_rot_i = scale sum_j dS_ij k_rot_j
+ *   dK_nope_j = scale sum_i dS_ij q_nope_i,   dk_rot_j = scale sum_i dS_ij q_rot_i
+ *   dV_j = sum_i P_ij dO_i
+ *   RoPE is a rotation, so its transpose rotates by the opposite angle:
+ *     dq_pe_i = rope(dq_rot_i, -pos_i),  dk_pe_j = rope(dk_rot_j, -j) (summed over heads)
+ *   dW_K(h) = sum_j dK_nope_j chat_j^T,  dW_V(h) = sum_j dV_j chat_j^T,
+ *   dchat_j = sum_h W_K(h)^T dK_nope_j + W_V(h)^T dV_j
+ *   RMSNorm y = x w / r, r = sqrt(mean x^2 + eps):
+ *     dx = (dy . w) / r - x (sum_k dy_k w_k x_k) / (d r^3),  dw = sum_rows dy . x / r
+ * Outputs: dq_nope [B,s_q,hc,Dn], dq_pe [B,s_q,hc,Dr], dc_kv [B,s_kv,Dk],
+ * dk_pe [B,s_kv,Dr], dw_kv_b [n_heads*(Dn+Dv),Dk] (rows of heads outside the range
+ * stay zero), drms_w [Dk].  Keys that no query sees get zero gradients.
+ */
+void orc_mla_explicit_bwd(int B, int s_q, int s_kv, int q_off, int causal,
+                          int n_heads, int head_begin, int head_count,
+                          int Dk, int Dn, int Dr, int Dv,
+                          double base, double eps, double scale,
+                          const double *q_nope, const double *q_pe, const double *c_kv,
+                          const double *k_pe, const double *w_kv_b, const double *rms_w,
+                          const double *dout,
+                          double *dq_nope, double *dq_pe, double *dc_kv, double *dk_pe,
+                          double *dw_kv_b, double *drms_w)
+{
+    long kv_need = causal ? (long)q_off + s_q : s_kv;
+    if (kv_need > s_kv)
+        kv_need = s_kv;
+    const int Dh = Dn + Dv;
+    const long nk = kv_need > 0 ? kv_need : 1;
+    memset(dc_kv, 0, sizeof(double) * (size_t)B * s_kv * Dk);
+    memset(dk_pe, 0, sizeof(double) * (size_t)B * s_kv * Dr);
+    memset(dw_kv_b, 0, sizeof(double) * (size_t)n_heads * Dh * Dk);
+    memset(drms_w, 0, sizeof(double) * Dk);
+
+    /* forward step 1 again: normalised latent and rotated k_pe */
+    double *chat = (double *)malloc(sizeof(double) * (size_t)B * nk * Dk);
+    double *krot = (double *)malloc(sizeof(double) * (size_t)B * nk * Dr);
+    double *dchat = (double *)calloc((size_t)B * nk * Dk, sizeof(double));
+    double *dkrot = (double *)calloc((size_t)B * nk * Dr, sizeof(double));
+    for (int b = 0; b < B; ++b)
+        for (long j = 0; j < kv_need; ++j) {
+            rmsnorm_row(c_kv + ((size_t)b * s_kv + j) * Dk, rms_w, Dk, eps, chat + ((size_t)b * nk + j) * Dk);
+            rope_row(k_pe + ((size_t)b * s_kv + j) * Dr, (double)j, Dr, base, krot + ((size_t)b * nk + j) * Dr);
+        }
+
+    double *kn = (double *)malloc(sizeof(double) * nk * Dn);
+    double *vv = (double *)malloc(sizeof(double) * nk * Dv);
+    double *dkn = (double *)malloc(sizeof(double) * nk * Dn);
+    double *dvv = (double *)malloc(sizeof(double) * nk * Dv);
+    double *sc = (double *)malloc(sizeof(double) * nk);
+    double *pw = (double *)malloc(sizeof(double) * nk);
+    double qr[1024], dqr[1024], o[1024];
+    for (int b = 0; b < B; ++b)
+        for (int hl = 0; hl < head_count; ++hl) {
+            const int h = head_begin + hl;
+            const double *wk = w_kv_b + (size_t)h * Dh * Dk, *wv = wk + (size_t)Dn * Dk;
+            double *dwk = dw_kv_b + (size_t)h * Dh * Dk, *dwv = dwk + (size_t)Dn * Dk;
+            for (long j = 0; j < kv_need; ++j) {   /* forward step 2 again */
+                const double *cj = chat + ((size_t)b * nk + j) * Dk;
+                for (int d = 0; d < Dn; ++d)
+                    kn[j * Dn + d] = dot(wk + (size_t)d * Dk, cj, Dk);
+                for (int d = 0; d < Dv; ++d)
+                    vv[j * Dv + d] = dot(wv + (size_t)d * Dk, cj, Dk);
+            }
+            memset(dkn, 0, sizeof(double) * nk * Dn);
+            memset(dvv, 0, sizeof(double) * nk * Dv);
+            for (int i = 0; i < s_q; ++i) {
+                const long pos = (long)q_off + i;
+                const size_t qrow = ((size_t)b * s_q + i) * head_count + hl;
+                const double *qn = q_nope + qrow * Dn, *dO = dout + qrow * Dv;
+                rope_row(q_pe + qrow * Dr, (double)pos, Dr, base, qr);
+                const long n = visible_keys(causal, pos, s_kv);
+                for (long j = 0; j < n; ++j)
+                    sc[j] = scale * (dot(qn, kn + j * Dn, Dn) + dot(qr, krot + ((size_t)b * nk + j) * Dr, Dr));
+                double z;
+                softmax_weights(sc, n, pw, &z);
+                for (int d = 0; d < Dv; ++d) {
+                    double acc = 0.0;
+                    for (long j = 0; j < n; ++j)
+                        acc += pw[j] * vv[j * Dv + d];
+                    o[d] = n > 0 ? acc / z : 0.0;
+                }
+                const double Di = dot(dO, o, Dv);
+                double *dqn = dq_nope + qrow * Dn;
+                for (int d = 0; d < Dn; ++d)
+                    dqn[d] = 0.0;
+                for (int d = 0; d < Dr; ++d)
+                    dqr[d] = 0.0;
+                for (long j = 0; j < n; ++j) {
+                    const double p = pw[j] / z;
+                    const double ds = p * (dot(dO, vv + j * Dv, Dv) - Di);
+                    const double *kr = krot + ((size_t)b * nk + j) * Dr;
+                    double *dkr = dkrot + ((size_t)b * nk + j) * Dr;
+                    for (int d = 0; d < Dn; ++d) {
+                        dqn[d] += scale * ds * kn[j * Dn + d];
+                        dkn[j * Dn + d] += scale * ds * qn[d];
+                    }
+                    for (int d = 0; d < Dr; ++d) {
+                        dqr[d] += scale * ds * kr[d];
+                        dkr[d] += scale * ds * qr[d];
+                    }
+                    for (int d = 0; d < Dv; ++d)
+                        dvv[j * Dv + d] += p * dO[d];
+                }
+                rope_row(dqr, -(double)pos, Dr, base, dq_pe + qrow * Dr);
+            }
+            /* through the reconstruction: weight gradients and the latent's gradient */
+            for (long j = 0; j < kv_need; ++j) {
+                const double *cj = chat + ((size_t)b * nk + j) * Dk;
+                double *dcj = dchat + ((size_t)b * nk + j) * Dk;
+                for (int d = 0; d < Dn; ++d)
+                    for (int k = 0; k < Dk; ++k) {
+                        dwk[(size_t)d * Dk + k] += dkn[j * Dn + d] * cj[k];
+                        dcj[k] += wk[(size_t)d * Dk + k] * dkn[j * Dn + d];
+                    }
+                for (int d = 0; d < Dv; ++d)
+                    for (int k = 0; k < Dk; ++k) {
+                        dwv[(size_t)d * Dk + k] += dvv[j * Dv + d] * cj[k];
+                        dcj[k] += wv[(size_t)d * Dk + k] * dvv[j * Dv + d];
+                    }
+            }
+        }
+    /* through RoPE of the keys and the RMSNorm of the latent */
+    for (int b = 0; b < B; ++b)
+        for (long j = 0; j < kv_need; ++j) {
+            rope_row(dkrot + ((size_t)b * nk + j) * Dr, -(double)j, Dr, base, dk_pe + ((size_t)b * s_kv + j) * Dr);
+            const double *x = c_kv + ((size_t)b * s_kv + j) * Dk, *dy = dchat + ((size_t)b * nk + j) * Dk;
+            double ss = 0.0, g = 0.0;
+            for (int k = 0; k < Dk; ++k) {
+                ss += x[k] * x[k];
+                g += dy[k] * rms_w[k] * x[k];
+            }
+            const double r = sqrt(ss / Dk + eps);
+            double *dx = dc_kv + ((size_t)b * s_kv + j) * Dk;
+            for (int k = 0; k < Dk; ++k) {
+                dx[k] = dy[k] * rms_w[k] / r - x[k] * g / ((double)Dk * r * r * r);
+                drms_w[k] += dy[k] * x[k] / r;
+            }
+        }
+    free(kn);
+    free(vv);
+    free(dkn);
+    free(dvv);
+    free(sc);
+    free(pw);
+    free(chat);
+    free(krot);
+    free(dchat);
+    free(dkrot);
+}
+
 /* ------------------------------------------------- TPLA latent decode ---- */
 /*
  * TPLA, "The reading" and "What carries the argument": the latent c_KV and each head's

@@ -24,6 +24,12 @@ MUTATIONS = {
     "causal_off_by_one": ("long n = pos + 1;", "long n = pos;"),
     "combine_weight": ("acc += exp(part_lse[(size_t)s * rows + r] - l) *",
                        "acc += exp(part_lse[(size_t)s * rows + r] - m) *"),
+    "bwd_softmax_no_D": ("const double ds = p * (dot(dO, vv + j * Dv, Dv) - Di);",
+                         "const double ds = p * dot(dO, vv + j * Dv, Dv);"),
+    "bwd_rope_transpose_sign": ("rope_row(dqr, -(double)pos, Dr, base, dq_pe + qrow * Dr);",
+                                "rope_row(dqr, (double)pos, Dr, base, dq_pe + qrow * Dr);"),
+    "bwd_rms_dropped_term": ("dx[k] = dy[k] * rms_w[k] / r - x[k] * g / ((double)Dk * r * r * r);",
+                             "dx[k] = dy[k] * rms_w[k] / r;"),
     "absorb_transposed": ("acc += qn[d] * wk[(size_t)d * Dk + k];\n                    qa[k] = acc;",
                           "acc += qn[d] * wk[(size_t)k * Dn + d];\n                    qa[k] = acc;"),
 }

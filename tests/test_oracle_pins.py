@@ -18,6 +18,10 @@
               latent decodes over the shard slices (TPLA, "The reading"), and the same
               sum rebuilt from library routines (torch rms_norm per shard, matmul,
               softmax, logsumexp).
+* Backward  -- every entry of every gradient of the explicit path against central finite
+              differences of the (pinned) forward in fp64, for causal with an offset,
+              non-causal and a head range (LAGA, "What carries the argument": the method's
+              gradients match the baseline's).
 """
 import math
 
@@ -365,6 +369,46 @@ def test_tpla_matches_library_composition(oracle):
         ref_o += torch.einsum("hdk,bhk->bhd", W[:, dn:, sl], o_lat)
         np.testing.assert_allclose(slse[i], torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
     np.testing.assert_allclose(out, ref_o.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("q_off,causal,s_q,head_begin,hc", [(4, True, 5, 0, 3), (0, False, 4, 0, 3),
+                                                            (2, True, 3, 1, 2)])
+def test_explicit_backward_matches_finite_differences(oracle, q_off, causal, s_q, head_begin, hc):
+    B, S, H, dk, dn, dr, dv = 2, 9, 3, 16, 8, 8, 8
+    inp = _make(B, S, H, dk, dn, dr, dv, 101, s_q=s_q, q_off=q_off)
+    inp["q_nope"], inp["q_pe"] = inp["q_nope"][:, :, :hc].copy(), inp["q_pe"][:, :, :hc].copy()
+    inp["rms_w"] = 1.0 + 0.3 * _rand(dk, 102)
+    G = _rand((B, s_q, hc, dv), 103)
+    kw = dict(n_heads=H, q_offset=q_off, causal=causal, head_begin=head_begin, eps=EPS)
+    grads = oracle.mla_explicit_bwd(**inp, dout=G, **kw)
+
+    def loss(d):
+        out, _ = oracle.mla_explicit(**d, **kw)
+        return float((out * G).sum())
+
+    h = 1e-5
+    for name in ("q_nope", "q_pe", "c_kv", "k_pe", "w_kv_b", "rms_w"):
+        x = inp[name]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            keep = x[idx]
+            x[idx] = keep + h
+            up = loss(inp)
+            x[idx] = keep - h
+            dn_ = loss(inp)
+            x[idx] = keep
+            fd[idx] = (up - dn_) / (2 * h)
+        assert np.abs(fd).max() > 0, name
+        np.testing.assert_allclose(grads[name], fd, rtol=0, atol=1e-7 * max(1.0, np.abs(fd).max()),
+                                   err_msg=name)
+    if causal:   # keys no query sees carry no gradient
+        n_vis = q_off + s_q
+        assert np.all(grads["c_kv"][:, n_vis:] == 0) and np.all(grads["k_pe"][:, n_vis:] == 0)
+    # heads outside the range get no weight gradient
+    Wg = grads["w_kv_b"].reshape(H, dn + dv, dk)
+    for hh in range(H):
+        if not head_begin <= hh < head_begin + hc:
+            assert np.all(Wg[hh] == 0)
 
 
 def test_golden_rows_unchanged(oracle):
