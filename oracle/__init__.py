@@ -11,7 +11,7 @@ module compiles it with gcc and exposes numpy-in / numpy-out wrappers.
 
 Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``):
   rmsnorm, rope, mla_explicit, mla_absorbed, mla_decode, lse_combine, tpla_decode,
-  mla_explicit_bwd -- all pinned.
+  mla_explicit_bwd, rmsnorm_bwd -- all pinned.
 """
 from __future__ import annotations
 
@@ -56,9 +56,11 @@ def _load():
         lib.orc_mla_decode.argtypes = [i, i, i, i, i, i, i, i, d, d] + [_dp] * 9
         lib.orc_lse_combine.argtypes = [i, l, i, _dp, _dp, _dp, _dp]
         lib.orc_tpla_decode.argtypes = [i, i, i, i, i, i, i, i, d, d, d] + [_dp] * 8
+        lib.orc_rmsnorm_bwd.argtypes = [_dp, _dp, l, i, i, d, _dp, _dp, _dp]
         lib.orc_mla_explicit_bwd.argtypes = [i, i, i, i, i, i, i, i, i, i, i, i, d, d, d] + [_dp] * 13
         for f in ("orc_rmsnorm", "orc_rope", "orc_mla_explicit", "orc_mla_absorbed",
-                  "orc_mla_decode", "orc_lse_combine", "orc_tpla_decode", "orc_mla_explicit_bwd"):
+                  "orc_mla_decode", "orc_lse_combine", "orc_tpla_decode", "orc_mla_explicit_bwd",
+                  "orc_rmsnorm_bwd"):
             getattr(lib, f).restype = None
         _lib = lib
     return _lib
@@ -118,6 +120,15 @@ def _fwd(fn, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, n_heads, q_offset=0, ca
 def mla_explicit(*args, **kw):
     """Explicit/LAGA MLA forward.  Returns (out [B,s_q,H_loc,Dv], lse [B,H_loc,s_q])."""
     return _fwd(_load().orc_mla_explicit, *args, **kw)
+
+
+def rmsnorm_bwd(x, w, dy, *, shards=1, eps=1e-6):
+    """Gradient of the per-shard RMSNorm over the last dim.  Returns (dx, dw)."""
+    x, w, dy = map(_f64, (x, w, dy))
+    d = x.shape[-1]
+    dx, dw = np.zeros_like(x), np.zeros(d)
+    _load().orc_rmsnorm_bwd(_p(x), _p(w), x.size // d, d, shards, float(eps), _p(dy), _p(dx), _p(dw))
+    return dx, dw
 
 
 def mla_explicit_bwd(q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, dout, *, n_heads, q_offset=0, causal=True,

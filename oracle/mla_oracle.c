@@ -395,6 +395,37 @@ void orc_mla_decode(int B, int kv_len, int n_splits, int n_heads,
         }
 }
 
+/* ------------------------------------------------- RMSNorm backward ---- */
+/*
+ * Gradient of y = per-shard RMSNorm(x) * w (orc_rmsnorm on each of g shards of d/g
+ * columns; g = 1 the LAGA page's latent norm, g > 1 TPLA's per-shard norm) for an
+ * upstream gradient dy [rows, d]: with r the shard's sqrt(mean x^2 + eps) and ds = d/g,
+ *   dx_k = dy_k w_k / r - x_k (sum over the shard of dy_m w_m x_m) / (ds r^3)
+ *   dw_k = sum over rows of dy_k x_k / r
+ */
+void orc_rmsnorm_bwd(const double *x, const double *w, long rows, int d, int g, double eps,
+                     const double *dy, double *dx, double *dw)
+{
+    const int ds = d / g;
+    for (int k = 0; k < d; ++k)
+        dw[k] = 0.0;
+    for (long r = 0; r < rows; ++r)
+        for (int i = 0; i < g; ++i) {
+            const double *xs = x + r * d + (size_t)i * ds, *dys = dy + r * d + (size_t)i * ds;
+            const double *ws = w + (size_t)i * ds;
+            double ss = 0.0, gs = 0.0;
+            for (int k = 0; k < ds; ++k) {
+                ss += xs[k] * xs[k];
+                gs += dys[k] * ws[k] * xs[k];
+            }
+            const double rr = sqrt(ss / ds + eps);
+            for (int k = 0; k < ds; ++k) {
+                dx[r * d + (size_t)i * ds + k] = dys[k] * ws[k] / rr - xs[k] * gs / ((double)ds * rr * rr * rr);
+                dw[(size_t)i * ds + k] += dys[k] * xs[k] / rr;
+            }
+        }
+}
+
 /* ------------------------------------------------- explicit backward ---- */
 /*
  * Gradients of the explicit forward (orc_mla_explicit) for a given upstream gradient

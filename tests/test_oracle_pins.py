@@ -371,6 +371,31 @@ def test_tpla_matches_library_composition(oracle):
     np.testing.assert_allclose(out, ref_o.numpy(), rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("shards", [1, 2, 4])
+def test_rmsnorm_backward_matches_finite_differences(oracle, shards):
+    rows, d = 5, 24
+    x, w, G = _rand((rows, d), 111) * 2.0, 1.0 + 0.3 * _rand(d, 112), _rand((rows, d), 113)
+    dx, dw = oracle.rmsnorm_bwd(x, w, G, shards=shards, eps=EPS)
+    ds = d // shards
+
+    def loss(x_, w_):
+        y = np.concatenate([oracle.rmsnorm(np.ascontiguousarray(x_[:, i * ds:(i + 1) * ds]),
+                                           w_[i * ds:(i + 1) * ds], EPS) for i in range(shards)], 1)
+        return float((y * G).sum())
+
+    h = 1e-6
+    for arr, grad in ((x, dx), (w, dw)):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + h
+            up = loss(x, w)
+            arr[idx] = keep - h
+            fd[idx] = (up - loss(x, w)) / (2 * h)
+            arr[idx] = keep
+        np.testing.assert_allclose(grad, fd, rtol=0, atol=1e-7)
+
+
 @pytest.mark.parametrize("q_off,causal,s_q,head_begin,hc", [(4, True, 5, 0, 3), (0, False, 4, 0, 3),
                                                             (2, True, 3, 1, 2)])
 def test_explicit_backward_matches_finite_differences(oracle, q_off, causal, s_q, head_begin, hc):
