@@ -255,6 +255,15 @@ def tpla_extra(dcfg, stream, hbm_peak, n_shards=2, steps=10, warmup=3):
     nfn = lambda: mla.rmsnorm(t["c_raw"], t["norm_w"], n_shards=n_shards, out=normed)  # noqa: E731
     n_ms = statistics.mean(timed(nfn, steps, warmup, 1))
     n_bytes = 2 * t["c_raw"].numel() * t["c_raw"].element_size() + t["norm_w"].numel() * 2
+    # its backward over the same rows (x, dy read; dx written)
+    dw = torch.empty(dcfg.d_kv, dtype=torch.float32, device="cuda")
+    bws = torch.empty(mla.mla_rmsnorm_bwd_workspace(mla.MLA_BF16, t["c_raw"].numel() // dcfg.d_kv, dcfg.d_kv,
+                                                    n_shards), dtype=torch.uint8, device="cuda")
+    bfn = lambda: mla.rmsnorm_bwd(t["c_raw"], t["norm_w"], t["c_cache"], n_shards=n_shards, dx=normed, dw=dw,  # noqa: E731
+                                  workspace=bws)
+    b_ms = statistics.mean(timed(bfn, steps, warmup, 1))
+    b_bytes = 3 * t["c_raw"].numel() * t["c_raw"].element_size()
+    del dw, bws
     mla.profile_reset()
     mla.profile_enable(True)
     fn()
@@ -270,7 +279,10 @@ def tpla_extra(dcfg, stream, hbm_peak, n_shards=2, steps=10, warmup=3):
             "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()},
             "cache_rmsnorm": {"rows": dcfg.batch * dcfg.kv_len, "ms": round(n_ms, 4), "bytes": n_bytes,
                               "GB/s": round(n_bytes / (n_ms * 1e-3) / 1e9, 1),
-                              "frac_of_measured_hbm": round(n_bytes / (n_ms * 1e-3) / 1e9 / hbm_peak, 4)}}
+                              "frac_of_measured_hbm": round(n_bytes / (n_ms * 1e-3) / 1e9 / hbm_peak, 4)},
+            "cache_rmsnorm_bwd": {"rows": dcfg.batch * dcfg.kv_len, "ms": round(b_ms, 4), "bytes": b_bytes,
+                                  "GB/s": round(b_bytes / (b_ms * 1e-3) / 1e9, 1),
+                                  "frac_of_measured_hbm": round(b_bytes / (b_ms * 1e-3) / 1e9 / hbm_peak, 4)}}
 
 
 def timed(fn, steps, warmup, world, flush=None):

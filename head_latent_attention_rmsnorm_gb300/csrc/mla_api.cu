@@ -724,6 +724,31 @@ mla_status mla_tpla_decode(const mla_dims *dims, mla_dtype dtype, int B, int kv_
                        shard_lse, nullptr, nullptr, workspace, workspace_bytes, cuda_stream);
 }
 
+size_t mla_rmsnorm_bwd_workspace(mla_dtype dtype, long rows, int d, int n_shards) {
+    if (!valid_dtype(dtype) || rows < 0 || d < 1 || n_shards < 1 || d % n_shards) return 0;
+    return align_up(rmsnorm_bwd_ws(ty_of(dtype), rows, d, n_shards), 256);
+}
+
+mla_status mla_rmsnorm_bwd(mla_dtype dtype, long rows, int d, int n_shards, float eps, const void *x, const void *w,
+                           const void *dy, void *dx, float *dw, void *workspace, size_t workspace_bytes,
+                           void *cuda_stream) {
+    if (!valid_dtype(dtype)) return MLA_ERR_DTYPE;
+    if (rows < 0 || d < 1 || n_shards < 1 || d % n_shards || !(eps >= 0.f)) return MLA_ERR_SHAPE;
+    if (!x || !w || !dy || !dx || !dw || !workspace) return MLA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(dx) || !aligned16(dw) || !aligned16(workspace))
+        return MLA_ERR_ALIGN;
+    const size_t need = mla_rmsnorm_bwd_workspace(dtype, rows, d, n_shards);
+    if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
+    const size_t es = ty_size(ty_of(dtype));
+    Range in[] = {rng(x, (size_t)rows * d * es), rng(w, (size_t)d * es), rng(dy, (size_t)rows * d * es)};
+    Range outs[] = {rng(dx, (size_t)rows * d * es), rng(dw, (size_t)d * 4), rng(workspace, need)};
+    mla_status st = check_alias(in, 3, outs, 3);
+    if (st != MLA_OK) return st;
+    g_last_path = 1;
+    return cuda_status(launch_rmsnorm_bwd(ty_of(dtype), rows, d, n_shards, eps, x, w, dy, dx, dw, (float *)workspace,
+                                          (cudaStream_t)cuda_stream));
+}
+
 mla_status mla_rmsnorm(mla_dtype dtype, long rows, int d, int n_shards, float eps, const void *x, const void *w,
                        void *y, void *cuda_stream) {
     if (!valid_dtype(dtype)) return MLA_ERR_DTYPE;

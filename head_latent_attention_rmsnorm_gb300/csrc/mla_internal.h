@@ -100,6 +100,12 @@ cudaError_t launch_lse_combine(int tout, int n, long rows, int D, const float *p
 cudaError_t launch_rmsnorm_shards(int ty, long rows, int D, int g, float eps, const void *x, const void *w, void *y,
                                   cudaStream_t st);
 
+// Backward of launch_rmsnorm_shards for an upstream dy: dx (storage ty) and dw (fp32, summed
+// over rows).  ws: fp32 scratch of rmsnorm_bwd_ws(...) bytes.
+size_t rmsnorm_bwd_ws(int ty, long rows, int D, int g);
+cudaError_t launch_rmsnorm_bwd(int ty, long rows, int D, int g, float eps, const void *x, const void *w,
+                               const void *dy, void *dx, float *dw, float *ws, cudaStream_t st);
+
 // TPLA decode around the latent decode kernels: qa [B][H][Dk], qp [B][H][Dr] -> qx
 // [B][g][H][Dk] (row (b,i,h) zero outside shard i's dims), qpx [B][g][H][Dr] (replicated);
 // storage ty.

@@ -844,6 +844,138 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(int ty, long rows, in
     }
 }
 
+// Backward of the per-shard RMSNorm: with r the shard's sqrt(mean x^2 + eps) and ds its
+// width, dx_k = dy_k w_k / r - x_k (sum_shard dy w x) / (ds r^3) and dw_k = sum_rows
+// dy_k x_k / r.  Whole rows in registers as in rmsnorm_rows_kernel (NP pieces of 16
+// bytes per lane, shards of whole 512-byte rounds); each warp walks rows with a grid
+// stride and keeps its dw terms in registers; the block's warps add theirs into shared
+// memory in a fixed order and the block writes one partial row of dw (fp32).
+template <int NP>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(int ty, long rows, int D, int g, float eps,
+                                                               const uint4 *x, const uint4 *w, const uint4 *dy,
+                                                               uint4 *dx, float *dw_part) {
+    __shared__ float red[NP * 256];
+    const int lane = threadIdx.x % 32, wib = threadIdx.x / 32, nwb = blockDim.x / 32;
+    const int per = ty == TY_F32 ? 4 : 8, sp = NP / g;
+    const float ds = (float)(D / g);
+    float acc[NP][8];
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[p][t] = 0.f;
+    const long stride = (long)gridDim.x * nwb;
+    for (long r = (long)blockIdx.x * nwb + wib; r < rows; r += stride) {
+        uint4 xv[NP], gv[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            xv[p] = x[r * (NP * 32) + p * 32 + lane];
+            gv[p] = dy[r * (NP * 32) + p * 32 + lane];
+        }
+        float ss[NP], gg[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            float xf[8], gf[8], wf[8];
+            unpack16(xv[p], ty, xf);
+            unpack16(gv[p], ty, gf);
+            unpack16(w[p * 32 + lane], ty, wf);
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (t < per) {
+                    a = fmaf(xf[t], xf[t], a);
+                    b = fmaf(gf[t] * wf[t], xf[t], b);
+                }
+            ss[p] = a;
+            gg[p] = b;
+        }
+        float inv[NP], coef[NP];
+        for (int i = 0; i < g; ++i) {
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+                if (p / sp == i) {
+                    a += ss[p];
+                    b += gg[p];
+                }
+            const float ri = 1.0f / sqrtf(warp_sum(a) / ds + eps);
+            const float c = warp_sum(b) * ri * ri * ri / ds;
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+                if (p / sp == i) {
+                    inv[p] = ri;
+                    coef[p] = c;
+                }
+        }
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            float xf[8], gf[8], wf[8], o[8];
+            unpack16(xv[p], ty, xf);
+            unpack16(gv[p], ty, gf);
+            unpack16(w[p * 32 + lane], ty, wf);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                o[t] = gf[t] * wf[t] * inv[p] - xf[t] * coef[p];
+                acc[p][t] = fmaf(gf[t] * xf[t], inv[p], acc[p][t]);
+            }
+            dx[r * (NP * 32) + p * 32 + lane] = pack16(o, ty);
+        }
+    }
+    for (int v = 0; v < nwb; ++v) {   // warp v adds its terms: the same order in every run
+        if (wib == v)
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    if (t < per) {
+                        const int k = (p * 32 + lane) * per + t;
+                        red[k] = (v == 0 ? 0.f : red[k]) + acc[p][t];
+                    }
+        __syncthreads();
+    }
+    for (int k = threadIdx.x; k < D; k += blockDim.x) dw_part[(long)blockIdx.x * D + k] = red[k];
+}
+
+// The same gradient for any shape: one warp per (row, shard) writes dx and the shard's
+// 1/r; then a thread per column sums dw over the rows.
+__global__ void rmsnorm_bwd_kernel(int ty, long rows, int D, int g, float eps, const void *x, const void *w,
+                                   const void *dy, void *dx, float *inv_r) {
+    const long u = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (u >= rows * g) return;
+    const int ds = D / g, k0 = (int)(u % g) * ds;
+    const long o = (u / g) * D + k0;
+    float ss = 0.f, gs = 0.f;
+    for (int k = lane; k < ds; k += 32) {
+        const float xv = ldx(x, ty, o + k);
+        ss = fmaf(xv, xv, ss);
+        gs = fmaf(ldx(dy, ty, o + k) * ldx(w, ty, k0 + k), xv, gs);
+    }
+    const float ri = 1.0f / sqrtf(warp_sum(ss) / (float)ds + eps);
+    const float c = warp_sum(gs) * ri * ri * ri / (float)ds;
+    for (int k = lane; k < ds; k += 32)
+        stx(dx, ty, o + k, ldx(dy, ty, o + k) * ldx(w, ty, k0 + k) * ri - ldx(x, ty, o + k) * c);
+    if (lane == 0) inv_r[u] = ri;
+}
+
+__global__ void rmsnorm_dw_kernel(int ty, long rows, int D, int g, const void *x, const void *dy, const float *inv_r,
+                                  float *dw) {
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= D) return;
+    const int i = k / (D / g);
+    float a = 0.f;
+    for (long r = 0; r < rows; ++r) a = fmaf(ldx(dy, ty, r * D + k) * ldx(x, ty, r * D + k), inv_r[r * g + i], a);
+    dw[k] = a;
+}
+
+// dw[k] = sum over the partial rows in order
+__global__ void dw_reduce_kernel(int nparts, int D, const float *part, float *dw) {
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= D) return;
+    float a = 0.f;
+    for (int b = 0; b < nparts; ++b) a += part[(long)b * D + k];
+    dw[k] = a;
+}
+
 // TPLA decode, query side: every head becomes g query rows, one per latent shard.  Row
 // (b, i, h) keeps q_abs[b][h] on shard i's dims and zero elsewhere, so its score over
 // the full latent row is the shard-local score q_abs_i . c_i; the rotated q_pe is
@@ -955,6 +1087,44 @@ cudaError_t launch_rmsnorm_shards(int ty, long rows, int D, int g, float eps, co
         return cudaGetLastError();
     }
     rmsnorm_shards_kernel<<<blocks_for(rows * g, 8), 256, 0, st>>>(ty, rows, D, g, eps, vec, x, w, y);
+    return cudaGetLastError();
+}
+
+namespace {
+constexpr long BWD_BLOCKS = 152L * 4;   // fused backward: blocks of 8 warps, grid-strided over rows
+long bwd_np(int ty, int D, int g) {    // pieces per lane of the fused kernel, 0 = other shapes
+    const long es = (long)ty_size(ty), np = (long)D * es / 512;
+    const bool ok = ((long)(D / g) * es) % 512 == 0 && (np == 1 || np == 2 || np == 4);
+    return ok ? np : 0;
+}
+}  // namespace
+
+size_t rmsnorm_bwd_ws(int ty, long rows, int D, int g) {
+    const size_t fused = (size_t)std::min<long>(BWD_BLOCKS, std::max<long>((rows + 7) / 8, 1)) * D * 4;
+    const size_t plain = (size_t)rows * g * 4;
+    return std::max(fused, plain);
+}
+
+cudaError_t launch_rmsnorm_bwd(int ty, long rows, int D, int g, float eps, const void *x, const void *w,
+                               const void *dy, void *dx, float *dw, float *ws, cudaStream_t st) {
+    ProfScope ps("rmsnorm_bwd", st);
+    const long np = bwd_np(ty, D, g);
+    const bool vec = np && ((uintptr_t)x & 15) == 0 && ((uintptr_t)w & 15) == 0 && ((uintptr_t)dy & 15) == 0 &&
+                     ((uintptr_t)dx & 15) == 0;
+    if (rows > 0 && vec) {
+        const long nb = std::min<long>(BWD_BLOCKS, (rows + 7) / 8);
+        const uint4 *xv = (const uint4 *)x, *wv = (const uint4 *)w, *gv = (const uint4 *)dy;
+        uint4 *dxv = (uint4 *)dx;
+        if (np == 1) rmsnorm_bwd_rows_kernel<1><<<(unsigned)nb, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, gv, dxv, ws);
+        if (np == 2) rmsnorm_bwd_rows_kernel<2><<<(unsigned)nb, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, gv, dxv, ws);
+        if (np == 4) rmsnorm_bwd_rows_kernel<4><<<(unsigned)nb, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, gv, dxv, ws);
+        dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>((int)nb, D, ws, dw);
+    } else if (rows > 0) {
+        rmsnorm_bwd_kernel<<<blocks_for(rows * g, 8), 256, 0, st>>>(ty, rows, D, g, eps, x, w, dy, dx, ws);
+        rmsnorm_dw_kernel<<<blocks_for(D, 128), 128, 0, st>>>(ty, rows, D, g, x, dy, ws, dw);
+    } else {
+        dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>(0, D, ws, dw);   // no rows: dw = 0
+    }
     return cudaGetLastError();
 }
 

@@ -6,7 +6,7 @@ Two layers, argument marshalling only:
   ``mla_status_string``, ``mla_check_device_error``: the C entry points under their
   own names, taking integers for pointers and sizes.
 * ``latent_attn_fwd``, ``absorbed_attn_fwd``, ``decode_splitkv``, ``lse_combine``,
-  ``tpla_decode``, ``rmsnorm``:
+  ``tpla_decode``, ``rmsnorm``, ``rmsnorm_bwd``:
   the same calls taking torch tensors; they allocate any output or workspace the
   caller did not pass (through torch's allocator, so the CUDA caching allocator sees
   every byte) and raise :class:`MlaError` on a non-OK status.
@@ -85,6 +85,10 @@ def lib() -> ctypes.CDLL:
         L.mla_tpla_decode_workspace.restype = _sz
         L.mla_rmsnorm.argtypes = [_i, ctypes.c_long, _i, _i, ctypes.c_float, _vp, _vp, _vp, _vp]
         L.mla_rmsnorm.restype = _i
+        L.mla_rmsnorm_bwd.argtypes = [_i, ctypes.c_long, _i, _i, ctypes.c_float] + [_vp] * 6 + [_sz, _vp]
+        L.mla_rmsnorm_bwd.restype = _i
+        L.mla_rmsnorm_bwd_workspace.argtypes = [_i, ctypes.c_long, _i, _i]
+        L.mla_rmsnorm_bwd_workspace.restype = _sz
         L.mla_status_string.argtypes = [_i]
         L.mla_status_string.restype = ctypes.c_char_p
         L.mla_check_device_error.argtypes = [_vp]
@@ -154,6 +158,14 @@ def mla_rmsnorm(*args) -> int:
     return lib().mla_rmsnorm(*args)
 
 
+def mla_rmsnorm_bwd(*args) -> int:
+    return lib().mla_rmsnorm_bwd(*args)
+
+
+def mla_rmsnorm_bwd_workspace(*args) -> int:
+    return lib().mla_rmsnorm_bwd_workspace(*args)
+
+
 def mla_status_string(status: int) -> str:
     return lib().mla_status_string(status).decode()
 
@@ -171,7 +183,7 @@ def set_path_override(mode: int) -> None:
 
 
 KERNELS = ("prep", "latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
-           "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "tpla_expand",
+           "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
            "tpla_combine")
 
 
@@ -313,6 +325,22 @@ def rmsnorm(x, w, *, n_shards=1, eps=1e-6, out=None, stream=None):
                      _stream(stream))
     _check(st, "mla_rmsnorm")
     return out
+
+
+def rmsnorm_bwd(x, w, dy, *, n_shards=1, eps=1e-6, dx=None, dw=None, workspace=None, stream=None):
+    """Backward of :func:`rmsnorm`.  Returns (dx like x, dw fp32 [d])."""
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    dt = _dt(x)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty(d, dtype=torch.float32, device=x.device)
+    ws = _workspace(mla_rmsnorm_bwd_workspace(dt, rows, d, n_shards), x.device, workspace)
+    st = mla_rmsnorm_bwd(dt, rows, d, n_shards, float(eps), _ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ptr(dw),
+                         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "mla_rmsnorm_bwd")
+    return dx, dw
 
 
 def lse_combine(part_out, part_lse, *, out_dtype=torch.float32, out=None, lse=None, stream=None):

@@ -164,6 +164,20 @@ mla_status mla_rmsnorm(mla_dtype dtype, long rows, int d, int n_shards, float ep
                        const void *w, void *y, void *cuda_stream);
 
 /*
+ * Backward of mla_rmsnorm for an upstream gradient dy [rows, d] (the first piece of the
+ * backward pass; LAGA page, "What carries the argument": its equivalence claim covers
+ * gradients).  Per shard of ds = d/n_shards columns with r = sqrt(mean x^2 + eps):
+ *   dx_k = dy_k w_k / r - x_k (sum over the shard of dy w x) / (ds r^3)   (dtype, [rows, d])
+ *   dw_k = sum over rows of dy_k x_k / r                                  (fp32, [d])
+ * dw is summed in a fixed order (the same bits on every run).  Scratch: the caller's
+ * workspace of mla_rmsnorm_bwd_workspace bytes.  rows = 0 sets dw to zero.
+ */
+mla_status mla_rmsnorm_bwd(mla_dtype dtype, long rows, int d, int n_shards, float eps,
+                           const void *x, const void *w, const void *dy, void *dx, float *dw,
+                           void *workspace, size_t workspace_bytes, void *cuda_stream);
+size_t mla_rmsnorm_bwd_workspace(mla_dtype dtype, long rows, int d, int n_shards);
+
+/*
  * Log-sum-exp merge (Helix / Flash-Decoding combine):
  *   lse[r] = log sum_s exp(part_lse[s][r]);  out[r][:] = sum_s exp(part_lse[s][r]-lse[r]) part_out[s][r][:]
  * part_out fp32 [n_splits, rows, D], part_lse fp32 [n_splits, rows] -> out (out_dtype)
@@ -244,7 +258,8 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   the number of launches and their summed device time in milliseconds (0 launches
  *   for an unknown name).  Names: "prep", "latent_prep", "rope_table", "rope_rows",
  *   "convert", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
- *   "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "tpla_expand", "tpla_combine".
+ *   "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
+ *   "tpla_combine".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
  * Not thread-safe: profile from one host thread at a time.
  */

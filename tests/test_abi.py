@@ -204,6 +204,18 @@ def test_rmsnorm_rejects(L, args, status):
     assert mla.mla_rmsnorm(*args, None) == status
 
 
+@pytest.mark.parametrize("over,status", [
+    (dict(dy=None), -1), (dict(ws=None), -1), (dict(n_shards=3), -2), (dict(rows=-1), -2), (dict(dtype=4), -3),
+    (dict(dw=fake(5) + 4), -4), (dict(ws_bytes=16), -5), (dict(dx=fake(1) + 64), -9), (dict(dw=fake(3) + 16), -9),
+])
+def test_rmsnorm_bwd_rejects(L, over, status):
+    a = dict(dtype=mla.MLA_BF16, rows=1000, d=512, n_shards=2, eps=1e-6, x=fake(1), w=fake(2), dy=fake(3),
+             dx=fake(4), dw=fake(5), ws=fake(6), ws_bytes=1 << 30, stream=None)
+    a.update(over)
+    assert mla.mla_rmsnorm_bwd(*a.values()) == status
+    assert mla.mla_rmsnorm_bwd_workspace(mla.MLA_BF16, 1000, 512, 2) >= 1000 * 2 * 4
+
+
 @pytest.mark.parametrize("args,status", [
     ((mla.MLA_F32, 0, 10, 8, fake(1), fake(2), fake(3), fake(4), None), -2),
     ((mla.MLA_F32, 4, 10, 8, None, fake(2), fake(3), fake(4), None), -1),

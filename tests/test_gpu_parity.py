@@ -431,3 +431,22 @@ def test_tpla_full_size_sampled(oracle):
                                      shards=2, base=cfg.rope_base)
         check_out(o[b:b + 1], ro, torch.bfloat16, "tpla out b=%d" % b)
         check_lse(sl[:, b:b + 1], rsl, "tpla lse b=%d" % b)
+
+
+@pytest.mark.parametrize("dtype,rows,d,g", [("bf16", 1000, 512, 1), ("bf16", 777, 512, 2), ("bf16", 50, 1024, 1),
+                                            ("f32", 333, 256, 2), ("f32", 9000, 128, 1), ("bf16", 333, 512, 4),
+                                            ("f32", 100, 30, 3), ("bf16", 50, 36, 3)])
+def test_rmsnorm_bwd(oracle, dtype, rows, d, g):
+    """The per-shard RMSNorm backward against the oracle's, fused and two-kernel paths;
+    dw (fp32, a sum over rows) must also come out bit-identical on a second call."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = inputs.to_torch(inputs.normal_rows(4, inputs.DEC_C_CACHE, rows, d, 2.0), tdt, (rows, d))
+    gy = inputs.to_torch(inputs.normal_rows(5, inputs.DEC_KPE_CACHE, rows, d), tdt, (rows, d))
+    w = inputs.norm_weight(d, tdt, seed=4)
+    dx, dw = mla.rmsnorm_bwd(x.cuda(), w.cuda(), gy.cuda(), n_shards=g, eps=1e-6)
+    dx2, dw2 = mla.rmsnorm_bwd(x.cuda(), w.cuda(), gy.cuda(), n_shards=g, eps=1e-6)
+    torch.cuda.synchronize()
+    rdx, rdw = oracle.rmsnorm_bwd(to64(x), to64(w), to64(gy), shards=g, eps=1e-6)
+    check_out(dx, rdx, tdt, "rmsnorm bwd dx")
+    np.testing.assert_allclose(to64(dw), rdw, rtol=1e-4, atol=1e-4 * max(1.0, np.abs(rdw).max()))
+    assert torch.equal(dw, dw2) and torch.equal(dx, dx2)
