@@ -4,7 +4,9 @@ Each rank takes its block of query positions (LAGA sequence-parallel view), of h
 (head-parallel view) or of decode key splits (Helix KV-parallel view) with
 `sharding`, computes it with the oracle, and the blocks are exchanged with
 all_gather; the concatenation (or the log-sum-exp merge of the split partials) must
-equal the single-process result.  Also checks the max-over-ranks timing reduction
+equal the single-process result.  A TPLA rank decodes with its latent shard (its own
+RMSNorm, local softmax, its slice of W_kv_b), and the all-reduced sum must equal the
+two-shard TPLA decode.  Also checks the max-over-ranks timing reduction
 the benchmark uses.
 """
 import os
@@ -67,10 +69,19 @@ def _worker(rank, port, q):
         s0, sc = sharding.split_shard(n_splits, WORLD, rank)
         parts = [None] * WORLD
         dist.all_gather_object(parts, (po[s0:s0 + sc], pl[s0:s0 + sc]))
+        # TPLA tensor-parallel rank: its latent shard, every head; outputs all-reduced
+        k0, kd = sharding.latent_shard(inp["c_kv"].shape[-1], WORLD, rank)
+        sl = slice(k0, k0 + kd)
+        to, _ = oracle.tpla_decode(inp["q_nope"][:, -1], inp["q_pe"][:, -1],
+                                   np.ascontiguousarray(inp["c_kv"][..., sl]), kpe,
+                                   np.ascontiguousarray(inp["w_kv_b"][:, sl]), 1.0 + 0.1 * np.arange(kd) / kd,
+                                   shards=1, scale=oracle.default_scale(inp["q_nope"].shape[-1], kpe.shape[-1]))
+        tsum = torch.from_numpy(np.ascontiguousarray(to))
+        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
         t = torch.tensor([float(rank + 1)], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         if rank == 0:
-            q.put((outs, houts, parts, t.item()))
+            q.put((outs, houts, parts, t.item(), tsum.numpy()))
     finally:
         dist.destroy_process_group()
 
@@ -83,7 +94,7 @@ def test_two_rank_partitions_reassemble(oracle):
     procs = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(WORLD)]
     for p in procs:
         p.start()
-    outs, houts, parts, tmax = q.get(timeout=240)
+    outs, houts, parts, tmax, tpla_sum = q.get(timeout=240)
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
@@ -109,6 +120,12 @@ def test_two_rank_partitions_reassemble(oracle):
     out = np.einsum("hdk,bhk->bhd", W, o_lat.reshape(1, H, dk))
     np.testing.assert_allclose(out, do, rtol=0, atol=1e-12)
     assert tmax == float(WORLD)
+    # the all-reduced TPLA rank outputs = the two-shard TPLA decode (norm weight as the ranks drew it)
+    dkv = inp["c_kv"].shape[-1]
+    w_norm = np.concatenate([1.0 + 0.1 * np.arange(dkv // WORLD) / (dkv // WORLD)] * WORLD)
+    ref, _ = oracle.tpla_decode(inp["q_nope"][:, -1], inp["q_pe"][:, -1], inp["c_kv"], kpe, inp["w_kv_b"], w_norm,
+                                shards=WORLD)
+    np.testing.assert_allclose(tpla_sum, ref, rtol=0, atol=1e-12)
 
 
 def test_block_partition_covers_exactly():
@@ -120,3 +137,10 @@ def test_block_partition_covers_exactly():
                 b, c = sharding.block(n, world, r)
                 covered.extend(range(b, b + c))
             assert covered == list(range(n))
+
+
+def test_latent_shard_needs_even_split():
+    from head_latent_attention_rmsnorm_gb300 import sharding
+    assert [sharding.latent_shard(512, 2, r) for r in range(2)] == [(0, 256), (256, 256)]
+    with pytest.raises(ValueError):
+        sharding.latent_shard(512, 3, 0)
