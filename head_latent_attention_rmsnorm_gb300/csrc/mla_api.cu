@@ -734,6 +734,13 @@ mla_status mla_rmsnorm_bwd(mla_dtype dtype, long rows, int d, int n_shards, floa
                            void *cuda_stream) {
     if (!valid_dtype(dtype)) return MLA_ERR_DTYPE;
     if (rows < 0 || d < 1 || n_shards < 1 || d % n_shards || !(eps >= 0.f)) return MLA_ERR_SHAPE;
+    if (rows == 0) {   // only dw is written (zeros)
+        if (!dw) return MLA_ERR_NULL;
+        if (!aligned16(dw)) return MLA_ERR_ALIGN;
+        g_last_path = 1;
+        return cuda_status(launch_rmsnorm_bwd(ty_of(dtype), 0, d, n_shards, eps, nullptr, nullptr, nullptr, nullptr, dw,
+                                              nullptr, (cudaStream_t)cuda_stream));
+    }
     if (!x || !w || !dy || !dx || !dw || !workspace) return MLA_ERR_NULL;
     if (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(dx) || !aligned16(dw) || !aligned16(workspace))
         return MLA_ERR_ALIGN;

@@ -170,7 +170,8 @@ mla_status mla_rmsnorm(mla_dtype dtype, long rows, int d, int n_shards, float ep
  *   dx_k = dy_k w_k / r - x_k (sum over the shard of dy w x) / (ds r^3)   (dtype, [rows, d])
  *   dw_k = sum over rows of dy_k x_k / r                                  (fp32, [d])
  * dw is summed in a fixed order (the same bits on every run).  Scratch: the caller's
- * workspace of mla_rmsnorm_bwd_workspace bytes.  rows = 0 sets dw to zero.
+ * workspace of mla_rmsnorm_bwd_workspace bytes.  rows = 0 sets dw to zero and reads
+ * nothing else (x, w, dy, dx and the workspace may then be NULL).
  */
 mla_status mla_rmsnorm_bwd(mla_dtype dtype, long rows, int d, int n_shards, float eps,
                            const void *x, const void *w, const void *dy, void *dx, float *dw,

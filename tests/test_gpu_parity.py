@@ -450,3 +450,12 @@ def test_rmsnorm_bwd(oracle, dtype, rows, d, g):
     check_out(dx, rdx, tdt, "rmsnorm bwd dx")
     np.testing.assert_allclose(to64(dw), rdw, rtol=1e-4, atol=1e-4 * max(1.0, np.abs(rdw).max()))
     assert torch.equal(dw, dw2) and torch.equal(dx, dx2)
+
+
+def test_rmsnorm_bwd_no_rows_zeroes_dw():
+    x = torch.empty(0, 512, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(512, dtype=torch.bfloat16, device="cuda")
+    dw = torch.full((512,), 7.0, device="cuda")
+    mla.rmsnorm_bwd(x, w, x, dw=dw)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dw).item() == 0
