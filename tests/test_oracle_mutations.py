@@ -30,6 +30,12 @@ MUTATIONS = {
                                 "rope_row(dqr, (double)pos, Dr, base, dq_pe + qrow * Dr);"),
     "bwd_rms_dropped_term": ("dx[k] = dy[k] * rms_w[k] / r - x[k] * g / ((double)Dk * r * r * r);",
                              "dx[k] = dy[k] * rms_w[k] / r;"),
+    "tpla_rope_band_dropped": ("sc[j] = scale * (dot(qa + k0, cb + j * Dk + k0, ds) + dot(qr, kb + j * Dr, Dr));",
+                               "sc[j] = scale * dot(qa + k0, cb + j * Dk + k0, ds);"),
+    "tpla_wv_shard_offset": ("out[row * Dv + d] += dot(wv + (size_t)d * Dk + k0, ol + k0, ds);",
+                             "out[row * Dv + d] += dot(wv + (size_t)d * Dk, ol + k0, ds);"),
+    "tpla_norm_weight_slice": ("rmsnorm_row(c_raw + r * Dk + (size_t)i * ds, rms_w + (size_t)i * ds, ds, eps,",
+                               "rmsnorm_row(c_raw + r * Dk + (size_t)i * ds, rms_w, ds, eps,"),
     "absorb_transposed": ("acc += qn[d] * wk[(size_t)d * Dk + k];\n                    qa[k] = acc;",
                           "acc += qn[d] * wk[(size_t)k * Dn + d];\n                    qa[k] = acc;"),
 }
