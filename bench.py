@@ -1,18 +1,20 @@
 #!/usr/bin/env python3
 """Benchmark of MLA attention from the compressed latent on GB300.
 
-One step = one explicit (LAGA per-rank) prefill call on the DeepSeek-V2-Lite-shaped
-workload (bf16, batch 1, 4096 tokens, 16 heads, d_kv 512, qk 192, v 128, causal)
-followed by one split-KV latent decode call (bf16, batch 64, 128 heads, 32768 cached
-tokens, 8 splits).  The headline ``value`` is the prefill's TFLOP/s (algorithmic
-FLOPs: visible causal pairs x 2 x (192 + 128) plus the K/V reconstruction GEMM); the
-``decode`` object carries the decode's HBM GB/s.  Both are timed per call with CUDA
-events on the launching stream; the prefill's inputs fit in L2, so a 256 MB buffer
-is written between timed calls; the decode's 2.4 GB cache does not.  After the timed
-regions, rank 0 at N = 1 also reports the V3-shaped prefill and the simulated SP=8
-rank-7 prefill (``other_prefill_configs``) and the allocator's peak memory of the
-explicit against the absorbed V3 prefill (``activation_memory``); --no-extras skips
-them.
+One step = one explicit (LAGA per-rank) prefill call on the largest single-GPU
+prefill workload: the simulated sequence-parallel rank 7 of 8 on DeepSeek-V3 dims
+(bf16, 16384 gathered latent rows + k_pe, the last 2048 query rows at offset 14336,
+128 heads rebuilt in head shards of 16, causal).  The headline ``value`` is its
+TFLOP/s (algorithmic FLOPs: visible causal pairs x 2 x (192 + 128) per head plus the
+K/V reconstruction GEMM), timed per call with CUDA events on the launching stream,
+a 256 MB buffer written between timed calls; ``roofline`` is the attention kernel's,
+``e2e`` the same call with its inputs copied from pinned host memory and its outputs
+copied back inside every timed step, ``cpu_baseline`` the fp64 oracle on a sample of
+the same workload on the host's cores.  After the headline, rank 0 at N = 1 also
+times, with the same step count, the V2-Lite and V3-shaped prefills, the V3 absorbed
+form (``other_prefill_configs``), the split-KV decode (``decode``: HBM GB/s), the TPLA
+decode, and measures the allocator's peak memory of the explicit against the
+absorbed form beside its closed form (``activation_memory``); --no-extras skips them.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -36,11 +38,12 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA prefill fwd TFLOP/s (% of BF16 peak); decode HBM GB/s (% of 8 TB/s)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max clock
-# DRAM bytes (read + write) per launch of the dominant kernels, from the ncu captures
-# summarised under profiles/ (None until the current kernel has been captured).  The
-# decode capture runs B = 8; its traffic grows in proportion to the batch, so the
-# B = 64 launch is 8x that.
-NCU_TRAFFIC = {"tc_attn": 62.01e6, "tc_decode_attn": 310.95e6 * 8}
+# DRAM bytes (read + write) per launch of the dominant kernels, keyed by (kernel,
+# workload, absorbed), from the ncu captures summarised under profiles/ (absent until the
+# current kernel has been captured on that workload).  The decode capture runs B = 8; its
+# traffic grows in proportion to the batch, so the B = 64 launch is 8x that.
+NCU_TRAFFIC = {("tc_attn", "v2lite_prefill_s4096_h16", False): 62.01e6,
+               ("tc_decode_attn", "v3_decode_b64_l32768_split8", False): 310.95e6 * 8}
 
 
 def load_peaks():
@@ -152,7 +155,7 @@ def randn(shape, std, dtype, g):
     return (torch.randn(shape, generator=g, device="cuda", dtype=torch.float32) * std).to(dtype)
 
 
-def prefill_setup(cfg, seed=0):
+def prefill_setup(cfg, seed=0, absorbed=False, fused=False):
     import torch
     from head_latent_attention_rmsnorm_gb300 import mla
     g = torch.Generator(device="cuda")
@@ -166,22 +169,36 @@ def prefill_setup(cfg, seed=0):
     d = mla.dims_of(cfg)
     out = torch.empty(B, S, H, cfg.d_v, dtype=dt, device="cuda")
     lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
-    nbytes = mla.mla_latent_attn_workspace(ctypes.byref(d), 1 if dt == torch.bfloat16 else 0, B, S, cfg.s_kv,
-                                           cfg.q_offset, int(cfg.causal), H, cfg.head_shard)
+    if fused:
+        nbytes = mla.mla_latent_attn_fused_workspace(ctypes.byref(d), 1 if dt == torch.bfloat16 else 0, B, S,
+                                                     cfg.s_kv, cfg.q_offset, int(cfg.causal), H)
+    else:
+        wsq = mla.mla_absorbed_attn_workspace if absorbed else mla.mla_latent_attn_workspace
+        nbytes = wsq(ctypes.byref(d), 1 if dt == torch.bfloat16 else 0, B, S, cfg.s_kv, cfg.q_offset,
+                     int(cfg.causal), H, cfg.head_shard)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
     return d, t, out, lse, ws
 
 
-def prefill_call(cfg, d, t, out, lse, ws, stream):
+def prefill_call(cfg, d, t, out, lse, ws, stream, absorbed=False, fused=False):
     from head_latent_attention_rmsnorm_gb300 import mla
-    st = mla.lib().mla_latent_attn_fwd(ctypes.byref(d), mla.MLA_BF16 if cfg.dtype == "bf16" else mla.MLA_F32,
-                                       cfg.batch, cfg.s_q, cfg.s_kv, cfg.q_offset, int(cfg.causal), 0,
-                                       cfg.n_heads, cfg.head_shard, t["q_nope"].data_ptr(), t["q_pe"].data_ptr(),
-                                       t["c_kv"].data_ptr(), t["k_pe"].data_ptr(), t["w_kv_b"].data_ptr(),
-                                       t["rms_w"].data_ptr(), out.data_ptr(), lse.data_ptr(), ws.data_ptr(),
-                                       ws.numel(), stream)
+    if fused:
+        st = mla.lib().mla_latent_attn_fused_fwd(
+            ctypes.byref(d), mla.MLA_BF16 if cfg.dtype == "bf16" else mla.MLA_F32, cfg.batch, cfg.s_q, cfg.s_kv,
+            cfg.q_offset, int(cfg.causal), 0, cfg.n_heads, t["q_nope"].data_ptr(), t["q_pe"].data_ptr(),
+            t["c_kv"].data_ptr(), t["k_pe"].data_ptr(), t["w_kv_b"].data_ptr(), t["rms_w"].data_ptr(), out.data_ptr(),
+            lse.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+        if st != 0:
+            raise RuntimeError("mla_latent_attn_fused_fwd: " + mla.mla_status_string(st))
+        return
+    f = mla.lib().mla_absorbed_attn_fwd if absorbed else mla.lib().mla_latent_attn_fwd
+    st = f(ctypes.byref(d), mla.MLA_BF16 if cfg.dtype == "bf16" else mla.MLA_F32, cfg.batch, cfg.s_q, cfg.s_kv,
+           cfg.q_offset, int(cfg.causal), 0, cfg.n_heads, cfg.head_shard, t["q_nope"].data_ptr(), t["q_pe"].data_ptr(),
+           t["c_kv"].data_ptr(), t["k_pe"].data_ptr(), t["w_kv_b"].data_ptr(), t["rms_w"].data_ptr(), out.data_ptr(),
+           lse.data_ptr(), ws.data_ptr(), ws.numel(), stream)
     if st != 0:
-        raise RuntimeError("mla_latent_attn_fwd: " + mla.mla_status_string(st))
+        raise RuntimeError(("mla_absorbed_attn_fwd: " if absorbed else "mla_latent_attn_fwd: ") +
+                           mla.mla_status_string(st))
 
 
 def decode_setup(cfg, seed=1):
@@ -315,51 +332,176 @@ def dominant(prof: dict, candidates):
     return best
 
 
-def other_prefill_configs(stream, steps=5, warmup=3):
-    """Whole-call throughput of the V3-shaped prefill (128 heads, shards of 16) and of
-    the simulated SP=8 rank 7 (16384 latent rows, last 2048 queries): reported beside
-    the headline, not part of it."""
+def prefill_measure(cfg, stream, steps, warmup, world, flush, peaks, peak_kind, absorbed=False, fused=False):
+    """One prefill workload: per-call time of `steps` calls after `warmup` (L2 flushed
+    between calls), then a second pass with a CUDA-event pair around every launch for
+    the per-kernel split and the dominant kernel's roofline.  The fused form's FLOPs are
+    counted as the explicit form's (the method's own work; its extra reconstructions are
+    the kernel's overhead)."""
+    from head_latent_attention_rmsnorm_gb300 import mla
+    d, t, out, lse, ws = prefill_setup(cfg, absorbed=absorbed, fused=fused)
+    fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream, absorbed=absorbed, fused=fused)  # noqa: E731
+    fn()
     import torch
-    from head_latent_attention_rmsnorm_gb300 import configs
-    res = {}
-    for cfg in (configs.V3, configs.SP8_RANK7):
-        d, t, out, lse, ws = prefill_setup(cfg)
-        fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
-        ms = statistics.mean(timed(fn, steps, warmup, 1))
-        fl = cfg.flops()["total"]
-        res[cfg.name] = {"ms_per_call": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1),
-                         "flops_per_call": fl, "head_shard": cfg.head_shard}
-        del d, t, out, lse, ws
-        torch.cuda.empty_cache()
-    return res
+    torch.cuda.synchronize()
+    path = mla.last_path()
+    n0 = mla.launch_count()
+    times = timed(fn, steps, warmup, world, flush)
+    launches = (mla.launch_count() - n0) * steps // (steps + warmup)
+    mla.profile_enable(True)
+    mla.profile_reset()
+    timed(fn, steps, warmup, world, flush)
+    prof = mla.profile_all()
+    mla.profile_enable(False)
+    ms = max_over_ranks(statistics.mean(times), world)
+    fl = cfg.absorbed_flops() if absorbed else cfg.flops()
+    calls = steps + warmup
+    kern = dominant(prof, ("tc_latent_attn", "attn_simt") if absorbed else
+                    (("tc_fused_attn",) if fused else ("tc_attn", "attn_simt")))
+    roof = None
+    if kern:
+        n, kms = prof[kern]
+        # the fused kernel does the reconstruction too
+        per_launch = (fl["total"] if fused else fl["attention"]) * calls / n
+        ach = per_launch / (kms / n * 1e-3) / 1e12
+        if kern.startswith("tc_"):
+            peak, bound, note = peaks.get("bf16_tflops", 1900.0), "tensor", "bf16 dense burst, " + peak_kind
+        else:
+            peak, bound, note = FP32_ALU_TFLOPS, "alu", "fp32 FMA lanes x max clock (SIMT kernel)"
+        roof = {"kernel": kern, "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": NCU_TRAFFIC.get((kern, cfg.name, absorbed or fused)),
+                "peak_kind": note, "launches": n, "avg_launch_us": round(kms / n * 1e3, 2),
+                "flops_per_launch": per_launch,
+                "share_of_step": round(kms / (sum(v[1] for v in prof.values()) or 1), 3)}
+    form = "absorbed" if absorbed else ("fused" if fused else "explicit")
+    res = {"workload": cfg.name + ("" if form == "explicit" else "_" + form), "form": form,
+           "ms_per_call": round(ms, 4), "TFLOP/s": round(world * fl["total"] / (ms * 1e-3) / 1e12, 2),
+           "frac_of_bf16_peak": round(fl["total"] / (ms * 1e-3) / 1e12 / peaks.get("bf16_tflops", 1900.0), 4),
+           "flops_per_call": fl["total"], "tokens_per_s": round(world * cfg.batch * cfg.s_q / (ms * 1e-3), 1),
+           "head_shard": cfg.head_shard, "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"),
+           "steps": steps, "warmup": warmup, "gpu_launches": launches, "roofline": roof,
+           "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
+    return res, (d, t, out, lse, ws, fn)
+
+
+def decode_measure(dcfg, stream, steps, warmup, world, peaks, peak_kind):
+    """The split-KV decode workload (inputs larger than L2): per-call time and the
+    decode kernel's HBM roofline."""
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import mla
+    dd, dt_, dout, dlse, dws = decode_setup(dcfg)
+    fn = lambda: decode_call(dcfg, dd, dt_, dout, dlse, dws, stream)  # noqa: E731
+    fn()
+    torch.cuda.synchronize()
+    path = mla.last_path()
+    times = timed(fn, steps, warmup, world)
+    mla.profile_enable(True)
+    mla.profile_reset()
+    timed(fn, steps, warmup, world)
+    prof = mla.profile_all()
+    mla.profile_enable(False)
+    ms = max_over_ranks(statistics.mean(times), world)
+    dbytes = dcfg.algorithmic_bytes()
+    gbs = world * dbytes / (ms * 1e-3) / 1e9
+    calls = steps + warmup
+    kd = dominant(prof, ("tc_decode_attn", "attn_simt"))
+    droof = None
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    if kd:
+        n, kms = prof[kd]
+        per_launch = dcfg.cache_bytes() * calls / n
+        ach = per_launch / (kms / n * 1e-3) / 1e9
+        droof = {"kernel": kd, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                 "frac": round(ach / hbm, 4), "traffic": NCU_TRAFFIC.get((kd, dcfg.name, False)),
+                 "peak_kind": "copy bandwidth, " + peak_kind, "launches": n, "avg_launch_us": round(kms / n * 1e3, 2),
+                 "bytes_per_launch": per_launch}
+    del dd, dt_, dout, dlse, dws
+    torch.cuda.empty_cache()
+    return {"workload": dcfg.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_call": round(ms, 4),
+            "bytes_per_call": dbytes, "frac_of_8TBps": round(gbs / world / 8000.0, 4),
+            "frac_of_measured_hbm": round(gbs / world / hbm, 4),
+            "tokens_per_s": round(world * dcfg.batch / (ms * 1e-3), 1), "steps": steps, "warmup": warmup,
+            "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"), "roofline": droof,
+            "l2": "inputs (2.4 GB) larger than L2",
+            "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
 
 
 def activation_memory():
-    """Peak device memory the CUDA caching allocator sees for one V3-shaped prefill call
-    (outputs + workspace), explicit (head shards of 16 and 128) against absorbed."""
+    """Peak device memory the CUDA caching allocator sees for one prefill call (outputs +
+    workspace), explicit against absorbed, at head shards of 16 and of all heads, on the
+    V3-shaped prefill and the simulated SP=8 rank 7; each beside its closed form."""
     import torch
     from head_latent_attention_rmsnorm_gb300 import configs, mla
-    cfg = configs.V3
-    d, t, _, _, _ = prefill_setup(cfg)
     res = {}
-    for absorbed in (False, True):
-        for hs in (16, cfg.n_heads):
-            torch.cuda.synchronize()
-            torch.cuda.empty_cache()
-            base = torch.cuda.memory_allocated()
-            torch.cuda.reset_peak_memory_stats()
-            fn = mla.absorbed_attn_fwd if absorbed else mla.latent_attn_fwd
-            o, l = fn(d, t["q_nope"], t["q_pe"], t["c_kv"], t["k_pe"], t["w_kv_b"], t["rms_w"], head_shard=hs)
-            torch.cuda.synchronize()
-            res["%s_hs%d_MB" % ("absorbed" if absorbed else "explicit", hs)] = round(
-                (torch.cuda.max_memory_allocated() - base) / 1e6, 1)
-            del o, l
-    res["workload"] = cfg.name
+    for cfg in (configs.V3, configs.SP8_RANK7):
+        d, t, _, _, _ = prefill_setup(cfg)
+        r = {}
+        for absorbed in (False, True):
+            for hs in (16, cfg.n_heads):
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()
+                base = torch.cuda.memory_allocated()
+                torch.cuda.reset_peak_memory_stats()
+                fn = mla.absorbed_attn_fwd if absorbed else mla.latent_attn_fwd
+                o, l = fn(d, t["q_nope"], t["q_pe"], t["c_kv"], t["k_pe"], t["w_kv_b"], t["rms_w"], head_shard=hs,
+                          q_offset=cfg.q_offset)
+                torch.cuda.synchronize()
+                key = "%s_hs%d" % ("absorbed" if absorbed else "explicit", hs)
+                cf = cfg.activation_bytes(absorbed, hs)
+                r[key + "_MB"] = round((torch.cuda.max_memory_allocated() - base) / 1e6, 1)
+                r[key + "_closed_form_MB"] = round(cf["total"] / 1e6, 1)
+                del o, l
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        o, l = mla.latent_attn_fused_fwd(d, t["q_nope"], t["q_pe"], t["c_kv"], t["k_pe"], t["w_kv_b"], t["rms_w"],
+                                         q_offset=cfg.q_offset)
+        torch.cuda.synchronize()
+        r["fused_MB"] = round((torch.cuda.max_memory_allocated() - base) / 1e6, 1)
+        cf = cfg.activation_bytes(False, 0)
+        r["fused_closed_form_MB"] = round(cf["total"] / 1e6, 1)
+        del o, l
+        per_tok = {"explicit": cfg.n_heads * (cfg.d_nope + cfg.d_v) * 2, "absorbed": cfg.n_heads * 2 * cfg.d_kv * 2}
+        r["per_token_head_bytes_all_heads"] = per_tok
+        r["closed_form"] = ("outputs + normalised latent and rotated bands + RoPE table + fp16 W rows + "
+                            "per shard: explicit K_nope,V^T = B*kv_pad*hs*(d_nope+d_v)*2; absorbed q_abs,o_lat = "
+                            "2*B*s_q*hs*d_kv*2; fused: nothing per shard")
+        res[cfg.name] = r
+        del d, t
+        torch.cuda.empty_cache()
     res["counts"] = "out + lse + workspace, torch.cuda.max_memory_allocated() minus the inputs"
     return res
 
 
+def e2e_measure(cfg, bufs, steps, warmup, world):
+    """The headline call end to end through the C ABI: every step copies the inputs from
+    pinned host memory to the device, runs the call and copies out + lse back."""
+    import torch
+    d, t, out, lse, ws, fn = bufs
+    host_in = {k: v.cpu().pin_memory() for k, v in t.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def step():
+        for k, v in host_in.items():
+            t[k].copy_(v, non_blocking=True)
+        fn()
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    times = timed(step, steps, warmup, world)
+    ms = max_over_ranks(statistics.mean(times), world)
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+    return {"value": round(world * cfg.flops()["total"] / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
+
+
 # -------------------------------------------------------------- our arm ----
+HEADLINE = "v3_sp8_rank7_skv16384_q2048"
+
+
 def run_ours(args, world, rank, local):
     import torch
     from head_latent_attention_rmsnorm_gb300 import build as mla_build
@@ -370,145 +512,71 @@ def run_ours(args, world, rank, local):
     barrier(world)
     mla.lib()
     peaks, peak_kind = load_peaks()
-    pcfg, dcfg = configs.V2LITE, configs.DECODE
+    pcfg = configs.ALL[HEADLINE]
     stream = torch.cuda.current_stream().cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    steps, warmup = args.steps, args.warmup
 
-    # ---- prefill and decode: the timed passes carry no per-launch events
-    d, t, out, lse, ws = prefill_setup(pcfg)
-    pf = lambda: prefill_call(pcfg, d, t, out, lse, ws, stream)  # noqa: E731
-    pf()
-    torch.cuda.synchronize()
-    path = mla.last_path()
-    dd, dt_, dout, dlse, dws = decode_setup(dcfg)
-    dfn = lambda: decode_call(dcfg, dd, dt_, dout, dlse, dws, stream)  # noqa: E731
-    dfn()
-    torch.cuda.synchronize()
-    dpath = mla.last_path()
+    # ---- the headline: the simulated SP=8 rank 7 (the largest single-GPU prefill)
     with ClockSampler(local) as clk:
-        n0 = mla.launch_count()
-        p_times = timed(pf, args.steps, args.warmup, world, flush)
-        launches_p = mla.launch_count() - n0
-        n1 = mla.launch_count()
-        d_times = timed(dfn, args.steps, args.warmup, world)
-        launches_d = mla.launch_count() - n1
-    per_call_p = launches_p / (args.steps + args.warmup)
-    per_call_d = launches_d / (args.steps + args.warmup)
-
-    # ---- second pass of the same calls with a CUDA-event pair around every launch
-    # (on the launching stream): per-kernel times for the roofline
-    def profiled(fn, fl):
-        mla.profile_enable(True)
-        mla.profile_reset()
-        timed(fn, args.steps, args.warmup, world, fl)
-        prof = mla.profile_all()
-        mla.profile_enable(False)
-        return prof
-    prof_p = profiled(pf, flush)
-    prof_d = profiled(dfn, None)
-
-    flops = pcfg.flops()
-    p_ms = max_over_ranks(statistics.mean(p_times), world)
-    d_ms = max_over_ranks(statistics.mean(d_times), world)
-    value = world * flops["total"] / (p_ms * 1e-3) / 1e12
-    dbytes = dcfg.algorithmic_bytes()
-    d_gbs = world * dbytes / (d_ms * 1e-3) / 1e9
-
-    # ---- roofline of the dominant kernels (from the profiled pass)
-    calls = args.steps + args.warmup
-    kp = dominant(prof_p, ("tc_attn", "attn_simt"))
-    roof = None
-    if kp:
-        n, ms = prof_p[kp]
-        per_launch_flops = flops["attention"] * calls / n
-        ach = per_launch_flops / (ms / n * 1e-3) / 1e12
-        if kp == "tc_attn":
-            peak, bound, note = peaks.get("bf16_tflops", 1900.0), "tensor", "bf16 dense burst, " + peak_kind
-        else:
-            peak, bound, note = FP32_ALU_TFLOPS, "alu", "fp32 FMA lanes x max clock (SIMT kernel)"
-        roof = {"kernel": kp, "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": NCU_TRAFFIC.get(kp), "peak_kind": note,
-                "launches": n, "avg_launch_us": round(ms / n * 1e3, 2),
-                "share_of_step": round(ms / (sum(v[1] for v in prof_p.values()) or 1), 3)}
-    kd = dominant(prof_d, ("tc_decode_attn", "attn_simt"))
-    droof = None
-    if kd:
-        n, ms = prof_d[kd]
-        per_launch = dcfg.cache_bytes() * calls / n
-        ach = per_launch / (ms / n * 1e-3) / 1e9
-        droof = {"kernel": kd, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks.get("hbm_gbs", 6800.0),
-                 "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4),
-                 "traffic": NCU_TRAFFIC.get(kd),
-                 "peak_kind": peak_kind, "launches": n, "avg_launch_us": round(ms / n * 1e3, 2)}
-
-    # ---- end to end through the C ABI with pinned host buffers (prefill)
+        head, bufs = prefill_measure(pcfg, stream, steps, warmup, world, flush, peaks, peak_kind)
+    value = head["TFLOP/s"]
+    p_ms = head["ms_per_call"]
     e2e = None
     try:
-        host_in = {k: v.cpu().pin_memory() for k, v in t.items()}
-        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        s = torch.cuda.current_stream()
-
-        def e2e_step():
-            for k, v in host_in.items():
-                t[k].copy_(v, non_blocking=True)
-            pf()
-            host_out.copy_(out, non_blocking=True)
-            host_lse.copy_(lse, non_blocking=True)
-
-        ke = max(1, min(args.steps, 20))
-        e_times = timed(e2e_step, ke, min(args.warmup, 3), world)
-        e_ms = max_over_ranks(statistics.mean(e_times), world)
-        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
-        e2e = {"value": round(world * flops["total"] / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
-        del s
+        e2e = e2e_measure(pcfg, bufs, max(1, min(steps, 20)), min(warmup, 3), world)
     except Exception as ex:  # keep the kernel numbers even if pinning fails
         e2e = {"value": None, "unit": "TFLOP/s", "error": str(ex)[:200]}
+    del bufs
+    torch.cuda.empty_cache()
 
-    # ---- beside the headline: the other prefill configs and the activation memory
-    # (after every timed region; rank 0 at N = 1 only, so replicas are not slowed)
-    others, mem, tpla = None, None, None
+    # ---- beside the headline, with the same step count: the other prefill workloads,
+    # the absorbed form, the decode (rank 0 at N = 1 only, so replicas are not slowed)
+    side, decode, mem, tpla = {}, None, None, None
     if rank == 0 and world == 1 and not args.no_extras:
-        del d, t, out, lse, ws, dd, dt_, dout, dlse, dws, flush
-        torch.cuda.empty_cache()
-        others = other_prefill_configs(stream)
+        with ClockSampler(local) as clk_side:
+            for cfg, absorbed, fused in ((configs.V2LITE, False, False), (configs.V3, False, False),
+                                         (configs.V3, True, False), (configs.V2LITE, False, True),
+                                         (configs.V3, False, True), (configs.SP8_RANK7, False, True)):
+                r, bufs = prefill_measure(cfg, stream, steps, warmup, 1, flush, peaks, peak_kind, absorbed=absorbed,
+                                          fused=fused)
+                side[r["workload"]] = r
+                del bufs
+                torch.cuda.empty_cache()
+            del flush
+            torch.cuda.empty_cache()
+            decode = decode_measure(configs.DECODE, stream, steps, warmup, 1, peaks, peak_kind)
+        side["clocks"] = clk_side.summary()
         mem = activation_memory()
-        tpla = tpla_extra(dcfg, stream, peaks.get("hbm_gbs", 6800.0))
+        tpla = tpla_extra(configs.DECODE, stream, peaks.get("hbm_gbs", 6800.0))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_prefill()
+        cpu = cpu_baseline_headline()
 
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(p_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(p_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn, N(0,1); W_kv_b N(0,1/512))",
-        "config": {"workload": pcfg.name, "batch": pcfg.batch, "seq_len": pcfg.s_q, "n_heads": pcfg.n_heads,
-                   "head_shard": pcfg.head_shard, "causal": True,
-                   "flops_per_step": flops["total"], "l2": "256 MB buffer written between timed calls",
-                   "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"), "parallelism": "replicas" if world > 1 else "single"},
-        "frac_of_bf16_peak": round(value / world / peaks.get("bf16_tflops", 1900.0), 4),
-        "tokens_per_s": round(world * pcfg.batch * pcfg.s_q / (p_ms * 1e-3), 1),
+        "config": {"workload": pcfg.name, "batch": pcfg.batch, "seq_len_kv": pcfg.s_kv, "query_rows": pcfg.s_q,
+                   "q_offset": pcfg.q_offset, "n_heads": pcfg.n_heads, "head_shard": pcfg.head_shard,
+                   "causal": True, "flops_per_step": pcfg.flops()["total"],
+                   "l2": "256 MB buffer written between timed calls",
+                   "kernel_path": head["kernel_path"], "parallelism": "replicas" if world > 1 else "single"},
+        "frac_of_bf16_peak": head["frac_of_bf16_peak"],
+        "tokens_per_s": head["tokens_per_s"],
         "clocks": clk.summary(),
         "e2e": e2e,
-        "gpu_launches": int(round((per_call_p + per_call_d) * args.steps)),
-        "roofline": roof,
+        "gpu_launches": head["gpu_launches"],
+        "roofline": head["roofline"],
         "cpu_baseline": cpu,
-        "decode": {"workload": dcfg.name, "value": round(d_gbs, 1), "unit": "GB/s", "ms_per_call": round(d_ms, 4),
-                   "bytes_per_call": dbytes, "frac_of_8TBps": round(d_gbs / world / 8000.0, 4),
-                   "frac_of_measured_hbm": round(d_gbs / world / peaks.get("hbm_gbs", 6800.0), 4),
-                   "tokens_per_s": round(world * dcfg.batch / (d_ms * 1e-3), 1),
-                   "kernel_path": {1: "simt", 2: "tcgen05"}.get(dpath, "?"), "roofline": droof,
-                   "l2": "inputs (2.4 GB) larger than L2"},
-        "other_prefill_configs": others,
+        "kernels_prefill": head["kernels"],
+        "decode": decode,
+        "other_prefill_configs": side or None,
         "tpla_decode": tpla,
         "activation_memory": mem,
-        "kernels_prefill": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_p.items()},
-        "kernels_decode": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof_d.items()},
         "peaks": {"kind": peak_kind, "hbm_gbs": peaks.get("hbm_gbs"), "bf16_tflops": peaks.get("bf16_tflops")},
     }
     print(json.dumps(line), flush=True)
@@ -524,9 +592,9 @@ def run_case(args):
     mla.lib()
     stream = torch.cuda.current_stream().cuda_stream
     if args.only == "prefill":
-        cfg = configs.ALL[args.workload] if args.workload else configs.V2LITE
-        d, t, out, lse, ws = prefill_setup(cfg)
-        fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream)  # noqa: E731
+        cfg = configs.ALL[args.workload] if args.workload else configs.ALL[HEADLINE]
+        d, t, out, lse, ws = prefill_setup(cfg, absorbed=args.absorbed, fused=args.fused)
+        fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream, absorbed=args.absorbed, fused=args.fused)  # noqa: E731
     else:
         cfg = configs.DECODE
         if args.batch:
@@ -549,33 +617,43 @@ def run_case(args):
 
 
 # -------------------------------------------------------- oracle (CPU) ----
-def oracle_prefill_sample(rows: int):
-    """Time the oracle on the last `rows` query rows of the V2-Lite prefill, all 16 heads.
+def oracle_prefill_sample(cfg, rows: int, heads: int):
+    """Time the oracle on the last `rows` query rows of workload `cfg`, heads [0, heads).
 
-    Returns (seconds, algorithmic FLOPs of the sample, threads used)."""
+    Returns (seconds, algorithmic FLOPs of the sample, threads used).  The sample's FLOPs
+    are its own: the visible pairs of those rows and heads x 2 x (qk + v dims), plus the
+    K/V reconstruction of those heads over every key the rows see."""
     import dataclasses
 
     import oracle
-    from head_latent_attention_rmsnorm_gb300 import configs, inputs
-    cfg = configs.V2LITE
-    q0 = cfg.s_kv - rows
-    sub = dataclasses.replace(cfg, s_q=rows, q_offset=q0)
-    inp = {k: v.double().numpy() for k, v in inputs.prefill_inputs(sub).items()}
+    from head_latent_attention_rmsnorm_gb300 import inputs
+    q0 = cfg.q_offset + cfg.s_q - rows
+    full = inputs.prefill_inputs(cfg, q_rows=(q0, q0 + rows))
+    sub = dataclasses.replace(cfg, s_q=rows, q_offset=q0, n_heads=heads)
+    inp = {k: v.double().numpy() for k, v in full.items()}
+    inp["q_nope"] = inp["q_nope"][:, :, :heads].copy()
+    inp["q_pe"] = inp["q_pe"][:, :, :heads].copy()
     t0 = time.perf_counter()
     oracle.mla_explicit(**inp, n_heads=cfg.n_heads, q_offset=q0, causal=True, base=cfg.rope_base, eps=cfg.rms_eps)
     dt = time.perf_counter() - t0
-    f = sub.flops()
-    return dt, f["total"], int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return dt, sub.flops()["total"], int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
-def cpu_baseline_prefill():
+CPU_SAMPLE = (512, 48)    # rows, heads of the cpu_baseline leg (10-20 s of the host's cores)
+REF_SAMPLE = (32, 16)     # rows, heads of each step of the --impl reference arm
+
+
+def cpu_baseline_headline():
+    from head_latent_attention_rmsnorm_gb300 import configs
     oracle_build()
-    rows = 4096
-    dt, fl, cores = oracle_prefill_sample(rows)
+    cfg = configs.ALL[HEADLINE]
+    rows, heads = CPU_SAMPLE
+    dt, fl, cores = oracle_prefill_sample(cfg, rows, heads)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "seconds": round(dt, 3),
-            "sample": "fp64 oracle, V2-Lite prefill, all 16 heads, last %d of 4096 query rows "
-                      "(K/V rebuilt for all 4096 keys)" % rows}
+            "sample": "fp64 oracle, %s: the last %d query rows (positions %d-%d), heads 0-%d, K/V rebuilt "
+                      "for every key they see" % (cfg.name, rows, cfg.q_offset + cfg.s_q - rows,
+                                                   cfg.q_offset + cfg.s_q - 1, heads - 1)}
 
 
 def oracle_build():
@@ -584,25 +662,27 @@ def oracle_build():
 
 
 def run_reference(args, world, rank):
-    """The oracle as the reference arm (rank 0 only)."""
+    """The oracle as the reference arm (rank 0 only), on the headline workload."""
     if rank != 0:
         return
+    from head_latent_attention_rmsnorm_gb300 import configs
     oracle_build()
-    rows = 256
+    cfg = configs.ALL[HEADLINE]
+    rows, heads = REF_SAMPLE
     for _ in range(args.warmup):
-        oracle_prefill_sample(rows)
+        oracle_prefill_sample(cfg, rows, heads)
     times, fl, cores = [], 0, 1
     for _ in range(args.steps):
-        dt, fl, cores = oracle_prefill_sample(rows)
+        dt, fl, cores = oracle_prefill_sample(cfg, rows, heads)
         times.append(dt)
     ms = statistics.mean(times) * 1e3
     v = fl / (ms * 1e-3) / 1e12
-    sample = ("fp64 oracle, V2-Lite prefill, all 16 heads, last %d of 4096 query rows "
-              "(K/V rebuilt for all 4096 keys)" % rows)
+    sample = ("fp64 oracle, %s: the last %d query rows, heads 0-%d, K/V rebuilt for every key they see"
+              % (cfg.name, rows, heads - 1))
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64, N(0,1))",
-            "config": {"workload": "v2lite_prefill_s4096_h16", "sample_rows": rows},
+            "config": {"workload": cfg.name, "sample_rows": rows, "sample_heads": heads},
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -617,7 +697,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the V3 / SP=8-rank prefill timings and the activation-memory measurement")
+                    help="skip the side workloads (V2-Lite, V3, absorbed, decode, TPLA) and the memory measurement")
+    ap.add_argument("--absorbed", action="store_true", help="--only prefill: the absorbed form")
+    ap.add_argument("--fused", action="store_true", help="--only prefill: the fused explicit form")
     ap.add_argument("--only", choices=("prefill", "decode", "tpla"), default=None,
                     help="run only this workload's calls, without timing (profiling target)")
     ap.add_argument("--workload", default=None, help="prefill workload name for --only prefill")

@@ -50,6 +50,38 @@ class Prefill:
         recon = 2 * self.batch * self.kv_needed() * self.d_kv * self.n_heads * (self.d_nope + self.d_v)
         return {"attention": attn, "reconstruct": recon, "total": attn + recon}
 
+    def absorbed_flops(self) -> dict:
+        """Algorithmic FLOPs of one absorbed-form call: latent-space attention over
+        d_kv + d_rope score dims and d_kv value dims, plus the absorb (q_nope -> q_abs) and
+        un-absorb (o_lat -> out) products."""
+        attn = self.batch * self.n_heads * self.pairs() * 2 * ((self.d_kv + self.d_rope) + self.d_kv)
+        rows = self.batch * self.s_q * self.n_heads
+        absorb = 2 * rows * self.d_nope * self.d_kv
+        unabsorb = 2 * rows * self.d_kv * self.d_v
+        return {"attention": attn, "absorb": absorb, "unabsorb": unabsorb, "total": attn + absorb + unabsorb}
+
+    def activation_bytes(self, absorbed: bool, head_shard: int) -> dict:
+        """Closed form of the per-call intermediates a caller allocates (outputs + the
+        workspace the library asks for), in bytes, at the tensor-core path's storage
+        (16-bit intermediates).  The head-dependent part is what separates the two forms
+        (the LAGA page's per-token footprint: n_h (d_nope + d_v) against n_h d_kv):
+        explicit K_nope and V^T of one head shard, absorbed q_abs and o_lat of one; with
+        head_shard = 0 the fused explicit form, which keeps no K/V at all."""
+        kv_pad = (self.kv_needed() + 127) // 128 * 128
+        rows = self.batch * self.s_q
+        out = rows * self.n_heads * self.d_v * 2 + rows * self.n_heads * 4
+        positions = max(self.kv_needed(), self.q_offset + self.s_q)
+        common = (self.batch * kv_pad * (self.d_kv + self.d_rope) * 2 + rows * self.n_heads * self.d_rope * 2
+                  + positions * (self.d_rope // 2) * 8)   # normalised latent, rotated bands, RoPE table
+        if absorbed:
+            w16 = head_shard * (self.d_nope + self.d_v) * self.d_kv * 2
+            shard = 2 * rows * head_shard * self.d_kv * 2
+        else:
+            w16 = self.n_heads * (self.d_nope + self.d_v) * self.d_kv * 2
+            shard = self.batch * head_shard * kv_pad * (self.d_nope + self.d_v) * 2
+        return {"outputs": out, "common": common, "w16": w16, "per_shard": shard,
+                "total": out + common + w16 + shard}
+
 
 @dataclass(frozen=True)
 class Decode:

@@ -24,6 +24,7 @@ using namespace mla;
 
 thread_local int g_last_path = 0;
 thread_local int g_path_override = 0;
+thread_local int g_fused_cluster = 0;   // 0: chosen per call
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -138,7 +139,9 @@ struct PrefillWs {
 // [q_offset, q_offset + s_q) (beyond kv_need only for non-causal calls).
 long rope_positions(const Prefill &p) { return std::max(p.kv_need, (long)p.q_offset + p.s_q); }
 
-PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
+// `fused`: the explicit form with the K/V reconstruction inside the attention kernel
+// (no per-shard K_nope / V^T).
+PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base, bool fused_kv = false) {
     Carve c;
     c.base = (char *)base;
     PrefillWs w{};
@@ -150,7 +153,9 @@ PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
     w.rtab = (float2 *)c.take((size_t)rope_positions(p) * (p.Dr / 2) * sizeof(float2));
     // fp16 W_kv_b rows: all heads of the call (explicit), one shard (absorbed transposes)
     if (p.tc) w.w16 = c.take((size_t)(fused ? p.head_count : p.hs) * (p.Dn + p.Dv) * p.Dk * 2);
-    if (!absorbed) {
+    if (fused_kv) {
+        // nothing per shard: K_nope and V^T tiles live only in shared memory
+    } else if (!absorbed) {
         // per-shard K_nope and V (tensor-core path: V stored transposed)
         w.k = c.take((size_t)p.B * p.hs * p.kv_pad * p.Dn * es);
         w.v = c.take((size_t)p.B * p.hs * p.kv_pad * p.Dv * es);
@@ -165,14 +170,15 @@ PrefillWs prefill_ws(const Prefill &p, bool absorbed, void *base) {
 
 mla_status prefill_common_checks(const Prefill &p, bool absorbed, const void *q_nope, const void *q_pe,
                                  const void *c_kv, const void *k_pe, const void *w_kv_b, const void *rms_w,
-                                 void *out, float *lse, void *workspace, size_t workspace_bytes) {
+                                 void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                 bool fused_kv = false) {
     const size_t es = ty_size(p.tin);
     const void *ptrs[] = {q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse};
     for (const void *q : ptrs)
         if (!q) return MLA_ERR_NULL;
     for (const void *q : ptrs)
         if (!aligned16(q)) return MLA_ERR_ALIGN;
-    PrefillWs w = prefill_ws(p, absorbed, nullptr);
+    PrefillWs w = prefill_ws(p, absorbed, nullptr, fused_kv);
     if (workspace_bytes < w.bytes) return MLA_ERR_WORKSPACE;
     if (w.bytes && !workspace) return MLA_ERR_NULL;
     if (workspace && !aligned16(workspace)) return MLA_ERR_ALIGN;
@@ -572,27 +578,37 @@ mla_status decode_simt(const Decode &p, float scale, const mla_dims *d, const vo
     return MLA_OK;
 }
 
+// Query tiles of a head that share each rebuilt key tile in the fused kernel.
+int fused_cluster(const Prefill &p) {
+    if (g_fused_cluster == 4 || g_fused_cluster == 8) return g_fused_cluster;
+    return (p.s_q + 127) / 128 >= 8 ? 8 : 4;
+}
+
 mla_status prefill_entry(bool absorbed, const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
                          int q_offset, int causal, int head_begin, int head_count, int head_shard, const void *q_nope,
                          const void *q_pe, const void *c_kv, const void *k_pe, const void *w_kv_b, const void *rms_w,
-                         void *out, float *lse, void *workspace, size_t workspace_bytes, void *cuda_stream) {
+                         void *out, float *lse, void *workspace, size_t workspace_bytes, void *cuda_stream,
+                         bool fused_kv = false) {
     Prefill p;
     mla_status st = prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count, head_shard,
                                   absorbed, &p);
     if (st != MLA_OK) return st;
+    if (fused_kv && !p.tc) return MLA_ERR_UNSUPPORTED;   // the fused kernel is the tensor-core path only
     if (B == 0 || s_q == 0 || head_count == 0) return MLA_OK;
     st = prefill_common_checks(p, absorbed, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, workspace,
-                               workspace_bytes);
+                               workspace_bytes, fused_kv);
     if (st != MLA_OK) return st;
     cudaStream_t cs = (cudaStream_t)cuda_stream;
-    PrefillWs w = prefill_ws(p, absorbed, workspace);
+    PrefillWs w = prefill_ws(p, absorbed, workspace, fused_kv);
     float scale = scale_of(dims);
     st = prefill_prep(p, absorbed, dims, q_pe, c_kv, k_pe, w_kv_b, rms_w, w, cs);
     if (st != MLA_OK) return st;
-    g_last_path = p.tc ? 2 : 1;
+    g_last_path = p.tc ? (fused_kv ? 3 : 2) : 1;
     if (p.tc) {
         TcPrefill t{p.B, p.s_q, p.s_kv, p.q_offset, p.causal, p.head_begin, p.head_count, p.hs, p.n_shards,
                     p.Dk, p.Dn, p.Dr, p.Dv, p.H, p.kv_need, scale};
+        if (fused_kv)
+            return cuda_status(tc_fused_prefill(t, q_nope, out, lse, w.chat, w.kpe, w.qpe, w.w16, fused_cluster(p), cs));
         cudaError_t e = absorbed ? tc_absorbed_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.qabs,
                                                        w.olat, w.w16, cs)
                                  : tc_explicit_prefill(t, q_nope, w_kv_b, out, lse, w.chat, w.kpe, w.qpe, w.k,
@@ -633,6 +649,26 @@ size_t mla_latent_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, i
     if (B == 0 || s_q == 0 || head_count == 0) return 0;
     return prefill_ws(p, false, nullptr).bytes;
 }
+
+mla_status mla_latent_attn_fused_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                                     int causal, int head_begin, int head_count, const void *q_nope, const void *q_pe,
+                                     const void *c_kv, const void *k_pe, const void *w_kv_b, const void *rms_w,
+                                     void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                     void *cuda_stream) {
+    return prefill_entry(false, dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count, 0, q_nope, q_pe,
+                         c_kv, k_pe, w_kv_b, rms_w, out, lse, workspace, workspace_bytes, cuda_stream, true);
+}
+
+size_t mla_latent_attn_fused_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                                       int causal, int head_count) {
+    Prefill p;
+    if (prefill_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, 0, head_count, 0, false, &p) != MLA_OK || !p.tc)
+        return 0;
+    if (B == 0 || s_q == 0 || head_count == 0) return 0;
+    return prefill_ws(p, false, nullptr, true).bytes;
+}
+
+void mla_set_fused_cluster(int size) { g_fused_cluster = size; }
 
 size_t mla_absorbed_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
                                    int causal, int head_count, int head_shard) {
@@ -812,6 +848,11 @@ mla_status mla_check_device_error(void *cuda_stream) {
     unsigned int flags = 0;
     if (tc_read_and_clear_error(&flags, cs) != cudaSuccess) return MLA_ERR_CUDA;
     return flags ? MLA_ERR_DEVICE_TIMEOUT : MLA_OK;
+}
+
+mla_status mla_selftest_bounded_wait(unsigned limit_us, void *cuda_stream) {
+    if (limit_us < 1 || limit_us > 100000) return MLA_ERR_SHAPE;
+    return cuda_status(launch_wait_probe((uint64_t)limit_us * 1000u, (cudaStream_t)cuda_stream));
 }
 
 int mla_last_path(void) { return g_last_path; }

@@ -116,6 +116,10 @@ cudaError_t launch_tpla_expand(int ty, int B, int H, int g, int Dk, int Dr, cons
 cudaError_t launch_tpla_combine(int tout, int n, int B, int H, int g, int Dk, const float *po, const float *pl,
                                 void *out, float *slse, cudaStream_t st);
 
+// One-thread kernel whose bounded mbarrier wait (limit_ns) runs out by construction and
+// records the timeout in the device error word (the self-test of that mechanism).
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st);
+
 // Reads and clears the bounded-wait error words of the tensor-core kernels.
 cudaError_t tc_read_and_clear_error(unsigned int *flags, cudaStream_t st);
 

@@ -936,7 +936,9 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(int ty, long rows
 }
 
 // The same gradient for any shape: one warp per (row, shard) writes dx and the shard's
-// 1/r; then a thread per column sums dw over the rows.
+// 1/r; then dw in two fixed-order passes: block column y of rmsnorm_dw_kernel sums its
+// contiguous run of rows per column into partial row y, and dw_reduce_kernel adds the
+// partial rows in order.
 __global__ void rmsnorm_bwd_kernel(int ty, long rows, int D, int g, float eps, const void *x, const void *w,
                                    const void *dy, void *dx, float *inv_r) {
     const long u = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -958,13 +960,14 @@ __global__ void rmsnorm_bwd_kernel(int ty, long rows, int D, int g, float eps, c
 }
 
 __global__ void rmsnorm_dw_kernel(int ty, long rows, int D, int g, const void *x, const void *dy, const float *inv_r,
-                                  float *dw) {
+                                  long rows_per_part, float *dw_part) {
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= D) return;
     const int i = k / (D / g);
+    const long r0 = (long)blockIdx.y * rows_per_part, r1 = min(rows, r0 + rows_per_part);
     float a = 0.f;
-    for (long r = 0; r < rows; ++r) a = fmaf(ldx(dy, ty, r * D + k) * ldx(x, ty, r * D + k), inv_r[r * g + i], a);
-    dw[k] = a;
+    for (long r = r0; r < r1; ++r) a = fmaf(ldx(dy, ty, r * D + k) * ldx(x, ty, r * D + k), inv_r[r * g + i], a);
+    dw_part[(long)blockIdx.y * D + k] = a;
 }
 
 // dw[k] = sum over the partial rows in order
@@ -1099,9 +1102,15 @@ long bwd_np(int ty, int D, int g) {    // pieces per lane of the fused kernel, 0
 }
 }  // namespace
 
+namespace {
+// Partial rows of the general-shape dw pass: runs of at least 64 rows, at most 256 parts.
+long dw_parts(long rows) { return std::max<long>(1, std::min<long>(256, (rows + 63) / 64)); }
+}  // namespace
+
 size_t rmsnorm_bwd_ws(int ty, long rows, int D, int g) {
     const size_t fused = (size_t)std::min<long>(BWD_BLOCKS, std::max<long>((rows + 7) / 8, 1)) * D * 4;
-    const size_t plain = (size_t)rows * g * 4;
+    // 1/r of every (row, shard), 256-byte aligned, then the partial dw rows
+    const size_t plain = ((size_t)rows * g * 4 + 255) / 256 * 256 + (size_t)dw_parts(rows) * D * 4;
     return std::max(fused, plain);
 }
 
@@ -1121,7 +1130,11 @@ cudaError_t launch_rmsnorm_bwd(int ty, long rows, int D, int g, float eps, const
         dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>((int)nb, D, ws, dw);
     } else if (rows > 0) {
         rmsnorm_bwd_kernel<<<blocks_for(rows * g, 8), 256, 0, st>>>(ty, rows, D, g, eps, x, w, dy, dx, ws);
-        rmsnorm_dw_kernel<<<blocks_for(D, 128), 128, 0, st>>>(ty, rows, D, g, x, dy, ws, dw);
+        const long parts = dw_parts(rows), per = (rows + parts - 1) / parts;
+        float *part = ws + ((size_t)rows * g * 4 + 255) / 256 * 64;
+        rmsnorm_dw_kernel<<<dim3(blocks_for(D, 128), (unsigned)parts), 128, 0, st>>>(ty, rows, D, g, x, dy, ws, per,
+                                                                                      part);
+        dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>((int)parts, D, part, dw);
     } else {
         dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>(0, D, ws, dw);   // no rows: dw = 0
     }

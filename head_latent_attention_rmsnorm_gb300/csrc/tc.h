@@ -31,6 +31,11 @@ bool tc_decode_supported(int Dk, int Dn, int Dr, int Dv, int H);
 cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
                                 float *lse, const void *chat, const void *kpe, const void *qpe, void *kws,
                                 void *vws, const void *w16, cudaStream_t st);
+// Explicit prefill with the K_nope / V^T reconstruction inside the attention kernel
+// (tc_fused.cu): no K/V workspace; `cluster` (4 or 8) query tiles of a head share every
+// rebuilt key tile.  Inputs as tc_explicit_prefill (w16 holds all head_count heads).
+cudaError_t tc_fused_prefill(const TcPrefill &p, const void *q_nope, void *out, float *lse, const void *chat,
+                             const void *kpe, const void *qpe, const void *w16, int cluster, cudaStream_t st);
 cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
                                 float *lse, const void *chat, const void *kpe, const void *qpe, void *qabs,
                                 void *olat, void *w16, cudaStream_t st);

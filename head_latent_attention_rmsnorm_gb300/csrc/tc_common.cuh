@@ -80,23 +80,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase of `bar` with parity `parity` to complete.  Gives up after
-// WAIT_NS, or as soon as *abort is set by another thread of the CTA; on a timeout it
-// records ERR_WAIT_TIMEOUT in *err and sets *abort.  Returns false when the wait did
-// not complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          unsigned *err) {
+// limit_ns of the global timer (checked every 64 polls), or as soon as *abort is set by
+// another thread of the CTA; on a timeout it records ERR_WAIT_TIMEOUT in *err and sets
+// *abort.  Returns false when the wait did not complete.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                unsigned *err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1; i < WAIT_LIMIT; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63) == 0) {
             if (*abort) return false;
-            if (global_ns() - t0 > WAIT_NS) break;
+            if (global_ns() - t0 > limit_ns) break;
         }
     }
     atomicOr(err, ERR_WAIT_TIMEOUT);
     *abort = 1;
     return false;
+}
+// The wait every kernel of the library uses: limit WAIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          unsigned *err) {
+    return mbar_wait_limit(bar, parity, abort, err, WAIT_NS);
 }
 
 // ----------------------------------------------------------------------- TMA ----

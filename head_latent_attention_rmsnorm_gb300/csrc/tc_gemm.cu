@@ -647,6 +647,31 @@ cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int 
     return tc_gemm_group(&g, 1, f16, st);
 }
 
+namespace {
+// A wait that nothing ends: one thread waits on a fresh mbarrier (phase 0, which no
+// thread ever arrives at) with the library's bounded wait and a short limit.  The wait
+// runs out, records the timeout in the same error word the GEMM kernels use, and the
+// kernel returns.  No TMA, bulk copy, MMA or TMEM allocation is in flight.
+__global__ void wait_probe_kernel(uint64_t limit_ns) {
+    using namespace tc;
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_limit(&bar, 0, &abort_flag, &g_tc_gemm_err, limit_ns);
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st) {
+    ProfScope ps("wait_probe", st);
+    wait_probe_kernel<<<1, 32, 0, st>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t tc_gemm_read_and_clear_error(unsigned *flags, cudaStream_t st) {
     unsigned v = 0;
     cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tc_gemm_err, sizeof(v), 0, cudaMemcpyDeviceToHost, st);

@@ -51,6 +51,7 @@ cudaError_t tc_gemm_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_attn_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_latent_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_decode_read_and_clear_error(unsigned *flags, cudaStream_t st);
+cudaError_t tc_fused_read_and_clear_error(unsigned *flags, cudaStream_t st);
 
 // Split-KV latent decode attention (tc_decode.cu): partial latent outputs and
 // log-sum-exps of every (sequence, key split, 128 heads).  qa: q_abs [B][H][512] fp16;

@@ -28,7 +28,7 @@ MLA_F32, MLA_BF16 = 0, 1
 STATUS = {0: "MLA_OK", -1: "MLA_ERR_NULL", -2: "MLA_ERR_SHAPE", -3: "MLA_ERR_DTYPE", -4: "MLA_ERR_ALIGN",
           -5: "MLA_ERR_WORKSPACE", -6: "MLA_ERR_UNSUPPORTED", -7: "MLA_ERR_CUDA",
           -8: "MLA_ERR_DEVICE_TIMEOUT", -9: "MLA_ERR_ALIAS"}
-PATH_NONE, PATH_SIMT, PATH_TC = 0, 1, 2
+PATH_NONE, PATH_SIMT, PATH_TC, PATH_TC_FUSED = 0, 1, 2, 3
 
 
 class MlaError(RuntimeError):
@@ -68,6 +68,12 @@ def lib() -> ctypes.CDLL:
         for f in ("mla_latent_attn_fwd", "mla_absorbed_attn_fwd"):
             getattr(L, f).argtypes = fwd
             getattr(L, f).restype = _i
+        L.mla_latent_attn_fused_fwd.argtypes = [D, _i, _i, _i, _i, _i, _i, _i, _i] + [_vp] * 8 + [_vp, _sz, _vp]
+        L.mla_latent_attn_fused_fwd.restype = _i
+        L.mla_latent_attn_fused_workspace.argtypes = [D, _i, _i, _i, _i, _i, _i, _i]
+        L.mla_latent_attn_fused_workspace.restype = _sz
+        L.mla_set_fused_cluster.argtypes = [_i]
+        L.mla_set_fused_cluster.restype = None
         L.mla_decode_splitkv.argtypes = [D, _i, _i, _i, _i] + [_vp] * 9 + [_vp, _sz, _vp]
         L.mla_decode_splitkv.restype = _i
         L.mla_decode_splitkv_noalloc.argtypes = [D, _i, _i, _i, _i] + [_vp] * 7 + [_vp]
@@ -93,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.mla_status_string.restype = ctypes.c_char_p
         L.mla_check_device_error.argtypes = [_vp]
         L.mla_check_device_error.restype = _i
+        L.mla_selftest_bounded_wait.argtypes = [ctypes.c_uint, _vp]
+        L.mla_selftest_bounded_wait.restype = _i
         L.mla_last_path.argtypes = []
         L.mla_last_path.restype = _i
         L.mla_set_path_override.argtypes = [_i]
@@ -117,6 +125,14 @@ def mla_latent_attn_fwd(*args) -> int:
 
 def mla_absorbed_attn_fwd(*args) -> int:
     return lib().mla_absorbed_attn_fwd(*args)
+
+
+def mla_latent_attn_fused_fwd(*args) -> int:
+    return lib().mla_latent_attn_fused_fwd(*args)
+
+
+def mla_latent_attn_fused_workspace(*args) -> int:
+    return lib().mla_latent_attn_fused_workspace(*args)
 
 
 def mla_decode_splitkv(*args) -> int:
@@ -174,6 +190,10 @@ def mla_check_device_error(stream: int | None = None) -> int:
     return lib().mla_check_device_error(stream)
 
 
+def mla_selftest_bounded_wait(limit_us: int, stream: int | None = None) -> int:
+    return lib().mla_selftest_bounded_wait(limit_us, stream)
+
+
 def last_path() -> int:
     return lib().mla_last_path()
 
@@ -184,7 +204,7 @@ def set_path_override(mode: int) -> None:
 
 KERNELS = ("prep", "latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
            "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
-           "tpla_combine")
+           "tpla_combine", "wait_probe", "tc_fused_attn")
 
 
 def launch_count() -> int:
@@ -274,6 +294,30 @@ def latent_attn_fwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, q_offse
 
 def absorbed_attn_fwd(d: Dims, *args, **kw):
     return latent_attn_fwd(d, *args, absorbed=True, **kw)
+
+
+def latent_attn_fused_fwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, q_offset=0, causal=True,
+                          head_begin=0, out=None, lse=None, workspace=None, stream=None):
+    """Explicit MLA prefill with the K/V up-projection inside the attention kernel (no
+    K/V workspace).  Returns (out, lse)."""
+    B, s_q, hc, _ = q_nope.shape
+    s_kv = c_kv.shape[1]
+    dt = _dt(q_nope)
+    if out is None:
+        out = torch.empty(B, s_q, hc, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty(B, hc, s_q, dtype=torch.float32, device=q_nope.device)
+    nbytes = mla_latent_attn_fused_workspace(ctypes.byref(d), dt, B, s_q, s_kv, q_offset, int(causal), hc)
+    ws = _workspace(nbytes, q_nope.device, workspace)
+    st = mla_latent_attn_fused_fwd(ctypes.byref(d), dt, B, s_q, s_kv, q_offset, int(causal), head_begin, hc,
+                                   _ptr(q_nope), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe), _ptr(w_kv_b), _ptr(rms_w),
+                                   _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "mla_latent_attn_fused_fwd")
+    return out, lse
+
+
+def set_fused_cluster(size: int) -> None:
+    lib().mla_set_fused_cluster(size)
 
 
 def decode_splitkv(d: Dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_splits=1, out=None, lse=None,

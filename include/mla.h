@@ -33,6 +33,14 @@
  *    input or each other (MLA_ERR_ALIAS).
  *  - On any error status nothing has been launched, except MLA_ERR_CUDA, which
  *    reports a failed launch or failed CUDA runtime call.
+ *  - Precision of the bf16 tensor-core kernels: their score operands (normalised
+ *    latent, rotated RoPE bands, K_nope, q_abs) and P are fp16, so every such value
+ *    must lie inside fp16's range (|x| < 65504), and a log-sum-exp carries an absolute
+ *    error of up to about 2^-11 of the largest |lse| of the call (measured 5.7e-4 at
+ *    unit-scale inputs, whose |lse| stays below ~8; 0.1 at scores near 500).  Callers
+ *    whose scores go well beyond that range and who need a tighter log-sum-exp select
+ *    the CUDA-core kernels, which keep fp32 intermediates, with
+ *    mla_set_path_override(1).
  *  - Positions: query row i of a prefill call sits at absolute position q_offset+i,
  *    key j at position j; a decode query sits at kv_len-1.  RoPE pairs (t, t+d/2)
  *    with angle pos * rope_base^(-2t/d_rope).  Causal: key j visible iff
@@ -80,8 +88,11 @@ typedef struct {
  * Queries are rows [q_offset, q_offset+s_q) of a sequence whose full latent of
  * s_kv tokens is given (a simulated sequence-parallel rank when q_offset > 0).
  * Heads [head_begin, head_begin+head_count) are computed; per-head K_nope/V are
- * rebuilt head_shard heads at a time (0 = all at once) into the workspace, so the
- * workspace grows with head_shard, not with head_count.
+ * rebuilt head_shard heads at a time (0 = all at once) into the workspace, so the K/V
+ * part of the workspace grows with head_shard, not with head_count; the rest (the
+ * normalised latent, the rotated RoPE bands of the keys and of every query row and
+ * head, the RoPE table and, on the tensor-core path, an fp16 copy of the call's
+ * W_kv_b rows) grows with the call's tokens and heads.
  *   q_nope [B, s_q, head_count, d_nope]     q_pe [B, s_q, head_count, d_rope] (not rotated)
  *   c_kv   [B, s_kv, d_kv]                  k_pe [B, s_kv, d_rope] (not rotated)
  *   w_kv_b [n_heads*(d_nope+d_v), d_kv]: head h owns rows h*(d_nope+d_v) ..,
@@ -110,6 +121,28 @@ mla_status mla_absorbed_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, i
                                  const void *c_kv, const void *k_pe, const void *w_kv_b,
                                  const void *rms_w, void *out, float *lse, void *workspace,
                                  size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * Prefill, explicit form with the per-head up-projection fused into the attention
+ * kernel (LAGA page, "Where Pith is reading between the lines": the fused
+ * up-projection that completes LAGA).  Same arguments, layouts and result as
+ * mla_latent_attn_fwd, without head_shard: K_nope and V are rebuilt from the
+ * normalised latent 64 keys at a time inside the attention kernel, each rebuilt tile
+ * shared through distributed shared memory by a cluster of 4 or 8 query tiles of its
+ * head, and never written to device memory.  The workspace
+ * (mla_latent_attn_fused_workspace) holds only the normalised latent, the rotated RoPE
+ * bands, the RoPE table and an fp16 copy of the call's W_kv_b rows.  Each key tile is
+ * rebuilt once per cluster rather than once per call, so the call does more tensor
+ * work than mla_latent_attn_fwd in exchange for no K/V intermediates.
+ * Needs bf16 and d_kv = 512, d_nope = d_v = 128, d_rope = 64 (MLA_ERR_UNSUPPORTED
+ * otherwise, nothing launched).
+ */
+mla_status mla_latent_attn_fused_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
+                                     int q_offset, int causal, int head_begin, int head_count,
+                                     const void *q_nope, const void *q_pe, const void *c_kv,
+                                     const void *k_pe, const void *w_kv_b, const void *rms_w, void *out,
+                                     float *lse, void *workspace, size_t workspace_bytes,
+                                     void *cuda_stream);
 
 /*
  * Decode over a latent cache: one query per sequence at position kv_len-1, all
@@ -194,6 +227,8 @@ size_t mla_latent_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, i
                                  int q_offset, int causal, int head_count, int head_shard);
 size_t mla_absorbed_attn_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
                                    int q_offset, int causal, int head_count, int head_shard);
+size_t mla_latent_attn_fused_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
+                                       int q_offset, int causal, int head_count);
 size_t mla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv_len, int n_splits);
 size_t mla_tpla_decode_workspace(const mla_dims *dims, mla_dtype dtype, int B, int kv_len,
                                  int n_splits, int n_shards);
@@ -211,15 +246,34 @@ const char *mla_status_string(mla_status status);
 mla_status mla_check_device_error(void *cuda_stream);
 
 /*
+ * Self-test of the bounded device wait behind MLA_ERR_DEVICE_TIMEOUT (the pages have
+ * no counterpart).  Launches one tiny kernel on `cuda_stream` in which one thread waits,
+ * with the library's bounded mbarrier wait and a limit of limit_us microseconds, on an
+ * mbarrier that no thread ever arrives at; no copy, MMA or tensor-memory allocation is
+ * in flight.  The wait runs out (within about limit_us plus up to 64 ms of polling),
+ * records the timeout in the device error word and the kernel returns, so the context
+ * stays usable.  The next mla_check_device_error on that stream then returns
+ * MLA_ERR_DEVICE_TIMEOUT (and clears the word).  1 <= limit_us <= 100000, else
+ * MLA_ERR_SHAPE with nothing launched.
+ */
+mla_status mla_selftest_bounded_wait(unsigned limit_us, void *cuda_stream);
+
+/*
  * Which kernel family the last call on this host thread used, for tests and the
  * benchmark: 0 = none yet, 1 = SIMT (CUDA cores, any dimensions, fp32 or bf16),
- * 2 = tensor cores (tcgen05 + TMA, bf16 at the DeepSeek dimensions).
+ * 2 = tensor cores (tcgen05 + TMA, bf16 at the DeepSeek dimensions), 3 = the fused
+ * tensor-core prefill of mla_latent_attn_fused_fwd.
  */
 int mla_last_path(void);
 
 /* Overrides the path choice on this host thread: 0 = automatic (default),
  * 1 = force the SIMT kernels.  Used by tests to compare the two families. */
 void mla_set_path_override(int mode);
+
+/* Query tiles per cluster of the fused prefill on this host thread: 4 or 8; anything
+ * else = chosen per call (8 when the call has at least 8 query tiles).  For tests and
+ * tuning. */
+void mla_set_fused_cluster(int size);
 
 /*
  * Split-KV decode that allocates nothing.  The pages have no counterpart: this is
@@ -235,7 +289,10 @@ void mla_set_path_override(int mode);
  *    returns MLA_ERR_WORKSPACE and launches nothing.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream
- *    capture begins.
+ *    capture begins.  The address is kept for the life of the process: after a
+ *    cudaDeviceReset (or anything else that destroys and recreates the device's
+ *    primary context) it is stale, so do not call this entry point on that device
+ *    again in the same process.
  *  - Every call shares the one array and leaves its contents behind.  Nothing in it
  *    needs to start at zero: each call writes all the scratch it reads.  Calls
  *    that overlap on the GPU (other streams, other host threads) race on it;
@@ -260,7 +317,7 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   for an unknown name).  Names: "prep", "latent_prep", "rope_table", "rope_rows",
  *   "convert", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
  *   "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
- *   "tpla_combine".
+ *   "tpla_combine", "wait_probe", "tc_fused_attn".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
  * Not thread-safe: profile from one host thread at a time.
  */

@@ -33,7 +33,7 @@
  *    partial attention outputs plus log-sum-exp scalars are rescaled and summed to
  *    give the exact softmax output (the Flash-Decoding combine).
  *
- * Readings where the pages are silent (each one is listed in the design notes):
+ * Readings where the pages are silent:
  *  - RMSNorm: y = x * w / sqrt(mean(x^2) + eps), no mean subtraction, no bias;
  *    applied to c_KV only, never to k_pe.
  *  - RoPE: half-split pairing (t, t + d_rope/2), theta_t = base^(-2t/d_rope);
@@ -592,8 +592,7 @@ void orc_mla_explicit_bwd(int B, int s_q, int s_kv, int q_off, int causal,
  * input dimension are split into g shards; every shard attends with all query heads over
  * its own part of the latent (a local softmax over its own scores) and the shards'
  * outputs are summed (the all-reduce).  The page calls the result a grouped latent
- * attention with replicated heads.  Readings where the page is silent (each one is in
- * the design notes):
+ * attention with replicated heads.  Readings where the page is silent:
  *  - no orthogonal reparameterisation (U = I): its Hadamard and PCA forms need
  *    calibration data;
  *  - shard i owns latent dims [i Dk/g, (i+1) Dk/g) and normalises them by its own

@@ -233,3 +233,8 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         mla.lib()
+
+
+@pytest.mark.parametrize("limit_us", [0, 100001, 1 << 31])
+def test_selftest_wait_limit_checked_before_launch(L, limit_us):
+    assert mla.mla_selftest_bounded_wait(limit_us, None) == -2

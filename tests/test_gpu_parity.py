@@ -114,6 +114,7 @@ def test_ragged_bf16(oracle, absorbed):
     inp = inputs.prefill_inputs(cfg)
     sub = dict(inp, q_nope=inp["q_nope"][:, :, 2:7].contiguous(), q_pe=inp["q_pe"][:, :, 2:7].contiguous())
     o, l = run_prefill(cfg, dev(sub), absorbed=absorbed, head_begin=2)
+    assert mla.last_path() == mla.PATH_TC
     ro, rl = oracle_prefill(oracle, cfg, sub, absorbed=absorbed, head_begin=2)
     check_out(o, ro, torch.bfloat16)
     check_lse(l, rl)
@@ -157,14 +158,36 @@ def test_v3_sampled_heads_and_absorbed(oracle):
     inp = inputs.prefill_inputs(cfg)
     d_in = dev(inp)
     o, l = run_prefill(cfg, d_in)
+    assert mla.last_path() == mla.PATH_TC
+    oa, la = run_prefill(cfg, d_in, absorbed=True)
+    assert mla.last_path() == mla.PATH_TC
+    # the sampled heads of both forms against the oracle (its explicit and absorbed forms
+    # agree to 1e-10 in fp64: tests/test_oracle_pins.py), plus the whole of both outputs
+    # against each other
     for h0, hc in ((0, 2), (77, 1), (127, 1)):
         sub = dict(inp, q_nope=inp["q_nope"][:, :, h0:h0 + hc], q_pe=inp["q_pe"][:, :, h0:h0 + hc])
         ro, rl = oracle_prefill(oracle, cfg, sub, head_begin=h0)
         check_out(o[:, :, h0:h0 + hc], ro, torch.bfloat16, "v3 heads %d+%d" % (h0, hc))
         check_lse(l[:, h0:h0 + hc], rl)
-    oa, la = run_prefill(cfg, d_in, absorbed=True)
+        check_out(oa[:, :, h0:h0 + hc], ro, torch.bfloat16, "v3 absorbed heads %d+%d" % (h0, hc))
+        check_lse(la[:, h0:h0 + hc], rl, "v3 absorbed lse")
     check_out(oa, o.float(), torch.bfloat16, "absorbed vs explicit")
     check_lse(la, l)
+
+
+def test_v3_absorbed_sampled_rows_against_absorbed_oracle(oracle):
+    """The absorbed V3 call's rows near the causal diagonal and at the end of the
+    sequence, two heads, against the oracle's own absorbed form."""
+    cfg = configs.V3
+    d_in = dev(inputs.prefill_inputs(cfg))
+    oa, la = run_prefill(cfg, d_in, absorbed=True)
+    assert mla.last_path() == mla.PATH_TC
+    for q0, n, h0 in ((100, 56, 5), (cfg.s_kv - 40, 40, 126)):
+        inp = inputs.prefill_inputs(cfg, q_rows=(q0, q0 + n))
+        sub = dict(inp, q_nope=inp["q_nope"][:, :, h0:h0 + 1], q_pe=inp["q_pe"][:, :, h0:h0 + 1])
+        ro, rl = oracle_prefill(oracle, cfg, sub, absorbed=True, q_offset=q0, head_begin=h0)
+        check_out(oa[:, q0:q0 + n, h0:h0 + 1], ro, torch.bfloat16, "absorbed rows %d head %d" % (q0, h0))
+        check_lse(la[:, h0:h0 + 1, q0:q0 + n], rl, "absorbed lse rows %d head %d" % (q0, h0))
 
 
 def test_v3_activation_memory_explicit_below_absorbed():
@@ -198,7 +221,21 @@ def test_sp8_rank_sweep_concatenates_and_matches_oracle(oracle):
         lses.append(l)
     assert torch.equal(torch.cat(outs, 1), full_o), "rank outputs do not concatenate to SP=1"
     assert torch.equal(torch.cat(lses, 2), full_l)
-    # oracle on sampled rows/heads of the last rank (query offset 14336)
+    # every rank against the oracle: 64 rows straddling the boundary between two of the
+    # rank's 128-row query tiles (so both tiles' diagonal key tiles are in play), four
+    # heads spread over the head shards
+    for r, off in enumerate(cfg.sweep_offsets):
+        k = 1 + (5 * r) % 15
+        q0, n = off + 128 * k - 32, 64
+        heads = sorted({(37 * r + dh) % cfg.n_heads for dh in (0, 41, 83, 127)})
+        inp = inputs.prefill_inputs(cfg, q_rows=(q0, q0 + n))
+        for h0 in heads:
+            sub = dict(inp, q_nope=inp["q_nope"][:, :, h0:h0 + 1], q_pe=inp["q_pe"][:, :, h0:h0 + 1])
+            ro, rl = oracle_prefill(oracle, cfg, sub, q_offset=q0, head_begin=h0)
+            i0 = q0 - off
+            check_out(outs[r][:, i0:i0 + n, h0:h0 + 1], ro, torch.bfloat16, "rank %d rows %d head %d" % (r, q0, h0))
+            check_lse(lses[r][:, h0:h0 + 1, i0:i0 + n], rl, "rank %d lse rows %d head %d" % (r, q0, h0))
+    # and sampled rows/heads of the last rank (query offset 14336), its end included
     rank7 = outs[-1]
     for q0, h0 in ((cfg.q_offset, 0), (cfg.q_offset + 1000, 64), (S - 48, 127)):
         n = 48
@@ -289,6 +326,7 @@ def test_tensor_core_path_matches_simt_path(absorbed):
     d_in = dev(inputs.prefill_inputs(cfg))
     o_tc, l_tc = run_prefill(cfg, d_in, absorbed=absorbed)
     path_tc = mla.last_path()
+    assert path_tc == mla.PATH_TC
     mla.set_path_override(1)
     try:
         o_s, l_s = run_prefill(cfg, d_in, absorbed=absorbed)
@@ -366,6 +404,26 @@ def test_tpla_one_shard_is_plain_decode():
     o1, sl = run_tpla(cfg, inp, 1)
     o, l, _, _ = run_decode(cfg, inp, cfg.n_splits, partials=False)
     assert torch.equal(o1, o) and torch.equal(sl[0], l)
+
+
+def test_tpla_shard_decodes_sum_to_the_two_shard_decode():
+    """What two tensor-parallel ranks would each compute and then all-reduce: each latent
+    shard decoded on its own by the product call (a one-shard TPLA decode over the shard's
+    latent columns and the matching W_kv_b columns, the RoPE band whole), the two outputs
+    added, equals the two-shard TPLA decode; each shard's LSE is its shard LSE."""
+    cfg = tpla_cfg("bf16", 1000, 4)
+    inp = dev(inputs.decode_inputs(cfg))
+    o2, sl2 = run_tpla(cfg, inp, 2)
+    ds = cfg.d_kv // 2
+    scfg = dataclasses.replace(cfg, d_kv=ds)
+    total = torch.zeros_like(o2, dtype=torch.float32)
+    for i in range(2):
+        sub = dict(inp, c_cache=inp["c_cache"][..., i * ds:(i + 1) * ds].contiguous(),
+                   w_kv_b=inp["w_kv_b"][:, i * ds:(i + 1) * ds].contiguous())
+        o, sl = run_tpla(scfg, sub, 1)
+        total += o.float()
+        check_lse(sl[0], sl2[i], "shard %d lse" % i)
+    check_out(o2, total, torch.bfloat16, "sum of shard decodes")
 
 
 def test_tpla_tensor_core_path_matches_simt_path():
@@ -459,3 +517,52 @@ def test_rmsnorm_bwd_no_rows_zeroes_dw():
     mla.rmsnorm_bwd(x, w, x, dw=dw)
     torch.cuda.synchronize()
     assert torch.count_nonzero(dw).item() == 0
+
+
+# ------------------------------------------------ inputs far from unit scale ----
+def _scaled(inp, q=1.0, w=1.0):
+    out = dict(inp)
+    out["q_nope"] = (inp["q_nope"].float() * q).to(torch.bfloat16)
+    out["q_pe"] = (inp["q_pe"].float() * q).to(torch.bfloat16)
+    out["rms_w"] = (inp["rms_w"].float() * w).to(torch.bfloat16)
+    return out
+
+
+LARGE = configs.Prefill("large_bf16", "bf16", batch=1, s_kv=600, s_q=600, q_offset=0, n_heads=4, d_kv=512,
+                        d_nope=128, d_rope=64, d_v=128, head_shard=4)
+
+
+@pytest.mark.parametrize("absorbed", [False, True])
+def test_large_scores_on_the_simt_route(oracle, absorbed):
+    """q x 100 and a norm weight of 8 (scores up to ~3000): the CUDA-core kernels, which
+    keep fp32 intermediates (selected with mla_set_path_override(1), the route include/mla.h
+    names for scores this large), meet the bars scaled to the magnitudes: bf16 output
+    rounding grows with |out| and fp32 score rounding with |score|."""
+    inp = _scaled(inputs.prefill_inputs(LARGE), q=100.0, w=8.0)
+    ro, rl = oracle_prefill(oracle, LARGE, inp, absorbed=absorbed)
+    mla.set_path_override(1)
+    try:
+        o, l = run_prefill(LARGE, dev(inp), absorbed=absorbed)
+        assert mla.last_path() == mla.PATH_SIMT
+    finally:
+        mla.set_path_override(0)
+    g, r = to64(o), ro
+    assert np.all(np.isfinite(g))
+    assert np.abs(g - r).max() <= 3e-2 * max(1.0, np.abs(r).max())
+    assert np.linalg.norm(g - r) / np.linalg.norm(r) <= 1e-2
+    assert np.abs(to64(l) - rl).max() <= 1e-3 * max(1.0, np.abs(rl).max() / 300.0)
+
+
+@pytest.mark.parametrize("qs,ws", [(1.0, 1.0), (4.0, 4.0), (100.0, 8.0)])
+def test_tensor_core_error_grows_with_the_scores_as_documented(oracle, qs, ws):
+    """The tensor-core path's score operands are fp16 (11-bit significand): its LSE error
+    is bounded by about 2^-11 of the largest |lse| (include/mla.h), its outputs stay finite
+    and within 1e-2 relative L2.  At unit scale that bound is inside the 1e-3 bar."""
+    inp = _scaled(inputs.prefill_inputs(LARGE), q=qs, w=ws)
+    ro, rl = oracle_prefill(oracle, LARGE, inp)
+    o, l = run_prefill(LARGE, dev(inp))
+    assert mla.last_path() == mla.PATH_TC
+    g = to64(o)
+    assert np.all(np.isfinite(g)) and np.all(np.isfinite(to64(l)))
+    assert np.linalg.norm(g - ro) / np.linalg.norm(ro) <= 1e-2
+    assert np.abs(to64(l) - rl).max() <= 2.0 ** -11 * max(2.0, np.abs(rl).max())

@@ -55,4 +55,7 @@ def test_planted_mistake_is_caught(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, "pins did not catch mutation %s:\n%s" % (name, r.stdout[-2000:])
+    # caught = a test FAILED (pytest exit code 1), not a collection error or a crash
+    tail = r.stdout.strip().splitlines()[-1] if r.stdout.strip() else ""
+    assert r.returncode == 1, "pins did not catch mutation %s (rc %d):\n%s" % (name, r.returncode, r.stdout[-2000:])
+    assert " failed" in tail and "error" not in tail, "mutation %s: %s" % (name, tail)
