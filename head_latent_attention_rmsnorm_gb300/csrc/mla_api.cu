@@ -619,9 +619,170 @@ mla_status prefill_entry(bool absorbed, const mla_dims *dims, mla_dtype dtype, i
                     : explicit_simt(p, scale, q_nope, w_kv_b, out, lse, w, cs);
 }
 
+// ------------------------------------------------------------------ backward ----
+struct BwdWs {
+    PrefillWs f;   // the forward's recomputed intermediates (K / V per head shard)
+    float *D, *dqr, *dK, *dV, *dkr, *dkr_acc, *dchat, *rms_part;
+    size_t bytes;
+};
+
+BwdWs bwd_ws(const Prefill &p, void *base) {
+    BwdWs w{};
+    w.f = prefill_ws(p, false, base);
+    Carve c;
+    c.base = (char *)base;
+    c.off = w.f.bytes;
+    const size_t nq = (size_t)p.B * p.s_q * p.head_count;
+    w.D = (float *)c.take(nq * 4);
+    w.dqr = (float *)c.take(nq * p.Dr * 4);
+    w.dK = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dn * 4);
+    w.dV = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dv * 4);
+    w.dkr = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dr * 4);
+    w.dkr_acc = (float *)c.take((size_t)p.B * p.kv_pad * p.Dr * 4);
+    w.dchat = (float *)c.take((size_t)p.B * p.kv_pad * p.Dk * 4);
+    w.rms_part = (float *)c.take(rms_bwd_parts(p.s_kv) * p.Dk * 4);
+    w.bytes = align_up(c.off, 256);
+    return w;
+}
+
+mla_status bwd_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_kv, int q_offset, int causal,
+                     int head_begin, int head_count, int head_shard, Prefill *p) {
+    mla_status st = prefill_shape(d, dt, B, s_q, s_kv, q_offset, causal, head_begin, head_count, head_shard, false, p);
+    if (st != MLA_OK) return st;
+    if (!bwd_simt_supported(p->Dn, p->Dr, p->Dv)) return MLA_ERR_UNSUPPORTED;
+    p->tc = false;   // the backward's recomputed intermediates are fp32
+    p->tmid = TY_F32;
+    return MLA_OK;
+}
+
+// The backward on the CUDA-core kernels: recompute the forward's normalised latent,
+// rotated bands and per-shard K / V, then per head shard the attention backward, the
+// weight gradients (dW = dKV^T chat, summed over the batch) and the latent gradient
+// (dchat += dKV W); finally the rotations' transposes and the RMSNorm backward.
+mla_status bwd_simt(const Prefill &p, const mla_dims *d, float scale, const void *q_nope, const void *q_pe,
+                    const void *c_kv, const void *k_pe, const void *w_kv_b, const void *rms_w, const void *out,
+                    const float *lse, const void *dout, void *dq_nope, void *dq_pe, void *dc_kv, void *dk_pe,
+                    float *dw_kv_b, float *drms_w, const BwdWs &w, cudaStream_t st) {
+    const long Dh = p.Dn + p.Dv, kvn = p.kv_need;
+    const size_t ein = ty_size(p.tin);
+    mla_status ms = prefill_prep(p, false, d, q_pe, c_kv, k_pe, w_kv_b, rms_w, w.f, st);
+    if (ms != MLA_OK) return ms;
+    MLA_TRY(launch_bwd_rowdot(p.tin, p.B, p.s_q, p.head_count, p.Dv, dout, out, w.D, st));
+    for (int s = 0; s < p.n_shards; ++s) {
+        const int h0 = s * p.hs, nh = std::min(p.hs, p.head_count - h0);
+        const long hg = p.head_begin + h0;
+        for (int part = 0; part < 2; ++part) {   // this shard's K_nope, V (fp32)
+            GemmArgs g{};
+            const int Dp = part == 0 ? p.Dn : p.Dv;
+            g.M = (int)kvn; g.N = Dp; g.K = p.Dk; g.nzb = p.B; g.nzh = nh;
+            g.A = w.f.chat; g.ta = p.tmid; g.a_zb = p.kv_pad * p.Dk; g.a_m = p.Dk; g.a_k = 1;
+            g.B = (const char *)w_kv_b + ((hg * Dh + (part ? p.Dn : 0)) * p.Dk) * ein;
+            g.tb = p.tin; g.b_zh = Dh * p.Dk; g.b_n = p.Dk; g.b_k = 1;
+            g.C = part == 0 ? w.f.k : w.f.v; g.tc = p.tmid; g.c_zh = kvn * Dp; g.c_zb = (long)p.hs * g.c_zh;
+            g.c_m = Dp; g.c_n = 1;
+            MLA_TRY(launch_gemm_simt(g, st));
+        }
+        BwdSimtArgs a{};
+        a.B = p.B; a.s_q = p.s_q; a.hc = p.head_count; a.h0 = h0; a.nh = nh;
+        a.Dn = p.Dn; a.Dr = p.Dr; a.Dv = p.Dv; a.kv = kvn; a.kv_pad = p.kv_pad;
+        a.causal = p.causal; a.q_off = p.q_offset; a.scale = scale; a.ty = p.tin;
+        a.q_nope = q_nope; a.qr = (const float *)w.f.qpe; a.kr = (const float *)w.f.kpe;
+        a.K = (const float *)w.f.k; a.V = (const float *)w.f.v;
+        a.k_b = (long)p.hs * kvn * p.Dn; a.k_h = kvn * p.Dn; a.v_b = (long)p.hs * kvn * p.Dv; a.v_h = kvn * p.Dv;
+        a.lse = lse; a.D = w.D; a.dout = dout; a.dq_nope = dq_nope; a.dqr = w.dqr;
+        a.dK = w.dK; a.dV = w.dV; a.dkr = w.dkr;
+        MLA_TRY(launch_attn_bwd_simt(a, st));
+        // dW_K(h) = dK^T chat and dW_V(h) = dV^T chat, summed over the batch
+        for (int part = 0; part < 2; ++part)
+            for (int b = 0; b < p.B; ++b) {
+                GemmArgs g{};
+                const int Dp = part == 0 ? p.Dn : p.Dv;
+                g.M = Dp; g.N = p.Dk; g.K = (int)kvn; g.nzb = 1; g.nzh = nh;
+                g.A = (part == 0 ? w.dK : w.dV) + (size_t)b * nh * kvn * Dp; g.ta = TY_F32;
+                g.a_zh = kvn * Dp; g.a_m = 1; g.a_k = Dp;
+                g.B = (const char *)w.f.chat + (size_t)b * p.kv_pad * p.Dk * 4; g.tb = p.tmid;
+                g.b_n = 1; g.b_k = p.Dk;
+                g.C = dw_kv_b + (size_t)(hg * Dh + (part ? p.Dn : 0)) * p.Dk; g.tc = TY_F32;
+                g.c_zh = Dh * p.Dk; g.c_m = p.Dk; g.c_n = 1;
+                g.accumulate = b > 0;
+                MLA_TRY(launch_gemm_simt(g, st));
+            }
+        // dchat += dK W_K(h) + dV W_V(h), head by head (a fixed order)
+        for (int hl = 0; hl < nh; ++hl)
+            for (int part = 0; part < 2; ++part) {
+                GemmArgs g{};
+                const int Dp = part == 0 ? p.Dn : p.Dv;
+                g.M = (int)kvn; g.N = p.Dk; g.K = Dp; g.nzb = p.B; g.nzh = 1;
+                g.A = (part == 0 ? w.dK : w.dV) + (size_t)hl * kvn * Dp; g.ta = TY_F32;
+                g.a_zb = (long)nh * kvn * Dp; g.a_m = Dp; g.a_k = 1;
+                g.B = (const char *)w_kv_b + (((hg + hl) * Dh + (part ? p.Dn : 0)) * p.Dk) * ein; g.tb = p.tin;
+                g.b_n = 1; g.b_k = p.Dk;
+                g.C = w.dchat; g.tc = TY_F32; g.c_zb = p.kv_pad * p.Dk; g.c_m = p.Dk; g.c_n = 1;
+                g.accumulate = !(s == 0 && hl == 0 && part == 0);
+                MLA_TRY(launch_gemm_simt(g, st));
+            }
+        MLA_TRY(launch_head_sum(p.B, nh, kvn, p.Dr, p.kv_pad, w.dkr, w.dkr_acc, s > 0, st));
+    }
+    // the rotations' transposes: dq_pe at the query positions, dk_pe at the keys (zeros past kv_need)
+    const long nq = (long)p.B * p.s_q * p.head_count;
+    MLA_TRY(launch_rope_inv(nq, p.Dr, w.dqr, p.Dr, p.q_offset, p.head_count, p.s_q, 1L << 40, w.f.rtab, dq_pe,
+                            p.tin, p.Dr, st));
+    for (int b = 0; b < p.B; ++b) {
+        MLA_TRY(launch_rope_inv(p.s_kv, p.Dr, w.dkr_acc + (size_t)b * p.kv_pad * p.Dr, p.Dr, 0, 1, 1L << 40, kvn,
+                                w.f.rtab, (char *)dk_pe + (size_t)b * p.s_kv * p.Dr * ein, p.tin, p.Dr, st));
+        MLA_TRY(launch_rms_bwd_f32dy(p.tin, kvn, p.s_kv, p.Dk, d->rms_eps, (const char *)c_kv + (size_t)b * p.s_kv * p.Dk * ein,
+                                     rms_w, w.dchat + (size_t)b * p.kv_pad * p.Dk,
+                                     (char *)dc_kv + (size_t)b * p.s_kv * p.Dk * ein, drms_w, b > 0, w.rms_part, st));
+    }
+    return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t mla_latent_attn_bwd_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                                     int causal, int head_count, int head_shard) {
+    Prefill p;
+    if (bwd_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, 0, head_count, head_shard, &p) != MLA_OK) return 0;
+    if (B == 0 || s_q == 0 || head_count == 0) return 0;
+    return bwd_ws(p, nullptr).bytes;
+}
+
+mla_status mla_latent_attn_bwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
+                               int causal, int head_begin, int head_count, int head_shard, const void *q_nope,
+                               const void *q_pe, const void *c_kv, const void *k_pe, const void *w_kv_b,
+                               const void *rms_w, const void *out, const float *lse, const void *dout,
+                               void *dq_nope, void *dq_pe, void *dc_kv, void *dk_pe, float *dw_kv_b,
+                               float *drms_w, void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    Prefill p;
+    mla_status st = bwd_shape(dims, dtype, B, s_q, s_kv, q_offset, causal, head_begin, head_count, head_shard, &p);
+    if (st != MLA_OK) return st;
+    if (B == 0 || s_q == 0 || head_count == 0) return MLA_OK;
+    const void *ptrs[] = {q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, dout,
+                          dq_nope, dq_pe, dc_kv, dk_pe, dw_kv_b, drms_w, workspace};
+    for (const void *q : ptrs)
+        if (!q) return MLA_ERR_NULL;
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return MLA_ERR_ALIGN;
+    const BwdWs wsz = bwd_ws(p, nullptr);
+    if (workspace_bytes < wsz.bytes) return MLA_ERR_WORKSPACE;
+    const size_t es = ty_size(p.tin), nq = (size_t)p.B * p.s_q * p.head_count;
+    const size_t nw = (size_t)p.H * (p.Dn + p.Dv) * p.Dk;
+    Range in[] = {rng(q_nope, nq * p.Dn * es), rng(q_pe, nq * p.Dr * es), rng(c_kv, (size_t)p.B * p.s_kv * p.Dk * es),
+                  rng(k_pe, (size_t)p.B * p.s_kv * p.Dr * es), rng(w_kv_b, nw * es), rng(rms_w, (size_t)p.Dk * es),
+                  rng(out, nq * p.Dv * es), rng(lse, nq * 4), rng(dout, nq * p.Dv * es)};
+    Range outs[] = {rng(dq_nope, nq * p.Dn * es), rng(dq_pe, nq * p.Dr * es),
+                    rng(dc_kv, (size_t)p.B * p.s_kv * p.Dk * es), rng(dk_pe, (size_t)p.B * p.s_kv * p.Dr * es),
+                    rng(dw_kv_b, nw * 4), rng(drms_w, (size_t)p.Dk * 4), rng(workspace, wsz.bytes)};
+    st = check_alias(in, 9, outs, 7);
+    if (st != MLA_OK) return st;
+    cudaStream_t cs = (cudaStream_t)cuda_stream;
+    const BwdWs w = bwd_ws(p, workspace);
+    g_last_path = 1;
+    return bwd_simt(p, dims, scale_of(dims), q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, dout, dq_nope, dq_pe,
+                    dc_kv, dk_pe, dw_kv_b, drms_w, w, cs);
+}
 
 mla_status mla_latent_attn_fwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv, int q_offset,
                                int causal, int head_begin, int head_count, int head_shard, const void *q_nope,

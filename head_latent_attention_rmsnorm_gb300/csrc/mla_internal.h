@@ -65,6 +65,7 @@ struct GemmArgs {
     const void *A; int ta; long a_zb, a_zh, a_m, a_k;
     const void *B; int tb; long b_zb, b_zh, b_n, b_k;
     void *C; int tc; long c_zb, c_zh, c_m, c_n;
+    int accumulate;   // 1: C += A B^T (C read in its storage type), 0: C = A B^T
 };
 cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t st);
 
@@ -119,6 +120,45 @@ cudaError_t launch_tpla_combine(int tout, int n, int B, int H, int g, int Dk, co
 // One-thread kernel whose bounded mbarrier wait (limit_ns) runs out by construction and
 // records the timeout in the device error word (the self-test of that mechanism).
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st);
+
+// ------------------------------------------------------------------ backward ----
+// D[b][h][i] = dO[b][i][h] . out[b][i][h] (fp32 [B][hc][s_q]).
+cudaError_t launch_bwd_rowdot(int ty, int B, int s_q, int hc, int Dv, const void *dout, const void *out, float *D,
+                              cudaStream_t st);
+// CUDA-core attention backward of one head shard (heads h0 .. h0 + nh of the call):
+// dq_nope (storage ty) and the rotated dq (fp32) of every query row, dK / dV / this
+// shard's per-head dk_rot (fp32 [B][nh][kv][..]) of every key below kv.  K / V fp32 with
+// batch and head strides; qr, kr fp32 (the forward's rotated bands); lse, D fp32.
+struct BwdSimtArgs {
+    int B, s_q, hc, h0, nh, Dn, Dr, Dv;
+    long kv, kv_pad;
+    int causal;
+    long q_off;
+    float scale;
+    int ty;
+    const void *q_nope;
+    const float *qr, *K, *V, *kr, *lse, *D;
+    long k_b, k_h, v_b, v_h;
+    const void *dout;
+    void *dq_nope;
+    float *dqr, *dK, *dV, *dkr;
+};
+bool bwd_simt_supported(int Dn, int Dr, int Dv);
+cudaError_t launch_attn_bwd_simt(const BwdSimtArgs &a, cudaStream_t st);
+// acc[b][j][:] (+)= sum_hl part[b][hl][j][:] for j < kv (acc row pitch acc_pitch rows).
+cudaError_t launch_head_sum(int B, int nh, long kv, int Dr, long acc_pitch, const float *part, float *acc,
+                            bool accumulate, cudaStream_t st);
+// y = RoPE(x, -pos) (the transpose of the forward rotation), rows at positions
+// pos0 + (r / pos_div) % pos_mod, zeros at positions >= pos_end; tab from position 0.
+cudaError_t launch_rope_inv(long rows, int Dr, const float *x, long x_pitch, long pos0, long pos_div, long pos_mod,
+                            long pos_end, const float2 *tab, void *y, int ty, long y_pitch, cudaStream_t st);
+// RMSNorm backward of one batch's latent rows with an fp32 upstream gradient: dx for rows
+// < n_rows, zeros for rows [n_rows, s_kv); dw (fp32) set or accumulated in a fixed order.
+// part: fp32 scratch of rms_bwd_parts(s_kv) * Dk floats.
+size_t rms_bwd_parts(long s_kv);
+cudaError_t launch_rms_bwd_f32dy(int ty, long n_rows, long s_kv, int Dk, float eps, const void *x, const void *w,
+                                 const float *dy, void *dx, float *dw, bool accumulate, float *part,
+                                 cudaStream_t st);
 
 // Reads and clears the bounded-wait error words of the tensor-core kernels.
 cudaError_t tc_read_and_clear_error(unsigned int *flags, cudaStream_t st);

@@ -373,7 +373,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             int m = m0 + ty + 16 * i, n = n0 + tx + 16 * j;
-            if (m < g.M && n < g.N) stx(g.C, g.tc, co + m * g.c_m + n * g.c_n, acc[i][j]);
+            if (m < g.M && n < g.N) {
+                const long o = co + m * g.c_m + n * g.c_n;
+                stx(g.C, g.tc, o, g.accumulate ? ldx(g.C, g.tc, o) + acc[i][j] : acc[i][j]);
+            }
         }
 }
 

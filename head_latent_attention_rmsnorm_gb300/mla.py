@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
         L.mla_latent_attn_fused_workspace.restype = _sz
         L.mla_set_fused_cluster.argtypes = [_i]
         L.mla_set_fused_cluster.restype = None
+        L.mla_latent_attn_bwd.argtypes = [D, _i, _i, _i, _i, _i, _i, _i, _i, _i] + [_vp] * 15 + [_vp, _sz, _vp]
+        L.mla_latent_attn_bwd.restype = _i
+        L.mla_latent_attn_bwd_workspace.argtypes = [D, _i, _i, _i, _i, _i, _i, _i, _i]
+        L.mla_latent_attn_bwd_workspace.restype = _sz
         L.mla_decode_splitkv.argtypes = [D, _i, _i, _i, _i] + [_vp] * 9 + [_vp, _sz, _vp]
         L.mla_decode_splitkv.restype = _i
         L.mla_decode_splitkv_noalloc.argtypes = [D, _i, _i, _i, _i] + [_vp] * 7 + [_vp]
@@ -133,6 +137,14 @@ def mla_latent_attn_fused_fwd(*args) -> int:
 
 def mla_latent_attn_fused_workspace(*args) -> int:
     return lib().mla_latent_attn_fused_workspace(*args)
+
+
+def mla_latent_attn_bwd(*args) -> int:
+    return lib().mla_latent_attn_bwd(*args)
+
+
+def mla_latent_attn_bwd_workspace(*args) -> int:
+    return lib().mla_latent_attn_bwd_workspace(*args)
 
 
 def mla_decode_splitkv(*args) -> int:
@@ -204,7 +216,7 @@ def set_path_override(mode: int) -> None:
 
 KERNELS = ("prep", "latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
            "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
-           "tpla_combine", "wait_probe", "tc_fused_attn")
+           "tpla_combine", "wait_probe", "tc_fused_attn", "bwd_rowdot", "attn_bwd_simt", "bwd_rows")
 
 
 def launch_count() -> int:
@@ -314,6 +326,33 @@ def latent_attn_fused_fwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, q
                                    _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "mla_latent_attn_fused_fwd")
     return out, lse
+
+
+def latent_attn_bwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, dout, *, q_offset=0, causal=True,
+                    head_begin=0, head_shard=0, grads=None, workspace=None, stream=None):
+    """Backward of :func:`latent_attn_fwd` for an upstream gradient ``dout`` of its output.
+    Returns a dict of gradients: q_nope, q_pe, c_kv, k_pe (input dtype), w_kv_b, rms_w
+    (fp32; w_kv_b rows outside the call's heads are zero when this call allocates it)."""
+    B, s_q, hc, _ = q_nope.shape
+    s_kv = c_kv.shape[1]
+    dt = _dt(q_nope)
+    dev = q_nope.device
+    g = grads or {}
+    g.setdefault("q_nope", torch.empty_like(q_nope))
+    g.setdefault("q_pe", torch.empty_like(q_pe))
+    g.setdefault("c_kv", torch.empty_like(c_kv))
+    g.setdefault("k_pe", torch.empty_like(k_pe))
+    g.setdefault("w_kv_b", torch.zeros(w_kv_b.shape, dtype=torch.float32, device=dev))
+    g.setdefault("rms_w", torch.empty(rms_w.shape, dtype=torch.float32, device=dev))
+    nbytes = mla_latent_attn_bwd_workspace(ctypes.byref(d), dt, B, s_q, s_kv, q_offset, int(causal), hc, head_shard)
+    ws = _workspace(nbytes, dev, workspace)
+    st = mla_latent_attn_bwd(ctypes.byref(d), dt, B, s_q, s_kv, q_offset, int(causal), head_begin, hc, head_shard,
+                             _ptr(q_nope), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe), _ptr(w_kv_b), _ptr(rms_w), _ptr(out),
+                             _ptr(lse), _ptr(dout), _ptr(g["q_nope"]), _ptr(g["q_pe"]), _ptr(g["c_kv"]),
+                             _ptr(g["k_pe"]), _ptr(g["w_kv_b"]), _ptr(g["rms_w"]), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "mla_latent_attn_bwd")
+    return g
 
 
 def set_fused_cluster(size: int) -> None:

@@ -145,6 +145,37 @@ mla_status mla_latent_attn_fused_fwd(const mla_dims *dims, mla_dtype dtype, int 
                                      void *cuda_stream);
 
 /*
+ * Backward of mla_latent_attn_fwd (LAGA page, "What carries the argument": the method's
+ * equivalence claim covers gradients).  The chain rule through the forward's own steps:
+ * softmax, scores, the RoPE rotations (whose transposes rotate by the opposite angle),
+ * the per-head reconstruction through W_kv_b, the latent RMSNorm.  Inputs: the forward's
+ * inputs and arguments, its out and lse, and an upstream gradient dout of out
+ * [B, s_q, head_count, d_v] (dtype); lse is not differentiated.  Outputs:
+ *   dq_nope, dq_pe     like q_nope, q_pe (dtype)
+ *   dc_kv, dk_pe       like c_kv, k_pe (dtype): summed over the call's heads; rows of keys
+ *                      that no query of the call sees are zero
+ *   dw_kv_b (fp32)     like w_kv_b: only the rows of heads [head_begin, head_begin +
+ *                      head_count) are written, the others are left as they are
+ *   drms_w (fp32)      [d_kv]
+ * A call over one query shard (q_offset > 0) writes that shard's contributions: the
+ * gradients of c_kv, k_pe, w_kv_b and rms_w of the shards of a sequence add up to those
+ * of one call over the whole sequence.  K/V are recomputed head_shard heads at a time.
+ * Every band (d_nope, d_rope, d_v) up to 256 wide; B, s_q or head_count of 0 is a no-op.
+ * Workspace: mla_latent_attn_bwd_workspace.
+ */
+mla_status mla_latent_attn_bwd(const mla_dims *dims, mla_dtype dtype, int B, int s_q, int s_kv,
+                               int q_offset, int causal, int head_begin, int head_count,
+                               int head_shard, const void *q_nope, const void *q_pe,
+                               const void *c_kv, const void *k_pe, const void *w_kv_b,
+                               const void *rms_w, const void *out, const float *lse,
+                               const void *dout, void *dq_nope, void *dq_pe, void *dc_kv,
+                               void *dk_pe, float *dw_kv_b, float *drms_w, void *workspace,
+                               size_t workspace_bytes, void *cuda_stream);
+size_t mla_latent_attn_bwd_workspace(const mla_dims *dims, mla_dtype dtype, int B, int s_q,
+                                     int s_kv, int q_offset, int causal, int head_count,
+                                     int head_shard);
+
+/*
  * Decode over a latent cache: one query per sequence at position kv_len-1, all
  * n_heads heads, absorbed-form scores, keys split into n_splits contiguous chunks
  * of ceil(kv_len/n_splits) (the last may be short or empty), partials merged by the
@@ -317,7 +348,8 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   for an unknown name).  Names: "prep", "latent_prep", "rope_table", "rope_rows",
  *   "convert", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
  *   "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
- *   "tpla_combine", "wait_probe", "tc_fused_attn".
+ *   "tpla_combine", "wait_probe", "tc_fused_attn", "bwd_rowdot",
+ *   "attn_bwd_simt", "bwd_rows".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
  * Not thread-safe: profile from one host thread at a time.
  */

@@ -238,3 +238,25 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 @pytest.mark.parametrize("limit_us", [0, 100001, 1 << 31])
 def test_selftest_wait_limit_checked_before_launch(L, limit_us):
     assert mla.mla_selftest_bounded_wait(limit_us, None) == -2
+
+
+def test_backward_validates_before_launch(L):
+    d = mla.dims(**V3)
+    base = [ctypes.byref(d), mla.MLA_BF16, 1, 2048, 16384, 14336, 1, 0, 128, 16] + [fake(i) for i in range(1, 16)]
+    ws = mla.mla_latent_attn_bwd_workspace(ctypes.byref(d), mla.MLA_BF16, 1, 2048, 16384, 14336, 1, 128, 16)
+    assert ws > 0
+    args = base + [fake(20), ws, None]
+    bad = list(args)
+    bad[10] = None                                        # q_nope
+    assert mla.mla_latent_attn_bwd(*bad) == -1
+    bad = list(args)
+    bad[19] = fake(19) + 8                                # dq_nope misaligned
+    assert mla.mla_latent_attn_bwd(*bad) == -4
+    bad = list(args)
+    bad[26] = ws - 1                                      # workspace too small
+    assert mla.mla_latent_attn_bwd(*bad) == -5
+    bad = list(args)
+    bad[19] = fake(1)                                     # dq_nope over q_nope
+    assert mla.mla_latent_attn_bwd(*bad) == -9
+    d2 = mla.dims(n_heads=128, d_kv=64, d_nope=300, d_rope=16, d_v=32)
+    assert mla.mla_latent_attn_bwd(ctypes.byref(d2), mla.MLA_F32, *args[2:]) == -6
