@@ -17,6 +17,7 @@
 
 #include "mla_internal.h"
 #include "tc.h"
+#include "tc_internal.h"
 
 namespace {
 
@@ -623,6 +624,7 @@ mla_status prefill_entry(bool absorbed, const mla_dims *dims, mla_dtype dtype, i
 struct BwdWs {
     PrefillWs f;   // the forward's recomputed intermediates (K / V per head shard)
     float *D, *dqr, *dK, *dV, *dkr, *dkr_acc, *dchat, *rms_part;
+    void *qn16, *do16, *dkvt, *chatT, *wT;   // tensor-core path
     size_t bytes;
 };
 
@@ -635,8 +637,16 @@ BwdWs bwd_ws(const Prefill &p, void *base) {
     const size_t nq = (size_t)p.B * p.s_q * p.head_count;
     w.D = (float *)c.take(nq * 4);
     w.dqr = (float *)c.take(nq * p.Dr * 4);
-    w.dK = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dn * 4);
-    w.dV = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dv * 4);
+    if (p.tc) {
+        w.qn16 = c.take(nq * p.Dn * 2);
+        w.do16 = c.take(nq * p.Dv * 2);
+        w.dkvt = c.take((size_t)p.hs * (p.Dn + p.Dv) * p.B * p.kv_pad * 2);
+        w.chatT = c.take((size_t)p.Dk * p.B * p.kv_pad * 2);
+        w.wT = c.take((size_t)p.Dk * p.head_count * (p.Dn + p.Dv) * 2);
+    } else {
+        w.dK = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dn * 4);
+        w.dV = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dv * 4);
+    }
     w.dkr = (float *)c.take((size_t)p.B * p.hs * p.kv_pad * p.Dr * 4);
     w.dkr_acc = (float *)c.take((size_t)p.B * p.kv_pad * p.Dr * 4);
     w.dchat = (float *)c.take((size_t)p.B * p.kv_pad * p.Dk * 4);
@@ -649,9 +659,61 @@ mla_status bwd_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_kv, 
                      int head_begin, int head_count, int head_shard, Prefill *p) {
     mla_status st = prefill_shape(d, dt, B, s_q, s_kv, q_offset, causal, head_begin, head_count, head_shard, false, p);
     if (st != MLA_OK) return st;
-    if (!bwd_simt_supported(p->Dn, p->Dr, p->Dv)) return MLA_ERR_UNSUPPORTED;
-    p->tc = false;   // the backward's recomputed intermediates are fp32
-    p->tmid = TY_F32;
+    if (!p->tc) {   // the CUDA-core backward keeps fp32 intermediates
+        if (!bwd_simt_supported(p->Dn, p->Dr, p->Dv)) return MLA_ERR_UNSUPPORTED;
+        p->tmid = TY_F32;
+    }
+    return MLA_OK;
+}
+
+// The backward on the tensor cores (bf16 at the DeepSeek dimensions): the forward's prep
+// and per-shard K / V reconstruction again, the two attention-backward kernels, the
+// weight gradients dW = [dK_nope^T ; dV^T] chat (summed over the batch by running the
+// GEMM's k over batch and keys) and dchat += dKV W (W^T as the B operand), then the
+// rotations' transposes and the RMSNorm backward.
+mla_status bwd_tc(const Prefill &p, const mla_dims *d, float scale, const void *q_nope, const void *q_pe,
+                  const void *c_kv, const void *k_pe, const void *w_kv_b, const void *rms_w, const void *out,
+                  const float *lse, const void *dout, void *dq_nope, void *dq_pe, void *dc_kv, void *dk_pe,
+                  float *dw_kv_b, float *drms_w, const BwdWs &w, cudaStream_t st) {
+    const long Dh = p.Dn + p.Dv, kvn = p.kv_need, BK = (long)p.B * p.kv_pad;
+    const size_t ein = ty_size(p.tin);
+    mla_status ms = prefill_prep(p, false, d, q_pe, c_kv, k_pe, w_kv_b, rms_w, w.f, st);
+    if (ms != MLA_OK) return ms;
+    MLA_TRY(launch_bwd_prep_tc(p.B, p.s_q, p.head_count, q_nope, dout, out, w.qn16, w.do16, w.D, st));
+    MLA_TRY(launch_transpose16(BK, p.Dk, w.f.chat, w.chatT, st));                       // chat^T [Dk][B*kv_pad]
+    MLA_TRY(launch_transpose16((long)p.head_count * Dh, p.Dk, w.f.w16, w.wT, st));      // W^T [Dk][hc*Dh]
+    TcPrefill t{p.B, p.s_q, p.s_kv, p.q_offset, p.causal, p.head_begin, p.head_count, p.hs, p.n_shards,
+                p.Dk, p.Dn, p.Dr, p.Dv, p.H, p.kv_need, scale};
+    for (int s = 0; s < p.n_shards; ++s) {
+        const int h0 = s * p.hs, nh = std::min(p.hs, p.head_count - h0);
+        MLA_TRY(tc_reconstruct(t, h0, nh, w.f.chat, w.f.w16, w.f.k, w.f.v, st));
+        MLA_TRY(tc_bwd_attn(t, h0, nh, w.f.k, w.f.v, w.f.kpe, w.qn16, w.f.qpe, w.do16, lse, w.D, dq_nope, w.dqr,
+                            w.dkvt, w.dkr, st));
+        // dW rows of the shard's heads: [nh*Dh][Dk] = dKV^T [nh*Dh][B*kv_pad] x chat^T [Dk][B*kv_pad]^T
+        TmaOperand A{w.dkvt, BK, (long)nh * Dh, 1, BK * 2, 0, (int)(nh * Dh), 0, 0};
+        TmaOperand Bc{w.chatT, BK, p.Dk, 1, BK * 2, 0, p.Dk, 0, 0};
+        MLA_TRY(tc_gemm(A, Bc, (int)(nh * Dh), p.Dk, (int)BK, 1, true,
+                        dw_kv_b + (size_t)(p.head_begin + h0) * Dh * p.Dk, p.Dk, 1, 0, 2, st));
+        // dchat [B*kv_pad][Dk] += dKV [B*kv_pad][nh*Dh] x W [nh*Dh][Dk], 128 latent columns per launch
+        TmaOperand Am{w.dkvt, BK, (long)nh * Dh, 1, BK * 2, 0, (int)BK, 0, 0};   // m-major: rows are k
+        for (int c = 0; c < p.Dk / 128; ++c) {
+            TmaOperand Bw{(const char *)w.wT + ((size_t)c * 128 * p.head_count * Dh + (size_t)h0 * Dh) * 2,
+                          (long)nh * Dh, 128, 1, (long)p.head_count * Dh * 2, 0, 128, 0, 0};
+            MLA_TRY(tc_gemm(Am, Bw, (int)BK, 128, (int)(nh * Dh), 1, true, w.dchat + (size_t)c * 128, p.Dk, 1, 0, 2,
+                            st, true, s > 0));
+        }
+        MLA_TRY(launch_head_sum(p.B, nh, p.kv_pad, p.Dr, p.kv_pad, w.dkr, w.dkr_acc, s > 0, st));
+    }
+    const long nq = (long)p.B * p.s_q * p.head_count;
+    MLA_TRY(launch_rope_inv(nq, p.Dr, w.dqr, p.Dr, p.q_offset, p.head_count, p.s_q, 1L << 40, w.f.rtab, dq_pe,
+                            p.tin, p.Dr, st));
+    for (int b = 0; b < p.B; ++b) {
+        MLA_TRY(launch_rope_inv(p.s_kv, p.Dr, w.dkr_acc + (size_t)b * p.kv_pad * p.Dr, p.Dr, 0, 1, 1L << 40, kvn,
+                                w.f.rtab, (char *)dk_pe + (size_t)b * p.s_kv * p.Dr * ein, p.tin, p.Dr, st));
+        MLA_TRY(launch_rms_bwd_f32dy(p.tin, kvn, p.s_kv, p.Dk, d->rms_eps, (const char *)c_kv + (size_t)b * p.s_kv * p.Dk * ein,
+                                     rms_w, w.dchat + (size_t)b * p.kv_pad * p.Dk,
+                                     (char *)dc_kv + (size_t)b * p.s_kv * p.Dk * ein, drms_w, b > 0, w.rms_part, st));
+    }
     return MLA_OK;
 }
 
@@ -779,7 +841,10 @@ mla_status mla_latent_attn_bwd(const mla_dims *dims, mla_dtype dtype, int B, int
     if (st != MLA_OK) return st;
     cudaStream_t cs = (cudaStream_t)cuda_stream;
     const BwdWs w = bwd_ws(p, workspace);
-    g_last_path = 1;
+    g_last_path = p.tc ? 2 : 1;
+    if (p.tc)
+        return bwd_tc(p, dims, scale_of(dims), q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, dout, dq_nope, dq_pe,
+                      dc_kv, dk_pe, dw_kv_b, drms_w, w, cs);
     return bwd_simt(p, dims, scale_of(dims), q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, dout, dq_nope, dq_pe,
                     dc_kv, dk_pe, dw_kv_b, drms_w, w, cs);
 }

@@ -36,6 +36,19 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
 // rebuilt key tile.  Inputs as tc_explicit_prefill (w16 holds all head_count heads).
 cudaError_t tc_fused_prefill(const TcPrefill &p, const void *q_nope, void *out, float *lse, const void *chat,
                              const void *kpe, const void *qpe, const void *w16, int cluster, cudaStream_t st);
+// The K_nope / V^T reconstruction of heads h0 .. h0 + nh of the call into the per-shard
+// workspace (kws [B][kv_pad][hs*128], vws [B][hs*128][kv_pad], fp16).
+cudaError_t tc_reconstruct(const TcPrefill &p, int h0, int nh, const void *chat, const void *w16, void *kws,
+                           void *vws, cudaStream_t st);
+// Backward (tc_bwd.cu): q_nope / dO widened to fp16 and D = dO . out; a 16-bit transpose;
+// the attention backward of one head shard (dq_nope bf16, rotated dq fp32, [dK_nope^T ;
+// dV^T] per head fp16 [nh][256][B][kv_pad], dk_rot per head fp32 [B][nh][kv_pad][64]).
+cudaError_t launch_bwd_prep_tc(int B, int s_q, int hc, const void *q_nope, const void *dout, const void *out,
+                               void *qn16, void *do16, float *D, cudaStream_t st);
+cudaError_t launch_transpose16(long R, long C, const void *x, void *y, cudaStream_t st);
+cudaError_t tc_bwd_attn(const TcPrefill &p, int h0, int nh, const void *kws, const void *vws, const void *kpe,
+                        const void *qn16, const void *qpe, const void *do16, const float *lse, const float *D,
+                        void *dq_nope, float *dqr, void *dkvt, float *dkr, cudaStream_t st);
 cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
                                 float *lse, const void *chat, const void *kpe, const void *qpe, void *qabs,
                                 void *olat, void *w16, cudaStream_t st);

@@ -521,12 +521,30 @@ bool tc_explicit_supported(int Dk, int Dn, int Dr, int Dv) {
     return prep_tc_supported(Dk, Dr) && Dn == 128 && Dv == 128;
 }
 
+// The per-head K / V reconstruction of one head shard (heads h0 .. h0 + nh of the call),
+// both products in one persistent launch:
+//   K_nope[b][j][hl*Dn + d] = chat[b][j] . W_K(head_begin+h0+hl)[d]
+//   V^T[b][hl*Dv + d][j]    = W_V(head_begin+h0+hl)[d] . chat[b][j]
+// w16: fp16 copy of the call's W_kv_b rows [head_count][Dn+Dv][Dk].
+cudaError_t tc_reconstruct(const TcPrefill &p, int h0, int nh, const void *chat, const void *w16, void *kws,
+                           void *vws, cudaStream_t st) {
+    const long kv_pad = (p.kv_need + 127) / 128 * 128;
+    const long Dh = p.Dn + p.Dv;
+    TmaOperand latent{chat, p.Dk, kv_pad, p.B, (long)p.Dk * 2, kv_pad * p.Dk * 2, (int)kv_pad, 0, 1};
+    const char *ws = (const char *)w16 + (long)h0 * Dh * p.Dk * 2;
+    TmaOperand wk{ws, p.Dk, p.Dn, nh, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dn, 0, 0};
+    TmaOperand wv{ws + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, nh, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dv, 0, 0};
+    const GemmProblem kv[2] = {
+        {latent, wk, (int)kv_pad, nh * p.Dn, p.Dk, p.B, kws, (long)p.hs * p.Dn, 1, kv_pad * p.hs * p.Dn, 0},
+        {wv, latent, nh * p.Dv, (int)kv_pad, p.Dk, p.B, vws, kv_pad, 1, (long)p.hs * p.Dv * kv_pad, 0}};
+    return tc_gemm_group(kv, 2, true, st);
+}
+
 cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out, float *lse,
                                 const void *chat, const void *kpe, const void *qpe, void *kws, void *vws,
                                 const void *w16, cudaStream_t st) {
     (void)w_kv_b;   // read through its fp16 copy w16
     const long kv_pad = (p.kv_need + 127) / 128 * 128;
-    const long Dh = p.Dn + p.Dv;
     cudaError_t e;
     // maps that do not change across shards
     CUtensorMap mQn, mQr, mKr;
@@ -590,22 +608,10 @@ cudaError_t tc_explicit_prefill(const TcPrefill &p, const void *q_nope, const vo
     a.idesc_s = idesc_f16(128, 128, true);
     a.idesc_pv = idesc_f16(128, 144, true);   // 128 dv columns + the row-sum column block
 
-    TmaOperand latent{chat, p.Dk, kv_pad, p.B, (long)p.Dk * 2, kv_pad * p.Dk * 2, (int)kv_pad, 0, 1};
     for (int s = 0; s < p.n_shards; ++s) {
         const int h0 = s * p.hs;
         const int nh = std::min(p.hs, p.head_count - h0);
-        // this shard's rows of the fp16 W_kv_b copy: [nh][Dn+Dv][Dk]
-        const char *ws = (const char *)w16 + (long)h0 * Dh * p.Dk * 2;
-        // K_nope[b][j][hl*Dn + d] = chat[b][j] . W_K(head_begin+h0+hl)[d]
-        TmaOperand wk{ws, p.Dk, p.Dn, nh, (long)p.Dk * 2, Dh * p.Dk * 2, p.Dn, 0, 0};
-        // V^T[b][hl*Dv + d][j] = W_V(head_begin+h0+hl)[d] . chat[b][j]
-        TmaOperand wv{ws + (long)p.Dn * p.Dk * 2, p.Dk, p.Dv, nh, (long)p.Dk * 2, Dh * p.Dk * 2,
-                      p.Dv, 0, 0};
-        // both products in one persistent launch
-        const GemmProblem kv[2] = {
-            {latent, wk, (int)kv_pad, nh * p.Dn, p.Dk, p.B, kws, (long)p.hs * p.Dn, 1, kv_pad * p.hs * p.Dn, 0},
-            {wv, latent, nh * p.Dv, (int)kv_pad, p.Dk, p.B, vws, kv_pad, 1, (long)p.hs * p.Dv * kv_pad, 0}};
-        if ((e = tc_gemm_group(kv, 2, true, st)) != cudaSuccess) return e;
+        if ((e = tc_reconstruct(p, h0, nh, chat, w16, kws, vws, st)) != cudaSuccess) return e;
         a.head_off = h0;
         a.nh = nh;
         a.nb = p.B;

@@ -46,6 +46,7 @@ struct GemmP {
     int out_kind;  // 0 fp16, 1 bf16, 2 fp32
     int tiles_n, tiles_m, tiles;
     int c_stage;   // pair kernel: C staged per warp and written in whole 128-byte rows (16-bit, n contiguous, aligned)
+    int acc;       // fp32 C accumulated (single-CTA kernel)
 };
 
 struct GemmK {
@@ -221,9 +222,17 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                     } else {
-                        uint4 *dst = (uint4 *)(C + (base + nb) * 4);
+                        float4 *dst = (float4 *)(C + (base + nb) * 4);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                        for (int i = 0; i < 8; ++i) {
+                            float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                            if (q.acc) {
+                                const float4 o = dst[i];
+                                v.x += o.x, v.y += o.y, v.z += o.z, v.w += o.w;
+                            }
+                            dst[i] = v;
+                        }
                     }
                 } else {
                     for (int i = 0; i < 32; ++i) {
@@ -233,7 +242,7 @@ __global__ void __launch_bounds__(256, 1)
                         const long off = base + (long)n * q.c_n;
                         if (q.out_kind == 0) ((__half *)C)[off] = __float2half_rn(x);
                         else if (q.out_kind == 1) ((__nv_bfloat16 *)C)[off] = __float2bfloat16_rn(x);
-                        else ((float *)C)[off] = x;
+                        else ((float *)C)[off] = q.acc ? ((float *)C)[off] + x : x;
                     }
                 }
             }
@@ -577,6 +586,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
     int maxN = 0;
     for (int i = 0; i < n_probs; ++i) {
         if (probs[i].K % BK || probs[i].K != probs[0].K || probs[i].a_mn != probs[0].a_mn) return cudaErrorInvalidValue;
+        if (probs[i].accumulate && probs[i].out_kind != 2) return cudaErrorInvalidValue;
         maxN = std::max(maxN, probs[i].N);
     }
     const int BN = maxN >= 256 ? 256 : (maxN >= 128 ? 128 : 64);
@@ -584,6 +594,8 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
     // 256-wide problems run on SM pairs: 256 x 256 tiles, A boxes of 128 rows per CTA,
     // B boxes of 64 rows (two per CTA)
     const bool pair = BN == 256;
+    for (int i = 0; i < n_probs; ++i)
+        if (pair && probs[i].accumulate) return cudaErrorInvalidValue;   // accumulation: single-CTA tiles only
     const int TM = pair ? 256 : BM, TN = BN;
     CUtensorMap maps[4];
     GemmK p{};
@@ -615,6 +627,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         q.c_n = g.c_n;
         q.c_batch = g.c_batch;
         q.out_kind = g.out_kind;
+        q.acc = g.accumulate ? 1 : 0;
         q.tiles_n = (g.N + TN - 1) / TN;
         q.tiles_m = (g.M + TM - 1) / TM;
         q.tiles = (g.M == 0 || g.N == 0) ? 0 : q.tiles_n * q.tiles_m * g.batch;
@@ -641,9 +654,10 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
 }
 
 cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int K, int batch, bool f16,
-                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st, bool a_mn) {
+                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st, bool a_mn,
+                    bool accumulate) {
     if (M == 0 || N == 0 || batch == 0) return cudaSuccess;
-    GemmProblem g{A, B, M, N, K, batch, C, c_m, c_n, c_batch, out_kind, a_mn};
+    GemmProblem g{A, B, M, N, K, batch, C, c_m, c_n, c_batch, out_kind, a_mn, accumulate};
     return tc_gemm_group(&g, 1, f16, st);
 }
 

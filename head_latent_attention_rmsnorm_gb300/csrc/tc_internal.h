@@ -40,9 +40,12 @@ struct GemmProblem {
     // A stored m-major (m contiguous, one row per k): then A.k_extent is the m extent and
     // A.rows the k extent.  Tiles of 64 or 128 columns only (not the pair kernel).
     bool a_mn = false;
+    // C += A B^T instead of C = A B^T (fp32 C, tiles of 64 or 128 columns only).
+    bool accumulate = false;
 };
 cudaError_t tc_gemm(const TmaOperand &A, const TmaOperand &B, int M, int N, int K, int batch, bool f16,
-                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st, bool a_mn = false);
+                    void *C, long c_m, long c_n, long c_batch, int out_kind, cudaStream_t st, bool a_mn = false,
+                    bool accumulate = false);
 // One persistent launch over the tiles of one or two problems (same K, same operand
 // type): the explicit path's K_nope and V^T products share one launch.
 cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaStream_t st);
@@ -52,6 +55,7 @@ cudaError_t tc_attn_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_latent_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_decode_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_fused_read_and_clear_error(unsigned *flags, cudaStream_t st);
+cudaError_t tc_bwd_read_and_clear_error(unsigned *flags, cudaStream_t st);
 
 // Split-KV latent decode attention (tc_decode.cu): partial latent outputs and
 // log-sum-exps of every (sequence, key split, 128 heads).  qa: q_abs [B][H][512] fp16;

@@ -128,3 +128,59 @@ def test_ragged_bf16_backward(oracle, causal):
     check_grads(g, r, torch.bfloat16, rows_w=rows, what="ragged bf16 causal %d: " % causal)
     if causal:   # keys past q_offset + s_q are seen by no query
         assert np.all(g["c_kv"][:, cfg.q_offset + cfg.s_q:] == 0) and np.all(g["k_pe"][:, cfg.q_offset + cfg.s_q:] == 0)
+
+
+def test_bf16_backward_tensor_core_path_matches_simt_path():
+    """The same bf16 backward through the tcgen05 kernels and through the CUDA-core
+    kernels (forced): both within the bf16 bars of each other."""
+    cfg = dataclasses.replace(RAGGED, s_kv=700, s_q=500, q_offset=200, batch=1, n_heads=4, head_shard=4)
+    inp = inputs.prefill_inputs(cfg)
+    dout = dout_for(cfg, cfg.s_q, cfg.n_heads)
+    g_tc = gpu_fwd_bwd(cfg, inp, dout, q_offset=cfg.q_offset, causal=True)
+    assert mla.last_path() == mla.PATH_TC
+    mla.set_path_override(1)
+    try:
+        g_s = gpu_fwd_bwd(cfg, inp, dout, q_offset=cfg.q_offset, causal=True)
+        assert mla.last_path() == mla.PATH_SIMT
+    finally:
+        mla.set_path_override(0)
+    check_grads(g_tc, g_s, torch.bfloat16, what="tc vs simt: ")
+
+
+def test_bf16_backward_query_shards_sum_to_one_call():
+    """Two query shards of one bf16 sequence on the tensor-core path: the latent, band and
+    parameter gradients of the shards add up to the single call's (within fp32 rounding of
+    the different summation order), the shards' query gradients are its rows."""
+    cfg = dataclasses.replace(RAGGED, s_kv=512, s_q=512, q_offset=0, batch=1, n_heads=2, head_shard=2)
+    S = cfg.s_kv
+    full = inputs.prefill_inputs(cfg, q_rows=(0, S))
+    dfull = dout_for(cfg, S, cfg.n_heads)
+    g1 = gpu_fwd_bwd(cfg, full, dfull, q_offset=0, causal=True)
+    parts = []
+    for lo, hi in ((0, 256), (256, S)):
+        sub = dict(full, q_nope=full["q_nope"][:, lo:hi].contiguous(), q_pe=full["q_pe"][:, lo:hi].contiguous())
+        parts.append(gpu_fwd_bwd(cfg, sub, dfull[:, lo:hi].contiguous(), q_offset=lo, causal=True))
+    for k in ("w_kv_b", "rms_w"):
+        np.testing.assert_allclose(parts[0][k] + parts[1][k], g1[k], rtol=0, atol=2e-3 * max(1, np.abs(g1[k]).max()))
+    for k in ("c_kv", "k_pe"):   # bf16 outputs: each side rounded once
+        np.testing.assert_allclose(parts[0][k] + parts[1][k], g1[k], rtol=0, atol=2e-2 * max(1, np.abs(g1[k]).max()))
+    for k in ("q_nope", "q_pe"):
+        assert np.array_equal(np.concatenate([parts[0][k], parts[1][k]], 1), g1[k]), k
+
+
+def test_v2lite_backward_sampled_against_simt():
+    """The bench's backward workload size (V2-Lite prefill, 4096 tokens, 16 heads) on the
+    tensor cores against the CUDA-core backward on two heads."""
+    cfg = configs.V2LITE
+    inp = inputs.prefill_inputs(cfg)
+    sub = dict(inp, q_nope=inp["q_nope"][:, :, 5:7].contiguous(), q_pe=inp["q_pe"][:, :, 5:7].contiguous())
+    dout = dout_for(cfg, cfg.s_q, 2)
+    g_tc = gpu_fwd_bwd(cfg, sub, dout, q_offset=0, causal=True, head_begin=5, head_shard=2)
+    assert mla.last_path() == mla.PATH_TC
+    mla.set_path_override(1)
+    try:
+        g_s = gpu_fwd_bwd(cfg, sub, dout, q_offset=0, causal=True, head_begin=5, head_shard=2)
+    finally:
+        mla.set_path_override(0)
+    rows = slice(5 * 256, 7 * 256)
+    check_grads(g_tc, g_s, torch.bfloat16, rows_w=rows, what="v2lite tc vs simt: ")
