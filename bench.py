@@ -428,6 +428,63 @@ def decode_measure(dcfg, stream, steps, warmup, world, peaks, peak_kind):
             "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
 
 
+def backward_measure(cfg, stream, steps, warmup, flush, peaks, peak_kind):
+    """The backward call (mla_latent_attn_bwd) of workload `cfg` for a random upstream
+    gradient, given the forward's out and lse: per-call time, the per-kernel split and the
+    two attention-backward kernels' rooflines (their algorithmic FLOPs: dV + dK for the
+    key-stationary kernel, dQ for the query-stationary one)."""
+    import torch
+    from head_latent_attention_rmsnorm_gb300 import mla
+    d, t, out, lse, ws = prefill_setup(cfg)
+    prefill_call(cfg, d, t, out, lse, ws, stream)
+    del ws
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    dout = randn(out.shape, 1.0, out.dtype, g)
+    grads = {"q_nope": torch.empty_like(t["q_nope"]), "q_pe": torch.empty_like(t["q_pe"]),
+             "c_kv": torch.empty_like(t["c_kv"]), "k_pe": torch.empty_like(t["k_pe"]),
+             "w_kv_b": torch.zeros(t["w_kv_b"].shape, dtype=torch.float32, device="cuda"),
+             "rms_w": torch.empty(cfg.d_kv, dtype=torch.float32, device="cuda")}
+    nbytes = mla.mla_latent_attn_bwd_workspace(ctypes.byref(d), mla.MLA_BF16, cfg.batch, cfg.s_q, cfg.s_kv,
+                                               cfg.q_offset, int(cfg.causal), cfg.n_heads, cfg.head_shard)
+    bws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+    def fn():
+        mla.latent_attn_bwd(d, t["q_nope"], t["q_pe"], t["c_kv"], t["k_pe"], t["w_kv_b"], t["rms_w"], out, lse, dout,
+                            q_offset=cfg.q_offset, causal=cfg.causal, head_shard=cfg.head_shard, grads=grads,
+                            workspace=bws, stream=stream)
+    fn()
+    torch.cuda.synchronize()
+    path = mla.last_path()
+    times = timed(fn, steps, warmup, 1, flush)
+    mla.profile_enable(True)
+    mla.profile_reset()
+    timed(fn, steps, warmup, 1, flush)
+    prof = mla.profile_all()
+    mla.profile_enable(False)
+    ms = statistics.mean(times)
+    fl = cfg.backward_flops()
+    calls = steps + warmup
+    roof = {}
+    peak = peaks.get("bf16_tflops", 1900.0)
+    for kern, key in (("tc_bwd_dkv", "dkv_kernel"), ("tc_bwd_dq", "dq_kernel")):
+        if kern in prof:
+            n, kms = prof[kern]
+            per_launch = fl[key] * calls / n
+            ach = per_launch / (kms / n * 1e-3) / 1e12
+            roof[kern] = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                          "frac": round(ach / peak, 4), "launches": n, "avg_launch_us": round(kms / n * 1e3, 2),
+                          "flops_per_launch": per_launch, "peak_kind": "bf16 dense burst, " + peak_kind}
+    del d, t, out, lse, dout, grads, bws
+    torch.cuda.empty_cache()
+    return {"workload": cfg.name + "_backward", "ms_per_call": round(ms, 4),
+            "TFLOP/s": round(fl["total"] / (ms * 1e-3) / 1e12, 2),
+            "frac_of_bf16_peak": round(fl["total"] / (ms * 1e-3) / 1e12 / peak, 4), "flops_per_call": fl["total"],
+            "flops_counted": "dV, dP, dQ, dK per visible pair and head; dW and dchat per key and head (no recompute)",
+            "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"), "steps": steps, "warmup": warmup,
+            "roofline": roof, "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
+
+
 def activation_memory():
     """Peak device memory the CUDA caching allocator sees for one prefill call (outputs +
     workspace), explicit against absorbed, at head shards of 16 and of all heads, on the
@@ -545,6 +602,9 @@ def run_ours(args, world, rank, local):
                 side[r["workload"]] = r
                 del bufs
                 torch.cuda.empty_cache()
+            for cfg in (configs.V2LITE, configs.SP8_RANK7):
+                r = backward_measure(cfg, stream, steps, warmup, flush, peaks, peak_kind)
+                side[r["workload"]] = r
             del flush
             torch.cuda.empty_cache()
             decode = decode_measure(configs.DECODE, stream, steps, warmup, 1, peaks, peak_kind)

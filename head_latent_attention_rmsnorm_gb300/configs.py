@@ -50,6 +50,19 @@ class Prefill:
         recon = 2 * self.batch * self.kv_needed() * self.d_kv * self.n_heads * (self.d_nope + self.d_v)
         return {"attention": attn, "reconstruct": recon, "total": attn + recon}
 
+    def backward_flops(self) -> dict:
+        """Algorithmic FLOPs of one backward call (masked pairs excluded), without the
+        recomputation an implementation chooses: per visible pair and head dV = P^T dO and
+        dP = dO V^T (2 d_v each), dQ = dS K and dK = dS^T Q (2 (d_nope + d_rope) each); per
+        key and head the weight gradient dW = dKV^T chat and the latent gradient
+        dchat = dKV W (2 d_kv (d_nope + d_v) each)."""
+        dqk = self.d_nope + self.d_rope
+        pairs = self.batch * self.n_heads * self.pairs()
+        attn = pairs * 2 * (2 * self.d_v + 2 * dqk)
+        recon = 2 * (2 * self.batch * self.kv_needed() * self.d_kv * self.n_heads * (self.d_nope + self.d_v))
+        return {"attention": attn, "reconstruct": recon, "dkv_kernel": pairs * 2 * (self.d_v + dqk),
+                "dq_kernel": pairs * 2 * dqk, "total": attn + recon}
+
     def absorbed_flops(self) -> dict:
         """Algorithmic FLOPs of one absorbed-form call: latent-space attention over
         d_kv + d_rope score dims and d_kv value dims, plus the absorb (q_nope -> q_abs) and

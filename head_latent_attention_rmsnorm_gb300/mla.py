@@ -216,7 +216,8 @@ def set_path_override(mode: int) -> None:
 
 KERNELS = ("prep", "latent_prep", "rope_table", "rope_rows", "convert", "gemm_simt", "attn_simt", "lse_combine",
            "tc_gemm", "tc_attn", "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
-           "tpla_combine", "wait_probe", "tc_fused_attn", "bwd_rowdot", "attn_bwd_simt", "bwd_rows")
+           "tpla_combine", "wait_probe", "tc_fused_attn", "bwd_rowdot", "attn_bwd_simt", "bwd_rows",
+           "bwd_prep", "tc_bwd_dkv", "tc_bwd_dq")
 
 
 def launch_count() -> int:

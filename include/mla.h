@@ -349,7 +349,7 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   "convert", "gemm_simt", "attn_simt", "lse_combine", "tc_gemm", "tc_attn",
  *   "tc_latent_attn", "tc_decode_attn", "transpose", "rmsnorm", "rmsnorm_bwd", "tpla_expand",
  *   "tpla_combine", "wait_probe", "tc_fused_attn", "bwd_rowdot",
- *   "attn_bwd_simt", "bwd_rows".
+ *   "attn_bwd_simt", "bwd_rows", "bwd_prep", "tc_bwd_dkv", "tc_bwd_dq".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
  * Not thread-safe: profile from one host thread at a time.
  */
