@@ -318,7 +318,9 @@ cudaError_t launch_rope_inv(long rows, int Dr, const float *x, long x_pitch, lon
     return cudaGetLastError();
 }
 
-size_t rms_bwd_parts(long s_kv) { return (size_t)std::max<long>(1, std::min<long>(512, (s_kv + RW - 1) / RW)); }
+// Partial dw rows: at most 128, so that the ordered sum over them stays short; each block
+// walks s_kv / (parts * RW) rows per warp.
+size_t rms_bwd_parts(long s_kv) { return (size_t)std::max<long>(1, std::min<long>(128, (s_kv + RW - 1) / RW)); }
 
 cudaError_t launch_rms_bwd_f32dy(int ty, long n_rows, long s_kv, int Dk, float eps, const void *x, const void *w,
                                  const float *dy, void *dx, float *dw, bool accumulate, float *part,

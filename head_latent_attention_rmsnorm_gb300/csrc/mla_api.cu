@@ -689,19 +689,20 @@ mla_status bwd_tc(const Prefill &p, const mla_dims *d, float scale, const void *
         MLA_TRY(tc_reconstruct(t, h0, nh, w.f.chat, w.f.w16, w.f.k, w.f.v, st));
         MLA_TRY(tc_bwd_attn(t, h0, nh, w.f.k, w.f.v, w.f.kpe, w.qn16, w.f.qpe, w.do16, lse, w.D, dq_nope, w.dqr,
                             w.dkvt, w.dkr, st));
-        // dW rows of the shard's heads: [nh*Dh][Dk] = dKV^T [nh*Dh][B*kv_pad] x chat^T [Dk][B*kv_pad]^T
+        // dW rows of the shard's heads: [nh*Dh][Dk] = dKV^T [nh*Dh][B*kv_pad] x chat^T [Dk][B*kv_pad]^T,
+        // the Dk output columns as a batch of 128-column blocks (single-CTA tiles: four times
+        // the tiles of one 256-wide problem)
+        const int nb = p.Dk / 128;
         TmaOperand A{w.dkvt, BK, (long)nh * Dh, 1, BK * 2, 0, (int)(nh * Dh), 0, 0};
-        TmaOperand Bc{w.chatT, BK, p.Dk, 1, BK * 2, 0, p.Dk, 0, 0};
-        MLA_TRY(tc_gemm(A, Bc, (int)(nh * Dh), p.Dk, (int)BK, 1, true,
-                        dw_kv_b + (size_t)(p.head_begin + h0) * Dh * p.Dk, p.Dk, 1, 0, 2, st));
-        // dchat [B*kv_pad][Dk] += dKV [B*kv_pad][nh*Dh] x W [nh*Dh][Dk], 128 latent columns per launch
+        TmaOperand Bc{w.chatT, BK, 128, nb, BK * 2, 128 * BK * 2, 128, 0, 1};
+        MLA_TRY(tc_gemm(A, Bc, (int)(nh * Dh), 128, (int)BK, nb, true,
+                        dw_kv_b + (size_t)(p.head_begin + h0) * Dh * p.Dk, p.Dk, 1, 128, 2, st));
+        // dchat [B*kv_pad][Dk] += dKV [B*kv_pad][nh*Dh] x W [nh*Dh][Dk], the latent columns as a
+        // batch of 128-column blocks (W^T rows 128 c .. 128 c + 127 for block c)
         TmaOperand Am{w.dkvt, BK, (long)nh * Dh, 1, BK * 2, 0, (int)BK, 0, 0};   // m-major: rows are k
-        for (int c = 0; c < p.Dk / 128; ++c) {
-            TmaOperand Bw{(const char *)w.wT + ((size_t)c * 128 * p.head_count * Dh + (size_t)h0 * Dh) * 2,
-                          (long)nh * Dh, 128, 1, (long)p.head_count * Dh * 2, 0, 128, 0, 0};
-            MLA_TRY(tc_gemm(Am, Bw, (int)BK, 128, (int)(nh * Dh), 1, true, w.dchat + (size_t)c * 128, p.Dk, 1, 0, 2,
-                            st, true, s > 0));
-        }
+        TmaOperand Bw{(const char *)w.wT + (size_t)h0 * Dh * 2, (long)nh * Dh, 128, nb, (long)p.head_count * Dh * 2,
+                      (long)128 * p.head_count * Dh * 2, 128, 0, 1};
+        MLA_TRY(tc_gemm(Am, Bw, (int)BK, 128, (int)(nh * Dh), nb, true, w.dchat, p.Dk, 1, 128, 2, st, true, s > 0));
         MLA_TRY(launch_head_sum(p.B, nh, p.kv_pad, p.Dr, p.kv_pad, w.dkr, w.dkr_acc, s > 0, st));
     }
     const long nq = (long)p.B * p.s_q * p.head_count;

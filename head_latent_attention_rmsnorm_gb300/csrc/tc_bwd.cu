@@ -96,8 +96,9 @@ constexpr uint32_t B_STAGE = 5 * QBOX64;   // Q (q_nope lo, hi, rotated q_pe) + 
 constexpr uint32_t B_OFF_LD = B_OFF_Q + 2 * B_STAGE;   // [2][2][64] lse (log2 domain) and D of a q tile
 constexpr uint32_t B_OFF_BAR = B_OFF_LD + 2 * 2 * 64 * 4;
 constexpr uint32_t B_SMEM = B_OFF_BAR + 256 + 1024;
-// TMEM: S^T / P^T 0-63, dP^T / dS^T 64-127, dV 128-255, dK (d_nope 128 + band 64) 256-447
-constexpr uint32_t B_ST = 0, B_DPT = 64, B_DV = 128, B_DK = 256;
+// TMEM: S^T / P^T double-buffered 0-63 and 64-127, dP^T / dS^T 128-191, dV 192-319, dK
+// (d_nope 128 + band 64) 320-511
+constexpr uint32_t B_ST = 0, B_DPT = 128, B_DV = 192, B_DK = 320;
 
 struct DkvK {
     int s_q, kv_need, q_offset, causal, hc, h0, nh, n_kt;
@@ -117,9 +118,11 @@ __global__ void __launch_bounds__(384, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + B_OFF_BAR);
-    uint64_t *kv_full = bars, *qd_full = bars + 1, *qd_empty = bars + 3, *st_full = bars + 5, *dpt_full = bars + 6;
-    uint64_t *ps_full = bars + 7, *tile_free = bars + 8, *acc_done = bars + 9;
-    uint32_t *tslot = (uint32_t *)(bars + 12);
+    // st_full / pt_free [buffer]: S^T landed / P^T read by the dV MMAs; dpt_full / dpt_free:
+    // dP^T landed / dS^T read by the dK MMAs; ps_full: the softmax warps wrote P^T and dS^T
+    uint64_t *kv_full = bars, *qd_full = bars + 1, *qd_empty = bars + 3, *st_full = bars + 5, *dpt_full = bars + 7;
+    uint64_t *ps_full = bars + 8, *pt_free = bars + 9, *dpt_free = bars + 11, *acc_done = bars + 12;
+    uint32_t *tslot = (uint32_t *)(bars + 14);
     volatile int *abort = (volatile int *)(tslot + 1);
     float *ld = (float *)(smem + B_OFF_LD);
     unsigned *err = &g_tc_bwd_err;
@@ -141,10 +144,13 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&qd_full[i], 1);
             mbar_init(&qd_empty[i], 1);
         }
-        mbar_init(st_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&st_full[i], 1);
+            mbar_init(&pt_free[i], 1);
+        }
         mbar_init(dpt_full, 1);
+        mbar_init(dpt_free, 1);
         mbar_init(ps_full, 8);
-        mbar_init(tile_free, 1);
         mbar_init(acc_done, 1);
         *abort = 0;
         fence_mbar_init();
@@ -182,12 +188,14 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------ S^T = K Q^T, dP^T = V dO^T
+        // S^T of tile t + 1 goes into the other buffer as soon as dP^T of tile t is issued,
+        // so it overlaps the softmax of tile t
         bool ok = nqt > 0 && __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort, err));
         for (int t = 0; t < nqt && ok; ++t) {
             const int st = t & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&qd_full[st], (t >> 1) & 1, abort, err));
-            // the previous tile's dV / dK MMAs have read P^T and dS^T out of these columns
-            if (ok && t > 0) ok = __all_sync(0xffffffffu, mbar_wait(tile_free, (t - 1) & 1, abort, err));
+            // the dV MMAs of tile t - 2 have read P^T out of this buffer
+            if (ok && t >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&pt_free[st], ((t - 2) >> 1) & 1, abort, err));
             if (!ok) break;
             tc_fence_after();
             const uint8_t *q = smem + B_OFF_Q + st * B_STAGE;
@@ -197,9 +205,16 @@ __global__ void __launch_bounds__(384, 1)
                     const uint64_t da = sdesc_kmajor(smem + B_OFF_K + kb * KBOX), db = sdesc_kmajor(q + kb * QBOX64);
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4)
-                        mma_ss(tmem + B_ST, da + 2 * k4, db + 2 * k4, p.idesc_st, (kb | k4) != 0);
+                        mma_ss(tmem + B_ST + st * 64, da + 2 * k4, db + 2 * k4, p.idesc_st, (kb | k4) != 0);
                 }
-                mma_commit(st_full);
+                mma_commit(&st_full[st]);
+            }
+            __syncwarp();
+            // the dK MMAs of tile t - 1 have read dS^T out of the dP^T columns
+            if (t >= 1) ok = __all_sync(0xffffffffu, mbar_wait(dpt_free, (t - 1) & 1, abort, err));
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
                 // A = V (keys x d_v) read from V^T as an MN-major operand: two 64-key blocks
                 const uint64_t dv = sdesc_mnmajor(smem + B_OFF_V, KBOX);
 #pragma unroll
@@ -224,12 +239,14 @@ __global__ void __launch_bounds__(384, 1)
                 const uint64_t bq = sdesc_mnmajor(q, QBOX64);                 // Q^T: three 64-dim blocks
 #pragma unroll
                 for (int k = 0; k < 4; ++k)   // 16 queries per step
-                    mma_ts(tmem + B_DV, tmem + B_ST + k * 8, bdo + (uint64_t)(k * (2048 >> 4)), p.idesc_dv, (t | k) != 0);
+                    mma_ts(tmem + B_DV, tmem + B_ST + st * 64 + k * 8, bdo + (uint64_t)(k * (2048 >> 4)), p.idesc_dv,
+                           (t | k) != 0);
+                mma_commit(&pt_free[st]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_ts(tmem + B_DK, tmem + B_DPT + k * 8, bq + (uint64_t)(k * (2048 >> 4)), p.idesc_dk, (t | k) != 0);
+                mma_commit(dpt_free);
                 mma_commit(&qd_empty[st]);
-                mma_commit(tile_free);
                 if (t == nqt - 1) mma_commit(acc_done);
             }
             __syncwarp();
@@ -250,12 +267,13 @@ __global__ void __launch_bounds__(384, 1)
                 const long li = ((long)b * p.hc + hq) * p.s_q + i;
                 lt[row] = i < p.s_q ? (row < 64 ? p.lse[li] * 1.4426950408889634f : p.D[li]) : 0.f;
             }
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(st_full, t & 1, abort, err));
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&st_full[t & 1], (t >> 1) & 1, abort, err));
             ok = __all_sync(0xffffffffu, ok && mbar_wait(dpt_full, t & 1, abort, err));
             tc_fence_after();
+            const uint32_t sbuf = B_ST + (t & 1) * 64;
             uint32_t sr[32], dr[32];
             if (ok) {
-                tmem_ld32(lb + B_ST + 32 * h, sr);
+                tmem_ld32(lb + sbuf + 32 * h, sr);
                 tmem_ld32(lb + B_DPT + 32 * h, dr);
                 tmem_ld_wait();
             } else {
@@ -281,7 +299,7 @@ __global__ void __launch_bounds__(384, 1)
                 dk[c / 2] = pack_f16(dsv[0], dsv[1]);
             }
             if (ok) {
-                tmem_st16(lb + B_ST + 16 * h, pk);
+                tmem_st16(lb + sbuf + 16 * h, pk);
                 tmem_st16(lb + B_DPT + 16 * h, dk);
                 tmem_st_wait();
             }
