@@ -16,6 +16,8 @@
 #include <algorithm>
 
 #include "mla_internal.h"
+#include "tc_common.cuh"
+#include "tc_internal.h"
 
 namespace mla {
 namespace {
@@ -851,28 +853,68 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(int ty, long rows, in
 // width, dx_k = dy_k w_k / r - x_k (sum_shard dy w x) / (ds r^3) and dw_k = sum_rows
 // dy_k x_k / r.  Whole rows in registers as in rmsnorm_rows_kernel (NP pieces of 16
 // bytes per lane, shards of whole 512-byte rounds); each warp walks rows with a grid
-// stride and keeps its dw terms in registers; the block's warps add theirs into shared
-// memory in a fixed order and the block writes one partial row of dw (fp32).
+// stride.  Its rows' x and dy arrive by bulk copies into a ring of PF shared-memory slots
+// (one mbarrier each), so PF rows per warp are in flight without holding registers; a
+// slot is refilled with the row PF strides ahead once the warp has used the one it held.
+// The dw terms and the weight row stay in registers; the block's warps add their dw terms
+// into shared memory in a fixed order and the block writes one partial row of dw (fp32).
+constexpr int RMS_BWD_PF = 4;
+__device__ unsigned g_rms_err = 0;
+
+template <int NP>
+constexpr uint32_t rms_bwd_smem() {
+    return 8 * RMS_BWD_PF * (2 * NP * 512 + 8) + NP * 256 * 4 + 16;
+}
+
 template <int NP>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(int ty, long rows, int D, int g, float eps,
                                                                const uint4 *x, const uint4 *w, const uint4 *dy,
                                                                uint4 *dx, float *dw_part) {
-    __shared__ float red[NP * 256];
+    using namespace tc;
+    constexpr int PF = RMS_BWD_PF;
+    constexpr uint32_t ROW = NP * 512;   // bytes of one row of x (and of dy)
+    extern __shared__ __align__(16) uint8_t sm[];
     const int lane = threadIdx.x % 32, wib = threadIdx.x / 32, nwb = blockDim.x / 32;
+    uint8_t *slots = sm + wib * PF * 2 * ROW;                           // [PF][x, dy] of this warp
+    uint64_t *bar = (uint64_t *)(sm + 8 * PF * 2 * ROW) + wib * PF;    // [PF] of this warp
+    float *red = (float *)(sm + 8 * PF * (2 * ROW + 8));
+    volatile int *abort = (volatile int *)(red + NP * 256);
     const int per = ty == TY_F32 ? 4 : 8, sp = NP / g;
     const float ds = (float)(D / g);
+    if (threadIdx.x == 0) *abort = 0;
+    if (lane == 0)
+        for (int s = 0; s < PF; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+    __syncthreads();
     float acc[NP][8];
 #pragma unroll
     for (int p = 0; p < NP; ++p)
 #pragma unroll
         for (int t = 0; t < 8; ++t) acc[p][t] = 0.f;
-    const long stride = (long)gridDim.x * nwb;
-    for (long r = (long)blockIdx.x * nwb + wib; r < rows; r += stride) {
+    uint4 wr[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) wr[p] = w[p * 32 + lane];
+    const long stride = (long)gridDim.x * nwb, r_first = (long)blockIdx.x * nwb + wib;
+    auto issue = [&](int s, long r) {
+        if (lane == 0 && r < rows) {
+            mbar_arrive_expect_tx(&bar[s], 2 * ROW);
+            bulk_load(slots + s * 2 * ROW, (const uint8_t *)x + r * ROW, ROW, &bar[s]);
+            bulk_load(slots + s * 2 * ROW + ROW, (const uint8_t *)dy + r * ROW, ROW, &bar[s]);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < PF; ++s) issue(s, r_first + s * stride);
+    bool ok = true;
+    long k = 0;   // rows this warp has walked
+    for (long r = r_first; r < rows && ok; r += stride, ++k) {
+        const int s = (int)(k % PF);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar[s], (uint32_t)(k / PF) & 1, abort, &g_rms_err));
+        if (!ok) break;
         uint4 xv[NP], gv[NP];
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
-            xv[p] = x[r * (NP * 32) + p * 32 + lane];
-            gv[p] = dy[r * (NP * 32) + p * 32 + lane];
+            xv[p] = *(const uint4 *)(slots + s * 2 * ROW + p * 512 + lane * 16);
+            gv[p] = *(const uint4 *)(slots + s * 2 * ROW + ROW + p * 512 + lane * 16);
         }
         float ss[NP], gg[NP];
 #pragma unroll
@@ -880,7 +922,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(int ty, long rows
             float xf[8], gf[8], wf[8];
             unpack16(xv[p], ty, xf);
             unpack16(gv[p], ty, gf);
-            unpack16(w[p * 32 + lane], ty, wf);
+            unpack16(wr[p], ty, wf);
             float a = 0.f, b = 0.f;
 #pragma unroll
             for (int t = 0; t < 8; ++t)
@@ -891,30 +933,38 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(int ty, long rows
             ss[p] = a;
             gg[p] = b;
         }
+        // every lane has its values of the slot (used above): the slot may be refilled
+        fence_proxy_async_smem();
+        __syncwarp();
+        issue(s, r + PF * stride);
+        // every piece's two sums across the warp at once (independent shuffle chains),
+        // then each shard adds its pieces' totals
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                ss[p] += __shfl_xor_sync(0xffffffffu, ss[p], off);
+                gg[p] += __shfl_xor_sync(0xffffffffu, gg[p], off);
+            }
         float inv[NP], coef[NP];
-        for (int i = 0; i < g; ++i) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
             float a = 0.f, b = 0.f;
 #pragma unroll
-            for (int p = 0; p < NP; ++p)
-                if (p / sp == i) {
-                    a += ss[p];
-                    b += gg[p];
+            for (int q = 0; q < NP; ++q)
+                if (q / sp == p / sp) {
+                    a += ss[q];
+                    b += gg[q];
                 }
-            const float ri = 1.0f / sqrtf(warp_sum(a) / ds + eps);
-            const float c = warp_sum(b) * ri * ri * ri / ds;
-#pragma unroll
-            for (int p = 0; p < NP; ++p)
-                if (p / sp == i) {
-                    inv[p] = ri;
-                    coef[p] = c;
-                }
+            inv[p] = 1.0f / sqrtf(a / ds + eps);
+            coef[p] = b * inv[p] * inv[p] * inv[p] / ds;
         }
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             float xf[8], gf[8], wf[8], o[8];
             unpack16(xv[p], ty, xf);
             unpack16(gv[p], ty, gf);
-            unpack16(w[p * 32 + lane], ty, wf);
+            unpack16(wr[p], ty, wf);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 o[t] = gf[t] * wf[t] * inv[p] - xf[t] * coef[p];
@@ -923,6 +973,13 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(int ty, long rows
             dx[r * (NP * 32) + p * 32 + lane] = pack16(o, ty);
         }
     }
+    if (!ok) {
+        // after a failed wait: the copies of rows k .. k + PF - 1 were issued; let them land
+        // (each wait bounded again) before the block exits
+        int no_abort = 0;
+        for (long kk = k; kk < k + PF && r_first + kk * stride < rows; ++kk)
+            mbar_wait_limit(&bar[kk % PF], (uint32_t)(kk / PF) & 1, &no_abort, &g_rms_err, WAIT_NS);
+    }
     for (int v = 0; v < nwb; ++v) {   // warp v adds its terms: the same order in every run
         if (wib == v)
 #pragma unroll
@@ -930,12 +987,12 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(int ty, long rows
 #pragma unroll
                 for (int t = 0; t < 8; ++t)
                     if (t < per) {
-                        const int k = (p * 32 + lane) * per + t;
-                        red[k] = (v == 0 ? 0.f : red[k]) + acc[p][t];
+                        const int kc = (p * 32 + lane) * per + t;
+                        red[kc] = (v == 0 ? 0.f : red[kc]) + acc[p][t];
                     }
         __syncthreads();
     }
-    for (int k = threadIdx.x; k < D; k += blockDim.x) dw_part[(long)blockIdx.x * D + k] = red[k];
+    for (int kc = threadIdx.x; kc < D; kc += blockDim.x) dw_part[(long)blockIdx.x * D + kc] = red[kc];
 }
 
 // The same gradient for any shape: one warp per (row, shard) writes dx and the shard's
@@ -971,6 +1028,34 @@ __global__ void rmsnorm_dw_kernel(int ty, long rows, int D, int g, const void *x
     float a = 0.f;
     for (long r = r0; r < r1; ++r) a = fmaf(ldx(dy, ty, r * D + k) * ldx(x, ty, r * D + k), inv_r[r * g + i], a);
     dw_part[(long)blockIdx.y * D + k] = a;
+}
+
+// The general-shape dw pass with 16-byte loads (row bytes a multiple of 16, aligned
+// pointers): thread c of block column y sums dy_k x_k / r over its run of rows for the
+// per16 columns [per16 c, per16 c + per16), each column with its own shard's 1/r.
+__global__ void rmsnorm_dw_vec_kernel(int ty, long rows, int D, int g, const uint4 *x, const uint4 *dy,
+                                      const float *inv_r, long rows_per_part, float *dw_part) {
+    const int per = ty == TY_F32 ? 4 : 8, nc = D / per;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= nc) return;
+    const int ds = D / g;
+    int sh[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) sh[t] = min((c * per + t) / ds, g - 1);
+    const long r0 = (long)blockIdx.y * rows_per_part, r1 = min(rows, r0 + rows_per_part);
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (long r = r0; r < r1; ++r) {
+        float xf[8], gf[8];
+        unpack16(x[r * nc + c], ty, xf);
+        unpack16(dy[r * nc + c], ty, gf);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            if (t < per) a[t] = fmaf(gf[t] * xf[t], inv_r[r * g + sh[t]], a[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+        if (t < per) dw_part[(long)blockIdx.y * D + c * per + t] = a[t];
 }
 
 // dw[k] = sum over the partial rows in order
@@ -1097,7 +1182,7 @@ cudaError_t launch_rmsnorm_shards(int ty, long rows, int D, int g, float eps, co
 }
 
 namespace {
-constexpr long BWD_BLOCKS = 152L * 4;   // fused backward: blocks of 8 warps, grid-strided over rows
+constexpr long BWD_BLOCKS = 152L * 2;   // fused backward: blocks of 8 warps (two resident per SM), grid-strided over rows
 long bwd_np(int ty, int D, int g) {    // pieces per lane of the fused kernel, 0 = other shapes
     const long es = (long)ty_size(ty), np = (long)D * es / 512;
     const bool ok = ((long)(D / g) * es) % 512 == 0 && (np == 1 || np == 2 || np == 4);
@@ -1106,9 +1191,19 @@ long bwd_np(int ty, int D, int g) {    // pieces per lane of the fused kernel, 0
 }  // namespace
 
 namespace {
-// Partial rows of the general-shape dw pass: runs of at least 64 rows, at most 256 parts.
-long dw_parts(long rows) { return std::max<long>(1, std::min<long>(256, (rows + 63) / 64)); }
+// Partial rows of the general-shape dw pass: runs of at least 64 rows, at most 1024 parts.
+long dw_parts(long rows) { return std::max<long>(1, std::min<long>(1024, (rows + 63) / 64)); }
 }  // namespace
+
+template <int NP>
+cudaError_t launch_rms_bwd_rows(long nb, int ty, long rows, int D, int g, float eps, const uint4 *x, const uint4 *w,
+                                const uint4 *dy, uint4 *dx, float *ws, cudaStream_t st) {
+    constexpr uint32_t smem = rms_bwd_smem<NP>();
+    cudaError_t e = cudaFuncSetAttribute(rmsnorm_bwd_rows_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    rmsnorm_bwd_rows_kernel<NP><<<(unsigned)nb, 256, smem, st>>>(ty, rows, D, g, eps, x, w, dy, dx, ws);
+    return cudaGetLastError();
+}
 
 size_t rmsnorm_bwd_ws(int ty, long rows, int D, int g) {
     const size_t fused = (size_t)std::min<long>(BWD_BLOCKS, std::max<long>((rows + 7) / 8, 1)) * D * 4;
@@ -1127,21 +1222,46 @@ cudaError_t launch_rmsnorm_bwd(int ty, long rows, int D, int g, float eps, const
         const long nb = std::min<long>(BWD_BLOCKS, (rows + 7) / 8);
         const uint4 *xv = (const uint4 *)x, *wv = (const uint4 *)w, *gv = (const uint4 *)dy;
         uint4 *dxv = (uint4 *)dx;
-        if (np == 1) rmsnorm_bwd_rows_kernel<1><<<(unsigned)nb, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, gv, dxv, ws);
-        if (np == 2) rmsnorm_bwd_rows_kernel<2><<<(unsigned)nb, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, gv, dxv, ws);
-        if (np == 4) rmsnorm_bwd_rows_kernel<4><<<(unsigned)nb, 256, 0, st>>>(ty, rows, D, g, eps, xv, wv, gv, dxv, ws);
+        cudaError_t e = cudaSuccess;
+        if (np == 1) e = launch_rms_bwd_rows<1>(nb, ty, rows, D, g, eps, xv, wv, gv, dxv, ws, st);
+        if (np == 2) e = launch_rms_bwd_rows<2>(nb, ty, rows, D, g, eps, xv, wv, gv, dxv, ws, st);
+        if (np == 4) e = launch_rms_bwd_rows<4>(nb, ty, rows, D, g, eps, xv, wv, gv, dxv, ws, st);
+        if (e != cudaSuccess) return e;
         dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>((int)nb, D, ws, dw);
     } else if (rows > 0) {
         rmsnorm_bwd_kernel<<<blocks_for(rows * g, 8), 256, 0, st>>>(ty, rows, D, g, eps, x, w, dy, dx, ws);
         const long parts = dw_parts(rows), per = (rows + parts - 1) / parts;
         float *part = ws + ((size_t)rows * g * 4 + 255) / 256 * 64;
-        rmsnorm_dw_kernel<<<dim3(blocks_for(D, 128), (unsigned)parts), 128, 0, st>>>(ty, rows, D, g, x, dy, ws, per,
-                                                                                      part);
+        const long es = (long)ty_size(ty);
+        const bool dw_vec = ((long)D * es) % 16 == 0 && ((uintptr_t)x & 15) == 0 && ((uintptr_t)dy & 15) == 0;
+        if (dw_vec) {
+            const int nc = (int)((long)D * es / 16);
+            rmsnorm_dw_vec_kernel<<<dim3(blocks_for(nc, 64), (unsigned)parts), 64, 0, st>>>(
+                ty, rows, D, g, (const uint4 *)x, (const uint4 *)dy, ws, per, part);
+        } else {
+            rmsnorm_dw_kernel<<<dim3(blocks_for(D, 128), (unsigned)parts), 128, 0, st>>>(ty, rows, D, g, x, dy, ws,
+                                                                                          per, part);
+        }
         dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>((int)parts, D, part, dw);
     } else {
         dw_reduce_kernel<<<blocks_for(D, 256), 256, 0, st>>>(0, D, ws, dw);   // no rows: dw = 0
     }
     return cudaGetLastError();
+}
+
+cudaError_t simt_read_and_clear_error(unsigned *flags, cudaStream_t st) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_rms_err, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return e;
+    if (v) {
+        unsigned z = 0;
+        e = cudaMemcpyToSymbolAsync(g_rms_err, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    *flags |= v;
+    return e;
 }
 
 cudaError_t launch_tpla_expand(int ty, int B, int H, int g, int Dk, int Dr, const void *qa, const void *qp, void *qx,

@@ -359,6 +359,14 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t local_saddr, uint32_t rank
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into another
 // CTA's shared memory (`dst`, `peer_bar`: shared::cluster addresses); completes as
 // transaction bytes on the destination mbarrier.
+// 1-D bulk copy from global memory into this CTA's shared memory, completing on `bar`
+// (both addresses 16-byte aligned, `bytes` a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void *src, uint32_t bytes, uint32_t peer_bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),

@@ -56,6 +56,7 @@ cudaError_t tc_latent_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_decode_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_fused_read_and_clear_error(unsigned *flags, cudaStream_t st);
 cudaError_t tc_bwd_read_and_clear_error(unsigned *flags, cudaStream_t st);
+cudaError_t simt_read_and_clear_error(unsigned *flags, cudaStream_t st);   // the row kernels' bounded waits
 
 // Split-KV latent decode attention (tc_decode.cu): partial latent outputs and
 // log-sum-exps of every (sequence, key split, 128 heads).  qa: q_abs [B][H][512] fp16;

@@ -618,6 +618,7 @@ cudaError_t tc_read_and_clear_error(unsigned int *flags, cudaStream_t st) {
     if (e == cudaSuccess) e = tc_decode_read_and_clear_error(flags, st);
     if (e == cudaSuccess) e = tc_fused_read_and_clear_error(flags, st);
     if (e == cudaSuccess) e = tc_bwd_read_and_clear_error(flags, st);
+    if (e == cudaSuccess) e = simt_read_and_clear_error(flags, st);
     return e;
 }
 

@@ -493,10 +493,14 @@ def test_tpla_full_size_sampled(oracle):
 
 @pytest.mark.parametrize("dtype,rows,d,g", [("bf16", 1000, 512, 1), ("bf16", 777, 512, 2), ("bf16", 50, 1024, 1),
                                             ("f32", 333, 256, 2), ("f32", 9000, 128, 1), ("bf16", 333, 512, 4),
-                                            ("f32", 100, 30, 3), ("bf16", 50, 36, 3)])
+                                            ("f32", 100, 30, 3), ("bf16", 50, 36, 3), ("bf16", 60001, 512, 2),
+                                            ("bf16", 20000, 512, 4)])
 def test_rmsnorm_bwd(oracle, dtype, rows, d, g):
     """The per-shard RMSNorm backward against the oracle's, fused and two-kernel paths;
-    dw (fp32, a sum over rows) must also come out bit-identical on a second call."""
+    dw (fp32, a sum over rows) must also come out bit-identical on a second call.  The
+    60001-row case walks each warp's ring of staged rows many times round (and ends on a
+    ragged last stride); the 20000-row, four-shard case takes the two-kernel path with
+    its 16-byte dw pass over many partial rows."""
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     x = inputs.to_torch(inputs.normal_rows(4, inputs.DEC_C_CACHE, rows, d, 2.0), tdt, (rows, d))
     gy = inputs.to_torch(inputs.normal_rows(5, inputs.DEC_KPE_CACHE, rows, d), tdt, (rows, d))
