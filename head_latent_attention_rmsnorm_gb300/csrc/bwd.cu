@@ -40,6 +40,11 @@ __device__ __forceinline__ float wsum(float v) {
     return v;
 }
 inline unsigned nblocks(long n, int per) { return (unsigned)((n + per - 1) / per); }
+// fp32 pair -> packed bf16x2 (low half = first argument), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *(const uint32_t *)&h;
+}
 
 constexpr int PL = 8;   // values per lane: bands up to 256 wide
 
@@ -258,13 +263,112 @@ __global__ void __launch_bounds__(RW * 32) rms_bwd_kernel(long n_rows, long s_kv
     }
 }
 
-// dw[k] (+)= sum of the partial rows, in order
-__global__ void part_sum_kernel(int nparts, int Dk, const float *part, float *dw, int accumulate) {
-    const int k = blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= Dk) return;
-    float s = accumulate ? dw[k] : 0.f;
-    for (int i = 0; i < nparts; ++i) s += part[(long)i * Dk + k];
-    dw[k] = s;
+// The same backward for bf16 x, w, dx with Dk a multiple of 256 and 16-byte aligned rows:
+// lane l holds the 8-element pieces l, l + 32, ... of a row (NC = Dk / 256 of them), so
+// every load and store is 16 bytes (x, w, dx) or 32 bytes (dy) per lane; the warp's two
+// sums reduce together; dw terms stay in registers and the block's warps add them into
+// one partial row in a fixed order.
+template <int NC>
+__global__ void __launch_bounds__(RW * 32) rms_bwd_vec_kernel(long n_rows, long s_kv, float eps, const uint4 *x,
+                                                              const uint4 *w, const float4 *dy, uint4 *dx,
+                                                              float *part) {
+    constexpr int Dk = NC * 256;
+    __shared__ float red[Dk];
+    const int lane = threadIdx.x % 32, wi = threadIdx.x / 32;
+    float acc[NC][8];
+    float wf[NC][8];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const uint4 q = w[c * 32 + lane];
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            wf[c][2 * e] = __uint_as_float(u[e] << 16);
+            wf[c][2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[c][t] = 0.f;
+    }
+    for (long r = (long)blockIdx.x * RW + wi; r < s_kv; r += (long)gridDim.x * RW) {
+        if (r >= n_rows) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) dx[r * (Dk / 8) + c * 32 + lane] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        float xf[NC][8], gf[NC][8];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint4 q = x[r * (Dk / 8) + c * 32 + lane];
+            const float4 g0 = dy[r * (Dk / 4) + 2 * (c * 32 + lane)], g1 = dy[r * (Dk / 4) + 2 * (c * 32 + lane) + 1];
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                xf[c][2 * e] = __uint_as_float(u[e] << 16);
+                xf[c][2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+            }
+            gf[c][0] = g0.x, gf[c][1] = g0.y, gf[c][2] = g0.z, gf[c][3] = g0.w;
+            gf[c][4] = g1.x, gf[c][5] = g1.y, gf[c][6] = g1.z, gf[c][7] = g1.w;
+        }
+        float ss = 0.f, g = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                ss = fmaf(xf[c][t], xf[c][t], ss);
+                g = fmaf(gf[c][t] * wf[c][t], xf[c][t], g);
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            g += __shfl_xor_sync(0xffffffffu, g, off);
+        }
+        const float ri = 1.0f / sqrtf(ss / (float)Dk + eps);
+        const float cc = g * ri * ri * ri / (float)Dk;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float y0 = gf[c][2 * e] * wf[c][2 * e] * ri - xf[c][2 * e] * cc;
+                const float y1 = gf[c][2 * e + 1] * wf[c][2 * e + 1] * ri - xf[c][2 * e + 1] * cc;
+                o[e] = pack_bf16x2(y0, y1);
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc[c][t] = fmaf(gf[c][t] * xf[c][t], ri, acc[c][t]);
+            dx[r * (Dk / 8) + c * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    for (int v = 0; v < RW; ++v) {   // warp v adds its terms: the same order in every run
+        if (wi == v)
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int k = (c * 32 + lane) * 8 + t;
+                    red[k] = (v == 0 ? 0.f : red[k]) + acc[c][t];
+                }
+        __syncthreads();
+    }
+    for (int k = threadIdx.x; k < Dk; k += blockDim.x) part[(long)blockIdx.x * Dk + k] = red[k];
+}
+
+// dw[k] (+)= sum of the partial rows: thread (gi, c) of a block of 32 x 32 sums the fixed
+// run of parts [gi * n / 32, (gi + 1) * n / 32) of column k = 32 blockIdx.x + c, then the 32
+// run sums are added in order (the same order in every run).
+__global__ void __launch_bounds__(1024) part_sum_kernel(int nparts, int Dk, const float *part, float *dw,
+                                                        int accumulate) {
+    __shared__ float s32[32][33];
+    const int c = threadIdx.x % 32, gi = threadIdx.x / 32, k = blockIdx.x * 32 + c;
+    float s = 0.f;
+    if (k < Dk)
+        for (int i = gi * nparts / 32; i < (gi + 1) * nparts / 32; ++i) s += part[(long)i * Dk + k];
+    s32[gi][c] = s;
+    __syncthreads();
+    if (gi == 0 && k < Dk) {
+        float t = accumulate ? dw[k] : 0.f;
+        for (int j = 0; j < 32; ++j) t += s32[j][c];
+        dw[k] = t;
+    }
 }
 
 }  // namespace
@@ -320,7 +424,7 @@ cudaError_t launch_rope_inv(long rows, int Dr, const float *x, long x_pitch, lon
 
 // Partial dw rows: at most 128, so that the ordered sum over them stays short; each block
 // walks s_kv / (parts * RW) rows per warp.
-size_t rms_bwd_parts(long s_kv) { return (size_t)std::max<long>(1, std::min<long>(128, (s_kv + RW - 1) / RW)); }
+size_t rms_bwd_parts(long s_kv) { return (size_t)std::max<long>(1, std::min<long>(304, (s_kv + RW - 1) / RW)); }
 
 cudaError_t launch_rms_bwd_f32dy(int ty, long n_rows, long s_kv, int Dk, float eps, const void *x, const void *w,
                                  const float *dy, void *dx, float *dw, bool accumulate, float *part,
@@ -330,8 +434,19 @@ cudaError_t launch_rms_bwd_f32dy(int ty, long n_rows, long s_kv, int Dk, float e
     cudaError_t e = cudaFuncSetAttribute(rms_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     ProfScope ps("bwd_rows", st);
-    if (s_kv > 0) rms_bwd_kernel<<<nb, RW * 32, smem, st>>>(n_rows, s_kv, Dk, eps, x, w, ty, dy, dx, part);
-    part_sum_kernel<<<nblocks(Dk, 256), 256, 0, st>>>(s_kv > 0 ? (int)nb : 0, Dk, part, dw, accumulate ? 1 : 0);
+    const bool vec = ty == TY_BF16 && (Dk == 256 || Dk == 512 || Dk == 1024) && ((uintptr_t)x & 15) == 0 &&
+                     ((uintptr_t)w & 15) == 0 && ((uintptr_t)dy & 15) == 0 && ((uintptr_t)dx & 15) == 0;
+    if (s_kv > 0 && vec) {
+        const uint4 *xv = (const uint4 *)x, *wv = (const uint4 *)w;
+        const float4 *gv = (const float4 *)dy;
+        uint4 *dxv = (uint4 *)dx;
+        if (Dk == 256) rms_bwd_vec_kernel<1><<<nb, RW * 32, 0, st>>>(n_rows, s_kv, eps, xv, wv, gv, dxv, part);
+        if (Dk == 512) rms_bwd_vec_kernel<2><<<nb, RW * 32, 0, st>>>(n_rows, s_kv, eps, xv, wv, gv, dxv, part);
+        if (Dk == 1024) rms_bwd_vec_kernel<4><<<nb, RW * 32, 0, st>>>(n_rows, s_kv, eps, xv, wv, gv, dxv, part);
+    } else if (s_kv > 0) {
+        rms_bwd_kernel<<<nb, RW * 32, smem, st>>>(n_rows, s_kv, Dk, eps, x, w, ty, dy, dx, part);
+    }
+    part_sum_kernel<<<nblocks(Dk, 32), 1024, 0, st>>>(s_kv > 0 ? (int)nb : 0, Dk, part, dw, accumulate ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -88,6 +88,40 @@ __global__ void transpose16_kernel(long R, long C, const uint16_t *x, uint16_t *
         if (c0 + k < C && r0 + tx < R) y[(c0 + k) * R + r0 + tx] = t[tx][k];
 }
 
+// The same transpose with 16-byte global accesses (R and C multiples of 8, rows 16-byte
+// aligned): 64 x 64 tiles; a row pitch of 65 elements in shared memory keeps the column
+// gathers of eight consecutive rows on distinct banks.
+__global__ void __launch_bounds__(256) transpose16_vec_kernel(long R, long C, const uint4 *x, uint4 *y) {
+    __shared__ uint16_t t[64][65];
+    const long r0 = (long)blockIdx.y * 64, c0 = (long)blockIdx.x * 64;
+    const int ch = threadIdx.x % 8, rr = threadIdx.x / 8;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int row = rr + 32 * i;
+        if (r0 + row < R && c0 + ch * 8 < C) {
+            const uint4 v = x[((r0 + row) * C + c0) / 8 + ch];
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                t[row][ch * 8 + 2 * e] = (uint16_t)(u[e] & 0xffffu);
+                t[row][ch * 8 + 2 * e + 1] = (uint16_t)(u[e] >> 16);
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int orow = rr + 32 * i;   // output row = input column c0 + orow
+        if (c0 + orow < C && r0 + ch * 8 < R) {
+            uint32_t u[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                u[e] = (uint32_t)t[ch * 8 + 2 * e][orow] | ((uint32_t)t[ch * 8 + 2 * e + 1][orow] << 16);
+            y[((c0 + orow) * R + r0) / 8 + ch] = make_uint4(u[0], u[1], u[2], u[3]);
+        }
+    }
+}
+
 // ------------------------------------------------------------ key-stationary ----
 constexpr uint32_t KBOX = 128 * 128;   // 128 rows x 64 fp16
 constexpr uint32_t QBOX64 = 64 * 128;  // 64 rows x 64 fp16
@@ -593,8 +627,12 @@ cudaError_t launch_bwd_prep_tc(int B, int s_q, int hc, const void *q_nope, const
 cudaError_t launch_transpose16(long R, long C, const void *x, void *y, cudaStream_t st) {
     if (R == 0 || C == 0) return cudaSuccess;
     ProfScope ps("bwd_rows", st);
-    transpose16_kernel<<<dim3((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32)), 256, 0, st>>>(
-        R, C, (const uint16_t *)x, (uint16_t *)y);
+    if (R % 8 == 0 && C % 8 == 0 && ((uintptr_t)x & 15) == 0 && ((uintptr_t)y & 15) == 0)
+        transpose16_vec_kernel<<<dim3((unsigned)((C + 63) / 64), (unsigned)((R + 63) / 64)), 256, 0, st>>>(
+            R, C, (const uint4 *)x, (uint4 *)y);
+    else
+        transpose16_kernel<<<dim3((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32)), 256, 0, st>>>(
+            R, C, (const uint16_t *)x, (uint16_t *)y);
     return cudaGetLastError();
 }
 
