@@ -552,16 +552,24 @@ __global__ void __launch_bounds__(32 * (A_NSM + 4), 1)
             tc_fence_before();
             named_bar_sync(1, 32 * A_NSM);
             if (warp == 4 && lane == 0) mbar_arrive(s_free);
+            // the visibility test only where the chunk can hold hidden keys (warp-uniform)
+            const int j0 = T * 128 + 32 * qr;
+            const bool edge = j0 + 32 > p.kv_need || (p.causal && j0 + 31 > p.q_offset + q0);
+            const bool row_ok = i < p.s_q;
+            const float nDs = -Di * p.scale;
             uint32_t dk[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
                 float dsv[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int key = T * 128 + 32 * qr + c + e;
-                    const bool vis = i < p.s_q && key < p.kv_need && (!p.causal || key <= pos);
-                    const float pr = vis ? ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lse2)) : 0.f;
-                    dsv[e] = pr * (__uint_as_float(dr[c + e]) - Di) * p.scale;
+                    float pr = ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lse2));
+                    if (edge) {
+                        const int key = j0 + c + e;
+                        if (key >= p.kv_need || (p.causal && key > pos)) pr = 0.f;
+                    }
+                    pr = row_ok ? pr : 0.f;
+                    dsv[e] = pr * fmaf(__uint_as_float(dr[c + e]), p.scale, nDs);
                 }
                 dk[c / 2] = pack_f16(dsv[0], dsv[1]);
             }
