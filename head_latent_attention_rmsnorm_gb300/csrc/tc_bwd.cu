@@ -557,21 +557,33 @@ __global__ void __launch_bounds__(32 * (A_NSM + 4), 1)
             const bool edge = j0 + 32 > p.kv_need || (p.causal && j0 + 31 > p.q_offset + q0);
             const bool row_ok = i < p.s_q;
             const float nDs = -Di * p.scale;
+            // (two whole loops rather than a test inside one, so that each stays one straight
+            // run the compiler can interleave)
             uint32_t dk[16];
+            if (edge) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-                float dsv[2];
+                for (int c = 0; c < 32; c += 2) {
+                    float dsv[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float pr = ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lse2));
-                    if (edge) {
+                    for (int e = 0; e < 2; ++e) {
                         const int key = j0 + c + e;
-                        if (key >= p.kv_need || (p.causal && key > pos)) pr = 0.f;
+                        const bool vis = row_ok && key < p.kv_need && (!p.causal || key <= pos);
+                        const float pr = vis ? ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lse2)) : 0.f;
+                        dsv[e] = pr * fmaf(__uint_as_float(dr[c + e]), p.scale, nDs);
                     }
-                    pr = row_ok ? pr : 0.f;
-                    dsv[e] = pr * fmaf(__uint_as_float(dr[c + e]), p.scale, nDs);
+                    dk[c / 2] = pack_f16(dsv[0], dsv[1]);
                 }
-                dk[c / 2] = pack_f16(dsv[0], dsv[1]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float dsv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float pr = ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lse2));
+                        dsv[e] = (row_ok ? pr : 0.f) * fmaf(__uint_as_float(dr[c + e]), p.scale, nDs);
+                    }
+                    dk[c / 2] = pack_f16(dsv[0], dsv[1]);
+                }
             }
             if (ok) {
                 tmem_st16(lb + A_DP + 16 * qr, dk);
