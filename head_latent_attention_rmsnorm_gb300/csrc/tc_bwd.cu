@@ -317,20 +317,44 @@ __global__ void __launch_bounds__(384, 1)
             // every thread has read its S^T and dP^T columns (and the lse / D rows are in
             // place) before any writes P^T / dS^T over them
             named_bar_sync(1, 256);
+            // The visibility test only where the warp's 32 keys can miss some of the half-tile's
+            // queries (warp-uniform), in a loop of its own: a test inside one loop serialises
+            // the exponentials.  lse and D are the same for every lane: 16-byte shared loads.
+            const int kmax = k0 + quad * 32 + 31;
+            const bool interior = kmax < p.kv_need && (!p.causal || kmax <= p.q_offset + q0 + 32 * h) &&
+                                  q0 + 32 * h + 32 <= p.s_q;
             uint32_t pk[16], dk[16];
+            if (interior) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-                float pv[2], dsv[2];
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 l4 = *(const float4 *)(lt + 32 * h + c), d4 = *(const float4 *)(lt + 64 + 32 * h + c);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], dsv[4];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int qi = 32 * h + c + e, i = q0 + qi;
-                    const bool vis = i < p.s_q && j < p.kv_need && (!p.causal || j <= p.q_offset + i);
-                    const float pr = vis ? ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lt[qi])) : 0.f;
-                    pv[e] = pr;
-                    dsv[e] = pr * (__uint_as_float(dr[c + e]) - lt[64 + qi]) * p.scale;
+                    for (int e = 0; e < 4; ++e) {
+                        pv[e] = ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lv[e]));
+                        dsv[e] = pv[e] * (__uint_as_float(dr[c + e]) - dv4[e]) * p.scale;
+                    }
+                    pk[c / 2] = pack_f16(pv[0], pv[1]);
+                    pk[c / 2 + 1] = pack_f16(pv[2], pv[3]);
+                    dk[c / 2] = pack_f16(dsv[0], dsv[1]);
+                    dk[c / 2 + 1] = pack_f16(dsv[2], dsv[3]);
                 }
-                pk[c / 2] = pack_f16(pv[0], pv[1]);
-                dk[c / 2] = pack_f16(dsv[0], dsv[1]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int qi = 32 * h + c + e, i = q0 + qi;
+                        const bool vis = i < p.s_q && j < p.kv_need && (!p.causal || j <= p.q_offset + i);
+                        const float pr = vis ? ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, -lt[qi])) : 0.f;
+                        pv[e] = pr;
+                        dsv[e] = pr * (__uint_as_float(dr[c + e]) - lt[64 + qi]) * p.scale;
+                    }
+                    pk[c / 2] = pack_f16(pv[0], pv[1]);
+                    dk[c / 2] = pack_f16(dsv[0], dsv[1]);
+                }
             }
             if (ok) {
                 tmem_st16(lb + sbuf + 16 * h, pk);
