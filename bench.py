@@ -646,7 +646,8 @@ def run_ours(args, world, rank, local):
 
 def run_case(args):
     """Only `warmup + steps` calls of one workload, no timing or report: the target of
-    ncu captures.  --only prefill|decode; --workload picks a prefill config by name."""
+    ncu captures.  --only prefill|backward|decode|tpla; --workload picks a prefill config by
+    name (backward: one forward call, then the backward calls)."""
     import torch
     from head_latent_attention_rmsnorm_gb300 import build as mla_build
     from head_latent_attention_rmsnorm_gb300 import configs, mla
@@ -657,6 +658,19 @@ def run_case(args):
         cfg = configs.ALL[args.workload] if args.workload else configs.ALL[HEADLINE]
         d, t, out, lse, ws = prefill_setup(cfg, absorbed=args.absorbed, fused=args.fused)
         fn = lambda: prefill_call(cfg, d, t, out, lse, ws, stream, absorbed=args.absorbed, fused=args.fused)  # noqa: E731
+    elif args.only == "backward":
+        cfg = configs.ALL[args.workload] if args.workload else configs.ALL[HEADLINE]
+        d, t, out, lse, ws = prefill_setup(cfg)
+        prefill_call(cfg, d, t, out, lse, ws, stream)
+        del ws
+        g = torch.Generator(device="cuda")
+        g.manual_seed(3)
+        dout = randn(out.shape, 1.0, out.dtype, g)
+
+        def fn():
+            mla.latent_attn_bwd(d, t["q_nope"], t["q_pe"], t["c_kv"], t["k_pe"], t["w_kv_b"], t["rms_w"], out, lse,
+                                dout, q_offset=cfg.q_offset, causal=cfg.causal, head_shard=cfg.head_shard,
+                                stream=stream)
     else:
         cfg = configs.DECODE
         if args.batch:
@@ -762,7 +776,7 @@ def main():
                     help="skip the side workloads (V2-Lite, V3, absorbed, decode, TPLA) and the memory measurement")
     ap.add_argument("--absorbed", action="store_true", help="--only prefill: the absorbed form")
     ap.add_argument("--fused", action="store_true", help="--only prefill: the fused explicit form")
-    ap.add_argument("--only", choices=("prefill", "decode", "tpla"), default=None,
+    ap.add_argument("--only", choices=("prefill", "backward", "decode", "tpla"), default=None,
                     help="run only this workload's calls, without timing (profiling target)")
     ap.add_argument("--workload", default=None, help="prefill workload name for --only prefill")
     ap.add_argument("--batch", type=int, default=0, help="decode batch for --only decode (default 64)")
