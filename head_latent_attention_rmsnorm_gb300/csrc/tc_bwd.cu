@@ -130,8 +130,10 @@ constexpr uint32_t B_STAGE = 5 * QBOX64;   // Q (q_nope lo, hi, rotated q_pe) + 
 constexpr uint32_t B_OFF_LD = B_OFF_Q + 2 * B_STAGE;   // [2][2][64] lse (log2 domain) and D of a q tile
 constexpr uint32_t B_OFF_BAR = B_OFF_LD + 2 * 2 * 64 * 4;
 constexpr uint32_t B_SMEM = B_OFF_BAR + 256 + 1024;
-// TMEM: S^T / P^T double-buffered 0-63 and 64-127, dP^T / dS^T 128-191, dV 192-319, dK
-// (d_nope 128 + band 64) 320-511
+// TMEM: S^T double-buffered 0-63 and 64-127 (P^T then goes in its first 32 columns as fp16
+// and dS^T in the other 32), dP^T 128-191, dV 192-319, dK (d_nope 128 + band 64) 320-511.
+// With dS^T beside P^T, the dP^T columns are free as soon as the softmax has read them,
+// so the next tile's dP^T overlaps this tile's softmax instead of waiting for its dK.
 constexpr uint32_t B_ST = 0, B_DPT = 128, B_DV = 192, B_DK = 320;
 
 struct DkvK {
@@ -152,8 +154,9 @@ __global__ void __launch_bounds__(384, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + B_OFF_BAR);
-    // st_full / pt_free [buffer]: S^T landed / P^T read by the dV MMAs; dpt_full / dpt_free:
-    // dP^T landed / dS^T read by the dK MMAs; ps_full: the softmax warps wrote P^T and dS^T
+    // st_full / pt_free [buffer]: S^T landed / P^T and dS^T read by the dV and dK MMAs;
+    // dpt_full / dpt_free: dP^T landed / read by the softmax warps; ps_full: the softmax
+    // warps wrote P^T and dS^T
     uint64_t *kv_full = bars, *qd_full = bars + 1, *qd_empty = bars + 3, *st_full = bars + 5, *dpt_full = bars + 7;
     uint64_t *ps_full = bars + 8, *pt_free = bars + 9, *dpt_free = bars + 11, *acc_done = bars + 12;
     uint32_t *tslot = (uint32_t *)(bars + 14);
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(384, 1)
                 mma_commit(&st_full[st]);
             }
             __syncwarp();
-            // the dK MMAs of tile t - 1 have read dS^T out of the dP^T columns
+            // the softmax warps have read dP^T of tile t - 1
             if (t >= 1) ok = __all_sync(0xffffffffu, mbar_wait(dpt_free, (t - 1) & 1, abort, err));
             if (!ok) break;
             tc_fence_after();
@@ -275,11 +278,11 @@ __global__ void __launch_bounds__(384, 1)
                 for (int k = 0; k < 4; ++k)   // 16 queries per step
                     mma_ts(tmem + B_DV, tmem + B_ST + st * 64 + k * 8, bdo + (uint64_t)(k * (2048 >> 4)), p.idesc_dv,
                            (t | k) != 0);
-                mma_commit(&pt_free[st]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ts(tmem + B_DK, tmem + B_DPT + k * 8, bq + (uint64_t)(k * (2048 >> 4)), p.idesc_dk, (t | k) != 0);
-                mma_commit(dpt_free);
+                    mma_ts(tmem + B_DK, tmem + B_ST + st * 64 + 32 + k * 8, bq + (uint64_t)(k * (2048 >> 4)), p.idesc_dk,
+                           (t | k) != 0);
+                mma_commit(&pt_free[st]);
                 mma_commit(&qd_empty[st]);
                 if (t == nqt - 1) mma_commit(acc_done);
             }
@@ -315,8 +318,10 @@ __global__ void __launch_bounds__(384, 1)
                 for (int c = 0; c < 32; ++c) sr[c] = dr[c] = 0u;
             }
             // every thread has read its S^T and dP^T columns (and the lse / D rows are in
-            // place) before any writes P^T / dS^T over them
+            // place) before any writes P^T / dS^T over them; dP^T may then take the next tile
+            tc_fence_before();
             named_bar_sync(1, 256);
+            if (warp == 4 && lane == 0) mbar_arrive(dpt_free);
             // The visibility test only where the warp's 32 keys can miss some of the half-tile's
             // queries (warp-uniform), in a loop of its own: a test inside one loop serialises
             // the exponentials.  lse and D are the same for every lane: 16-byte shared loads.
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (ok) {
                 tmem_st16(lb + sbuf + 16 * h, pk);
-                tmem_st16(lb + B_DPT + 16 * h, dk);
+                tmem_st16(lb + sbuf + 32 + 16 * h, dk);
                 tmem_st_wait();
             }
             tc_fence_before();
