@@ -127,7 +127,8 @@ constexpr uint32_t KBOX = 128 * 128;   // 128 rows x 64 fp16
 constexpr uint32_t QBOX64 = 64 * 128;  // 64 rows x 64 fp16
 constexpr uint32_t B_OFF_K = 0, B_OFF_V = 3 * KBOX, B_OFF_Q = B_OFF_V + 2 * KBOX;
 constexpr uint32_t B_STAGE = 5 * QBOX64;   // Q (q_nope lo, hi, rotated q_pe) + dO (lo, hi)
-constexpr uint32_t B_OFF_LD = B_OFF_Q + 2 * B_STAGE;   // [2][2][64] lse (log2 domain) and D of a q tile
+constexpr int B_QST = 3;                     // Q / dO stages: a tile's loads start two tiles ahead of its use
+constexpr uint32_t B_OFF_LD = B_OFF_Q + B_QST * B_STAGE;   // [2][2][64] lse (log2 domain) and D of a q tile
 constexpr uint32_t B_OFF_BAR = B_OFF_LD + 2 * 2 * 64 * 4;
 constexpr uint32_t B_SMEM = B_OFF_BAR + 256 + 1024;
 // TMEM: S^T double-buffered 0-63 and 64-127 (P^T then goes in its first 32 columns as fp16
@@ -157,9 +158,10 @@ __global__ void __launch_bounds__(384, 1)
     // st_full / pt_free [buffer]: S^T landed / P^T and dS^T read by the dV and dK MMAs;
     // dpt_full / dpt_free: dP^T landed / read by the softmax warps; ps_full: the softmax
     // warps wrote P^T and dS^T
-    uint64_t *kv_full = bars, *qd_full = bars + 1, *qd_empty = bars + 3, *st_full = bars + 5, *dpt_full = bars + 7;
-    uint64_t *ps_full = bars + 8, *pt_free = bars + 9, *dpt_free = bars + 11, *acc_done = bars + 12;
-    uint32_t *tslot = (uint32_t *)(bars + 14);
+    uint64_t *kv_full = bars, *qd_full = bars + 1, *qd_empty = bars + 1 + B_QST, *st_full = bars + 1 + 2 * B_QST;
+    uint64_t *dpt_full = st_full + 2, *ps_full = dpt_full + 1, *pt_free = ps_full + 1, *dpt_free = pt_free + 2;
+    uint64_t *acc_done = dpt_free + 1;
+    uint32_t *tslot = (uint32_t *)(acc_done + 2);
     volatile int *abort = (volatile int *)(tslot + 1);
     float *ld = (float *)(smem + B_OFF_LD);
     unsigned *err = &g_tc_bwd_err;
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(384, 1)
 
     if (tid == 0) {
         mbar_init(kv_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < B_QST; ++i) {
             mbar_init(&qd_full[i], 1);
             mbar_init(&qd_empty[i], 1);
         }
@@ -211,16 +213,16 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(smem + B_OFF_V, &mV, kv_full, k0, hl * 128, b);
             tma_load_3d(smem + B_OFF_V + KBOX, &mV, kv_full, k0 + 64, hl * 128, b);
             for (int t = 0; t < nqt; ++t) {
-                const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&qd_empty[st], ((t >> 1) - 1) & 1, abort, err)) break;
-                uint8_t *q = smem + B_OFF_Q + st * B_STAGE;
+                const int qs = t % B_QST;
+                if (t >= B_QST && !mbar_wait(&qd_empty[qs], ((t / B_QST) - 1) & 1, abort, err)) break;
+                uint8_t *q = smem + B_OFF_Q + qs * B_STAGE;
                 const int q0 = (qt0 + t) * 64;
-                mbar_arrive_expect_tx(&qd_full[st], B_STAGE);
-                tma_load_4d(q, &mQn, &qd_full[st], 0, hq, q0, b);
-                tma_load_4d(q + QBOX64, &mQn, &qd_full[st], 64, hq, q0, b);
-                tma_load_4d(q + 2 * QBOX64, &mQr, &qd_full[st], 0, hq, q0, b);
-                tma_load_4d(q + 3 * QBOX64, &mDo, &qd_full[st], 0, hq, q0, b);
-                tma_load_4d(q + 4 * QBOX64, &mDo, &qd_full[st], 64, hq, q0, b);
+                mbar_arrive_expect_tx(&qd_full[qs], B_STAGE);
+                tma_load_4d(q, &mQn, &qd_full[qs], 0, hq, q0, b);
+                tma_load_4d(q + QBOX64, &mQn, &qd_full[qs], 64, hq, q0, b);
+                tma_load_4d(q + 2 * QBOX64, &mQr, &qd_full[qs], 0, hq, q0, b);
+                tma_load_4d(q + 3 * QBOX64, &mDo, &qd_full[qs], 0, hq, q0, b);
+                tma_load_4d(q + 4 * QBOX64, &mDo, &qd_full[qs], 64, hq, q0, b);
             }
         }
     } else if (warp == 1) {
@@ -230,12 +232,13 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = nqt > 0 && __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort, err));
         for (int t = 0; t < nqt && ok; ++t) {
             const int st = t & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&qd_full[st], (t >> 1) & 1, abort, err));
+            const int qs = t % B_QST;
+            ok = __all_sync(0xffffffffu, mbar_wait(&qd_full[qs], (t / B_QST) & 1, abort, err));
             // the dV MMAs of tile t - 2 have read P^T out of this buffer
             if (ok && t >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&pt_free[st], ((t - 2) >> 1) & 1, abort, err));
             if (!ok) break;
             tc_fence_after();
-            const uint8_t *q = smem + B_OFF_Q + st * B_STAGE;
+            const uint8_t *q = smem + B_OFF_Q + (t % B_QST) * B_STAGE;
             if (elect_one()) {
 #pragma unroll
                 for (int kb = 0; kb < 3; ++kb) {
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(384, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(ps_full, t & 1, abort, err));
             if (!ok) break;
             tc_fence_after();
-            const uint8_t *q = smem + B_OFF_Q + st * B_STAGE;
+            const uint8_t *q = smem + B_OFF_Q + (t % B_QST) * B_STAGE;
             if (elect_one()) {
                 const uint64_t bdo = sdesc_mnmajor(q + 3 * QBOX64, QBOX64);   // dO^T: two 64-dim blocks
                 const uint64_t bq = sdesc_mnmajor(q, QBOX64);                 // Q^T: three 64-dim blocks
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(384, 1)
                     mma_ts(tmem + B_DK, tmem + B_ST + st * 64 + 32 + k * 8, bq + (uint64_t)(k * (2048 >> 4)), p.idesc_dk,
                            (t | k) != 0);
                 mma_commit(&pt_free[st]);
-                mma_commit(&qd_empty[st]);
+                mma_commit(&qd_empty[t % B_QST]);
                 if (t == nqt - 1) mma_commit(acc_done);
             }
             __syncwarp();
