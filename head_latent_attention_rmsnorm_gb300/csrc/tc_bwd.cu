@@ -298,14 +298,22 @@ __global__ void __launch_bounds__(384, 1)
         const int j = k0 + row;
         const uint32_t lb = tmem + ((uint32_t)(quad * 32) << 16);
         bool ok = true;
+        // lse (scaled to log2) and D of query tile tt's queries: half 0's thread `row` holds
+        // the value of query row & 63 (lse for rows 0-63, D for 64-127).  Loaded a tile ahead
+        // (the global load's latency had sat at the top of every tile)
+        auto lse_d = [&](int tt) -> float {
+            const int i = (qt0 + tt) * 64 + (row & 63);
+            const long li = ((long)b * p.hc + hq) * p.s_q + i;
+            return i < p.s_q ? (row < 64 ? p.lse[li] * 1.4426950408889634f : p.D[li]) : 0.f;
+        };
+        float ld_next = (h == 0 && nqt > 0) ? lse_d(0) : 0.f;
         for (int t = 0; t < nqt; ++t) {
             const int q0 = (qt0 + t) * 64;
-            // lse (scaled to log2) and D of this tile's queries, in shared memory
+            // this tile's lse and D into shared memory
             float *lt = ld + (t & 1) * 128;
             if (h == 0) {
-                const int i = q0 + (row & 63);
-                const long li = ((long)b * p.hc + hq) * p.s_q + i;
-                lt[row] = i < p.s_q ? (row < 64 ? p.lse[li] * 1.4426950408889634f : p.D[li]) : 0.f;
+                lt[row] = ld_next;
+                if (t + 1 < nqt) ld_next = lse_d(t + 1);
             }
             ok = __all_sync(0xffffffffu, ok && mbar_wait(&st_full[t & 1], (t >> 1) & 1, abort, err));
             ok = __all_sync(0xffffffffu, ok && mbar_wait(dpt_full, t & 1, abort, err));
