@@ -9,7 +9,8 @@ TFLOP/s (algorithmic FLOPs: visible causal pairs x 2 x (192 + 128) per head plus
 K/V reconstruction GEMM), timed per call with CUDA events on the launching stream,
 a 256 MB buffer written between timed calls; ``roofline`` is the attention kernel's,
 ``e2e`` the same call with its inputs copied from pinned host memory and its outputs
-copied back inside every timed step, ``cpu_baseline`` the fp64 oracle on a sample of
+copied back inside every timed step (uploads and downloads on streams of their own,
+overlapping the neighbouring steps' calls; the serial form beside it), ``cpu_baseline`` the fp64 oracle on a sample of
 the same workload on the host's cores.  After the headline, rank 0 at N = 1 also
 times, with the same step count, the V2-Lite and V3-shaped prefills, the V3 absorbed
 form (``other_prefill_configs``), the split-KV decode (``decode``: HBM GB/s), the TPLA
@@ -550,11 +551,78 @@ def e2e_measure(cfg, bufs, steps, warmup, world):
         host_lse.copy_(lse, non_blocking=True)
 
     times = timed(step, steps, warmup, world)
-    ms = max_over_ranks(statistics.mean(times), world)
+    serial_ms = max_over_ranks(statistics.mean(times), world)
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
-    return {"value": round(world * cfg.flops()["total"] / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
+    ms = max_over_ranks(e2e_pipelined(cfg, bufs, host_in, steps, warmup, world), world)
+    flops = world * cfg.flops()["total"]
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps,
+            "mode": "pipelined: two input and two output sets, uploads on one stream and downloads on "
+                    "another, ordered by events, so step i+1's upload and step i-1's download run "
+                    "beside step i's call; the region spans the first upload to the last download",
+            "serial": {"value": round(flops / (serial_ms * 1e-3) / 1e12, 3), "ms_per_step": round(serial_ms, 4),
+                       "mode": "upload, call and download one after another on the call's stream"}}
+
+
+def e2e_pipelined(cfg, bufs, host_in, steps, warmup, world):
+    """Mean ms per step of `steps` pipelined steps (after `warmup`), timed from an event
+    before the first upload to one after the last download, on the call's stream."""
+    import torch
+    d, t, out, lse, ws, _ = bufs
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    sets = [(t, out, lse), ({k: torch.empty_like(v) for k, v in t.items()}, torch.empty_like(out),
+                            torch.empty_like(lse))]
+    h_out = [(torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+              torch.empty(lse.shape, dtype=lse.dtype).pin_memory()) for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+    stream = comp.cuda_stream
+
+    def run(n, start_ev):
+        up.wait_event(start_ev)
+        down.wait_event(start_ev)
+        for i in range(n):
+            j = i & 1
+            ti, oj, lj = sets[j]
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(in_free[j])
+                for k, v in host_in.items():
+                    ti[k].copy_(v, non_blocking=True)
+                in_ready[j].record(up)
+            comp.wait_event(in_ready[j])
+            if i >= 2:
+                comp.wait_event(out_free[j])
+            prefill_call(cfg, d, ti, oj, lj, ws, stream)
+            in_free[j].record(comp)
+            out_ready[j].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(out_ready[j])
+                h_out[j][0].copy_(oj, non_blocking=True)
+                h_out[j][1].copy_(lj, non_blocking=True)
+                out_free[j].record(down)
+        for j in range(min(n, 2)):
+            comp.wait_event(out_free[j])
+
+    s0 = torch.cuda.Event()
+    s0.record(comp)
+    run(warmup, s0)
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    run(steps, a)
+    b.record(comp)
+    torch.cuda.synchronize()
+    barrier(world)
+    ok = torch.equal(h_out[(steps - 1) & 1][0].to(out.device), out) if steps >= 1 else True
+    if not ok:
+        raise RuntimeError("pipelined end-to-end output differs from the device-resident call's")
+    return a.elapsed_time(b) / steps
 
 
 # -------------------------------------------------------------- our arm ----
@@ -583,7 +651,9 @@ def run_ours(args, world, rank, local):
     p_ms = head["ms_per_call"]
     e2e = None
     try:
-        e2e = e2e_measure(pcfg, bufs, max(1, min(steps, 20)), min(warmup, 3), world)
+        with ClockSampler(local) as clk_e2e:
+            e2e = e2e_measure(pcfg, bufs, max(1, min(steps, 20)), min(warmup, 3), world)
+        e2e["clocks"] = clk_e2e.summary()
     except Exception as ex:  # keep the kernel numbers even if pinning fails
         e2e = {"value": None, "unit": "TFLOP/s", "error": str(ex)[:200]}
     del bufs
