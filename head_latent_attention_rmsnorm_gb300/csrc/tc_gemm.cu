@@ -258,15 +258,15 @@ __global__ void __launch_bounds__(256, 1)
 
 // ---------------------------------------------------------------- pair kernel ----
 // The same GEMM on 256 x 256 tiles computed by a cluster of two CTAs (two SMs) with
-// cta_group::2 MMAs (M = 256): CTA r holds A rows [m0 + 128 r, +128) and, of the 256 B
-// rows (output columns), [n0 + 64 r, +64) and [n0 + 128 + 64 r, +64), so every MMA reads
-// half of its operand bytes from each SM.  A one-CTA 128 x 256 tile loads 12 KB of
-// operands per 16-deep MMA step into its SM; the pair loads 8 KB per SM, and the
-// operand loads (about 90-130 GB/s per SM from L2) pace this GEMM.  The
-// leader (rank 0) issues the MMAs from two warps, each owning 128 output columns
-// (N = 128 per MMA: 64 columns from each CTA); both CTAs load, and both drain their own
-// accumulator rows: 16-bit outputs through a per-warp shared-memory staging of the whole
-// tile slice (accumulator released before the stores), written in whole 128-byte rows.
+// cta_group::2 MMAs (M = 256, N = 256): CTA r holds A rows [m0 + 128 r, +128) and B rows
+// (output columns) [n0 + 128 r, +128), so every MMA reads half of its operand bytes from
+// each SM.  Shared memory bandwidth paces this GEMM: per CTA and tile the TMA writes 256 KB
+// of operands, the MMAs read A and B once (256 KB) and the epilogue stages 64 KB in and
+// out, at 128 bytes per clock (N = 128 MMAs from two issuers read A twice: 768 KB, ~2.9
+// us per tile).  The leader (rank 0) issues the MMAs from one warp; both CTAs load, and
+// both drain their own accumulator rows: 16-bit outputs through a per-warp shared-memory
+// staging of the whole tile slice (accumulator released before the stores), written in
+// whole 128-byte rows.
 constexpr int PST = 5;   // stages of the pair kernel's ring
 constexpr uint32_t PA_BYTES = 128 * BK * 2, PB_BYTES = 128 * BK * 2;
 constexpr uint32_t PC_BYTES = 4 * 4 * 4096;   // four epilogue warps x a 32-row x 256-column 16-bit tile slice
@@ -305,10 +305,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     if (tid == 0) {
         for (int s = 0; s < PST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);   // one commit per issuing thread
+            mbar_init(&empty[s], 1);   // the issuer's commit
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&acc_full[a], 2);
+            mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], 8);   // the epilogue warps of both CTAs
         }
         *abort = 0;
@@ -344,12 +344,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 const CUtensorMap *ma = w.prob ? &ta1 : &ta0, *mb = w.prob ? &tb1 : &tb0;
                 const int ar = w.m0 + 128 * (int)rank;
                 const int a_r = ar % q.a_rows_per_z, a_z = q.a_zbase + ar / q.a_rows_per_z + w.batch * q.a_z_per_batch;
-                int b_r[2], b_z[2];
-                for (int h = 0; h < 2; ++h) {
-                    const int br = w.n0 + 128 * h + 64 * (int)rank;
-                    b_r[h] = br % q.b_rows_per_z;
-                    b_z[h] = q.b_zbase + br / q.b_rows_per_z + w.batch * q.b_z_per_batch;
-                }
+                const int br = w.n0 + 128 * (int)rank;
+                const int b_r = br % q.b_rows_per_z, b_z = q.b_zbase + br / q.b_rows_per_z + w.batch * q.b_z_per_batch;
                 for (int kb = 0; kb < q.K / BK; ++kb, ++it) {
                     const int s = it % PST;
                     if (it >= PST && !mbar_wait(&empty[s], ((it / PST) - 1) & 1, abort, &g_tc_gemm_err)) {
@@ -359,16 +355,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                     if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (PA_BYTES + PB_BYTES));
                     const uint32_t bar = full0 + s * 8;
                     tma_load_3d_pair(sA + s * PA_BYTES, ma, bar, kb * BK, a_r, a_z);
-                    tma_load_3d_pair(sB + s * PB_BYTES, mb, bar, kb * BK, b_r[0], b_z[0]);
-                    tma_load_3d_pair(sB + s * PB_BYTES + PB_BYTES / 2, mb, bar, kb * BK, b_r[1], b_z[1]);
+                    tma_load_3d_pair(sB + s * PB_BYTES, mb, bar, kb * BK, b_r, b_z);
                 }
             }
         }
-    } else if (rank == 0 && (warp == 1 || warp == 6)) {
-        // -------------------------- MMA issuers (leader): output columns [128 h, +128)
+    } else if (rank == 0 && warp == 1) {
+        // ----------------------------------------------------- MMA issuer (leader)
         // (warp-uniform loop; one elected lane issues)
         {
-            const int h = warp == 1 ? 0 : 1;
             int it = 0, lt = 0;
             bool ok = true;
             for (int t = pair; t < p.total && ok; t += pairs, ++lt) {
@@ -378,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 if (lt >= 2 &&
                     !__all_sync(0xffffffffu, mbar_wait_cluster(&acc_empty[a], ((lt >> 1) - 1) & 1, abort, &g_tc_gemm_err)))
                     break;
-                const uint32_t d = tmem + a * 256 + h * 128;
+                const uint32_t d = tmem + a * 256;
                 const int nk = p.pr[w.prob].K / BK;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % PST;
@@ -388,7 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                     }
                     tc_fence_after();
                     const uint64_t da = sdesc_kmajor(sA + s * PA_BYTES);
-                    const uint64_t db = sdesc_kmajor(sB + s * PB_BYTES + h * (PB_BYTES / 2));
+                    const uint64_t db = sdesc_kmajor(sB + s * PB_BYTES);
                     if (elect_one()) {
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) mma_ss_pair(d, da + 2 * k, db + 2 * k, p.idesc, (kb | k) != 0);
@@ -589,13 +583,17 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         if (probs[i].accumulate && probs[i].out_kind != 2) return cudaErrorInvalidValue;
         maxN = std::max(maxN, probs[i].N);
     }
-    const int BN = maxN >= 256 ? 256 : (maxN >= 128 ? 128 : 64);
+    int BN = maxN >= 256 ? 256 : (maxN >= 128 ? 128 : 64);
     if (probs[0].a_mn && BN == 256) return cudaErrorInvalidValue;   // m-major A: single-CTA tiles only
-    // 256-wide problems run on SM pairs: 256 x 256 tiles, A boxes of 128 rows per CTA,
-    // B boxes of 64 rows (two per CTA)
-    const bool pair = BN == 256;
-    for (int i = 0; i < n_probs; ++i)
+    // 256-wide problems run on SM pairs: 256 x 256 tiles, A and B boxes of 128 rows per
+    // CTA (a B box must not straddle two z blocks of the operand: otherwise 128-wide
+    // single-CTA tiles)
+    bool pair = BN == 256;
+    for (int i = 0; i < n_probs; ++i) {
         if (pair && probs[i].accumulate) return cudaErrorInvalidValue;   // accumulation: single-CTA tiles only
+        if (probs[i].B.rows_per_z % 128 != 0) pair = false;
+    }
+    if (BN == 256 && !pair) BN = 128;
     const int TM = pair ? 256 : BM, TN = BN;
     CUtensorMap maps[4];
     GemmK p{};
@@ -611,7 +609,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
         const GemmProblem &g = probs[i];
         cudaError_t e = g.a_mn ? make_operand_map_mn(&maps[2 * i], g.A) : make_operand_map(&maps[2 * i], g.A, BM);
         if (e != cudaSuccess) return e;
-        e = make_operand_map(&maps[2 * i + 1], g.B, pair ? 64 : BN);
+        e = make_operand_map(&maps[2 * i + 1], g.B, pair ? 128 : BN);
         if (e != cudaSuccess) return e;
         q.M = g.M;
         q.N = g.N;
@@ -642,7 +640,7 @@ cudaError_t tc_gemm_group(const GemmProblem *probs, int n_probs, bool f16, cudaS
     ProfScope ps("tc_gemm", st);
     switch (BN) {
         case 256:
-            p.idesc = tc::idesc_f16(256, 128, f16);   // cta_group::2: M = 256 across the pair
+            p.idesc = tc::idesc_f16(256, 256, f16);   // cta_group::2: M = 256 across the pair
             return launch_gemm_pair(maps, p, st);
         case 128:
             p.idesc = tc::idesc_f16(BM, 128, f16, false, p.a_mn != 0);
