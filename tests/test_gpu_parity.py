@@ -247,6 +247,28 @@ def test_sp8_rank_sweep_concatenates_and_matches_oracle(oracle):
         check_lse(lses[-1][:, h0:h0 + 1, i0:i0 + n], rl)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_long_keys_rows_and_tail_tile(oracle, causal):
+    """30000 keys (235 key tiles per (query tile, head) unit, a ragged last tile): sampled
+    rows against the oracle, causal at the end of the sequence and non-causal, and the last
+    query tile computed alone comes out bit-identical to the same tile of a longer call."""
+    s_kv, s_q = 30000, 384
+    q_off = s_kv - s_q if causal else 0
+    cfg = dataclasses.replace(configs.V2LITE, name="cut3", s_kv=s_kv, s_q=s_q, q_offset=q_off, causal=causal)
+    full_in = dev(inputs.prefill_inputs(cfg))
+    out, lse = run_prefill(cfg, full_in)
+    tail = dict(full_in, q_nope=full_in["q_nope"][:, 256:].contiguous(), q_pe=full_in["q_pe"][:, 256:].contiguous())
+    o2, l2 = run_prefill(dataclasses.replace(cfg, s_q=128), tail, q_offset=q_off + 256)
+    assert torch.equal(o2, out[:, 256:]) and torch.equal(l2, lse[:, :, 256:])
+    for q0, h0 in ((0, 3), (200, 9), (s_q - 40, 15)):
+        n = 40
+        inp = inputs.prefill_inputs(cfg, q_rows=(q_off + q0, q_off + q0 + n))
+        sub = dict(inp, q_nope=inp["q_nope"][:, :, h0:h0 + 1], q_pe=inp["q_pe"][:, :, h0:h0 + 1])
+        ro, rl = oracle_prefill(oracle, cfg, sub, q_offset=q_off + q0, head_begin=h0)
+        check_out(out[:, q0:q0 + n, h0:h0 + 1], ro, torch.bfloat16, "rows %d head %d" % (q0, h0))
+        check_lse(lse[:, h0:h0 + 1, q0:q0 + n], rl, "lse rows %d head %d" % (q0, h0))
+
+
 # ------------------------------------------------------------------- decode ----
 def run_decode(cfg, inp, n_splits, partials=True):
     d = mla.dims(cfg.n_heads, cfg.d_kv, cfg.d_nope, cfg.d_rope, cfg.d_v, cfg.rope_base)
