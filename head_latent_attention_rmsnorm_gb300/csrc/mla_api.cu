@@ -481,8 +481,7 @@ mla_status decode_simt(const Decode &p, float scale, const mla_dims *d, const vo
     const size_t ein = ty_size(p.tin);
     const long Dh = p.Dn + p.Dv;
     long rows = (long)p.B * p.H;
-    MLA_TRY(launch_rope_table(p.L - 1, 1, p.Dr, d->rope_base, w.rtab, st));
-    MLA_TRY(launch_rope_rows(p.tin, p.tmid, rows, p.Dr, q_pe, p.L - 1, 1, 1, w.rtab, p.L - 1, w.qpe, st));
+    MLA_TRY(launch_rope_rows_at(p.tin, p.tmid, rows, p.Dr, q_pe, p.L - 1, d->rope_base, w.qpe, st));
     GemmArgs g{};
     g.M = p.B;
     g.N = p.Dk;
@@ -953,7 +952,7 @@ mla_status decode_call(const mla_dims *dims, mla_dtype dtype, int B, int kv_len,
                     rng(part_out, (size_t)p.n * rows * p.Dk * 4), rng(part_lse, (size_t)p.n * rows * 4)};
     st = check_alias(in, 5, outs, 5);
     if (st != MLA_OK) return st;
-    DecodeWs w = decode_ws(p, workspace, own);
+    DecodeWs w = decode_ws(p, workspace, true);   // its partials buffer also serves as fp16 scratch
     float *po = own ? w.po : part_out;
     float *pl = own ? w.pl : part_lse;
     cudaStream_t cs = (cudaStream_t)cuda_stream;
@@ -961,11 +960,10 @@ mla_status decode_call(const mla_dims *dims, mla_dtype dtype, int B, int kv_len,
     g_last_path = p.tc ? 2 : 1;
     if (p.tc) {
         const long rows = (long)p.B * p.H;
-        MLA_TRY(launch_rope_table(p.L - 1, 1, p.Dr, dims->rope_base, w.rtab, cs));
-        MLA_TRY(launch_rope_rows(p.tin, TY_F16, rows, p.Dr, q_pe, p.L - 1, 1, 1, w.rtab, p.L - 1, w.qpe, cs));
+        MLA_TRY(launch_rope_rows_at(p.tin, TY_F16, rows, p.Dr, q_pe, p.L - 1, dims->rope_base, w.qpe, cs));
         TcDecode t{p.B, p.L, p.n, p.H, p.Dk, p.Dn, p.Dr, p.Dv, p.chunk, scale, dims->rope_base, p.g};
-        return cuda_status(tc_decode(t, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w.qabs, w.qpe,
-                                     w.olat, w.qx, w.qpx, cs));
+        return cuda_status(tc_decode(t, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w.po, !own,
+                                     w.qabs, w.qpe, w.olat, w.qx, w.qpx, cs));
     }
     return decode_simt(p, scale, dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out, lse, po, pl, w, cs);
 }

@@ -39,6 +39,10 @@ cudaError_t launch_latent_prep(int tin, int tout, int B, int s_kv, int n_rows, i
 
 // RoPE on `rows` rows of width Dr; row r sits at position pos0 + (r / pos_div) % pos_mod;
 // `tab` starts at position tab_pos0.
+// Rows at one position `pos` (the decode query): RoPE with the position's table computed
+// inside the launch (one launch instead of launch_rope_table + launch_rope_rows).
+cudaError_t launch_rope_rows_at(int tin, int tout, long rows, int Dr, const void *x, long pos, float base, void *y,
+                                cudaStream_t st);
 cudaError_t launch_rope_rows(int tin, int tout, long rows, int Dr, const void *x, long pos0, long pos_div,
                              long pos_mod, const float2 *tab, long tab_pos0, void *y, cudaStream_t st);
 
@@ -93,6 +97,9 @@ struct AttnArgs {
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
 
 // lse-combine: part_out [n][rows][D], part_lse [n][rows] -> out [rows][D] (storage tout), lse [rows]
+// The same merge over fp16 partials (n <= 32 splits, D % 128 == 0, D <= 1024), bf16 out.
+cudaError_t launch_lse_combine16(int n, long rows, int D, const void *po, const float *pl, void *out, float *lse,
+                                 cudaStream_t st);
 cudaError_t launch_lse_combine(int tout, int n, long rows, int D, const float *po, const float *pl, void *out,
                                float *lse, cudaStream_t st);
 

@@ -333,6 +333,19 @@ __global__ void rope_rows_kernel(long rows, int Dr, const void *x, int tin, long
     rope_band(x, tin, r * Dr, y, tout, r * Dr, Dr, tab + (pos - tab_pos0) * (Dr / 2), threadIdx.x % 32);
 }
 
+// RoPE of rows that all sit at one position (the decode query): the block computes the
+// position's (cos, sin) pairs into shared memory as rope_table_kernel would, then one warp
+// rotates each row.
+__global__ void rope_rows_at_kernel(long rows, int Dr, const void *x, int tin, long pos,
+                                    const __grid_constant__ RopeTheta th, void *y, int tout) {
+    __shared__ float2 cs[ROPE_MAX_HALF];
+    for (int i = threadIdx.x; i < Dr / 2; i += blockDim.x) cs[i] = rope_cs(pos, th.v[i]);
+    __syncthreads();
+    long r = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (r >= rows) return;
+    rope_band(x, tin, r * Dr, y, tout, r * Dr, Dr, cs, threadIdx.x % 32);
+}
+
 __global__ void convert_kernel(const void *x, int tin, void *y, int tout, long n) {
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
         stx(y, tout, i, ldx(x, tin, i));
@@ -535,8 +548,8 @@ __global__ void lse_combine_kernel(int n, long rows, int D, const float *po, con
 // split s's weight, each lane accumulates D/128 float4 columns in registers with all
 // of them loaded as 16-byte vectors.  Same weights and the same split order as
 // lse_combine_kernel, so the results are identical.
-template <typename TO>
-__global__ void lse_combine_vec_kernel(int n, long rows, int D, const float *po, const float *pl, TO *out,
+template <typename TO, typename TP = float>
+__global__ void lse_combine_vec_kernel(int n, long rows, int D, const TP *po, const float *pl, TO *out,
                                        float *lse) {
     const long r = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -558,11 +571,18 @@ __global__ void lse_combine_vec_kernel(int n, long rows, int D, const float *po,
     for (int s = 0; s < n; ++s) {
         const float ws = __shfl_sync(0xffffffffu, w, s);
         if (ws > 0.f) {
-            const float4 *src = (const float4 *)(po + ((long)s * rows + r) * D) + lane;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 if (k < nc) {
-                    const float4 v = src[k * 32];
+                    float4 v;
+                    if (sizeof(TP) == 4) {
+                        v = ((const float4 *)(po + ((long)s * rows + r) * D))[lane + k * 32];
+                    } else {   // fp16 partials: four per lane, the same elements
+                        const uint2 u = ((const uint2 *)(po + ((long)s * rows + r) * D))[lane + k * 32];
+                        const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+                        const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+                        v = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    }
                     acc[k].x = fmaf(ws, v.x, acc[k].x);
                     acc[k].y = fmaf(ws, v.y, acc[k].y);
                     acc[k].z = fmaf(ws, v.z, acc[k].z);
@@ -627,6 +647,17 @@ cudaError_t launch_rope_rows(int tin, int tout, long rows, int Dr, const void *x
     ProfScope ps("rope_rows", st);
     rope_rows_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(rows, Dr, x, tin, pos0, pos_div, pos_mod, tab, tab_pos0,
                                                           y, tout);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_rows_at(int tin, int tout, long rows, int Dr, const void *x, long pos, float base, void *y,
+                                cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    if (Dr / 2 > ROPE_MAX_HALF) return cudaErrorInvalidValue;
+    RopeTheta th;
+    for (int t = 0; t < Dr / 2; ++t) th.v[t] = pow((double)base, -2.0 * (double)t / (double)Dr);
+    ProfScope ps("rope_rows", st);
+    rope_rows_at_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(rows, Dr, x, tin, pos, th, y, tout);
     return cudaGetLastError();
 }
 
@@ -709,6 +740,16 @@ cudaError_t launch_lse_combine(int tout, int n, long rows, int D, const float *p
             <<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, (__nv_bfloat16 *)out, lse);
     else
         lse_combine_kernel<<<blocks_for(rows, 8), 256, 0, st>>>(n, rows, D, po, pl, out, tout, lse);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse_combine16(int n, long rows, int D, const void *po, const float *pl, void *out, float *lse,
+                                 cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    if (n > 32 || D % 128 != 0 || D > 1024 || (((uintptr_t)po | (uintptr_t)out) & 7) != 0) return cudaErrorInvalidValue;
+    ProfScope ps("lse_combine", st);
+    lse_combine_vec_kernel<__nv_bfloat16, __half><<<blocks_for(rows, 8), 256, 0, st>>>(
+        n, rows, D, (const __half *)po, pl, (__nv_bfloat16 *)out, lse);
     return cudaGetLastError();
 }
 

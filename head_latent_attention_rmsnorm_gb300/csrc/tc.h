@@ -52,8 +52,13 @@ cudaError_t tc_bwd_attn(const TcPrefill &p, int h0, int nh, const void *kws, con
 cudaError_t tc_absorbed_prefill(const TcPrefill &p, const void *q_nope, const void *w_kv_b, void *out,
                                 float *lse, const void *chat, const void *kpe, const void *qpe, void *qabs,
                                 void *olat, void *w16, cudaStream_t st);
+// po / pl: the split partials (the caller's, fp32, when user_po; else the workspace's);
+// po16: workspace room for the partials in fp16 (the plain decode with n <= 32 splits merges
+// fp16 partials: written so by the kernel, or rounded from the caller's fp32 ones, so the
+// output does not depend on whether the caller asked for the partials).
 cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, const void *c_cache,
                       const void *kpe_cache, const void *w_kv_b, void *out, float *lse, float *po, float *pl,
-                      void *qabs, void *qpe, void *olat, void *qx, void *qpx, cudaStream_t st);
+                      void *po16, bool user_po, void *qabs, void *qpe, void *olat, void *qx, void *qpx,
+                      cudaStream_t st);
 
 }  // namespace mla

@@ -124,6 +124,7 @@ struct DecK {
     const __nv_bfloat16 *cache, *kpe;   // [B][kv_len][512], [B][kv_len][64] (for the L2 prefetch)
     float scale_log2;
     float *po, *pl;                     // partials [split][b][h][512], [split][b][h]
+    int po16;                           // the partial outputs in fp16 (else fp32)
     long po_s, po_b, pl_s, pl_b;
     uint32_t idesc_s, idesc_pv;
     // TPLA with two latent shards: rows [b][i][h] of g = 2 shards x shard_rows heads
@@ -677,19 +678,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     float ov[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(o[e]) * inv_l;
-                    if (cc >= 1) {   // the previous chunk's store has read the buffer
-                        if (lane == 0) bulk_wait_read<0>();
-                        __syncwarp();
-                    }
+                    if (!p.po16) {
+                        if (cc >= 1) {   // the previous chunk's store has read the buffer
+                            if (lane == 0) bulk_wait_read<0>();
+                            __syncwarp();
+                        }
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        *(float4 *)(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
-                            make_float4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {   // columns in fp16 units of the map: 2 per fp32 value
-                        tma_store_2d(&mP, buf, (od0 + 32 * cc) * 2, prow);
-                        bulk_commit();
+                        for (int v = 0; v < 8; ++v)
+                            *(float4 *)(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+                                make_float4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {   // columns in fp16 units of the map: 2 per fp32 value
+                            tma_store_2d(&mP, buf, (od0 + 32 * cc) * 2, prow);
+                            bulk_commit();
+                        }
+                    } else {
+                        // fp16: two chunks fill one 128-byte row (chunk cc in its half cc & 1),
+                        // one TMA tile store per pair
+                        const int h = cc & 1;
+                        if (cc >= 2 && h == 0) {   // the previous pair's store has read the buffer
+                            if (lane == 0) bulk_wait_read<0>();
+                            __syncwarp();
+                        }
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            *(uint4 *)(buf + lane * 128 + (((4 * h + v) ^ (lane & 7)) << 4)) =
+                                make_uint4(pack_f16(ov[8 * v], ov[8 * v + 1]), pack_f16(ov[8 * v + 2], ov[8 * v + 3]),
+                                           pack_f16(ov[8 * v + 4], ov[8 * v + 5]), pack_f16(ov[8 * v + 6], ov[8 * v + 7]));
+                        if (h == 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&mP, buf, od0 + 32 * (cc - 1), prow);
+                                bulk_commit();
+                            }
+                        }
                     }
                     // dims od0 + 32 cc .. +31: half (od / 32) & 1 of the row of box od / 64
                     const int od = od0 + 32 * cc;
@@ -733,7 +757,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 // kpe [B][L][64] bf16; po [n][B][H][512] fp32, pl [n][B][H].
 cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache, const void *kpe, int B, long L,
                                int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st,
-                               int shard_rows) {
+                               int shard_rows, bool po16) {
+    if (po16 && shard_rows) return cudaErrorInvalidValue;   // the two-shard units write fp32 only
     const long units = (long)B * n_splits * (H / ROWS);
     if (units == 0) return cudaSuccess;
     if (shard_rows && (shard_rows % ROWS != 0 || H != 2 * shard_rows)) return cudaErrorInvalidValue;
@@ -746,9 +771,14 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
         unsigned long long dp[2] = {64, (unsigned long long)B * H}, sp[1] = {128};
         if ((e = make_tma_map(&mQp, qp, 2, dp, sp, box)) != cudaSuccess) return e;
     }
-    {   // the fp32 partial output as rows of 1024 16-bit units (2 KB), boxes of 32 x 32 fp32
+    if (!po16) {   // the fp32 partial output as rows of 1024 16-bit units (2 KB), boxes of 32 x 32 fp32
         unsigned long long d[2] = {1024, (unsigned long long)n_splits * B * H};
         unsigned long long s[1] = {2048};
+        unsigned box[2] = {64, 32};
+        if ((e = make_tma_map(&mP, po, 2, d, s, box)) != cudaSuccess) return e;
+    } else {       // fp16 partials: rows of 512 (1 KB), boxes of 32 rows x 64
+        unsigned long long d[2] = {512, (unsigned long long)n_splits * B * H};
+        unsigned long long s[1] = {1024};
         unsigned box[2] = {64, 32};
         if ((e = make_tma_map(&mP, po, 2, d, s, box)) != cudaSuccess) return e;
     }
@@ -787,6 +817,7 @@ cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache
     p.idesc_s = idesc_f16(128, NK, false);
     p.idesc_pv = idesc_f16(128, 256, false, true);
     p.shard_rows = shard_rows;
+    p.po16 = po16 ? 1 : 0;
     ProfScope ps("tc_decode_attn", st);
     auto kern = shard_rows ? tc_decode_kernel<true> : tc_decode_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);

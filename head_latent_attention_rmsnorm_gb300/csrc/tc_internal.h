@@ -61,12 +61,12 @@ cudaError_t simt_read_and_clear_error(unsigned *flags, cudaStream_t st);   // th
 // Split-KV latent decode attention (tc_decode.cu): partial latent outputs and
 // log-sum-exps of every (sequence, key split, 128 heads).  qa: q_abs [B][H][512] fp16;
 // qp: rotated q_pe [B][H][64] fp16; cache [B][L][512], kpe [B][L][64] bf16;
-// po [n_splits][B][H][512] fp32, pl [n_splits][B][H] fp32.  H % 128 == 0.
+// po [n_splits][B][H][512] fp32 (po16: fp16), pl [n_splits][B][H] fp32.  H % 128 == 0.
 // shard_rows > 0 (TPLA, two latent shards): the rows are [B][2][shard_rows] with
 // shard_rows % 128 == 0, rows of shard i attend over latent dims [256 i, 256 i + 256)
 // and the RoPE band only, and only those dims of their partial output are written.
 cudaError_t launch_decode_attn(const void *qa, const void *qp, const void *cache, const void *kpe, int B, long L,
                                int H, int n_splits, long chunk, float scale, float *po, float *pl, cudaStream_t st,
-                               int shard_rows = 0);
+                               int shard_rows = 0, bool po16 = false);
 
 }  // namespace mla

@@ -494,7 +494,8 @@ bool tc_decode_supported(int Dk, int Dn, int Dr, int Dv, int H) {
 
 cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, const void *c_cache,
                       const void *kpe_cache, const void *w_kv_b, void *out, float *lse, float *po, float *pl,
-                      void *qabs, void *qpe, void *olat, void *qx, void *qpx, cudaStream_t st) {
+                      void *po16, bool user_po, void *qabs, void *qpe, void *olat, void *qx, void *qpx,
+                      cudaStream_t st) {
     (void)q_pe;   // rotated into qpe (fp16) by the caller
     const long Dh = p.Dn + p.Dv, rows = (long)p.B * p.H;
     cudaError_t e;
@@ -528,11 +529,18 @@ cudaError_t tc_decode(const TcDecode &p, const void *q_nope, const void *q_pe, c
         // 3. each shard's merge over its own dims -> o_lat (bf16), shard lse [g][B][H]
         e = launch_tpla_combine(TY_BF16, p.n, p.B, p.H, p.g, p.Dk, po, pl, olat, lse, st);
     } else {
-        // 2. per (sequence, split, 128 heads): partial latent output and its lse
-        e = launch_decode_attn(qabs, qpe, c_cache, kpe_cache, p.B, p.L, p.H, p.n, p.chunk, p.scale, po, pl, st);
+        // 2. per (sequence, split, 128 heads): partial latent output and its lse; 3. the
+        //    log-sum-exp merge of the splits -> o_lat (bf16) and lse.  Up to 32 splits the
+        //    merge reads fp16 partials (half the bytes of fp32 to write and to read back).
+        const bool f16 = p.n <= 32;
+        const bool direct16 = f16 && !user_po;
+        e = launch_decode_attn(qabs, qpe, c_cache, kpe_cache, p.B, p.L, p.H, p.n, p.chunk, p.scale,
+                               direct16 ? (float *)po16 : po, pl, st, 0, direct16);
         if (e != cudaSuccess) return e;
-        // 3. log-sum-exp merge of the splits -> o_lat (bf16) and lse
-        e = launch_lse_combine(TY_BF16, p.n, rows, p.Dk, po, pl, olat, lse, st);
+        if (f16 && user_po) e = launch_convert(TY_F32, po, TY_F16, po16, (long)p.n * rows * p.Dk, st);
+        if (e != cudaSuccess) return e;
+        e = f16 ? launch_lse_combine16(p.n, rows, p.Dk, po16, pl, olat, lse, st)
+                : launch_lse_combine(TY_BF16, p.n, rows, p.Dk, po, pl, olat, lse, st);
     }
     if (e != cudaSuccess) return e;
     // 4. out[b][h][d] = sum_k o_lat[b][h][k] W_V(h)[d][k]: rows b (M), columns d (N), so

@@ -297,7 +297,7 @@ def test_decode_full_size(oracle):
 
 @pytest.mark.parametrize("dtype,L,n_splits", [
     ("bf16", 1000, 1), ("bf16", 1000, 2), ("bf16", 1000, 8), ("bf16", 1000, 13), ("bf16", 5, 8),
-    ("bf16", 1, 1), ("f32", 333, 13), ("f32", 64, 3)])
+    ("bf16", 1, 1), ("bf16", 5000, 40), ("f32", 333, 13), ("f32", 64, 3)])
 def test_decode_splits(oracle, dtype, L, n_splits):
     if dtype == "bf16":
         cfg = dataclasses.replace(configs.DECODE, batch=3, kv_len=L, n_splits=n_splits)
