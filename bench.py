@@ -46,7 +46,7 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max
 NCU_TRAFFIC = {("tc_attn", "v2lite_prefill_s4096_h16", False): 62.01e6,
                ("tc_attn", "v3_sp8_rank7_skv16384_q2048", False): 282.76e6,
                ("tc_fused_attn", "v2lite_prefill_s4096_h16", True): 34.19e6,
-               ("tc_decode_attn", "v3_decode_b64_l32768_split8", False): 310.95e6 * 8}
+               ("tc_decode_attn", "v3_decode_b64_l32768_split8", False): 313.52e6 * 8}
 
 
 def load_peaks():
