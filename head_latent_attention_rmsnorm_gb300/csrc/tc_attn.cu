@@ -8,26 +8,28 @@
 //   s_ij = scale * (q_nope_i . K_nope_j + RoPE(q_pe_i) . RoPE(k_pe_j)),
 // softmax over visible keys (j <= q_offset + i), output plus log-sum-exp.
 //
-// Kernel: persistent, one CTA per SM (640 threads) walking work units = (128-query
+// Kernel: persistent, one CTA per SM (256 threads) walking work units = (128-query
 // tile, head, batch), heaviest first under the causal mask, in rounds that alternate
 // direction; TMEM, barriers and the TMA rings carry over from one unit to the next.
-//   warp 0    TMA producer of K tiles (K_nope 128 + RoPE band 64 dims), 3-deep ring.
-//   warp 18   TMA producer of V^T tiles, 2-deep ring (separate, so that a wait for a
+//   warp 0    TMA producer of each unit's Q (staged in shared memory) and of the K tiles
+//             (K_nope 128 + RoPE band 64 dims), 2-deep ring.
+//   warp 6    TMA producer of V^T tiles, 2-deep ring (separate, so that a wait for a
 //             free V slot never holds back the next K tile).
 //   warp 1    tcgen05 issuer of the scores: S_j = Q K_j^T (M=128, N=128, K=192, Q from
 //             TMEM) into TMEM S buffer j & 1, as soon as K_j has landed and P.V_{j-2}
 //             (which read that buffer) is done.  Also owns the TMEM allocation.
-//   warp 19   tcgen05 issuer of O += P_j V_j (M=128, N=128, K=128), P read from TMEM
+//   warp 7    tcgen05 issuer of O += P_j V_j (M=128, N=128, K=128), P read from TMEM
 //             where the softmax wrote it over S_j.  Two issuing threads keep the tensor
 //             pipe fed: a thread that waits on an mbarrier between MMA batches leaves
 //             the pipe idle for ~100-200 cycles, so neither issuer waits on the other.
-//   warps 2-17 first load this row's Q (bf16 q_nope widened to fp16, q_pe rotated by
-//             RoPE) straight into TMEM; then softmax, four threads per query row (TMEM
-//             lane = row; 32 keys of each tile each): online softmax in the log2
-//             domain; O in TMEM is rescaled only when a row maximum grows by more than
-//             2^8 (the stale maximum keeps every p <= 256, exact after the final
-//             division); epilogue O / l and lse.  Sixteen softmax warps (four per
-//             scheduler) hide the TMEM-load and exp latencies of one another.
+//   warps 2-5 first move the row's Q (bf16 q_nope widened to fp16, q_pe rotated by
+//             RoPE) into TMEM; then the softmax, one thread per query row (TMEM lane =
+//             row; the tile's 128 scores in the thread's registers, so the row maximum
+//             needs no exchange between threads and no CTA barrier): online softmax in
+//             the log2 domain; O in TMEM is rescaled only when a row maximum grows by
+//             more than 2^8 (the stale maximum keeps every p <= 256, exact after the
+//             final division); epilogue O / l and lse.  (Sixteen warps with four threads
+//             per row and a barrier for the row maximum ran the same tiles no faster.)
 // Operands are fp16 (11-bit significand); K_nope, V^T and the rotated k_pe band are
 // produced in fp16 by the reconstruction GEMMs and the prep launch.
 #include <cuda_bf16.h>
@@ -60,9 +62,9 @@ constexpr uint32_t VBOX = BOX + ONES;          // one key half of a V slot
 constexpr uint32_t V_SLOT = 2 * VBOX;
 constexpr int KST = 2, VST = 2;
 constexpr uint32_t QS_BYTES = 3 * BOX;         // staged Q of the next unit: q_nope lo, hi (bf16), rotated q_pe (fp16)
-constexpr int NSM = 16;                       // softmax warps: four threads per query row
-// Q staging, K/V rings, 1 KB alignment slack, 256 B of barriers, row-max exchange [2][4][BQ]
-constexpr uint32_t SMEM_BYTES = QS_BYTES + KST * K_BYTES + VST * V_SLOT + 1024 + 256 + 4 * (2 * 4) * BQ;
+constexpr int NSM = 4;                        // softmax warps: one thread per query row
+// Q staging, K/V rings, 1 KB alignment slack, 256 B of barriers
+constexpr uint32_t SMEM_BYTES = QS_BYTES + KST * K_BYTES + VST * V_SLOT + 1024 + 256;
 // TMEM columns: S buffers 0-127 and 128-255, O 256-399 (dv 0-127, row sum 128, zeros),
 // Q (192 fp16 = 96 columns) 400-495
 constexpr uint32_t T_O = 256, T_L = T_O + 128, T_Q = 400;
@@ -123,7 +125,6 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
     uint64_t *s_full = v_empty + VST, *p_full = s_full + 2, *pv_done = p_full + 2;
     uint64_t *o_done = pv_done + 2, *o_final = o_done + 1, *o_free = o_final + 1, *qs_full = o_free + 1;
     uint32_t *tslot = (uint32_t *)(bars + 24);
-    float (*red)[4][BQ] = (float (*)[4][BQ])(bars + 32);   // [tile parity][quarter][row] partial maxima
     volatile int *abort = (volatile int *)(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -322,16 +323,14 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
         }
     } else if (warp >= 2 && warp < 2 + NSM) {
         // ---------------------------------------------------------- softmax warps
-        // Four threads per query row: warps 2-5 take keys 0-31 of each tile, warps 6-9
-        // keys 32-63, 10-13 keys 64-95, 14-17 keys 96-127 (warps w, w+4, w+8, w+12 reach
-        // the same TMEM lanes).  The quarters combine their row maxima through shared
-        // memory once per tile.
-        const int quad = warp & 3, qr = (warp - 2) >> 2;
+        // One thread per query row (TMEM lane = row: warp w reaches lanes 32 (w & 3) ..);
+        // a tile's 128 scores of the row sit in the thread's registers, so its maximum
+        // needs no exchange with other threads and the warps never wait on one another.
+        const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        // A failed wait clears `ok` (warp-uniform) but never leaves the loops early:
-        // every softmax thread passes the same named barriers, so an abort cannot strand
-        // one.
+        // A failed wait clears `ok` (warp-uniform); the loops run on so that every role
+        // keeps its barrier counts.
         bool ok = true;
         int T = 0, n = 0;
         // this CTA's units in order: round k, skipping rounds past the end
@@ -343,36 +342,39 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
         // ---- a unit's Q from the staging buffer into TMEM (the previous unit's score MMAs
         // have all completed: their S tiles were read).  Run for unit n + 1 right after unit
         // n's last tile, before unit n's epilogue, so that the next unit's first score MMAs
-        // overlap the last P.V and the epilogue.  Quarter qr widens q_nope dims [32 qr,
-        // 32 qr + 32) to fp16 (columns 16 qr ...); quarters 0 and 1 also copy the rotated q_pe
-        // elements t and t + 32 for t in [16 qr, 16 qr + 16) (columns 64 + 8 qr ... and
-        // 80 + 8 qr ...).  Rows past s_q arrive as zeros.  16-byte chunk c of row r of a staged
-        // box sits at chunk c ^ (r & 7).
+        // overlap the last P.V and the epilogue.  The row's q_nope (bf16, two 64-dim boxes)
+        // widened to fp16 into columns 0-63, its rotated q_pe (fp16) into columns 64-95; rows
+        // past s_q arrive as zeros.  16-byte chunk c of row r of a staged box sits at chunk
+        // c ^ (r & 7).
         auto load_q = [&](int nn) {
             ok = __all_sync(0xffffffffu, ok && mbar_wait(qs_full, nn & 1, abort, &g_tc_attn_err));
-            const uint8_t *qrow_s = sQs + (qr >> 1) * BOX + row * 128;
-            uint32_t qn[16];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const uint4 v = *(const uint4 *)(qrow_s + (((4 * (qr & 1) + cc) ^ (row & 7)) << 4));
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            for (int h = 0; h < 2; ++h) {
+                const uint8_t *qrow_s = sQs + h * BOX + row * 128;
+                uint32_t qn[2][16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    qn[4 * cc + i] = pack_f16(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xffff0000u));
-            }
-            tmem_st16(lane_base + T_Q + qr * 16, qn);
-            if (qr < 2) {   // warp-uniform
-                const uint8_t *prow = sQs + 2 * BOX + row * 128;
-                uint32_t ra8[8], rb8[8];
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 v = *(const uint4 *)(qrow_s + ((cc ^ (row & 7)) << 4));
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 va = *(const uint4 *)(prow + (((2 * qr + h) ^ (row & 7)) << 4));
-                    const uint4 vb = *(const uint4 *)(prow + (((2 * qr + 4 + h) ^ (row & 7)) << 4));
-                    ra8[4 * h] = va.x, ra8[4 * h + 1] = va.y, ra8[4 * h + 2] = va.z, ra8[4 * h + 3] = va.w;
-                    rb8[4 * h] = vb.x, rb8[4 * h + 1] = vb.y, rb8[4 * h + 2] = vb.z, rb8[4 * h + 3] = vb.w;
+                    for (int i = 0; i < 4; ++i)
+                        qn[cc >> 2][4 * (cc & 3) + i] =
+                            pack_f16(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xffff0000u));
                 }
-                tmem_st8(lane_base + T_Q + 64 + qr * 8, ra8);
-                tmem_st8(lane_base + T_Q + 80 + qr * 8, rb8);
+                tmem_st16(lane_base + T_Q + 32 * h, qn[0]);
+                tmem_st16(lane_base + T_Q + 32 * h + 16, qn[1]);
+            }
+            {
+                const uint8_t *prow = sQs + 2 * BOX + row * 128;
+                uint32_t pe[2][16];
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 v = *(const uint4 *)(prow + ((cc ^ (row & 7)) << 4));
+                    pe[cc >> 2][4 * (cc & 3)] = v.x, pe[cc >> 2][4 * (cc & 3) + 1] = v.y;
+                    pe[cc >> 2][4 * (cc & 3) + 2] = v.z, pe[cc >> 2][4 * (cc & 3) + 3] = v.w;
+                }
+                tmem_st16(lane_base + T_Q + 64, pe[0]);
+                tmem_st16(lane_base + T_Q + 80, pe[1]);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -391,39 +393,39 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
                 const int sb = T & 1;
                 ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[sb], (T >> 1) & 1, abort, &g_tc_attn_err));
                 tc_fence_after();
-                uint32_t sr[32];
+                uint32_t sr[4][32];
                 if (ok) {
-                    tmem_ld32(lane_base + sb * 128 + qr * 32, sr);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + sb * 128 + 32 * q, sr[q]);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) sr[i] = 0u;
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sr[q][i] = 0u;
                 }
-                const int j0 = j * BKV + qr * 32;
-                const bool masked = (j0 + 32 > p.kv_need) || (p.causal && j0 + 31 > p.q_offset + q0);
-                float x[32];
+                float x[128];
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) x[cc] = __uint_as_float(sr[cc]);
-                if (masked) {
+                for (int cc = 0; cc < 128; ++cc) x[cc] = __uint_as_float(sr[cc >> 5][cc & 31]);
+                // keys that can be hidden lie only in a unit's last tiles (a warp-uniform
+                // test); the masking is a pass of its own so that the maximum and the
+                // exponentials stay straight runs
+                const int j0 = j * BKV;
+                if ((j0 + BKV > p.kv_need) || (p.causal && j0 + BKV - 1 > p.q_offset + q0)) {
+                    // the row sees keys j0 .. j0 + lim - 1 of this tile
+                    const int lim = min(p.kv_need, p.causal ? pos + 1 : p.kv_need) - j0;
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const int key = j0 + cc;
-                        if (key >= p.kv_need || (p.causal && key > pos)) x[cc] = -INFINITY;
-                    }
+                    for (int cc = 0; cc < 128; ++cc) x[cc] = cc < lim ? x[cc] : -INFINITY;
                 }
-                // independent accumulators: the reductions are latency chains otherwise
-                float mx[4];
+                // independent accumulators: the reduction is a latency chain otherwise
+                float mx[8];
 #pragma unroll
-                for (int a = 0; a < 4; ++a) mx[a] = x[a];
+                for (int a = 0; a < 8; ++a) mx[a] = x[a];
 #pragma unroll
-                for (int cc = 4; cc < 32; ++cc) mx[cc & 3] = fmaxf(mx[cc & 3], x[cc]);
-                const float ml = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                // all four quarters have read their S columns before any writes P over them
-                red[sb][qr][row] = ml;
-                named_bar_sync(1, 32 * NSM);
-                const float mt =
-                    fmaxf(fmaxf(red[sb][0][row], red[sb][1][row]), fmaxf(red[sb][2][row], red[sb][3][row])) *
-                    p.scale_log2;
+                for (int cc = 8; cc < 128; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], x[cc]);
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                                 p.scale_log2;
                 const float m_new = fmaxf(m, mt);
                 const bool need = m_new > m + RESCALE_LOG2;   // also true on the first finite maximum
                 if (__any_sync(0xffffffffu, need)) {
@@ -434,77 +436,82 @@ __global__ void __launch_bounds__(32 * (NSM + 4), 1)
                     if (j > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, (T - 1) & 1, abort, &g_tc_attn_err));
                     if (j > 0 && ok) {
                         tc_fence_after();
-                        uint32_t o[32];
-                        tmem_ld32(lane_base + T_O + qr * 32, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(lane_base + T_O + qr * 32, o);
-                        if (qr == 0) {   // the row sum is rescaled with the row (warp-uniform)
-                            const uint32_t lv = tmem_ld1(lane_base + T_L);
+#pragma unroll 1
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t o[32];
+                            tmem_ld32(lane_base + T_O + 32 * q, o);
                             tmem_ld_wait();
-                            tmem_st1(lane_base + T_L, __float_as_uint(__uint_as_float(lv) * alpha));
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(lane_base + T_O + 32 * q, o);
                         }
+                        const uint32_t lv = tmem_ld1(lane_base + T_L);   // the row sum, rescaled with the row
+                        tmem_ld_wait();
+                        tmem_st1(lane_base + T_L, __float_as_uint(__uint_as_float(lv) * alpha));
                         tmem_st_wait();
                     }
                     m = m_use;
                 }
                 const float nm = (m == -INFINITY) ? 0.f : -m;
-                uint32_t pk[16];
+                // P over the S columns it came from, 32 keys (16 columns) at a time
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_f16(ex2(fmaf(x[2 * i], p.scale_log2, nm)), ex2(fmaf(x[2 * i + 1], p.scale_log2, nm)));
-                if (ok) {
-                    tmem_st16(lane_base + sb * 128 + qr * 16, pk);
-                    tmem_st_wait();
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_f16(ex2(fmaf(x[32 * q + 2 * i], p.scale_log2, nm)),
+                                         ex2(fmaf(x[32 * q + 2 * i + 1], p.scale_log2, nm)));
+                    if (ok) tmem_st16(lane_base + sb * 128 + 16 * q, pk);
                 }
+                if (ok) tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[sb]);
             }
             const int k_next = next_unit(k + 1);
             if (k_next * G < p.units) load_q(n + 1);
-            // ---- epilogue: the row sum is O's column 128; each quarter stores 32 columns
+            // ---- epilogue: the row sum is O's column 128; the row's 128 outputs in bf16
             if (nt > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(o_final, n & 1, abort, &g_tc_attn_err));
             tc_fence_after();
             const int qi = q0 + row;
-            uint32_t o[32];
+            uint32_t o[4][32];
             float l = 0.f;
             if (nt > 0) {
-                tmem_ld32(lane_base + T_O + qr * 32, o);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + T_O + 32 * q, o[q]);
                 const uint32_t lv = tmem_ld1(lane_base + T_L);
                 tmem_ld_wait();
                 l = __uint_as_float(lv);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = 0u;
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[q][i] = 0u;
             }
             const float inv = l > 0.f ? 1.f / l : 0.f;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);   // the next unit's P.V_0 may overwrite O
-            // the row-sum array is rewritten by the next unit only after its first tile's
-            // barrier, which every quarter reaches after reading it here
             if (ok && qi < p.s_q) {
-                // this quarter's 64 bytes of the row in two 32-byte stores (the epilogue's time
-                // went with the number of store instructions: 1.8 us with four 16-byte stores
-                // per thread, 1.2 us with two)
-                uint32_t *dst = (uint32_t *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h + qr * 32);
-                uint32_t wv[16];
+                // the row's 256 bytes in 32-byte stores (16-byte ones when the rows are not
+                // 32-byte aligned)
+                uint32_t *dst = (uint32_t *)(p.out + b * p.out_b + (long)qi * p.out_i + (long)hq * p.out_h);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    wv[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-                if (p.out_v8) {
-                    st_global_v8(dst, wv);
-                    st_global_v8(dst + 8, wv + 8);
-                } else {
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t wv[16];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        ((uint4 *)dst)[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+                    for (int i = 0; i < 16; ++i)
+                        wv[i] = pack_bf16(__uint_as_float(o[q][2 * i]) * inv, __uint_as_float(o[q][2 * i + 1]) * inv);
+                    if (p.out_v8) {
+                        st_global_v8(dst + 16 * q, wv);
+                        st_global_v8(dst + 16 * q + 8, wv + 8);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            ((uint4 *)(dst + 16 * q))[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+                    }
                 }
-                if (qr == 0)
-                    p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] =
-                        l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                p.lse[b * p.lse_b + (long)hq * p.lse_h + qi] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
             ++n;
             k = k_next;
