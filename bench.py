@@ -43,8 +43,8 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x FMA x max
 # workload, absorbed), from the ncu captures summarised under profiles/ (absent until the
 # current kernel has been captured on that workload).  The decode capture runs B = 8; its
 # traffic grows in proportion to the batch, so the B = 64 launch is 8x that.
-NCU_TRAFFIC = {("tc_attn", "v2lite_prefill_s4096_h16", False): 62.01e6,
-               ("tc_attn", "v3_sp8_rank7_skv16384_q2048", False): 282.76e6,
+NCU_TRAFFIC = {("tc_attn", "v2lite_prefill_s4096_h16", False): 61.52e6,
+               ("tc_attn", "v3_sp8_rank7_skv16384_q2048", False): 282.72e6,
                ("tc_fused_attn", "v2lite_prefill_s4096_h16", True): 34.19e6,
                ("tc_decode_attn", "v3_decode_b64_l32768_split8", False): 313.52e6 * 8}
 
