@@ -18,13 +18,18 @@ std::mutex g_mu;
 void *g_addr[MAX_DEVICES] = {};
 
 // Device address of the scratch on the current device.  In host code the array's
-// name is only a stand-in, so the address comes from cudaGetSymbolAddress, looked
-// up once per device with that device current.
-mla_status scratch_address(void **out) {
+// name is only a stand-in, so the address comes from cudaGetSymbolAddress.  It is looked
+// up on every call made outside stream capture (so a context torn down and created again
+// after a device reset gets the address in the new context) and remembered per device;
+// a call made while `st` is capturing uses the remembered address, and looks it up only
+// if it has none yet.
+mla_status scratch_address(void **out, cudaStream_t st) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return MLA_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MLA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone || !g_addr[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MLA_ERR_CUDA;
         g_addr[dev] = p;
@@ -46,7 +51,7 @@ extern "C" mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype
                                   out, lse, nullptr, nullptr, nullptr, 0, cuda_stream);
     if (need > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
     void *scratch = nullptr;
-    mla_status st = scratch_address(&scratch);
+    mla_status st = scratch_address(&scratch, (cudaStream_t)cuda_stream);
     if (st != MLA_OK) return st;
     return mla_decode_splitkv(dims, dtype, B, kv_len, n_splits, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out,
                               lse, nullptr, nullptr, scratch, MLA_NOALLOC_SCRATCH_BYTES, cuda_stream);

@@ -318,12 +318,10 @@ void mla_set_fused_cluster(int size);
  * GPU that loads the library holds that array until the process exits.
  *  - A call needing more scratch than the array holds (see mla_decode_workspace)
  *    returns MLA_ERR_WORKSPACE and launches nothing.
- *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any stream
- *    capture begins.  The address is kept for the life of the process: after a
- *    cudaDeviceReset (or anything else that destroys and recreates the device's
- *    primary context) it is stale, so do not call this entry point on that device
- *    again in the same process.
+ *  - A call outside stream capture looks up the array's device address in the current
+ *    context (so calls after a cudaDeviceReset find the new one) and remembers it per
+ *    device; a call made while cuda_stream is capturing uses the remembered address.
+ *    Make one call on the device before capturing, and capture again after a reset.
  *  - Every call shares the one array and leaves its contents behind.  Nothing in it
  *    needs to start at zero: each call writes all the scratch it reads.  Calls
  *    that overlap on the GPU (other streams, other host threads) race on it;
