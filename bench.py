@@ -295,7 +295,7 @@ def tpla_extra(dcfg, stream, hbm_peak, n_shards=2, steps=10, warmup=3):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": dcfg.name + "_tpla%d" % n_shards, "n_shards": n_shards, "ms_per_call": round(ms, 4),
             "GB/s": round(gbs, 1), "bytes_per_call": nbytes, "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
-            "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"),
+            "kernel_path": path_name(path),
             "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()},
             "cache_rmsnorm": {"rows": dcfg.batch * dcfg.kv_len, "ms": round(n_ms, 4), "bytes": n_bytes,
                               "GB/s": round(n_bytes / (n_ms * 1e-3) / 1e9, 1),
@@ -325,6 +325,13 @@ def timed(fn, steps, warmup, world, flush=None):
     torch.cuda.synchronize()
     barrier(world)
     return [a.elapsed_time(b) for a, b in ev]
+
+
+def path_name(path: int) -> str:
+    """The kernel family the library reports for its last call (mla_last_path)."""
+    from head_latent_attention_rmsnorm_gb300 import mla
+    return {mla.PATH_SIMT: "simt", mla.PATH_TC: "tcgen05",
+            mla.PATH_TC_FUSED: "tcgen05 fused"}.get(path, "?")
 
 
 def dominant(prof: dict, candidates):
@@ -381,7 +388,7 @@ def prefill_measure(cfg, stream, steps, warmup, world, flush, peaks, peak_kind, 
            "ms_per_call": round(ms, 4), "TFLOP/s": round(world * fl["total"] / (ms * 1e-3) / 1e12, 2),
            "frac_of_bf16_peak": round(fl["total"] / (ms * 1e-3) / 1e12 / peaks.get("bf16_tflops", 1900.0), 4),
            "flops_per_call": fl["total"], "tokens_per_s": round(world * cfg.batch * cfg.s_q / (ms * 1e-3), 1),
-           "head_shard": cfg.head_shard, "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"),
+           "head_shard": cfg.head_shard, "kernel_path": path_name(path),
            "steps": steps, "warmup": warmup, "gpu_launches": launches, "roofline": roof,
            "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
     return res, (d, t, out, lse, ws, fn)
@@ -424,7 +431,7 @@ def decode_measure(dcfg, stream, steps, warmup, world, peaks, peak_kind):
             "bytes_per_call": dbytes, "frac_of_8TBps": round(gbs / world / 8000.0, 4),
             "frac_of_measured_hbm": round(gbs / world / hbm, 4),
             "tokens_per_s": round(world * dcfg.batch / (ms * 1e-3), 1), "steps": steps, "warmup": warmup,
-            "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"), "roofline": droof,
+            "kernel_path": path_name(path), "roofline": droof,
             "l2": "inputs (2.4 GB) larger than L2",
             "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
 
@@ -482,7 +489,7 @@ def backward_measure(cfg, stream, steps, warmup, flush, peaks, peak_kind):
             "TFLOP/s": round(fl["total"] / (ms * 1e-3) / 1e12, 2),
             "frac_of_bf16_peak": round(fl["total"] / (ms * 1e-3) / 1e12 / peak, 4), "flops_per_call": fl["total"],
             "flops_counted": "dV, dP, dQ, dK per visible pair and head; dW and dchat per key and head (no recompute)",
-            "kernel_path": {1: "simt", 2: "tcgen05"}.get(path, "?"), "steps": steps, "warmup": warmup,
+            "kernel_path": path_name(path), "steps": steps, "warmup": warmup,
             "roofline": roof, "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
 
 
