@@ -793,7 +793,7 @@ def oracle_prefill_sample(cfg, rows: int, heads: int):
 
 
 CPU_SAMPLE = (512, 48)    # rows, heads of the cpu_baseline leg (10-20 s of the host's cores)
-REF_SAMPLE = (32, 16)     # rows, heads of each step of the --impl reference arm
+REF_SAMPLE = (32, 8)      # rows, heads of each step of the --impl reference arm (~3 s on 8 cores)
 
 
 def cpu_baseline_headline():
