@@ -97,7 +97,7 @@ mla_status prefill_shape(const mla_dims *d, mla_dtype dt, int B, int s_q, int s_
     if (st != MLA_OK) return st;
     if (!valid_dtype(dt)) return MLA_ERR_DTYPE;
     if (B < 0 || s_q < 0 || s_kv < 0 || q_offset < 0 || head_begin < 0 || head_count < 0 || head_shard < 0 ||
-        head_begin + head_count > d->n_heads)
+        (long)head_begin + head_count > d->n_heads)
         return MLA_ERR_SHAPE;
     if (causal && (long)q_offset + s_q > s_kv) return MLA_ERR_SHAPE;
     p->B = B;

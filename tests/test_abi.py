@@ -75,6 +75,7 @@ def call_prefill(fn, a):
     (dict(workspace=None), -1),
     (dict(s_q=4096), -2),                     # causal rows beyond the latent
     (dict(head_begin=120, head_count=16), -2),
+    (dict(head_begin=2 ** 31 - 1, head_count=1), -2),   # the head range's end past INT_MAX
     (dict(q_offset=-1), -2),
     (dict(dtype=7), -3),
     (dict(out=fake(7) + 8), -4),
