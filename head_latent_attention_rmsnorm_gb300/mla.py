@@ -258,6 +258,72 @@ def _dt(t: torch.Tensor) -> int:
     raise TypeError("unsupported dtype %s" % t.dtype)
 
 
+def _device(t: torch.Tensor) -> torch.device:
+    """The call's device: that of its first tensor, which must be a CUDA device (the
+    library's kernels dereference every pointer on the GPU)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor, got %s" % type(t).__name__)
+    if t.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device, got %s" % t.device)
+    return t.device
+
+
+def _expect(name: str, t, numel: int, dtype: torch.dtype, device: torch.device) -> None:
+    """Check one tensor argument before the call: the library reads or writes exactly
+    ``numel`` elements of ``dtype`` behind its pointer on ``device``, so a tensor on
+    another device, of another dtype or of another size would be misread or accessed
+    out of bounds.  None passes (optional arguments)."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s: expected a torch.Tensor, got %s" % (name, type(t).__name__))
+    if t.device != device:
+        raise ValueError("%s: on %s, the call's tensors are on %s" % (name, t.device, device))
+    if t.dtype != dtype:
+        raise TypeError("%s: dtype %s, expected %s" % (name, t.dtype, dtype))
+    if t.numel() != numel:
+        raise ValueError("%s: %d elements, expected %d" % (name, t.numel(), numel))
+    if not t.is_contiguous():
+        raise ValueError("%s: tensors must be contiguous" % name)
+
+
+def _prefill_checks(d, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse):
+    dev = _device(q_nope)
+    _dt(q_nope)
+    tdt = q_nope.dtype
+    if q_nope.dim() != 4 or c_kv.dim() != 3:
+        raise ValueError("q_nope must be [B, s_q, heads, d_nope] and c_kv [B, s_kv, d_kv]")
+    B, s_q, hc, _ = q_nope.shape
+    s_kv = c_kv.shape[1]
+    _expect("q_nope", q_nope, B * s_q * hc * d.d_nope, tdt, dev)
+    _expect("q_pe", q_pe, B * s_q * hc * d.d_rope, tdt, dev)
+    _expect("c_kv", c_kv, B * s_kv * d.d_kv, tdt, dev)
+    _expect("k_pe", k_pe, B * s_kv * d.d_rope, tdt, dev)
+    _expect("w_kv_b", w_kv_b, d.n_heads * (d.d_nope + d.d_v) * d.d_kv, tdt, dev)
+    _expect("rms_w", rms_w, d.d_kv, tdt, dev)
+    _expect("out", out, B * s_q * hc * d.d_v, tdt, dev)
+    _expect("lse", lse, B * hc * s_q, torch.float32, dev)
+    return dev, B, s_q, hc, s_kv
+
+
+def _decode_checks(d, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out):
+    dev = _device(q_nope)
+    _dt(q_nope)
+    tdt = q_nope.dtype
+    if q_nope.dim() != 3 or c_cache.dim() != 3:
+        raise ValueError("q_nope must be [B, n_heads, d_nope] and c_cache [B, kv_len, d_kv]")
+    B = q_nope.shape[0]
+    L = c_cache.shape[1]
+    H = d.n_heads
+    _expect("q_nope", q_nope, B * H * d.d_nope, tdt, dev)
+    _expect("q_pe", q_pe, B * H * d.d_rope, tdt, dev)
+    _expect("c_cache", c_cache, B * L * d.d_kv, tdt, dev)
+    _expect("kpe_cache", kpe_cache, B * L * d.d_rope, tdt, dev)
+    _expect("w_kv_b", w_kv_b, H * (d.d_nope + d.d_v) * d.d_kv, tdt, dev)
+    _expect("out", out, B * H * d.d_v, tdt, dev)
+    return dev, B, L, H
+
+
 def _ptr(t) -> int | None:
     if t is None:
         return None
@@ -279,6 +345,8 @@ def _check(status: int, where: str) -> None:
 
 def _workspace(nbytes: int, device, workspace):
     if workspace is not None:
+        if not isinstance(workspace, torch.Tensor) or workspace.device != device:
+            raise ValueError("workspace: must be a tensor on %s" % device)
         return workspace
     return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
 
@@ -287,8 +355,7 @@ def latent_attn_fwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, q_offse
                     head_begin=0, head_shard=0, out=None, lse=None, workspace=None, stream=None,
                     absorbed=False):
     """Explicit (or, with ``absorbed=True``, absorbed) MLA prefill.  Returns (out, lse)."""
-    B, s_q, hc, _ = q_nope.shape
-    s_kv = c_kv.shape[1]
+    _, B, s_q, hc, s_kv = _prefill_checks(d, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse)
     dt = _dt(q_nope)
     if out is None:
         out = torch.empty(B, s_q, hc, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
@@ -313,8 +380,7 @@ def latent_attn_fused_fwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, *, q
                           head_begin=0, out=None, lse=None, workspace=None, stream=None):
     """Explicit MLA prefill with the K/V up-projection inside the attention kernel (no
     K/V workspace).  Returns (out, lse)."""
-    B, s_q, hc, _ = q_nope.shape
-    s_kv = c_kv.shape[1]
+    _, B, s_q, hc, s_kv = _prefill_checks(d, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse)
     dt = _dt(q_nope)
     if out is None:
         out = torch.empty(B, s_q, hc, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
@@ -334,11 +400,16 @@ def latent_attn_bwd(d: Dims, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse, 
     """Backward of :func:`latent_attn_fwd` for an upstream gradient ``dout`` of its output.
     Returns a dict of gradients: q_nope, q_pe, c_kv, k_pe (input dtype), w_kv_b, rms_w
     (fp32; w_kv_b rows outside the call's heads are zero when this call allocates it)."""
-    B, s_q, hc, _ = q_nope.shape
-    s_kv = c_kv.shape[1]
+    dev, B, s_q, hc, s_kv = _prefill_checks(d, q_nope, q_pe, c_kv, k_pe, w_kv_b, rms_w, out, lse)
+    if out is None or lse is None:
+        raise ValueError("the forward's out and lse are required")
+    _expect("dout", dout, out.numel(), out.dtype, dev)
     dt = _dt(q_nope)
-    dev = q_nope.device
     g = grads or {}
+    for k, like in (("q_nope", q_nope), ("q_pe", q_pe), ("c_kv", c_kv), ("k_pe", k_pe)):
+        _expect("grads[%s]" % k, g.get(k), like.numel(), like.dtype, dev)
+    _expect("grads[w_kv_b]", g.get("w_kv_b"), w_kv_b.numel(), torch.float32, dev)
+    _expect("grads[rms_w]", g.get("rms_w"), rms_w.numel(), torch.float32, dev)
     g.setdefault("q_nope", torch.empty_like(q_nope))
     g.setdefault("q_pe", torch.empty_like(q_pe))
     g.setdefault("c_kv", torch.empty_like(c_kv))
@@ -363,8 +434,12 @@ def set_fused_cluster(size: int) -> None:
 def decode_splitkv(d: Dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_splits=1, out=None, lse=None,
                    part_out=None, part_lse=None, workspace=None, stream=None):
     """Split-KV latent decode.  Returns (out, lse)."""
-    B, H, _ = q_nope.shape
-    L = c_cache.shape[1]
+    dev, B, L, H = _decode_checks(d, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out)
+    _expect("lse", lse, B * H, torch.float32, dev)
+    if (part_out is None) != (part_lse is None):
+        raise ValueError("part_out and part_lse go together")
+    _expect("part_out", part_out, n_splits * B * H * d.d_kv, torch.float32, dev)
+    _expect("part_lse", part_lse, n_splits * B * H, torch.float32, dev)
     dt = _dt(q_nope)
     if out is None:
         out = torch.empty(B, H, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
@@ -383,8 +458,8 @@ def tpla_decode(d: Dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_shards=2
                 shard_lse=None, workspace=None, stream=None):
     """TPLA decode over ``n_shards`` latent shards (``c_cache`` normalised per shard, as
     :func:`rmsnorm` with the same ``n_shards`` writes it).  Returns (out, shard_lse)."""
-    B, H, _ = q_nope.shape
-    L = c_cache.shape[1]
+    dev, B, L, H = _decode_checks(d, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, out)
+    _expect("shard_lse", shard_lse, n_shards * B * H, torch.float32, dev)
     dt = _dt(q_nope)
     if out is None:
         out = torch.empty(B, H, d.d_v, dtype=q_nope.dtype, device=q_nope.device)
@@ -402,7 +477,12 @@ def tpla_decode(d: Dims, q_nope, q_pe, c_cache, kpe_cache, w_kv_b, *, n_shards=2
 def rmsnorm(x, w, *, n_shards=1, eps=1e-6, out=None, stream=None):
     """RMSNorm over the last dim of ``x``, cut into ``n_shards`` shards normalised on
     their own.  Returns ``out``."""
+    dev = _device(x)
+    _dt(x)
     d = x.shape[-1]
+    _expect("x", x, x.numel(), x.dtype, dev)
+    _expect("w", w, d, x.dtype, dev)
+    _expect("out", out, x.numel(), x.dtype, dev)
     if out is None:
         out = torch.empty_like(x)
     st = mla_rmsnorm(_dt(x), x.numel() // d if d else 0, d, n_shards, float(eps), _ptr(x), _ptr(w), _ptr(out),
@@ -413,7 +493,14 @@ def rmsnorm(x, w, *, n_shards=1, eps=1e-6, out=None, stream=None):
 
 def rmsnorm_bwd(x, w, dy, *, n_shards=1, eps=1e-6, dx=None, dw=None, workspace=None, stream=None):
     """Backward of :func:`rmsnorm`.  Returns (dx like x, dw fp32 [d])."""
+    dev = _device(x)
+    _dt(x)
     d = x.shape[-1]
+    _expect("x", x, x.numel(), x.dtype, dev)
+    _expect("w", w, d, x.dtype, dev)
+    _expect("dy", dy, x.numel(), x.dtype, dev)
+    _expect("dx", dx, x.numel(), x.dtype, dev)
+    _expect("dw", dw, d, torch.float32, dev)
     rows = x.numel() // d if d else 0
     dt = _dt(x)
     if dx is None:
@@ -429,7 +516,16 @@ def rmsnorm_bwd(x, w, dy, *, n_shards=1, eps=1e-6, dx=None, dw=None, workspace=N
 
 def lse_combine(part_out, part_lse, *, out_dtype=torch.float32, out=None, lse=None, stream=None):
     """Merge fp32 split partials [n, rows, D] / [n, rows].  Returns (out, lse)."""
+    dev = _device(part_out)
+    if part_out.dim() != 3:
+        raise ValueError("part_out must be [n_splits, rows, D]")
     n, rows, D = part_out.shape
+    _expect("part_out", part_out, n * rows * D, torch.float32, dev)
+    _expect("part_lse", part_lse, n * rows, torch.float32, dev)
+    if out is not None:
+        _dt(out)
+        _expect("out", out, rows * D, out.dtype, dev)
+    _expect("lse", lse, rows, torch.float32, dev)
     if out is None:
         out = torch.empty(rows, D, dtype=out_dtype, device=part_out.device)
     if lse is None:
