@@ -261,3 +261,47 @@ def test_backward_validates_before_launch(L):
     assert mla.mla_latent_attn_bwd(*bad) == -9
     d2 = mla.dims(n_heads=128, d_kv=64, d_nope=300, d_rope=16, d_v=32)
     assert mla.mla_latent_attn_bwd(ctypes.byref(d2), mla.MLA_F32, *args[2:]) == -6
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "mla.h"
+int main(void) {
+    mla_dims d = {128, 512, 128, 64, 128, 10000.0f, 1e-6f, 0.0f};
+    /* workspace query (host arithmetic only) */
+    printf("%zu\n", mla_latent_attn_workspace(&d, MLA_BF16, 1, 2048, 16384, 14336, 1, 128, 16));
+    /* validation before any launch: missing pointers, then a causal call past its keys */
+    printf("%d\n", (int)mla_latent_attn_fwd(&d, MLA_BF16, 1, 16, 64, 0, 1, 0, 128, 16, NULL, NULL, NULL, NULL,
+                                            NULL, NULL, NULL, NULL, NULL, 0, NULL));
+    printf("%d\n", (int)mla_decode_splitkv(&d, MLA_BF16, 1, 0, 1, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                                           NULL, NULL, NULL, 0, NULL));
+    /* an empty call is a no-op */
+    printf("%d\n", (int)mla_latent_attn_fwd(&d, MLA_BF16, 0, 16, 64, 0, 1, 0, 128, 16, NULL, NULL, NULL, NULL,
+                                            NULL, NULL, NULL, NULL, NULL, 0, NULL));
+    printf("%s\n", mla_status_string(MLA_ERR_SHAPE));
+    return 0;
+}
+"""
+
+
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_header_builds_and_links_as_plain_c_and_cpp(L, tmp_path, lang):
+    """A program in plain C11 (and the same as C++17, through the header's extern "C"
+    block) includes include/mla.h, links libmla.so and calls the ABI without Python."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "t"
+    libdir = os.path.dirname(mla.LIB_PATH)
+    std = ["-std=c11"] if lang == "c" else ["-std=c++17"]
+    subprocess.check_call([cc] + std + ["-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                                        "-L", libdir, "-lmla", "-Wl,-rpath," + libdir, "-o", str(exe)])
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    d = mla.dims(**V3)
+    assert int(lines[0]) == mla.mla_latent_attn_workspace(ctypes.byref(d), mla.MLA_BF16, 1, 2048, 16384, 14336, 1,
+                                                          128, 16)
+    assert lines[1:5] == ["-1", "-2", "0", mla.mla_status_string(-2)]
