@@ -36,6 +36,12 @@ MUTATIONS = {
                              "out[row * Dv + d] += dot(wv + (size_t)d * Dk, ol + k0, ds);"),
     "tpla_norm_weight_slice": ("rmsnorm_row(c_raw + r * Dk + (size_t)i * ds, rms_w + (size_t)i * ds, ds, eps,",
                                "rmsnorm_row(c_raw + r * Dk + (size_t)i * ds, rms_w, ds, eps,"),
+    "rms_weight_dropped": ("y[k] = x[k] * inv * w[k];", "y[k] = x[k] * inv;"),
+    "head_offset_ignored": ("int h = head_begin + hl;", "int h = hl;"),
+    "decode_query_position": ("(double)(kv_len - 1)", "(double)kv_len"),
+    "split_chunk_rounded_down": ("((long)kv_len + n_splits - 1) / n_splits", "(long)kv_len / n_splits"),
+    "unabsorb_reads_k_rows": ("                const double *wv = wk + (size_t)Dn * Dk;\n                double *qa",
+                              "                const double *wv = wk;\n                double *qa"),
     "absorb_transposed": ("acc += qn[d] * wk[(size_t)d * Dk + k];\n                    qa[k] = acc;",
                           "acc += qn[d] * wk[(size_t)k * Dn + d];\n                    qa[k] = acc;"),
 }
