@@ -1,6 +1,7 @@
 // profile.cu -- launch accounting and opt-in per-kernel event timing of libmla.
 #include <atomic>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -10,7 +11,8 @@ namespace mla {
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
-bool g_prof_on = false;
+std::atomic<bool> g_prof_on{false};
+std::mutex g_mu;   // guards the event pool and the records (several host threads may launch)
 
 struct Pair {
     cudaEvent_t a, b;
@@ -19,6 +21,7 @@ std::map<std::string, std::vector<Pair>> g_rec;
 std::vector<cudaEvent_t> g_pool;
 thread_local cudaEvent_t g_open = nullptr;
 
+// Callers hold g_mu.
 cudaEvent_t get_event() {
     if (!g_pool.empty()) {
         cudaEvent_t e = g_pool.back();
@@ -30,6 +33,7 @@ cudaEvent_t get_event() {
     return e;
 }
 
+// Callers hold g_mu.
 void recycle_all() {
     for (auto &kv : g_rec)
         for (auto &p : kv.second) {
@@ -43,13 +47,15 @@ void recycle_all() {
 
 void prof_begin(const char *, cudaStream_t st) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (!g_prof_on) return;
+    if (!g_prof_on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lock(g_mu);
     g_open = get_event();
     if (g_open) cudaEventRecord(g_open, st);
 }
 
 void prof_end(const char *name, cudaStream_t st) {
-    if (!g_prof_on || !g_open) return;
+    if (!g_prof_on.load(std::memory_order_relaxed) || !g_open) return;
+    std::lock_guard<std::mutex> lock(g_mu);
     cudaEvent_t b = get_event();
     if (!b) return;
     cudaEventRecord(b, st);
@@ -67,21 +73,28 @@ void mla_profile_enable(int on) {
     mla::g_prof_on = on != 0;
     if (!on) {
         cudaDeviceSynchronize();
+        std::lock_guard<std::mutex> lock(mla::g_mu);
         mla::recycle_all();
     }
 }
 
 void mla_profile_reset(void) {
     cudaDeviceSynchronize();
+    std::lock_guard<std::mutex> lock(mla::g_mu);
     mla::recycle_all();
 }
 
 int mla_profile_kernel(const char *name, long long *launches, double *total_ms) {
     *launches = 0;
     *total_ms = 0.0;
-    auto it = mla::g_rec.find(name);
-    if (it == mla::g_rec.end()) return 0;
-    for (auto &p : it->second) {
+    std::vector<mla::Pair> pairs;
+    {
+        std::lock_guard<std::mutex> lock(mla::g_mu);
+        auto it = mla::g_rec.find(name);
+        if (it == mla::g_rec.end()) return 0;
+        pairs = it->second;
+    }
+    for (auto &p : pairs) {
         if (cudaEventSynchronize(p.b) != cudaSuccess) return -1;
         float ms = 0.f;
         if (cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess) return -1;
