@@ -82,3 +82,21 @@ def test_activation_closed_form_matches_the_workspace_query(cfg, form):
             # copy) the closed form does not describe
             continue
         assert 0 <= ws - need < 16 * 256, (hs, ws, need)
+
+
+def test_decode_bytes_are_the_call_tensors_bytes():
+    """The decode GB/s figure divides by the bytes of what a call must move: the cache,
+    W_kv_b and the queries in, the output and its LSE out (Helix, "What carries the
+    argument": decode is bound by reading the KV cache)."""
+    import torch
+
+    from head_latent_attention_rmsnorm_gb300 import inputs
+    cfg = dataclasses.replace(configs.DECODE, batch=3, kv_len=50)
+    t = inputs.decode_inputs(cfg)
+    nbytes = lambda x: x.numel() * x.element_size()  # noqa: E731
+    assert cfg.cache_bytes() == nbytes(t["c_cache"]) + nbytes(t["kpe_cache"])
+    out = torch.empty(cfg.batch, cfg.n_heads, cfg.d_v, dtype=cfg.torch_dtype)
+    lse = torch.empty(cfg.batch, cfg.n_heads, dtype=torch.float32)
+    assert cfg.algorithmic_bytes() == sum(nbytes(v) for v in t.values()) + nbytes(out) + nbytes(lse)
+    # at the bench's size the cache is 98 % of the bytes
+    assert configs.DECODE.cache_bytes() / configs.DECODE.algorithmic_bytes() > 0.98
