@@ -337,7 +337,10 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
 
 /*
  * Measurement hooks (not part of the computation).
- * mla_launch_count: kernels this library has launched since load, all threads.
+ * mla_launch_count: launches this library has made since load, all threads, counted
+ *   per launch step: one per kernel on the forward and decode paths; a few backward
+ *   steps that launch a fixed pair of kernels (a row pass and its fixed-order sum)
+ *   count once.
  * mla_profile_enable(1): from now on every launch is bracketed by a pair of CUDA
  *   events recorded on the launching stream (the caller's stream), grouped by
  *   kernel name; mla_profile_enable(0) stops recording and drops what was recorded.
@@ -349,7 +352,8 @@ mla_status mla_decode_splitkv_noalloc(const mla_dims *dims, mla_dtype dtype, int
  *   "tpla_combine", "wait_probe", "tc_fused_attn", "bwd_rowdot",
  *   "attn_bwd_simt", "bwd_rows", "bwd_prep", "tc_bwd_dkv", "tc_bwd_dq".
  * mla_profile_reset: forgets recorded events, keeps recording on/off as it was.
- * Not thread-safe: profile from one host thread at a time.
+ * Launches from several host threads are recorded safely; call enable, reset and the
+ * queries between computations, not while another thread's calls are in flight.
  */
 unsigned long long mla_launch_count(void);
 void mla_profile_enable(int on);
