@@ -9,7 +9,8 @@ The arithmetic lives in ``mla_oracle.c`` (IEEE double, plain loops; see its head
 for the page citations and the readings taken where the pages are silent).  This
 module compiles it with gcc and exposes numpy-in / numpy-out wrappers.
 
-Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``):
+Parity status of each function (what pins it: ``tests/test_oracle_pins.py``, repeated over
+random small shapes in ``tests/test_oracle_sweep.py``):
   rmsnorm, rope, mla_explicit, mla_absorbed, mla_decode, lse_combine, tpla_decode,
   mla_explicit_bwd, rmsnorm_bwd -- all pinned.
 """
