@@ -6,8 +6,10 @@ Each rank takes its block of query positions (LAGA sequence-parallel view), of h
 all_gather; the concatenation (or the log-sum-exp merge of the split partials) must
 equal the single-process result.  A TPLA rank decodes with its latent shard (its own
 RMSNorm, local softmax, its slice of W_kv_b), and the all-reduced sum must equal the
-two-shard TPLA decode.  Also checks the max-over-ranks timing reduction
-the benchmark uses.
+two-shard TPLA decode.  In the backward, each sequence-parallel rank's latent, RoPE
+band and weight gradients are all-reduced and must equal one call's, with the query
+gradients reassembling by rows.  Also checks the max-over-ranks timing reduction the
+benchmark uses.
 """
 import os
 import socket
@@ -144,3 +146,67 @@ def test_latent_shard_needs_even_split():
     assert [sharding.latent_shard(512, 2, r) for r in range(2)] == [(0, 256), (256, 256)]
     with pytest.raises(ValueError):
         sharding.latent_shard(512, 3, 0)
+
+
+def _bwd_inputs():
+    g = np.random.default_rng(5)
+    B, S, H, dk, dn, dr, dv = 1, 24, 3, 16, 8, 4, 8
+    inp = dict(q_nope=g.standard_normal((B, S, H, dn)), q_pe=g.standard_normal((B, S, H, dr)),
+               c_kv=g.standard_normal((B, S, dk)), k_pe=g.standard_normal((B, S, dr)),
+               w_kv_b=g.standard_normal((H * (dn + dv), dk)) / np.sqrt(dk), rms_w=1.0 + 0.2 * g.standard_normal(dk))
+    return inp, g.standard_normal((B, S, H, dv)), H
+
+
+def _bwd_worker(rank, port, q):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import oracle
+    from head_latent_attention_rmsnorm_gb300 import sharding
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD)
+    try:
+        inp, dout, H = _bwd_inputs()
+        S = inp["c_kv"].shape[1]
+        q0, n = sharding.query_shard(S, WORLD, rank)
+        part = dict(inp, q_nope=inp["q_nope"][:, q0:q0 + n].copy(), q_pe=inp["q_pe"][:, q0:q0 + n].copy())
+        g = oracle.mla_explicit_bwd(**part, dout=dout[:, q0:q0 + n].copy(), n_heads=H, q_offset=q0)
+        # the gradients of what every rank shares (the gathered latent, its RoPE band, the
+        # weights) are summed over the ranks: the reduce-scatter / all-reduce that mirrors
+        # the forward's all-gather; the query gradients stay with their rank's rows
+        summed = {}
+        for k in ("c_kv", "k_pe", "w_kv_b", "rms_w"):
+            t = torch.from_numpy(np.ascontiguousarray(g[k]))
+            dist.all_reduce(t, op=dist.ReduceOp.SUM)
+            summed[k] = t.numpy()
+        rows = [None] * WORLD
+        dist.all_gather_object(rows, (q0, g["q_nope"], g["q_pe"]))
+        if rank == 0:
+            q.put((summed, rows))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(300)
+def test_two_rank_backward_gradients_sum_to_one_call(oracle):
+    """LAGA, "If this is right": sequence-parallel ranks give the gradients of one call.
+    Two gloo ranks each back-propagate their block of query rows; the summed latent, RoPE
+    band and weight gradients equal one call's, and the query gradients reassemble."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_bwd_worker, args=(r, port, q)) for r in range(WORLD)]
+    for p in procs:
+        p.start()
+    summed, rows = q.get(timeout=240)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    inp, dout, H = _bwd_inputs()
+    full = oracle.mla_explicit_bwd(**inp, dout=dout, n_heads=H)
+    for k in ("c_kv", "k_pe", "w_kv_b", "rms_w"):
+        np.testing.assert_allclose(summed[k], full[k], rtol=0, atol=1e-12 * max(1.0, np.abs(full[k]).max()),
+                                   err_msg=k)
+    rows = sorted(rows, key=lambda x: x[0])
+    np.testing.assert_array_equal(np.concatenate([r[1] for r in rows], 1), full["q_nope"])
+    np.testing.assert_array_equal(np.concatenate([r[2] for r in rows], 1), full["q_pe"])
