@@ -54,3 +54,13 @@ def test_every_profiled_launch_has_a_reported_name():
         names |= set(re.findall(r'ProfScope \w+\("(\w+)"', open(f).read()))
     assert len(names) > 10
     assert names <= set(mla.KERNELS), names - set(mla.KERNELS)
+
+
+def test_header_lists_the_profiled_names():
+    """include/mla.h documents the names mla_profile_kernel answers to; they are the
+    binding's and the launch sites'."""
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mla.h")).read()
+    block = hdr[hdr.index("Names:"):hdr.index("mla_profile_reset:")]
+    assert set(re.findall(r'"(\w+)"', block)) == set(mla.KERNELS)
